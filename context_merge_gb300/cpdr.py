@@ -1,0 +1,230 @@
+"""Thin ctypes binding of libcpdr.so (include/cpdr.h).
+
+Argument marshalling only: tensors are passed as raw device pointers and the
+current torch CUDA stream as a cudaStream_t; every step of the computation
+runs in the library's CUDA kernels.  The library must have been built
+(``python -c "import __graft_entry__ as g; g.build()"``); loading raises if it
+is missing -- there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcpdr.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = range(6)
+FLAG_HOST_ONLY = 1 << 0
+FLAG_FORCE_SIMT = 1 << 1
+FRAG_CONT_PREV, FRAG_CONT_NEXT, FRAG_ENDS_SEQ = 1, 2, 4
+
+EXPORTED = ["cpdr_ctx_create", "cpdr_ctx_destroy", "cpdr_buffer_sizes", "cpdr_plan_num_fragments",
+            "cpdr_plan_fragments", "cpdr_plan_counts", "cpdr_preprocess", "cpdr_merge", "cpdr_fwd", "cpdr_host_workspace_bytes",
+            "cpdr_forward_host", "cpdr_check_device_status", "cpdr_last_error", "cpdr_version"]
+
+
+class CpdrError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"cpdr status {status}: {msg}")
+        self.status = status
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
+                ("R", ctypes.c_int32), ("num_seqs", ctypes.c_int32), ("T", ctypes.c_int64),
+                ("cu_seqlens_host", ctypes.POINTER(ctypes.c_int64)), ("gate_kind", ctypes.c_int32),
+                ("in_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32), ("scale", ctypes.c_float)]
+
+
+class Fragment(ctypes.Structure):
+    _fields_ = [("tok0", ctypes.c_int64), ("len", ctypes.c_int32), ("seg", ctypes.c_int32),
+                ("seq", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load():
+    """Load libcpdr.so and declare its signatures (raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, sz = ctypes.c_void_p, ctypes.c_size_t
+        st = ctypes.c_int
+        lib.cpdr_ctx_create.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(vp)]
+        lib.cpdr_ctx_destroy.argtypes = [vp]
+        lib.cpdr_ctx_destroy.restype = None
+        lib.cpdr_buffer_sizes.argtypes = [vp] + [ctypes.POINTER(sz)] * 4
+        lib.cpdr_plan_num_fragments.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        lib.cpdr_plan_fragments.argtypes = [vp, ctypes.POINTER(Fragment), ctypes.c_int32]
+        lib.cpdr_plan_counts.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        lib.cpdr_preprocess.argtypes = [vp] * 8
+        lib.cpdr_merge.argtypes = [vp] * 5
+        lib.cpdr_fwd.argtypes = [vp] * 10
+        lib.cpdr_host_workspace_bytes.argtypes = [vp, ctypes.POINTER(sz)]
+        lib.cpdr_forward_host.argtypes = [vp] * 9 + [sz, vp]
+        lib.cpdr_check_device_status.argtypes = [vp, vp]
+        for name in EXPORTED:
+            f = getattr(lib, name)
+            if name not in ("cpdr_ctx_destroy", "cpdr_last_error", "cpdr_version"):
+                f.restype = st
+        lib.cpdr_last_error.restype = ctypes.c_char_p
+        lib.cpdr_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != OK:
+        raise CpdrError(status, load().cpdr_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Context:
+    """One planned problem: shapes, the R-segment cut, dtype and gate kind.
+
+    ``gate`` is "gdn" (scalar gate g [B,T,H]) or "kda" (per-dim gk [B,T,H,d]);
+    ``dtype`` is "fp32" or "bf16" for q, k, v, beta and o; gates are fp32.
+    With ``cu_seqlens`` (N+1 offsets) the batch is packed: B must be 1.
+    """
+
+    def __init__(self, B, T, H, d, R, gate="gdn", dtype="bf16", cu_seqlens=None, scale=1.0,
+                 host_only=False, force_simt=False):
+        lib = load()
+        self.B, self.T, self.H, self.d, self.R = int(B), int(T), int(H), int(d), int(R)
+        self.gate, self.dtype = gate, dtype
+        self.torch_dtype = torch.float32 if dtype == "fp32" else torch.bfloat16
+        self._cu = None
+        n = self.B
+        cu_ptr = None
+        if cu_seqlens is not None:
+            cu = [int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+            self._cu = (ctypes.c_int64 * len(cu))(*cu)
+            cu_ptr = ctypes.cast(self._cu, ctypes.POINTER(ctypes.c_int64))
+            n = len(cu) - 1
+        self.N = n
+        flags = (FLAG_HOST_ONLY if host_only else 0) | (FLAG_FORCE_SIMT if force_simt else 0)
+        desc = Desc(self.B, self.H, self.d, self.d, self.R, n, self.T, cu_ptr,
+                    0 if gate == "gdn" else 1, 0 if dtype == "fp32" else 1, flags, float(scale))
+        h = ctypes.c_void_p()
+        _check(lib.cpdr_ctx_create(ctypes.byref(desc), ctypes.byref(h)))
+        self._h = h
+        self._lib = lib
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.cpdr_ctx_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---- plan ---------------------------------------------------------
+    def fragments(self):
+        n = ctypes.c_int32()
+        _check(self._lib.cpdr_plan_num_fragments(self._h, ctypes.byref(n)))
+        arr = (Fragment * max(1, n.value))()
+        _check(self._lib.cpdr_plan_fragments(self._h, arr, n.value))
+        return [(f.tok0, f.len, f.seg, f.seq, f.flags) for f in arr[:n.value]]
+
+    def counts(self):
+        """Plan counters: fragments, pre items, merge chains, zeroed S_ext/M
+        segments, zeroed S_init segments, empty sequences, kernel launches per
+        step, tensor-core path selected."""
+        out = (ctypes.c_int32 * 8)()
+        _check(self._lib.cpdr_plan_counts(self._h, out))
+        keys = ["fragments", "pre_items", "chains", "zero_pre", "zero_init", "empty_seqs", "launches", "tc"]
+        return dict(zip(keys, list(out)))
+
+    def buffer_sizes(self):
+        s = [ctypes.c_size_t() for _ in range(4)]
+        _check(self._lib.cpdr_buffer_sizes(self._h, *[ctypes.byref(x) for x in s]))
+        return [x.value for x in s]
+
+    def alloc_buffers(self, device="cuda"):
+        """Caller-owned exchange buffers S_ext, M, S_init and final_state (fp32)."""
+        d, R, B, H, N = self.d, self.R, self.B, self.H, self.N
+        f32 = torch.float32
+        return dict(S_ext=torch.empty((R, B, H, d, d), dtype=f32, device=device),
+                    M=torch.empty((R, B, H, d, d), dtype=f32, device=device),
+                    S_init=torch.empty((R, B, H, d, d), dtype=f32, device=device),
+                    final_state=torch.empty((N, H, d, d), dtype=f32, device=device))
+
+    # ---- the three stages ------------------------------------------------
+    def _check_inputs(self, **ts):
+        B, T, H, d = self.B, self.T, self.H, self.d
+        shapes = dict(q=(B, T, H, d), k=(B, T, H, d), v=(B, T, H, d), beta=(B, T, H), o=(B, T, H, d),
+                      g=(B, T, H) if self.gate == "gdn" else (B, T, H, d))
+        for name, t in ts.items():
+            if t is None:
+                continue
+            if tuple(t.shape) != shapes[name]:
+                raise ValueError(f"{name}: expected shape {shapes[name]}, got {tuple(t.shape)}")
+            want = torch.float32 if name == "g" else self.torch_dtype
+            if t.dtype != want:
+                raise ValueError(f"{name}: expected {want}, got {t.dtype}")
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+
+    def preprocess(self, k, v, beta, g, S_ext, M, stream=None):
+        self._check_inputs(k=k, v=v, beta=beta, g=g)
+        _check(self._lib.cpdr_preprocess(self._h, _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(S_ext),
+                                         _ptr(M), _stream(stream)))
+
+    def merge(self, S_ext, M, S_init, stream=None):
+        _check(self._lib.cpdr_merge(self._h, _ptr(S_ext), _ptr(M), _ptr(S_init), _stream(stream)))
+
+    def fwd(self, q, k, v, beta, g, S_init, o, final_state=None, stream=None):
+        self._check_inputs(q=q, k=k, v=v, beta=beta, g=g, o=o)
+        _check(self._lib.cpdr_fwd(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(S_init),
+                                  _ptr(o), _ptr(final_state), _stream(stream)))
+
+    def run(self, q, k, v, beta, g, bufs=None, o=None, stream=None):
+        """preprocess -> merge -> fwd on device tensors; returns (o, buffers)."""
+        if bufs is None:
+            bufs = self.alloc_buffers(q.device)
+        if o is None:
+            o = torch.empty_like(v)
+        self.preprocess(k, v, beta, g, bufs["S_ext"], bufs["M"], stream)
+        self.merge(bufs["S_ext"], bufs["M"], bufs["S_init"], stream)
+        self.fwd(q, k, v, beta, g, bufs["S_init"], o, bufs["final_state"], stream)
+        return o, bufs
+
+    # ---- whole path from host memory --------------------------------------
+    def host_workspace_bytes(self):
+        n = ctypes.c_size_t()
+        _check(self._lib.cpdr_host_workspace_bytes(self._h, ctypes.byref(n)))
+        return n.value
+
+    def forward_host(self, q, k, v, beta, g, o, final_state, workspace, stream=None):
+        """Host tensors in (pinned for async copies), host o / final_state out."""
+        self._check_inputs(q=q, k=k, v=v, beta=beta, g=g, o=o)
+        _check(self._lib.cpdr_forward_host(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(o),
+                                           _ptr(final_state), _ptr(workspace),
+                                           ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                           _stream(stream)))
+
+    def check_device_status(self, stream=None):
+        _check(self._lib.cpdr_check_device_status(self._h, _stream(stream)))

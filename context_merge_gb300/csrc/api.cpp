@@ -1,0 +1,294 @@
+// C-ABI layer: argument validation, the plan's device tables, and dispatch to
+// the kernel launchers.  Declarations and contracts: include/cpdr.h.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "cpdr_internal.hpp"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+cpdr_status set_err(cpdr_status s, const std::string &msg) {
+    g_last_error = msg;
+    return s;
+}
+
+cpdr_status cuda_err(cudaError_t e, const char *what) {
+    return set_err(CPDR_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" +
+                                      cudaGetErrorString(e) + ")");
+}
+
+template <typename T>
+cudaError_t upload(T **dst, const std::vector<T> &src) {
+    *dst = nullptr;
+    if (src.empty()) return cudaSuccess;
+    cudaError_t e = cudaMalloc((void **)dst, sizeof(T) * src.size());
+    if (e != cudaSuccess) return e;
+    return cudaMemcpy(*dst, src.data(), sizeof(T) * src.size(), cudaMemcpyHostToDevice);
+}
+
+void free_tables(cpdr::DeviceTables &t) {
+    cudaFree(t.frags);
+    cudaFree(t.pre_items);
+    cudaFree(t.fwd_order);
+    cudaFree(t.chains);
+    cudaFree(t.zero_pre);
+    cudaFree(t.zero_init);
+    cudaFree(t.empty_seqs);
+    cudaFree(t.status);
+    t = cpdr::DeviceTables();
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+cpdr_status check_ctx(const cpdr_ctx *c) {
+    if (!c) return set_err(CPDR_ERR_INVALID, "null context");
+    if (!c->has_device) return set_err(CPDR_ERR_INVALID, "context was created with CPDR_FLAG_HOST_ONLY");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_err(e, "cudaGetDevice");
+    if (dev != c->device)
+        return set_err(CPDR_ERR_INVALID, "current device differs from the device the context was created on");
+    return CPDR_OK;
+}
+
+cpdr_status check_ptr(const void *p, const char *name, bool nullable = false) {
+    if (!p) {
+        if (nullable) return CPDR_OK;
+        return set_err(CPDR_ERR_INVALID, std::string("null pointer: ") + name);
+    }
+    if (!aligned16(p)) return set_err(CPDR_ERR_INVALID, std::string("pointer not 16-byte aligned: ") + name);
+    return CPDR_OK;
+}
+
+#define CPDR_TRY(x)                          \
+    do {                                     \
+        cpdr_status _s = (x);                \
+        if (_s != CPDR_OK) return _s;        \
+    } while (0)
+
+cpdr_status launch_rc(int rc, const char *what) {
+    if (rc != 0) return cuda_err((cudaError_t)rc, what);
+    return CPDR_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Sizes {
+    size_t qk, v, beta, gate, o, sext, m, sinit, fin;
+};
+
+Sizes sizes_of(const cpdr::Plan &p) {
+    Sizes s;
+    const size_t es = p.in_dtype == CPDR_DTYPE_F32 ? 4 : 2;
+    const size_t tok = (size_t)p.B * (size_t)p.T;
+    s.qk = tok * p.H * p.dk * es;
+    s.v = tok * p.H * p.dv * es;
+    s.beta = tok * p.H * es;
+    s.gate = tok * p.H * (p.gate_kind == CPDR_GATE_PER_DIM ? p.dk : 1) * sizeof(float);
+    s.o = s.v;
+    s.sext = (size_t)p.R * p.B * p.H * p.dk * p.dv * sizeof(float);
+    s.m = (size_t)p.R * p.B * p.H * p.dk * p.dk * sizeof(float);
+    s.sinit = s.sext;
+    s.fin = (size_t)p.N * p.H * p.dk * p.dv * sizeof(float);
+    return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *cpdr_last_error(void) { return g_last_error.c_str(); }
+
+const char *cpdr_version(void) { return "cpdr 0.1 (sm_103a)"; }
+
+cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
+    if (!out) return set_err(CPDR_ERR_INVALID, "null output pointer");
+    *out = nullptr;
+    if (!desc) return set_err(CPDR_ERR_INVALID, "null descriptor");
+    cpdr_ctx *c = new (std::nothrow) cpdr_ctx();
+    if (!c) return set_err(CPDR_ERR_INVALID, "out of host memory");
+    std::string err;
+    cpdr_status s = cpdr::build_plan(*desc, c->plan, err);
+    if (s != CPDR_OK) {
+        delete c;
+        return set_err(s, err);
+    }
+    c->use_tc = false;
+    if (!(desc->flags & CPDR_FLAG_HOST_ONLY)) {
+        cudaError_t e = cudaGetDevice(&c->device);
+        auto &p = c->plan;
+        auto &t = c->dev;
+        if (e == cudaSuccess) e = upload(&t.frags, p.frags);
+        if (e == cudaSuccess) e = upload(&t.pre_items, p.pre_items);
+        if (e == cudaSuccess) e = upload(&t.fwd_order, p.fwd_order);
+        if (e == cudaSuccess) e = upload(&t.chains, p.chains);
+        if (e == cudaSuccess) e = upload(&t.zero_pre, p.zero_pre);
+        if (e == cudaSuccess) e = upload(&t.zero_init, p.zero_init);
+        if (e == cudaSuccess) e = upload(&t.empty_seqs, p.empty_seqs);
+        if (e == cudaSuccess) e = cudaMalloc((void **)&t.status, 64);
+        if (e == cudaSuccess) e = cudaMemset(t.status, 0, 64);
+        if (e != cudaSuccess) {
+            free_tables(t);
+            delete c;
+            return cuda_err(e, "cpdr_ctx_create: device tables");
+        }
+        c->has_device = true;
+    }
+    *out = c;
+    return CPDR_OK;
+}
+
+void cpdr_ctx_destroy(cpdr_ctx *c) {
+    if (!c) return;
+    if (c->has_device) free_tables(c->dev);
+    delete c;
+}
+
+cpdr_status cpdr_buffer_sizes(const cpdr_ctx *c, size_t *sext, size_t *m, size_t *sinit, size_t *fin) {
+    if (!c) return set_err(CPDR_ERR_INVALID, "null context");
+    const Sizes s = sizes_of(c->plan);
+    if (sext) *sext = s.sext;
+    if (m) *m = s.m;
+    if (sinit) *sinit = s.sinit;
+    if (fin) *fin = s.fin;
+    return CPDR_OK;
+}
+
+cpdr_status cpdr_plan_num_fragments(const cpdr_ctx *c, int32_t *n) {
+    if (!c || !n) return set_err(CPDR_ERR_INVALID, "null argument");
+    *n = (int32_t)c->plan.frags.size();
+    return CPDR_OK;
+}
+
+cpdr_status cpdr_plan_fragments(const cpdr_ctx *c, cpdr_fragment *out, int32_t cap) {
+    if (!c || (!out && cap > 0)) return set_err(CPDR_ERR_INVALID, "null argument");
+    const int32_t n = (int32_t)c->plan.frags.size();
+    for (int32_t i = 0; i < n && i < cap; i++) out[i] = c->plan.frags[i];
+    return CPDR_OK;
+}
+
+cpdr_status cpdr_plan_counts(const cpdr_ctx *c, int32_t out[8]) {
+    if (!c || !out) return set_err(CPDR_ERR_INVALID, "null argument");
+    const auto &p = c->plan;
+    out[0] = (int32_t)p.frags.size();
+    out[1] = (int32_t)p.pre_items.size();
+    out[2] = (int32_t)p.chains.size();
+    out[3] = (int32_t)p.zero_pre.size();
+    out[4] = (int32_t)p.zero_init.size();
+    out[5] = (int32_t)p.empty_seqs.size();
+    out[6] = cpdr::launches_per_step(c);
+    out[7] = c->use_tc ? 1 : 0;
+    return CPDR_OK;
+}
+
+cpdr_status cpdr_preprocess(const cpdr_ctx *c, const void *k, const void *v, const void *beta,
+                            const float *gate, float *S_ext, float *M, void *stream) {
+    CPDR_TRY(check_ctx(c));
+    CPDR_TRY(check_ptr(k, "k"));
+    CPDR_TRY(check_ptr(v, "v"));
+    CPDR_TRY(check_ptr(beta, "beta"));
+    CPDR_TRY(check_ptr(gate, "gate"));
+    CPDR_TRY(check_ptr(S_ext, "S_ext"));
+    CPDR_TRY(check_ptr(M, "M"));
+    int rc = c->use_tc ? cpdr::launch_tc_pre(c, k, v, beta, gate, S_ext, M, stream)
+                       : cpdr::launch_simt_pre(c, k, v, beta, gate, S_ext, M, stream);
+    CPDR_TRY(launch_rc(rc, "cpdr_preprocess"));
+    return launch_rc(cpdr::launch_zero_segments(c, S_ext, M, nullptr, nullptr, 0, stream),
+                     "cpdr_preprocess: zero fill");
+}
+
+cpdr_status cpdr_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init, void *stream) {
+    CPDR_TRY(check_ctx(c));
+    CPDR_TRY(check_ptr(S_ext, "S_ext"));
+    CPDR_TRY(check_ptr(M, "M"));
+    CPDR_TRY(check_ptr(S_init, "S_init"));
+    CPDR_TRY(launch_rc(cpdr::launch_zero_segments(c, nullptr, nullptr, S_init, nullptr, 1, stream),
+                       "cpdr_merge: zero fill"));
+    return launch_rc(cpdr::launch_merge(c, S_ext, M, S_init, stream), "cpdr_merge");
+}
+
+cpdr_status cpdr_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta,
+                     const float *gate, const float *S_init, void *o, float *final_state, void *stream) {
+    CPDR_TRY(check_ctx(c));
+    CPDR_TRY(check_ptr(q, "q"));
+    CPDR_TRY(check_ptr(k, "k"));
+    CPDR_TRY(check_ptr(v, "v"));
+    CPDR_TRY(check_ptr(beta, "beta"));
+    CPDR_TRY(check_ptr(gate, "gate"));
+    CPDR_TRY(check_ptr(S_init, "S_init"));
+    CPDR_TRY(check_ptr(o, "o"));
+    CPDR_TRY(check_ptr(final_state, "final_state", true));
+    int rc = c->use_tc ? cpdr::launch_tc_fwd(c, q, k, v, beta, gate, S_init, o, final_state, stream)
+                       : cpdr::launch_simt_fwd(c, q, k, v, beta, gate, S_init, o, final_state, stream);
+    CPDR_TRY(launch_rc(rc, "cpdr_fwd"));
+    return launch_rc(cpdr::launch_zero_segments(c, nullptr, nullptr, nullptr, final_state, 2, stream),
+                     "cpdr_fwd: zero fill");
+}
+
+cpdr_status cpdr_host_workspace_bytes(const cpdr_ctx *c, size_t *bytes) {
+    if (!c || !bytes) return set_err(CPDR_ERR_INVALID, "null argument");
+    const Sizes s = sizes_of(c->plan);
+    *bytes = round256(s.qk) * 2 + round256(s.v) + round256(s.beta) + round256(s.gate) + round256(s.o) +
+             round256(s.sext) + round256(s.m) + round256(s.sinit) + round256(s.fin);
+    return CPDR_OK;
+}
+
+cpdr_status cpdr_forward_host(const cpdr_ctx *c, const void *q, const void *k, const void *v,
+                              const void *beta, const float *gate, void *o, float *final_state,
+                              void *ws, size_t ws_bytes, void *stream) {
+    CPDR_TRY(check_ctx(c));
+    if (!q || !k || !v || !beta || !gate || !o) return set_err(CPDR_ERR_INVALID, "null host pointer");
+    CPDR_TRY(check_ptr(ws, "device_workspace"));
+    size_t need = 0;
+    cpdr_host_workspace_bytes(c, &need);
+    if (ws_bytes < need) return set_err(CPDR_ERR_WORKSPACE, "device workspace too small");
+    if (((uintptr_t)ws & 255u) != 0) return set_err(CPDR_ERR_INVALID, "device workspace not 256-byte aligned");
+    const Sizes s = sizes_of(c->plan);
+    char *p = (char *)ws;
+    auto take = [&](size_t n) { char *r = p; p += round256(n); return r; };
+    void *dq = take(s.qk), *dk = take(s.qk), *dv = take(s.v), *db = take(s.beta);
+    float *dg = (float *)take(s.gate);
+    void *dout = take(s.o);
+    float *dse = (float *)take(s.sext), *dm = (float *)take(s.m), *dsi = (float *)take(s.sinit);
+    float *dfin = (float *)take(s.fin);
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dq, q, s.qk, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k, s.qk, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v, s.v, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(db, beta, s.beta, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dg, gate, s.gate, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: host-to-device copy");
+    CPDR_TRY(cpdr_preprocess(c, dk, dv, db, dg, dse, dm, stream));
+    CPDR_TRY(cpdr_merge(c, dse, dm, dsi, stream));
+    CPDR_TRY(cpdr_fwd(c, dq, dk, dv, db, dg, dsi, dout, dfin, stream));
+    e = cudaMemcpyAsync(o, dout, s.o, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && final_state) e = cudaMemcpyAsync(final_state, dfin, s.fin, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: device-to-host copy");
+    return CPDR_OK;
+}
+
+cpdr_status cpdr_check_device_status(const cpdr_ctx *c, void *stream) {
+    CPDR_TRY(check_ctx(c));
+    int32_t h[16];
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(h, c->dev.status, sizeof(h), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_err(e, "cpdr_check_device_status");
+    if (h[0] != 0) {
+        cudaMemsetAsync(c->dev.status, 0, 64, st);
+        cudaStreamSynchronize(st);
+        char buf[160];
+        snprintf(buf, sizeof(buf), "a bounded device wait gave up: code %d (site %d, block %d)", h[0], h[1], h[2]);
+        return set_err(CPDR_ERR_TIMEOUT, buf);
+    }
+    return CPDR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// Internal declarations shared by the C-ABI layer, the host planner and the
+// kernel launchers.  Nothing here is visible through include/cpdr.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/cpdr.h"
+
+namespace cpdr {
+
+constexpr int kChunk = 64;  // chunk size fixed by the article's Code Flow (chunk_size=64)
+
+// A chain of segments r0 < r1 of one row b crossed by one sequence: the merge
+// scan writes S_init for segments r0+1 .. r1 ([FLA-CP] §2.1 merge, §5.2).
+struct MergeChain {
+    int32_t b, r0, r1, pad;
+};
+
+// Host plan ([FLA-CP] §3.2-§3.3): fragments per segment and the derived
+// work lists.  All token indices are on the flattened [B*T] axis.
+struct Plan {
+    int32_t B = 0, H = 0, dk = 0, dv = 0, R = 0, N = 0;
+    int64_t T = 0;           // tokens per row (or packed total)
+    int64_t L = 0;           // segment length
+    int32_t gate_kind = 0, in_dtype = 0;
+    uint32_t flags = 0;
+    float scale = 1.f;
+    bool packed = false;
+    std::vector<int64_t> cu;                 // N+1 offsets on the flattened axis
+    std::vector<cpdr_fragment> frags;        // every fragment, segment-major order
+    std::vector<int32_t> pre_items;          // fragments with CPDR_FRAG_CONT_NEXT
+    std::vector<int32_t> fwd_order;          // fragments, longest first (fwd launch order)
+    std::vector<MergeChain> chains;          // sequences spanning >= 2 segments
+    std::vector<int32_t> zero_pre;           // segment indices with no continuing fragment
+    std::vector<int32_t> zero_init;          // segment indices whose S_init is zero
+    std::vector<int32_t> empty_seqs;         // zero-length sequences (final state = 0)
+    int32_t max_pre_chunks = 0, max_fwd_chunks = 0;
+
+    int32_t nseg() const { return R * B; }
+};
+
+// Builds the plan; returns CPDR_OK or an error with `err` set.
+cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err);
+
+// Device copies of the plan tables.
+struct DeviceTables {
+    cpdr_fragment *frags = nullptr;
+    int32_t *pre_items = nullptr;
+    int32_t *fwd_order = nullptr;
+    MergeChain *chains = nullptr;
+    int32_t *zero_pre = nullptr;
+    int32_t *zero_init = nullptr;
+    int32_t *empty_seqs = nullptr;
+    int32_t *status = nullptr;   // device status word (bounded waits)
+};
+
+}  // namespace cpdr
+
+struct cpdr_ctx {
+    cpdr::Plan plan;
+    cpdr::DeviceTables dev;
+    bool has_device = false;
+    bool use_tc = false;        // tcgen05 kernels for the bf16, d = 128 path
+    int device = -1;
+};
+
+namespace cpdr {
+
+// Launchers (kernels live in the .cu files).  Each returns a CUDA error code
+// (0 = success) of the launch it enqueued.
+int launch_simt_pre(const cpdr_ctx *c, const void *k, const void *v, const void *beta,
+                    const float *g, float *S_ext, float *M, void *stream);
+int launch_simt_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v,
+                    const void *beta, const float *g, const float *S_init, void *o,
+                    float *final_state, void *stream);
+int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init,
+                 void *stream);
+int launch_zero_segments(const cpdr_ctx *c, float *S_ext, float *M, float *S_init,
+                         float *final_state, int which, void *stream);
+// Number of kernels one preprocess + merge + fwd step enqueues (final_state given).
+int launches_per_step(const cpdr_ctx *c);
+
+int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const void *beta,
+                  const float *g, float *S_ext, float *M, void *stream);
+int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v,
+                  const void *beta, const float *g, const float *S_init, void *o,
+                  float *final_state, void *stream);
+
+}  // namespace cpdr

@@ -1,0 +1,204 @@
+/*
+ * cpdr.h -- C ABI of the segmented ("True CP") gated delta-rule forward for
+ * GB300 (sm_103a).
+ *
+ * The operation is the one described in the article
+ *   "flash-linear-attention 上下文并行CP从 CP2TP、Ring CP 到 True CP 的设计取舍
+ *    与源码实现"                                     (cited below as [FLA-CP])
+ * run on ONE GPU with the sequence cut into R contiguous segments that play
+ * the role of context-parallel ranks:
+ *
+ *   per token      S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *                  o_t = scale * S_t^T q_t                      alpha_t = exp(g_t)
+ *   preprocess     every segment j computes, from a zero state, the state of
+ *                  its trailing fragment S_ext,j (dk x dv) and the product of
+ *                  that fragment's transfer matrices M_j (dk x dk), in the
+ *                  chunk (WY) form with 64-token chunks    ([FLA-CP] §2.1-§2.3)
+ *   merge          S_init,r = sum over predecessors: S <- M_j S + S_ext,j
+ *                                                          ([FLA-CP] §2.1, §5.2)
+ *   fwd            every fragment restarts from S_init (its segment's first
+ *                  fragment, when it continues a sequence) or zero, and emits
+ *                  o and the final state of sequences ending in it
+ *                                                          ([FLA-CP] §4, §5.2)
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * Layout.  q, k: [B, T, H, dk]; v, o: [B, T, H, dv]; beta: [B, T, H];
+ *          gate: [B, T, H] (scalar, GDN) or [B, T, H, dk] (per key dim, KDA),
+ *          all contiguous, row-major.  Packed variable-length batches use
+ *          B == 1 and global cu_seqlens ([FLA-CP] §3.1, §4 NOTE).
+ *          S_ext, S_init: [R, B, H, dk, dv] fp32; M: [R, B, H, dk, dk] fp32
+ *          (entry (r, b, h) belongs to segment r of row b; the layout of the
+ *          gathered buffer of [FLA-CP] §2.4 with world_size = R);
+ *          final_state: [N, H, dk, dv] fp32 ([N, HV, K, V] of the KDA
+ *          initial_state description in hyper-parallel issue #7).
+ * Types.   q, k, v, beta, o share the input dtype (fp32 or bf16); gates are
+ *          fp32 natural-log gates g = log(alpha).  Arithmetic is fp32 or
+ *          bf16 tensor-core products with fp32 accumulation; the M chain is
+ *          kept at fp32 accuracy ([FLA-CP] §2.2).
+ * Memory.  Every tensor argument is a DEVICE pointer owned by the caller, and
+ *          must be 16-byte aligned.  The library owns only the cpdr_ctx
+ *          (host tables plus small device metadata allocated at create).
+ *          No call below allocates device memory.
+ * Streams. `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *          stream).  Calls enqueue work and return; they never synchronise.
+ * Errors.  Every call validates its arguments on the host before any
+ *          launch and returns a cpdr_status; on failure nothing is launched
+ *          and cpdr_last_error() gives a message (thread-local).  Launch
+ *          failures come back as CPDR_ERR_CUDA.
+ */
+#ifndef CPDR_H_
+#define CPDR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CPDR_OK = 0,
+    CPDR_ERR_INVALID = 1,      /* bad shapes, cut rule violated, null/misaligned pointers */
+    CPDR_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. dk != dv, d not in {64,128}) */
+    CPDR_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    CPDR_ERR_WORKSPACE = 4,    /* a caller-provided buffer is too small */
+    CPDR_ERR_TIMEOUT = 5       /* a bounded device-side wait gave up (see cpdr_check_device_status) */
+} cpdr_status;
+
+/* desc.flags */
+#define CPDR_FLAG_HOST_ONLY   (1u << 0)  /* plan only: no device tables; launch calls are rejected */
+#define CPDR_FLAG_FORCE_SIMT  (1u << 1)  /* use the fp32 CUDA-core kernels even where tensor cores apply */
+
+/* desc.gate_kind */
+#define CPDR_GATE_SCALAR  0   /* GDN: g [B, T, H] */
+#define CPDR_GATE_PER_DIM 1   /* KDA: gk [B, T, H, dk] */
+
+/* desc.in_dtype */
+#define CPDR_DTYPE_F32  0
+#define CPDR_DTYPE_BF16 1
+
+typedef struct {
+    int32_t B, H, dk, dv;   /* batch rows, heads, key dim, value dim */
+    int32_t R;              /* number of contiguous segments (virtual context ranks) */
+    int32_t num_seqs;       /* N: sequences (== B without cu_seqlens) */
+    int64_t T;              /* tokens per row, or total tokens when packed */
+    const int64_t *cu_seqlens_host; /* NULL: B rows of T tokens; else N+1 global offsets
+                                       (host memory, read during create only), B == 1 */
+    int32_t gate_kind;      /* CPDR_GATE_* */
+    int32_t in_dtype;       /* CPDR_DTYPE_* */
+    uint32_t flags;         /* CPDR_FLAG_* */
+    float scale;            /* output scale */
+} cpdr_desc;
+
+typedef struct cpdr_ctx cpdr_ctx;
+
+/* One local fragment: the intersection of a segment with a sequence. */
+typedef struct {
+    int64_t tok0;    /* first token on the flattened [B*T] token axis */
+    int32_t len;     /* tokens (>= 1) */
+    int32_t seg;     /* segment buffer index r*B + b */
+    int32_t seq;     /* sequence index */
+    int32_t flags;   /* CPDR_FRAG_* */
+} cpdr_fragment;
+
+#define CPDR_FRAG_CONT_PREV 1   /* continues a sequence from segment r-1: starts from S_init[seg] */
+#define CPDR_FRAG_CONT_NEXT 2   /* continues into segment r+1: pre-processed into S_ext/M[seg] */
+#define CPDR_FRAG_ENDS_SEQ  4   /* the sequence ends here: final_state[seq] is written */
+
+/*
+ * Build the partition plan ([FLA-CP] §3.2-§3.3: contiguous layout, the cut
+ * rule "tokens >= R and divisible by R" per row, searchsorted-style
+ * intersection of the global cu_seqlens with each segment) and upload its
+ * small device tables (unless CPDR_FLAG_HOST_ONLY).  The plan is built once
+ * and reused, like the memoised context of [FLA-CP] §3.3.
+ * Errors: CPDR_ERR_INVALID (cut rule, non-monotone cu_seqlens, B != 1 with
+ * cu_seqlens, non-positive sizes), CPDR_ERR_UNSUPPORTED (dk != dv or
+ * d not in {64, 128}), CPDR_ERR_CUDA (table upload).  *out is NULL on error.
+ */
+cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out);
+
+/* Free the context and its device tables.  NULL is accepted. */
+void cpdr_ctx_destroy(cpdr_ctx *ctx);
+
+/* Byte sizes of the caller-owned exchange buffers S_ext, M, S_init and of
+ * final_state.  Any pointer may be NULL. */
+cpdr_status cpdr_buffer_sizes(const cpdr_ctx *ctx, size_t *sext_bytes, size_t *m_bytes,
+                              size_t *sinit_bytes, size_t *final_bytes);
+
+/* Plan introspection (host memory): number of fragments, and a copy of the
+ * fragment table into out[0 .. min(cap, n)). */
+cpdr_status cpdr_plan_num_fragments(const cpdr_ctx *ctx, int32_t *n);
+cpdr_status cpdr_plan_fragments(const cpdr_ctx *ctx, cpdr_fragment *out, int32_t cap);
+
+/* Plan counters (host memory): out[0] fragments, [1] pre-processed
+ * fragments, [2] merge chains, [3] segments with zeroed S_ext/M, [4]
+ * segments with zeroed S_init, [5] empty sequences, [6] kernel launches per
+ * preprocess+merge+fwd step, [7] 1 if the tensor-core kernels are selected. */
+cpdr_status cpdr_plan_counts(const cpdr_ctx *ctx, int32_t out[8]);
+
+/*
+ * Pre-process ([FLA-CP] §2.1-§2.3, pre_process_fwd in its Code Flow of §4):
+ * for every segment whose trailing fragment continues into the next
+ * segment, S_ext = state of that fragment from zero, M = chained transfer
+ * matrix  M <- (Diag(gamma^C) - (Gamma ⊙ K)^T W) M  over its 64-token
+ * chunks.  Entries of segments with no continuing fragment are zeroed.
+ * In: k, v, beta, gate (device).  Out: S_ext, M (device, sizes from
+ * cpdr_buffer_sizes).
+ */
+cpdr_status cpdr_preprocess(const cpdr_ctx *ctx, const void *k, const void *v, const void *beta,
+                            const float *gate, float *S_ext, float *M, void *stream);
+
+/*
+ * Merge ([FLA-CP] §2.1; ownership rule of §5.2): for every segment r whose
+ * first fragment continues a sequence begun in segment r - n_pre,
+ *     S = 0;  for j = r - n_pre .. r - 1:  S <- M_j S + S_ext,j
+ * and S_init[r] = S; all other entries are zeroed.  Evaluated as one
+ * sequential scan per sequence (equal in exact arithmetic).
+ */
+cpdr_status cpdr_merge(const cpdr_ctx *ctx, const float *S_ext, const float *M, float *S_init,
+                       void *stream);
+
+/*
+ * Forward ([FLA-CP] §4, chunk_gated_delta_rule_fwd_h plus the output step):
+ * every fragment runs the 64-token chunk recurrence from S_init[seg] (first
+ * fragment continuing a sequence) or zero, writes o = scale * S_t^T q_t per
+ * token and, when its sequence ends there, final_state[seq].
+ * final_state may be NULL.
+ */
+cpdr_status cpdr_fwd(const cpdr_ctx *ctx, const void *q, const void *k, const void *v,
+                     const void *beta, const float *gate, const float *S_init, void *o,
+                     float *final_state, void *stream);
+
+/*
+ * Whole path from HOST memory: copies q, k, v, beta, gate into the
+ * caller-provided device workspace, runs preprocess, merge and fwd on
+ * `stream`, and copies o and final_state back (host pointers; use pinned
+ * memory for asynchronous copies).  Returns after enqueuing; the caller
+ * synchronises the stream before reading o.  The workspace must hold
+ * cpdr_host_workspace_bytes() bytes (256-byte aligned device memory).
+ */
+cpdr_status cpdr_host_workspace_bytes(const cpdr_ctx *ctx, size_t *bytes);
+cpdr_status cpdr_forward_host(const cpdr_ctx *ctx, const void *q, const void *k, const void *v,
+                              const void *beta, const float *gate, void *o, float *final_state,
+                              void *device_workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Device status: kernels that wait on an mbarrier do so for a bounded number
+ * of polls; when a wait gives up, the kernel records a nonzero code in the
+ * context's device status word and returns instead of hanging.  This call
+ * synchronises `stream`, reads and clears that word, and returns
+ * CPDR_ERR_TIMEOUT (with the code in the message) if it was set.
+ */
+cpdr_status cpdr_check_device_status(const cpdr_ctx *ctx, void *stream);
+
+/* Thread-local message for the last non-OK status of this thread. */
+const char *cpdr_last_error(void);
+
+/* Library version string. */
+const char *cpdr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CPDR_H_ */

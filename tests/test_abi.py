@@ -1,0 +1,74 @@
+"""The C-ABI library loads, exports every symbol include/cpdr.h declares, and
+validates on the host before touching the GPU (no compute call here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from context_merge_gb300 import cpdr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "cpdr.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cpdr_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(cpdr_lib):
+    names = declared_symbols()
+    assert "cpdr_preprocess" in names and "cpdr_merge" in names and "cpdr_fwd" in names
+    for name in names:
+        assert hasattr(cpdr_lib, name), name
+    assert set(cpdr.EXPORTED) >= set(names)
+
+
+def test_version(cpdr_lib):
+    assert b"sm_103a" in cpdr_lib.cpdr_version()
+
+
+def make(**kw):
+    base = dict(B=1, T=1024, H=2, d=64, R=4, gate="gdn", dtype="fp32", host_only=True)
+    base.update(kw)
+    return cpdr.Context(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=1000, R=3), cpdr.ERR_INVALID),            # not divisible
+    (dict(T=2, R=4), cpdr.ERR_INVALID),               # fewer tokens than segments
+    (dict(d=96), cpdr.ERR_UNSUPPORTED),
+    (dict(B=2, T=100, cu_seqlens=[0, 50, 100], R=2), cpdr.ERR_INVALID),   # packed needs B == 1
+    (dict(T=100, cu_seqlens=[0, 60, 50, 100], R=2), cpdr.ERR_INVALID),   # non-monotone
+    (dict(T=100, cu_seqlens=[0, 60, 90], R=2), cpdr.ERR_INVALID),        # does not end at T
+    (dict(R=0), cpdr.ERR_INVALID),
+])
+def test_create_validation(cpdr_lib, kw, status):
+    with pytest.raises(cpdr.CpdrError) as ei:
+        make(**kw)
+    assert ei.value.status == status
+    assert cpdr_lib.cpdr_last_error()
+
+
+def test_host_only_context_rejects_launches(cpdr_lib):
+    ctx = make()
+    rc = cpdr_lib.cpdr_merge(ctx._h, ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), None)
+    assert rc == cpdr.ERR_INVALID
+    assert b"HOST_ONLY" in cpdr_lib.cpdr_last_error()
+
+
+def test_null_descriptor(cpdr_lib):
+    h = ctypes.c_void_p()
+    assert cpdr_lib.cpdr_ctx_create(None, ctypes.byref(h)) == cpdr.ERR_INVALID
+    assert not h.value
+
+
+def test_buffer_sizes(cpdr_lib):
+    ctx = make(B=2, T=512, H=3, d=128, R=8, dtype="bf16")
+    se, m, si, fin = ctx.buffer_sizes()
+    assert se == si == 8 * 2 * 3 * 128 * 128 * 4
+    assert m == se
+    assert fin == 2 * 3 * 128 * 128 * 4
+    ws = ctx.host_workspace_bytes()
+    assert ws >= 3 * 2 * 512 * 3 * 128 * 2 + se + m + si + fin

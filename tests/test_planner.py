@@ -1,0 +1,86 @@
+"""Host planner (segment/fragment tables) against the article's cut rules:
+golden fragment tables for the test-matrix cut patterns and the debug
+example (tests/golden/partitions.json, each with its citation), plus
+structural properties on other patterns.  CPU only."""
+import json
+import os
+
+import pytest
+
+from context_merge_gb300 import cpdr
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "partitions.json")))
+
+
+def ctx_for(lengths, R, H=1, d=64):
+    cu = [0]
+    for x in lengths:
+        cu.append(cu[-1] + x)
+    return cpdr.Context(B=1, T=cu[-1], H=H, d=d, R=R, gate="gdn", dtype="bf16", cu_seqlens=cu, host_only=True)
+
+
+@pytest.mark.parametrize("case", GOLD["cases"], ids=[c["name"] for c in GOLD["cases"]])
+def test_golden_fragments(cpdr_lib, case):
+    frags = ctx_for(case["lengths"], case["R"]).fragments()
+    assert [list(f) for f in frags] == case["fragments"]
+    if "chunk_starts" in case:
+        starts = [list(range(f[0], f[0] + f[1], 64)) for f in frags]
+        assert starts == case["chunk_starts"]
+
+
+@pytest.mark.parametrize("case", GOLD["invalid"], ids=[c["cite"] for c in GOLD["invalid"]])
+def test_golden_invalid(cpdr_lib, case):
+    with pytest.raises(cpdr.CpdrError) as ei:
+        ctx_for(case["lengths"], case["R"])
+    assert ei.value.status == cpdr.ERR_INVALID
+
+
+def check_structure(frags, cu, R):
+    T = cu[-1]
+    L = T // R
+    # fragments tile the token axis in order, never cross a segment or sequence boundary
+    pos = 0
+    for tok0, ln, seg, seq, fl in frags:
+        assert tok0 == pos and ln >= 1
+        pos += ln
+        assert tok0 // L == seg and (tok0 + ln - 1) // L == seg
+        assert cu[seq] <= tok0 and tok0 + ln <= cu[seq + 1]
+        assert bool(fl & cpdr.FRAG_CONT_PREV) == (cu[seq] < tok0)
+        assert bool(fl & cpdr.FRAG_ENDS_SEQ) == (tok0 + ln == cu[seq + 1])
+        assert bool(fl & cpdr.FRAG_CONT_NEXT) == (tok0 + ln < cu[seq + 1])
+    assert pos == T
+    # only a segment's first fragment may continue, only its last may cross
+    by_seg = {}
+    for f in frags:
+        by_seg.setdefault(f[2], []).append(f)
+    for seg, fs in by_seg.items():
+        for f in fs[1:]:
+            assert not f[4] & cpdr.FRAG_CONT_PREV
+        for f in fs[:-1]:
+            assert not f[4] & cpdr.FRAG_CONT_NEXT
+
+
+@pytest.mark.parametrize("lengths,R", [
+    ([5, 7, 6, 9, 4, 11, 6, 16], 2),      # many short sequences
+    ([64] * 8, 4),                         # cuts exactly on sequence starts
+    ([100, 0, 28], 2),                     # an empty sequence
+    ([1] * 64, 64),                        # one token per segment
+    ([4097, 3, 4092], 4),
+])
+def test_structure(cpdr_lib, lengths, R):
+    cu = [0]
+    for x in lengths:
+        cu.append(cu[-1] + x)
+    check_structure(ctx_for(lengths, R).fragments(), cu, R)
+
+
+def test_fixed_rows(cpdr_lib):
+    ctx = cpdr.Context(B=3, T=256, H=1, d=64, R=4, gate="gdn", dtype="fp32", host_only=True)
+    frags = ctx.fragments()
+    assert len(frags) == 12
+    for r in range(4):
+        for b in range(3):
+            f = frags[r * 3 + b] if False else [x for x in frags if x[2] == r * 3 + b][0]
+            assert f[0] == b * 256 + r * 64 and f[1] == 64 and f[3] == b
+            want = (cpdr.FRAG_CONT_PREV if r > 0 else 0) | (cpdr.FRAG_CONT_NEXT if r < 3 else cpdr.FRAG_ENDS_SEQ)
+            assert f[4] == want
