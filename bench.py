@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-heads", type=int, default=4)
     ap.add_argument("--force-simt", action="store_true")
+    # profiling aids: shrink the workload (same shapes otherwise) for ncu captures
+    ap.add_argument("--T", type=int, default=None, help="override tokens per row (profiling only)")
+    ap.add_argument("--H", type=int, default=None, help="override heads (profiling only)")
     return ap.parse_args()
 
 
@@ -243,7 +246,7 @@ def run_ours(args, ws, rank, local):
     from context_merge_gb300 import cpdr
     w = inputs.WORKLOADS[args.workload]
     dev = torch.device("cuda", torch.cuda.current_device())
-    inp = inputs.make_inputs(w, device=dev, seed=w.seed + 1000 * rank)
+    inp = inputs.make_inputs(w, device=dev, seed=w.seed + 1000 * rank, T=args.T, H=args.H)
     B, T, H, d, R = inp["B"], inp["T"], inp["H"], inp["d"], inp["R"]
     ctx = cpdr.Context(B, T, H, d, R, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"],
                        force_simt=args.force_simt)

@@ -119,7 +119,7 @@ cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
         delete c;
         return set_err(s, err);
     }
-    c->use_tc = false;
+    c->use_tc = cpdr::tc_supported(c->plan) && !(desc->flags & CPDR_FLAG_FORCE_SIMT);
     if (!(desc->flags & CPDR_FLAG_HOST_ONLY)) {
         cudaError_t e = cudaGetDevice(&c->device);
         auto &p = c->plan;

@@ -80,6 +80,9 @@ int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S
                  void *stream);
 int launch_zero_segments(const cpdr_ctx *c, float *S_ext, float *M, float *S_init,
                          float *final_state, int which, void *stream);
+// True when the tcgen05 kernels cover this problem (bf16, dk = dv = 128, scalar gate).
+bool tc_supported(const Plan &p);
+
 // Number of kernels one preprocess + merge + fwd step enqueues (final_state given).
 int launches_per_step(const cpdr_ctx *c);
 
