@@ -485,7 +485,7 @@ int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S
 int launches_per_step(const cpdr_ctx *c) {
     const auto &p = c->plan;
     int n = 0;
-    n += p.pre_items.empty() ? 0 : 1;          // pre-process
+    n += p.pre_items.empty() ? 0 : (c->use_tc ? 2 : 1);   // pre-process (S and M kernels on the tensor-core path)
     n += p.zero_pre.empty() ? 0 : 2;           // zero S_ext and M
     n += p.zero_init.empty() ? 0 : 1;          // zero S_init
     n += p.chains.empty() ? 0 : 1;             // merge

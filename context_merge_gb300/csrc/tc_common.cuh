@@ -37,6 +37,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Same, but the thread may stay suspended (not issuing) for up to `ns`
+// nanoseconds while the phase is incomplete; it resumes when the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 
 // Shared control block: an abort flag every bounded wait checks, so that one
 // expired wait makes every other role fall through to the kernel's teardown.
@@ -48,14 +61,14 @@ struct Ctl {
 // About two seconds at the maximum SM clock.
 constexpr long long kWaitCycles = 4000000000LL;
 
-// Bounded wait on phase `parity`.  On expiry records (code, site, block) in
-// the device status word, raises the CTA's abort flag and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of the bounded wait (kept out of line: it is rare and would
+// otherwise be inlined at every wait site).
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
     const long long t0 = clock64();
     for (;;) {
+        // suspended (not spinning) while the phase is incomplete
+        if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
         if (ctl->abort) return false;
-        if (mbar_try_wait(bar, parity)) return true;
         if (clock64() - t0 > kWaitCycles) {
             if (atomicCAS(status, 0, 1) == 0) {
                 status[1] = site;
@@ -65,6 +78,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Ctl *c
             return false;
         }
     }
+}
+// Bounded wait on phase `parity`.  On expiry records (code, site, block) in
+// the device status word, raises the CTA's abort flag and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, ctl, status, site);
 }
 
 // ------------------------------------------------------------------ fences
@@ -139,6 +158,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+// 32 lanes x 16 columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
