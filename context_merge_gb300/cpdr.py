@@ -25,7 +25,7 @@ FRAG_CONT_PREV, FRAG_CONT_NEXT, FRAG_ENDS_SEQ = 1, 2, 4
 
 EXPORTED = ["cpdr_ctx_create", "cpdr_ctx_destroy", "cpdr_buffer_sizes", "cpdr_plan_num_fragments",
             "cpdr_plan_fragments", "cpdr_plan_counts", "cpdr_preprocess", "cpdr_merge", "cpdr_fwd", "cpdr_host_workspace_bytes",
-            "cpdr_forward_host", "cpdr_check_device_status", "cpdr_last_error", "cpdr_version"]
+            "cpdr_forward_host", "cpdr_forward_noalloc", "cpdr_check_device_status", "cpdr_last_error", "cpdr_version"]
 
 
 class CpdrError(RuntimeError):
@@ -73,6 +73,7 @@ def load():
         lib.cpdr_fwd.argtypes = [vp] * 10
         lib.cpdr_host_workspace_bytes.argtypes = [vp, ctypes.POINTER(sz)]
         lib.cpdr_forward_host.argtypes = [vp] * 9 + [sz, vp]
+        lib.cpdr_forward_noalloc.argtypes = [vp] * 9
         lib.cpdr_check_device_status.argtypes = [vp, vp]
         for name in EXPORTED:
             f = getattr(lib, name)
@@ -225,6 +226,14 @@ class Context:
                                            _ptr(final_state), _ptr(workspace),
                                            ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                                            _stream(stream)))
+
+    def forward_noalloc(self, q, k, v, beta, g, o, final_state=None, stream=None):
+        """Whole path through the allocation-free entry point: the library
+        keeps its exchange buffers and tables in a fixed device array and
+        allocates nothing (works with a host_only context)."""
+        self._check_inputs(q=q, k=k, v=v, beta=beta, g=g, o=o)
+        _check(self._lib.cpdr_forward_noalloc(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(o),
+                                              _ptr(final_state), _stream(stream)))
 
     def check_device_status(self, stream=None):
         _check(self._lib.cpdr_check_device_status(self._h, _stream(stream)))

@@ -101,6 +101,12 @@ Sizes sizes_of(const cpdr::Plan &p) {
 
 }  // namespace
 
+namespace cpdr {
+// Records `msg` as this thread's last error and returns `s` (for other
+// translation units of the library).
+cpdr_status fail_with(cpdr_status s, const std::string &msg) { return set_err(s, msg); }
+}  // namespace cpdr
+
 extern "C" {
 
 const char *cpdr_last_error(void) { return g_last_error.c_str(); }

@@ -83,6 +83,9 @@ int launch_zero_segments(const cpdr_ctx *c, float *S_ext, float *M, float *S_ini
 // True when the tcgen05 kernels cover this problem (bf16, dk = dv = 128, scalar gate).
 bool tc_supported(const Plan &p);
 
+// Sets this thread's last-error message and returns the status.
+cpdr_status fail_with(cpdr_status s, const std::string &msg);
+
 // Number of kernels one preprocess + merge + fwd step enqueues (final_state given).
 int launches_per_step(const cpdr_ctx *c);
 

@@ -1,0 +1,124 @@
+// Allocation-free whole-path entry point (cpdr_forward_noalloc).
+//
+// Some callers cannot allocate device memory at all: for example code that
+// runs inside a runtime which owns every byte of device memory through its
+// own pool or static memory plan, where an allocation would break the plan,
+// or a process that must keep its device footprint fixed after start-up.
+// Such callers cannot create the caller-owned exchange buffers (S_ext, M,
+// S_init) nor let the context allocate its device tables.  This entry point
+// serves them: it keeps everything the path needs besides the caller's
+// inputs and outputs -- the status word of the bounded waits, the plan
+// tables and the three exchange buffers -- in one file-scope device array
+// of fixed size, and calls no allocating routine.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "cpdr_internal.hpp"
+
+namespace {
+
+// Fixed maximum of the static scratch: 16 MiB per device.  Every GPU that
+// loads the library holds this array until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_cpdr_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_mu;                 // serialises set-up and the context swap below
+void *g_scratch_addr[256] = {};  // device address of the array, per device (set up once)
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" cpdr_status cpdr_forward_noalloc(const cpdr_ctx *c, const void *q, const void *k, const void *v,
+                                            const void *beta, const float *gate, void *o, float *final_state,
+                                            void *stream) {
+    if (!c) return cpdr::fail_with(CPDR_ERR_INVALID, "null context");
+    if (!q || !k || !v || !beta || !gate || !o) return cpdr::fail_with(CPDR_ERR_INVALID, "null device pointer");
+    const cpdr::Plan &p = c->plan;
+    // scratch layout: status word | plan tables | S_ext | M | S_init
+    const size_t n_frag = p.frags.size(), n_pre = p.pre_items.size(), n_ch = p.chains.size();
+    const size_t b_status = 256;
+    const size_t b_frags = round256(n_frag * sizeof(cpdr_fragment));
+    const size_t b_pre = round256(n_pre * sizeof(int32_t)), b_ord = round256(n_frag * sizeof(int32_t));
+    const size_t b_ch = round256(n_ch * sizeof(cpdr::MergeChain));
+    const size_t b_zp = round256(p.zero_pre.size() * sizeof(int32_t));
+    const size_t b_zi = round256(p.zero_init.size() * sizeof(int32_t));
+    const size_t b_es = round256(p.empty_seqs.size() * sizeof(int32_t));
+    const size_t per_seg = (size_t)p.R * p.B * p.H * p.dk;
+    const size_t b_sext = round256(per_seg * p.dv * sizeof(float)), b_m = round256(per_seg * p.dk * sizeof(float));
+    const size_t need = b_status + b_frags + b_pre + b_ord + b_ch + b_zp + b_zi + b_es + 2 * b_sext + b_m;
+    if (need > kNoAllocScratchBytes) {
+        char buf[256];
+        snprintf(buf, sizeof(buf),
+                 "cpdr_forward_noalloc: this problem needs %zu bytes of device scratch (exchange buffers "
+                 "R*B*H*dk*(2*dv+dk)*4 bytes plus plan tables); the allocation-free entry point holds at most %zu",
+                 need, kNoAllocScratchBytes);
+        return cpdr::fail_with(CPDR_ERR_WORKSPACE, buf);
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 256)
+        return cpdr::fail_with(CPDR_ERR_CUDA, "cpdr_forward_noalloc: no current device");
+    if (!g_scratch_addr[dev]) {
+        // set-up, once per device, with that device current: the array's
+        // host-side name is not a device address; ask the runtime for it
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_cpdr_noalloc_scratch);
+        if (e != cudaSuccess || !addr)
+            return cpdr::fail_with(CPDR_ERR_CUDA, std::string("cpdr_forward_noalloc: cudaGetSymbolAddress: ") +
+                                                      cudaGetErrorString(e));
+        g_scratch_addr[dev] = addr;
+    }
+    char *base = static_cast<char *>(g_scratch_addr[dev]);
+    cpdr::DeviceTables t;
+    char *cur = base;
+    auto take = [&](size_t n) { char *r = cur; cur += n; return r; };
+    t.status = reinterpret_cast<int32_t *>(take(b_status));
+    t.frags = reinterpret_cast<cpdr_fragment *>(take(b_frags));
+    t.pre_items = reinterpret_cast<int32_t *>(take(b_pre));
+    t.fwd_order = reinterpret_cast<int32_t *>(take(b_ord));
+    t.chains = reinterpret_cast<cpdr::MergeChain *>(take(b_ch));
+    t.zero_pre = reinterpret_cast<int32_t *>(take(b_zp));
+    t.zero_init = reinterpret_cast<int32_t *>(take(b_zi));
+    t.empty_seqs = reinterpret_cast<int32_t *>(take(b_es));
+    float *S_ext = reinterpret_cast<float *>(take(b_sext));
+    float *M = reinterpret_cast<float *>(take(b_m));
+    float *S_init = reinterpret_cast<float *>(take(b_sext));
+    // the array keeps the previous call's contents: clear the status word,
+    // copy this context's tables (the exchange buffers are fully written)
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(t.status, 0, b_status, st);
+    auto put = [&](void *dst, const void *src, size_t n) {
+        if (e == cudaSuccess && n) e = cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st);
+    };
+    put(t.frags, p.frags.data(), n_frag * sizeof(cpdr_fragment));
+    put(t.pre_items, p.pre_items.data(), n_pre * sizeof(int32_t));
+    put(t.fwd_order, p.fwd_order.data(), n_frag * sizeof(int32_t));
+    put(t.chains, p.chains.data(), n_ch * sizeof(cpdr::MergeChain));
+    put(t.zero_pre, p.zero_pre.data(), p.zero_pre.size() * sizeof(int32_t));
+    put(t.zero_init, p.zero_init.data(), p.zero_init.size() * sizeof(int32_t));
+    put(t.empty_seqs, p.empty_seqs.data(), p.empty_seqs.size() * sizeof(int32_t));
+    if (e != cudaSuccess)
+        return cpdr::fail_with(CPDR_ERR_CUDA, std::string("cpdr_forward_noalloc: table upload: ") + cudaGetErrorString(e));
+    // run the three stages against the static tables: the context is
+    // pointed at them for the duration of the launches and restored after
+    cpdr_ctx *mc = const_cast<cpdr_ctx *>(c);
+    const cpdr::DeviceTables saved = mc->dev;
+    const bool saved_has = mc->has_device;
+    const int saved_dev = mc->device;
+    mc->dev = t;
+    mc->has_device = true;
+    mc->device = dev;
+    cpdr_status s = cpdr_preprocess(c, k, v, beta, gate, S_ext, M, stream);
+    if (s == CPDR_OK) s = cpdr_merge(c, S_ext, M, S_init, stream);
+    if (s == CPDR_OK) s = cpdr_fwd(c, q, k, v, beta, gate, S_init, o, final_state, stream);
+    mc->dev = saved;
+    mc->has_device = saved_has;
+    mc->device = saved_dev;
+    return s;
+}

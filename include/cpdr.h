@@ -184,6 +184,33 @@ cpdr_status cpdr_forward_host(const cpdr_ctx *ctx, const void *q, const void *k,
                               void *device_workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Allocation-free whole path (no counterpart in the article: it is an
+ * interface for callers that cannot allocate device memory, e.g. code inside
+ * a runtime that owns all device memory through its own pool or static
+ * memory plan).  Runs preprocess, merge and fwd like the three calls above,
+ * but keeps everything except the caller's inputs and outputs -- the
+ * exchange buffers S_ext, M, S_init, the plan tables and the status word of
+ * the bounded waits -- in one file-scope device array of 16 MiB per device
+ * (held by every GPU that loads the library until the process exits).  It
+ * calls no cudaMalloc, cudaFree or other allocating routine, and accepts a
+ * context created with CPDR_FLAG_HOST_ONLY.
+ * In: q, k, v, beta, gate (device).  Out: o, final_state (device; final_state
+ * may be NULL).  Errors: CPDR_ERR_WORKSPACE when the problem needs more than
+ * the array holds (R*B*H*dk*(2*dv + dk)*4 bytes of exchange buffers plus the
+ * plan tables), CPDR_ERR_INVALID / CPDR_ERR_CUDA as for the other calls.
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array and overwrites
+ * it: calls whose work overlaps on the GPU (other streams, other contexts)
+ * race, and a call must not run concurrently with another call on the same
+ * context from another host thread.  A bounded wait that expires inside this
+ * call records its code in the array's status word (cleared at the start of
+ * every call), not in the context's.
+ */
+cpdr_status cpdr_forward_noalloc(const cpdr_ctx *ctx, const void *q, const void *k, const void *v,
+                                 const void *beta, const float *gate, void *o, float *final_state, void *stream);
+
+/*
  * Device status: kernels that wait on an mbarrier do so for a bounded number
  * of polls; when a wait gives up, the kernel records a nonzero code in the
  * context's device status word and returns instead of hanging.  This call
