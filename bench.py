@@ -176,7 +176,10 @@ def stage_bytes(w, ctx, inp):
     pre = pre_tok * tok_bytes_pre + n_pre * 2 * state
     # merge: every chain step reads M_j and S_ext_j once and writes S_init
     merge = n_cont * 3 * state
-    return {"pre": pre, "merge": merge, "fwd": fwd, "chains": c["chains"]}
+    # WY build: k, beta and g of every token (the tiles it writes are an
+    # intermediate of this implementation, not algorithmic bytes)
+    wy = tokens * H * (d * es + es + gate_w * 4) if c["tc"] else 0
+    return {"wy": wy, "pre": pre, "merge": merge, "fwd": fwd, "chains": c["chains"]}
 
 
 def traffic_record(kernel_tag):
@@ -255,25 +258,30 @@ def run_ours(args, ws, rank, local):
     q, k, v, beta, g = (inp[x] for x in ("q", "k", "v", "beta", "g"))
     stream = torch.cuda.current_stream()
 
+    wy = bufs["wy"]
+
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        ctx.preprocess(k, v, beta, g, bufs["S_ext"], bufs["M"], stream)
+        ctx.wy_build(k, beta, g, wy, stream)
         if ev is not None:
             ev[1].record(stream)
-        ctx.merge(bufs["S_ext"], bufs["M"], bufs["S_init"], stream)
+        ctx.preprocess(k, v, beta, g, bufs["S_ext"], bufs["M"], wy=wy, stream=stream)
         if ev is not None:
             ev[2].record(stream)
-        ctx.fwd(q, k, v, beta, g, bufs["S_init"], o, bufs["final_state"], stream)
+        ctx.merge(bufs["S_ext"], bufs["M"], bufs["S_init"], stream)
         if ev is not None:
             ev[3].record(stream)
+        ctx.fwd(q, k, v, beta, g, bufs["S_init"], o, bufs["final_state"], wy=wy, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     ctx.check_device_status()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks = ClockSampler() if rank == 0 else None
     if clocks:
         clocks.start()
@@ -290,11 +298,10 @@ def run_ours(args, ws, rank, local):
     clk = clocks.stop() if clocks else None
     ctx.check_device_status()
     elapsed_ms = start.elapsed_time(end)
-    stage_ms = {"pre": [], "merge": [], "fwd": []}
+    stage_ms = {"wy": [], "pre": [], "merge": [], "fwd": []}
     for e in evs:
-        stage_ms["pre"].append(e[0].elapsed_time(e[1]))
-        stage_ms["merge"].append(e[1].elapsed_time(e[2]))
-        stage_ms["fwd"].append(e[2].elapsed_time(e[3]))
+        for j, name in enumerate(stage_ms):
+            stage_ms[name].append(e[j].elapsed_time(e[j + 1]))
     elapsed_ms = max_over_ranks(elapsed_ms, ws)
     tokens = B * T
     value = tokens * ws * args.steps / (elapsed_ms / 1e3)
@@ -332,7 +339,7 @@ def run_ours(args, ws, rank, local):
     # ---- roofline of the dominant stage (HBM-bound)
     nbytes = stage_bytes(w, ctx, inp)
     mean_ms = {s: statistics.mean(v) for s, v in stage_ms.items()}
-    dom = max(("pre", "fwd"), key=lambda s: mean_ms[s])
+    dom = max(("wy", "pre", "fwd"), key=lambda s: mean_ms[s])
     peak, peak_kind = hbm_peak()
     achieved = nbytes[dom] / (mean_ms[dom] / 1e3) / 1e9
     counts = ctx.counts()

@@ -24,7 +24,8 @@ FLAG_FORCE_SIMT = 1 << 1
 FRAG_CONT_PREV, FRAG_CONT_NEXT, FRAG_ENDS_SEQ = 1, 2, 4
 
 EXPORTED = ["cpdr_ctx_create", "cpdr_ctx_destroy", "cpdr_buffer_sizes", "cpdr_plan_num_fragments",
-            "cpdr_plan_fragments", "cpdr_plan_counts", "cpdr_preprocess", "cpdr_merge", "cpdr_fwd", "cpdr_host_workspace_bytes",
+            "cpdr_plan_fragments", "cpdr_plan_counts", "cpdr_wy_bytes", "cpdr_wy_build", "cpdr_preprocess",
+            "cpdr_merge", "cpdr_fwd", "cpdr_host_workspace_bytes",
             "cpdr_forward_host", "cpdr_forward_noalloc", "cpdr_check_device_status", "cpdr_last_error", "cpdr_version"]
 
 
@@ -68,9 +69,11 @@ def load():
         lib.cpdr_plan_num_fragments.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         lib.cpdr_plan_fragments.argtypes = [vp, ctypes.POINTER(Fragment), ctypes.c_int32]
         lib.cpdr_plan_counts.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
-        lib.cpdr_preprocess.argtypes = [vp] * 8
+        lib.cpdr_wy_bytes.argtypes = [vp, ctypes.POINTER(sz)]
+        lib.cpdr_wy_build.argtypes = [vp] * 6
+        lib.cpdr_preprocess.argtypes = [vp] * 9
         lib.cpdr_merge.argtypes = [vp] * 5
-        lib.cpdr_fwd.argtypes = [vp] * 10
+        lib.cpdr_fwd.argtypes = [vp] * 11
         lib.cpdr_host_workspace_bytes.argtypes = [vp, ctypes.POINTER(sz)]
         lib.cpdr_forward_host.argtypes = [vp] * 9 + [sz, vp]
         lib.cpdr_forward_noalloc.argtypes = [vp] * 9
@@ -164,14 +167,23 @@ class Context:
         _check(self._lib.cpdr_buffer_sizes(self._h, *[ctypes.byref(x) for x in s]))
         return [x.value for x in s]
 
+    def wy_bytes(self):
+        """Bytes of the WY tile workspace (0 on the CUDA-core path)."""
+        n = ctypes.c_size_t()
+        _check(self._lib.cpdr_wy_bytes(self._h, ctypes.byref(n)))
+        return n.value
+
     def alloc_buffers(self, device="cuda"):
-        """Caller-owned exchange buffers S_ext, M, S_init and final_state (fp32)."""
+        """Caller-owned exchange buffers S_ext, M, S_init and final_state (fp32)
+        and the WY tile workspace ``wy`` (bytes; None when not needed)."""
         d, R, B, H, N = self.d, self.R, self.B, self.H, self.N
         f32 = torch.float32
+        nwy = self.wy_bytes()
         return dict(S_ext=torch.empty((R, B, H, d, d), dtype=f32, device=device),
                     M=torch.empty((R, B, H, d, d), dtype=f32, device=device),
                     S_init=torch.empty((R, B, H, d, d), dtype=f32, device=device),
-                    final_state=torch.empty((N, H, d, d), dtype=f32, device=device))
+                    final_state=torch.empty((N, H, d, d), dtype=f32, device=device),
+                    wy=torch.empty(nwy, dtype=torch.uint8, device=device) if nwy else None)
 
     # ---- the three stages ------------------------------------------------
     def _check_inputs(self, **ts):
@@ -189,28 +201,34 @@ class Context:
             if not t.is_contiguous():
                 raise ValueError(f"{name} must be contiguous")
 
-    def preprocess(self, k, v, beta, g, S_ext, M, stream=None):
+    def wy_build(self, k, beta, g, wy, stream=None):
+        self._check_inputs(k=k, beta=beta, g=g)
+        _check(self._lib.cpdr_wy_build(self._h, _ptr(k), _ptr(beta), _ptr(g), _ptr(wy), _stream(stream)))
+
+    def preprocess(self, k, v, beta, g, S_ext, M, wy=None, stream=None):
         self._check_inputs(k=k, v=v, beta=beta, g=g)
-        _check(self._lib.cpdr_preprocess(self._h, _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(S_ext),
+        _check(self._lib.cpdr_preprocess(self._h, _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(wy), _ptr(S_ext),
                                          _ptr(M), _stream(stream)))
 
     def merge(self, S_ext, M, S_init, stream=None):
         _check(self._lib.cpdr_merge(self._h, _ptr(S_ext), _ptr(M), _ptr(S_init), _stream(stream)))
 
-    def fwd(self, q, k, v, beta, g, S_init, o, final_state=None, stream=None):
+    def fwd(self, q, k, v, beta, g, S_init, o, final_state=None, wy=None, stream=None):
         self._check_inputs(q=q, k=k, v=v, beta=beta, g=g, o=o)
-        _check(self._lib.cpdr_fwd(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(S_init),
-                                  _ptr(o), _ptr(final_state), _stream(stream)))
+        _check(self._lib.cpdr_fwd(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(wy),
+                                  _ptr(S_init), _ptr(o), _ptr(final_state), _stream(stream)))
 
     def run(self, q, k, v, beta, g, bufs=None, o=None, stream=None):
-        """preprocess -> merge -> fwd on device tensors; returns (o, buffers)."""
+        """WY build -> preprocess -> merge -> fwd on device tensors; returns (o, buffers)."""
         if bufs is None:
             bufs = self.alloc_buffers(q.device)
         if o is None:
             o = torch.empty_like(v)
-        self.preprocess(k, v, beta, g, bufs["S_ext"], bufs["M"], stream)
+        wy = bufs.get("wy")
+        self.wy_build(k, beta, g, wy, stream)
+        self.preprocess(k, v, beta, g, bufs["S_ext"], bufs["M"], wy=wy, stream=stream)
         self.merge(bufs["S_ext"], bufs["M"], bufs["S_init"], stream)
-        self.fwd(q, k, v, beta, g, bufs["S_init"], o, bufs["final_state"], stream)
+        self.fwd(q, k, v, beta, g, bufs["S_init"], o, bufs["final_state"], wy=wy, stream=stream)
         return o, bufs
 
     # ---- whole path from host memory --------------------------------------

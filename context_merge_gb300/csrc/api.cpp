@@ -40,6 +40,8 @@ void free_tables(cpdr::DeviceTables &t) {
     cudaFree(t.zero_pre);
     cudaFree(t.zero_init);
     cudaFree(t.empty_seqs);
+    cudaFree(t.frag_chunk0);
+    cudaFree(t.wy_chunks);
     cudaFree(t.status);
     t = cpdr::DeviceTables();
 }
@@ -137,6 +139,8 @@ cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
         if (e == cudaSuccess) e = upload(&t.zero_pre, p.zero_pre);
         if (e == cudaSuccess) e = upload(&t.zero_init, p.zero_init);
         if (e == cudaSuccess) e = upload(&t.empty_seqs, p.empty_seqs);
+        if (e == cudaSuccess) e = upload(&t.frag_chunk0, p.frag_chunk0);
+        if (e == cudaSuccess) e = upload(&t.wy_chunks, p.wy_chunks);
         if (e == cudaSuccess) e = cudaMalloc((void **)&t.status, 64);
         if (e == cudaSuccess) e = cudaMemset(t.status, 0, 64);
         if (e != cudaSuccess) {
@@ -193,16 +197,34 @@ cpdr_status cpdr_plan_counts(const cpdr_ctx *c, int32_t out[8]) {
     return CPDR_OK;
 }
 
+cpdr_status cpdr_wy_bytes(const cpdr_ctx *c, size_t *bytes) {
+    if (!c || !bytes) return set_err(CPDR_ERR_INVALID, "null argument");
+    *bytes = cpdr::wy_bytes(c);
+    return CPDR_OK;
+}
+
+cpdr_status cpdr_wy_build(const cpdr_ctx *c, const void *k, const void *beta, const float *gate, void *wy,
+                          void *stream) {
+    CPDR_TRY(check_ctx(c));
+    if (cpdr::wy_bytes(c) == 0) return CPDR_OK;
+    CPDR_TRY(check_ptr(k, "k"));
+    CPDR_TRY(check_ptr(beta, "beta"));
+    CPDR_TRY(check_ptr(gate, "gate"));
+    CPDR_TRY(check_ptr(wy, "wy"));
+    return launch_rc(cpdr::launch_tc_wy(c, k, beta, gate, wy, stream), "cpdr_wy_build");
+}
+
 cpdr_status cpdr_preprocess(const cpdr_ctx *c, const void *k, const void *v, const void *beta,
-                            const float *gate, float *S_ext, float *M, void *stream) {
+                            const float *gate, const void *wy, float *S_ext, float *M, void *stream) {
     CPDR_TRY(check_ctx(c));
     CPDR_TRY(check_ptr(k, "k"));
     CPDR_TRY(check_ptr(v, "v"));
     CPDR_TRY(check_ptr(beta, "beta"));
     CPDR_TRY(check_ptr(gate, "gate"));
+    CPDR_TRY(check_ptr(wy, "wy", cpdr::wy_bytes(c) == 0));
     CPDR_TRY(check_ptr(S_ext, "S_ext"));
     CPDR_TRY(check_ptr(M, "M"));
-    int rc = c->use_tc ? cpdr::launch_tc_pre(c, k, v, beta, gate, S_ext, M, stream)
+    int rc = c->use_tc ? cpdr::launch_tc_pre(c, k, v, gate, wy, S_ext, M, stream)
                        : cpdr::launch_simt_pre(c, k, v, beta, gate, S_ext, M, stream);
     CPDR_TRY(launch_rc(rc, "cpdr_preprocess"));
     return launch_rc(cpdr::launch_zero_segments(c, S_ext, M, nullptr, nullptr, 0, stream),
@@ -220,17 +242,19 @@ cpdr_status cpdr_merge(const cpdr_ctx *c, const float *S_ext, const float *M, fl
 }
 
 cpdr_status cpdr_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta,
-                     const float *gate, const float *S_init, void *o, float *final_state, void *stream) {
+                     const float *gate, const void *wy, const float *S_init, void *o, float *final_state,
+                     void *stream) {
     CPDR_TRY(check_ctx(c));
     CPDR_TRY(check_ptr(q, "q"));
     CPDR_TRY(check_ptr(k, "k"));
     CPDR_TRY(check_ptr(v, "v"));
     CPDR_TRY(check_ptr(beta, "beta"));
     CPDR_TRY(check_ptr(gate, "gate"));
+    CPDR_TRY(check_ptr(wy, "wy", cpdr::wy_bytes(c) == 0));
     CPDR_TRY(check_ptr(S_init, "S_init"));
     CPDR_TRY(check_ptr(o, "o"));
     CPDR_TRY(check_ptr(final_state, "final_state", true));
-    int rc = c->use_tc ? cpdr::launch_tc_fwd(c, q, k, v, beta, gate, S_init, o, final_state, stream)
+    int rc = c->use_tc ? cpdr::launch_tc_fwd(c, q, k, v, gate, wy, S_init, o, final_state, stream)
                        : cpdr::launch_simt_fwd(c, q, k, v, beta, gate, S_init, o, final_state, stream);
     CPDR_TRY(launch_rc(rc, "cpdr_fwd"));
     return launch_rc(cpdr::launch_zero_segments(c, nullptr, nullptr, nullptr, final_state, 2, stream),
@@ -241,7 +265,8 @@ cpdr_status cpdr_host_workspace_bytes(const cpdr_ctx *c, size_t *bytes) {
     if (!c || !bytes) return set_err(CPDR_ERR_INVALID, "null argument");
     const Sizes s = sizes_of(c->plan);
     *bytes = round256(s.qk) * 2 + round256(s.v) + round256(s.beta) + round256(s.gate) + round256(s.o) +
-             round256(s.sext) + round256(s.m) + round256(s.sinit) + round256(s.fin);
+             round256(s.sext) + round256(s.m) + round256(s.sinit) + round256(s.fin) +
+             round256(cpdr::wy_bytes(c));
     return CPDR_OK;
 }
 
@@ -263,6 +288,8 @@ cpdr_status cpdr_forward_host(const cpdr_ctx *c, const void *q, const void *k, c
     void *dout = take(s.o);
     float *dse = (float *)take(s.sext), *dm = (float *)take(s.m), *dsi = (float *)take(s.sinit);
     float *dfin = (float *)take(s.fin);
+    const size_t nwy = cpdr::wy_bytes(c);
+    void *dwy = nwy ? take(nwy) : nullptr;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
     if (e == cudaSuccess) e = cudaMemcpyAsync(dq, q, s.qk, cudaMemcpyHostToDevice, st);
@@ -271,9 +298,10 @@ cpdr_status cpdr_forward_host(const cpdr_ctx *c, const void *q, const void *k, c
     if (e == cudaSuccess) e = cudaMemcpyAsync(db, beta, s.beta, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dg, gate, s.gate, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: host-to-device copy");
-    CPDR_TRY(cpdr_preprocess(c, dk, dv, db, dg, dse, dm, stream));
+    CPDR_TRY(cpdr_wy_build(c, dk, db, dg, dwy, stream));
+    CPDR_TRY(cpdr_preprocess(c, dk, dv, db, dg, dwy, dse, dm, stream));
     CPDR_TRY(cpdr_merge(c, dse, dm, dsi, stream));
-    CPDR_TRY(cpdr_fwd(c, dq, dk, dv, db, dg, dsi, dout, dfin, stream));
+    CPDR_TRY(cpdr_fwd(c, dq, dk, dv, db, dg, dwy, dsi, dout, dfin, stream));
     e = cudaMemcpyAsync(o, dout, s.o, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess && final_state) e = cudaMemcpyAsync(final_state, dfin, s.fin, cudaMemcpyDeviceToHost, st);
     if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: device-to-host copy");

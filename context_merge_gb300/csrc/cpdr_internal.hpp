@@ -19,6 +19,19 @@ struct MergeChain {
     int32_t b, r0, r1, pad;
 };
 
+// One chunk of one fragment (the unit of the WY build): first token on the
+// flattened axis and its number of valid rows (<= 64; the rest is padding).
+struct WyChunk {
+    int64_t tok0;
+    int32_t nv, pad;
+};
+
+// Bytes of the WY tiles of one (chunk, head): T' = T diag(beta), and
+// T'' = T diag(beta gamma) as a bf16 hi/lo pair, each a 64 x 64 bf16 tile
+// stored as the 128-byte-swizzled shared-memory image the MMA reads.
+constexpr size_t kWyTileBytes = 8192;
+constexpr size_t kWyUnitBytes = 3 * kWyTileBytes;
+
 // Host plan ([FLA-CP] §3.2-§3.3): fragments per segment and the derived
 // work lists.  All token indices are on the flattened [B*T] axis.
 struct Plan {
@@ -38,6 +51,8 @@ struct Plan {
     std::vector<int32_t> zero_init;          // segment indices whose S_init is zero
     std::vector<int32_t> empty_seqs;         // zero-length sequences (final state = 0)
     int32_t max_pre_chunks = 0, max_fwd_chunks = 0;
+    std::vector<int32_t> frag_chunk0;        // first global chunk of each fragment (+ total)
+    std::vector<WyChunk> wy_chunks;          // every chunk of every fragment
 
     int32_t nseg() const { return R * B; }
 };
@@ -54,6 +69,8 @@ struct DeviceTables {
     int32_t *zero_pre = nullptr;
     int32_t *zero_init = nullptr;
     int32_t *empty_seqs = nullptr;
+    int32_t *frag_chunk0 = nullptr;
+    WyChunk *wy_chunks = nullptr;
     int32_t *status = nullptr;   // device status word (bounded waits)
 };
 
@@ -89,10 +106,14 @@ cpdr_status fail_with(cpdr_status s, const std::string &msg);
 // Number of kernels one preprocess + merge + fwd step enqueues (final_state given).
 int launches_per_step(const cpdr_ctx *c);
 
-int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const void *beta,
-                  const float *g, float *S_ext, float *M, void *stream);
-int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v,
-                  const void *beta, const float *g, const float *S_init, void *o,
-                  float *final_state, void *stream);
+// Bytes of the WY tile workspace (0 when the CUDA-core kernels are used).
+size_t wy_bytes(const cpdr_ctx *c);
+
+int launch_tc_wy(const cpdr_ctx *c, const void *k, const void *beta, const float *g, void *wy,
+                 void *stream);
+int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy,
+                  float *S_ext, float *M, void *stream);
+int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const float *g,
+                  const void *wy, const float *S_init, void *o, float *final_state, void *stream);
 
 }  // namespace cpdr

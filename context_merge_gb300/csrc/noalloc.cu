@@ -8,7 +8,7 @@
 // S_init) nor let the context allocate its device tables.  This entry point
 // serves them: it keeps everything the path needs besides the caller's
 // inputs and outputs -- the status word of the bounded waits, the plan
-// tables and the three exchange buffers -- in one file-scope device array
+// tables, the WY tiles and the three exchange buffers -- in one file-scope device array
 // of fixed size, and calls no allocating routine.
 #include <cuda_runtime.h>
 
@@ -21,9 +21,9 @@
 
 namespace {
 
-// Fixed maximum of the static scratch: 16 MiB per device.  Every GPU that
+// Fixed maximum of the static scratch: 32 MiB per device.  Every GPU that
 // loads the library holds this array until the process exits.
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_cpdr_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mu;                 // serialises set-up and the context swap below
@@ -39,7 +39,7 @@ extern "C" cpdr_status cpdr_forward_noalloc(const cpdr_ctx *c, const void *q, co
     if (!c) return cpdr::fail_with(CPDR_ERR_INVALID, "null context");
     if (!q || !k || !v || !beta || !gate || !o) return cpdr::fail_with(CPDR_ERR_INVALID, "null device pointer");
     const cpdr::Plan &p = c->plan;
-    // scratch layout: status word | plan tables | S_ext | M | S_init
+    // scratch layout: status word | plan tables | S_ext | M | S_init | WY tiles
     const size_t n_frag = p.frags.size(), n_pre = p.pre_items.size(), n_ch = p.chains.size();
     const size_t b_status = 256;
     const size_t b_frags = round256(n_frag * sizeof(cpdr_fragment));
@@ -48,14 +48,19 @@ extern "C" cpdr_status cpdr_forward_noalloc(const cpdr_ctx *c, const void *q, co
     const size_t b_zp = round256(p.zero_pre.size() * sizeof(int32_t));
     const size_t b_zi = round256(p.zero_init.size() * sizeof(int32_t));
     const size_t b_es = round256(p.empty_seqs.size() * sizeof(int32_t));
+    const size_t b_c0 = round256(p.frag_chunk0.size() * sizeof(int32_t));
+    const size_t b_wc = round256(p.wy_chunks.size() * sizeof(cpdr::WyChunk));
+    const size_t b_wy = round256(cpdr::wy_bytes(c));
     const size_t per_seg = (size_t)p.R * p.B * p.H * p.dk;
     const size_t b_sext = round256(per_seg * p.dv * sizeof(float)), b_m = round256(per_seg * p.dk * sizeof(float));
-    const size_t need = b_status + b_frags + b_pre + b_ord + b_ch + b_zp + b_zi + b_es + 2 * b_sext + b_m;
+    const size_t need =
+        b_status + b_frags + b_pre + b_ord + b_ch + b_zp + b_zi + b_es + b_c0 + b_wc + 2 * b_sext + b_m + b_wy;
     if (need > kNoAllocScratchBytes) {
         char buf[256];
         snprintf(buf, sizeof(buf),
                  "cpdr_forward_noalloc: this problem needs %zu bytes of device scratch (exchange buffers "
-                 "R*B*H*dk*(2*dv+dk)*4 bytes plus plan tables); the allocation-free entry point holds at most %zu",
+                 "R*B*H*dk*(2*dv+dk)*4 bytes, WY tiles and plan tables); the allocation-free entry point holds at "
+                 "most %zu",
                  need, kNoAllocScratchBytes);
         return cpdr::fail_with(CPDR_ERR_WORKSPACE, buf);
     }
@@ -86,9 +91,12 @@ extern "C" cpdr_status cpdr_forward_noalloc(const cpdr_ctx *c, const void *q, co
     t.zero_pre = reinterpret_cast<int32_t *>(take(b_zp));
     t.zero_init = reinterpret_cast<int32_t *>(take(b_zi));
     t.empty_seqs = reinterpret_cast<int32_t *>(take(b_es));
+    t.frag_chunk0 = reinterpret_cast<int32_t *>(take(b_c0));
+    t.wy_chunks = reinterpret_cast<cpdr::WyChunk *>(take(b_wc));
     float *S_ext = reinterpret_cast<float *>(take(b_sext));
     float *M = reinterpret_cast<float *>(take(b_m));
     float *S_init = reinterpret_cast<float *>(take(b_sext));
+    void *wy = b_wy ? take(b_wy) : nullptr;
     // the array keeps the previous call's contents: clear the status word,
     // copy this context's tables (the exchange buffers are fully written)
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -103,6 +111,8 @@ extern "C" cpdr_status cpdr_forward_noalloc(const cpdr_ctx *c, const void *q, co
     put(t.zero_pre, p.zero_pre.data(), p.zero_pre.size() * sizeof(int32_t));
     put(t.zero_init, p.zero_init.data(), p.zero_init.size() * sizeof(int32_t));
     put(t.empty_seqs, p.empty_seqs.data(), p.empty_seqs.size() * sizeof(int32_t));
+    put(t.frag_chunk0, p.frag_chunk0.data(), p.frag_chunk0.size() * sizeof(int32_t));
+    put(t.wy_chunks, p.wy_chunks.data(), p.wy_chunks.size() * sizeof(cpdr::WyChunk));
     if (e != cudaSuccess)
         return cpdr::fail_with(CPDR_ERR_CUDA, std::string("cpdr_forward_noalloc: table upload: ") + cudaGetErrorString(e));
     // run the three stages against the static tables: the context is
@@ -114,9 +124,10 @@ extern "C" cpdr_status cpdr_forward_noalloc(const cpdr_ctx *c, const void *q, co
     mc->dev = t;
     mc->has_device = true;
     mc->device = dev;
-    cpdr_status s = cpdr_preprocess(c, k, v, beta, gate, S_ext, M, stream);
+    cpdr_status s = cpdr_wy_build(c, k, beta, gate, wy, stream);
+    if (s == CPDR_OK) s = cpdr_preprocess(c, k, v, beta, gate, wy, S_ext, M, stream);
     if (s == CPDR_OK) s = cpdr_merge(c, S_ext, M, S_init, stream);
-    if (s == CPDR_OK) s = cpdr_fwd(c, q, k, v, beta, gate, S_init, o, final_state, stream);
+    if (s == CPDR_OK) s = cpdr_fwd(c, q, k, v, beta, gate, wy, S_init, o, final_state, stream);
     mc->dev = saved;
     mc->has_device = saved_has;
     mc->device = saved_dev;

@@ -116,6 +116,18 @@ cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err) {
     // longest pre items first as well
     std::stable_sort(p.pre_items.begin(), p.pre_items.end(),
                      [&](int32_t a, int32_t b) { return p.frags[a].len > p.frags[b].len; });
+    // every chunk of every fragment, fragment by fragment (the WY tiles'
+    // order): fragment f's chunk c is global chunk frag_chunk0[f] + c
+    p.frag_chunk0.resize(p.frags.size() + 1);
+    int32_t acc = 0;
+    for (size_t i = 0; i < p.frags.size(); i++) {
+        const cpdr_fragment &f = p.frags[i];
+        p.frag_chunk0[i] = acc;
+        for (int32_t c = 0; c < chunks(f.len); c++)
+            p.wy_chunks.push_back(WyChunk{f.tok0 + (int64_t)c * kChunk, std::min(kChunk, f.len - c * kChunk), 0});
+        acc += chunks(f.len);
+    }
+    p.frag_chunk0.back() = acc;
     return CPDR_OK;
 }
 

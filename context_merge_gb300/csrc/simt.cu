@@ -342,46 +342,87 @@ simt_pre_kernel(const cpdr_fragment *__restrict__ frags, const int32_t *__restri
     }
 }
 
-// Merge: grid (chains, H, D / BV).  S = S_ext[r0]; then for j = r0+1 .. r1-1:
+// Merge: grid (chains, H, D / MBV).  S = S_ext[r0]; then for j = r0+1 .. r1-1:
 // S <- M_j S + S_ext[j]; S_init[j] written after each step (S_init[r0+1] = S_ext[r0]).
+// Each thread owns an (RPT x 4) register tile of the (D x MBV) state tile; M_j is
+// staged row-major in shared memory with cp.async, the next step's M prefetched
+// while the current one is applied.
+constexpr int MBV = 16;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 template <int D>
 __global__ void __launch_bounds__(NT, 1)
 merge_kernel(const MergeChain *__restrict__ chains, const float *__restrict__ S_ext,
              const float *__restrict__ M, float *__restrict__ S_init, int H, int B) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float *Ms = reinterpret_cast<float *>(smem_raw);          // D x (D + 1)
-    float *Ss = Ms + D * (D + 1);                              // D x (BV + 1)
-    constexpr int LM = D + 1, LB = BV + 1;
+    constexpr int LM = D + 4;                                  // padded row stride (16-byte rows)
+    constexpr int RPT = D / 64;                                // rows per thread
+    float *Mn = reinterpret_cast<float *>(smem_raw);           // [2][D][LM]
+    float *Ss = Mn + 2 * D * LM;                               // [D][MBV]
     const MergeChain ch = chains[blockIdx.x];
-    const int h = blockIdx.y, col0 = blockIdx.z * BV;
+    const int h = blockIdx.y, col0 = blockIdx.z * MBV;
     auto idx_of = [&](int r) { return ((int64_t)(r * B + ch.b) * H + h) * D * D; };
-    for (int idx = threadIdx.x; idx < D * BV; idx += NT) {
-        const int d = idx / BV, c = idx % BV;
+    auto stage_M = [&](int j, int buf) {
+        const float *Mj = M + idx_of(j);
+        float *dst = Mn + buf * D * LM;
+        for (int idx = threadIdx.x; idx < D * D / 4; idx += NT) {
+            const int d = idx / (D / 4), l4 = idx % (D / 4);
+            cp_async16(dst + d * LM + 4 * l4, Mj + d * D + 4 * l4);
+        }
+        cp_async_commit();
+    };
+    for (int idx = threadIdx.x; idx < D * MBV; idx += NT) {
+        const int d = idx / MBV, c = idx % MBV;
         const float x = S_ext[idx_of(ch.r0) + d * D + col0 + c];
-        Ss[d * LB + c] = x;
+        Ss[d * MBV + c] = x;
         S_init[idx_of(ch.r0 + 1) + d * D + col0 + c] = x;
     }
-    const int c = threadIdx.x % BV, db = threadIdx.x / BV;
-    constexpr int RPT = D / 8;
+    if (ch.r0 + 1 < ch.r1) stage_M(ch.r0 + 1, 0);
+    const int rb = threadIdx.x >> 2, cb = (threadIdx.x & 3) * 4;
     for (int j = ch.r0 + 1; j < ch.r1; j++) {
-        __syncthreads();
-        const float *Mj = M + idx_of(j);
-        for (int idx = threadIdx.x; idx < D * D; idx += NT) Ms[(idx / D) * LM + idx % D] = Mj[idx];
-        __syncthreads();
-        float acc[RPT];
-#pragma unroll
-        for (int r = 0; r < RPT; r++) acc[r] = S_ext[idx_of(j) + (db * RPT + r) * D + col0 + c];
-        for (int l = 0; l < D; l++) {
-            const float sv = Ss[l * LB + c];
-#pragma unroll
-            for (int r = 0; r < RPT; r++) acc[r] = fmaf(Ms[(db * RPT + r) * LM + l], sv, acc[r]);
-        }
-        __syncthreads();
+        const int buf = (j - ch.r0 - 1) & 1;
+        cp_async_wait_all();
+        __syncthreads();   // M_j staged; the previous step's state tile written
+        if (j + 1 < ch.r1) stage_M(j + 1, buf ^ 1);
+        const float *Mb = Mn + buf * D * LM;
+        float acc[RPT][4];
 #pragma unroll
         for (int r = 0; r < RPT; r++) {
-            const int d = db * RPT + r;
-            Ss[d * LB + c] = acc[r];
-            S_init[idx_of(j + 1) + d * D + col0 + c] = acc[r];
+            const float4 e = *reinterpret_cast<const float4 *>(S_ext + idx_of(j) + (RPT * rb + r) * D + col0 + cb);
+            acc[r][0] = e.x; acc[r][1] = e.y; acc[r][2] = e.z; acc[r][3] = e.w;
+        }
+#pragma unroll 2
+        for (int l = 0; l < D; l += 4) {
+            float4 sv[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) sv[u] = *reinterpret_cast<const float4 *>(Ss + (l + u) * MBV + cb);
+#pragma unroll
+            for (int r = 0; r < RPT; r++) {
+                const float4 m = *reinterpret_cast<const float4 *>(Mb + (RPT * rb + r) * LM + l);
+                const float mv[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    acc[r][0] = fmaf(mv[u], sv[u].x, acc[r][0]);
+                    acc[r][1] = fmaf(mv[u], sv[u].y, acc[r][1]);
+                    acc[r][2] = fmaf(mv[u], sv[u].z, acc[r][2]);
+                    acc[r][3] = fmaf(mv[u], sv[u].w, acc[r][3]);
+                }
+            }
+        }
+        __syncthreads();   // every thread has read the old state tile
+#pragma unroll
+        for (int r = 0; r < RPT; r++) {
+            const int d = RPT * rb + r;
+            const float4 o = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+            *reinterpret_cast<float4 *>(Ss + d * MBV + cb) = o;
+            *reinterpret_cast<float4 *>(S_init + idx_of(j + 1) + d * D + col0 + cb) = o;
         }
     }
 }
@@ -468,14 +509,16 @@ int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S
     cudaStream_t st = (cudaStream_t)stream;
     const auto &p = c->plan;
     if (p.chains.empty()) return 0;
-    dim3 grid((unsigned)p.chains.size(), (unsigned)p.H, (unsigned)(p.dk / BV));
+    dim3 grid((unsigned)p.chains.size(), (unsigned)p.H, (unsigned)(p.dk / MBV));
+    cudaError_t e;
     if (p.dk == 64) {
-        const size_t sm = sizeof(float) * (64 * 65 + 64 * (BV + 1));
-        cudaFuncSetAttribute(merge_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        const size_t sm = sizeof(float) * (2 * 64 * 68 + 64 * MBV);
+        e = cudaFuncSetAttribute(merge_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        if (e != cudaSuccess) return (int)e;
         merge_kernel<64><<<grid, NT, sm, st>>>(c->dev.chains, S_ext, M, S_init, p.H, p.B);
     } else {
-        const size_t sm = sizeof(float) * (128 * 129 + 128 * (BV + 1));
-        cudaError_t e = cudaFuncSetAttribute(merge_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        const size_t sm = sizeof(float) * (2 * 128 * 132 + 128 * MBV);
+        e = cudaFuncSetAttribute(merge_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         if (e != cudaSuccess) return (int)e;
         merge_kernel<128><<<grid, NT, sm, st>>>(c->dev.chains, S_ext, M, S_init, p.H, p.B);
     }
@@ -485,6 +528,7 @@ int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S
 int launches_per_step(const cpdr_ctx *c) {
     const auto &p = c->plan;
     int n = 0;
+    n += (c->use_tc && !p.wy_chunks.empty()) ? 1 : 0;   // WY build (tensor-core path)
     n += p.pre_items.empty() ? 0 : (c->use_tc ? 2 : 1);   // pre-process (S and M kernels on the tensor-core path)
     n += p.zero_pre.empty() ? 0 : 2;           // zero S_ext and M
     n += p.zero_init.empty() ? 0 : 1;          // zero S_init

@@ -1,62 +1,44 @@
-// Tensor-core (tcgen05 / TMEM / TMA) kernels for the bf16, d = 128 path of
-// the segmented delta-rule forward, scalar gate (GDN).
+// Tensor-core (tcgen05 / TMEM / TMA) chain kernels for the bf16, d = 128
+// path of the segmented delta-rule forward, scalar gate (GDN).
 //
 // One CTA runs one chain: a (fragment, head) pair, 64-token chunks in order.
-// Per chunk, following the chunk form of the article "flash-linear-attention
-// 上下文并行CP ..." ([FLA-CP] §2.2) in transposed storage (state rows = value
-// dims, so every product has M = 128 on the tensor core):
-//   P      = [K; Q] K^T                 (K K^T and Q K^T in one M=128 MMA)
-//   A      = beta_i 2^(G_i - G_j) (K K^T)_ij, j < i          (SIMT)
-//   T      = (I + A)^-1, T' = T diag(beta), T'' = T diag(beta gamma)   (SIMT, fp32)
+// The per-chunk inverse T = (I + A)^-1 comes precomputed from the WY build
+// (tc_wy.cu) as bf16 tiles T' = T diag(beta) and T'' = T diag(beta gamma)
+// (hi, and lo for the split M chain).  Per chunk, following the chunk form of
+// the article "flash-linear-attention 上下文并行CP ..." ([FLA-CP] §2.2) in
+// transposed storage (state rows = value dims, so every product has M = 128
+// on the tensor core):
 //   W^T    = K^T T''^T,  U^T = V^T T'^T                      (MMA)
 //   Delta^T= U^T - S^T W^T                                   (MMA, accumulate)
-//   O^T    = S^T Q^T scaled by gamma_i + Delta^T mask^T,  mask_ij = (Q K^T)_ij 2^(G_i - G_j), j <= i
+//   O^T    = S^T Q^T scaled by gamma_i + Delta^T mask^T,
+//            mask_ij = (Q K^T)_ij 2^(G_i - G_j), j <= i      (forward)
 //   S^T   <- gamma^C S^T + (Delta diag(Gamma))^T K,  Gamma_j = 2^(G_C - G_j)
-// The pre-process runs the same chain without outputs on the S columns
-// (role S) and, in the same launch, the transfer-matrix chain
+// The pre-process runs the same chain without outputs (role S) and, in a
+// second launch, the transfer-matrix chain
 //   M <- M_[t] M,  M_[t] = Diag(gamma^C) - (Gamma ⊙ K)^T W   ([FLA-CP] §2.2)
 // (role M: U = 0, M_0 = I).  The M chain keeps fp32 accuracy, as the article
 // requires: its accumulator lives in fp32 registers and every tensor-core
-// operand derived from a rounded quantity (T'', W, M, Delta) is split into a
-// bf16 hi/lo pair, so each product is hi*hi + lo*hi + hi*lo.
+// operand derived from a rounded quantity (T'', W, M, Delta) is a bf16 hi/lo
+// pair, so each product is hi*hi + lo*hi + hi*lo.
 //
-// Warp roles (16 warps): 0 TMA producer; 1 MMA issuer (+ TMEM owner);
-// 2-3 causal mask (forward only); 4-7 gates, solve and the W epilogue;
-// 8-15 state warps (Delta, S and O epilogues; the fp32 state lives in their
-// registers, 64 values per thread).  Roles and shared-memory layouts are
-// compile-time and every role function is inlined, so per-CTA state stays in
-// registers.  Every mbarrier wait is bounded: on expiry the kernel records a
-// status code, raises an abort flag that makes every other wait fall
-// through, drains its MMAs and loads, frees TMEM and returns.  The solve
-// warpgroup synchronises with a hardware named barrier; its mbarrier waits
-// are taken by one warp and the verdict is broadcast across that barrier, so
-// an abort can never strand a warp inside it.
+// Warp roles (16 warps): 0 TMA producer and in-chunk gates; 1 MMA issuer
+// (+ TMEM owner); 2-3 causal mask (forward only); 4-7 W epilogue; 8-15 state
+// warps (Delta, S and O epilogues; the fp32 state lives in their registers,
+// 64 values per thread).  The critical path per chunk is
+//   Delta MMA -> Delta epilogue -> P_S MMA -> S update -> Delta MMA,
+// and the next chunk's W, U (and Q K^T) products are issued into the gaps.
+// Roles and shared-memory layouts are compile-time and every role function
+// is inlined, so per-CTA state stays in registers.  Every mbarrier wait is
+// bounded: on expiry the kernel records a status code, raises an abort flag
+// that makes every other wait fall through, drains its MMAs and loads, frees
+// TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "cpdr_internal.hpp"
 #include "tc_common.cuh"
-
-// Optional event trace (compile with -DCPDR_TRACE): CTA (0, 0) of each
-// launch records %globaltimer stamps per role, chunk and event.
-#ifdef CPDR_TRACE
-__device__ unsigned long long g_cpdr_trace[3][8][64][16];
-__device__ __forceinline__ unsigned long long gtimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-#define TR(role, chunk, ev)                                                                \
-    do {                                                                                   \
-        if (blockIdx.x == 0 && blockIdx.y == 0 && (threadIdx.x & 31) == 0 && (chunk) < 64) \
-            g_cpdr_trace[MODE * (1 + ROLE)][role][chunk][ev] = gtimer();                                \
-    } while (0)
-#else
-#define TR(role, chunk, ev) \
-    do {                    \
-    } while (0)
-#endif
+#include "tc_gates.cuh"
 
 namespace cpdr {
 namespace {
@@ -66,10 +48,24 @@ using namespace tc;
 constexpr int C = 64;
 constexpr int D = 128;
 constexpr int NTHREADS = 512;
-constexpr float kLog2e = 1.4426950408889634f;
 
 enum Mode { MODE_FWD = 0, MODE_PRE = 1 };
 enum Role { ROLE_S = 0, ROLE_M = 1 };
+
+// Optional event trace (compile with -DCPDR_TRACE): CTA (0, 0) of each
+// launch records SM clock stamps per role, chunk and event.
+#ifdef CPDR_TRACE
+__device__ unsigned long long g_cpdr_trace[3][8][64][16];
+#define TR(role, chunk, ev)                                                                \
+    do {                                                                                   \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && (threadIdx.x & 31) == 0 && (chunk) < 64) \
+            g_cpdr_trace[MODE * (1 + ROLE)][role][chunk][ev] = (unsigned long long)clock64(); \
+    } while (0)
+#else
+#define TR(role, chunk, ev) \
+    do {                    \
+    } while (0)
+#endif
 
 // TMEM columns (fp32, 128 lanes each)
 constexpr uint32_t TM_P = 0, TM_W = 64, TM_DL = 128, TM_O1 = 192, TM_O2 = 256, TM_PS = 320;
@@ -77,16 +73,17 @@ constexpr uint32_t TM_COLS = 512;
 
 // mbarrier indices
 enum Bar {
-    B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_PFULL, B_PFREE, B_TREADY, B_TFREE, B_MREADY, B_MFREE,
-    B_WFULL, B_WREADY, B_DLFULL, B_DLREADY, B_PSFULL, B_SREADY, B_OFULL, B_OFREE,
-    B_GATE0, B_GATE1, B_GATE2, B_GATE3, B_DRAIN, NBARS
+    B_FULL0, B_FULL1, B_FULL2, B_EMPTY0, B_EMPTY1, B_EMPTY2, B_PFULL, B_PFREE, B_WFULL, B_WREADY, B_WBFREE,
+    B_DLFULL, B_DLREADY, B_PSFULL, B_SREADY, B_OFULL, B_OFREE, B_MREADY, B_MFREE,
+    B_GATE0, B_GATE1, B_GATE2, B_GATE3, B_GATE4, B_DRAIN, NBARS
 };
-constexpr int kSolveBar = 1;   // named barrier id of the solve warpgroup
+constexpr int kMaxGateSlots = 5;
 
 struct Params {
     const cpdr_fragment *frags;
     const int32_t *items;
-    const __nv_bfloat16 *beta;
+    const int32_t *chunk0;    // first global chunk of each fragment (WY tile order)
+    const uint8_t *wy;        // WY tiles: [chunk][head][T', hi(T''), lo(T'')]
     const float *g;
     const float *S_init;
     __nv_bfloat16 *o;
@@ -99,29 +96,42 @@ struct Params {
 };
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base).
+//   stage ring: K (and Q, V) tiles as two 64-column swizzled atoms each, and
+//   the chunk's two WY tiles t1, t2 (T', hi(T'') for roles S and forward;
+//   hi(T''), lo(T'') for role M)
 struct Lay {
-    uint32_t stage_bytes, kc0, kc1, qc0, qc1, vc0, vc1, k_lbo, v_lbo, tx_bytes;
-    uint32_t tp, tpp, tpp_lo, mask, wb, wb_lo, sb, sb_lo, db, dgb, dgb_lo, scr, tmp, gates, graw, bars, ctl, verdict,
-        tslot, total;
+    uint32_t nstage, stage_bytes, kc0, kc1, qc0, qc1, vc0, vc1, t1, t2, k_lbo, v_lbo, tx_bytes, wy_off;
+    uint32_t ngate, gate_floats;
+    uint32_t mask, wb, wb_lo, sb, sb_lo, db, dgb, dgb_lo, gates, bars, ctl, tslot, total;
 };
 
 __host__ __device__ constexpr Lay make_lay(int mode, int role) {
     Lay L{};
     if (mode == MODE_FWD) {
-        L.stage_bytes = 49152; L.kc0 = 0; L.qc0 = 8192; L.kc1 = 16384; L.qc1 = 24576; L.vc0 = 32768; L.vc1 = 40960;
-        L.k_lbo = 16384; L.v_lbo = 8192; L.tx_bytes = 49152;
+        L.stage_bytes = 65536; L.kc0 = 0; L.qc0 = 8192; L.kc1 = 16384; L.qc1 = 24576; L.vc0 = 32768; L.vc1 = 40960;
+        L.t1 = 49152; L.t2 = 57344;
+        L.k_lbo = 16384; L.v_lbo = 8192; L.wy_off = 0;
     } else if (role == ROLE_S) {
-        L.stage_bytes = 32768; L.kc0 = 0; L.vc0 = 8192; L.kc1 = 16384; L.vc1 = 24576; L.qc0 = 0; L.qc1 = 0;
-        L.k_lbo = 16384; L.v_lbo = 16384; L.tx_bytes = 32768;
+        L.stage_bytes = 49152; L.kc0 = 0; L.vc0 = 8192; L.kc1 = 16384; L.vc1 = 24576; L.qc0 = 0; L.qc1 = 0;
+        L.t1 = 32768; L.t2 = 40960;
+        L.k_lbo = 16384; L.v_lbo = 16384; L.wy_off = 0;
     } else {
-        L.stage_bytes = 16384; L.kc0 = 0; L.kc1 = 8192; L.qc0 = 0; L.qc1 = 0; L.vc0 = 0; L.vc1 = 0;
-        L.k_lbo = 8192; L.v_lbo = 0; L.tx_bytes = 16384;
+        L.stage_bytes = 32768; L.kc0 = 0; L.kc1 = 8192; L.qc0 = 0; L.qc1 = 0; L.vc0 = 0; L.vc1 = 0;
+        L.t1 = 16384; L.t2 = 24576;
+        L.k_lbo = 8192; L.v_lbo = 0; L.wy_off = (uint32_t)kWyTileBytes;
     }
-    uint32_t o = 2 * L.stage_bytes;
+    L.tx_bytes = L.stage_bytes;
+    // three stages for the pre-process (loads start two chunks ahead), two
+    // for the forward (shared memory bound)
+    L.nstage = (mode == MODE_FWD) ? 2 : 3;
+    // gate slots: a slot is rewritten once the chunk NG before it is
+    // finished, which the stage ring guarantees for NG = stages + 2
+    L.ngate = L.nstage + 2;
+    // forward: G, gamma, Gamma, e, f (64 each), gamma^C, exact flag;
+    // pre-process: Gamma, gamma^C
+    L.gate_floats = (mode == MODE_FWD) ? 5 * 64 + 4 : 64 + 4;
     const bool split = (mode == MODE_PRE && role == ROLE_M);
-    L.tp = o; o += (split ? 0 : 8192);
-    L.tpp = o; o += 8192;
-    L.tpp_lo = o; o += (split ? 8192 : 0);
+    uint32_t o = L.nstage * L.stage_bytes;
     L.mask = o; o += (mode == MODE_FWD ? 8192 : 0);
     L.wb = o; o += 16384;
     L.wb_lo = o; o += (split ? 16384 : 0);
@@ -130,14 +140,10 @@ __host__ __device__ constexpr Lay make_lay(int mode, int role) {
     L.db = o; o += (mode == MODE_FWD ? 16384 : 0);
     L.dgb = o; o += 16384;
     L.dgb_lo = o; o += (split ? 16384 : 0);
-    L.scr = o; o += 64 * 68 * 4;              // solve scratch, fp32 [64][68] (16-byte rows)
-    L.tmp = o; o += 48 * 16 * 4;              // solve temporary
-    L.gates = o; o += 4 * (4 * 64 + 4) * 4;   // 4 slots: G, beta, gamma, Gamma, gamma^C
-    L.graw = o; o += 2 * 128 * 4;             // per stage: raw beta[64], log2 gate[64]
+    L.gates = o; o += L.ngate * L.gate_floats * 4;
     o = (o + 15) & ~15u;
     L.bars = o; o += NBARS * 8;
     L.ctl = o; o += 16;
-    L.verdict = o; o += 16;
     L.tslot = o; o += 16;
     L.total = o;
     return L;
@@ -149,7 +155,7 @@ struct Run {
     uint64_t *bar;
     Ctl *ctl;
     uint32_t tmem;
-    int n, nlast, h;
+    int n, nlast, h, chunk0;
     int64_t tok0;
     int seg, seq, flags;
     const Params *p;
@@ -157,14 +163,19 @@ struct Run {
 
 // gate slot arrays
 struct Gates {
-    float *G, *beta, *gam, *Gam, *gC;
+    float *G, *gam, *Gam, *e, *f, *gC;   // gC[0] = gamma^C, gC[1] = 1 when the exponentials must be exact
 };
 template <int MODE, int ROLE>
 __device__ __forceinline__ Gates gates_of(const Run &r, int slot) {
     constexpr Lay L = make_lay(MODE, ROLE);
-    float *q = reinterpret_cast<float *>(r.base + L.gates) + slot * (4 * 64 + 4);
-    return Gates{q, q + 64, q + 128, q + 192, q + 256};
+    float *q = reinterpret_cast<float *>(r.base + L.gates) + slot * L.gate_floats;
+    if (MODE == MODE_FWD) return Gates{q, q + 64, q + 128, q + 192, q + 256, q + 320};
+    return Gates{nullptr, nullptr, q, nullptr, nullptr, q + 64};
 }
+template <int MODE, int ROLE>
+__device__ __forceinline__ int gate_slot(int c) { return c % (int)make_lay(MODE, ROLE).ngate; }
+template <int MODE, int ROLE>
+__device__ __forceinline__ uint32_t gate_parity(int c) { return (uint32_t)(c / (int)make_lay(MODE, ROLE).ngate) & 1u; }
 
 __device__ __forceinline__ int rows_of(const Run &r, int chunk) { return chunk == r.n - 1 ? r.nlast : C; }
 
@@ -174,22 +185,6 @@ __device__ __forceinline__ bool warp_wait(const Run &r, int b, uint32_t parity, 
     int ok = 0;
     if ((threadIdx.x & 31) == 0) ok = mbar_wait(&r.bar[b], parity, r.ctl, r.p->status, site) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_try_wait(&r.bar[b], parity);
-    return ok != 0;
-}
-
-// Solve-warpgroup wait: warp 4 waits (bounded), writes the verdict, and the
-// named barrier publishes it to warps 5..7.  Two alternating verdict slots.
-__device__ __forceinline__ bool group_wait(const Run &r, volatile int *verdict, int &vslot, int b, uint32_t parity,
-                                           int site) {
-    volatile int *v = verdict + (vslot & 1);
-    vslot++;
-    if ((threadIdx.x >> 5) == 4) {
-        const bool ok = warp_wait(r, b, parity, site);
-        if ((threadIdx.x & 31) == 0) *v = ok ? 1 : 0;
-    }
-    named_bar(kSolveBar, 128);
-    const int ok = *v;
     if (ok) mbar_try_wait(&r.bar[b], parity);
     return ok != 0;
 }
@@ -225,6 +220,15 @@ __device__ __forceinline__ void store_row(uint8_t *tile, uint8_t *lo, uint32_t r
     }
 }
 
+// Bulk (non-tensor) copy global -> shared, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------------------ producer
 template <int MODE, int ROLE>
 __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq, const CUtensorMap *tk,
@@ -232,11 +236,38 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
     constexpr Lay L = make_lay(MODE, ROLE);
     const int lane = threadIdx.x & 31;
     const int H = r.p->H;
-    int issued[2] = {-1, -1};
+    int issued[3] = {-1, -1, -1};
+    // in-chunk gates of chunk c (padded rows: 0) -> its gate slot
+    auto produce_gates = [&](int c) {
+        const int nv = rows_of(r, c);
+        const int64_t tk0 = r.tok0 + (int64_t)c * C;
+        const int i0 = 2 * lane, i1 = 2 * lane + 1;
+        float g0 = 0.f, g1 = 0.f;
+        if (i0 < nv) g0 = r.p->g[(tk0 + i0) * H + r.h] * kLog2e;
+        if (i1 < nv) g1 = r.p->g[(tk0 + i1) * H + r.h] * kLog2e;
+        const LaneGates lg = scan_gates(g0, g1);
+        const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(c));
+        gs.Gam[i0] = exp2f(lg.GC - lg.G0);
+        gs.Gam[i1] = exp2f(lg.GC - lg.G1);
+        if (MODE == MODE_FWD) {
+            gs.G[i0] = lg.G0; gs.G[i1] = lg.G1;
+            gs.gam[i0] = exp2f(lg.G0); gs.gam[i1] = exp2f(lg.G1);
+            gs.e[i0] = exp2f(lg.G0 - lg.Gr); gs.e[i1] = exp2f(lg.G1 - lg.Gr);
+            gs.f[i0] = exp2f(lg.Gr - lg.G0); gs.f[i1] = exp2f(lg.Gr - lg.G1);
+        }
+        if (lane == 0) {
+            gs.gC[0] = exp2f(lg.GC);
+            gs.gC[1] = lg.exact ? 1.f : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&r.bar[B_GATE0 + gate_slot<MODE, ROLE>(c)]);
+    };
+    produce_gates(0);
+    constexpr int NS = (int)L.nstage;
     for (int t = 0; t < r.n; t++) {
-        const int s = t & 1;
+        const int s = t % NS;
         int ok = 1;
-        if (lane == 0 && t >= 2) ok = mbar_wait(&r.bar[B_EMPTY0 + s], ((t >> 1) - 1) & 1, r.ctl, r.p->status, 10);
+        if (lane == 0 && t >= NS) ok = mbar_wait(&r.bar[B_EMPTY0 + s], ((t / NS) - 1) & 1, r.ctl, r.p->status, 10);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         TR(0, t, 0);
         uint64_t *fb = &r.bar[B_FULL0 + s];
@@ -254,33 +285,19 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
                 tma_load_3d(st + L.vc0, tv, fb, 0, r.h, tok);
                 tma_load_3d(st + L.vc1, tv, fb, 64, r.h, tok);
             }
+            const uint8_t *src = r.p->wy + ((size_t)(r.chunk0 + t) * H + r.h) * kWyUnitBytes + L.wy_off;
+            bulk_load(st + L.t1, src, 2 * (uint32_t)kWyTileBytes, fb);
         }
-        // beta and the log2 gate of the chunk's rows (padded rows: 0), second arrival on FULL
-        {
-            const int nv = rows_of(r, t);
-            float *raw = reinterpret_cast<float *>(r.base + L.graw) + s * 128;
-#pragma unroll
-            for (int e = 0; e < 2; e++) {
-                const int i = lane + 32 * e;
-                float b = 0.f, gg = 0.f;
-                if (i < nv) {
-                    b = __bfloat162float(r.p->beta[((int64_t)tok + i) * H + r.h]);
-                    gg = r.p->g[((int64_t)tok + i) * H + r.h] * kLog2e;
-                }
-                raw[i] = b;
-                raw[64 + i] = gg;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(fb);
-        }
+        // gates one chunk ahead of the stage ring
+        if (t + 1 < r.n) produce_gates(t + 1);
         issued[s] = t;
     }
     // drain: every issued load must have landed before the CTA exits
     if (lane == 0) {
         Ctl local;
         local.abort = 0;
-        for (int s = 0; s < 2; s++)
-            if (issued[s] >= 0) mbar_wait(&r.bar[B_FULL0 + s], (issued[s] >> 1) & 1, &local, r.p->status, 11);
+        for (int s = 0; s < NS; s++)
+            if (issued[s] >= 0) mbar_wait(&r.bar[B_FULL0 + s], (issued[s] / NS) & 1, &local, r.p->status, 11);
     }
 }
 
@@ -326,48 +343,46 @@ __device__ __forceinline__ void run_mma(const Run &r) {
     constexpr Lay L = make_lay(MODE, ROLE);
     constexpr bool FWD = MODE == MODE_FWD, SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
     constexpr bool HAS_U = FWD || ROLE == ROLE_S;
+    constexpr int NS = (int)L.nstage;
     if ((threadIdx.x & 31) != 0) return;
     const uint32_t tm = r.tmem;
     int32_t *st = r.p->status;
     Ctl *ctl = r.ctl;
     const uint32_t b0 = smem_u32(r.base);
-    // per-stage operand descriptors (stage 1 = stage 0 + stage_bytes >> 4)
+    // stage-0 operand descriptors; stage s adds s * stage_bytes >> 4
     const uint64_t d_stack0 = kdesc(b0 + L.kc0), d_kmn0 = mndesc(b0 + L.kc0, L.k_lbo);
     const uint64_t d_vmn0 = mndesc(b0 + L.vc0, L.v_lbo), d_q0 = kdesc(b0 + L.qc0);
-    auto stg = [&](uint64_t d, int t) { return d + (uint64_t)((t & 1) * (L.stage_bytes >> 4)); };
-    const uint64_t d_tp = kdesc(b0 + L.tp), d_tpp = kdesc(b0 + L.tpp), d_tpplo = kdesc(b0 + L.tpp_lo);
+    const uint64_t d_t10 = kdesc(b0 + L.t1), d_t20 = kdesc(b0 + L.t2);
+    auto stg = [&](uint64_t d, int t) { return d + (uint64_t)((t % NS) * (L.stage_bytes >> 4)); };
     const uint64_t d_sb = kdesc(b0 + L.sb), d_sblo = kdesc(b0 + L.sb_lo);
     const uint64_t d_wb = mndesc(b0 + L.wb, 16384), d_wblo = mndesc(b0 + L.wb_lo, 16384);
     const uint64_t d_dgb = kdesc(b0 + L.dgb), d_dgblo = kdesc(b0 + L.dgb_lo), d_db = kdesc(b0 + L.db);
     const uint64_t d_mask = kdesc(b0 + L.mask);
     constexpr uint32_t KATOM = L.kc1 - L.kc0, QATOM = L.qc1 - L.qc0;
 
-    auto mma1 = [&](int t) {   // P = [K; Q] K^T  (rows 64..127 of the A tile: Q, V or unused)
-        mma_kk<64, 128, false>(tm + TM_P, stg(d_stack0, t), KATOM, stg(d_stack0, t), KATOM, false);
-        mma_commit(&r.bar[B_PFULL]);
-    };
-    auto emma = [&](int t) {   // W^T = K^T T''^T (hi + lo when split), U^T = V^T T'^T
-        mma_mnk<64, 64>(tm + TM_W, stg(d_kmn0, t), d_tpp, 8192, false);
-        if (SPLIT) mma_mnk<64, 64>(tm + TM_W, stg(d_kmn0, t), d_tpplo, 8192, true);
+    // chunk t's loads have landed: Q K^T (forward) and W^T = K^T T''^T (hi + lo when split)
+    auto front = [&](int t) {
+        if (FWD) {   // P = [K; Q] K^T, rows 64..127 = Q K^T
+            mma_kk<64, 128, false>(tm + TM_P, stg(d_stack0, t), KATOM, stg(d_stack0, t), KATOM, false);
+            mma_commit(&r.bar[B_PFULL]);
+        }
+        const uint64_t tpp = SPLIT ? stg(d_t10, t) : stg(d_t20, t);
+        mma_mnk<64, 64>(tm + TM_W, stg(d_kmn0, t), tpp, 8192, false);
+        if (SPLIT) mma_mnk<64, 64>(tm + TM_W, stg(d_kmn0, t), stg(d_t20, t), 8192, true);
         mma_commit(&r.bar[B_WFULL]);
-        if (HAS_U) mma_mnk<64, 64>(tm + TM_DL, stg(d_vmn0, t), d_tp, 8192, false);
-        mma_commit(&r.bar[B_TFREE]);
+    };
+    // U^T = V^T T'^T into the Delta accumulator
+    auto umma = [&](int t) {
+        if (HAS_U) mma_mnk<64, 64>(tm + TM_DL, stg(d_vmn0, t), stg(d_t10, t), 8192, false);
     };
     do {
         if (!mbar_wait(&r.bar[B_FULL0], 0, ctl, st, 20)) break;
         tc_fence_after();
-        mma1(0);
-        if (!mbar_wait(&r.bar[B_TREADY], 0, ctl, st, 21)) break;
-        tc_fence_after();
-        emma(0);
+        front(0);
+        umma(0);
+        bool ahead = false;   // chunk t+1's front() already issued
         for (int t = 0; t < r.n; t++) {
-            const int s = t & 1;
-            if (t + 1 < r.n) {
-                if (!mbar_wait(&r.bar[B_FULL0 + ((t + 1) & 1)], ((t + 1) >> 1) & 1, ctl, st, 22)) break;
-                if (!mbar_wait(&r.bar[B_PFREE], t & 1, ctl, st, 23)) break;
-                tc_fence_after();
-                mma1(t + 1);
-            }
+            const int s = t % NS;
             TR(1, t, 0);
             if (!mbar_wait(&r.bar[B_SREADY], t & 1, ctl, st, 24)) break;
             TR(1, t, 1);
@@ -382,6 +397,7 @@ __device__ __forceinline__ void run_mma(const Run &r) {
                 mma_kmn<64, 128, true>(tm + TM_DL, d_sblo, 16384, d_wb, true);
                 mma_kmn<64, 128, true>(tm + TM_DL, d_sb, 16384, d_wblo, true);
             }
+            mma_commit(&r.bar[B_WBFREE]);
             if (FWD) {
                 if (t >= 1 && !mbar_wait(&r.bar[B_OFREE], (t - 1) & 1, ctl, st, 26)) break;
                 tc_fence_after();
@@ -389,6 +405,15 @@ __device__ __forceinline__ void run_mma(const Run &r) {
             }
             mma_commit(&r.bar[B_DLFULL]);
             TR(1, t, 3);
+            // the next chunk's front products, if its loads are in (and, in
+            // the forward, the mask warps have read this chunk's P)
+            ahead = false;
+            if (t + 1 < r.n && mbar_test_wait(&r.bar[B_FULL0 + (t + 1) % NS], ((t + 1) / NS) & 1) &&
+                (!FWD || mbar_test_wait(&r.bar[B_PFREE], t & 1))) {
+                tc_fence_after();
+                front(t + 1);
+                ahead = true;
+            }
             if (!mbar_wait(&r.bar[B_DLREADY], t & 1, ctl, st, 27)) break;
             TR(1, t, 4);
             tc_fence_after();
@@ -396,6 +421,16 @@ __device__ __forceinline__ void run_mma(const Run &r) {
             mma_kmn<128, 64, false>(tm + TM_PS, d_dgb, 16384, stg(d_kmn0, t), false);
             if (SPLIT) mma_kmn<128, 64, false>(tm + TM_PS, d_dgblo, 16384, stg(d_kmn0, t), true);
             mma_commit(&r.bar[B_PSFULL]);
+            TR(1, t, 5);
+            if (t + 1 < r.n) {
+                if (!ahead) {
+                    if (!mbar_wait(&r.bar[B_FULL0 + (t + 1) % NS], ((t + 1) / NS) & 1, ctl, st, 22)) break;
+                    if (FWD && !mbar_wait(&r.bar[B_PFREE], t & 1, ctl, st, 23)) break;
+                    tc_fence_after();
+                    front(t + 1);
+                }
+                umma(t + 1);
+            }
             if (FWD) {
                 if (!mbar_wait(&r.bar[B_MREADY], t & 1, ctl, st, 28)) break;
                 tc_fence_after();
@@ -404,13 +439,7 @@ __device__ __forceinline__ void run_mma(const Run &r) {
                 mma_commit(&r.bar[B_MFREE]);
             }
             mma_commit(&r.bar[B_EMPTY0 + s]);
-            TR(1, t, 5);
-            if (t + 1 < r.n) {
-                if (!mbar_wait(&r.bar[B_TREADY], (t + 1) & 1, ctl, st, 29)) break;
-                TR(1, t, 6);
-                tc_fence_after();
-                emma(t + 1);
-            }
+            TR(1, t, 6);
         }
     } while (0);
     // drain every MMA this thread issued
@@ -420,215 +449,6 @@ __device__ __forceinline__ void run_mma(const Run &r) {
     mbar_wait(&r.bar[B_DRAIN], 0, &local, st, 30);
 }
 
-// ------------------------------------------------------------------ gates
-// Warp 4: in-chunk cumulative log2 gate G of chunk t and its exponentials,
-// from the raw beta / log2 gate the producer warp staged with the chunk,
-// into gate slot t % 4.  Padded rows carry beta = g = 0.
-__device__ __forceinline__ void write_gates(const Gates &gs, const float *raw) {
-    const int lane = threadIdx.x & 31;
-    const int i0 = 2 * lane, i1 = 2 * lane + 1;
-    const float2 bb = *reinterpret_cast<const float2 *>(raw + i0);
-    const float2 gg = *reinterpret_cast<const float2 *>(raw + 64 + i0);
-    float x = gg.x + gg.y;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    const float G1 = x, G0 = x - gg.y;
-    const float GC = __shfl_sync(0xffffffffu, x, 31);
-    gs.G[i0] = G0; gs.G[i1] = G1;
-    gs.beta[i0] = bb.x; gs.beta[i1] = bb.y;
-    gs.gam[i0] = exp2f(G0); gs.gam[i1] = exp2f(G1);
-    gs.Gam[i0] = exp2f(GC - G0); gs.Gam[i1] = exp2f(GC - G1);
-    if (lane == 0) gs.gC[0] = exp2f(GC);
-}
-
-// ------------------------------------------------------------------ solve warpgroup
-// In-place inverse of the unit lower-triangular (I + A) held in scr[64][68]
-// (strictly lower part = A, the rest 0), by 16x16 blocks: diagonal blocks by
-// forward substitution, then block columns right to left,
-//   X[ib][jb] = -( sum_{kb = jb+1..ib} X[ib][kb] A[kb][jb] ) X[jb][jb].
-// Afterwards scr holds T = (I + A)^-1 with its unit diagonal written out.
-
-// One block column JB (rows below the diagonal block):
-//   temp[r][cc] = sum_k X[r0 + r][k] A[k][16 JB + cc]     (X lower, upper part 0)
-//   X[r0 + r][16 JB + cc] = -sum_m temp[r][m] X[16 JB + m][16 JB + cc]
-// Each thread owns column cc and rows t/16 + 8 m, all m interleaved for ILP.
-template <int JB>
-__device__ __forceinline__ void solve_block_column(float *S, float *Tm, int t) {
-    constexpr int LS = 68, r0 = 16 * (JB + 1), R = 64 - r0, NM = R / 8;
-    const int cc = t & 15, rb = t >> 4;
-    float acc[NM];
-#pragma unroll
-    for (int m = 0; m < NM; m++) acc[m] = 0.f;
-#pragma unroll 2
-    for (int k = r0; k < 64; k += 4) {
-        const float a0 = S[k * LS + 16 * JB + cc], a1 = S[(k + 1) * LS + 16 * JB + cc];
-        const float a2 = S[(k + 2) * LS + 16 * JB + cc], a3 = S[(k + 3) * LS + 16 * JB + cc];
-#pragma unroll
-        for (int m = 0; m < NM; m++) {
-            const float4 x = *reinterpret_cast<const float4 *>(S + (r0 + rb + 8 * m) * LS + k);
-            acc[m] = fmaf(x.x, a0, acc[m]);
-            acc[m] = fmaf(x.y, a1, acc[m]);
-            acc[m] = fmaf(x.z, a2, acc[m]);
-            acc[m] = fmaf(x.w, a3, acc[m]);
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < NM; m++) Tm[(rb + 8 * m) * 16 + cc] = acc[m];
-    named_bar(kSolveBar, 128);
-#pragma unroll
-    for (int m = 0; m < NM; m++) acc[m] = 0.f;
-#pragma unroll 4
-    for (int mm = 0; mm < 16; mm++) {
-        const float x = S[(16 * JB + mm) * LS + 16 * JB + cc];
-#pragma unroll
-        for (int m = 0; m < NM; m++) acc[m] = fmaf(Tm[(rb + 8 * m) * 16 + mm], x, acc[m]);
-    }
-#pragma unroll
-    for (int m = 0; m < NM; m++) S[(r0 + rb + 8 * m) * LS + 16 * JB + cc] = -acc[m];
-    named_bar(kSolveBar, 128);
-}
-
-__device__ __forceinline__ void solve_inverse(float *S, float *Tm, int t) {
-    constexpr int LS = 68;
-    float x[16];
-    const int b = t >> 4, col = t & 15;
-    if (t < 64) {   // diagonal block b, column col
-        const float *Ab = S + (16 * b) * LS + 16 * b;
-#pragma unroll
-        for (int i = 0; i < 16; i++) {
-            float s = 0.f;
-#pragma unroll
-            for (int k = 0; k < i; k++) s = fmaf(Ab[i * LS + k], x[k], s);
-            x[i] = (i < col) ? 0.f : (i == col ? 1.f : -s);
-        }
-    }
-    named_bar(kSolveBar, 128);
-    if (t < 64) {
-        float *Ab = S + (16 * b) * LS + 16 * b;
-#pragma unroll
-        for (int i = 0; i < 16; i++) Ab[i * LS + col] = x[i];
-    }
-    named_bar(kSolveBar, 128);
-    solve_block_column<2>(S, Tm, t);
-    solve_block_column<1>(S, Tm, t);
-    solve_block_column<0>(S, Tm, t);
-}
-
-template <int MODE, int ROLE>
-__device__ __forceinline__ void run_solve(const Run &r) {
-    constexpr Lay L = make_lay(MODE, ROLE);
-    constexpr bool SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x - 128;
-    float *S = reinterpret_cast<float *>(r.base + L.scr);
-    float *Tm = reinterpret_cast<float *>(r.base + L.tmp);
-    volatile int *verdict = reinterpret_cast<volatile int *>(r.base + L.verdict);
-    int vslot = 0;
-    for (int ch = 0; ch < r.n; ch++) {
-        const int slot = ch & 3;
-        const Gates gs = gates_of<MODE, ROLE>(r, slot);
-        if (w == 4) {
-            TR(2, ch, 0);
-            if (!warp_wait(r, B_FULL0 + (ch & 1), (ch >> 1) & 1, 44)) return;
-            write_gates(gs, reinterpret_cast<const float *>(r.base + L.graw) + (ch & 1) * 128);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&r.bar[B_GATE0 + slot]);
-            TR(2, ch, 1);
-        }
-        if (!group_wait(r, verdict, vslot, B_PFULL, ch & 1, 45)) return;
-        TR(2, ch, 2);
-        tc_fence_after();
-        // A from K K^T (TMEM lanes 0..63 -> warps 4, 5)
-        if (w < 6) {
-            const int i = 32 * (w - 4) + lane;
-            const float bi = gs.beta[i], Gi = gs.G[i];
-#pragma unroll 1
-            for (int half = 0; half < 2; half++) {
-                float v[32];
-                tmem_ld32(r.tmem + ((uint32_t)(32 * (w - 4)) << 16) + TM_P + 32 * half, v);
-                float Gj[32];
-#pragma unroll
-                for (int q4 = 0; q4 < 8; q4++) {
-                    const float4 g4 = *reinterpret_cast<const float4 *>(gs.G + 32 * half + 4 * q4);
-                    Gj[4 * q4] = g4.x; Gj[4 * q4 + 1] = g4.y; Gj[4 * q4 + 2] = g4.z; Gj[4 * q4 + 3] = g4.w;
-                }
-                tmem_ld_wait();
-#pragma unroll
-                for (int q4 = 0; q4 < 8; q4++) {
-                    float e[4];
-#pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        const int jj = 4 * q4 + u, j = 32 * half + jj;
-                        e[u] = (j < i) ? bi * exp2f(Gi - Gj[jj]) * v[jj] : 0.f;
-                    }
-                    *reinterpret_cast<float4 *>(S + i * 68 + 32 * half + 4 * q4) = make_float4(e[0], e[1], e[2], e[3]);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&r.bar[B_PFREE]);
-        }
-        named_bar(kSolveBar, 128);
-        TR(2, ch, 3);
-        solve_inverse(S, Tm, t);
-        TR(2, ch, 4);
-        // T' = T diag(beta), T'' = T diag(beta gamma) (hi/lo when split), bf16 swizzled
-        if (ch >= 1 && !group_wait(r, verdict, vslot, B_TFREE, (ch - 1) & 1, 47)) return;
-        {
-            const int i = t >> 1, hf = t & 1;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; q4++) {
-                float a[8], bb[8];
-#pragma unroll
-                for (int e4 = 0; e4 < 2; e4++) {
-                    const int j0 = 32 * hf + 8 * q4 + 4 * e4;
-                    const float4 t4 = *reinterpret_cast<const float4 *>(S + i * 68 + j0);
-                    const float4 b4 = *reinterpret_cast<const float4 *>(gs.beta + j0);
-                    const float4 g4 = *reinterpret_cast<const float4 *>(gs.gam + j0);
-                    const float tv[4] = {t4.x, t4.y, t4.z, t4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
-                    const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        const float tij = (j0 + u <= i) ? tv[u] : 0.f;
-                        a[4 * e4 + u] = tij * bv[u];
-                        bb[4 * e4 + u] = a[4 * e4 + u] * gv[u];
-                    }
-                }
-                const uint32_t off = sw128(i, 4 * hf + q4);
-                const uint4 hi = pack8(bb);
-                *reinterpret_cast<uint4 *>(r.base + L.tpp + off) = hi;
-                if (SPLIT) *reinterpret_cast<uint4 *>(r.base + L.tpp_lo + off) = pack8_residual(bb, hi);
-                else *reinterpret_cast<uint4 *>(r.base + L.tp + off) = pack8(a);
-            }
-        }
-        fence_async_smem();
-        named_bar(kSolveBar, 128);
-        if (t == 0) mbar_arrive(&r.bar[B_TREADY]);
-        TR(2, ch, 5);
-        // W epilogue: W^T (lanes = dk) -> bf16 MN-major B tile (hi/lo when split)
-        if (!group_wait(r, verdict, vslot, B_WFULL, ch & 1, 49)) return;
-        TR(2, ch, 6);
-        tc_fence_after();
-        {
-            const int dk = 32 * (w - 4) + lane;
-#pragma unroll 1
-            for (int half = 0; half < 2; half++) {
-                float v[32];
-                tmem_ld32(r.tmem + ((uint32_t)(32 * (w - 4)) << 16) + TM_W + 32 * half, v);
-                tmem_ld_wait();
-                store_row<4>(r.base + L.wb, SPLIT ? r.base + L.wb_lo : nullptr, dk, 4 * half, v);
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&r.bar[B_WREADY]);
-        TR(2, ch, 7);
-    }
-}
-
 // ------------------------------------------------------------------ mask warps (forward)
 template <int MODE, int ROLE>
 __device__ __forceinline__ void run_mask(const Run &r) {
@@ -636,13 +456,14 @@ __device__ __forceinline__ void run_mask(const Run &r) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i = 32 * (w - 2) + lane;   // row of Q K^T (TMEM lane 64 + i)
     for (int ch = 0; ch < r.n; ch++) {
-        if (!warp_wait(r, B_GATE0 + (ch & 3), (ch >> 2) & 1, 50)) return;
-        const Gates gs = gates_of<MODE, ROLE>(r, ch & 3);
+        if (!warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 50)) return;
+        const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(ch));
         if (w == 2) TR(4, ch, 0);
         if (!warp_wait(r, B_PFULL, ch & 1, 51)) return;
         if (w == 2) TR(4, ch, 1);
         tc_fence_after();
-        const float Gi = gs.G[i];
+        const float Gi = gs.G[i], ei = gs.e[i];
+        const bool exact = gs.gC[1] != 0.f;
         float m[64];
 #pragma unroll
         for (int half = 0; half < 2; half++) {
@@ -651,12 +472,14 @@ __device__ __forceinline__ void run_mask(const Run &r) {
             tmem_ld_wait();
 #pragma unroll
             for (int q4 = 0; q4 < 8; q4++) {
-                const float4 g4 = *reinterpret_cast<const float4 *>(gs.G + 32 * half + 4 * q4);
-                const float gj[4] = {g4.x, g4.y, g4.z, g4.w};
+                const int j0 = 32 * half + 4 * q4;
+                const float4 f4 = *reinterpret_cast<const float4 *>(gs.f + j0);
+                const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
                 for (int u = 0; u < 4; u++) {
-                    const int jj = 4 * q4 + u, j = 32 * half + jj;
-                    m[j] = (j <= i) ? v[jj] * exp2f(Gi - gj[u]) : 0.f;
+                    const float x = v[4 * q4 + u];
+                    const float val = exact ? x * exp2f(Gi - gs.G[j0 + u]) : x * ei * fv[u];
+                    m[j0 + u] = (j0 + u <= i) ? val : 0.f;
                 }
             }
         }
@@ -670,6 +493,35 @@ __device__ __forceinline__ void run_mask(const Run &r) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&r.bar[B_MREADY]);
         if (w == 2) TR(4, ch, 2);
+    }
+}
+
+// ------------------------------------------------------------------ W epilogue warps
+// W^T (TMEM lanes = dk) -> bf16 MN-major B tile of the Delta product (hi/lo when split)
+template <int MODE, int ROLE>
+__device__ __forceinline__ void run_wepi(const Run &r) {
+    constexpr Lay L = make_lay(MODE, ROLE);
+    constexpr bool SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = w & 3, row = 32 * q + lane;
+    const uint32_t lane_base = r.tmem + ((uint32_t)(32 * q) << 16);
+    for (int t = 0; t < r.n; t++) {
+        if (!warp_wait(r, B_WFULL, t & 1, 40)) return;
+        if (w == 4) TR(2, t, 0);
+        tc_fence_after();
+        float v0[32], v1[32];
+        tmem_ld32(lane_base + TM_W, v0);
+        tmem_ld32(lane_base + TM_W + 32, v1);
+        tmem_ld_wait();
+        tc_fence_before();
+        // the previous chunk's Delta product must have read the tile
+        if (t >= 1 && !warp_wait(r, B_WBFREE, (t - 1) & 1, 41)) return;
+        store_row<4>(r.base + L.wb, SPLIT ? r.base + L.wb_lo : nullptr, row, 0, v0);
+        store_row<4>(r.base + L.wb, SPLIT ? r.base + L.wb_lo : nullptr, row, 4, v1);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&r.bar[B_WREADY]);
+        if (w == 4) TR(2, t, 1);
     }
 }
 
@@ -702,8 +554,8 @@ __device__ __forceinline__ void run_state(const Run &r) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&r.bar[B_SREADY]);
     for (int ch = 0; ch < r.n; ch++) {
-        if (!warp_wait(r, B_GATE0 + (ch & 3), (ch >> 2) & 1, 60)) return;
-        const Gates gs = gates_of<MODE, ROLE>(r, ch & 3);
+        if (!warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 60)) return;
+        const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(ch));
         // Delta epilogue
         if (w == 8) TR(3, ch, 0);
         if (!warp_wait(r, B_DLFULL, ch & 1, 61)) return;
@@ -798,7 +650,8 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     r.bar = reinterpret_cast<uint64_t *>(base + L.bars);
     r.ctl = reinterpret_cast<Ctl *>(base + L.ctl);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + L.tslot);
-    const cpdr_fragment f = p.frags[p.items[item]];
+    const int fi = p.items[item];
+    const cpdr_fragment f = p.frags[fi];
     r.tok0 = f.tok0;
     r.seg = f.seg;
     r.seq = f.seq;
@@ -806,11 +659,19 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     r.h = blockIdx.y;
     r.n = (f.len + C - 1) / C;
     r.nlast = f.len - (r.n - 1) * C;
+    r.chunk0 = p.chunk0[fi];
     r.p = &p;
     if (threadIdx.x == 0) {
-        const uint32_t cnt[NBARS] = {2, 2, 1, 1, 1, (uint32_t)(MODE == MODE_FWD ? 4 : 2), 1, 1, 2, 1,
-                                     1, 4, 1, 8, 1, 8, 1, 8,
-                                     1, 1, 1, 1, 1};
+        // arrival counts: PFREE 2 mask warps, WREADY 4 W-epilogue warps,
+        // DLREADY / SREADY / OFREE 8 state warps, MREADY 2 mask warps
+        uint32_t cnt[NBARS];
+        for (int i = 0; i < NBARS; i++) cnt[i] = 1;
+        cnt[B_PFREE] = 2;
+        cnt[B_WREADY] = 4;
+        cnt[B_DLREADY] = 8;
+        cnt[B_SREADY] = 8;
+        cnt[B_OFREE] = 8;
+        cnt[B_MREADY] = 2;
         for (int i = 0; i < NBARS; i++) mbar_init(&r.bar[i], cnt[i]);
         r.ctl->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -831,7 +692,7 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     if (w == 0) run_producer<MODE, ROLE>(r, tq, tk, tv);
     else if (w == 1) run_mma<MODE, ROLE>(r);
     else if (w < 4) { if (MODE == MODE_FWD) run_mask<MODE, ROLE>(r); }
-    else if (w < 8) run_solve<MODE, ROLE>(r);
+    else if (w < 8) run_wepi<MODE, ROLE>(r);
     else run_state<MODE, ROLE>(r);
     tc_fence_before();
     __syncthreads();
@@ -881,6 +742,13 @@ bool make_tmap(CUtensorMap *m, const void *ptr, int64_t tokens, int H) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr size_t kMaxSmem = 232448;   // 227 KiB opt-in per CTA
+static_assert(make_lay(MODE_FWD, ROLE_S).total + 1024 <= kMaxSmem, "forward layout exceeds shared memory");
+static_assert(make_lay(MODE_PRE, ROLE_S).total + 1024 <= kMaxSmem, "pre-process S layout exceeds shared memory");
+static_assert(make_lay(MODE_PRE, ROLE_M).total + 1024 <= kMaxSmem, "pre-process M layout exceeds shared memory");
+static_assert(make_lay(MODE_FWD, ROLE_S).ngate <= kMaxGateSlots && make_lay(MODE_PRE, ROLE_M).ngate <= kMaxGateSlots,
+              "gate slots exceed their barriers");
+
 size_t smem_for(int mode, int role) { return make_lay(mode, role).total + 1024; }
 
 template <int MODE, int ROLE>
@@ -908,7 +776,7 @@ bool tc_supported(const Plan &p) {
     return p.in_dtype == CPDR_DTYPE_BF16 && p.dk == 128 && p.dv == 128 && p.gate_kind == CPDR_GATE_SCALAR;
 }
 
-int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const void *beta, const float *g, float *S_ext,
+int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy, float *S_ext,
                   float *M, void *stream) {
     const auto &p = c->plan;
     if (p.pre_items.empty()) return 0;
@@ -918,7 +786,8 @@ int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const void *b
     Params prm{};
     prm.frags = c->dev.frags;
     prm.items = c->dev.pre_items;
-    prm.beta = (const __nv_bfloat16 *)beta;
+    prm.chunk0 = c->dev.frag_chunk0;
+    prm.wy = (const uint8_t *)wy;
     prm.g = g;
     prm.S_ext = S_ext;
     prm.M = M;
@@ -933,7 +802,7 @@ int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const void *b
                                           (cudaStream_t)stream);
 }
 
-int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta, const float *g,
+int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const float *g, const void *wy,
                   const float *S_init, void *o, float *final_state, void *stream) {
     const auto &p = c->plan;
     if (p.frags.empty()) return 0;
@@ -944,7 +813,8 @@ int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v
     Params prm{};
     prm.frags = c->dev.frags;
     prm.items = c->dev.fwd_order;
-    prm.beta = (const __nv_bfloat16 *)beta;
+    prm.chunk0 = c->dev.frag_chunk0;
+    prm.wy = (const uint8_t *)wy;
     prm.g = g;
     prm.S_init = S_init;
     prm.o = (__nv_bfloat16 *)o;

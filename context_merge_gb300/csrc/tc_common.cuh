@@ -37,7 +37,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Same, but the thread may stay suspended (not issuing) for up to `ns`
+// Non-blocking test of phase `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Same as mbar_try_wait, but the thread may stay suspended (not issuing) for up to `ns`
 // nanoseconds while the phase is incomplete; it resumes when the phase completes.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
     uint32_t ok;
@@ -63,7 +75,7 @@ constexpr long long kWaitCycles = 4000000000LL;
 
 // Slow path of the bounded wait (kept out of line: it is rare and would
 // otherwise be inlined at every wait site).
-__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
     const long long t0 = clock64();
     for (;;) {
         // suspended (not spinning) while the phase is incomplete

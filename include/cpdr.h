@@ -138,16 +138,38 @@ cpdr_status cpdr_plan_fragments(const cpdr_ctx *ctx, cpdr_fragment *out, int32_t
 cpdr_status cpdr_plan_counts(const cpdr_ctx *ctx, int32_t out[8]);
 
 /*
+ * WY build ([FLA-CP] §2.2 and the recompute_w_u step of its §4 Code Flow):
+ * for every 64-token chunk of every fragment and every head,
+ *     A_ij = beta_i exp(G_i - G_j) k_i . k_j  (j < i),   T = (I + A)^-1,
+ * with G the in-chunk cumulative log gate, and the tiles W and U are built
+ * from:  T' = T diag(beta)  (U = T' V)  and  T'' = T diag(beta gamma)
+ * (W = T'' K, gamma_j = exp(G_j)).  Each (chunk, head) gets three 64 x 64
+ * bf16 tiles -- T', T'' rounded (hi) and T'' - hi rounded (lo) -- stored as
+ * 8 KiB 128-byte-swizzled images, in the chunk order of the plan's fragment
+ * table, heads innermost.  The chunk recurrences of cpdr_preprocess and
+ * cpdr_fwd read them (the triangular solve is independent across chunks, so
+ * it runs here once, fully parallel, instead of inside every chain).
+ * cpdr_wy_bytes() gives the workspace size: 24 KiB per (chunk, head) on the
+ * tensor-core path (bf16, dk = dv = 128, scalar gate), 0 otherwise (then
+ * this call does nothing and `wy` may be NULL).
+ * In: k, beta, gate (device).  Out: wy (device, caller-owned).
+ */
+cpdr_status cpdr_wy_bytes(const cpdr_ctx *ctx, size_t *bytes);
+cpdr_status cpdr_wy_build(const cpdr_ctx *ctx, const void *k, const void *beta, const float *gate,
+                          void *wy, void *stream);
+
+/*
  * Pre-process ([FLA-CP] §2.1-§2.3, pre_process_fwd in its Code Flow of §4):
  * for every segment whose trailing fragment continues into the next
  * segment, S_ext = state of that fragment from zero, M = chained transfer
  * matrix  M <- (Diag(gamma^C) - (Gamma ⊙ K)^T W) M  over its 64-token
  * chunks.  Entries of segments with no continuing fragment are zeroed.
- * In: k, v, beta, gate (device).  Out: S_ext, M (device, sizes from
- * cpdr_buffer_sizes).
+ * In: k, v, beta, gate (device); wy: the tiles cpdr_wy_build wrote for the
+ * same k, beta and gate (NULL when cpdr_wy_bytes() is 0).  Out: S_ext, M
+ * (device, sizes from cpdr_buffer_sizes).
  */
 cpdr_status cpdr_preprocess(const cpdr_ctx *ctx, const void *k, const void *v, const void *beta,
-                            const float *gate, float *S_ext, float *M, void *stream);
+                            const float *gate, const void *wy, float *S_ext, float *M, void *stream);
 
 /*
  * Merge ([FLA-CP] §2.1; ownership rule of §5.2): for every segment r whose
@@ -164,15 +186,15 @@ cpdr_status cpdr_merge(const cpdr_ctx *ctx, const float *S_ext, const float *M, 
  * every fragment runs the 64-token chunk recurrence from S_init[seg] (first
  * fragment continuing a sequence) or zero, writes o = scale * S_t^T q_t per
  * token and, when its sequence ends there, final_state[seq].
- * final_state may be NULL.
+ * wy: as for cpdr_preprocess.  final_state may be NULL.
  */
 cpdr_status cpdr_fwd(const cpdr_ctx *ctx, const void *q, const void *k, const void *v,
-                     const void *beta, const float *gate, const float *S_init, void *o,
+                     const void *beta, const float *gate, const void *wy, const float *S_init, void *o,
                      float *final_state, void *stream);
 
 /*
  * Whole path from HOST memory: copies q, k, v, beta, gate into the
- * caller-provided device workspace, runs preprocess, merge and fwd on
+ * caller-provided device workspace, runs the WY build, preprocess, merge and fwd on
  * `stream`, and copies o and final_state back (host pointers; use pinned
  * memory for asynchronous copies).  Returns after enqueuing; the caller
  * synchronises the stream before reading o.  The workspace must hold
@@ -187,17 +209,18 @@ cpdr_status cpdr_forward_host(const cpdr_ctx *ctx, const void *q, const void *k,
  * Allocation-free whole path (no counterpart in the article: it is an
  * interface for callers that cannot allocate device memory, e.g. code inside
  * a runtime that owns all device memory through its own pool or static
- * memory plan).  Runs preprocess, merge and fwd like the three calls above,
- * but keeps everything except the caller's inputs and outputs -- the
- * exchange buffers S_ext, M, S_init, the plan tables and the status word of
- * the bounded waits -- in one file-scope device array of 16 MiB per device
+ * memory plan).  Runs the WY build, preprocess, merge and fwd like the calls
+ * above, but keeps everything except the caller's inputs and outputs -- the
+ * WY tiles, the exchange buffers S_ext, M, S_init, the plan tables and the
+ * status word of the bounded waits -- in one file-scope device array of
+ * 32 MiB per device
  * (held by every GPU that loads the library until the process exits).  It
  * calls no cudaMalloc, cudaFree or other allocating routine, and accepts a
  * context created with CPDR_FLAG_HOST_ONLY.
  * In: q, k, v, beta, gate (device).  Out: o, final_state (device; final_state
  * may be NULL).  Errors: CPDR_ERR_WORKSPACE when the problem needs more than
- * the array holds (R*B*H*dk*(2*dv + dk)*4 bytes of exchange buffers plus the
- * plan tables), CPDR_ERR_INVALID / CPDR_ERR_CUDA as for the other calls.
+ * the array holds (R*B*H*dk*(2*dv + dk)*4 bytes of exchange buffers, the WY
+ * tiles of cpdr_wy_bytes() and the plan tables), CPDR_ERR_INVALID / CPDR_ERR_CUDA as for the other calls.
  * Set-up: the first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Every call shares the one array and overwrites

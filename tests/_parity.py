@@ -19,19 +19,20 @@ TOL = {"fp32": 1e-4, "bf16": 2e-2}
 
 
 def run_gpu(inp, force_simt=False, scale=1.0):
-    """preprocess -> merge -> fwd through the C-ABI on cuda:0; CPU results."""
+    """WY build -> preprocess -> merge -> fwd through the C-ABI on cuda:0; CPU results."""
     B, T, H, d, R = inp["B"], inp["T"], inp["H"], inp["d"], inp["R"]
     ctx = cpdr.Context(B, T, H, d, R, gate=inp["gate"], dtype=inp["dtype"], cu_seqlens=inp["cu_seqlens"],
                        scale=scale, force_simt=force_simt)
     dev = {k: inp[k].cuda() for k in ("q", "k", "v", "beta", "g")}
     bufs = ctx.alloc_buffers("cuda")
-    for t in bufs.values():
-        t.fill_(float("nan"))          # poison: every element must be written
+    for t in bufs.values():            # poison: every element must be written
+        if t is not None:              # (WY tiles: 0xffff is a bf16 NaN)
+            t.fill_(255 if t.dtype == torch.uint8 else float("nan"))
     o = torch.full_like(dev["v"], float("nan"))
     ctx.run(dev["q"], dev["k"], dev["v"], dev["beta"], dev["g"], bufs=bufs, o=o)
     torch.cuda.synchronize()
     ctx.check_device_status()
-    out = {k: v.cpu() for k, v in bufs.items()}
+    out = {k: v.cpu() for k, v in bufs.items() if k != "wy"}
     out["o"] = o.cpu()
     out["counts"] = ctx.counts()
     return out

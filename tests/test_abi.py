@@ -72,3 +72,20 @@ def test_buffer_sizes(cpdr_lib):
     assert fin == 2 * 3 * 128 * 128 * 4
     ws = ctx.host_workspace_bytes()
     assert ws >= 3 * 2 * 512 * 3 * 128 * 2 + se + m + si + fin
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=1, T=4096, H=4, d=128, R=4, dtype="bf16"),
+    dict(B=2, T=1000, H=3, d=128, R=5, dtype="bf16"),
+    dict(B=1, T=2048, H=16, d=128, R=2, dtype="bf16", cu_seqlens=[0, 700, 1800, 2048]),
+])
+def test_wy_workspace_covers_every_chunk_of_every_fragment(cpdr_lib, kw):
+    """24 KiB of WY tiles per (64-token chunk of a fragment, head) on the
+    tensor-core path; nothing on the CUDA-core path."""
+    ctx = make(**kw)
+    chunks = sum((f[1] + 63) // 64 for f in ctx.fragments())
+    assert ctx.counts()["tc"] == 1
+    assert ctx.wy_bytes() == chunks * kw["H"] * 3 * 8192
+    simt = make(**kw, force_simt=True)
+    assert simt.wy_bytes() == 0
+    assert make(**dict(kw, dtype="fp32")).wy_bytes() == 0

@@ -97,6 +97,15 @@ def test_tiny_and_ragged(case, gate, dtype):
     print(case, compare(run_gpu(inp), run_oracle(inp), inp))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_steep_decay(dtype):
+    """alpha ~ sigmoid(N(-3, 0.5)) ~ 0.05 per token: the in-chunk decay spans
+    far more than 2^100, which takes the exact-exponential branch."""
+    w = inputs.Workload("steep", "gdn", dtype, 1, 2048, 4, 128, 4, gate_dist=("sigmoid", -3.0, 0.5), seed=21)
+    inp = inputs.make_inputs(w, device="cpu")
+    print(compare(run_gpu(inp), run_oracle(inp), inp))
+
+
 @pytest.mark.parametrize("name", ["gdn_bf16_b2_t8192_h16_d128_r8"])
 def test_fp32_cuda_core_path_cross_check(name):
     inp = gen(name, B=1, T=2048, H=4)

@@ -62,11 +62,12 @@ def test_noalloc_matches_regular_entry_points(cpdr_lib, name, kw, kind):
 def test_noalloc_rejects_problems_beyond_its_scratch(cpdr_lib):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
-    # headline shape: 3 x 64 x 16 x 64 KiB of exchange buffers >> 16 MiB
+    # T = 262144, H = 16, R = 64: 3 x 64 x 16 x 64 KiB of exchange buffers and
+    # 4096 x 16 x 24 KiB of WY tiles >> 32 MiB
     ctx = cpdr.Context(1, 262144, 16, 128, 64, gate="gdn", dtype="bf16", host_only=True)
     x = torch.zeros(16, device="cuda")
     with pytest.raises(cpdr.CpdrError) as ei:
         cpdr_lib_call = ctx._lib.cpdr_forward_noalloc
         cpdr._check(cpdr_lib_call(ctx._h, *[cpdr._ptr(x)] * 7, cpdr._stream(None)))
     assert ei.value.status == cpdr.ERR_WORKSPACE
-    assert b"16777216" in cpdr_lib.cpdr_last_error()
+    assert b"33554432" in cpdr_lib.cpdr_last_error()
