@@ -10,7 +10,7 @@
 // on the tensor core):
 //   W^T    = K^T T''^T,  U^T = V^T T'^T                      (MMA)
 //   Delta^T= U^T - S^T W^T                                   (MMA, accumulate)
-//   O^T    = S^T Q^T scaled by gamma_i + Delta^T mask^T,
+//   O^T    = S^T (gamma ⊙ Q)^T + Delta^T mask^T,  gamma_i = 2^(G_i),
 //            mask_ij = (Q K^T)_ij 2^(G_i - G_j), j <= i      (forward)
 //   S^T   <- gamma^C S^T + (Delta diag(Gamma))^T K,  Gamma_j = 2^(G_C - G_j)
 // The pre-process runs the same chain without outputs (role S) and, in a
@@ -22,9 +22,9 @@
 // pair, so each product is hi*hi + lo*hi + hi*lo.
 //
 // Warp roles (16 warps): 0 TMA producer and in-chunk gates; 1 MMA issuer
-// (+ TMEM owner); 2-3 causal mask (forward only); 4-7 W epilogue; 8-15 state
-// warps (Delta, S and O epilogues; the fp32 state lives in their registers,
-// 64 values per thread).  The critical path per chunk is
+// (+ TMEM owner); 2-3 causal mask (forward only); 4-7 W and O epilogues;
+// 8-15 state warps (Delta epilogue and S update; the fp32 state lives in
+// their registers, 64 values per thread).  The critical path per chunk is
 //   Delta MMA -> Delta epilogue -> P_S MMA -> S update -> Delta MMA,
 // and the next chunk's W, U (and Q K^T) products are issued into the gaps.
 // Roles and shared-memory layouts are compile-time and every role function
@@ -67,14 +67,20 @@ __device__ unsigned long long g_cpdr_trace[3][8][64][16];
     } while (0)
 #endif
 
-// TMEM columns (fp32, 128 lanes each)
-constexpr uint32_t TM_P = 0, TM_W = 64, TM_DL = 128, TM_O1 = 192, TM_O2 = 256, TM_PS = 320;
+// TMEM columns (128 lanes each).  fp32 accumulators: P = [K; Q] K^T, W^T,
+// Delta^T (over U^T), O^T, P_S.  bf16 A operands of later products, two
+// values per column: -S^T (SB), -Delta^T (DB, forward) and (Delta diag
+// Gamma)^T (DGB); the M chain's lo halves of -M^T and of (Delta diag Gamma)^T
+// use the columns that P and DB occupy in the forward.
+constexpr uint32_t TM_P = 0, TM_W = 64, TM_DL = 128, TM_O = 192, TM_PS = 256, TM_SB = 384, TM_DB = 448,
+                   TM_DGB = 480;
+constexpr uint32_t TM_SB_LO = 0, TM_DGB_LO = 448;
 constexpr uint32_t TM_COLS = 512;
 
 // mbarrier indices
 enum Bar {
     B_FULL0, B_FULL1, B_FULL2, B_EMPTY0, B_EMPTY1, B_EMPTY2, B_PFULL, B_PFREE, B_WFULL, B_WREADY, B_WBFREE,
-    B_DLFULL, B_DLREADY, B_PSFULL, B_SREADY, B_OFULL, B_OFREE, B_MREADY, B_MFREE,
+    B_DLFULL, B_DLREADY, B_PSFULL, B_SREADY, B_OFULL, B_OFREE, B_QREADY, B_MREADY, B_MFREE,
     B_GATE0, B_GATE1, B_GATE2, B_GATE3, B_GATE4, B_DRAIN, NBARS
 };
 constexpr int kMaxGateSlots = 5;
@@ -102,7 +108,7 @@ struct Params {
 struct Lay {
     uint32_t nstage, stage_bytes, kc0, kc1, qc0, qc1, vc0, vc1, t1, t2, k_lbo, v_lbo, tx_bytes, wy_off;
     uint32_t ngate, gate_floats;
-    uint32_t mask, wb, wb_lo, sb, sb_lo, db, dgb, dgb_lo, gates, bars, ctl, tslot, total;
+    uint32_t mask, wb, wb_lo, gates, bars, ctl, tslot, total;
 };
 
 __host__ __device__ constexpr Lay make_lay(int mode, int role) {
@@ -121,9 +127,8 @@ __host__ __device__ constexpr Lay make_lay(int mode, int role) {
         L.k_lbo = 8192; L.v_lbo = 0; L.wy_off = (uint32_t)kWyTileBytes;
     }
     L.tx_bytes = L.stage_bytes;
-    // three stages for the pre-process (loads start two chunks ahead), two
-    // for the forward (shared memory bound)
-    L.nstage = (mode == MODE_FWD) ? 2 : 3;
+    // three stages: a chunk's loads start two chunks ahead
+    L.nstage = 3;
     // gate slots: a slot is rewritten once the chunk NG before it is
     // finished, which the stage ring guarantees for NG = stages + 2
     L.ngate = L.nstage + 2;
@@ -135,11 +140,6 @@ __host__ __device__ constexpr Lay make_lay(int mode, int role) {
     L.mask = o; o += (mode == MODE_FWD ? 8192 : 0);
     L.wb = o; o += 16384;
     L.wb_lo = o; o += (split ? 16384 : 0);
-    L.sb = o; o += 32768;
-    L.sb_lo = o; o += (split ? 32768 : 0);
-    L.db = o; o += (mode == MODE_FWD ? 16384 : 0);
-    L.dgb = o; o += 16384;
-    L.dgb_lo = o; o += (split ? 16384 : 0);
     L.gates = o; o += L.ngate * L.gate_floats * 4;
     o = (o + 15) & ~15u;
     L.bars = o; o += NBARS * 8;
@@ -338,6 +338,24 @@ __device__ __forceinline__ void mma_mnk(uint32_t d, uint64_t a, uint64_t b, uint
     }
 }
 
+// D(128 x N) (+)= A(128 x K, in TMEM from column a) * B(MN-major, 2048 B per k-step)
+template <int N, int K>
+__device__ __forceinline__ void mma_tmn(uint32_t d, uint32_t a, uint64_t b, bool acc) {
+    constexpr uint32_t id = idesc_bf16(128, N, false, true);
+#pragma unroll
+    for (int k = 0; k < K / 16; k++) mma_bf16_ts(d, a + 8 * k, b + (uint64_t)(k * 128), id, (acc || k > 0) ? 1u : 0u);
+}
+// D(128 x N) (+)= A(128 x K, in TMEM from column a) * B(K-major rows = N)
+template <int N, int K>
+__device__ __forceinline__ void mma_tk(uint32_t d, uint32_t a, uint64_t b, uint32_t katom_b, bool acc) {
+    constexpr uint32_t id = idesc_bf16(128, N, false, false);
+#pragma unroll
+    for (int k = 0; k < K / 16; k++) {
+        const uint64_t bo = ((k & 3) * 32 + (k >> 2) * katom_b) >> 4;
+        mma_bf16_ts(d, a + 8 * k, b + bo, id, (acc || k > 0) ? 1u : 0u);
+    }
+}
+
 template <int MODE, int ROLE>
 __device__ __forceinline__ void run_mma(const Run &r) {
     constexpr Lay L = make_lay(MODE, ROLE);
@@ -354,9 +372,7 @@ __device__ __forceinline__ void run_mma(const Run &r) {
     const uint64_t d_vmn0 = mndesc(b0 + L.vc0, L.v_lbo), d_q0 = kdesc(b0 + L.qc0);
     const uint64_t d_t10 = kdesc(b0 + L.t1), d_t20 = kdesc(b0 + L.t2);
     auto stg = [&](uint64_t d, int t) { return d + (uint64_t)((t % NS) * (L.stage_bytes >> 4)); };
-    const uint64_t d_sb = kdesc(b0 + L.sb), d_sblo = kdesc(b0 + L.sb_lo);
     const uint64_t d_wb = mndesc(b0 + L.wb, 16384), d_wblo = mndesc(b0 + L.wb_lo, 16384);
-    const uint64_t d_dgb = kdesc(b0 + L.dgb), d_dgblo = kdesc(b0 + L.dgb_lo), d_db = kdesc(b0 + L.db);
     const uint64_t d_mask = kdesc(b0 + L.mask);
     constexpr uint32_t KATOM = L.kc1 - L.kc0, QATOM = L.qc1 - L.qc0;
 
@@ -389,22 +405,26 @@ __device__ __forceinline__ void run_mma(const Run &r) {
             if (!mbar_wait(&r.bar[B_WREADY], t & 1, ctl, st, 25)) break;
             TR(1, t, 2);
             tc_fence_after();
-            // Delta^T (+)= -S^T W^T
+            // Delta^T (+)= (-S^T) W^T
             if (!SPLIT) {
-                mma_kmn<64, 128, true>(tm + TM_DL, d_sb, 16384, d_wb, HAS_U);
+                mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d_wb, HAS_U);
             } else {
-                mma_kmn<64, 128, true>(tm + TM_DL, d_sb, 16384, d_wb, false);
-                mma_kmn<64, 128, true>(tm + TM_DL, d_sblo, 16384, d_wb, true);
-                mma_kmn<64, 128, true>(tm + TM_DL, d_sb, 16384, d_wblo, true);
+                mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d_wb, false);
+                mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB_LO, d_wb, true);
+                mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d_wblo, true);
             }
             mma_commit(&r.bar[B_WBFREE]);
-            if (FWD) {
-                if (t >= 1 && !mbar_wait(&r.bar[B_OFREE], (t - 1) & 1, ctl, st, 26)) break;
-                tc_fence_after();
-                mma_kk<64, 128, false>(tm + TM_O1, d_sb, 16384, stg(d_q0, t), QATOM, false);   // O1^T = S^T Q^T
-            }
             mma_commit(&r.bar[B_DLFULL]);
             TR(1, t, 3);
+            // O^T = S^T (gamma ⊙ Q)^T, before S is rewritten after P_S,
+            // and before chunk t+1's front products: those let the mask warps
+            // signal QREADY for t+1, which must not pass this wait's phase
+            if (FWD) {
+                if (t >= 1 && !mbar_wait(&r.bar[B_OFREE], (t - 1) & 1, ctl, st, 26)) break;
+                if (!mbar_wait(&r.bar[B_QREADY], t & 1, ctl, st, 31)) break;
+                tc_fence_after();
+                mma_tk<64, 128>(tm + TM_O, tm + TM_SB, stg(d_q0, t), QATOM, false);   // holds -O^T
+            }
             // the next chunk's front products, if its loads are in (and, in
             // the forward, the mask warps have read this chunk's P)
             ahead = false;
@@ -414,12 +434,13 @@ __device__ __forceinline__ void run_mma(const Run &r) {
                 front(t + 1);
                 ahead = true;
             }
+            TR(1, t, 7);
             if (!mbar_wait(&r.bar[B_DLREADY], t & 1, ctl, st, 27)) break;
             TR(1, t, 4);
             tc_fence_after();
             // P_S = (Delta diag Gamma)^T K
-            mma_kmn<128, 64, false>(tm + TM_PS, d_dgb, 16384, stg(d_kmn0, t), false);
-            if (SPLIT) mma_kmn<128, 64, false>(tm + TM_PS, d_dgblo, 16384, stg(d_kmn0, t), true);
+            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg(d_kmn0, t), false);
+            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg(d_kmn0, t), true);
             mma_commit(&r.bar[B_PSFULL]);
             TR(1, t, 5);
             if (t + 1 < r.n) {
@@ -434,7 +455,7 @@ __device__ __forceinline__ void run_mma(const Run &r) {
             if (FWD) {
                 if (!mbar_wait(&r.bar[B_MREADY], t & 1, ctl, st, 28)) break;
                 tc_fence_after();
-                mma_kk<64, 64, false>(tm + TM_O2, d_db, 16384, d_mask, 8192, false);   // O2^T = Delta^T mask^T
+                mma_tk<64, 64>(tm + TM_O, tm + TM_DB, d_mask, 8192, true);   // -O^T += (-Delta^T) mask^T
                 mma_commit(&r.bar[B_OFULL]);
                 mma_commit(&r.bar[B_MFREE]);
             }
@@ -462,6 +483,28 @@ __device__ __forceinline__ void run_mask(const Run &r) {
         if (!warp_wait(r, B_PFULL, ch & 1, 51)) return;
         if (w == 2) TR(4, ch, 1);
         tc_fence_after();
+        // Q K^T has been computed (first: the O product waits for it): scale
+        // row i of this chunk's Q tile by gamma_i in place, so that
+        // S^T (gamma ⊙ Q)^T and Delta^T mask^T accumulate into one TMEM tile
+        {
+            uint8_t *st = r.base + (ch % (int)L.nstage) * L.stage_bytes;
+            const __nv_bfloat162 g2 = __float2bfloat162_rn(gs.gam[i]);
+#pragma unroll
+            for (int a = 0; a < 2; a++) {
+                uint8_t *tile = st + (a ? L.qc1 : L.qc0);
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    uint4 u = *reinterpret_cast<uint4 *>(tile + sw128(i, c));
+                    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+                    for (int e = 0; e < 4; e++) h[e] = __hmul2(h[e], g2);
+                    *reinterpret_cast<uint4 *>(tile + sw128(i, c)) = u;
+                }
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&r.bar[B_QREADY]);
+        }
         const float Gi = gs.G[i], ei = gs.e[i];
         const bool exact = gs.gC[1] != 0.f;
         float m[64];
@@ -496,17 +539,23 @@ __device__ __forceinline__ void run_mask(const Run &r) {
     }
 }
 
-// ------------------------------------------------------------------ W epilogue warps
-// W^T (TMEM lanes = dk) -> bf16 MN-major B tile of the Delta product (hi/lo when split)
+// ------------------------------------------------------------------ W and O epilogue warps
+// W epilogue: W^T (TMEM lanes = dk) -> bf16 MN-major B tile of the Delta
+// product (hi/lo when split).  O epilogue (forward): o = scale (gamma_i O1 +
+// O2) for the 64 tokens of a chunk, TMEM lane = value dim; O1 + O2 arrive
+// as one accumulator (the gamma_i row scale is folded into Q).  Per chunk t the
+// warps handle W of chunk t+1 first (it gates the next Delta product), then O
+// of chunk t.
 template <int MODE, int ROLE>
 __device__ __forceinline__ void run_wepi(const Run &r) {
     constexpr Lay L = make_lay(MODE, ROLE);
-    constexpr bool SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
+    constexpr bool FWD = MODE == MODE_FWD, SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
+    const Params &p = *r.p;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = w & 3, row = 32 * q + lane;
     const uint32_t lane_base = r.tmem + ((uint32_t)(32 * q) << 16);
-    for (int t = 0; t < r.n; t++) {
-        if (!warp_wait(r, B_WFULL, t & 1, 40)) return;
+    auto w_epilogue = [&](int t) -> bool {
+        if (!warp_wait(r, B_WFULL, t & 1, 40)) return false;
         if (w == 4) TR(2, t, 0);
         tc_fence_after();
         float v0[32], v1[32];
@@ -515,20 +564,65 @@ __device__ __forceinline__ void run_wepi(const Run &r) {
         tmem_ld_wait();
         tc_fence_before();
         // the previous chunk's Delta product must have read the tile
-        if (t >= 1 && !warp_wait(r, B_WBFREE, (t - 1) & 1, 41)) return;
+        if (t >= 1 && !warp_wait(r, B_WBFREE, (t - 1) & 1, 41)) return false;
         store_row<4>(r.base + L.wb, SPLIT ? r.base + L.wb_lo : nullptr, row, 0, v0);
         store_row<4>(r.base + L.wb, SPLIT ? r.base + L.wb_lo : nullptr, row, 4, v1);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&r.bar[B_WREADY]);
         if (w == 4) TR(2, t, 1);
+        return true;
+    };
+    if (!w_epilogue(0)) return;
+    for (int t = 0; t < r.n; t++) {
+        if (t + 1 < r.n && !w_epilogue(t + 1)) return;
+        if (FWD) {
+            if (!warp_wait(r, B_OFULL, t & 1, 43)) return;
+            if (w == 4) TR(2, t, 3);
+            tc_fence_after();
+            const int nv = rows_of(r, t);
+            const int64_t ostride = (int64_t)p.H * D;
+            __nv_bfloat16 *op = p.o + ((r.tok0 + (int64_t)t * C) * p.H + r.h) * D + row;
+            const float sc = -p.scale;   // the accumulator holds -O^T
+            float a[32], b[32];
+            tmem_ld32(lane_base + TM_O, a);
+            tmem_ld32(lane_base + TM_O + 32, b);
+            tmem_ld_wait();
+            if (w == 4) TR(2, t, 4);
+            // the accumulator is in registers: release it before the stores
+            // (an arrive after them would wait for the stores to complete)
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&r.bar[B_OFREE]);
+#pragma unroll
+            for (int i = 0; i < 32; i++)
+                if (i < nv) op[i * ostride] = __float2bfloat16_rn(sc * a[i]);
+#pragma unroll
+            for (int i = 0; i < 32; i++)
+                if (32 + i < nv) op[(32 + i) * ostride] = __float2bfloat16_rn(sc * b[i]);
+            if (w == 4) TR(2, t, 2);
+        }
     }
 }
 
 // ------------------------------------------------------------------ state warps
+// -x as bf16 pairs (and the residual pairs -x - bf16(-x) when lo != nullptr):
+// column c of the pair array holds x[2c], x[2c+1].
+template <int NC>
+__device__ __forceinline__ void neg_pairs(const float *x, uint32_t (&hi)[NC], uint32_t *lo) {
+#pragma unroll
+    for (int c = 0; c < NC; c++) {
+        const float a = -x[2 * c], b = -x[2 * c + 1];
+        hi[c] = pack_bf16(a, b);
+        if (lo) {
+            const float2 h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hi[c]));
+            lo[c] = pack_bf16(a - h.x, b - h.y);
+        }
+    }
+}
+
 template <int MODE, int ROLE>
 __device__ __forceinline__ void run_state(const Run &r) {
-    constexpr Lay L = make_lay(MODE, ROLE);
     constexpr bool FWD = MODE == MODE_FWD, SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
     const Params &p = *r.p;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -536,10 +630,23 @@ __device__ __forceinline__ void run_state(const Run &r) {
     const int row = 32 * q + lane;                       // TMEM lane: value dim (or M column)
     const uint32_t lane_base = r.tmem + ((uint32_t)(32 * q) << 16);
     const int H = p.H;
-    uint8_t *sb = r.base + L.sb + half * 16384;
-    uint8_t *sb_lo = SPLIT ? r.base + L.sb_lo + half * 16384 : nullptr;
     float S[64];
     const int64_t sidx = ((int64_t)r.seg * H + r.h) * D * D;
+    // -S^T[row][64 half .. 64 half + 63] as the bf16 A operand (hi, lo) of the
+    // next Delta and O products
+    auto put_state = [&]() {
+#pragma unroll
+        for (int part = 0; part < 2; part++) {
+            uint32_t hi[16], lo[16];
+            neg_pairs<16>(S + 32 * part, hi, SPLIT ? lo : nullptr);
+            tmem_st16(lane_base + TM_SB + 32 * half + 16 * part, hi);
+            if (SPLIT) tmem_st16(lane_base + TM_SB_LO + 32 * half + 16 * part, lo);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&r.bar[B_SREADY]);
+    };
     // initial state: S^T[row][64 half + i]
 #pragma unroll
     for (int i = 0; i < 64; i++) {
@@ -549,14 +656,11 @@ __device__ __forceinline__ void run_state(const Run &r) {
         else if (FWD && (r.flags & CPDR_FRAG_CONT_PREV)) x = p.S_init[sidx + (int64_t)dk * D + row];
         S[i] = x;
     }
-    store_row<8>(sb, sb_lo, row, 0, S);
-    fence_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&r.bar[B_SREADY]);
+    put_state();
     for (int ch = 0; ch < r.n; ch++) {
         if (!warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 60)) return;
         const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(ch));
-        // Delta epilogue
+        // Delta epilogue: tokens 32 half .. 32 half + 31 of Delta^T[row]
         if (w == 8) TR(3, ch, 0);
         if (!warp_wait(r, B_DLFULL, ch & 1, 61)) return;
         if (w == 8) TR(3, ch, 1);
@@ -565,12 +669,22 @@ __device__ __forceinline__ void run_state(const Run &r) {
             float v[32];
             tmem_ld32(lane_base + TM_DL + 32 * half, v);
             tmem_ld_wait();
-            if (FWD) store_row<4>(r.base + L.db, nullptr, row, 4 * half, v);
+            if (w == 8) TR(3, ch, 5);
+            if (FWD) {   // -Delta^T for the masked output product
+                uint32_t d16[16];
+                neg_pairs<16>(v, d16, nullptr);
+                tmem_st16(lane_base + TM_DB + 16 * half, d16);
+            }
+            // (Delta diag Gamma)^T for P_S (negated here, so that the pair
+            // conversion below stores it with a plus sign)
 #pragma unroll
-            for (int jj = 0; jj < 32; jj++) v[jj] *= gs.Gam[32 * half + jj];
-            store_row<4>(r.base + L.dgb, SPLIT ? r.base + L.dgb_lo : nullptr, row, 4 * half, v);
+            for (int jj = 0; jj < 32; jj++) v[jj] = -(v[jj] * gs.Gam[32 * half + jj]);
+            uint32_t hi[16], lo[16];
+            neg_pairs<16>(v, hi, SPLIT ? lo : nullptr);
+            tmem_st16(lane_base + TM_DGB + 16 * half, hi);
+            if (SPLIT) tmem_st16(lane_base + TM_DGB_LO + 16 * half, lo);
+            tmem_st_wait();
         }
-        fence_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&r.bar[B_DLREADY]);
@@ -589,41 +703,10 @@ __device__ __forceinline__ void run_state(const Run &r) {
 #pragma unroll
                 for (int i = 0; i < 32; i++) S[32 * piece + i] = fmaf(gC, S[32 * piece + i], v[i]);
             }
+            if (w == 8) TR(3, ch, 6);
         }
-        store_row<8>(sb, sb_lo, row, 0, S);
-        fence_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&r.bar[B_SREADY]);
+        put_state();
         if (w == 8) TR(3, ch, 4);
-        if (FWD) {
-            // O = scale (gamma_i O1 + O2)
-            if (!warp_wait(r, B_OFULL, ch & 1, 63)) return;
-            tc_fence_after();
-            const int nv = rows_of(r, ch) - 32 * half;   // valid rows of this thread's half
-            const int64_t ostride = (int64_t)H * D;
-            __nv_bfloat16 *op = p.o + ((r.tok0 + (int64_t)ch * C + 32 * half) * H + r.h) * D + row;
-            const float sc = p.scale;
-            const float *gam = gs.gam + 32 * half;
-#pragma unroll
-            for (int piece = 0; piece < 2; piece++) {
-                float a[16], b[16];
-                tmem_ld16(lane_base + TM_O1 + 32 * half + 16 * piece, a);
-                tmem_ld16(lane_base + TM_O2 + 32 * half + 16 * piece, b);
-                tmem_ld_wait();
-                if (piece == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&r.bar[B_OFREE]);
-                }
-#pragma unroll
-                for (int ii = 0; ii < 16; ii++) {
-                    const int i = 16 * piece + ii;
-                    if (i < nv) op[i * ostride] = __float2bfloat16_rn(sc * fmaf(gam[i], a[ii], b[ii]));
-                }
-            }
-            if (w == 8) TR(3, ch, 5);
-        }
     }
     // outputs of the chain
     if (FWD) {
@@ -662,16 +745,17 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     r.chunk0 = p.chunk0[fi];
     r.p = &p;
     if (threadIdx.x == 0) {
-        // arrival counts: PFREE 2 mask warps, WREADY 4 W-epilogue warps,
-        // DLREADY / SREADY / OFREE 8 state warps, MREADY 2 mask warps
+        // arrival counts: PFREE / QREADY / MREADY 2 mask warps, WREADY / OFREE
+        // 4 W/O-epilogue warps, DLREADY / SREADY 8 state warps
         uint32_t cnt[NBARS];
         for (int i = 0; i < NBARS; i++) cnt[i] = 1;
         cnt[B_PFREE] = 2;
         cnt[B_WREADY] = 4;
         cnt[B_DLREADY] = 8;
         cnt[B_SREADY] = 8;
-        cnt[B_OFREE] = 8;
+        cnt[B_OFREE] = 4;
         cnt[B_MREADY] = 2;
+        cnt[B_QREADY] = 2;
         for (int i = 0; i < NBARS; i++) mbar_init(&r.bar[i], cnt[i]);
         r.ctl->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
