@@ -80,10 +80,11 @@ constexpr uint32_t TM_COLS = 512;
 // mbarrier indices
 enum Bar {
     B_FULL0, B_FULL1, B_FULL2, B_EMPTY0, B_EMPTY1, B_EMPTY2, B_PFULL, B_PFREE, B_WFULL, B_WREADY, B_WBFREE,
-    B_DLFULL, B_DLREADY, B_PSFULL, B_SREADY, B_OFULL, B_OFREE, B_QREADY, B_MREADY, B_MFREE,
-    B_GATE0, B_GATE1, B_GATE2, B_GATE3, B_GATE4, B_DRAIN, NBARS
+    B_UFULL, B_DLFULL, B_DLREADY, B_PSFULL, B_OFULL, B_OFREE, B_QREADY0, B_QREADY1, B_MREADY, B_MFREE,
+    B_GATE0, B_GATE1, B_GATE2, B_GATE3, B_GATE4, B_DRAIN, B_DRAIN2, NBARS
 };
 constexpr int kMaxGateSlots = 5;
+constexpr int kStateBar = 1;   // named barrier of the 8 state warps
 
 struct Params {
     const cpdr_fragment *frags;
@@ -356,6 +357,36 @@ __device__ __forceinline__ void mma_tk(uint32_t d, uint32_t a, uint64_t b, uint3
     }
 }
 
+// Shared-memory operand descriptors of one CTA (stage-0 addresses; stage s
+// adds s * stage_bytes >> 4).
+struct Descs {
+    uint64_t stack0, kmn0, vmn0, q0, t10, t20, wb, wblo, mask;
+};
+template <int MODE, int ROLE>
+__device__ __forceinline__ Descs make_descs(const Run &r) {
+    constexpr Lay L = make_lay(MODE, ROLE);
+    const uint32_t b0 = smem_u32(r.base);
+    Descs d;
+    d.stack0 = kdesc(b0 + L.kc0);
+    d.kmn0 = mndesc(b0 + L.kc0, L.k_lbo);
+    d.vmn0 = mndesc(b0 + L.vc0, L.v_lbo);
+    d.q0 = kdesc(b0 + L.qc0);
+    d.t10 = kdesc(b0 + L.t1);
+    d.t20 = kdesc(b0 + L.t2);
+    d.wb = mndesc(b0 + L.wb, 16384);
+    d.wblo = mndesc(b0 + L.wb_lo, 16384);
+    d.mask = kdesc(b0 + L.mask);
+    return d;
+}
+template <int MODE, int ROLE>
+__device__ __forceinline__ uint64_t stg(uint64_t d, int t) {
+    constexpr Lay L = make_lay(MODE, ROLE);
+    return d + (uint64_t)((t % (int)L.nstage) * (L.stage_bytes >> 4));
+}
+
+// MMA warp: the products off the chain's critical path, as early as their
+// inputs and TMEM columns allow -- chunk t's Q K^T (forward), W^T = K^T T''^T
+// (hi + lo when split) and U^T = V^T T'^T.
 template <int MODE, int ROLE>
 __device__ __forceinline__ void run_mma(const Run &r) {
     constexpr Lay L = make_lay(MODE, ROLE);
@@ -366,103 +397,39 @@ __device__ __forceinline__ void run_mma(const Run &r) {
     const uint32_t tm = r.tmem;
     int32_t *st = r.p->status;
     Ctl *ctl = r.ctl;
-    const uint32_t b0 = smem_u32(r.base);
-    // stage-0 operand descriptors; stage s adds s * stage_bytes >> 4
-    const uint64_t d_stack0 = kdesc(b0 + L.kc0), d_kmn0 = mndesc(b0 + L.kc0, L.k_lbo);
-    const uint64_t d_vmn0 = mndesc(b0 + L.vc0, L.v_lbo), d_q0 = kdesc(b0 + L.qc0);
-    const uint64_t d_t10 = kdesc(b0 + L.t1), d_t20 = kdesc(b0 + L.t2);
-    auto stg = [&](uint64_t d, int t) { return d + (uint64_t)((t % NS) * (L.stage_bytes >> 4)); };
-    const uint64_t d_wb = mndesc(b0 + L.wb, 16384), d_wblo = mndesc(b0 + L.wb_lo, 16384);
-    const uint64_t d_mask = kdesc(b0 + L.mask);
-    constexpr uint32_t KATOM = L.kc1 - L.kc0, QATOM = L.qc1 - L.qc0;
-
-    // chunk t's loads have landed: Q K^T (forward) and W^T = K^T T''^T (hi + lo when split)
-    auto front = [&](int t) {
+    const Descs d = make_descs<MODE, ROLE>(r);
+    constexpr uint32_t KATOM = L.kc1 - L.kc0;
+    for (int t = 0; t < r.n; t++) {
+        if (!mbar_wait(&r.bar[B_FULL0 + t % NS], (t / NS) & 1, ctl, st, 20)) break;
+        // TMEM columns of W and P are free once chunk t-1's were read; the
+        // products go into the tensor pipe after chunk t-1's Delta product
+        // has completed (W behind it would delay the chain)
+        if (t >= 1 && !mbar_wait(&r.bar[B_WREADY], (t - 1) & 1, ctl, st, 21)) break;
+        if (t >= 1 && !mbar_wait(&r.bar[B_WBFREE], (t - 1) & 1, ctl, st, 24)) break;
+        if (FWD && t >= 1 && !mbar_wait(&r.bar[B_PFREE], (t - 1) & 1, ctl, st, 22)) break;
+        tc_fence_after();
+        TR(1, t, 0);
         if (FWD) {   // P = [K; Q] K^T, rows 64..127 = Q K^T
-            mma_kk<64, 128, false>(tm + TM_P, stg(d_stack0, t), KATOM, stg(d_stack0, t), KATOM, false);
+            mma_kk<64, 128, false>(tm + TM_P, stg<MODE, ROLE>(d.stack0, t), KATOM, stg<MODE, ROLE>(d.stack0, t),
+                                   KATOM, false);
             mma_commit(&r.bar[B_PFULL]);
         }
-        const uint64_t tpp = SPLIT ? stg(d_t10, t) : stg(d_t20, t);
-        mma_mnk<64, 64>(tm + TM_W, stg(d_kmn0, t), tpp, 8192, false);
-        if (SPLIT) mma_mnk<64, 64>(tm + TM_W, stg(d_kmn0, t), stg(d_t20, t), 8192, true);
+        const uint64_t tpp = SPLIT ? stg<MODE, ROLE>(d.t10, t) : stg<MODE, ROLE>(d.t20, t);
+        mma_mnk<64, 64>(tm + TM_W, stg<MODE, ROLE>(d.kmn0, t), tpp, 8192, false);
+        if (SPLIT) mma_mnk<64, 64>(tm + TM_W, stg<MODE, ROLE>(d.kmn0, t), stg<MODE, ROLE>(d.t20, t), 8192, true);
         mma_commit(&r.bar[B_WFULL]);
-    };
-    // U^T = V^T T'^T into the Delta accumulator
-    auto umma = [&](int t) {
-        if (HAS_U) mma_mnk<64, 64>(tm + TM_DL, stg(d_vmn0, t), stg(d_t10, t), 8192, false);
-    };
-    do {
-        if (!mbar_wait(&r.bar[B_FULL0], 0, ctl, st, 20)) break;
-        tc_fence_after();
-        front(0);
-        umma(0);
-        bool ahead = false;   // chunk t+1's front() already issued
-        for (int t = 0; t < r.n; t++) {
-            const int s = t % NS;
-            TR(1, t, 0);
-            if (!mbar_wait(&r.bar[B_SREADY], t & 1, ctl, st, 24)) break;
-            TR(1, t, 1);
-            if (!mbar_wait(&r.bar[B_WREADY], t & 1, ctl, st, 25)) break;
-            TR(1, t, 2);
+        if (HAS_U) {
+            // the Delta accumulator is free once chunk t-1's Delta was read;
+            // U goes in after chunk t-1's P_S has completed
+            if (t >= 1 && !mbar_wait(&r.bar[B_DLREADY], (t - 1) & 1, ctl, st, 23)) break;
+            if (t >= 1 && !mbar_wait(&r.bar[B_PSFULL], (t - 1) & 1, ctl, st, 25)) break;
             tc_fence_after();
-            // Delta^T (+)= (-S^T) W^T
-            if (!SPLIT) {
-                mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d_wb, HAS_U);
-            } else {
-                mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d_wb, false);
-                mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB_LO, d_wb, true);
-                mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d_wblo, true);
-            }
-            mma_commit(&r.bar[B_WBFREE]);
-            mma_commit(&r.bar[B_DLFULL]);
-            TR(1, t, 3);
-            // O^T = S^T (gamma ⊙ Q)^T, before S is rewritten after P_S,
-            // and before chunk t+1's front products: those let the mask warps
-            // signal QREADY for t+1, which must not pass this wait's phase
-            if (FWD) {
-                if (t >= 1 && !mbar_wait(&r.bar[B_OFREE], (t - 1) & 1, ctl, st, 26)) break;
-                if (!mbar_wait(&r.bar[B_QREADY], t & 1, ctl, st, 31)) break;
-                tc_fence_after();
-                mma_tk<64, 128>(tm + TM_O, tm + TM_SB, stg(d_q0, t), QATOM, false);   // holds -O^T
-            }
-            // the next chunk's front products, if its loads are in (and, in
-            // the forward, the mask warps have read this chunk's P)
-            ahead = false;
-            if (t + 1 < r.n && mbar_test_wait(&r.bar[B_FULL0 + (t + 1) % NS], ((t + 1) / NS) & 1) &&
-                (!FWD || mbar_test_wait(&r.bar[B_PFREE], t & 1))) {
-                tc_fence_after();
-                front(t + 1);
-                ahead = true;
-            }
-            TR(1, t, 7);
-            if (!mbar_wait(&r.bar[B_DLREADY], t & 1, ctl, st, 27)) break;
-            TR(1, t, 4);
-            tc_fence_after();
-            // P_S = (Delta diag Gamma)^T K
-            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg(d_kmn0, t), false);
-            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg(d_kmn0, t), true);
-            mma_commit(&r.bar[B_PSFULL]);
-            TR(1, t, 5);
-            if (t + 1 < r.n) {
-                if (!ahead) {
-                    if (!mbar_wait(&r.bar[B_FULL0 + (t + 1) % NS], ((t + 1) / NS) & 1, ctl, st, 22)) break;
-                    if (FWD && !mbar_wait(&r.bar[B_PFREE], t & 1, ctl, st, 23)) break;
-                    tc_fence_after();
-                    front(t + 1);
-                }
-                umma(t + 1);
-            }
-            if (FWD) {
-                if (!mbar_wait(&r.bar[B_MREADY], t & 1, ctl, st, 28)) break;
-                tc_fence_after();
-                mma_tk<64, 64>(tm + TM_O, tm + TM_DB, d_mask, 8192, true);   // -O^T += (-Delta^T) mask^T
-                mma_commit(&r.bar[B_OFULL]);
-                mma_commit(&r.bar[B_MFREE]);
-            }
-            mma_commit(&r.bar[B_EMPTY0 + s]);
-            TR(1, t, 6);
+            mma_mnk<64, 64>(tm + TM_DL, stg<MODE, ROLE>(d.vmn0, t), stg<MODE, ROLE>(d.t10, t), 8192, false);
+            mma_commit(&r.bar[B_UFULL]);
         }
-    } while (0);
+        mma_commit(&r.bar[B_EMPTY0 + t % NS]);   // this warp's reads of stage t
+        TR(1, t, 1);
+    }
     // drain every MMA this thread issued
     mma_commit(&r.bar[B_DRAIN]);
     Ctl local;
@@ -503,7 +470,7 @@ __device__ __forceinline__ void run_mask(const Run &r) {
             }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&r.bar[B_QREADY]);
+            if (lane == 0) mbar_arrive(&r.bar[B_QREADY0 + (ch & 1)]);
         }
         const float Gi = gs.G[i], ei = gs.e[i];
         const bool exact = gs.gC[1] != 0.f;
@@ -621,15 +588,27 @@ __device__ __forceinline__ void neg_pairs(const float *x, uint32_t (&hi)[NC], ui
     }
 }
 
+// State warps (8-15): Delta epilogue and S update; lane 0 of warp 8 issues the
+// chain's own products (Delta, O, P_S) right after the warps meet at a named
+// barrier, so the critical path has no mbarrier hand-off to another warp.
 template <int MODE, int ROLE>
 __device__ __forceinline__ void run_state(const Run &r) {
+    constexpr Lay L = make_lay(MODE, ROLE);
     constexpr bool FWD = MODE == MODE_FWD, SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
+    constexpr bool HAS_U = FWD || ROLE == ROLE_S;
+    constexpr int NS = (int)L.nstage;
     const Params &p = *r.p;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = w & 3, half = (w - 8) >> 2;
     const int row = 32 * q + lane;                       // TMEM lane: value dim (or M column)
-    const uint32_t lane_base = r.tmem + ((uint32_t)(32 * q) << 16);
+    const uint32_t tm = r.tmem;
+    const uint32_t lane_base = tm + ((uint32_t)(32 * q) << 16);
+    const bool issuer = (w == 8 && lane == 0);
     const int H = p.H;
+    int32_t *st = p.status;
+    Ctl *ctl = r.ctl;
+    const Descs d = make_descs<MODE, ROLE>(r);
+    constexpr uint32_t QATOM = L.qc1 - L.qc0;
     float S[64];
     const int64_t sidx = ((int64_t)r.seg * H + r.h) * D * D;
     // -S^T[row][64 half .. 64 half + 63] as the bf16 A operand (hi, lo) of the
@@ -644,8 +623,6 @@ __device__ __forceinline__ void run_state(const Run &r) {
         }
         tmem_st_wait();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&r.bar[B_SREADY]);
     };
     // initial state: S^T[row][64 half + i]
 #pragma unroll
@@ -657,19 +634,47 @@ __device__ __forceinline__ void run_state(const Run &r) {
         S[i] = x;
     }
     put_state();
-    for (int ch = 0; ch < r.n; ch++) {
-        if (!warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 60)) return;
+    int bad = named_bar_or(kStateBar, 256, 0);
+    for (int ch = 0; ch < r.n && !bad; ch++) {
+        // ---- Delta (and O) products of chunk ch
+        if (issuer) {
+            bool ok = mbar_wait(&r.bar[B_WREADY], ch & 1, ctl, st, 64);
+            if (ok && HAS_U) ok = mbar_wait(&r.bar[B_UFULL], ch & 1, ctl, st, 65);
+            if (ok) {
+                tc_fence_after();
+                TR(1, ch, 2);
+                // Delta^T (+)= (-S^T) W^T
+                if (!SPLIT) {
+                    mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wb, HAS_U);
+                } else {
+                    mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wb, false);
+                    mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB_LO, d.wb, true);
+                    mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wblo, true);
+                }
+                mma_commit(&r.bar[B_WBFREE]);
+            }
+            if (ok && FWD) {   // -O^T = (-S^T) (gamma ⊙ Q)^T, before S is rewritten after P_S
+                if (ch >= 1) ok = mbar_wait(&r.bar[B_OFREE], (ch - 1) & 1, ctl, st, 66);
+                if (ok) ok = mbar_wait(&r.bar[B_QREADY0 + (ch & 1)], (ch >> 1) & 1, ctl, st, 67);
+                if (ok) {
+                    tc_fence_after();
+                    mma_tk<64, 128>(tm + TM_O, tm + TM_SB, stg<MODE, ROLE>(d.q0, ch), QATOM, false);
+                }
+            }
+            if (ok) mma_commit(&r.bar[B_DLFULL]);
+            TR(1, ch, 3);
+        }
+        bool ok = warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 60);
         const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(ch));
-        // Delta epilogue: tokens 32 half .. 32 half + 31 of Delta^T[row]
+        // ---- Delta epilogue: tokens 32 half .. 32 half + 31 of Delta^T[row]
         if (w == 8) TR(3, ch, 0);
-        if (!warp_wait(r, B_DLFULL, ch & 1, 61)) return;
+        if (ok) ok = warp_wait(r, B_DLFULL, ch & 1, 61);
         if (w == 8) TR(3, ch, 1);
-        tc_fence_after();
-        {
+        if (ok) {
+            tc_fence_after();
             float v[32];
             tmem_ld32(lane_base + TM_DL + 32 * half, v);
             tmem_ld_wait();
-            if (w == 8) TR(3, ch, 5);
             if (FWD) {   // -Delta^T for the masked output product
                 uint32_t d16[16];
                 neg_pairs<16>(v, d16, nullptr);
@@ -684,16 +689,38 @@ __device__ __forceinline__ void run_state(const Run &r) {
             tmem_st16(lane_base + TM_DGB + 16 * half, hi);
             if (SPLIT) tmem_st16(lane_base + TM_DGB_LO + 16 * half, lo);
             tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (HAS_U && lane == 0) mbar_arrive(&r.bar[B_DLREADY]);   // the U product may reuse the columns
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&r.bar[B_DLREADY]);
         if (w == 8) TR(3, ch, 2);
-        // state update: S <- gamma^C S + P_S
-        if (!warp_wait(r, B_PSFULL, ch & 1, 62)) return;
+        if ((bad = named_bar_or(kStateBar, 256, ok ? 0 : 1))) break;
+        // ---- P_S (and the masked output product) of chunk ch
+        if (issuer) {
+            tc_fence_after();
+            // P_S = (Delta diag Gamma)^T K
+            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kmn0, ch), false);
+            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg<MODE, ROLE>(d.kmn0, ch), true);
+            mma_commit(&r.bar[B_PSFULL]);
+            TR(1, ch, 4);
+            bool iok = true;
+            if (FWD) {
+                iok = mbar_wait(&r.bar[B_MREADY], ch & 1, ctl, st, 68);
+                if (iok) {
+                    tc_fence_after();
+                    mma_tk<64, 64>(tm + TM_O, tm + TM_DB, d.mask, 8192, true);   // -O^T += (-Delta^T) mask^T
+                    mma_commit(&r.bar[B_OFULL]);
+                    mma_commit(&r.bar[B_MFREE]);
+                }
+            }
+            if (iok) mma_commit(&r.bar[B_EMPTY0 + ch % NS]);   // this thread's reads of stage ch
+            TR(1, ch, 5);
+        }
+        // ---- state update: S <- gamma^C S + P_S
+        ok = warp_wait(r, B_PSFULL, ch & 1, 62);
         if (w == 8) TR(3, ch, 3);
-        tc_fence_after();
-        {
+        if (ok) {
+            tc_fence_after();
             const float gC = gs.gC[0];
 #pragma unroll
             for (int piece = 0; piece < 2; piece++) {
@@ -703,11 +730,19 @@ __device__ __forceinline__ void run_state(const Run &r) {
 #pragma unroll
                 for (int i = 0; i < 32; i++) S[32 * piece + i] = fmaf(gC, S[32 * piece + i], v[i]);
             }
-            if (w == 8) TR(3, ch, 6);
+            put_state();
         }
-        put_state();
         if (w == 8) TR(3, ch, 4);
+        bad = named_bar_or(kStateBar, 256, (ok && !ctl->abort) ? 0 : 1);
     }
+    // drain every MMA the issuer issued
+    if (issuer) {
+        mma_commit(&r.bar[B_DRAIN2]);
+        Ctl local;
+        local.abort = 0;
+        mbar_wait(&r.bar[B_DRAIN2], 0, &local, st, 69);
+    }
+    if (bad) return;
     // outputs of the chain
     if (FWD) {
         if ((r.flags & CPDR_FRAG_ENDS_SEQ) && p.final_state) {
@@ -746,16 +781,16 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     r.p = &p;
     if (threadIdx.x == 0) {
         // arrival counts: PFREE / QREADY / MREADY 2 mask warps, WREADY / OFREE
-        // 4 W/O-epilogue warps, DLREADY / SREADY 8 state warps
+        // 4 W/O-epilogue warps, DLREADY 8 state warps, EMPTY 2 MMA issuers
         uint32_t cnt[NBARS];
         for (int i = 0; i < NBARS; i++) cnt[i] = 1;
         cnt[B_PFREE] = 2;
         cnt[B_WREADY] = 4;
         cnt[B_DLREADY] = 8;
-        cnt[B_SREADY] = 8;
+        cnt[B_EMPTY0] = cnt[B_EMPTY1] = cnt[B_EMPTY2] = 2;   // MMA warp + state issuer
         cnt[B_OFREE] = 4;
         cnt[B_MREADY] = 2;
-        cnt[B_QREADY] = 2;
+        cnt[B_QREADY0] = cnt[B_QREADY1] = 2;
         for (int i = 0; i < NBARS; i++) mbar_init(&r.bar[i], cnt[i]);
         r.ctl->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

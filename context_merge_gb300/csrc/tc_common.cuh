@@ -101,6 +101,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Ctl *c
     return mbar_wait_slow(bar, parity, ctl, status, site);
 }
 
+// Bounded wait for a single thread on a latency-critical path: polls with
+// the non-suspending test (a suspended thread resumes several hundred
+// cycles after the phase completes), checking the clock and the abort flag
+// every 256 polls.  Same failure behaviour as mbar_wait.
+static __device__ __noinline__ bool mbar_poll_slow(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
+    const long long t0 = clock64();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 256; i++)
+            if (mbar_test_wait(bar, parity)) return true;
+        if (ctl->abort) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            if (atomicCAS(status, 0, 1) == 0) {
+                status[1] = site;
+                status[2] = (int32_t)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+            }
+            ctl->abort = 1;
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
+    if (mbar_test_wait(bar, parity)) return true;
+    return mbar_poll_slow(bar, parity, ctl, status, site);
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
