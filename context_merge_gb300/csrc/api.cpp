@@ -46,6 +46,13 @@ void free_tables(cpdr::DeviceTables &t) {
     t = cpdr::DeviceTables();
 }
 
+void free_streams(cpdr_ctx *c) {
+    if (c->ev_fork) cudaEventDestroy((cudaEvent_t)c->ev_fork);
+    if (c->ev_join) cudaEventDestroy((cudaEvent_t)c->ev_join);
+    if (c->aux_stream) cudaStreamDestroy((cudaStream_t)c->aux_stream);
+    c->aux_stream = c->ev_fork = c->ev_join = nullptr;
+}
+
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 cpdr_status check_ctx(const cpdr_ctx *c) {
@@ -143,8 +150,19 @@ cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
         if (e == cudaSuccess) e = upload(&t.wy_chunks, p.wy_chunks);
         if (e == cudaSuccess) e = cudaMalloc((void **)&t.status, 64);
         if (e == cudaSuccess) e = cudaMemset(t.status, 0, 64);
+        if (e == cudaSuccess && c->use_tc) {
+            cudaStream_t aux = nullptr;
+            cudaEvent_t ef = nullptr, ej = nullptr;
+            e = cudaStreamCreateWithFlags(&aux, cudaStreamNonBlocking);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ef, cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ej, cudaEventDisableTiming);
+            c->aux_stream = aux;
+            c->ev_fork = ef;
+            c->ev_join = ej;
+        }
         if (e != cudaSuccess) {
             free_tables(t);
+            free_streams(c);
             delete c;
             return cuda_err(e, "cpdr_ctx_create: device tables");
         }
@@ -156,6 +174,7 @@ cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
 
 void cpdr_ctx_destroy(cpdr_ctx *c) {
     if (!c) return;
+    free_streams(c);
     if (c->has_device) free_tables(c->dev);
     delete c;
 }

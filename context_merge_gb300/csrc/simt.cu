@@ -345,9 +345,10 @@ simt_pre_kernel(const cpdr_fragment *__restrict__ frags, const int32_t *__restri
 // Merge: grid (chains, H, D / MBV).  S = S_ext[r0]; then for j = r0+1 .. r1-1:
 // S <- M_j S + S_ext[j]; S_init[j] written after each step (S_init[r0+1] = S_ext[r0]).
 // Each thread owns an (RPT x 4) register tile of the (D x MBV) state tile; M_j is
-// staged row-major in shared memory with cp.async, the next step's M prefetched
-// while the current one is applied.
+// staged row-major in shared memory with cp.async, MNBUF - 1 steps ahead, and
+// the step's S_ext tile is loaded into registers one step ahead.
 constexpr int MBV = 16;
+constexpr int MNBUF = 3;
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
@@ -355,7 +356,9 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// wait until at most N committed groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int D>
 __global__ void __launch_bounds__(NT, 1)
@@ -364,17 +367,20 @@ merge_kernel(const MergeChain *__restrict__ chains, const float *__restrict__ S_
     extern __shared__ __align__(16) unsigned char smem_raw[];
     constexpr int LM = D + 4;                                  // padded row stride (16-byte rows)
     constexpr int RPT = D / 64;                                // rows per thread
-    float *Mn = reinterpret_cast<float *>(smem_raw);           // [2][D][LM]
-    float *Ss = Mn + 2 * D * LM;                               // [D][MBV]
+    float *Mn = reinterpret_cast<float *>(smem_raw);           // [MNBUF][D][LM]
+    float *Ss = Mn + MNBUF * D * LM;                           // [D][MBV]
     const MergeChain ch = chains[blockIdx.x];
     const int h = blockIdx.y, col0 = blockIdx.z * MBV;
     auto idx_of = [&](int r) { return ((int64_t)(r * B + ch.b) * H + h) * D * D; };
-    auto stage_M = [&](int j, int buf) {
-        const float *Mj = M + idx_of(j);
-        float *dst = Mn + buf * D * LM;
-        for (int idx = threadIdx.x; idx < D * D / 4; idx += NT) {
-            const int d = idx / (D / 4), l4 = idx % (D / 4);
-            cp_async16(dst + d * LM + 4 * l4, Mj + d * D + 4 * l4);
+    // stage M_j into buffer j % MNBUF (one commit group per step, empty past the end)
+    auto stage_M = [&](int j) {
+        if (j < ch.r1) {
+            const float *Mj = M + idx_of(j);
+            float *dst = Mn + ((j - ch.r0 - 1) % MNBUF) * D * LM;
+            for (int idx = threadIdx.x; idx < D * D / 4; idx += NT) {
+                const int d = idx / (D / 4), l4 = idx % (D / 4);
+                cp_async16(dst + d * LM + 4 * l4, Mj + d * D + 4 * l4);
+            }
         }
         cp_async_commit();
     };
@@ -384,19 +390,30 @@ merge_kernel(const MergeChain *__restrict__ chains, const float *__restrict__ S_
         Ss[d * MBV + c] = x;
         S_init[idx_of(ch.r0 + 1) + d * D + col0 + c] = x;
     }
-    if (ch.r0 + 1 < ch.r1) stage_M(ch.r0 + 1, 0);
+#pragma unroll
+    for (int k = 1; k < MNBUF; k++) stage_M(ch.r0 + k);
     const int rb = threadIdx.x >> 2, cb = (threadIdx.x & 3) * 4;
+    float4 ext[RPT];   // S_ext tile of the current step, loaded one step ahead
+    if (ch.r0 + 1 < ch.r1) {
+#pragma unroll
+        for (int r = 0; r < RPT; r++)
+            ext[r] = *reinterpret_cast<const float4 *>(S_ext + idx_of(ch.r0 + 1) + (RPT * rb + r) * D + col0 + cb);
+    }
     for (int j = ch.r0 + 1; j < ch.r1; j++) {
-        const int buf = (j - ch.r0 - 1) & 1;
-        cp_async_wait_all();
+        const int buf = (j - ch.r0 - 1) % MNBUF;
+        cp_async_wait<MNBUF - 2>();
         __syncthreads();   // M_j staged; the previous step's state tile written
-        if (j + 1 < ch.r1) stage_M(j + 1, buf ^ 1);
+        stage_M(j + MNBUF - 1);
         const float *Mb = Mn + buf * D * LM;
         float acc[RPT][4];
 #pragma unroll
         for (int r = 0; r < RPT; r++) {
-            const float4 e = *reinterpret_cast<const float4 *>(S_ext + idx_of(j) + (RPT * rb + r) * D + col0 + cb);
-            acc[r][0] = e.x; acc[r][1] = e.y; acc[r][2] = e.z; acc[r][3] = e.w;
+            acc[r][0] = ext[r].x; acc[r][1] = ext[r].y; acc[r][2] = ext[r].z; acc[r][3] = ext[r].w;
+        }
+        if (j + 1 < ch.r1) {
+#pragma unroll
+            for (int r = 0; r < RPT; r++)
+                ext[r] = *reinterpret_cast<const float4 *>(S_ext + idx_of(j + 1) + (RPT * rb + r) * D + col0 + cb);
         }
 #pragma unroll 2
         for (int l = 0; l < D; l += 4) {
@@ -425,6 +442,7 @@ merge_kernel(const MergeChain *__restrict__ chains, const float *__restrict__ S_
             *reinterpret_cast<float4 *>(S_init + idx_of(j + 1) + d * D + col0 + cb) = o;
         }
     }
+    cp_async_wait<0>();
 }
 
 // Zero [H, rows, width] slabs of the listed entries of a [*, H, rows, width] buffer.
@@ -512,12 +530,12 @@ int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S
     dim3 grid((unsigned)p.chains.size(), (unsigned)p.H, (unsigned)(p.dk / MBV));
     cudaError_t e;
     if (p.dk == 64) {
-        const size_t sm = sizeof(float) * (2 * 64 * 68 + 64 * MBV);
+        const size_t sm = sizeof(float) * (MNBUF * 64 * 68 + 64 * MBV);
         e = cudaFuncSetAttribute(merge_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         if (e != cudaSuccess) return (int)e;
         merge_kernel<64><<<grid, NT, sm, st>>>(c->dev.chains, S_ext, M, S_init, p.H, p.B);
     } else {
-        const size_t sm = sizeof(float) * (2 * 128 * 132 + 128 * MBV);
+        const size_t sm = sizeof(float) * (MNBUF * 128 * 132 + 128 * MBV);
         e = cudaFuncSetAttribute(merge_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         if (e != cudaSuccess) return (int)e;
         merge_kernel<128><<<grid, NT, sm, st>>>(c->dev.chains, S_ext, M, S_init, p.H, p.B);

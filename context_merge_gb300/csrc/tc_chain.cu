@@ -652,6 +652,7 @@ __device__ __forceinline__ void run_state(const Run &r) {
                     mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wblo, true);
                 }
                 mma_commit(&r.bar[B_WBFREE]);
+                mma_commit(&r.bar[B_DLFULL]);   // the Delta epilogue need not wait for O1
             }
             if (ok && FWD) {   // -O^T = (-S^T) (gamma ⊙ Q)^T, before S is rewritten after P_S
                 if (ch >= 1) ok = mbar_wait(&r.bar[B_OFREE], (ch - 1) & 1, ctl, st, 66);
@@ -661,7 +662,6 @@ __device__ __forceinline__ void run_state(const Run &r) {
                     mma_tk<64, 128>(tm + TM_O, tm + TM_SB, stg<MODE, ROLE>(d.q0, ch), QATOM, false);
                 }
             }
-            if (ok) mma_commit(&r.bar[B_DLFULL]);
             TR(1, ch, 3);
         }
         bool ok = warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 60);
@@ -913,12 +913,27 @@ int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *
     prm.status = c->dev.status;
     prm.H = p.H;
     prm.scale = p.scale;
-    // the S chains and the transfer-matrix chains, one kernel each
-    int rc = launch_chain<MODE_PRE, ROLE_S>(tk, tk, tv, prm, (unsigned)p.pre_items.size(), (unsigned)p.H,
-                                            (cudaStream_t)stream);
+    // the S chains and the transfer-matrix chains, one kernel each; the M
+    // chains run on the context's second stream (forked from and joined back
+    // into the caller's), so each kernel's last wave overlaps the other's
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaStream_t aux = (cudaStream_t)c->aux_stream;
+    if (aux) {
+        cudaError_t e = cudaEventRecord((cudaEvent_t)c->ev_fork, st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(aux, (cudaEvent_t)c->ev_fork, 0);
+        if (e != cudaSuccess) return (int)e;
+    }
+    int rc = launch_chain<MODE_PRE, ROLE_M>(tk, tk, tv, prm, (unsigned)p.pre_items.size(), (unsigned)p.H,
+                                            aux ? aux : st);
     if (rc) return rc;
-    return launch_chain<MODE_PRE, ROLE_M>(tk, tk, tv, prm, (unsigned)p.pre_items.size(), (unsigned)p.H,
-                                          (cudaStream_t)stream);
+    rc = launch_chain<MODE_PRE, ROLE_S>(tk, tk, tv, prm, (unsigned)p.pre_items.size(), (unsigned)p.H, st);
+    if (rc) return rc;
+    if (aux) {
+        cudaError_t e = cudaEventRecord((cudaEvent_t)c->ev_join, aux);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, (cudaEvent_t)c->ev_join, 0);
+        if (e != cudaSuccess) return (int)e;
+    }
+    return 0;
 }
 
 int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const float *g, const void *wy,

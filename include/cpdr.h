@@ -38,8 +38,13 @@
  *          kept at fp32 accuracy ([FLA-CP] §2.2).
  * Memory.  Every tensor argument is a DEVICE pointer owned by the caller, and
  *          must be 16-byte aligned.  The library owns only the cpdr_ctx
- *          (host tables plus small device metadata allocated at create).
+ *          (host tables plus small device metadata allocated at create, and
+ *          on the tensor-core path one internal stream and two events).
  *          No call below allocates device memory.
+ * Streams. cpdr_preprocess forks its M-chain kernel onto the context's
+ *          internal stream and joins it back into `stream` before returning
+ *          (event record / wait), so ordering on `stream` is as if it ran
+ *          there; a context must not be used from two host threads at once.
  * Streams. `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *          stream).  Calls enqueue work and return; they never synchronise.
  * Errors.  Every call validates its arguments on the host before any
