@@ -603,7 +603,10 @@ __device__ __forceinline__ void run_state(const Run &r) {
     const int row = 32 * q + lane;                       // TMEM lane: value dim (or M column)
     const uint32_t tm = r.tmem;
     const uint32_t lane_base = tm + ((uint32_t)(32 * q) << 16);
-    const bool issuer = (w == 8 && lane == 0);
+    // the forward's products are issued by lane 0 of warp 8; in the
+    // pre-process by warp 2, which joins the state warps' named barrier
+    const bool issuer = FWD && (w == 8 && lane == 0);
+    constexpr int kBarThreads = FWD ? 256 : 288;
     const int H = p.H;
     int32_t *st = p.status;
     Ctl *ctl = r.ctl;
@@ -634,7 +637,7 @@ __device__ __forceinline__ void run_state(const Run &r) {
         S[i] = x;
     }
     put_state();
-    int bad = named_bar_or(kStateBar, 256, 0);
+    int bad = named_bar_or(kStateBar, kBarThreads, 0);
     for (int ch = 0; ch < r.n && !bad; ch++) {
         // ---- Delta (and O) products of chunk ch
         if (issuer) {
@@ -694,7 +697,7 @@ __device__ __forceinline__ void run_state(const Run &r) {
             if (HAS_U && lane == 0) mbar_arrive(&r.bar[B_DLREADY]);   // the U product may reuse the columns
         }
         if (w == 8) TR(3, ch, 2);
-        if ((bad = named_bar_or(kStateBar, 256, ok ? 0 : 1))) break;
+        if ((bad = named_bar_or(kStateBar, kBarThreads, ok ? 0 : 1))) break;
         // ---- P_S (and the masked output product) of chunk ch
         if (issuer) {
             tc_fence_after();
@@ -733,7 +736,7 @@ __device__ __forceinline__ void run_state(const Run &r) {
             put_state();
         }
         if (w == 8) TR(3, ch, 4);
-        bad = named_bar_or(kStateBar, 256, (ok && !ctl->abort) ? 0 : 1);
+        bad = named_bar_or(kStateBar, kBarThreads, (ok && !ctl->abort) ? 0 : 1);
     }
     // drain every MMA the issuer issued
     if (issuer) {
@@ -754,6 +757,64 @@ __device__ __forceinline__ void run_state(const Run &r) {
         float *dst = SPLIT ? p.M : p.S_ext;
 #pragma unroll
         for (int i = 0; i < 64; i++) dst[sidx + (int64_t)(64 * half + i) * D + row] = S[i];
+    }
+}
+
+// Pre-process issuer (warp 2): issues the chain's Delta and P_S products
+// right after the state warps meet at their named barrier, which it joins.
+template <int MODE, int ROLE>
+__device__ __forceinline__ void run_issuer(const Run &r) {
+    constexpr Lay L = make_lay(MODE, ROLE);
+    constexpr bool SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
+    constexpr bool HAS_U = ROLE == ROLE_S;
+    constexpr int NS = (int)L.nstage;
+    const bool lead = (threadIdx.x & 31) == 0;
+    const uint32_t tm = r.tmem;
+    int32_t *st = r.p->status;
+    Ctl *ctl = r.ctl;
+    const Descs d = make_descs<MODE, ROLE>(r);
+    int bad = named_bar_or(kStateBar, 288, 0);   // the initial state is in place
+    for (int ch = 0; ch < r.n && !bad; ch++) {
+        int ok = 1;
+        if (lead) {
+            ok = mbar_wait(&r.bar[B_WREADY], ch & 1, ctl, st, 64) ? 1 : 0;
+            if (ok && HAS_U) ok = mbar_wait(&r.bar[B_UFULL], ch & 1, ctl, st, 65) ? 1 : 0;
+            if (ok) {
+                tc_fence_after();
+                TR(1, ch, 2);
+                // Delta^T (+)= (-S^T) W^T
+                if (!SPLIT) {
+                    mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wb, HAS_U);
+                } else {
+                    mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wb, false);
+                    mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB_LO, d.wb, true);
+                    mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wblo, true);
+                }
+                mma_commit(&r.bar[B_WBFREE]);
+                mma_commit(&r.bar[B_DLFULL]);
+            }
+            TR(1, ch, 3);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        // the state warps' Delta epilogue
+        if ((bad = named_bar_or(kStateBar, 288, ok ? 0 : 1))) break;
+        if (lead) {
+            tc_fence_after();
+            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kmn0, ch), false);
+            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg<MODE, ROLE>(d.kmn0, ch), true);
+            mma_commit(&r.bar[B_PSFULL]);
+            mma_commit(&r.bar[B_EMPTY0 + ch % NS]);   // this thread's reads of stage ch
+            TR(1, ch, 4);
+        }
+        __syncwarp();
+        // the state warps' S update
+        bad = named_bar_or(kStateBar, 288, ctl->abort ? 1 : 0);
+    }
+    if (lead) {
+        mma_commit(&r.bar[B_DRAIN2]);
+        Ctl local;
+        local.abort = 0;
+        mbar_wait(&r.bar[B_DRAIN2], 0, &local, st, 69);
     }
 }
 
@@ -810,7 +871,10 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     r.tmem = *tmem_slot;
     if (w == 0) run_producer<MODE, ROLE>(r, tq, tk, tv);
     else if (w == 1) run_mma<MODE, ROLE>(r);
-    else if (w < 4) { if (MODE == MODE_FWD) run_mask<MODE, ROLE>(r); }
+    else if (w < 4) {
+        if (MODE == MODE_FWD) run_mask<MODE, ROLE>(r);
+        else if (w == 2) run_issuer<MODE, ROLE>(r);
+    }
     else if (w < 8) run_wepi<MODE, ROLE>(r);
     else run_state<MODE, ROLE>(r);
     tc_fence_before();
