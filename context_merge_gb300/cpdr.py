@@ -26,7 +26,8 @@ FRAG_CONT_PREV, FRAG_CONT_NEXT, FRAG_ENDS_SEQ = 1, 2, 4
 EXPORTED = ["cpdr_ctx_create", "cpdr_ctx_destroy", "cpdr_buffer_sizes", "cpdr_plan_num_fragments",
             "cpdr_plan_fragments", "cpdr_plan_counts", "cpdr_wy_bytes", "cpdr_wy_build", "cpdr_preprocess",
             "cpdr_merge", "cpdr_fwd", "cpdr_host_workspace_bytes",
-            "cpdr_forward_host", "cpdr_forward_noalloc", "cpdr_check_device_status", "cpdr_last_error", "cpdr_version"]
+            "cpdr_forward_host", "cpdr_forward_noalloc", "cpdr_check_device_status", "cpdr_selftest_wait_timeout",
+            "cpdr_last_error", "cpdr_version"]
 
 
 class CpdrError(RuntimeError):
@@ -78,6 +79,7 @@ def load():
         lib.cpdr_forward_host.argtypes = [vp] * 9 + [sz, vp]
         lib.cpdr_forward_noalloc.argtypes = [vp] * 9
         lib.cpdr_check_device_status.argtypes = [vp, vp]
+        lib.cpdr_selftest_wait_timeout.argtypes = [vp, ctypes.c_longlong, vp]
         for name in EXPORTED:
             f = getattr(lib, name)
             if name not in ("cpdr_ctx_destroy", "cpdr_last_error", "cpdr_version"):
@@ -255,3 +257,7 @@ class Context:
 
     def check_device_status(self, stream=None):
         _check(self._lib.cpdr_check_device_status(self._h, _stream(stream)))
+
+    def selftest_wait_timeout(self, max_cycles=20_000_000, stream=None):
+        """Make one bounded device wait give up on purpose (see include/cpdr.h)."""
+        _check(self._lib.cpdr_selftest_wait_timeout(self._h, ctypes.c_longlong(int(max_cycles)), _stream(stream)))

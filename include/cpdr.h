@@ -247,6 +247,18 @@ cpdr_status cpdr_forward_noalloc(const cpdr_ctx *ctx, const void *q, const void 
  */
 cpdr_status cpdr_check_device_status(const cpdr_ctx *ctx, void *stream);
 
+/*
+ * Self-test of the bounded-wait failure path (no counterpart in the article):
+ * launches one warp that waits, for at most `max_cycles` SM clock cycles
+ * (0 < max_cycles <= 4e9, about 2 s at the maximum clock), on an mbarrier
+ * phase that nothing completes, then records code 1 at site 99 in the
+ * context's device status word and returns -- what every bounded wait of the
+ * library does when it gives up.  cpdr_check_device_status then reports
+ * CPDR_ERR_TIMEOUT and clears the word; the context stays usable.  No fault,
+ * trap or unbounded wait is involved.
+ */
+cpdr_status cpdr_selftest_wait_timeout(const cpdr_ctx *ctx, long long max_cycles, void *stream);
+
 /* Thread-local message for the last non-OK status of this thread. */
 const char *cpdr_last_error(void);
 

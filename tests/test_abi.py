@@ -89,3 +89,10 @@ def test_wy_workspace_covers_every_chunk_of_every_fragment(cpdr_lib, kw):
     simt = make(**kw, force_simt=True)
     assert simt.wy_bytes() == 0
     assert make(**dict(kw, dtype="fp32")).wy_bytes() == 0
+
+
+def test_selftest_rejects_host_only_context(cpdr_lib):
+    ctx = make()
+    rc = cpdr_lib.cpdr_selftest_wait_timeout(ctx._h, ctypes.c_longlong(1000), None)
+    assert rc == cpdr.ERR_INVALID
+    assert b"HOST_ONLY" in cpdr_lib.cpdr_last_error()
