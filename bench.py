@@ -160,10 +160,11 @@ def stage_bytes(w, ctx, inp):
     """Algorithmic HBM bytes per launch of each stage (each tensor element
     read or written once)."""
     es = 4 if w.dtype == "fp32" else 2
-    H, d = inp["H"], inp["d"]
+    H, d, Hq = inp["H"], inp["d"], inp["Hq"]
     frags = ctx.fragments()
     gate_w = d if w.gate == "kda" else 1
-    tok_bytes_fwd = H * (3 * d * es + es + gate_w * 4 + d * es)      # q, k, v, beta, g in; o out
+    # q in and o out per query head; k, v, beta, g in per state head
+    tok_bytes_fwd = Hq * 2 * d * es + H * (2 * d * es + es + gate_w * 4)
     tok_bytes_pre = H * (2 * d * es + es + gate_w * 4)               # k, v, beta, g in
     state = H * d * d * 4
     pre_tok = sum(f[1] for f in frags if f[4] & 2)
@@ -200,19 +201,35 @@ def traffic_record(kernel_tag):
         return None
 
 
+def variant_keys(w, inp):
+    """Config keys of a layout variant (absent for the default layout)."""
+    out = {}
+    if w.layout != "contiguous":
+        out["layout"] = w.layout
+    if w.Hq:
+        out["Hq"] = w.Hq if inp is None else inp["Hq"]
+    if w.state_v_first:
+        out["state_v_first"] = True
+    return out
+
+
 # ---------------------------------------------------------------- CPU oracle
 def cpu_oracle_sample(inp_dev, w, heads):
     """Time the fp64 oracle (as it stands) on the first `heads` heads of the
     workload; returns (seconds, head-tokens processed, threads)."""
     import oracle
+    from oracle import layout
     hs = min(heads, inp_dev["H"])
+    G = inp_dev["Hq"] // inp_dev["H"]
     sub = {}
     for key in ("q", "k", "v", "beta", "g"):
-        sub[key] = inp_dev[key][:, :, :hs].contiguous().cpu()
+        x = inp_dev[key][:, :, :hs * G if key == "q" else hs].contiguous().cpu()
+        # the device tensors are in memory order; the oracle takes sequence order
+        sub[key] = layout.from_zigzag(x, w.R) if w.layout == "zigzag" else x
     P = oracle.Problem(sub["q"], sub["k"], sub["v"], sub["beta"], sub["g"], cu_seqlens=inp_dev["cu_seqlens"])
     threads = oracle.default_threads()
     t0 = time.perf_counter()
-    P.segmented(w.R, nthreads=threads)
+    P.segmented(2 * w.R if w.layout == "zigzag" else w.R, nthreads=threads)
     dt = time.perf_counter() - t0
     return dt, inp_dev["B"] * inp_dev["T"] * hs, threads
 
@@ -236,8 +253,8 @@ def run_reference(args, ws, rank):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": inp["B"], "T": inp["T"], "H": w.H, "d": w.d, "R": w.R,
-                       "gate": w.gate, "in_dtype": w.dtype},
+            "config": dict({"workload": w.name, "B": inp["B"], "T": inp["T"], "H": w.H, "d": w.d, "R": w.R,
+                            "gate": w.gate, "in_dtype": w.dtype}, **variant_keys(w, None)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"fp64 segmented oracle on {hs} of {w.H} heads per step, full T; "
                                        f"tokens scaled by heads sampled / heads"},
@@ -253,9 +270,9 @@ def run_ours(args, ws, rank, local):
     inp = inputs.make_inputs(w, device=dev, seed=w.seed + 1000 * rank, T=args.T, H=args.H)
     B, T, H, d, R = inp["B"], inp["T"], inp["H"], inp["d"], inp["R"]
     ctx = cpdr.Context(B, T, H, d, R, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"],
-                       force_simt=args.force_simt)
+                       force_simt=args.force_simt, layout=w.layout, Hq=inp["Hq"], state_v_first=w.state_v_first)
     bufs = ctx.alloc_buffers(dev)
-    o = torch.empty_like(inp["v"])
+    o = torch.empty((B, T, inp["Hq"], d), dtype=inp["v"].dtype, device=dev)
     q, k, v, beta, g = (inp[x] for x in ("q", "k", "v", "beta", "g"))
     stream = torch.cuda.current_stream()
 
@@ -368,9 +385,10 @@ def run_ours(args, ws, rank, local):
         "warmup": max(3, args.warmup), "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": B, "T": T, "H": H, "d": d, "R": R, "gate": w.gate,
-                   "in_dtype": w.dtype, "parallelism": f"replicas{ws}",
-                   "l2": "inputs larger than L2 (no flush)" if tokens * H * d * 2 > 256e6 else "inputs fit L2"},
+        "config": dict({"workload": w.name, "B": B, "T": T, "H": H, "d": d, "R": R, "gate": w.gate,
+                        "in_dtype": w.dtype, "parallelism": f"replicas{ws}",
+                        "l2": "inputs larger than L2 (no flush)" if tokens * H * d * 2 > 256e6 else "inputs fit L2"},
+                       **variant_keys(w, inp)),
         "stage_ms": mean_ms,
         "roofline": roof,
         "cpu_baseline": cpu,

@@ -21,6 +21,8 @@ LIB_PATH = os.path.join(_HERE, "libcpdr.so")
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = range(6)
 FLAG_HOST_ONLY = 1 << 0
 FLAG_FORCE_SIMT = 1 << 1
+FLAG_LAYOUT_ZIGZAG = 1 << 2
+FLAG_STATE_V_FIRST = 1 << 3
 FRAG_CONT_PREV, FRAG_CONT_NEXT, FRAG_ENDS_SEQ = 1, 2, 4
 
 EXPORTED = ["cpdr_ctx_create", "cpdr_ctx_destroy", "cpdr_buffer_sizes", "cpdr_plan_num_fragments",
@@ -40,7 +42,8 @@ class Desc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
                 ("R", ctypes.c_int32), ("num_seqs", ctypes.c_int32), ("T", ctypes.c_int64),
                 ("cu_seqlens_host", ctypes.POINTER(ctypes.c_int64)), ("gate_kind", ctypes.c_int32),
-                ("in_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32), ("scale", ctypes.c_float)]
+                ("in_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32), ("scale", ctypes.c_float),
+                ("Hq", ctypes.c_int32)]
 
 
 class Fragment(ctypes.Structure):
@@ -111,12 +114,23 @@ class Context:
     ``gate`` is "gdn" (scalar gate g [B,T,H]) or "kda" (per-dim gk [B,T,H,d]);
     ``dtype`` is "fp32" or "bf16" for q, k, v, beta and o; gates are fp32.
     With ``cu_seqlens`` (N+1 offsets) the batch is packed: B must be 1.
+    ``layout="zigzag"`` takes the token axis in the zigzag order of R ranks
+    (2R parts, rank r holding parts r and 2R-1-r); ``Hq`` (a multiple of H)
+    gives q and o grouped query heads; ``state_v_first`` stores the dk x dv
+    states S_ext, S_init and final_state as [.., dv, dk].
     """
 
     def __init__(self, B, T, H, d, R, gate="gdn", dtype="bf16", cu_seqlens=None, scale=1.0,
-                 host_only=False, force_simt=False):
+                 host_only=False, force_simt=False, layout="contiguous", Hq=None, state_v_first=False):
         lib = load()
+        if layout not in ("contiguous", "zigzag"):
+            raise ValueError(f"layout must be 'contiguous' or 'zigzag', got {layout!r}")
         self.B, self.T, self.H, self.d, self.R = int(B), int(T), int(H), int(d), int(R)
+        self.layout = layout
+        # segments of the exchange buffers: the ranks, or 2R zigzag pieces
+        self.pieces = 2 * self.R if layout == "zigzag" else self.R
+        self.Hq = self.H if Hq is None else int(Hq)
+        self.state_v_first = bool(state_v_first)
         self.gate, self.dtype = gate, dtype
         self.torch_dtype = torch.float32 if dtype == "fp32" else torch.bfloat16
         self._cu = None
@@ -128,9 +142,11 @@ class Context:
             cu_ptr = ctypes.cast(self._cu, ctypes.POINTER(ctypes.c_int64))
             n = len(cu) - 1
         self.N = n
-        flags = (FLAG_HOST_ONLY if host_only else 0) | (FLAG_FORCE_SIMT if force_simt else 0)
+        flags = ((FLAG_HOST_ONLY if host_only else 0) | (FLAG_FORCE_SIMT if force_simt else 0) |
+                 (FLAG_LAYOUT_ZIGZAG if layout == "zigzag" else 0) |
+                 (FLAG_STATE_V_FIRST if self.state_v_first else 0))
         desc = Desc(self.B, self.H, self.d, self.d, self.R, n, self.T, cu_ptr,
-                    0 if gate == "gdn" else 1, 0 if dtype == "fp32" else 1, flags, float(scale))
+                    0 if gate == "gdn" else 1, 0 if dtype == "fp32" else 1, flags, float(scale), self.Hq)
         h = ctypes.c_void_p()
         _check(lib.cpdr_ctx_create(ctypes.byref(desc), ctypes.byref(h)))
         self._h = h
@@ -177,8 +193,11 @@ class Context:
 
     def alloc_buffers(self, device="cuda"):
         """Caller-owned exchange buffers S_ext, M, S_init and final_state (fp32)
-        and the WY tile workspace ``wy`` (bytes; None when not needed)."""
-        d, R, B, H, N = self.d, self.R, self.B, self.H, self.N
+        and the WY tile workspace ``wy`` (bytes; None when not needed).  The
+        segment axis has one entry per segment (2R in the zigzag layout); the
+        last two axes of the states are (dk, dv), or (dv, dk) with
+        ``state_v_first``."""
+        d, R, B, H, N = self.d, self.pieces, self.B, self.H, self.N
         f32 = torch.float32
         nwy = self.wy_bytes()
         return dict(S_ext=torch.empty((R, B, H, d, d), dtype=f32, device=device),
@@ -189,8 +208,8 @@ class Context:
 
     # ---- the three stages ------------------------------------------------
     def _check_inputs(self, **ts):
-        B, T, H, d = self.B, self.T, self.H, self.d
-        shapes = dict(q=(B, T, H, d), k=(B, T, H, d), v=(B, T, H, d), beta=(B, T, H), o=(B, T, H, d),
+        B, T, H, d, Hq = self.B, self.T, self.H, self.d, self.Hq
+        shapes = dict(q=(B, T, Hq, d), k=(B, T, H, d), v=(B, T, H, d), beta=(B, T, H), o=(B, T, Hq, d),
                       g=(B, T, H) if self.gate == "gdn" else (B, T, H, d))
         for name, t in ts.items():
             if t is None:
@@ -225,7 +244,7 @@ class Context:
         if bufs is None:
             bufs = self.alloc_buffers(q.device)
         if o is None:
-            o = torch.empty_like(v)
+            o = torch.empty((self.B, self.T, self.Hq, self.d), dtype=v.dtype, device=v.device)
         wy = bufs.get("wy")
         self.wy_build(k, beta, g, wy, stream)
         self.preprocess(k, v, beta, g, bufs["S_ext"], bufs["M"], wy=wy, stream=stream)

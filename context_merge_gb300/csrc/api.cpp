@@ -89,18 +89,19 @@ cpdr_status launch_rc(int rc, const char *what) {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Sizes {
-    size_t qk, v, beta, gate, o, sext, m, sinit, fin;
+    size_t q, k, v, beta, gate, o, sext, m, sinit, fin;
 };
 
 Sizes sizes_of(const cpdr::Plan &p) {
     Sizes s;
     const size_t es = p.in_dtype == CPDR_DTYPE_F32 ? 4 : 2;
     const size_t tok = (size_t)p.B * (size_t)p.T;
-    s.qk = tok * p.H * p.dk * es;
+    s.q = tok * p.Hq * p.dk * es;
+    s.k = tok * p.H * p.dk * es;
     s.v = tok * p.H * p.dv * es;
     s.beta = tok * p.H * es;
     s.gate = tok * p.H * (p.gate_kind == CPDR_GATE_PER_DIM ? p.dk : 1) * sizeof(float);
-    s.o = s.v;
+    s.o = tok * p.Hq * p.dv * es;
     s.sext = (size_t)p.R * p.B * p.H * p.dk * p.dv * sizeof(float);
     s.m = (size_t)p.R * p.B * p.H * p.dk * p.dk * sizeof(float);
     s.sinit = s.sext;
@@ -283,7 +284,7 @@ cpdr_status cpdr_fwd(const cpdr_ctx *c, const void *q, const void *k, const void
 cpdr_status cpdr_host_workspace_bytes(const cpdr_ctx *c, size_t *bytes) {
     if (!c || !bytes) return set_err(CPDR_ERR_INVALID, "null argument");
     const Sizes s = sizes_of(c->plan);
-    *bytes = round256(s.qk) * 2 + round256(s.v) + round256(s.beta) + round256(s.gate) + round256(s.o) +
+    *bytes = round256(s.q) + round256(s.k) + round256(s.v) + round256(s.beta) + round256(s.gate) + round256(s.o) +
              round256(s.sext) + round256(s.m) + round256(s.sinit) + round256(s.fin) +
              round256(cpdr::wy_bytes(c));
     return CPDR_OK;
@@ -302,7 +303,7 @@ cpdr_status cpdr_forward_host(const cpdr_ctx *c, const void *q, const void *k, c
     const Sizes s = sizes_of(c->plan);
     char *p = (char *)ws;
     auto take = [&](size_t n) { char *r = p; p += round256(n); return r; };
-    void *dq = take(s.qk), *dk = take(s.qk), *dv = take(s.v), *db = take(s.beta);
+    void *dq = take(s.q), *dk = take(s.k), *dv = take(s.v), *db = take(s.beta);
     float *dg = (float *)take(s.gate);
     void *dout = take(s.o);
     float *dse = (float *)take(s.sext), *dm = (float *)take(s.m), *dsi = (float *)take(s.sinit);
@@ -311,8 +312,8 @@ cpdr_status cpdr_forward_host(const cpdr_ctx *c, const void *q, const void *k, c
     void *dwy = nwy ? take(nwy) : nullptr;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dq, q, s.qk, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k, s.qk, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dq, q, s.q, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k, s.k, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v, s.v, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(db, beta, s.beta, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dg, gate, s.gate, cudaMemcpyHostToDevice, st);

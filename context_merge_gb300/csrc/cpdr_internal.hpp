@@ -35,7 +35,10 @@ constexpr size_t kWyUnitBytes = 3 * kWyTileBytes;
 // Host plan ([FLA-CP] §3.2-§3.3): fragments per segment and the derived
 // work lists.  All token indices are on the flattened [B*T] axis.
 struct Plan {
-    int32_t B = 0, H = 0, dk = 0, dv = 0, R = 0, N = 0;
+    int32_t B = 0, H = 0, dk = 0, dv = 0, N = 0;
+    int32_t Hq = 0, G = 1;   // query heads of q and o, and query heads per state (Hq = G H)
+    bool vfirst = false;     // dk x dv state buffers stored [dv, dk]
+    int32_t R = 0;           // segments per row: the ranks, or 2 x ranks (zigzag pieces)
     int64_t T = 0;           // tokens per row (or packed total)
     int64_t L = 0;           // segment length
     int32_t gate_kind = 0, in_dtype = 0;

@@ -2,7 +2,8 @@
 // lists every local fragment with its role in the segmented scheme.
 //
 // Follows the article "flash-linear-attention 上下文并行CP ..." ([FLA-CP]):
-//   §3.2  contiguous layout: segment r holds tokens [r*T/R, (r+1)*T/R)
+//   §3.2  contiguous layout: segment r holds tokens [r*T/R, (r+1)*T/R);
+//         zigzag layout: 2R equal parts, rank r holding parts r and 2R-1-r
 //   §3.3  total tokens must be >= R and divisible by R (ValueError there,
 //         CPDR_ERR_INVALID here); sequences intersecting a segment are found
 //         by a sorted search over the global cu_seqlens and truncated to it
@@ -30,16 +31,27 @@ cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err) {
         return fail(err, CPDR_ERR_INVALID, "in_dtype must be CPDR_DTYPE_F32 or CPDR_DTYPE_BF16");
     if (d.dk != d.dv || (d.dk != 64 && d.dk != 128))
         return fail(err, CPDR_ERR_UNSUPPORTED, "only dk == dv in {64, 128} is implemented");
-    if (d.T % d.R != 0 || d.T < d.R)
+    if (d.Hq != 0 && (d.Hq < d.H || d.Hq % d.H != 0))
+        return fail(err, CPDR_ERR_INVALID, "Hq must be 0, H, or a multiple of H (grouped query heads)");
+    // zigzag placement ([FLA-CP] §3.2): 2R pieces, rank r holding pieces r and
+    // 2R-1-r; on one GPU every piece is a segment of its own, in sequence order
+    const bool zigzag = (d.flags & CPDR_FLAG_LAYOUT_ZIGZAG) != 0;
+    const int64_t pieces = zigzag ? 2 * (int64_t)d.R : d.R;
+    if (pieces > INT32_MAX / 2) return fail(err, CPDR_ERR_INVALID, "R too large");
+    if (d.T % pieces != 0 || d.T < pieces)
         return fail(err, CPDR_ERR_INVALID,
-                    "tokens per row (or packed total) must be >= R and divisible by R");
+                    zigzag ? "tokens per row (or packed total) must be >= 2R and divisible by 2R (zigzag layout)"
+                           : "tokens per row (or packed total) must be >= R and divisible by R");
     if (d.T > (int64_t)INT32_MAX * kChunk)
         return fail(err, CPDR_ERR_INVALID, "too many tokens");
 
     p = Plan();
-    p.B = d.B; p.H = d.H; p.dk = d.dk; p.dv = d.dv; p.R = d.R; p.T = d.T;
+    p.B = d.B; p.H = d.H; p.dk = d.dk; p.dv = d.dv; p.R = (int32_t)pieces; p.T = d.T;
     p.gate_kind = d.gate_kind; p.in_dtype = d.in_dtype; p.flags = d.flags; p.scale = d.scale;
-    p.L = d.T / d.R;
+    p.L = d.T / pieces;
+    p.Hq = d.Hq ? d.Hq : d.H;
+    p.G = p.Hq / p.H;
+    p.vfirst = (d.flags & CPDR_FLAG_STATE_V_FIRST) != 0;
     if (p.L > INT32_MAX) return fail(err, CPDR_ERR_INVALID, "segment length exceeds 2^31-1");
 
     if (d.cu_seqlens_host) {
@@ -61,8 +73,16 @@ cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err) {
     }
 
     // Fragments: for row b and segment r, intersect [base + r L, base + (r+1) L)
-    // with the sequences.  Fixed-length rows are one sequence each.
+    // with the sequences.  Fixed-length rows are one sequence each.  Segments
+    // and sequences live in sequence coordinates; tok0 is where a fragment's
+    // tokens are in memory: the same place in the contiguous layout, and in
+    // the zigzag layout part r sits at slot 2r (r < R) or 2(2R-1-r)+1 of its
+    // row, rank by rank, each rank's [front; back]
     const int64_t L = p.L;
+    auto mem_slot = [&](int r) -> int64_t {
+        if (!zigzag) return r;
+        return r < d.R ? 2 * (int64_t)r : 2 * (int64_t)(2 * d.R - 1 - r) + 1;
+    };
     std::vector<int32_t> first_frag_of_seg(p.nseg(), -1), last_frag_of_seg(p.nseg(), -1);
     for (int b = 0; b < p.B; b++) {
         const int64_t base = p.packed ? 0 : (int64_t)b * p.T;
@@ -75,7 +95,7 @@ cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err) {
                 const int64_t a = std::max(p.cu[n], s0), e = std::min(p.cu[n + 1], s1);
                 if (e <= a) continue;  // zero-length sequence
                 cpdr_fragment f;
-                f.tok0 = a;
+                f.tok0 = base + mem_slot(r) * L + (a - s0);
                 f.len = (int32_t)(e - a);
                 f.seg = seg;
                 f.seq = n;

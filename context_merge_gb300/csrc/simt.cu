@@ -36,6 +36,13 @@ __device__ __forceinline__ float ldf(const __nv_bfloat16 *p, int64_t i) { return
 __device__ __forceinline__ void stf(float *p, int64_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void stf(__nv_bfloat16 *p, int64_t i, float x) { p[i] = __float2bfloat16_rn(x); }
 
+// Offset of state element (key dim d, value dim c) inside one D x D state:
+// [dk][dv] by default, [dv][dk] in the state_v_first layout.
+template <int D>
+__device__ __forceinline__ int64_t st_off(int d, int c, bool vfirst) {
+    return vfirst ? (int64_t)c * D + d : (int64_t)d * D + c;
+}
+
 // Shared-memory layout of one chunk (row strides padded by one float).
 template <int D>
 struct Smem {
@@ -63,7 +70,7 @@ constexpr size_t smem_bytes() { return sizeof(Smem<D>); }
 // Load one chunk (rows >= n zero-filled) and build the gate factors.
 template <typename TIn, int D, bool PERDIM>
 __device__ void load_chunk(Smem<D> &s, const TIn *q, const TIn *k, const TIn *beta, const float *g,
-                           int64_t tok0, int n, int H, int h) {
+                           int64_t tok0, int n, int H, int h, int Hq, int hq) {
     constexpr int LD = Smem<D>::LD;
     const int tid = threadIdx.x;
     for (int idx = tid; idx < C * D; idx += NT) {
@@ -72,7 +79,7 @@ __device__ void load_chunk(Smem<D> &s, const TIn *q, const TIn *k, const TIn *be
         if (i < n) {
             const int64_t off = ((tok0 + i) * H + h) * (int64_t)D + d;
             kv = ldf(k, off);
-            if (q) qv = ldf(q, off);
+            if (q) qv = ldf(q, ((tok0 + i) * Hq + hq) * (int64_t)D + d);
             if (PERDIM) gv = g[off] * kLog2e;
         }
         s.Ki[i * LD + d] = kv;
@@ -207,7 +214,7 @@ __device__ void delta_step(Smem<D> &s) {
 
 // O = scale [(gamma ⊙ Q) S + (QK ⊙ Lambda) Delta], stored for valid rows
 template <typename TIn, int D, bool PERDIM>
-__device__ void output_step(Smem<D> &s, TIn *o, int64_t tok0, int n, int H, int h, int vcol0,
+__device__ void output_step(Smem<D> &s, TIn *o, int64_t tok0, int n, int Hq, int hq, int vcol0,
                             float scale) {
     constexpr int LD = Smem<D>::LD, LA = Smem<D>::LA, LB = Smem<D>::LB;
     const int c = threadIdx.x % BV, ib = threadIdx.x / BV;
@@ -224,7 +231,7 @@ __device__ void output_step(Smem<D> &s, TIn *o, int64_t tok0, int n, int H, int 
         const int i = ib * 8 + r;
         float x = PERDIM ? acc[r] : acc[r] * exp2f(s.g1[i]);
         for (int j = 0; j <= i; j++) x = fmaf(s.QK[i * LA + j], s.Dl[j * LB + c], x);
-        if (i < n) stf(o, ((tok0 + i) * H + h) * (int64_t)D + vcol0 + c, scale * x);
+        if (i < n) stf(o, ((tok0 + i) * Hq + hq) * (int64_t)D + vcol0 + c, scale * x);
     }
 }
 
@@ -235,11 +242,12 @@ __device__ void state_step(Smem<D> &s, int n) {
     const int c = threadIdx.x % BV, db = threadIdx.x / BV;   // 8 blocks of D/8 rows
     constexpr int RPT = D / 8;
     const float gC = PERDIM ? 0.f : s.g1[C - 1];
-    float acc[RPT];
+    float acc[RPT], cf[RPT];   // KDA: cf = 2^(G_C,d - G_ref,d), independent of the token
 #pragma unroll
     for (int r = 0; r < RPT; r++) {
         const int d = db * RPT + r;
         acc[r] = s.S[d * LB + c] * exp2f(PERDIM ? s.gC[d] : gC);
+        cf[r] = PERDIM ? exp2f(s.gC[d] - s.gref[d]) : 0.f;
     }
     for (int j = 0; j < C; j++) {
         const float dl = s.Dl[j * LB + c];
@@ -248,7 +256,7 @@ __device__ void state_step(Smem<D> &s, int n) {
         for (int r = 0; r < RPT; r++) {
             const int d = db * RPT + r;
             // KDA: Gamma_jd k_jd = Kj_jd * 2^(G_C,d - G_ref,d)
-            const float kg = PERDIM ? s.Kj[j * LD + d] * exp2f(s.gC[d] - s.gref[d]) : s.Ki[j * LD + d] * gam;
+            const float kg = PERDIM ? s.Kj[j * LD + d] * cf[r] : s.Ki[j * LD + d] * gam;
             acc[r] = fmaf(kg, dl, acc[r]);
         }
     }
@@ -258,49 +266,50 @@ __device__ void state_step(Smem<D> &s, int n) {
     (void)n;
 }
 
-// Forward: grid (fragments in fwd_order, H, dv / BV).
+// Forward: grid (fragments in fwd_order, Hq, dv / BV).  Query head hq runs
+// the chain of state head h = hq / G (grouped query heads recompute it); the
+// group's first query head writes the final state.
 template <typename TIn, int D, bool PERDIM>
 __global__ void __launch_bounds__(NT, 1)
 simt_fwd_kernel(const cpdr_fragment *__restrict__ frags, const int32_t *__restrict__ order,
                 const TIn *__restrict__ q, const TIn *__restrict__ k, const TIn *__restrict__ v,
                 const TIn *__restrict__ beta, const float *__restrict__ g,
                 const float *__restrict__ S_init, TIn *__restrict__ o, float *__restrict__ final_state,
-                int H, int B, float scale) {
+                int H, int G, bool vfirst, float scale) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem<D> &s = *reinterpret_cast<Smem<D> *>(smem_raw);
     constexpr int LB = Smem<D>::LB;
     const cpdr_fragment f = frags[order[blockIdx.x]];
-    const int h = blockIdx.y, vcol0 = blockIdx.z * BV;
-    // initial state
+    const int hq = blockIdx.y, h = hq / G, vcol0 = blockIdx.z * BV;
+    // initial state (vfirst: consecutive threads walk the key dim, contiguous there)
     for (int idx = threadIdx.x; idx < D * BV; idx += NT) {
-        const int d = idx / BV, c = idx % BV;
+        const int d = vfirst ? idx % D : idx / BV, c = vfirst ? idx / D : idx % BV;
         float x = 0.f;
         if (f.flags & CPDR_FRAG_CONT_PREV)
-            x = S_init[(((int64_t)f.seg * H + h) * D + d) * D + vcol0 + c];
+            x = S_init[((int64_t)f.seg * H + h) * D * D + st_off<D>(d, vcol0 + c, vfirst)];
         s.S[d * LB + c] = x;
     }
     for (int c0 = 0; c0 < f.len; c0 += C) {
         const int n = min(C, f.len - c0);
         const int64_t t0 = f.tok0 + c0;
         __syncthreads();
-        load_chunk<TIn, D, PERDIM>(s, q, k, beta, g, t0, n, H, h);
+        load_chunk<TIn, D, PERDIM>(s, q, k, beta, g, t0, n, H, h, H * G, hq);
         build_A_QK<D, PERDIM, true>(s);
         __syncthreads();
         solve_WU<TIn, D, PERDIM>(s, v, t0, n, H, h, vcol0, false);
         __syncthreads();
         delta_step<D>(s);
         __syncthreads();
-        output_step<TIn, D, PERDIM>(s, o, t0, n, H, h, vcol0, scale);
+        output_step<TIn, D, PERDIM>(s, o, t0, n, H * G, hq, vcol0, scale);
         state_step<D, PERDIM>(s, n);
     }
     __syncthreads();
-    if ((f.flags & CPDR_FRAG_ENDS_SEQ) && final_state) {
+    if ((f.flags & CPDR_FRAG_ENDS_SEQ) && final_state && hq % G == 0) {
         for (int idx = threadIdx.x; idx < D * BV; idx += NT) {
-            const int d = idx / BV, c = idx % BV;
-            final_state[(((int64_t)f.seq * H + h) * D + d) * D + vcol0 + c] = s.S[d * LB + c];
+            const int d = vfirst ? idx % D : idx / BV, c = vfirst ? idx / D : idx % BV;
+            final_state[((int64_t)f.seq * H + h) * D * D + st_off<D>(d, vcol0 + c, vfirst)] = s.S[d * LB + c];
         }
     }
-    (void)B;
 }
 
 // Pre-process: grid (pre items, H, 2 D / BV); column tiles < D/BV are S
@@ -309,7 +318,8 @@ template <typename TIn, int D, bool PERDIM>
 __global__ void __launch_bounds__(NT, 1)
 simt_pre_kernel(const cpdr_fragment *__restrict__ frags, const int32_t *__restrict__ items,
                 const TIn *__restrict__ k, const TIn *__restrict__ v, const TIn *__restrict__ beta,
-                const float *__restrict__ g, float *__restrict__ S_ext, float *__restrict__ M, int H) {
+                const float *__restrict__ g, float *__restrict__ S_ext, float *__restrict__ M, int H,
+                bool vfirst) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem<D> &s = *reinterpret_cast<Smem<D> *>(smem_raw);
     constexpr int LB = Smem<D>::LB;
@@ -325,7 +335,7 @@ simt_pre_kernel(const cpdr_fragment *__restrict__ frags, const int32_t *__restri
         const int n = min(C, f.len - c0);
         const int64_t t0 = f.tok0 + c0;
         __syncthreads();
-        load_chunk<TIn, D, PERDIM>(s, nullptr, k, beta, g, t0, n, H, h);
+        load_chunk<TIn, D, PERDIM>(s, nullptr, k, beta, g, t0, n, H, h, H, h);
         build_A_QK<D, PERDIM, false>(s);
         __syncthreads();
         solve_WU<TIn, D, PERDIM>(s, v, t0, n, H, h, col0, mcols);
@@ -335,10 +345,12 @@ simt_pre_kernel(const cpdr_fragment *__restrict__ frags, const int32_t *__restri
         state_step<D, PERDIM>(s, n);
     }
     __syncthreads();
+    // M keeps [dk][dk]; S_ext follows the state layout
     float *dst = mcols ? M : S_ext;
+    const bool vf = vfirst && !mcols;
     for (int idx = threadIdx.x; idx < D * BV; idx += NT) {
-        const int d = idx / BV, c = idx % BV;
-        dst[(((int64_t)f.seg * H + h) * D + d) * D + col0 + c] = s.S[d * LB + c];
+        const int d = vf ? idx % D : idx / BV, c = vf ? idx / D : idx % BV;
+        dst[((int64_t)f.seg * H + h) * D * D + st_off<D>(d, col0 + c, vf)] = s.S[d * LB + c];
     }
 }
 
@@ -360,7 +372,9 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int D>
+// VF: S_ext and S_init in the state_v_first layout [dv][dk]; the tile stays
+// (key dim x value dim) in shared memory and only the global accesses turn.
+template <int D, bool VF>
 __global__ void __launch_bounds__(NT, 1)
 merge_kernel(const MergeChain *__restrict__ chains, const float *__restrict__ S_ext,
              const float *__restrict__ M, float *__restrict__ S_init, int H, int B) {
@@ -385,20 +399,29 @@ merge_kernel(const MergeChain *__restrict__ chains, const float *__restrict__ S_
         cp_async_commit();
     };
     for (int idx = threadIdx.x; idx < D * MBV; idx += NT) {
-        const int d = idx / MBV, c = idx % MBV;
-        const float x = S_ext[idx_of(ch.r0) + d * D + col0 + c];
+        const int d = VF ? idx % D : idx / MBV, c = VF ? idx / D : idx % MBV;
+        const int64_t off = st_off<D>(d, col0 + c, VF);
+        const float x = S_ext[idx_of(ch.r0) + off];
         Ss[d * MBV + c] = x;
-        S_init[idx_of(ch.r0 + 1) + d * D + col0 + c] = x;
+        S_init[idx_of(ch.r0 + 1) + off] = x;
     }
 #pragma unroll
     for (int k = 1; k < MNBUF; k++) stage_M(ch.r0 + k);
     const int rb = threadIdx.x >> 2, cb = (threadIdx.x & 3) * 4;
     float4 ext[RPT];   // S_ext tile of the current step, loaded one step ahead
-    if (ch.r0 + 1 < ch.r1) {
+    auto load_ext = [&](int j) {
 #pragma unroll
-        for (int r = 0; r < RPT; r++)
-            ext[r] = *reinterpret_cast<const float4 *>(S_ext + idx_of(ch.r0 + 1) + (RPT * rb + r) * D + col0 + cb);
-    }
+        for (int r = 0; r < RPT; r++) {
+            const float *src = S_ext + idx_of(j);
+            const int d = RPT * rb + r;
+            if (VF)
+                ext[r] = make_float4(src[st_off<D>(d, col0 + cb, true)], src[st_off<D>(d, col0 + cb + 1, true)],
+                                     src[st_off<D>(d, col0 + cb + 2, true)], src[st_off<D>(d, col0 + cb + 3, true)]);
+            else
+                ext[r] = *reinterpret_cast<const float4 *>(src + d * D + col0 + cb);
+        }
+    };
+    if (ch.r0 + 1 < ch.r1) load_ext(ch.r0 + 1);
     for (int j = ch.r0 + 1; j < ch.r1; j++) {
         const int buf = (j - ch.r0 - 1) % MNBUF;
         cp_async_wait<MNBUF - 2>();
@@ -410,11 +433,7 @@ merge_kernel(const MergeChain *__restrict__ chains, const float *__restrict__ S_
         for (int r = 0; r < RPT; r++) {
             acc[r][0] = ext[r].x; acc[r][1] = ext[r].y; acc[r][2] = ext[r].z; acc[r][3] = ext[r].w;
         }
-        if (j + 1 < ch.r1) {
-#pragma unroll
-            for (int r = 0; r < RPT; r++)
-                ext[r] = *reinterpret_cast<const float4 *>(S_ext + idx_of(j + 1) + (RPT * rb + r) * D + col0 + cb);
-        }
+        if (j + 1 < ch.r1) load_ext(j + 1);
 #pragma unroll 2
         for (int l = 0; l < D; l += 4) {
             float4 sv[4];
@@ -439,7 +458,15 @@ merge_kernel(const MergeChain *__restrict__ chains, const float *__restrict__ S_
             const int d = RPT * rb + r;
             const float4 o = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
             *reinterpret_cast<float4 *>(Ss + d * MBV + cb) = o;
-            *reinterpret_cast<float4 *>(S_init + idx_of(j + 1) + d * D + col0 + cb) = o;
+            float *dst = S_init + idx_of(j + 1);
+            if (VF) {
+                dst[st_off<D>(d, col0 + cb, true)] = o.x;
+                dst[st_off<D>(d, col0 + cb + 1, true)] = o.y;
+                dst[st_off<D>(d, col0 + cb + 2, true)] = o.z;
+                dst[st_off<D>(d, col0 + cb + 3, true)] = o.w;
+            } else {
+                *reinterpret_cast<float4 *>(dst + d * D + col0 + cb) = o;
+            }
         }
     }
     cp_async_wait<0>();
@@ -463,10 +490,10 @@ int launch_fwd_t(const cpdr_ctx *c, const void *q, const void *k, const void *v,
     const size_t sm = smem_bytes<D>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid((unsigned)p.frags.size(), (unsigned)p.H, (unsigned)(D / BV));
+    dim3 grid((unsigned)p.frags.size(), (unsigned)p.Hq, (unsigned)(D / BV));
     kern<<<grid, NT, sm, st>>>(c->dev.frags, c->dev.fwd_order, (const TIn *)q, (const TIn *)k,
-                               (const TIn *)v, (const TIn *)beta, g, S_init, (TIn *)o, fs, p.H, p.B,
-                               p.scale);
+                               (const TIn *)v, (const TIn *)beta, g, S_init, (TIn *)o, fs, p.H, p.G,
+                               p.vfirst, p.scale);
     return (int)cudaGetLastError();
 }
 
@@ -481,7 +508,7 @@ int launch_pre_t(const cpdr_ctx *c, const void *k, const void *v, const void *be
     if (e != cudaSuccess) return (int)e;
     dim3 grid((unsigned)p.pre_items.size(), (unsigned)p.H, (unsigned)(2 * D / BV));
     kern<<<grid, NT, sm, st>>>(c->dev.frags, c->dev.pre_items, (const TIn *)k, (const TIn *)v,
-                               (const TIn *)beta, g, S_ext, M, p.H);
+                               (const TIn *)beta, g, S_ext, M, p.H, p.vfirst);
     return (int)cudaGetLastError();
 }
 
@@ -523,24 +550,26 @@ int launch_simt_pre(const cpdr_ctx *c, const void *k, const void *v, const void 
                       : dispatch_gate_pre<__nv_bfloat16, 128>(c, k, v, beta, g, S_ext, M, st);
 }
 
+template <int D, bool VF>
+int launch_merge_t(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init, cudaStream_t st) {
+    const auto &p = c->plan;
+    dim3 grid((unsigned)p.chains.size(), (unsigned)p.H, (unsigned)(D / MBV));
+    const size_t sm = sizeof(float) * (MNBUF * D * (D + 4) + D * MBV);
+    cudaError_t e = cudaFuncSetAttribute(merge_kernel<D, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return (int)e;
+    merge_kernel<D, VF><<<grid, NT, sm, st>>>(c->dev.chains, S_ext, M, S_init, p.H, p.B);
+    return (int)cudaGetLastError();
+}
+
 int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init, void *stream) {
     cudaStream_t st = (cudaStream_t)stream;
     const auto &p = c->plan;
     if (p.chains.empty()) return 0;
-    dim3 grid((unsigned)p.chains.size(), (unsigned)p.H, (unsigned)(p.dk / MBV));
-    cudaError_t e;
-    if (p.dk == 64) {
-        const size_t sm = sizeof(float) * (MNBUF * 64 * 68 + 64 * MBV);
-        e = cudaFuncSetAttribute(merge_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (e != cudaSuccess) return (int)e;
-        merge_kernel<64><<<grid, NT, sm, st>>>(c->dev.chains, S_ext, M, S_init, p.H, p.B);
-    } else {
-        const size_t sm = sizeof(float) * (MNBUF * 128 * 132 + 128 * MBV);
-        e = cudaFuncSetAttribute(merge_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (e != cudaSuccess) return (int)e;
-        merge_kernel<128><<<grid, NT, sm, st>>>(c->dev.chains, S_ext, M, S_init, p.H, p.B);
-    }
-    return (int)cudaGetLastError();
+    if (p.dk == 64)
+        return p.vfirst ? launch_merge_t<64, true>(c, S_ext, M, S_init, st)
+                        : launch_merge_t<64, false>(c, S_ext, M, S_init, st);
+    return p.vfirst ? launch_merge_t<128, true>(c, S_ext, M, S_init, st)
+                    : launch_merge_t<128, false>(c, S_ext, M, S_init, st);
 }
 
 int launches_per_step(const cpdr_ctx *c) {

@@ -99,6 +99,8 @@ struct Params {
     float *M;
     int32_t *status;
     int H;
+    int Hq, G;                // query heads of q and o, query heads per state (Hq = G H)
+    int vfirst;               // dk x dv states stored [dv][dk]
     float scale;
 };
 
@@ -157,6 +159,7 @@ struct Run {
     Ctl *ctl;
     uint32_t tmem;
     int n, nlast, h, chunk0;
+    int hq;                   // query head (forward; == h without grouped query heads)
     int64_t tok0;
     int seg, seq, flags;
     const Params *p;
@@ -279,8 +282,8 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
             tma_load_3d(st + L.kc0, tk, fb, 0, r.h, tok);
             tma_load_3d(st + L.kc1, tk, fb, 64, r.h, tok);
             if (MODE == MODE_FWD) {
-                tma_load_3d(st + L.qc0, tq, fb, 0, r.h, tok);
-                tma_load_3d(st + L.qc1, tq, fb, 64, r.h, tok);
+                tma_load_3d(st + L.qc0, tq, fb, 0, r.hq, tok);
+                tma_load_3d(st + L.qc1, tq, fb, 64, r.hq, tok);
             }
             if (MODE == MODE_FWD || ROLE == ROLE_S) {
                 tma_load_3d(st + L.vc0, tv, fb, 0, r.h, tok);
@@ -548,8 +551,8 @@ __device__ __forceinline__ void run_wepi(const Run &r) {
             if (w == 4) TR(2, t, 3);
             tc_fence_after();
             const int nv = rows_of(r, t);
-            const int64_t ostride = (int64_t)p.H * D;
-            __nv_bfloat16 *op = p.o + ((r.tok0 + (int64_t)t * C) * p.H + r.h) * D + row;
+            const int64_t ostride = (int64_t)p.Hq * D;
+            __nv_bfloat16 *op = p.o + ((r.tok0 + (int64_t)t * C) * p.Hq + r.hq) * D + row;
             const float sc = -p.scale;   // the accumulator holds -O^T
             float a[32], b[32];
             tmem_ld32(lane_base + TM_O, a);
@@ -633,7 +636,8 @@ __device__ __forceinline__ void run_state(const Run &r) {
         const int dk = 64 * half + i;
         float x = 0.f;
         if (SPLIT) x = (dk == row) ? 1.f : 0.f;
-        else if (FWD && (r.flags & CPDR_FRAG_CONT_PREV)) x = p.S_init[sidx + (int64_t)dk * D + row];
+        else if (FWD && (r.flags & CPDR_FRAG_CONT_PREV))
+            x = p.S_init[sidx + (p.vfirst ? (int64_t)row * D + dk : (int64_t)dk * D + row)];
         S[i] = x;
     }
     put_state();
@@ -748,11 +752,22 @@ __device__ __forceinline__ void run_state(const Run &r) {
     if (bad) return;
     // outputs of the chain
     if (FWD) {
-        if ((r.flags & CPDR_FRAG_ENDS_SEQ) && p.final_state) {
+        // the first query head of a group writes the state's final value
+        if ((r.flags & CPDR_FRAG_ENDS_SEQ) && p.final_state && r.hq % p.G == 0) {
             const int64_t fidx = ((int64_t)r.seq * H + r.h) * D * D;
+            if (p.vfirst) {   // [dv][dk]: this thread's row is contiguous
+                float4 *dst = reinterpret_cast<float4 *>(p.final_state + fidx + (int64_t)row * D + 64 * half);
 #pragma unroll
-            for (int i = 0; i < 64; i++) p.final_state[fidx + (int64_t)(64 * half + i) * D + row] = S[i];
+                for (int i = 0; i < 16; i++) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; i++) p.final_state[fidx + (int64_t)(64 * half + i) * D + row] = S[i];
+            }
         }
+    } else if (!SPLIT && p.vfirst) {   // S_ext [dv][dk]
+        float4 *dst = reinterpret_cast<float4 *>(p.S_ext + sidx + (int64_t)row * D + 64 * half);
+#pragma unroll
+        for (int i = 0; i < 16; i++) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
     } else {
         float *dst = SPLIT ? p.M : p.S_ext;
 #pragma unroll
@@ -835,7 +850,8 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     r.seg = f.seg;
     r.seq = f.seq;
     r.flags = f.flags;
-    r.h = blockIdx.y;
+    r.hq = blockIdx.y;
+    r.h = r.hq / p.G;
     r.n = (f.len + C - 1) / C;
     r.nlast = f.len - (r.n - 1) * C;
     r.chunk0 = p.chunk0[fi];
@@ -976,6 +992,9 @@ int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *
     prm.M = M;
     prm.status = c->dev.status;
     prm.H = p.H;
+    prm.Hq = p.H;
+    prm.G = 1;
+    prm.vfirst = p.vfirst;
     prm.scale = p.scale;
     // the S chains and the transfer-matrix chains, one kernel each; the M
     // chains run on the context's second stream (forked from and joined back
@@ -1006,7 +1025,7 @@ int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v
     if (p.frags.empty()) return 0;
     CUtensorMap tq, tk, tv;
     const int64_t tokens = (int64_t)p.B * p.T;
-    if (!make_tmap(&tq, q, tokens, p.H) || !make_tmap(&tk, k, tokens, p.H) || !make_tmap(&tv, v, tokens, p.H))
+    if (!make_tmap(&tq, q, tokens, p.Hq) || !make_tmap(&tk, k, tokens, p.H) || !make_tmap(&tv, v, tokens, p.H))
         return (int)cudaErrorInvalidValue;
     Params prm{};
     prm.frags = c->dev.frags;
@@ -1019,8 +1038,13 @@ int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v
     prm.final_state = final_state;
     prm.status = c->dev.status;
     prm.H = p.H;
+    prm.Hq = p.Hq;
+    prm.G = p.G;
+    prm.vfirst = p.vfirst;
     prm.scale = p.scale;
-    return launch_chain<MODE_FWD, ROLE_S>(tq, tk, tv, prm, (unsigned)p.frags.size(), (unsigned)p.H,
+    // one chain per (fragment, query head): grouped query heads each run
+    // their state head's chain
+    return launch_chain<MODE_FWD, ROLE_S>(tq, tk, tv, prm, (unsigned)p.frags.size(), (unsigned)p.Hq,
                                           (cudaStream_t)stream);
 }
 

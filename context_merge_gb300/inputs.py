@@ -16,7 +16,9 @@ CP2/CP4/CP8 cut patterns; no dataset is involved anywhere):
   KDA (per key dim) alpha = sigmoid(N(mu, s)) per (token, head, dim);
   "slow" alpha = 1 - 1e-3 u, u ~ U(0, 1) (the merge-sensitive workload).
 * Draw order: (varlen lengths,) q, k, v, beta, gate -- from one generator
-  seeded with ``seed`` (default 1000 + workload index).
+  seeded with ``seed`` (default 1000 + workload index).  With grouped query
+  heads q is drawn with Hq heads.  Tokens are drawn i.i.d., so a draw serves
+  as sequence-ordered input or, unchanged, as zigzag-ordered memory alike.
 """
 from __future__ import annotations
 
@@ -44,6 +46,9 @@ class Workload:
     len_range: tuple = (1024, 12288)
     lengths: Optional[tuple] = None  # explicit packed lengths (overrides the draw)
     seed: int = 0
+    Hq: int = 0                # > 0: query heads of q and o (grouped query heads, a multiple of H)
+    layout: str = "contiguous"  # token layout: "contiguous" or "zigzag"
+    state_v_first: bool = False  # dk x dv states stored [dv, dk]
 
     @property
     def torch_dtype(self):
@@ -72,6 +77,19 @@ WORKLOADS = {
     "merge_bf16_t16384_h4_d128_r16": Workload("merge_bf16_t16384_h4_d128_r16", "gdn", "bf16", 1, 16384, 4, 128,
                                               16, gate_dist=("slow",), beta_dist=(-3.0, 1.0), seed=1006),
 }
+# layout variants of the headline shape: zigzag token order, [dv, dk]
+# states, and two query heads per state head
+WORKLOADS.update({
+    "gdn_bf16_t262144_h16_d128_r64_zigzag": Workload("gdn_bf16_t262144_h16_d128_r64_zigzag", "gdn", "bf16", 1,
+                                                     262144, 16, 128, 64, gate_dist=("sigmoid", 4.0, 0.5),
+                                                     seed=1004, layout="zigzag"),
+    "gdn_bf16_t262144_h16_d128_r64_vfirst": Workload("gdn_bf16_t262144_h16_d128_r64_vfirst", "gdn", "bf16", 1,
+                                                     262144, 16, 128, 64, gate_dist=("sigmoid", 4.0, 0.5),
+                                                     seed=1004, state_v_first=True),
+    "gdn_bf16_t262144_h16_hq32_d128_r64": Workload("gdn_bf16_t262144_h16_hq32_d128_r64", "gdn", "bf16", 1,
+                                                   262144, 16, 128, 64, gate_dist=("sigmoid", 4.0, 0.5),
+                                                   seed=1004, Hq=32),
+})
 WORKLOAD_ORDER = list(WORKLOADS)[:5]
 HEADLINE = "gdn_bf16_t262144_h16_d128_r64"
 
@@ -112,7 +130,8 @@ def _gate(w: Workload, shape, gen, device):
 
 
 def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None, T: Optional[int] = None,
-                B: Optional[int] = None, H: Optional[int] = None, lengths: Optional[Sequence[int]] = None):
+                B: Optional[int] = None, H: Optional[int] = None, lengths: Optional[Sequence[int]] = None,
+                Hq: Optional[int] = None):
     """Draw one batch for workload ``w`` (optionally with shapes overridden).
 
     Returns a dict with q, k, v, beta (input dtype), g (fp32), cu_seqlens
@@ -122,6 +141,8 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None, T: Option
     B = w.B if B is None else B
     T = w.T if T is None else T
     H = w.H if H is None else H
+    if Hq is None:   # keep the workload's query heads per state head
+        Hq = H * (w.Hq // w.H) if w.Hq else H
     d = w.d
     cu = None
     if lengths is None and w.lengths is not None:
@@ -138,7 +159,7 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None, T: Option
         x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
         return (x / x.norm(dim=-1, keepdim=True)).to(dt)
 
-    q = unit((B, T, H, d))
+    q = unit((B, T, Hq, d))
     k = unit((B, T, H, d))
     v = torch.randn((B, T, H, d), generator=gen, device=device, dtype=torch.float32).to(dt)
     mb, sb = w.beta_dist
@@ -147,4 +168,4 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None, T: Option
     gshape = (B, T, H) if w.gate == "gdn" else (B, T, H, d)
     g = _gate(w, gshape, gen, device)
     return dict(q=q, k=k, v=v, beta=beta, g=g, cu_seqlens=cu, B=B, T=T, H=H, d=d, R=w.R,
-                gate=w.gate, dtype=w.dtype)
+                gate=w.gate, dtype=w.dtype, Hq=Hq, layout=w.layout, state_v_first=w.state_v_first)

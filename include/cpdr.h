@@ -23,7 +23,9 @@
  *
  * Conventions shared by every entry point
  * ----------------------------------------
- * Layout.  q, k: [B, T, H, dk]; v, o: [B, T, H, dv]; beta: [B, T, H];
+ * Layout.  q: [B, T, Hq, dk]; k: [B, T, H, dk]; v: [B, T, H, dv];
+ *          o: [B, T, Hq, dv] (Hq == H unless desc.Hq asks for grouped query
+ *          heads); beta: [B, T, H];
  *          gate: [B, T, H] (scalar, GDN) or [B, T, H, dk] (per key dim, KDA),
  *          all contiguous, row-major.  Packed variable-length batches use
  *          B == 1 and global cu_seqlens ([FLA-CP] §3.1, §4 NOTE).
@@ -31,7 +33,10 @@
  *          (entry (r, b, h) belongs to segment r of row b; the layout of the
  *          gathered buffer of [FLA-CP] §2.4 with world_size = R);
  *          final_state: [N, H, dk, dv] fp32 ([N, HV, K, V] of the KDA
- *          initial_state description in hyper-parallel issue #7).
+ *          initial_state description in hyper-parallel issue #7).  With
+ *          CPDR_FLAG_STATE_V_FIRST the dk x dv states are [.., dv, dk]; with
+ *          CPDR_FLAG_LAYOUT_ZIGZAG the token axis is in zigzag order and the
+ *          segment axis has 2R entries.
  * Types.   q, k, v, beta, o share the input dtype (fp32 or bf16); gates are
  *          fp32 natural-log gates g = log(alpha).  Arithmetic is fp32 or
  *          bf16 tensor-core products with fp32 accumulation; the M chain is
@@ -74,6 +79,18 @@ typedef enum {
 /* desc.flags */
 #define CPDR_FLAG_HOST_ONLY   (1u << 0)  /* plan only: no device tables; launch calls are rejected */
 #define CPDR_FLAG_FORCE_SIMT  (1u << 1)  /* use the fp32 CUDA-core kernels even where tensor cores apply */
+/* Zigzag token layout ([FLA-CP] §3.2).  Each row (or the packed batch) is cut
+ * into 2R equal parts; virtual rank r holds part r followed by part 2R-1-r, and
+ * the tensors q, k, v, beta, gate and o hold the R ranks' [front; back] inputs
+ * side by side, rank 0 first (for R = 2: parts 0, 3, 1, 2 in memory).
+ * cu_seqlens stays in sequence order.  Every part is a segment of its own, so
+ * the exchange buffers have 2R entries, indexed by part in sequence order, and
+ * the cut rule becomes "tokens >= 2R and divisible by 2R". */
+#define CPDR_FLAG_LAYOUT_ZIGZAG (1u << 2)
+/* state_v_first ([FLA-CP] §5.1; [N, HV, V, K] of hyper-parallel issue #7):
+ * every dk x dv state buffer -- S_ext, S_init and final_state -- is stored
+ * transposed, [.., dv, dk].  M keeps its [.., dk, dk] layout. */
+#define CPDR_FLAG_STATE_V_FIRST (1u << 3)
 
 /* desc.gate_kind */
 #define CPDR_GATE_SCALAR  0   /* GDN: g [B, T, H] */
@@ -85,7 +102,8 @@ typedef enum {
 
 typedef struct {
     int32_t B, H, dk, dv;   /* batch rows, heads, key dim, value dim */
-    int32_t R;              /* number of contiguous segments (virtual context ranks) */
+    int32_t R;              /* virtual context ranks: R contiguous segments per row (or 2R
+                               zigzag pieces, see CPDR_FLAG_LAYOUT_ZIGZAG) */
     int32_t num_seqs;       /* N: sequences (== B without cu_seqlens) */
     int64_t T;              /* tokens per row, or total tokens when packed */
     const int64_t *cu_seqlens_host; /* NULL: B rows of T tokens; else N+1 global offsets
@@ -94,13 +112,17 @@ typedef struct {
     int32_t in_dtype;       /* CPDR_DTYPE_* */
     uint32_t flags;         /* CPDR_FLAG_* */
     float scale;            /* output scale */
+    int32_t Hq;             /* query heads of q and o (GQA, [FLA-CP] §5.1): 0 or H for none,
+                               else a multiple G*H; q head hq reads the state of head hq / G,
+                               while k, v, beta, gate and every state keep H heads */
 } cpdr_desc;
 
 typedef struct cpdr_ctx cpdr_ctx;
 
 /* One local fragment: the intersection of a segment with a sequence. */
 typedef struct {
-    int64_t tok0;    /* first token on the flattened [B*T] token axis */
+    int64_t tok0;    /* first token on the flattened [B*T] token axis, where it is in
+                        memory (zigzag layout: its memory position, not its sequence position) */
     int32_t len;     /* tokens (>= 1) */
     int32_t seg;     /* segment buffer index r*B + b */
     int32_t seq;     /* sequence index */

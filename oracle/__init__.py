@@ -51,7 +51,7 @@ class _Problem(ctypes.Structure):
                 ("dv", ctypes.c_int32), ("T", ctypes.c_int64),
                 ("cu_seqlens", ctypes.POINTER(ctypes.c_int64)), ("num_seqs", ctypes.c_int32),
                 ("gate_kind", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
-                ("order", ctypes.c_int32), ("scale", ctypes.c_double)]
+                ("order", ctypes.c_int32), ("scale", ctypes.c_double), ("Hq", ctypes.c_int32)]
 
 
 def _load():
@@ -101,9 +101,12 @@ def default_threads() -> int:
 class Problem:
     """Shapes and options shared by every oracle call.
 
-    q, k: [B, T, H, dk]; v: [B, T, H, dv]; beta: [B, T, H]; g: [B, T, H] or
-    [B, T, H, dk] (float32, natural-log gates).  With ``cu_seqlens`` (N+1
-    int64 offsets) the batch is packed: B == 1 and T is the total.
+    q: [B, T, Hq, dk]; k: [B, T, H, dk]; v: [B, T, H, dv]; beta: [B, T, H];
+    g: [B, T, H] or [B, T, H, dk] (float32, natural-log gates).  Hq is H, or
+    a multiple G H of it (grouped query heads, [FLA-CP] §5.1: query head hq
+    reads the state of head hq // G; outputs o are [B, T, Hq, dv]).  With
+    ``cu_seqlens`` (N+1 int64 offsets) the batch is packed: B == 1 and T is
+    the total.
     """
 
     def __init__(self, q, k, v, beta, g, cu_seqlens=None, scale=1.0, order=0):
@@ -117,6 +120,9 @@ class Problem:
         self.g = np.ascontiguousarray(g, dtype=np.float32)
         B, T, H, dk = self.k.shape
         dv = self.v.shape[3]
+        Hq = self.q.shape[2]
+        if self.q.shape[:2] != (B, T) or self.q.shape[3] != dk or Hq % H != 0:
+            raise ValueError("q must be [B, T, Hq, dk] with Hq a multiple of k's H")
         if cu_seqlens is not None:
             cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
             if B != 1 or cu[0] != 0 or cu[-1] != T:
@@ -128,18 +134,19 @@ class Problem:
             n = B
         gate_kind = 0 if self.g.ndim == 3 else 1
         self.B, self.T, self.H, self.dk, self.dv, self.N = B, T, H, dk, dv, n
+        self.Hq = Hq
         self.gate_kind = gate_kind
         self._p = _Problem(B, H, dk, dv, T,
                            self.cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if self.cu is not None else None,
-                           n, gate_kind, dq, order, float(scale))
+                           n, gate_kind, dq, order, float(scale), Hq)
 
     def _ptr(self, a):
         return a.ctypes.data_as(ctypes.c_void_p)
 
     def scan(self, h0=None, nthreads=None):
-        """Serial scan: returns (o [B,T,H,dv] fp64, final states [N,H,dk,dv] fp64)."""
+        """Serial scan: returns (o [B,T,Hq,dv] fp64, final states [N,H,dk,dv] fp64)."""
         lib = _load()
-        o = np.zeros((self.B, self.T, self.H, self.dv), np.float64)
+        o = np.zeros((self.B, self.T, self.Hq, self.dv), np.float64)
         ht = np.zeros((self.N, self.H, self.dk, self.dv), np.float64)
         h0p = None
         if h0 is not None:
@@ -156,7 +163,7 @@ class Problem:
         """[FLA-CP] §2.1 on R contiguous segments.
 
         Returns dict with S_ext [R,B,H,dk,dv], M [R,B,H,dk,dk], S_init
-        [R,B,H,dk,dv], o [B,T,H,dv], ht [N,H,dk,dv] (all fp64).  Raises
+        [R,B,H,dk,dv], o [B,T,Hq,dv], ht [N,H,dk,dv] (all fp64).  Raises
         ValueError when the cut rule of [FLA-CP] §3.3 fails.
         """
         lib = _load()
@@ -164,7 +171,7 @@ class Problem:
         S_ext = np.zeros((R, self.B, self.H, self.dk, self.dv), np.float64)
         M = np.zeros((R, self.B, self.H, self.dk, self.dk), np.float64)
         S_init = np.zeros_like(S_ext)
-        o = np.zeros((self.B, self.T, self.H, self.dv), np.float64)
+        o = np.zeros((self.B, self.T, self.Hq, self.dv), np.float64)
         ht = np.zeros((self.N, self.H, self.dk, self.dv), np.float64)
         rc = lib.oracle_segmented(ctypes.byref(self._p), R, self._ptr(self.q), self._ptr(self.k),
                                   self._ptr(self.v), self._ptr(self.beta), self._ptr(self.g),
@@ -175,8 +182,10 @@ class Problem:
         return dict(S_ext=S_ext, M=M, S_init=S_init, o=o, ht=ht)
 
     def chunked(self, C):
-        """[FLA-CP] §2.2 chunk form from zero state: (o, final states), fp64."""
+        """[FLA-CP] §2.2 chunk form from zero state: (o, final states), fp64 (Hq == H only)."""
         lib = _load()
+        if self.Hq != self.H:
+            raise ValueError("the chunk restatement covers Hq == H only")
         o = np.zeros((self.B, self.T, self.H, self.dv), np.float64)
         ht = np.zeros((self.N, self.H, self.dk, self.dv), np.float64)
         rc = lib.oracle_chunked(ctypes.byref(self._p), int(C), self._ptr(self.q), self._ptr(self.k),

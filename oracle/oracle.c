@@ -59,7 +59,11 @@ typedef struct {
     int32_t in_dtype;             /* 0 fp32, 1 bf16 (q, k, v, beta) */
     int32_t order;                /* 0 pages' order, 1 gate-after-projection */
     double scale;
+    int32_t Hq;                   /* query heads (q and o): a multiple of H; 0 means H */
 } oracle_problem;
+
+/* query heads sharing each state: q head hq reads the state of head hq / G */
+static int q_group(const oracle_problem *P) { return P->Hq > 0 ? P->Hq / P->H : 1; }
 
 /* widen element i of an fp32 / bf16 array to double */
 static double ld_in(const void *p, int64_t i, int dtype) {
@@ -121,7 +125,9 @@ static void run_pool(item_fn fn, void *ctx, int64_t n, int nthreads, size_t scra
  * If with_v == 0 the v_t term is dropped: the update is then the linear
  * map T_t = (I - beta k k^T) Diag(alpha) alone (used to build M, whose
  * columns are states of width dk).  If o != NULL the output rows are
- * written (o is [tokens, H, dv] double, indexed by global token).
+ * written (o is [tokens, Hq, dv] double, indexed by global token): with
+ * grouped query heads (Hq = G H, the GQA mapping of [FLA-CP] §5.1) every
+ * query head hq in [h G, (h+1) G) reads this head's state, o = scale S^T q_hq.
  * width = number of state columns (dv for states, dk for M).
  */
 static void apply_tokens(const oracle_problem *P, const void *q, const void *k, const void *v,
@@ -165,11 +171,15 @@ static void apply_tokens(const oracle_problem *P, const void *q, const void *k, 
                 }
         }
         if (o) {
-            for (int d = 0; d < dk; d++) qq[d] = ld_in(q, th * dk + d, P->in_dtype);
-            for (int c = 0; c < width; c++) {
-                double acc = 0.0;
-                for (int d = 0; d < dk; d++) acc += S[d * width + c] * qq[d];
-                o[th * dv + c] = P->scale * acc;
+            const int G = q_group(P);
+            for (int j = 0; j < G; j++) {
+                const int64_t tq = t * (int64_t)(H * G) + (int64_t)h * G + j;
+                for (int d = 0; d < dk; d++) qq[d] = ld_in(q, tq * dk + d, P->in_dtype);
+                for (int c = 0; c < width; c++) {
+                    double acc = 0.0;
+                    for (int d = 0; d < dk; d++) acc += S[d * width + c] * qq[d];
+                    o[tq * dv + c] = P->scale * acc;
+                }
             }
         }
     }
@@ -203,7 +213,7 @@ static void scan_item(void *vctx, int64_t item, double *scratch) {
     if (c->ht) memcpy(c->ht + ((size_t)n * P->H + h) * sz, S, sz * sizeof(double));
 }
 
-/* o: [B*T, H, dv]; ht: [N, H, dk, dv] (nullable); h0: [N, H, dk, dv] (nullable) */
+/* o: [B*T, Hq, dv]; ht: [N, H, dk, dv] (nullable); h0: [N, H, dk, dv] (nullable) */
 int oracle_scan(const oracle_problem *P, const void *q, const void *k, const void *v,
                 const void *beta, const float *g, const double *h0, double *o, double *ht,
                 int nthreads) {
@@ -345,7 +355,7 @@ static void fwd_item(void *vctx, int64_t item, double *scratch) {
 }
 
 /*
- * S_ext, S_init: [R, B, H, dk, dv]; M: [R, B, H, dk, dk]; o: [B*T, H, dv];
+ * S_ext, S_init: [R, B, H, dk, dv]; M: [R, B, H, dk, dk]; o: [B*T, Hq, dv];
  * ht: [N, H, dk, dv].  Returns 1 when the cut rule of [FLA-CP] §3.3 fails
  * (tokens per row < R or not divisible by R).
  */
@@ -484,11 +494,13 @@ static void chunk_pass(const oracle_problem *P, int C, const void *q, const void
 }
 
 /*
- * Whole sequences in chunk form from zero state (o: [B*T,H,dv], ht: [N,H,dk,dv]).
+ * Whole sequences in chunk form from zero state (o: [B*T,H,dv], ht: [N,H,dk,dv]);
+ * returns 2 for grouped query heads, which it does not cover.
  * Single-threaded: it exists to pin the chunk equations on small inputs.
  */
 int oracle_chunked(const oracle_problem *P, int C, const void *q, const void *k, const void *v,
                    const void *beta, const float *g, double *o, double *ht) {
+    if (q_group(P) != 1) return 2;   /* the chunk restatement covers Hq == H only */
     if (P->order != 0 || C < 1) return 1;
     const size_t sz = (size_t)P->dk * P->dv;
     double *S = (double *)malloc(sizeof(double) * sz);

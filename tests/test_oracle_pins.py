@@ -353,3 +353,87 @@ def test_scale_is_linear():
     a, _ = oracle.Problem(**p, scale=1.0).scan()
     b, _ = oracle.Problem(**p, scale=0.25).scan()
     np.testing.assert_allclose(b, 0.25 * a, rtol=1e-15)
+
+
+# ---- grouped query heads ([FLA-CP] §5.1, GQA: Hq > H) --------------------
+def _gqa_problem(rng, G, T=11, H=2, dk=5, dv=3, gate="gdn", cu=None, B=1):
+    p = rand_problem(rng, B=B, T=T, H=H, dk=dk, dv=dv, gate=gate, cu=cu)
+    q = rng.standard_normal((B, T, H * G, dk)).astype(np.float32)
+    p["q"] = (q / np.linalg.norm(q, axis=-1, keepdims=True)).astype(np.float32)
+    return p
+
+
+@pytest.mark.parametrize("gate", ["gdn", "kda"])
+def test_gqa_brute_force(gate):
+    """Query head hq reads the state of head hq // G: explicit products per head."""
+    G, H = 3, 2
+    rng = np.random.default_rng(21)
+    p = _gqa_problem(rng, G, H=H, gate=gate)
+    o, ht = oracle.Problem(**p).scan()
+    assert o.shape[2] == G * H and ht.shape[1] == H
+    for hq in range(G * H):
+        h = hq // G
+        q2 = np.zeros_like(p["k"])
+        q2[:, :, h] = p["q"][:, :, hq]
+        ob, Sb = brute_force_single(dict(p, q=q2), h, 0, p["k"].shape[1], np.zeros((5, 3)))
+        np.testing.assert_allclose(o[0, :, hq], ob, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(ht[0, h], Sb, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("gate", ["gdn", "kda"])
+def test_gqa_equals_repeated_kv_heads(gate):
+    """Grouping query heads is the same as repeating every other input per group."""
+    G, H, R = 2, 3, 3
+    rng = np.random.default_rng(22)
+    p = _gqa_problem(rng, G, T=24, H=H, dk=6, dv=4, gate=gate, cu=[0, 5, 19, 24])
+    rep = {k: np.repeat(p[k], G, axis=2) for k in ("k", "v", "beta", "g")}
+    full = dict(p, **rep)
+    a = oracle.Problem(**p).segmented(R)
+    b = oracle.Problem(**full).segmented(R)
+    np.testing.assert_array_equal(a["o"], b["o"])
+    for key in ("ht", "S_ext", "M", "S_init"):
+        x = a[key]
+        y = b[key]
+        hax = 1 if key == "ht" else 2
+        np.testing.assert_array_equal(np.repeat(x, G, axis=hax), y)
+
+
+def test_gqa_rejects_bad_grouping():
+    rng = np.random.default_rng(23)
+    p = _gqa_problem(rng, 1, H=2)
+    p["q"] = p["q"][:, :, :1].repeat(3, axis=2)
+    with pytest.raises(ValueError):
+        oracle.Problem(**p)
+
+
+# ---- token layouts ([FLA-CP] §3.2 zigzag) ---------------------------------
+def test_zigzag_worked_example():
+    """W = 2 ranks, 8 tokens: 4 parts of 2; rank 0 holds parts 0 and 3,
+    rank 1 parts 1 and 2, each rank's input being [front; back]."""
+    from oracle import layout
+    np.testing.assert_array_equal(layout.zigzag_positions(8, 2), [0, 1, 6, 7, 2, 3, 4, 5])
+    np.testing.assert_array_equal(layout.zigzag_positions(6, 3), [0, 5, 1, 4, 2, 3])
+    np.testing.assert_array_equal(layout.zigzag_positions(10, 1), np.arange(10))
+
+
+def test_zigzag_is_a_permutation_and_round_trips():
+    from oracle import layout
+    rng = np.random.default_rng(24)
+    for total, W in [(64, 4), (96, 8), (4096, 16)]:
+        pos = layout.zigzag_positions(total, W)
+        assert sorted(pos.tolist()) == list(range(total))
+        P = total // (2 * W)
+        # every part is a run of P consecutive positions
+        assert all((np.diff(pos[i * P:(i + 1) * P]) == 1).all() for i in range(2 * W))
+        x = rng.standard_normal((2, total, 3))
+        z = layout.to_zigzag(x, W)
+        np.testing.assert_array_equal(z[:, np.argsort(pos)], x)
+        np.testing.assert_array_equal(layout.from_zigzag(z, W), x)
+
+
+def test_zigzag_cut_rule():
+    """[FLA-CP] §3.3: zigzag needs total >= 2W and divisible by 2W."""
+    from oracle import layout
+    for total, W in [(6, 4), (10, 2), (3, 1)]:
+        with pytest.raises(ValueError):
+            layout.zigzag_positions(total, W)

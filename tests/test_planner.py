@@ -84,3 +84,78 @@ def test_fixed_rows(cpdr_lib):
             assert f[0] == b * 256 + r * 64 and f[1] == 64 and f[3] == b
             want = (cpdr.FRAG_CONT_PREV if r > 0 else 0) | (cpdr.FRAG_CONT_NEXT if r < 3 else cpdr.FRAG_ENDS_SEQ)
             assert f[4] == want
+
+
+# ---- zigzag layout ([FLA-CP] §3.2) and grouped query heads (§5.1) ---------
+def test_zigzag_worked_example(cpdr_lib):
+    """One 8-token sequence, R = 2 ranks: parts [0,2) [2,4) [4,6) [6,8) sit in
+    memory as rank 0 = [part 0; part 3], rank 1 = [part 1; part 2]."""
+    ctx = cpdr.Context(B=1, T=8, H=1, d=64, R=2, gate="gdn", dtype="bf16", host_only=True, layout="zigzag")
+    P, N, E = cpdr.FRAG_CONT_PREV, cpdr.FRAG_CONT_NEXT, cpdr.FRAG_ENDS_SEQ
+    assert ctx.fragments() == [(0, 2, 0, 0, N), (4, 2, 1, 0, P | N), (6, 2, 2, 0, P | N), (2, 2, 3, 0, P | E)]
+    assert ctx.pieces == 4
+    sext, m, sinit, fin = ctx.buffer_sizes()
+    assert sext == 4 * 1 * 1 * 64 * 64 * 4 and fin == 64 * 64 * 4
+
+
+@pytest.mark.parametrize("lengths,R", [
+    ([3000, 4000, 3240], 2),
+    ([7000, 3240], 4),
+    ([5, 7, 6, 9, 4, 11, 6, 16], 2),
+    ([100, 0, 28], 2),
+    ([4097, 3, 4092], 4),
+    ([65536], 8),
+])
+def test_zigzag_is_the_contiguous_plan_of_2r_parts_moved(cpdr_lib, lengths, R):
+    """Mapped back to sequence positions, the zigzag plan is the contiguous
+    plan of 2R segments, and every fragment is contiguous in memory."""
+    from oracle import layout
+    cu = [0]
+    for x in lengths:
+        cu.append(cu[-1] + x)
+    zz = cpdr.Context(B=1, T=cu[-1], H=1, d=64, R=R, gate="gdn", dtype="bf16", cu_seqlens=cu, host_only=True,
+                      layout="zigzag").fragments()
+    pos = layout.zigzag_positions(cu[-1], R)
+    for tok0, ln, *_ in zz:
+        assert (pos[tok0:tok0 + ln] == pos[tok0] + list(range(ln))).all()
+    seq_order = [(int(pos[f[0]]),) + tuple(f[1:]) for f in zz]
+    assert seq_order == ctx_for(lengths, 2 * R).fragments()
+    check_structure(seq_order, cu, 2 * R)
+
+
+def test_zigzag_fixed_rows(cpdr_lib):
+    from oracle import layout
+    B, T, R = 3, 256, 4
+    zz = cpdr.Context(B=B, T=T, H=1, d=64, R=R, gate="gdn", dtype="fp32", host_only=True,
+                      layout="zigzag").fragments()
+    pos = layout.zigzag_positions(T, R)
+    assert len(zz) == B * 2 * R
+    for tok0, ln, seg, seq, fl in zz:
+        b = tok0 // T
+        r = seg // B
+        assert seq == b and seg == r * B + b and ln == T // (2 * R)
+        assert pos[tok0 - b * T] == r * ln
+
+
+@pytest.mark.parametrize("T,R,ok", [(12, 4, False), (16, 4, True), (6, 4, False), (8, 4, True)])
+def test_zigzag_cut_rule(cpdr_lib, T, R, ok):
+    """[FLA-CP] §3.3: zigzag needs tokens >= 2R and divisible by 2R."""
+    mk = lambda: cpdr.Context(B=1, T=T, H=1, d=64, R=R, gate="gdn", dtype="bf16", host_only=True, layout="zigzag")
+    if ok:
+        mk()
+    else:
+        with pytest.raises(cpdr.CpdrError) as ei:
+            mk()
+        assert ei.value.status == cpdr.ERR_INVALID
+
+
+@pytest.mark.parametrize("H,Hq,ok", [(2, 4, True), (2, 2, True), (4, 12, True), (2, 3, False), (4, 2, False)])
+def test_grouped_query_heads_validation(cpdr_lib, H, Hq, ok):
+    mk = lambda: cpdr.Context(B=1, T=256, H=H, d=64, R=2, gate="gdn", dtype="bf16", host_only=True, Hq=Hq)
+    if ok:
+        sext, m, sinit, fin = mk().buffer_sizes()
+        assert sext == 2 * H * 64 * 64 * 4 and fin == H * 64 * 64 * 4   # states keep H heads
+    else:
+        with pytest.raises(cpdr.CpdrError) as ei:
+            mk()
+        assert ei.value.status == cpdr.ERR_INVALID
