@@ -399,11 +399,136 @@ def run_ours(args, ws, rank, local):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- causal conv1d
+CONV_METRIC = "tokens/sec (causal conv1d, 1 GB300)"
+
+
+def conv_oracle_sample(inp, w, channels=8):
+    """Time the fp64 conv oracle on the first `channels` channels, full T;
+    returns (seconds, token-channels processed)."""
+    from oracle import conv as oconv
+    from oracle import layout
+    x = inp["x"][:, :, :channels].cpu()
+    if w.layout == "zigzag":
+        x = layout.from_zigzag(x, w.R)
+    t0 = time.perf_counter()
+    oconv.causal_conv1d(x, inp["weight"][:channels].cpu(), inp["bias"][:channels].cpu(),
+                        cu_seqlens=inp["cu_seqlens"])
+    return time.perf_counter() - t0, inp["B"] * inp["T"] * channels
+
+
+def conv_config(w, inp, ws):
+    return dict({"workload": w.name, "op": "conv1d", "B": inp["B"], "T": inp["T"], "C": inp["C"],
+                 "W": inp["W"], "R": w.R, "in_dtype": w.dtype, "activation": "silu",
+                 "parallelism": f"replicas{ws}", "l2": "inputs larger than L2 (no flush)"},
+                **variant_keys(w, None))
+
+
+def run_conv_reference(args, ws, rank):
+    w = inputs.WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    inp = inputs.make_conv_inputs(w, device="cpu")
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, tc = conv_oracle_sample(inp, w)
+        if i >= args.warmup:
+            times.append(dt)
+    value = tc / inp["C"] * len(times) / sum(times)
+    line = {"impl": "reference", "metric": CONV_METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": conv_config(w, inp, args.gpus),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"fp64 conv oracle on 8 of {inp['C']} channels per step, full T; "
+                                       f"tokens scaled by channels sampled / channels"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_conv(args, ws, rank):
+    from context_merge_gb300 import cpdr
+    w = inputs.WORKLOADS[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = inputs.make_conv_inputs(w, device=dev, seed=w.seed + 1000 * rank, T=args.T)
+    B, T, C = inp["B"], inp["T"], inp["C"]
+    ctx = cpdr.Context(B, T, 1, 64, w.R, gate="gdn", dtype=w.dtype, cu_seqlens=inp["cu_seqlens"],
+                       layout=w.layout, conv_width=inp["W"])
+    x, weight, bias = inp["x"], inp["weight"], inp["bias"]
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        ctx.conv1d_fwd(x, weight, bias, y, stream=stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler() if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        ctx.conv1d_fwd(x, weight, bias, y, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop() if clocks else None
+    ms = max_over_ranks(start.elapsed_time(end), ws) / args.steps
+    tokens = B * T
+    value = tokens * ws / (ms / 1e3)
+    e2e = None
+    if not args.no_e2e:
+        # host x in (pinned), conv, host y out, all inside the timed region
+        hx = x.cpu().pin_memory()
+        hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        k_e = max(3, min(10, args.steps))
+        barrier(ws)
+        s2 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(k_e):
+            x.copy_(hx, non_blocking=True)
+            ctx.conv1d_fwd(x, weight, bias, y, stream=stream)
+            hy.copy_(y, non_blocking=True)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(s2.elapsed_time(e2), ws)
+        nb = hx.numel() * hx.element_size()
+        e2e = {"value": tokens * ws * k_e / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": nb,
+               "d2h_bytes_per_step": nb, "steps": k_e}
+    if rank != 0:
+        return
+    es = 2 if w.dtype == "bf16" else 4
+    nbytes = 2 * tokens * C * es + C * (inp["W"] + 1) * 4      # x in, y out, weights
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    tag = f"conv1d:{w.name}"
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic_record(tag), "kernel": tag, "peak_source": peak_kind,
+            "algorithmic_bytes_per_launch": nbytes, "ms_per_launch": ms}
+    cpu = None
+    if not args.no_cpu_baseline:
+        dt, tc = conv_oracle_sample(inp, w)
+        cpu = {"value": tc / C / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"fp64 conv oracle on 8 of {C} channels, full T ({dt:.1f} s wall); "
+                         f"tokens scaled by channels sampled / channels"}
+    line = {"metric": CONV_METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": conv_config(w, inp, ws), "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup(args)
+    conv = inputs.WORKLOADS[args.workload].op == "conv1d"
     if args.impl == "reference":
-        run_reference(args, ws, rank)
+        (run_conv_reference if conv else run_reference)(args, ws, rank)
+    elif conv:
+        run_conv(args, ws, rank)
     else:
         run_ours(args, ws, rank, local)
     if ws > 1:

@@ -29,7 +29,7 @@ EXPORTED = ["cpdr_ctx_create", "cpdr_ctx_destroy", "cpdr_buffer_sizes", "cpdr_pl
             "cpdr_plan_fragments", "cpdr_plan_counts", "cpdr_wy_bytes", "cpdr_wy_build", "cpdr_preprocess",
             "cpdr_merge", "cpdr_fwd", "cpdr_host_workspace_bytes",
             "cpdr_forward_host", "cpdr_forward_noalloc", "cpdr_check_device_status", "cpdr_selftest_wait_timeout",
-            "cpdr_last_error", "cpdr_version"]
+            "cpdr_conv1d_fwd", "cpdr_plan_conv_tokens", "cpdr_last_error", "cpdr_version"]
 
 
 class CpdrError(RuntimeError):
@@ -43,7 +43,7 @@ class Desc(ctypes.Structure):
                 ("R", ctypes.c_int32), ("num_seqs", ctypes.c_int32), ("T", ctypes.c_int64),
                 ("cu_seqlens_host", ctypes.POINTER(ctypes.c_int64)), ("gate_kind", ctypes.c_int32),
                 ("in_dtype", ctypes.c_int32), ("flags", ctypes.c_uint32), ("scale", ctypes.c_float),
-                ("Hq", ctypes.c_int32)]
+                ("Hq", ctypes.c_int32), ("conv_width", ctypes.c_int32)]
 
 
 class Fragment(ctypes.Structure):
@@ -79,6 +79,8 @@ def load():
         lib.cpdr_merge.argtypes = [vp] * 5
         lib.cpdr_fwd.argtypes = [vp] * 11
         lib.cpdr_host_workspace_bytes.argtypes = [vp, ctypes.POINTER(sz)]
+        lib.cpdr_conv1d_fwd.argtypes = [vp, vp, vp, vp, ctypes.c_int32, ctypes.c_int32, vp, vp]
+        lib.cpdr_plan_conv_tokens.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]
         lib.cpdr_forward_host.argtypes = [vp] * 9 + [sz, vp]
         lib.cpdr_forward_noalloc.argtypes = [vp] * 9
         lib.cpdr_check_device_status.argtypes = [vp, vp]
@@ -117,11 +119,13 @@ class Context:
     ``layout="zigzag"`` takes the token axis in the zigzag order of R ranks
     (2R parts, rank r holding parts r and 2R-1-r); ``Hq`` (a multiple of H)
     gives q and o grouped query heads; ``state_v_first`` stores the dk x dv
-    states S_ext, S_init and final_state as [.., dv, dk].
+    states S_ext, S_init and final_state as [.., dv, dk].  ``conv_width``
+    (1..8) enables ``conv1d_fwd``, the causal conv1d on the same segments.
     """
 
     def __init__(self, B, T, H, d, R, gate="gdn", dtype="bf16", cu_seqlens=None, scale=1.0,
-                 host_only=False, force_simt=False, layout="contiguous", Hq=None, state_v_first=False):
+                 host_only=False, force_simt=False, layout="contiguous", Hq=None, state_v_first=False,
+                 conv_width=0):
         lib = load()
         if layout not in ("contiguous", "zigzag"):
             raise ValueError(f"layout must be 'contiguous' or 'zigzag', got {layout!r}")
@@ -131,6 +135,7 @@ class Context:
         self.pieces = 2 * self.R if layout == "zigzag" else self.R
         self.Hq = self.H if Hq is None else int(Hq)
         self.state_v_first = bool(state_v_first)
+        self.conv_width = int(conv_width)
         self.gate, self.dtype = gate, dtype
         self.torch_dtype = torch.float32 if dtype == "fp32" else torch.bfloat16
         self._cu = None
@@ -146,7 +151,8 @@ class Context:
                  (FLAG_LAYOUT_ZIGZAG if layout == "zigzag" else 0) |
                  (FLAG_STATE_V_FIRST if self.state_v_first else 0))
         desc = Desc(self.B, self.H, self.d, self.d, self.R, n, self.T, cu_ptr,
-                    0 if gate == "gdn" else 1, 0 if dtype == "fp32" else 1, flags, float(scale), self.Hq)
+                    0 if gate == "gdn" else 1, 0 if dtype == "fp32" else 1, flags, float(scale), self.Hq,
+                    self.conv_width)
         h = ctypes.c_void_p()
         _check(lib.cpdr_ctx_create(ctypes.byref(desc), ctypes.byref(h)))
         self._h = h
@@ -273,6 +279,31 @@ class Context:
         self._check_inputs(q=q, k=k, v=v, beta=beta, g=g, o=o)
         _check(self._lib.cpdr_forward_noalloc(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(o),
                                               _ptr(final_state), _stream(stream)))
+
+    # ---- causal conv1d on the same segments -------------------------------
+    def conv_pre_tokens(self):
+        """pre_num_conv_tokens per segment (entries: segments x rows)."""
+        n = self.pieces * self.B
+        out = (ctypes.c_int32 * n)()
+        _check(self._lib.cpdr_plan_conv_tokens(self._h, out, n))
+        return list(out)
+
+    def conv1d_fwd(self, x, weight, bias, y, activation="silu", stream=None):
+        """y = act(bias + causal depthwise conv of x), x and y [B, T, C] in the
+        context's token order and input dtype; weight [C, W] and bias [C] fp32."""
+        B, T = self.B, self.T
+        if x.dim() != 3 or tuple(x.shape[:2]) != (B, T) or x.dtype != self.torch_dtype or not x.is_contiguous():
+            raise ValueError(f"x must be a contiguous [{B}, {T}, C] {self.torch_dtype} tensor")
+        C = x.shape[2]
+        if tuple(y.shape) != tuple(x.shape) or y.dtype != x.dtype or not y.is_contiguous():
+            raise ValueError("y must match x")
+        if tuple(weight.shape) != (C, self.conv_width) or weight.dtype != torch.float32 or not weight.is_contiguous():
+            raise ValueError(f"weight must be a contiguous [{C}, {self.conv_width}] float32 tensor")
+        if bias is not None and (tuple(bias.shape) != (C,) or bias.dtype != torch.float32):
+            raise ValueError(f"bias must be a [{C}] float32 tensor")
+        act = {"silu": 1, None: 0, "none": 0}[activation]
+        _check(self._lib.cpdr_conv1d_fwd(self._h, _ptr(x), _ptr(weight), _ptr(bias), C, act, _ptr(y),
+                                         _stream(stream)))
 
     def check_device_status(self, stream=None):
         _check(self._lib.cpdr_check_device_status(self._h, _stream(stream)))

@@ -42,6 +42,8 @@ void free_tables(cpdr::DeviceTables &t) {
     cudaFree(t.empty_seqs);
     cudaFree(t.frag_chunk0);
     cudaFree(t.wy_chunks);
+    cudaFree(t.conv_tiles);
+    cudaFree(t.conv_halo);
     cudaFree(t.status);
     t = cpdr::DeviceTables();
 }
@@ -149,6 +151,8 @@ cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
         if (e == cudaSuccess) e = upload(&t.empty_seqs, p.empty_seqs);
         if (e == cudaSuccess) e = upload(&t.frag_chunk0, p.frag_chunk0);
         if (e == cudaSuccess) e = upload(&t.wy_chunks, p.wy_chunks);
+        if (e == cudaSuccess) e = upload(&t.conv_tiles, p.conv_tiles);
+        if (e == cudaSuccess) e = upload(&t.conv_halo, p.conv_halo);
         if (e == cudaSuccess) e = cudaMalloc((void **)&t.status, 64);
         if (e == cudaSuccess) e = cudaMemset(t.status, 0, 64);
         if (e == cudaSuccess && c->use_tc) {
@@ -279,6 +283,34 @@ cpdr_status cpdr_fwd(const cpdr_ctx *c, const void *q, const void *k, const void
     CPDR_TRY(launch_rc(rc, "cpdr_fwd"));
     return launch_rc(cpdr::launch_zero_segments(c, nullptr, nullptr, nullptr, final_state, 2, stream),
                      "cpdr_fwd: zero fill");
+}
+
+cpdr_status cpdr_conv1d_fwd(const cpdr_ctx *c, const void *x, const float *weight, const float *bias,
+                            int32_t channels, int32_t activation, void *y, void *stream) {
+    CPDR_TRY(check_ctx(c));
+    if (c->plan.conv_width < 1)
+        return set_err(CPDR_ERR_INVALID, "cpdr_conv1d_fwd: the context was created without a conv width");
+    if (channels < 1 || channels % 8 != 0)
+        return set_err(CPDR_ERR_INVALID, "cpdr_conv1d_fwd: channels must be a positive multiple of 8");
+    if (activation != 0 && activation != 1)
+        return set_err(CPDR_ERR_INVALID, "cpdr_conv1d_fwd: activation must be 0 (none) or 1 (SiLU)");
+    CPDR_TRY(check_ptr(x, "x"));
+    CPDR_TRY(check_ptr(weight, "weight"));
+    CPDR_TRY(check_ptr(bias, "bias", true));
+    CPDR_TRY(check_ptr(y, "y"));
+    const size_t es = c->plan.in_dtype == CPDR_DTYPE_F32 ? 4 : 2;
+    const size_t nbytes = (size_t)c->plan.B * (size_t)c->plan.T * (size_t)channels * es;
+    const char *xb = (const char *)x, *yb = (const char *)y;
+    if (xb < yb + nbytes && yb < xb + nbytes) return set_err(CPDR_ERR_INVALID, "cpdr_conv1d_fwd: y overlaps x");
+    return launch_rc(cpdr::launch_conv1d(c, x, weight, bias, channels, activation, y, stream), "cpdr_conv1d_fwd");
+}
+
+cpdr_status cpdr_plan_conv_tokens(const cpdr_ctx *c, int32_t *out, int32_t cap) {
+    if (!c || (!out && cap > 0)) return set_err(CPDR_ERR_INVALID, "null argument");
+    if (c->plan.conv_width < 1) return set_err(CPDR_ERR_INVALID, "the context was created without a conv width");
+    const int32_t n = std::min<int32_t>(cap, (int32_t)c->plan.conv_pre_tokens.size());
+    for (int32_t i = 0; i < n; i++) out[i] = c->plan.conv_pre_tokens[i];
+    return CPDR_OK;
 }
 
 cpdr_status cpdr_host_workspace_bytes(const cpdr_ctx *c, size_t *bytes) {

@@ -26,6 +26,19 @@ struct WyChunk {
     int32_t nv, pad;
 };
 
+// Causal-conv1d work unit: up to kConvTile tokens of one fragment (memory
+// positions tok0 .. tok0 + n - 1).  halo says where the conv_width - 1 inputs
+// before tok0 come from: kHaloMemory = the tokens right before tok0 (same
+// fragment), kHaloZero = none (the sequence starts at tok0), k >= 0 = row k
+// of the halo table (memory positions, -1 for positions before the sequence).
+constexpr int kConvTile = 64;
+constexpr int kMaxConvWidth = 8;
+constexpr int32_t kHaloMemory = -2, kHaloZero = -1;
+struct ConvTile {
+    int64_t tok0;
+    int32_t n, halo;
+};
+
 // Bytes of the WY tiles of one (chunk, head): T' = T diag(beta), and
 // T'' = T diag(beta gamma) as a bf16 hi/lo pair, each a 64 x 64 bf16 tile
 // stored as the 128-byte-swizzled shared-memory image the MMA reads.
@@ -56,6 +69,10 @@ struct Plan {
     int32_t max_pre_chunks = 0, max_fwd_chunks = 0;
     std::vector<int32_t> frag_chunk0;        // first global chunk of each fragment (+ total)
     std::vector<WyChunk> wy_chunks;          // every chunk of every fragment
+    int32_t conv_width = 0;                  // causal conv1d kernel size (0: no conv path)
+    std::vector<ConvTile> conv_tiles;        // conv work units, fragment by fragment
+    std::vector<int64_t> conv_halo;          // halo rows, conv_width - 1 memory positions each
+    std::vector<int32_t> conv_pre_tokens;    // per segment: halo tokens inside its first sequence
 
     int32_t nseg() const { return R * B; }
 };
@@ -74,6 +91,8 @@ struct DeviceTables {
     int32_t *empty_seqs = nullptr;
     int32_t *frag_chunk0 = nullptr;
     WyChunk *wy_chunks = nullptr;
+    ConvTile *conv_tiles = nullptr;
+    int64_t *conv_halo = nullptr;
     int32_t *status = nullptr;   // device status word (bounded waits)
 };
 
@@ -120,6 +139,8 @@ int launch_tc_wy(const cpdr_ctx *c, const void *k, const void *beta, const float
                  void *stream);
 int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy,
                   float *S_ext, float *M, void *stream);
+int launch_conv1d(const cpdr_ctx *c, const void *x, const float *weight, const float *bias, int channels,
+                  int activation, void *y, void *stream);
 int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const float *g,
                   const void *wy, const float *S_init, void *o, float *final_state, void *stream);
 

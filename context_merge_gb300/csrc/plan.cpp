@@ -31,6 +31,8 @@ cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err) {
         return fail(err, CPDR_ERR_INVALID, "in_dtype must be CPDR_DTYPE_F32 or CPDR_DTYPE_BF16");
     if (d.dk != d.dv || (d.dk != 64 && d.dk != 128))
         return fail(err, CPDR_ERR_UNSUPPORTED, "only dk == dv in {64, 128} is implemented");
+    if (d.conv_width < 0 || d.conv_width > kMaxConvWidth)
+        return fail(err, CPDR_ERR_UNSUPPORTED, "conv_width must be 0 (no conv path) or 1..8");
     if (d.Hq != 0 && (d.Hq < d.H || d.Hq % d.H != 0))
         return fail(err, CPDR_ERR_INVALID, "Hq must be 0, H, or a multiple of H (grouped query heads)");
     // zigzag placement ([FLA-CP] §3.2): 2R pieces, rank r holding pieces r and
@@ -52,6 +54,7 @@ cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err) {
     p.Hq = d.Hq ? d.Hq : d.H;
     p.G = p.Hq / p.H;
     p.vfirst = (d.flags & CPDR_FLAG_STATE_V_FIRST) != 0;
+    p.conv_width = d.conv_width;
     if (p.L > INT32_MAX) return fail(err, CPDR_ERR_INVALID, "segment length exceeds 2^31-1");
 
     if (d.cu_seqlens_host) {
@@ -84,6 +87,14 @@ cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err) {
         return r < d.R ? 2 * (int64_t)r : 2 * (int64_t)(2 * d.R - 1 - r) + 1;
     };
     std::vector<int32_t> first_frag_of_seg(p.nseg(), -1), last_frag_of_seg(p.nseg(), -1);
+    std::vector<int32_t> frag_halo;   // conv halo row of each fragment (or kHaloZero)
+    const int halo_w = d.conv_width > 0 ? d.conv_width - 1 : 0;
+    if (d.conv_width > 0) p.conv_pre_tokens.assign(p.nseg(), 0);
+    // memory position of sequence position x of row b (base = the row's start)
+    auto mem_of = [&](int64_t base, int64_t x) {
+        const int64_t off = x - base;
+        return base + mem_slot((int)(off / L)) * L + off % L;
+    };
     for (int b = 0; b < p.B; b++) {
         const int64_t base = p.packed ? 0 : (int64_t)b * p.T;
         for (int r = 0; r < p.R; r++) {
@@ -103,6 +114,20 @@ cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err) {
                 if (p.cu[n] < s0) f.flags |= CPDR_FRAG_CONT_PREV;
                 if (p.cu[n + 1] > s1) f.flags |= CPDR_FRAG_CONT_NEXT;
                 else f.flags |= CPDR_FRAG_ENDS_SEQ;
+                // causal conv1d ([FLA-CP] §2.4, §3.3): a segment's first
+                // fragment that continues a sequence reads the conv_width - 1
+                // inputs before it, in sequence order (wherever they are in
+                // memory), down to the sequence start: pre_num_conv_tokens
+                int32_t halo = kHaloZero;
+                if (d.conv_width > 0 && (f.flags & CPDR_FRAG_CONT_PREV)) {
+                    halo = (int32_t)(p.conv_halo.size() / std::max(halo_w, 1));
+                    const int64_t avail = a - p.cu[n];
+                    p.conv_pre_tokens[seg] = (int32_t)std::min<int64_t>(halo_w, avail);
+                    for (int j = halo_w; j >= 1; j--)   // oldest first
+                        p.conv_halo.push_back(j <= avail ? mem_of(base, a - j) : -1);
+                    if (halo_w == 0) halo = kHaloZero;
+                }
+                frag_halo.push_back(halo);
                 if (first_frag_of_seg[seg] < 0) first_frag_of_seg[seg] = (int32_t)p.frags.size();
                 last_frag_of_seg[seg] = (int32_t)p.frags.size();
                 p.frags.push_back(f);
@@ -148,6 +173,14 @@ cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err) {
         acc += chunks(f.len);
     }
     p.frag_chunk0.back() = acc;
+    if (d.conv_width > 0) {
+        for (size_t i = 0; i < p.frags.size(); i++) {
+            const cpdr_fragment &f = p.frags[i];
+            for (int32_t c = 0; c < f.len; c += kConvTile)
+                p.conv_tiles.push_back(ConvTile{f.tok0 + c, std::min(kConvTile, f.len - c),
+                                                c > 0 ? kHaloMemory : frag_halo[i]});
+        }
+    }
     return CPDR_OK;
 }
 

@@ -49,6 +49,9 @@ class Workload:
     Hq: int = 0                # > 0: query heads of q and o (grouped query heads, a multiple of H)
     layout: str = "contiguous"  # token layout: "contiguous" or "zigzag"
     state_v_first: bool = False  # dk x dv states stored [dv, dk]
+    op: str = "delta"          # "delta" (the delta-rule path) or "conv1d" (causal conv1d only)
+    conv_width: int = 0        # conv1d: kernel size W
+    conv_channels: int = 0     # conv1d: channels C of x [B, T, C]
 
     @property
     def torch_dtype(self):
@@ -89,6 +92,11 @@ WORKLOADS.update({
     "gdn_bf16_t262144_h16_hq32_d128_r64": Workload("gdn_bf16_t262144_h16_hq32_d128_r64", "gdn", "bf16", 1,
                                                    262144, 16, 128, 64, gate_dist=("sigmoid", 4.0, 0.5),
                                                    seed=1004, Hq=32),
+})
+# causal conv1d of the q, k, v projections (3 H d channels) at the headline shape
+WORKLOADS.update({
+    "conv_bf16_t262144_c6144_w4_r64": Workload("conv_bf16_t262144_c6144_w4_r64", "gdn", "bf16", 1, 262144, 16,
+                                               128, 64, seed=1010, op="conv1d", conv_width=4, conv_channels=6144),
 })
 WORKLOAD_ORDER = list(WORKLOADS)[:5]
 HEADLINE = "gdn_bf16_t262144_h16_d128_r64"
@@ -169,3 +177,28 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None, T: Option
     g = _gate(w, gshape, gen, device)
     return dict(q=q, k=k, v=v, beta=beta, g=g, cu_seqlens=cu, B=B, T=T, H=H, d=d, R=w.R,
                 gate=w.gate, dtype=w.dtype, Hq=Hq, layout=w.layout, state_v_first=w.state_v_first)
+
+
+def make_conv_inputs(w: Workload, device="cpu", seed: Optional[int] = None, T: Optional[int] = None,
+                     B: Optional[int] = None, C: Optional[int] = None, lengths: Optional[Sequence[int]] = None):
+    """Draw x [B, T, C] ~ N(0, 1) in the input dtype, weight [C, W] ~ N(0, 1/W)
+    and bias [C] ~ N(0, 0.1^2) in fp32 (draw order: lengths, x, weight, bias)."""
+    seed = w.seed if seed is None else seed
+    B = w.B if B is None else B
+    T = w.T if T is None else T
+    C = w.conv_channels if C is None else C
+    W = w.conv_width
+    cu = None
+    if lengths is None and w.lengths is not None:
+        lengths = w.lengths
+    if lengths is None and w.num_seqs:
+        lengths = varlen_lengths(T, w.num_seqs, w.len_range[0], w.len_range[1], seed)
+    if lengths is not None:
+        cu = cu_from_lengths(lengths)
+        B, T = 1, int(cu[-1])
+    gen = torch.Generator(device=device).manual_seed(seed)
+    x = torch.randn((B, T, C), generator=gen, device=device, dtype=torch.float32).to(w.torch_dtype)
+    weight = torch.randn((C, W), generator=gen, device=device, dtype=torch.float32) / math.sqrt(W)
+    bias = 0.1 * torch.randn((C,), generator=gen, device=device, dtype=torch.float32)
+    return dict(x=x, weight=weight, bias=bias, cu_seqlens=cu, B=B, T=T, C=C, W=W, R=w.R, dtype=w.dtype,
+                layout=w.layout)

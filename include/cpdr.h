@@ -115,6 +115,9 @@ typedef struct {
     int32_t Hq;             /* query heads of q and o (GQA, [FLA-CP] §5.1): 0 or H for none,
                                else a multiple G*H; q head hq reads the state of head hq / G,
                                while k, v, beta, gate and every state keep H heads */
+    int32_t conv_width;     /* causal conv1d kernel size W for cpdr_conv1d_fwd (the
+                               conv1d_kernel_size of [FLA-CP] §3.1-§3.2): 0 = no conv path,
+                               else 1..8 */
 } cpdr_desc;
 
 typedef struct cpdr_ctx cpdr_ctx;
@@ -218,6 +221,32 @@ cpdr_status cpdr_merge(const cpdr_ctx *ctx, const float *S_ext, const float *M, 
 cpdr_status cpdr_fwd(const cpdr_ctx *ctx, const void *q, const void *k, const void *v,
                      const void *beta, const float *gate, const void *wy, const float *S_init, void *o,
                      float *final_state, void *stream);
+
+/*
+ * Causal depthwise conv1d over the token axis, the layer step before the
+ * delta rule, on the context's segments ([FLA-CP] §2.4: the conv sees only
+ * the W - 1 tokens before each token, so a rank takes the tail of the
+ * previous rank's tokens; §3.2-§3.3: conv1d_kernel_size, pre_num_conv_tokens).
+ * Per channel c and token t of a sequence (positions before the sequence
+ * start read as zero):
+ *     y[t, c] = act( bias[c] + sum_{i=0}^{W-1} weight[c, i] * x[t - (W-1) + i, c] )
+ * act = identity (activation 0) or SiLU, z * sigmoid(z) (activation 1).
+ * On one device the previous segment's tail is read where it lies in memory
+ * (in the zigzag layout, another rank's part), so no exchange buffer exists.
+ * Layout: x, y [B, T, channels] in the context's token order and input dtype
+ * (fp32 or bf16), contiguous; weight [channels, W] fp32; bias [channels] fp32
+ * or NULL.  W = desc.conv_width (> 0).  channels % 8 == 0, 1 <= channels.
+ * Arithmetic in fp32, y rounded once.  y must not overlap x.
+ * Errors: CPDR_ERR_INVALID (context without a conv width, bad channels or
+ * activation, null or misaligned pointers), CPDR_ERR_CUDA.
+ */
+cpdr_status cpdr_conv1d_fwd(const cpdr_ctx *ctx, const void *x, const float *weight, const float *bias,
+                            int32_t channels, int32_t activation, void *y, void *stream);
+
+/* pre_num_conv_tokens ([FLA-CP] §3.3) per segment, host memory: how many of
+ * the W - 1 tokens before segment s's start belong to its first sequence
+ * (0 when the segment starts a sequence), out[0 .. min(cap, nseg)). */
+cpdr_status cpdr_plan_conv_tokens(const cpdr_ctx *ctx, int32_t *out, int32_t cap);
 
 /*
  * Whole path from HOST memory: copies q, k, v, beta, gate into the

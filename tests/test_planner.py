@@ -159,3 +159,38 @@ def test_grouped_query_heads_validation(cpdr_lib, H, Hq, ok):
         with pytest.raises(cpdr.CpdrError) as ei:
             mk()
         assert ei.value.status == cpdr.ERR_INVALID
+
+
+# ---- causal conv1d halo ([FLA-CP] §2.4, §3.3 pre_num_conv_tokens) ----------
+@pytest.mark.parametrize("lengths,R,W,zigzag", [
+    ([3000, 4000, 3240], 2, 4, False),
+    ([5118, 5122], 2, 4, False),
+    ([7000, 3240], 4, 4, False),
+    ([5, 7, 6, 9, 4, 11, 6, 16], 8, 8, False),
+    ([1] * 64, 32, 4, False),
+    ([100, 0, 28], 2, 3, True),
+    ([3000, 4000, 3240], 4, 4, True),
+    ([8], 2, 4, True),
+    ([3, 5], 2, 3, True),
+])
+def test_pre_num_conv_tokens(cpdr_lib, lengths, R, W, zigzag):
+    from oracle import conv
+    cu = [0]
+    for x in lengths:
+        cu.append(cu[-1] + x)
+    ctx = cpdr.Context(B=1, T=cu[-1], H=1, d=64, R=R, gate="gdn", dtype="bf16", cu_seqlens=cu, host_only=True,
+                       layout="zigzag" if zigzag else "contiguous", conv_width=W)
+    assert ctx.conv_pre_tokens() == conv.pre_num_conv_tokens(cu, cu[-1], R, W, zigzag=zigzag)
+
+
+def test_conv_width_validation(cpdr_lib):
+    mk = lambda W: cpdr.Context(B=1, T=256, H=1, d=64, R=2, gate="gdn", dtype="bf16", host_only=True,
+                                conv_width=W)
+    for W in (0, 1, 4, 8):
+        mk(W)
+    for W, st in ((9, cpdr.ERR_UNSUPPORTED), (-1, cpdr.ERR_UNSUPPORTED)):
+        with pytest.raises(cpdr.CpdrError) as ei:
+            mk(W)
+        assert ei.value.status == st
+    with pytest.raises(cpdr.CpdrError):
+        mk(0).conv_pre_tokens()
