@@ -281,7 +281,7 @@ def run_ours(args, ws, rank, local):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        ctx.wy_build(k, beta, g, wy, stream)
+        ctx.wy_build(q, k, beta, g, wy, stream)
         if ev is not None:
             ev[1].record(stream)
         ctx.preprocess(k, v, beta, g, bufs["S_ext"], bufs["M"], wy=wy, stream=stream)

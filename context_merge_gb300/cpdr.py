@@ -74,7 +74,7 @@ def load():
         lib.cpdr_plan_fragments.argtypes = [vp, ctypes.POINTER(Fragment), ctypes.c_int32]
         lib.cpdr_plan_counts.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         lib.cpdr_wy_bytes.argtypes = [vp, ctypes.POINTER(sz)]
-        lib.cpdr_wy_build.argtypes = [vp] * 6
+        lib.cpdr_wy_build.argtypes = [vp] * 7
         lib.cpdr_preprocess.argtypes = [vp] * 9
         lib.cpdr_merge.argtypes = [vp] * 5
         lib.cpdr_fwd.argtypes = [vp] * 11
@@ -228,9 +228,12 @@ class Context:
             if not t.is_contiguous():
                 raise ValueError(f"{name} must be contiguous")
 
-    def wy_build(self, k, beta, g, wy, stream=None):
-        self._check_inputs(k=k, beta=beta, g=g)
-        _check(self._lib.cpdr_wy_build(self._h, _ptr(k), _ptr(beta), _ptr(g), _ptr(wy), _stream(stream)))
+    def wy_build(self, q, k, beta, g, wy, stream=None):
+        """WY tiles (and, for the per-dim gate, the pre-gated operand tiles,
+        which read q) into ``wy``."""
+        self._check_inputs(q=q, k=k, beta=beta, g=g)
+        _check(self._lib.cpdr_wy_build(self._h, _ptr(q), _ptr(k), _ptr(beta), _ptr(g), _ptr(wy),
+                                       _stream(stream)))
 
     def preprocess(self, k, v, beta, g, S_ext, M, wy=None, stream=None):
         self._check_inputs(k=k, v=v, beta=beta, g=g)
@@ -252,7 +255,7 @@ class Context:
         if o is None:
             o = torch.empty((self.B, self.T, self.Hq, self.d), dtype=v.dtype, device=v.device)
         wy = bufs.get("wy")
-        self.wy_build(k, beta, g, wy, stream)
+        self.wy_build(q, k, beta, g, wy, stream)
         self.preprocess(k, v, beta, g, bufs["S_ext"], bufs["M"], wy=wy, stream=stream)
         self.merge(bufs["S_ext"], bufs["M"], bufs["S_init"], stream)
         self.fwd(q, k, v, beta, g, bufs["S_init"], o, bufs["final_state"], wy=wy, stream=stream)

@@ -227,15 +227,19 @@ cpdr_status cpdr_wy_bytes(const cpdr_ctx *c, size_t *bytes) {
     return CPDR_OK;
 }
 
-cpdr_status cpdr_wy_build(const cpdr_ctx *c, const void *k, const void *beta, const float *gate, void *wy,
-                          void *stream) {
+cpdr_status cpdr_wy_build(const cpdr_ctx *c, const void *q, const void *k, const void *beta, const float *gate,
+                          void *wy, void *stream) {
     CPDR_TRY(check_ctx(c));
     if (cpdr::wy_bytes(c) == 0) return CPDR_OK;
+    const bool kda = c->plan.gate_kind == CPDR_GATE_PER_DIM;
+    CPDR_TRY(check_ptr(q, "q", !kda));
     CPDR_TRY(check_ptr(k, "k"));
     CPDR_TRY(check_ptr(beta, "beta"));
     CPDR_TRY(check_ptr(gate, "gate"));
     CPDR_TRY(check_ptr(wy, "wy"));
-    return launch_rc(cpdr::launch_tc_wy(c, k, beta, gate, wy, stream), "cpdr_wy_build");
+    return launch_rc(kda ? cpdr::launch_tc_kda_prep(c, k, q, beta, gate, wy, stream)
+                         : cpdr::launch_tc_wy(c, k, beta, gate, wy, stream),
+                     "cpdr_wy_build");
 }
 
 cpdr_status cpdr_preprocess(const cpdr_ctx *c, const void *k, const void *v, const void *beta,
@@ -350,7 +354,7 @@ cpdr_status cpdr_forward_host(const cpdr_ctx *c, const void *q, const void *k, c
     if (e == cudaSuccess) e = cudaMemcpyAsync(db, beta, s.beta, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dg, gate, s.gate, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: host-to-device copy");
-    CPDR_TRY(cpdr_wy_build(c, dk, db, dg, dwy, stream));
+    CPDR_TRY(cpdr_wy_build(c, dq, dk, db, dg, dwy, stream));
     CPDR_TRY(cpdr_preprocess(c, dk, dv, db, dg, dwy, dse, dm, stream));
     CPDR_TRY(cpdr_merge(c, dse, dm, dsi, stream));
     CPDR_TRY(cpdr_fwd(c, dq, dk, dv, db, dg, dwy, dsi, dout, dfin, stream));

@@ -45,6 +45,22 @@ struct ConvTile {
 constexpr size_t kWyTileBytes = 8192;
 constexpr size_t kWyUnitBytes = 3 * kWyTileBytes;
 
+// Per-dim gate (KDA) units: the WY tiles (with gamma = 1: the gate lives in
+// the operand tiles), then the per-dim decay 2^(G_C) and the gated operand
+// tiles of the chunk, each 64 rows x 128 columns bf16 as two 8 KiB swizzled
+// 64-column images: Kg = k 2^G (hi, lo), Kgam = k 2^(G_C - G) (hi, lo),
+// Qg = q 2^G, and the masked intra-chunk product P = (Q K^T ⊙ Lambda)
+// (64 x 64, one image).  Offsets are multiples of 1 KiB (swizzle atoms).
+constexpr size_t kKdaOffGC = 3 * kWyTileBytes;          // 128 fp32 (1 KiB slot)
+constexpr size_t kKdaOffKg = kKdaOffGC + 1024;
+constexpr size_t kKdaOffKgam = kKdaOffKg + 16384;
+constexpr size_t kKdaOffKgLo = kKdaOffKgam + 16384;
+constexpr size_t kKdaOffKgamLo = kKdaOffKgLo + 16384;
+constexpr size_t kKdaOffQg = kKdaOffKgamLo + 16384;
+constexpr size_t kKdaOffP = kKdaOffQg + 16384;
+constexpr size_t kKdaUnitBytes = kKdaOffP + kWyTileBytes;   // 113 KiB
+static_assert(kKdaUnitBytes % 1024 == 0, "KDA unit must keep 1 KiB alignment");
+
 // Host plan ([FLA-CP] §3.2-§3.3): fragments per segment and the derived
 // work lists.  All token indices are on the flattened [B*T] axis.
 struct Plan {
@@ -135,6 +151,8 @@ int launches_per_step(const cpdr_ctx *c);
 // Bytes of the WY tile workspace (0 when the CUDA-core kernels are used).
 size_t wy_bytes(const cpdr_ctx *c);
 
+int launch_tc_kda_prep(const cpdr_ctx *c, const void *k, const void *q, const void *beta, const float *g,
+                       void *wy, void *stream);
 int launch_tc_wy(const cpdr_ctx *c, const void *k, const void *beta, const float *g, void *wy,
                  void *stream);
 int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy,

@@ -124,7 +124,7 @@ extern "C" cpdr_status cpdr_forward_noalloc(const cpdr_ctx *c, const void *q, co
     mc->dev = t;
     mc->has_device = true;
     mc->device = dev;
-    cpdr_status s = cpdr_wy_build(c, k, beta, gate, wy, stream);
+    cpdr_status s = cpdr_wy_build(c, q, k, beta, gate, wy, stream);
     if (s == CPDR_OK) s = cpdr_preprocess(c, k, v, beta, gate, wy, S_ext, M, stream);
     if (s == CPDR_OK) s = cpdr_merge(c, S_ext, M, S_init, stream);
     if (s == CPDR_OK) s = cpdr_fwd(c, q, k, v, beta, gate, wy, S_init, o, final_state, stream);

@@ -49,7 +49,11 @@ constexpr int C = 64;
 constexpr int D = 128;
 constexpr int NTHREADS = 512;
 
-enum Mode { MODE_FWD = 0, MODE_PRE = 1 };
+// Modes: bit 0 = pre-process (else forward), bit 1 = per-dim gate (KDA),
+// whose gate is folded into operand tiles precomputed per chunk (tc_kda.cu).
+enum Mode { MODE_FWD = 0, MODE_PRE = 1, MODE_FWD_KDA = 2, MODE_PRE_KDA = 3 };
+__host__ __device__ constexpr bool mode_fwd(int m) { return (m & 1) == 0; }
+__host__ __device__ constexpr bool mode_kda(int m) { return (m & 2) != 0; }
 enum Role { ROLE_S = 0, ROLE_M = 1 };
 
 // Optional event trace (compile with -DCPDR_TRACE): CTA (0, 0) of each
@@ -59,7 +63,7 @@ __device__ unsigned long long g_cpdr_trace[3][8][64][16];
 #define TR(role, chunk, ev)                                                                \
     do {                                                                                   \
         if (blockIdx.x == 0 && blockIdx.y == 0 && (threadIdx.x & 31) == 0 && (chunk) < 64) \
-            g_cpdr_trace[MODE * (1 + ROLE)][role][chunk][ev] = (unsigned long long)clock64(); \
+            g_cpdr_trace[(MODE & 1) * (1 + ROLE)][role][chunk][ev] = (unsigned long long)clock64(); \
     } while (0)
 #else
 #define TR(role, chunk, ev) \
@@ -112,11 +116,60 @@ struct Lay {
     uint32_t nstage, stage_bytes, kc0, kc1, qc0, qc1, vc0, vc1, t1, t2, k_lbo, v_lbo, tx_bytes, wy_off;
     uint32_t ngate, gate_floats;
     uint32_t mask, wb, wb_lo, gates, bars, ctl, tslot, total;
+    // per-dim gate: operand tiles of the stage (Kg is kc0), the chunk decay,
+    // the masked intra-chunk product, and the bulk copies from the unit
+    uint32_t kgam, kglo, kgamlo, gcv, pt, gcs;
+    uint32_t ncp, cp_src[3], cp_dst[3], cp_len[3];
 };
 
 __host__ __device__ constexpr Lay make_lay(int mode, int role) {
     Lay L{};
-    if (mode == MODE_FWD) {
+    if (mode_kda(mode)) {
+        // stage images copied from the unit (offsets as in cpdr_internal.hpp)
+        const uint32_t tp = 0, thi = (uint32_t)kWyTileBytes, tlo = 2 * (uint32_t)kWyTileBytes;
+        const uint32_t gc = (uint32_t)kKdaOffGC, qg = (uint32_t)kKdaOffQg;
+        if (mode_fwd(mode)) {
+            L.t1 = 0; L.gcv = 8192; L.kc0 = 9216; L.kgam = 25600; L.qc0 = 41984; L.pt = 58368;
+            L.vc0 = 66560; L.vc1 = 74752; L.stage_bytes = 82944;
+            L.ncp = 3;
+            L.cp_src[0] = tp; L.cp_dst[0] = L.t1; L.cp_len[0] = 8192;
+            L.cp_src[1] = gc; L.cp_dst[1] = L.gcv; L.cp_len[1] = (uint32_t)(kKdaOffKgLo - kKdaOffGC);
+            L.cp_src[2] = qg; L.cp_dst[2] = L.qc0; L.cp_len[2] = (uint32_t)(kKdaUnitBytes - kKdaOffQg);
+            L.nstage = 2;
+        } else if (role == ROLE_S) {
+            L.t1 = 0; L.gcv = 8192; L.kc0 = 9216; L.kgam = 25600; L.vc0 = 41984; L.vc1 = 50176;
+            L.stage_bytes = 58368;
+            L.ncp = 2;
+            L.cp_src[0] = tp; L.cp_dst[0] = L.t1; L.cp_len[0] = 8192;
+            L.cp_src[1] = gc; L.cp_dst[1] = L.gcv; L.cp_len[1] = (uint32_t)(kKdaOffKgLo - kKdaOffGC);
+            L.nstage = 3;
+        } else {
+            L.t1 = 0; L.t2 = 8192; L.gcv = 16384; L.kc0 = 17408; L.kgam = 33792; L.kglo = 50176;
+            L.kgamlo = 66560; L.stage_bytes = 82944;
+            L.ncp = 1;
+            L.cp_src[0] = thi; L.cp_dst[0] = 0; L.cp_len[0] = (uint32_t)(kKdaOffQg - kWyTileBytes);
+            L.nstage = 2;
+            (void)tlo;
+        }
+        if (mode_fwd(mode) || role == ROLE_S) L.t2 = L.t1;   // T'' = T' (gamma is in the tiles)
+        L.kc1 = L.kc0 + 8192; L.qc1 = L.qc0 + 8192; L.k_lbo = 8192; L.v_lbo = 8192; L.wy_off = 0;
+        L.tx_bytes = L.stage_bytes;
+        L.ngate = L.nstage + 2;
+        L.gate_floats = 0;
+        const bool split = !mode_fwd(mode) && role == ROLE_M;
+        uint32_t o = L.nstage * L.stage_bytes;
+        L.mask = o;
+        L.wb = o; o += 16384;
+        L.wb_lo = o; o += (split ? 16384 : 0);
+        L.gates = o;
+        L.gcs = o; o += 512;   // the state warps' copy of the chunk decay
+        L.bars = o; o += NBARS * 8;
+        L.ctl = o; o += 16;
+        L.tslot = o; o += 16;
+        L.total = o;
+        return L;
+    }
+    if (mode_fwd(mode)) {
         L.stage_bytes = 65536; L.kc0 = 0; L.qc0 = 8192; L.kc1 = 16384; L.qc1 = 24576; L.vc0 = 32768; L.vc1 = 40960;
         L.t1 = 49152; L.t2 = 57344;
         L.k_lbo = 16384; L.v_lbo = 8192; L.wy_off = 0;
@@ -137,10 +190,10 @@ __host__ __device__ constexpr Lay make_lay(int mode, int role) {
     L.ngate = L.nstage + 2;
     // forward: G, gamma, Gamma, e, f (64 each), gamma^C, exact flag;
     // pre-process: Gamma, gamma^C
-    L.gate_floats = (mode == MODE_FWD) ? 5 * 64 + 4 : 64 + 4;
-    const bool split = (mode == MODE_PRE && role == ROLE_M);
+    L.gate_floats = (mode_fwd(mode)) ? 5 * 64 + 4 : 64 + 4;
+    const bool split = (!mode_fwd(mode) && role == ROLE_M);
     uint32_t o = L.nstage * L.stage_bytes;
-    L.mask = o; o += (mode == MODE_FWD ? 8192 : 0);
+    L.mask = o; o += (mode_fwd(mode) ? 8192 : 0);
     L.wb = o; o += 16384;
     L.wb_lo = o; o += (split ? 16384 : 0);
     L.gates = o; o += L.ngate * L.gate_floats * 4;
@@ -149,6 +202,7 @@ __host__ __device__ constexpr Lay make_lay(int mode, int role) {
     L.ctl = o; o += 16;
     L.tslot = o; o += 16;
     L.total = o;
+    L.kgam = L.kc0;   // scalar gate: one K tile serves every product
     return L;
 }
 
@@ -173,7 +227,7 @@ template <int MODE, int ROLE>
 __device__ __forceinline__ Gates gates_of(const Run &r, int slot) {
     constexpr Lay L = make_lay(MODE, ROLE);
     float *q = reinterpret_cast<float *>(r.base + L.gates) + slot * L.gate_floats;
-    if (MODE == MODE_FWD) return Gates{q, q + 64, q + 128, q + 192, q + 256, q + 320};
+    if (mode_fwd(MODE)) return Gates{q, q + 64, q + 128, q + 192, q + 256, q + 320};
     return Gates{nullptr, nullptr, q, nullptr, nullptr, q + 64};
 }
 template <int MODE, int ROLE>
@@ -253,7 +307,7 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
         const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(c));
         gs.Gam[i0] = exp2f(lg.GC - lg.G0);
         gs.Gam[i1] = exp2f(lg.GC - lg.G1);
-        if (MODE == MODE_FWD) {
+        if (mode_fwd(MODE)) {
             gs.G[i0] = lg.G0; gs.G[i1] = lg.G1;
             gs.gam[i0] = exp2f(lg.G0); gs.gam[i1] = exp2f(lg.G1);
             gs.e[i0] = exp2f(lg.G0 - lg.Gr); gs.e[i1] = exp2f(lg.G1 - lg.Gr);
@@ -266,7 +320,8 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
         __syncwarp();
         if (lane == 0) mbar_arrive(&r.bar[B_GATE0 + gate_slot<MODE, ROLE>(c)]);
     };
-    produce_gates(0);
+    constexpr bool KDA = mode_kda(MODE);
+    if (!KDA) produce_gates(0);
     constexpr int NS = (int)L.nstage;
     for (int t = 0; t < r.n; t++) {
         const int s = t % NS;
@@ -276,16 +331,32 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
         TR(0, t, 0);
         uint64_t *fb = &r.bar[B_FULL0 + s];
         const int tok = (int)(r.tok0 + (int64_t)t * C);
+        if (KDA) {
+            if (lane == 0) {
+                // the unit's operand images, and V
+                uint8_t *st = r.base + s * L.stage_bytes;
+                const uint8_t *unit = r.p->wy + ((size_t)(r.chunk0 + t) * H + r.h) * kKdaUnitBytes;
+                mbar_arrive_expect_tx(fb, L.tx_bytes);
+#pragma unroll
+                for (int i = 0; i < (int)L.ncp; i++) bulk_load(st + L.cp_dst[i], unit + L.cp_src[i], L.cp_len[i], fb);
+                if (mode_fwd(MODE) || ROLE == ROLE_S) {
+                    tma_load_3d(st + L.vc0, tv, fb, 0, r.h, tok);
+                    tma_load_3d(st + L.vc1, tv, fb, 64, r.h, tok);
+                }
+            }
+            issued[s] = t;
+            continue;
+        }
         if (lane == 0) {
             uint8_t *st = r.base + s * L.stage_bytes;
             mbar_arrive_expect_tx(fb, L.tx_bytes);
             tma_load_3d(st + L.kc0, tk, fb, 0, r.h, tok);
             tma_load_3d(st + L.kc1, tk, fb, 64, r.h, tok);
-            if (MODE == MODE_FWD) {
+            if (mode_fwd(MODE)) {
                 tma_load_3d(st + L.qc0, tq, fb, 0, r.hq, tok);
                 tma_load_3d(st + L.qc1, tq, fb, 64, r.hq, tok);
             }
-            if (MODE == MODE_FWD || ROLE == ROLE_S) {
+            if (mode_fwd(MODE) || ROLE == ROLE_S) {
                 tma_load_3d(st + L.vc0, tv, fb, 0, r.h, tok);
                 tma_load_3d(st + L.vc1, tv, fb, 64, r.h, tok);
             }
@@ -364,6 +435,7 @@ __device__ __forceinline__ void mma_tk(uint32_t d, uint32_t a, uint64_t b, uint3
 // adds s * stage_bytes >> 4).
 struct Descs {
     uint64_t stack0, kmn0, vmn0, q0, t10, t20, wb, wblo, mask;
+    uint64_t kgam0, kglo0, kgamlo0, pt0;   // per-dim gate: P_S operands (hi, lo), W's lo operand, P
 };
 template <int MODE, int ROLE>
 __device__ __forceinline__ Descs make_descs(const Run &r) {
@@ -379,6 +451,10 @@ __device__ __forceinline__ Descs make_descs(const Run &r) {
     d.wb = mndesc(b0 + L.wb, 16384);
     d.wblo = mndesc(b0 + L.wb_lo, 16384);
     d.mask = kdesc(b0 + L.mask);
+    d.kgam0 = mndesc(b0 + L.kgam, L.k_lbo);
+    d.kglo0 = mndesc(b0 + L.kglo, L.k_lbo);
+    d.kgamlo0 = mndesc(b0 + L.kgamlo, L.k_lbo);
+    d.pt0 = kdesc(b0 + L.pt);
     return d;
 }
 template <int MODE, int ROLE>
@@ -393,8 +469,9 @@ __device__ __forceinline__ uint64_t stg(uint64_t d, int t) {
 template <int MODE, int ROLE>
 __device__ __forceinline__ void run_mma(const Run &r) {
     constexpr Lay L = make_lay(MODE, ROLE);
-    constexpr bool FWD = MODE == MODE_FWD, SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
+    constexpr bool FWD = mode_fwd(MODE), SPLIT = (!mode_fwd(MODE) && ROLE == ROLE_M);
     constexpr bool HAS_U = FWD || ROLE == ROLE_S;
+    constexpr bool KDA = mode_kda(MODE);
     constexpr int NS = (int)L.nstage;
     if ((threadIdx.x & 31) != 0) return;
     const uint32_t tm = r.tmem;
@@ -409,10 +486,10 @@ __device__ __forceinline__ void run_mma(const Run &r) {
         // has completed (W behind it would delay the chain)
         if (t >= 1 && !mbar_wait(&r.bar[B_WREADY], (t - 1) & 1, ctl, st, 21)) break;
         if (t >= 1 && !mbar_wait(&r.bar[B_WBFREE], (t - 1) & 1, ctl, st, 24)) break;
-        if (FWD && t >= 1 && !mbar_wait(&r.bar[B_PFREE], (t - 1) & 1, ctl, st, 22)) break;
+        if (FWD && !KDA && t >= 1 && !mbar_wait(&r.bar[B_PFREE], (t - 1) & 1, ctl, st, 22)) break;
         tc_fence_after();
         TR(1, t, 0);
-        if (FWD) {   // P = [K; Q] K^T, rows 64..127 = Q K^T
+        if (FWD && !KDA) {   // P = [K; Q] K^T, rows 64..127 = Q K^T
             mma_kk<64, 128, false>(tm + TM_P, stg<MODE, ROLE>(d.stack0, t), KATOM, stg<MODE, ROLE>(d.stack0, t),
                                    KATOM, false);
             mma_commit(&r.bar[B_PFULL]);
@@ -420,6 +497,8 @@ __device__ __forceinline__ void run_mma(const Run &r) {
         const uint64_t tpp = SPLIT ? stg<MODE, ROLE>(d.t10, t) : stg<MODE, ROLE>(d.t20, t);
         mma_mnk<64, 64>(tm + TM_W, stg<MODE, ROLE>(d.kmn0, t), tpp, 8192, false);
         if (SPLIT) mma_mnk<64, 64>(tm + TM_W, stg<MODE, ROLE>(d.kmn0, t), stg<MODE, ROLE>(d.t20, t), 8192, true);
+        // per-dim gate: the gated K tile is rounded too, W += lo(Kg) hi(T'')
+        if (SPLIT && KDA) mma_mnk<64, 64>(tm + TM_W, stg<MODE, ROLE>(d.kglo0, t), tpp, 8192, true);
         mma_commit(&r.bar[B_WFULL]);
         if (HAS_U) {
             // the Delta accumulator is free once chunk t-1's Delta was read;
@@ -445,6 +524,21 @@ template <int MODE, int ROLE>
 __device__ __forceinline__ void run_mask(const Run &r) {
     constexpr Lay L = make_lay(MODE, ROLE);
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (mode_kda(MODE)) {
+        // per-dim gate: gamma ⊙ Q and the masked product arrive with the
+        // stage; release them chunk by chunk, one chunk ahead of the issuer
+        constexpr int NS = (int)L.nstage;
+        for (int ch = 0; ch < r.n; ch++) {
+            if (ch >= 1 && !warp_wait(r, B_MFREE, (ch - 1) & 1, 53)) return;
+            if (!warp_wait(r, B_FULL0 + ch % NS, (ch / NS) & 1, 54)) return;
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&r.bar[B_QREADY0 + (ch & 1)]);
+                mbar_arrive(&r.bar[B_MREADY]);
+            }
+        }
+        return;
+    }
     const int i = 32 * (w - 2) + lane;   // row of Q K^T (TMEM lane 64 + i)
     for (int ch = 0; ch < r.n; ch++) {
         if (!warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 50)) return;
@@ -519,7 +613,7 @@ __device__ __forceinline__ void run_mask(const Run &r) {
 template <int MODE, int ROLE>
 __device__ __forceinline__ void run_wepi(const Run &r) {
     constexpr Lay L = make_lay(MODE, ROLE);
-    constexpr bool FWD = MODE == MODE_FWD, SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
+    constexpr bool FWD = mode_fwd(MODE), SPLIT = (!mode_fwd(MODE) && ROLE == ROLE_M);
     const Params &p = *r.p;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = w & 3, row = 32 * q + lane;
@@ -597,7 +691,8 @@ __device__ __forceinline__ void neg_pairs(const float *x, uint32_t (&hi)[NC], ui
 template <int MODE, int ROLE>
 __device__ __forceinline__ void run_state(const Run &r) {
     constexpr Lay L = make_lay(MODE, ROLE);
-    constexpr bool FWD = MODE == MODE_FWD, SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
+    constexpr bool FWD = mode_fwd(MODE), SPLIT = (!mode_fwd(MODE) && ROLE == ROLE_M);
+    constexpr bool KDA = mode_kda(MODE);
     constexpr bool HAS_U = FWD || ROLE == ROLE_S;
     constexpr int NS = (int)L.nstage;
     const Params &p = *r.p;
@@ -671,7 +766,7 @@ __device__ __forceinline__ void run_state(const Run &r) {
             }
             TR(1, ch, 3);
         }
-        bool ok = warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 60);
+        bool ok = KDA || warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 60);
         const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(ch));
         // ---- Delta epilogue: tokens 32 half .. 32 half + 31 of Delta^T[row]
         if (w == 8) TR(3, ch, 0);
@@ -688,9 +783,10 @@ __device__ __forceinline__ void run_state(const Run &r) {
                 tmem_st16(lane_base + TM_DB + 16 * half, d16);
             }
             // (Delta diag Gamma)^T for P_S (negated here, so that the pair
-            // conversion below stores it with a plus sign)
+            // conversion below stores it with a plus sign); per-dim gate:
+            // Delta^T, Gamma being in the K operand
 #pragma unroll
-            for (int jj = 0; jj < 32; jj++) v[jj] = -(v[jj] * gs.Gam[32 * half + jj]);
+            for (int jj = 0; jj < 32; jj++) v[jj] = KDA ? -v[jj] : -(v[jj] * gs.Gam[32 * half + jj]);
             uint32_t hi[16], lo[16];
             neg_pairs<16>(v, hi, SPLIT ? lo : nullptr);
             tmem_st16(lane_base + TM_DGB + 16 * half, hi);
@@ -699,15 +795,21 @@ __device__ __forceinline__ void run_state(const Run &r) {
             tc_fence_before();
             __syncwarp();
             if (HAS_U && lane == 0) mbar_arrive(&r.bar[B_DLREADY]);   // the U product may reuse the columns
+            if (KDA && w == 8) {
+                // the chunk's per-dim decay, kept past the stage's release
+                const float4 g4 = reinterpret_cast<const float4 *>(r.base + (ch % NS) * L.stage_bytes + L.gcv)[lane];
+                reinterpret_cast<float4 *>(r.base + L.gcs)[lane] = g4;
+            }
         }
         if (w == 8) TR(3, ch, 2);
         if ((bad = named_bar_or(kStateBar, kBarThreads, ok ? 0 : 1))) break;
         // ---- P_S (and the masked output product) of chunk ch
         if (issuer) {
             tc_fence_after();
-            // P_S = (Delta diag Gamma)^T K
-            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kmn0, ch), false);
-            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg<MODE, ROLE>(d.kmn0, ch), true);
+            // P_S = (Delta diag Gamma)^T K  (per-dim gate: Delta^T Kgam)
+            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kgam0, ch), false);
+            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg<MODE, ROLE>(d.kgam0, ch), true);
+            if (SPLIT && KDA) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kgamlo0, ch), true);
             mma_commit(&r.bar[B_PSFULL]);
             TR(1, ch, 4);
             bool iok = true;
@@ -715,7 +817,8 @@ __device__ __forceinline__ void run_state(const Run &r) {
                 iok = mbar_wait(&r.bar[B_MREADY], ch & 1, ctl, st, 68);
                 if (iok) {
                     tc_fence_after();
-                    mma_tk<64, 64>(tm + TM_O, tm + TM_DB, d.mask, 8192, true);   // -O^T += (-Delta^T) mask^T
+                    // -O^T += (-Delta^T) mask^T  (per-dim gate: the stage's P)
+                    mma_tk<64, 64>(tm + TM_O, tm + TM_DB, KDA ? stg<MODE, ROLE>(d.pt0, ch) : d.mask, 8192, true);
                     mma_commit(&r.bar[B_OFULL]);
                     mma_commit(&r.bar[B_MFREE]);
                 }
@@ -728,14 +831,16 @@ __device__ __forceinline__ void run_state(const Run &r) {
         if (w == 8) TR(3, ch, 3);
         if (ok) {
             tc_fence_after();
-            const float gC = gs.gC[0];
+            const float gC = KDA ? 0.f : gs.gC[0];
+            const float *gcd = reinterpret_cast<const float *>(r.base + L.gcs) + 64 * half;
 #pragma unroll
             for (int piece = 0; piece < 2; piece++) {
                 float v[32];
                 tmem_ld32(lane_base + TM_PS + 64 * half + 32 * piece, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; i++) S[32 * piece + i] = fmaf(gC, S[32 * piece + i], v[i]);
+                for (int i = 0; i < 32; i++)
+                    S[32 * piece + i] = fmaf(KDA ? gcd[32 * piece + i] : gC, S[32 * piece + i], v[i]);
             }
             put_state();
         }
@@ -780,7 +885,7 @@ __device__ __forceinline__ void run_state(const Run &r) {
 template <int MODE, int ROLE>
 __device__ __forceinline__ void run_issuer(const Run &r) {
     constexpr Lay L = make_lay(MODE, ROLE);
-    constexpr bool SPLIT = (MODE == MODE_PRE && ROLE == ROLE_M);
+    constexpr bool SPLIT = (!mode_fwd(MODE) && ROLE == ROLE_M);
     constexpr bool HAS_U = ROLE == ROLE_S;
     constexpr int NS = (int)L.nstage;
     const bool lead = (threadIdx.x & 31) == 0;
@@ -815,8 +920,10 @@ __device__ __forceinline__ void run_issuer(const Run &r) {
         if ((bad = named_bar_or(kStateBar, 288, ok ? 0 : 1))) break;
         if (lead) {
             tc_fence_after();
-            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kmn0, ch), false);
-            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg<MODE, ROLE>(d.kmn0, ch), true);
+            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kgam0, ch), false);
+            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg<MODE, ROLE>(d.kgam0, ch), true);
+            if (SPLIT && mode_kda(MODE))
+                mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kgamlo0, ch), true);
             mma_commit(&r.bar[B_PSFULL]);
             mma_commit(&r.bar[B_EMPTY0 + ch % NS]);   // this thread's reads of stage ch
             TR(1, ch, 4);
@@ -873,9 +980,9 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (w == 0 && (threadIdx.x & 31) == 0) {
-        tma_prefetch_desc(tk);
-        if (MODE == MODE_FWD) tma_prefetch_desc(tq);
-        if (MODE == MODE_FWD || ROLE == ROLE_S) tma_prefetch_desc(tv);
+        if (!mode_kda(MODE)) tma_prefetch_desc(tk);
+        if (mode_fwd(MODE) && !mode_kda(MODE)) tma_prefetch_desc(tq);
+        if (mode_fwd(MODE) || ROLE == ROLE_S) tma_prefetch_desc(tv);
     }
     if (w == 1) {
         tmem_alloc(tmem_slot, TM_COLS);
@@ -888,7 +995,7 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     if (w == 0) run_producer<MODE, ROLE>(r, tq, tk, tv);
     else if (w == 1) run_mma<MODE, ROLE>(r);
     else if (w < 4) {
-        if (MODE == MODE_FWD) run_mask<MODE, ROLE>(r);
+        if (mode_fwd(MODE)) run_mask<MODE, ROLE>(r);
         else if (w == 2) run_issuer<MODE, ROLE>(r);
     }
     else if (w < 8) run_wepi<MODE, ROLE>(r);
@@ -945,6 +1052,11 @@ constexpr size_t kMaxSmem = 232448;   // 227 KiB opt-in per CTA
 static_assert(make_lay(MODE_FWD, ROLE_S).total + 1024 <= kMaxSmem, "forward layout exceeds shared memory");
 static_assert(make_lay(MODE_PRE, ROLE_S).total + 1024 <= kMaxSmem, "pre-process S layout exceeds shared memory");
 static_assert(make_lay(MODE_PRE, ROLE_M).total + 1024 <= kMaxSmem, "pre-process M layout exceeds shared memory");
+static_assert(make_lay(MODE_FWD_KDA, ROLE_S).total + 1024 <= kMaxSmem, "per-dim forward layout exceeds shared memory");
+static_assert(make_lay(MODE_PRE_KDA, ROLE_S).total + 1024 <= kMaxSmem, "per-dim pre-process S layout too large");
+static_assert(make_lay(MODE_PRE_KDA, ROLE_M).total + 1024 <= kMaxSmem, "per-dim pre-process M layout too large");
+static_assert(make_lay(MODE_FWD_KDA, ROLE_S).tx_bytes < (1u << 20) && make_lay(MODE_PRE_KDA, ROLE_M).tx_bytes < (1u << 20),
+              "stage bytes exceed the mbarrier transaction count");
 static_assert(make_lay(MODE_FWD, ROLE_S).ngate <= kMaxGateSlots && make_lay(MODE_PRE, ROLE_M).ngate <= kMaxGateSlots,
               "gate slots exceed their barriers");
 
@@ -971,8 +1083,11 @@ extern "C" int cpdr_debug_trace(unsigned long long *host, int n) {
 }
 #endif
 
+// bf16, d = 128; the per-dim gate's pre-gated query tiles are per state
+// head, so grouped query heads take the CUDA-core kernels there
 bool tc_supported(const Plan &p) {
-    return p.in_dtype == CPDR_DTYPE_BF16 && p.dk == 128 && p.dv == 128 && p.gate_kind == CPDR_GATE_SCALAR;
+    if (p.in_dtype != CPDR_DTYPE_BF16 || p.dk != 128 || p.dv != 128) return false;
+    return p.gate_kind == CPDR_GATE_SCALAR || p.Hq == p.H;
 }
 
 int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy, float *S_ext,
@@ -981,7 +1096,8 @@ int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *
     if (p.pre_items.empty()) return 0;
     CUtensorMap tk, tv;
     const int64_t tokens = (int64_t)p.B * p.T;
-    if (!make_tmap(&tk, k, tokens, p.H) || !make_tmap(&tv, v, tokens, p.H)) return (int)cudaErrorInvalidValue;
+    const bool kda = p.gate_kind == CPDR_GATE_PER_DIM;   // K comes pre-gated in the units
+    if (!make_tmap(&tk, kda ? v : k, tokens, p.H) || !make_tmap(&tv, v, tokens, p.H)) return (int)cudaErrorInvalidValue;
     Params prm{};
     prm.frags = c->dev.frags;
     prm.items = c->dev.pre_items;
@@ -1006,10 +1122,12 @@ int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *
         if (e == cudaSuccess) e = cudaStreamWaitEvent(aux, (cudaEvent_t)c->ev_fork, 0);
         if (e != cudaSuccess) return (int)e;
     }
-    int rc = launch_chain<MODE_PRE, ROLE_M>(tk, tk, tv, prm, (unsigned)p.pre_items.size(), (unsigned)p.H,
-                                            aux ? aux : st);
+    const unsigned items = (unsigned)p.pre_items.size(), H = (unsigned)p.H;
+    int rc = kda ? launch_chain<MODE_PRE_KDA, ROLE_M>(tk, tk, tv, prm, items, H, aux ? aux : st)
+                 : launch_chain<MODE_PRE, ROLE_M>(tk, tk, tv, prm, items, H, aux ? aux : st);
     if (rc) return rc;
-    rc = launch_chain<MODE_PRE, ROLE_S>(tk, tk, tv, prm, (unsigned)p.pre_items.size(), (unsigned)p.H, st);
+    rc = kda ? launch_chain<MODE_PRE_KDA, ROLE_S>(tk, tk, tv, prm, items, H, st)
+             : launch_chain<MODE_PRE, ROLE_S>(tk, tk, tv, prm, items, H, st);
     if (rc) return rc;
     if (aux) {
         cudaError_t e = cudaEventRecord((cudaEvent_t)c->ev_join, aux);
@@ -1025,7 +1143,9 @@ int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v
     if (p.frags.empty()) return 0;
     CUtensorMap tq, tk, tv;
     const int64_t tokens = (int64_t)p.B * p.T;
-    if (!make_tmap(&tq, q, tokens, p.Hq) || !make_tmap(&tk, k, tokens, p.H) || !make_tmap(&tv, v, tokens, p.H))
+    const bool kda = p.gate_kind == CPDR_GATE_PER_DIM;   // Q and K come pre-gated in the units
+    if (!make_tmap(&tq, kda ? v : q, tokens, kda ? p.H : p.Hq) || !make_tmap(&tk, kda ? v : k, tokens, p.H) ||
+        !make_tmap(&tv, v, tokens, p.H))
         return (int)cudaErrorInvalidValue;
     Params prm{};
     prm.frags = c->dev.frags;
@@ -1044,6 +1164,9 @@ int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v
     prm.scale = p.scale;
     // one chain per (fragment, query head): grouped query heads each run
     // their state head's chain
+    if (kda)
+        return launch_chain<MODE_FWD_KDA, ROLE_S>(tq, tk, tv, prm, (unsigned)p.frags.size(), (unsigned)p.Hq,
+                                                  (cudaStream_t)stream);
     return launch_chain<MODE_FWD, ROLE_S>(tq, tk, tv, prm, (unsigned)p.frags.size(), (unsigned)p.Hq,
                                           (cudaStream_t)stream);
 }

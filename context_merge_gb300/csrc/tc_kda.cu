@@ -1,0 +1,258 @@
+// Per-dim gate (KDA) preparation for the tensor-core chains: the WY step of
+// the article "flash-linear-attention 上下文并行CP ..." ([FLA-CP]) for a
+// gate per key dimension.  §2.3: the per-dim Diag(alpha_t) is too costly
+// inside the chunk recurrence, so the WY stage pre-gates the operands
+// (kg = k 2^(g_last - g), qg = q 2^g) and the pre-process and the main
+// kernel read the same gated tensors.  Per (chunk, head) unit, with
+// G_i[d] = sum_{s <= i} g_s[d] / ln 2 inside the chunk and r = 31 the
+// reference row of the factorised exponentials:
+//   A_ij = beta_i sum_d k_id k_jd 2^(G_i[d] - G_j[d])      j < i
+//   P_ij = sum_d q_id k_jd 2^(G_i[d] - G_j[d])             j <= i
+//   T = (I + A)^-1;  T' = T diag(beta) (= T'': gamma lives in the tiles)
+//   Kg = k 2^G, Kgam = k 2^(G_C - G) (bf16 hi, lo), Qg = q 2^G, gC = 2^(G_C)
+// so that, in the chain, W = T' Kg, U = T' V, the state decays by Diag(gC)
+// and takes Delta^T Kgam, and the output is (Qg) S + P Delta.
+//
+// A and P are fp32 sums of the factorised products (k 2^(G - G_r)) .
+// (k 2^(G_r - G)) (the q factor rounded to bf16: P is a bf16 tile); a unit
+// whose in-chunk decay exceeds 2^100 either way of row r takes exact
+// per-term exponentials instead.  One CTA per unit, two per SM (CUDA
+// cores): coalesced loads, column scans, the gated tiles, A and P, then one
+// warp solves T with the scalar-gate path's solver.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "cpdr_internal.hpp"
+#include "tc_common.cuh"
+#include "tc_gates.cuh"
+#include "tc_solve.cuh"
+
+namespace cpdr {
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;
+constexpr int C = 64;
+constexpr int KP_THREADS = 256;
+constexpr int KP_LD = D + 4;     // fp32 row stride of the [64][D] smem tiles
+constexpr int kRef = 31;         // reference row of the factorised exponentials
+
+struct KdaParams {
+    const WyChunk *chunks;
+    const __nv_bfloat16 *k, *q, *beta;
+    const float *g;
+    uint8_t *wy;
+    int H;
+};
+
+// Shared memory (two CTAs per SM):
+//   GF  [64][KP_LD] fp32: G (log2 cumsum), then k 2^(G_r - G)      ("KF")
+//   KB  [64][KP_LD] fp32: k, then k 2^(G - G_r)                     ("KE")
+//   QB  [64][KQ_LD] bf16: q, then bf16(q 2^(G - G_r)); finally the
+//                         fp32 A scratch [64][kLS] of the solver (same bytes)
+// then beta, ones, G_r, G_C and the steep flag.
+constexpr int KQ_LD = 2 * kLS;   // bf16 row stride: the A scratch reuses the bytes
+constexpr int KP_OFF_KB = C * KP_LD * 4;
+constexpr int KP_OFF_QB = 2 * C * KP_LD * 4;
+constexpr int KP_OFF_BETA = KP_OFF_QB + C * kLS * 4;
+constexpr int KP_OFF_ONE = KP_OFF_BETA + C * 4;
+constexpr int KP_OFF_GR = KP_OFF_ONE + C * 4;
+constexpr int KP_OFF_GC = KP_OFF_GR + D * 4;
+constexpr int KP_OFF_FLAG = KP_OFF_GC + D * 4;
+constexpr size_t KP_SMEM = (size_t)KP_OFF_FLAG + 16;
+static_assert(C * KQ_LD * 2 == C * kLS * 4, "the A scratch must fit the q tile");
+static_assert(2 * (KP_SMEM + 1024) <= 233472, "two preparation CTAs must fit an SM");
+
+// element (i, d) of a 64 x 128 bf16 tile stored as two swizzled 64-column images
+__device__ __forceinline__ uint32_t img_off(int i, int d) {
+    return (uint32_t)(d >> 6) * 8192u + sw128((uint32_t)i, (uint32_t)((d & 63) >> 3)) + (uint32_t)(d & 7) * 2u;
+}
+__device__ __forceinline__ void put_bf16(uint8_t *img, uint32_t off, float x) {
+    *reinterpret_cast<__nv_bfloat16 *>(img + off) = __float2bfloat16_rn(x);
+}
+// hi = bf16(x), lo = bf16(x - hi)
+__device__ __forceinline__ void put_hilo(uint8_t *hi, uint8_t *lo, uint32_t off, float x) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    *reinterpret_cast<__nv_bfloat16 *>(hi + off) = h;
+    *reinterpret_cast<__nv_bfloat16 *>(lo + off) = __float2bfloat16_rn(x - __bfloat162float(h));
+}
+
+__global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid_constant__ KdaParams p) {
+    extern __shared__ __align__(16) uint8_t smb[];
+    float *GF = reinterpret_cast<float *>(smb);
+    float *KB = reinterpret_cast<float *>(smb + KP_OFF_KB);
+    __nv_bfloat16 *QB = reinterpret_cast<__nv_bfloat16 *>(smb + KP_OFF_QB);
+    float *A = reinterpret_cast<float *>(smb + KP_OFF_QB);
+    float *beta = reinterpret_cast<float *>(smb + KP_OFF_BETA), *one = reinterpret_cast<float *>(smb + KP_OFF_ONE);
+    float *Gr = reinterpret_cast<float *>(smb + KP_OFF_GR), *GCv = reinterpret_cast<float *>(smb + KP_OFF_GC);
+    int *steep = reinterpret_cast<int *>(smb + KP_OFF_FLAG);
+    const int tid = threadIdx.x;
+    const int unit = blockIdx.x, h = unit % p.H;
+    const WyChunk ck = p.chunks[unit / p.H];
+    const int nv = ck.nv;
+    uint8_t *dst = p.wy + (size_t)unit * kKdaUnitBytes;
+    auto tok = [&](int i) { return (ck.tok0 + i) * p.H + h; };
+
+    // ---- loads: g, k, q of the chunk (padded rows: 0), every load independent
+    for (int e = tid; e < C * D / 4; e += KP_THREADS) {
+        const int i = e / (D / 4), d = 4 * (e % (D / 4));
+        float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        uint2 k2 = make_uint2(0u, 0u), q2 = make_uint2(0u, 0u);
+        if (i < nv) {
+            g4 = __ldg(reinterpret_cast<const float4 *>(p.g + (int64_t)tok(i) * D + d));
+            k2 = __ldg(reinterpret_cast<const uint2 *>(p.k + (int64_t)tok(i) * D + d));
+            q2 = __ldg(reinterpret_cast<const uint2 *>(p.q + (int64_t)tok(i) * D + d));
+        }
+        *reinterpret_cast<float4 *>(GF + i * KP_LD + d) = g4;
+        const float2 ka = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&k2.x));
+        const float2 kb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&k2.y));
+        *reinterpret_cast<float4 *>(KB + i * KP_LD + d) = make_float4(ka.x, ka.y, kb.x, kb.y);
+        *reinterpret_cast<uint2 *>(QB + i * KQ_LD + d) = q2;
+    }
+    if (tid < C) {
+        beta[tid] = tid < nv ? __bfloat162float(p.beta[tok(tid)]) : 0.f;
+        one[tid] = 1.f;
+    }
+    if (tid == 0) *steep = 0;
+    __syncthreads();
+
+    // ---- in-chunk cumulative log2 gates per key dim
+    if (tid < D) {
+        float run = 0.f;
+        int far = 0;
+        for (int i = 0; i < C; i++) {
+            run += GF[i * KP_LD + tid] * kLog2e;
+            GF[i * KP_LD + tid] = run;
+        }
+        const float gr = GF[kRef * KP_LD + tid];
+        for (int i = 0; i < C; i++) far |= fabsf(GF[i * KP_LD + tid] - gr) > kFactorBound;
+        Gr[tid] = gr;
+        GCv[tid] = run;
+        reinterpret_cast<float *>(dst + kKdaOffGC)[tid] = exp2f(run);
+        if (__any_sync(0xffffffffu, far) && (tid & 31) == 0) atomicOr(steep, 1);
+    }
+    __syncthreads();
+    const bool exact = *steep != 0;
+
+    // ---- gated tiles; unless exact, the factorised operands replace the
+    // inputs in place (thread owns column d, rows i0, i0 + 2, ...)
+    {
+        const int d = tid & (D - 1), i0 = tid >> 7;
+        const float gr = Gr[d], gc = GCv[d];
+        for (int i = i0; i < C; i += 2) {
+            const float Gi = GF[i * KP_LD + d];
+            const float kv = KB[i * KP_LD + d];
+            const float qv = __bfloat162float(QB[i * KQ_LD + d]);
+            const uint32_t off = img_off(i, d);
+            const float gi = exp2f(Gi);
+            put_hilo(dst + kKdaOffKg, dst + kKdaOffKgLo, off, kv * gi);
+            put_hilo(dst + kKdaOffKgam, dst + kKdaOffKgamLo, off, kv * exp2f(gc - Gi));
+            put_bf16(dst + kKdaOffQg, off, qv * gi);
+            if (!exact) {
+                const float e = exp2f(Gi - gr);
+                GF[i * KP_LD + d] = kv * exp2f(gr - Gi);
+                KB[i * KP_LD + d] = kv * e;
+                QB[i * KQ_LD + d] = __float2bfloat16_rn(qv * e);
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- A (strict lower, times beta_i) and P (lower incl. the diagonal):
+    // thread = one 4 x 4 block, blocks above the diagonal idle
+    const int bi = tid >> 4, bj = tid & 15;
+    float a[4][4], pp[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; r++)
+#pragma unroll
+        for (int c = 0; c < 4; c++) a[r][c] = pp[r][c] = 0.f;
+    if (bj <= bi) {
+        if (!exact) {
+            for (int d = 0; d < D; d += 4) {
+                float4 ke[4], kf[4];
+                float qe[4][4];
+#pragma unroll
+                for (int r = 0; r < 4; r++) {
+                    ke[r] = *reinterpret_cast<const float4 *>(KB + (4 * bi + r) * KP_LD + d);
+                    kf[r] = *reinterpret_cast<const float4 *>(GF + (4 * bj + r) * KP_LD + d);
+                    const uint2 q2 = *reinterpret_cast<const uint2 *>(QB + (4 * bi + r) * KQ_LD + d);
+                    const float2 qa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q2.x));
+                    const float2 qb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q2.y));
+                    qe[r][0] = qa.x; qe[r][1] = qa.y; qe[r][2] = qb.x; qe[r][3] = qb.y;
+                }
+#pragma unroll
+                for (int r = 0; r < 4; r++)
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        a[r][c] = fmaf(ke[r].x, kf[c].x, a[r][c]);
+                        a[r][c] = fmaf(ke[r].y, kf[c].y, a[r][c]);
+                        a[r][c] = fmaf(ke[r].z, kf[c].z, a[r][c]);
+                        a[r][c] = fmaf(ke[r].w, kf[c].w, a[r][c]);
+                        pp[r][c] = fmaf(qe[r][0], kf[c].x, pp[r][c]);
+                        pp[r][c] = fmaf(qe[r][1], kf[c].y, pp[r][c]);
+                        pp[r][c] = fmaf(qe[r][2], kf[c].z, pp[r][c]);
+                        pp[r][c] = fmaf(qe[r][3], kf[c].w, pp[r][c]);
+                    }
+            }
+        } else {
+            // exact exponentials per term (decays beyond 2^100 around row r)
+            for (int d = 0; d < D; d++) {
+#pragma unroll
+                for (int r = 0; r < 4; r++) {
+                    const int i = 4 * bi + r;
+                    const float Gi = GF[i * KP_LD + d], kv = KB[i * KP_LD + d];
+                    const float qv = __bfloat162float(QB[i * KQ_LD + d]);
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        const int j = 4 * bj + c;
+                        if (j > i) continue;
+                        const float lam = exp2f(Gi - GF[j * KP_LD + d]) * KB[j * KP_LD + d];
+                        a[r][c] = fmaf(kv, lam, a[r][c]);
+                        pp[r][c] = fmaf(qv, lam, pp[r][c]);
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();   // the q tile's bytes become the A scratch
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+        const int i = 4 * bi + r;
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            const int j = 4 * bj + c;
+            A[i * kLS + j] = j < i ? beta[i] * a[r][c] : 0.f;
+            put_bf16(dst + kKdaOffP, sw128((uint32_t)i, (uint32_t)(j >> 3)) + (uint32_t)(j & 7) * 2u,
+                     j <= i ? pp[r][c] : 0.f);
+        }
+    }
+    __syncthreads();
+    // ---- T = (I + A)^-1 -> T', T'' (= T' here, hi and lo)
+    if (tid < 32) solve_unit(A, dst, beta, one);
+}
+
+}  // namespace
+
+int launch_tc_kda_prep(const cpdr_ctx *c, const void *k, const void *q, const void *beta, const float *g,
+                       void *wy, void *stream) {
+    const auto &pl = c->plan;
+    const int64_t units = (int64_t)pl.wy_chunks.size() * pl.H;
+    if (units == 0) return 0;
+    if (units > (int64_t)0x7fffffff) return (int)cudaErrorInvalidValue;
+    KdaParams prm{};
+    prm.chunks = c->dev.wy_chunks;
+    prm.k = (const __nv_bfloat16 *)k;
+    prm.q = (const __nv_bfloat16 *)q;
+    prm.beta = (const __nv_bfloat16 *)beta;
+    prm.g = g;
+    prm.wy = (uint8_t *)wy;
+    prm.H = pl.H;
+    cudaError_t e = cudaFuncSetAttribute(tc_kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)KP_SMEM);
+    if (e != cudaSuccess) return (int)e;
+    tc_kda_prep_kernel<<<(unsigned)units, KP_THREADS, KP_SMEM, (cudaStream_t)stream>>>(prm);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace cpdr

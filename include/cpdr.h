@@ -182,11 +182,19 @@ cpdr_status cpdr_plan_counts(const cpdr_ctx *ctx, int32_t out[8]);
  * cpdr_wy_bytes() gives the workspace size: 24 KiB per (chunk, head) on the
  * tensor-core path (bf16, dk = dv = 128, scalar gate), 0 otherwise (then
  * this call does nothing and `wy` may be NULL).
- * In: k, beta, gate (device).  Out: wy (device, caller-owned).
+ * Per-dim gate (KDA) on the tensor-core path: the gate cannot be applied
+ * inside the chunk recurrence as a scalar, so this step also pre-gates the
+ * operands, as [FLA-CP] §2.3 does at the WY stage (kg = k 2^(g_last - g),
+ * qg = q 2^g): per (chunk, head) it writes, after the three tiles above
+ * (built with gamma = 1), the per-dim chunk decay 2^(G_C), the bf16 tiles
+ * k 2^G (hi, lo), k 2^(G_C - G) (hi, lo), q 2^G and the masked intra-chunk
+ * product (Q K^T ⊙ Lambda) -- 113 KiB per (chunk, head).
+ * In: q (device; read only for the per-dim gate, else may be NULL), k,
+ * beta, gate (device).  Out: wy (device, caller-owned).
  */
 cpdr_status cpdr_wy_bytes(const cpdr_ctx *ctx, size_t *bytes);
-cpdr_status cpdr_wy_build(const cpdr_ctx *ctx, const void *k, const void *beta, const float *gate,
-                          void *wy, void *stream);
+cpdr_status cpdr_wy_build(const cpdr_ctx *ctx, const void *q, const void *k, const void *beta,
+                          const float *gate, void *wy, void *stream);
 
 /*
  * Pre-process ([FLA-CP] §2.1-§2.3, pre_process_fwd in its Code Flow of §4):

@@ -89,6 +89,11 @@ def test_wy_workspace_covers_every_chunk_of_every_fragment(cpdr_lib, kw):
     simt = make(**kw, force_simt=True)
     assert simt.wy_bytes() == 0
     assert make(**dict(kw, dtype="fp32")).wy_bytes() == 0
+    # per-dim gate: the WY tiles plus the pre-gated operand tiles, 113 KiB
+    kda = make(**dict(kw, gate="kda"))
+    assert kda.counts()["tc"] == 1 and kda.wy_bytes() == chunks * kw["H"] * 113 * 1024
+    # grouped query heads with the per-dim gate run on the CUDA cores
+    assert make(**dict(kw, gate="kda", Hq=2 * kw["H"])).wy_bytes() == 0
 
 
 def test_selftest_rejects_host_only_context(cpdr_lib):

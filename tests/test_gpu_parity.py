@@ -106,7 +106,7 @@ def test_steep_decay(dtype):
     print(compare(run_gpu(inp), run_oracle(inp), inp))
 
 
-@pytest.mark.parametrize("name", ["gdn_bf16_b2_t8192_h16_d128_r8"])
+@pytest.mark.parametrize("name", ["gdn_bf16_b2_t8192_h16_d128_r8", "kda_bf16_t32768_h32_d128_r16"])
 def test_fp32_cuda_core_path_cross_check(name):
     inp = gen(name, B=1, T=2048, H=4)
     print(name, compare(run_gpu(inp, force_simt=True), run_oracle(inp), inp))
