@@ -17,10 +17,13 @@
 // (k 2^(G_r - G)) (the q factor rounded to bf16: P is a bf16 tile); a unit
 // whose in-chunk decay exceeds 2^100 either way of row r takes exact
 // per-term exponentials instead.  One CTA per unit, two per SM (CUDA
-// cores): coalesced loads, column scans, the gated tiles, A and P, then one
-// warp solves T with the scalar-gate path's solver.
+// cores): coalesced loads, column scans, the gated tiles, A and P; then a
+// second kernel solves T, one warp per unit with the scalar-gate path's
+// solver, many units per SM at once.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "cpdr_internal.hpp"
 #include "tc_common.cuh"
@@ -49,19 +52,16 @@ struct KdaParams {
 // Shared memory (two CTAs per SM):
 //   GF  [64][KP_LD] fp32: G (log2 cumsum), then k 2^(G_r - G)      ("KF")
 //   KB  [64][KP_LD] fp32: k, then k 2^(G - G_r)                     ("KE")
-//   QB  [64][KQ_LD] bf16: q, then bf16(q 2^(G - G_r)); finally the
-//                         fp32 A scratch [64][kLS] of the solver (same bytes)
-// then beta, ones, G_r, G_C and the steep flag.
-constexpr int KQ_LD = 2 * kLS;   // bf16 row stride: the A scratch reuses the bytes
+//   QB  [64][KQ_LD] bf16: q, then bf16(q 2^(G - G_r))
+// then beta, G_r, G_C and the steep flag.
+constexpr int KQ_LD = D + 8;     // bf16 row stride (16-byte rows, offset banks)
 constexpr int KP_OFF_KB = C * KP_LD * 4;
 constexpr int KP_OFF_QB = 2 * C * KP_LD * 4;
-constexpr int KP_OFF_BETA = KP_OFF_QB + C * kLS * 4;
-constexpr int KP_OFF_ONE = KP_OFF_BETA + C * 4;
-constexpr int KP_OFF_GR = KP_OFF_ONE + C * 4;
+constexpr int KP_OFF_BETA = KP_OFF_QB + C * KQ_LD * 2;
+constexpr int KP_OFF_GR = KP_OFF_BETA + C * 4;
 constexpr int KP_OFF_GC = KP_OFF_GR + D * 4;
 constexpr int KP_OFF_FLAG = KP_OFF_GC + D * 4;
 constexpr size_t KP_SMEM = (size_t)KP_OFF_FLAG + 16;
-static_assert(C * KQ_LD * 2 == C * kLS * 4, "the A scratch must fit the q tile");
 static_assert(2 * (KP_SMEM + 1024) <= 233472, "two preparation CTAs must fit an SM");
 
 // element (i, d) of a 64 x 128 bf16 tile stored as two swizzled 64-column images
@@ -83,8 +83,7 @@ __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid
     float *GF = reinterpret_cast<float *>(smb);
     float *KB = reinterpret_cast<float *>(smb + KP_OFF_KB);
     __nv_bfloat16 *QB = reinterpret_cast<__nv_bfloat16 *>(smb + KP_OFF_QB);
-    float *A = reinterpret_cast<float *>(smb + KP_OFF_QB);
-    float *beta = reinterpret_cast<float *>(smb + KP_OFF_BETA), *one = reinterpret_cast<float *>(smb + KP_OFF_ONE);
+    float *beta = reinterpret_cast<float *>(smb + KP_OFF_BETA);
     float *Gr = reinterpret_cast<float *>(smb + KP_OFF_GR), *GCv = reinterpret_cast<float *>(smb + KP_OFF_GC);
     int *steep = reinterpret_cast<int *>(smb + KP_OFF_FLAG);
     const int tid = threadIdx.x;
@@ -110,10 +109,7 @@ __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid
         *reinterpret_cast<float4 *>(KB + i * KP_LD + d) = make_float4(ka.x, ka.y, kb.x, kb.y);
         *reinterpret_cast<uint2 *>(QB + i * KQ_LD + d) = q2;
     }
-    if (tid < C) {
-        beta[tid] = tid < nv ? __bfloat162float(p.beta[tok(tid)]) : 0.f;
-        one[tid] = 1.f;
-    }
+    if (tid < C) beta[tid] = tid < nv ? __bfloat162float(p.beta[tok(tid)]) : 0.f;
     if (tid == 0) *steep = 0;
     __syncthreads();
 
@@ -160,76 +156,104 @@ __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid
     __syncthreads();
 
     // ---- A (strict lower, times beta_i) and P (lower incl. the diagonal):
-    // thread = one 4 x 4 block, blocks above the diagonal idle
+    // thread (bi, bj) owns rows bi + 16 r and columns bj + 16 c (r, c < 4),
+    // so the 16 column rows a warp reads are consecutive (no bank conflicts)
     const int bi = tid >> 4, bj = tid & 15;
     float a[4][4], pp[4][4];
 #pragma unroll
     for (int r = 0; r < 4; r++)
 #pragma unroll
         for (int c = 0; c < 4; c++) a[r][c] = pp[r][c] = 0.f;
-    if (bj <= bi) {
-        if (!exact) {
-            for (int d = 0; d < D; d += 4) {
-                float4 ke[4], kf[4];
-                float qe[4][4];
+    if (!exact) {
+        for (int d = 0; d < D; d += 4) {
+            float4 ke[4], kf[4];
+            float qe[4][4];
 #pragma unroll
-                for (int r = 0; r < 4; r++) {
-                    ke[r] = *reinterpret_cast<const float4 *>(KB + (4 * bi + r) * KP_LD + d);
-                    kf[r] = *reinterpret_cast<const float4 *>(GF + (4 * bj + r) * KP_LD + d);
-                    const uint2 q2 = *reinterpret_cast<const uint2 *>(QB + (4 * bi + r) * KQ_LD + d);
-                    const float2 qa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q2.x));
-                    const float2 qb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q2.y));
-                    qe[r][0] = qa.x; qe[r][1] = qa.y; qe[r][2] = qb.x; qe[r][3] = qb.y;
-                }
-#pragma unroll
-                for (int r = 0; r < 4; r++)
-#pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        a[r][c] = fmaf(ke[r].x, kf[c].x, a[r][c]);
-                        a[r][c] = fmaf(ke[r].y, kf[c].y, a[r][c]);
-                        a[r][c] = fmaf(ke[r].z, kf[c].z, a[r][c]);
-                        a[r][c] = fmaf(ke[r].w, kf[c].w, a[r][c]);
-                        pp[r][c] = fmaf(qe[r][0], kf[c].x, pp[r][c]);
-                        pp[r][c] = fmaf(qe[r][1], kf[c].y, pp[r][c]);
-                        pp[r][c] = fmaf(qe[r][2], kf[c].z, pp[r][c]);
-                        pp[r][c] = fmaf(qe[r][3], kf[c].w, pp[r][c]);
-                    }
+            for (int r = 0; r < 4; r++) {
+                ke[r] = *reinterpret_cast<const float4 *>(KB + (bi + 16 * r) * KP_LD + d);
+                kf[r] = *reinterpret_cast<const float4 *>(GF + (bj + 16 * r) * KP_LD + d);
+                const uint2 q2 = *reinterpret_cast<const uint2 *>(QB + (bi + 16 * r) * KQ_LD + d);
+                const float2 qa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q2.x));
+                const float2 qb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q2.y));
+                qe[r][0] = qa.x; qe[r][1] = qa.y; qe[r][2] = qb.x; qe[r][3] = qb.y;
             }
-        } else {
-            // exact exponentials per term (decays beyond 2^100 around row r)
-            for (int d = 0; d < D; d++) {
 #pragma unroll
-                for (int r = 0; r < 4; r++) {
-                    const int i = 4 * bi + r;
-                    const float Gi = GF[i * KP_LD + d], kv = KB[i * KP_LD + d];
-                    const float qv = __bfloat162float(QB[i * KQ_LD + d]);
+            for (int r = 0; r < 4; r++)
 #pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        const int j = 4 * bj + c;
-                        if (j > i) continue;
-                        const float lam = exp2f(Gi - GF[j * KP_LD + d]) * KB[j * KP_LD + d];
-                        a[r][c] = fmaf(kv, lam, a[r][c]);
-                        pp[r][c] = fmaf(qv, lam, pp[r][c]);
-                    }
+                for (int c = 0; c < 4; c++) {
+                    a[r][c] = fmaf(ke[r].x, kf[c].x, a[r][c]);
+                    a[r][c] = fmaf(ke[r].y, kf[c].y, a[r][c]);
+                    a[r][c] = fmaf(ke[r].z, kf[c].z, a[r][c]);
+                    a[r][c] = fmaf(ke[r].w, kf[c].w, a[r][c]);
+                    pp[r][c] = fmaf(qe[r][0], kf[c].x, pp[r][c]);
+                    pp[r][c] = fmaf(qe[r][1], kf[c].y, pp[r][c]);
+                    pp[r][c] = fmaf(qe[r][2], kf[c].z, pp[r][c]);
+                    pp[r][c] = fmaf(qe[r][3], kf[c].w, pp[r][c]);
+                }
+        }
+    } else {
+        // exact exponentials per term (decays beyond 2^100 around row r)
+        for (int d = 0; d < D; d++) {
+#pragma unroll
+            for (int r = 0; r < 4; r++) {
+                const int i = bi + 16 * r;
+                const float Gi = GF[i * KP_LD + d], kv = KB[i * KP_LD + d];
+                const float qv = __bfloat162float(QB[i * KQ_LD + d]);
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const int j = bj + 16 * c;
+                    if (j > i) continue;
+                    const float lam = exp2f(Gi - GF[j * KP_LD + d]) * KB[j * KP_LD + d];
+                    a[r][c] = fmaf(kv, lam, a[r][c]);
+                    pp[r][c] = fmaf(qv, lam, pp[r][c]);
                 }
             }
         }
     }
-    __syncthreads();   // the q tile's bytes become the A scratch
+    // A (fp32, row-major 64 x 64) and beta go into the unit's first tiles,
+    // which the solve reads and then overwrites with T', hi(T''), lo(T'')
+    float *Ag = reinterpret_cast<float *>(dst);
 #pragma unroll
     for (int r = 0; r < 4; r++) {
-        const int i = 4 * bi + r;
+        const int i = bi + 16 * r;
 #pragma unroll
         for (int c = 0; c < 4; c++) {
-            const int j = 4 * bj + c;
-            A[i * kLS + j] = j < i ? beta[i] * a[r][c] : 0.f;
+            const int j = bj + 16 * c;
+            Ag[i * C + j] = j < i ? beta[i] * a[r][c] : 0.f;
             put_bf16(dst + kKdaOffP, sw128((uint32_t)i, (uint32_t)(j >> 3)) + (uint32_t)(j & 7) * 2u,
                      j <= i ? pp[r][c] : 0.f);
         }
     }
-    __syncthreads();
-    // ---- T = (I + A)^-1 -> T', T'' (= T' here, hi and lo)
-    if (tid < 32) solve_unit(A, dst, beta, one);
+    if (tid < C) reinterpret_cast<float *>(dst + 2 * kWyTileBytes)[tid] = beta[tid];
+}
+
+// T = (I + A)^-1 of every unit, one warp per unit (persistent warps): A and
+// beta from the unit (written above) into this warp's scratch, then the
+// solver overwrites the unit's first three tiles with T', hi(T''), lo(T'').
+constexpr int KS_WARPS = 4;
+constexpr size_t KS_SCRATCH = (size_t)C * kLS * 4 + 2 * C * 4;   // A, beta, ones
+__global__ void __launch_bounds__(32 * KS_WARPS) tc_kda_solve_kernel(uint8_t *wy, int n_units) {
+    extern __shared__ __align__(16) uint8_t sms[];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *S = reinterpret_cast<float *>(sms + w * KS_SCRATCH);
+    float *beta = S + C * kLS, *one = beta + C;
+    one[lane] = 1.f;
+    one[32 + lane] = 1.f;
+    for (int unit = blockIdx.x * KS_WARPS + w; unit < n_units; unit += gridDim.x * KS_WARPS) {
+        uint8_t *dst = wy + (size_t)unit * kKdaUnitBytes;
+        const float4 *Ag = reinterpret_cast<const float4 *>(dst);
+#pragma unroll 4
+        for (int e = lane; e < C * C / 4; e += 32) {
+            const int i = e / (C / 4), j = 4 * (e % (C / 4));
+            *reinterpret_cast<float4 *>(S + i * kLS + j) = Ag[e];
+        }
+        const float *bg = reinterpret_cast<const float *>(dst + 2 * kWyTileBytes);
+        beta[lane] = bg[lane];
+        beta[32 + lane] = bg[32 + lane];
+        __syncwarp();
+        solve_unit(S, dst, beta, one);
+        __syncwarp();
+    }
 }
 
 }  // namespace
@@ -252,6 +276,18 @@ int launch_tc_kda_prep(const cpdr_ctx *c, const void *k, const void *q, const vo
                                          (int)KP_SMEM);
     if (e != cudaSuccess) return (int)e;
     tc_kda_prep_kernel<<<(unsigned)units, KP_THREADS, KP_SMEM, (cudaStream_t)stream>>>(prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    const size_t ssm = KS_WARPS * KS_SCRATCH;
+    e = cudaFuncSetAttribute(tc_kda_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
+    if (e != cudaSuccess) return (int)e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+    const int64_t blocks = (units + KS_WARPS - 1) / KS_WARPS;
+    const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * 3);
+    tc_kda_solve_kernel<<<grid, 32 * KS_WARPS, ssm, (cudaStream_t)stream>>>((uint8_t *)wy, (int)units);
     return (int)cudaGetLastError();
 }
 
