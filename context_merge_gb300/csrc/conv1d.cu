@@ -8,10 +8,12 @@
 // tile, at the positions the planner's halo table lists (another part of the
 // zigzag layout, or earlier parts when parts are shorter than W - 1).
 //
-// HBM-bound streaming kernel: each thread owns 4 channels (8 bytes of bf16,
-// 16 of fp32) of one tile of up to 64 tokens, keeps the W - 1 previous inputs
+// HBM-bound streaming kernel: each thread owns 2 channels (4 bytes of bf16,
+// 8 of fp32) of one tile of up to 64 tokens, keeps the W - 1 previous inputs
 // in registers, and reads each input and writes each output once.  Loads go
-// out in groups of 8 tokens, the next group before the current one is used.
+// out in groups of 16 tokens, the next group before the current one is used;
+// few registers per thread keep the SM full of warps (the loads in flight
+// are what bounds a streaming kernel).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,57 +23,44 @@ namespace cpdr {
 namespace {
 
 constexpr int kConvThreads = 256;
-constexpr int kVec = 4;          // channels per thread
-constexpr int kAhead = 8;        // tokens per load group (two groups in flight)
+constexpr int kVec = 2;          // channels per thread
+constexpr int kAhead = 16;       // tokens per load group (two groups in flight)
 
-struct Vec4 {
+struct Vec2 {
     float v[kVec];
 };
 
-// 4 channels as loaded (raw bits), widened to fp32 where they are used
+// 2 channels as loaded (raw bits), widened to fp32 where they are used
 template <typename T>
-struct Raw4;
+struct Raw2;
 template <>
-struct Raw4<float> {
-    float4 a;
+struct Raw2<float> {
+    float2 a;
 };
 template <>
-struct Raw4<__nv_bfloat16> {
-    uint2 a;
+struct Raw2<__nv_bfloat16> {
+    uint32_t a;
 };
 
-__device__ __forceinline__ Raw4<float> load_raw(const float *p) {
-    return Raw4<float>{__ldg(reinterpret_cast<const float4 *>(p))};
+__device__ __forceinline__ Raw2<float> load_raw(const float *p) {
+    return Raw2<float>{__ldg(reinterpret_cast<const float2 *>(p))};
 }
-__device__ __forceinline__ Raw4<__nv_bfloat16> load_raw(const __nv_bfloat16 *p) {
-    return Raw4<__nv_bfloat16>{__ldg(reinterpret_cast<const uint2 *>(p))};
+__device__ __forceinline__ Raw2<__nv_bfloat16> load_raw(const __nv_bfloat16 *p) {
+    return Raw2<__nv_bfloat16>{__ldg(reinterpret_cast<const unsigned int *>(p))};
 }
-__device__ __forceinline__ Vec4 widen(const Raw4<float> &r) { return Vec4{{r.a.x, r.a.y, r.a.z, r.a.w}}; }
-__device__ __forceinline__ Vec4 widen(const Raw4<__nv_bfloat16> &r) {
-    const uint32_t w[2] = {r.a.x, r.a.y};
-    Vec4 o;
-#pragma unroll
-    for (int i = 0; i < 2; i++) {
-        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
-        const float2 f = __bfloat1622float2(h);
-        o.v[2 * i] = f.x;
-        o.v[2 * i + 1] = f.y;
-    }
-    return o;
+__device__ __forceinline__ Vec2 widen(const Raw2<float> &r) { return Vec2{{r.a.x, r.a.y}}; }
+__device__ __forceinline__ Vec2 widen(const Raw2<__nv_bfloat16> &r) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.a));
+    return Vec2{{f.x, f.y}};
 }
 template <typename T>
-__device__ __forceinline__ Vec4 load4(const T *p) { return widen(load_raw(p)); }
-__device__ __forceinline__ void store4(float *p, const Vec4 &x) {
-    *reinterpret_cast<float4 *>(p) = make_float4(x.v[0], x.v[1], x.v[2], x.v[3]);
+__device__ __forceinline__ Vec2 load2(const T *p) { return widen(load_raw(p)); }
+__device__ __forceinline__ void store2(float *p, const Vec2 &x) {
+    *reinterpret_cast<float2 *>(p) = make_float2(x.v[0], x.v[1]);
 }
-__device__ __forceinline__ void store4(__nv_bfloat16 *p, const Vec4 &x) {
-    uint32_t w[2];
-#pragma unroll
-    for (int i = 0; i < 2; i++) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(x.v[2 * i], x.v[2 * i + 1]);
-        w[i] = *reinterpret_cast<const uint32_t *>(&h);
-    }
-    *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
+__device__ __forceinline__ void store2(__nv_bfloat16 *p, const Vec2 &x) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x.v[0], x.v[1]);
+    *reinterpret_cast<__nv_bfloat162 *>(p) = h;
 }
 
 // SiLU z * sigmoid(z) = z / (1 + e^-z); the fast divide returns 0 once the
@@ -89,7 +78,7 @@ conv1d_kernel(const ConvTile *__restrict__ tiles, const int64_t *__restrict__ ha
     const T *xp = x + tl.tok0 * channels + c0;
     T *yp = y + tl.tok0 * channels + c0;
     // first load group in flight before anything else
-    Raw4<T> raw[2][kAhead];
+    Raw2<T> raw[2][kAhead];
 #pragma unroll
     for (int u = 0; u < kAhead; u++)
         if (u < tl.n) raw[0][u] = load_raw(xp + (int64_t)u * channels);
@@ -102,7 +91,7 @@ conv1d_kernel(const ConvTile *__restrict__ tiles, const int64_t *__restrict__ ha
     }
     // the W - 1 inputs before the tile, oldest first
     constexpr int NW = W > 1 ? W - 1 : 1;
-    Vec4 win[NW];
+    Vec2 win[NW];
 #pragma unroll
     for (int i = 0; i < NW; i++) {
         int64_t src = -1;
@@ -110,8 +99,8 @@ conv1d_kernel(const ConvTile *__restrict__ tiles, const int64_t *__restrict__ ha
             if (tl.halo == kHaloMemory) src = tl.tok0 - (W - 1) + i;
             else if (tl.halo >= 0) src = __ldg(halo + (int64_t)tl.halo * (W - 1) + i);
         }
-        if (src >= 0) win[i] = load4(x + src * channels + c0);
-        else win[i] = Vec4{{0.f, 0.f, 0.f, 0.f}};
+        if (src >= 0) win[i] = load2(x + src * channels + c0);
+        else win[i] = Vec2{{0.f, 0.f}};
     }
     // groups of kAhead tokens; group g + 1 is loaded before group g is computed
 #pragma unroll 1
@@ -127,8 +116,8 @@ conv1d_kernel(const ConvTile *__restrict__ tiles, const int64_t *__restrict__ ha
 #pragma unroll
             for (int u = 0; u < kAhead; u++) {
                 if (g0 + u < tl.n) {
-                    const Vec4 cur = widen(raw[half][u]);
-                    Vec4 out;
+                    const Vec2 cur = widen(raw[half][u]);
+                    Vec2 out;
 #pragma unroll
                     for (int j = 0; j < kVec; j++) {
                         float acc = b[j];
@@ -137,7 +126,7 @@ conv1d_kernel(const ConvTile *__restrict__ tiles, const int64_t *__restrict__ ha
                         acc = fmaf(w[j][W - 1], cur.v[j], acc);
                         out.v[j] = ACT ? silu(acc) : acc;
                     }
-                    store4(yp + (int64_t)(g0 + u) * channels, out);
+                    store2(yp + (int64_t)(g0 + u) * channels, out);
 #pragma unroll
                     for (int i = 0; i + 1 < W - 1; i++) win[i] = win[i + 1];
                     if (W > 1) win[NW - 1] = cur;
