@@ -49,10 +49,12 @@ void free_tables(cpdr::DeviceTables &t) {
 }
 
 void free_streams(cpdr_ctx *c) {
-    if (c->ev_fork) cudaEventDestroy((cudaEvent_t)c->ev_fork);
-    if (c->ev_join) cudaEventDestroy((cudaEvent_t)c->ev_join);
+    for (void *e : {c->ev_fork, c->ev_join, c->ev_start, c->ev_in0, c->ev_in1, c->ev_in2})
+        if (e) cudaEventDestroy((cudaEvent_t)e);
     if (c->aux_stream) cudaStreamDestroy((cudaStream_t)c->aux_stream);
+    if (c->copy_stream) cudaStreamDestroy((cudaStream_t)c->copy_stream);
     c->aux_stream = c->ev_fork = c->ev_join = nullptr;
+    c->copy_stream = c->ev_start = c->ev_in0 = c->ev_in1 = c->ev_in2 = nullptr;
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -164,6 +166,17 @@ cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
             c->aux_stream = aux;
             c->ev_fork = ef;
             c->ev_join = ej;
+        }
+        if (e == cudaSuccess) {
+            cudaStream_t cs = nullptr;
+            e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+            c->copy_stream = cs;
+            void **evs[4] = {&c->ev_start, &c->ev_in0, &c->ev_in1, &c->ev_in2};
+            for (int i = 0; i < 4 && e == cudaSuccess; i++) {
+                cudaEvent_t ev = nullptr;
+                e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+                *evs[i] = ev;
+            }
         }
         if (e != cudaSuccess) {
             free_tables(t);
@@ -346,17 +359,36 @@ cpdr_status cpdr_forward_host(const cpdr_ctx *c, const void *q, const void *k, c
     float *dfin = (float *)take(s.fin);
     const size_t nwy = cpdr::wy_bytes(c);
     void *dwy = nwy ? take(nwy) : nullptr;
-    cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dq, q, s.q, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k, s.k, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v, s.v, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(db, beta, s.beta, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dg, gate, s.gate, cudaMemcpyHostToDevice, st);
+    cudaStream_t st = (cudaStream_t)stream, cs = (cudaStream_t)c->copy_stream;
+    // The inputs go over on the copy stream in the order the stages need
+    // them -- k, beta, gate (the WY build; q too for the per-dim gate), then
+    // v (the pre-process), then q (the forward) -- and each stage on `stream`
+    // waits only for its own inputs, so the WY build, pre-process and merge
+    // run while the later inputs are still in transit.  The copy stream
+    // starts after everything enqueued on `stream` before this call.
+    const bool kda = c->plan.gate_kind == CPDR_GATE_PER_DIM;
+    cudaEvent_t ev_start = (cudaEvent_t)c->ev_start, ev_a = (cudaEvent_t)c->ev_in0,
+                ev_b = (cudaEvent_t)c->ev_in1, ev_c = (cudaEvent_t)c->ev_in2;
+    cudaError_t e = cudaEventRecord(ev_start, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev_start, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k, s.k, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(db, beta, s.beta, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dg, gate, s.gate, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess && kda) e = cudaMemcpyAsync(dq, q, s.q, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_a, cs);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v, s.v, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_b, cs);
+    if (e == cudaSuccess && !kda) e = cudaMemcpyAsync(dq, q, s.q, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_c, cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_a, 0);
     if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: host-to-device copy");
     CPDR_TRY(cpdr_wy_build(c, dq, dk, db, dg, dwy, stream));
+    e = cudaStreamWaitEvent(st, ev_b, 0);
+    if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: stream wait");
     CPDR_TRY(cpdr_preprocess(c, dk, dv, db, dg, dwy, dse, dm, stream));
     CPDR_TRY(cpdr_merge(c, dse, dm, dsi, stream));
+    e = cudaStreamWaitEvent(st, ev_c, 0);
+    if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: stream wait");
     CPDR_TRY(cpdr_fwd(c, dq, dk, dv, db, dg, dwy, dsi, dout, dfin, stream));
     e = cudaMemcpyAsync(o, dout, s.o, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess && final_state) e = cudaMemcpyAsync(final_state, dfin, s.fin, cudaMemcpyDeviceToHost, st);

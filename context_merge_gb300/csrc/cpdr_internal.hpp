@@ -124,6 +124,10 @@ struct cpdr_ctx {
     // back into the caller's stream with two events (created with the context)
     void *aux_stream = nullptr;
     void *ev_fork = nullptr, *ev_join = nullptr;
+    // host-buffer path: a copy stream for the host-to-device copies and the
+    // events that let compute start on the inputs that have arrived
+    void *copy_stream = nullptr;
+    void *ev_start = nullptr, *ev_in0 = nullptr, *ev_in1 = nullptr, *ev_in2 = nullptr;
 };
 
 namespace cpdr {
