@@ -43,18 +43,24 @@ void free_tables(cpdr::DeviceTables &t) {
     cudaFree(t.frag_chunk0);
     cudaFree(t.wy_chunks);
     cudaFree(t.conv_tiles);
+    cudaFree(t.host_items);
     cudaFree(t.conv_halo);
     cudaFree(t.status);
     t = cpdr::DeviceTables();
 }
 
 void free_streams(cpdr_ctx *c) {
-    for (void *e : {c->ev_fork, c->ev_join, c->ev_start, c->ev_in0, c->ev_in1, c->ev_in2})
+    for (void *e : {c->ev_fork, c->ev_join})
         if (e) cudaEventDestroy((cudaEvent_t)e);
+    for (void *&e : c->host_ev) {
+        if (e) cudaEventDestroy((cudaEvent_t)e);
+        e = nullptr;
+    }
     if (c->aux_stream) cudaStreamDestroy((cudaStream_t)c->aux_stream);
     if (c->copy_stream) cudaStreamDestroy((cudaStream_t)c->copy_stream);
+    if (c->out_stream) cudaStreamDestroy((cudaStream_t)c->out_stream);
     c->aux_stream = c->ev_fork = c->ev_join = nullptr;
-    c->copy_stream = c->ev_start = c->ev_in0 = c->ev_in1 = c->ev_in2 = nullptr;
+    c->copy_stream = c->out_stream = nullptr;
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -154,6 +160,7 @@ cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
         if (e == cudaSuccess) e = upload(&t.frag_chunk0, p.frag_chunk0);
         if (e == cudaSuccess) e = upload(&t.wy_chunks, p.wy_chunks);
         if (e == cudaSuccess) e = upload(&t.conv_tiles, p.conv_tiles);
+        if (e == cudaSuccess) e = upload(&t.host_items, p.host_items);
         if (e == cudaSuccess) e = upload(&t.conv_halo, p.conv_halo);
         if (e == cudaSuccess) e = cudaMalloc((void **)&t.status, 64);
         if (e == cudaSuccess) e = cudaMemset(t.status, 0, 64);
@@ -168,14 +175,15 @@ cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
             c->ev_join = ej;
         }
         if (e == cudaSuccess) {
-            cudaStream_t cs = nullptr;
+            cudaStream_t cs = nullptr, os = nullptr;
             e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
             c->copy_stream = cs;
-            void **evs[4] = {&c->ev_start, &c->ev_in0, &c->ev_in1, &c->ev_in2};
-            for (int i = 0; i < 4 && e == cudaSuccess; i++) {
+            if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&os, cudaStreamNonBlocking);
+            c->out_stream = os;
+            for (int i = 0; i < cpdr_ctx::kHostEvents && e == cudaSuccess; i++) {
                 cudaEvent_t ev = nullptr;
                 e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-                *evs[i] = ev;
+                c->host_ev[i] = ev;
             }
         }
         if (e != cudaSuccess) {
@@ -295,8 +303,10 @@ cpdr_status cpdr_fwd(const cpdr_ctx *c, const void *q, const void *k, const void
     CPDR_TRY(check_ptr(S_init, "S_init"));
     CPDR_TRY(check_ptr(o, "o"));
     CPDR_TRY(check_ptr(final_state, "final_state", true));
-    int rc = c->use_tc ? cpdr::launch_tc_fwd(c, q, k, v, gate, wy, S_init, o, final_state, stream)
-                       : cpdr::launch_simt_fwd(c, q, k, v, beta, gate, S_init, o, final_state, stream);
+    const int n = (int)c->plan.frags.size();
+    int rc = c->use_tc ? cpdr::launch_tc_fwd(c, c->dev.fwd_order, n, q, k, v, gate, wy, S_init, o, final_state, stream)
+                       : cpdr::launch_simt_fwd(c, c->dev.fwd_order, n, q, k, v, beta, gate, S_init, o, final_state,
+                                               stream);
     CPDR_TRY(launch_rc(rc, "cpdr_fwd"));
     return launch_rc(cpdr::launch_zero_segments(c, nullptr, nullptr, nullptr, final_state, 2, stream),
                      "cpdr_fwd: zero fill");
@@ -359,40 +369,69 @@ cpdr_status cpdr_forward_host(const cpdr_ctx *c, const void *q, const void *k, c
     float *dfin = (float *)take(s.fin);
     const size_t nwy = cpdr::wy_bytes(c);
     void *dwy = nwy ? take(nwy) : nullptr;
-    cudaStream_t st = (cudaStream_t)stream, cs = (cudaStream_t)c->copy_stream;
-    // The inputs go over on the copy stream in the order the stages need
-    // them -- k, beta, gate (the WY build; q too for the per-dim gate), then
-    // v (the pre-process), then q (the forward) -- and each stage on `stream`
-    // waits only for its own inputs, so the WY build, pre-process and merge
-    // run while the later inputs are still in transit.  The copy stream
-    // starts after everything enqueued on `stream` before this call.
-    const bool kda = c->plan.gate_kind == CPDR_GATE_PER_DIM;
-    cudaEvent_t ev_start = (cudaEvent_t)c->ev_start, ev_a = (cudaEvent_t)c->ev_in0,
-                ev_b = (cudaEvent_t)c->ev_in1, ev_c = (cudaEvent_t)c->ev_in2;
-    cudaError_t e = cudaEventRecord(ev_start, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev_start, 0);
+    cudaStream_t st = (cudaStream_t)stream, cs = (cudaStream_t)c->copy_stream, os = (cudaStream_t)c->out_stream;
+    // A pipeline over three streams.  The inputs go over on the copy stream
+    // in the order the stages need them -- k, beta, gate (the WY build; q
+    // too for the per-dim gate), then v (the pre-process), then q group by
+    // group -- and each stage on `stream` waits only for its own inputs: the
+    // WY build, pre-process and merge run while v and q are in transit, the
+    // forward runs group by group (kHostParts groups of consecutive tokens)
+    // as q arrives, and each group's o goes back on the output stream while
+    // the next group runs.  The copy stream starts after everything enqueued
+    // on `stream` before the call; `stream` ends after the last copy back.
+    const auto &pl = c->plan;
+    const bool kda = pl.gate_kind == CPDR_GATE_PER_DIM;
+    auto ev = [&](int i) { return (cudaEvent_t)c->host_ev[i]; };
+    constexpr int E_START = 0, E_IN0 = 1, E_IN1 = 2, E_OUT = 3, E_Q = 4, E_F = 4 + cpdr::kHostParts;
+    const size_t q_tok = s.q / ((size_t)pl.B * (size_t)pl.T), o_tok = s.o / ((size_t)pl.B * (size_t)pl.T);
+    cudaError_t e = cudaEventRecord(ev(E_START), st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev(E_START), 0);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k, s.k, cudaMemcpyHostToDevice, cs);
     if (e == cudaSuccess) e = cudaMemcpyAsync(db, beta, s.beta, cudaMemcpyHostToDevice, cs);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dg, gate, s.gate, cudaMemcpyHostToDevice, cs);
     if (e == cudaSuccess && kda) e = cudaMemcpyAsync(dq, q, s.q, cudaMemcpyHostToDevice, cs);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_a, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(ev(E_IN0), cs);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v, s.v, cudaMemcpyHostToDevice, cs);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_b, cs);
-    if (e == cudaSuccess && !kda) e = cudaMemcpyAsync(dq, q, s.q, cudaMemcpyHostToDevice, cs);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_c, cs);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_a, 0);
+    if (e == cudaSuccess) e = cudaEventRecord(ev(E_IN1), cs);
+    for (int g = 0; g < cpdr::kHostParts && e == cudaSuccess; g++) {
+        const size_t t0 = (size_t)pl.host_part_tok[g], t1 = (size_t)pl.host_part_tok[g + 1];
+        if (!kda && t1 > t0)
+            e = cudaMemcpyAsync((char *)dq + t0 * q_tok, (const char *)q + t0 * q_tok, (t1 - t0) * q_tok,
+                                cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = cudaEventRecord(ev(E_Q + g), cs);
+    }
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev(E_IN0), 0);
     if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: host-to-device copy");
     CPDR_TRY(cpdr_wy_build(c, dq, dk, db, dg, dwy, stream));
-    e = cudaStreamWaitEvent(st, ev_b, 0);
+    e = cudaStreamWaitEvent(st, ev(E_IN1), 0);
     if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: stream wait");
     CPDR_TRY(cpdr_preprocess(c, dk, dv, db, dg, dwy, dse, dm, stream));
     CPDR_TRY(cpdr_merge(c, dse, dm, dsi, stream));
-    e = cudaStreamWaitEvent(st, ev_c, 0);
+    for (int g = 0; g < cpdr::kHostParts; g++) {
+        const int off = pl.host_part_off[g], n = pl.host_part_off[g + 1] - off;
+        const size_t t0 = (size_t)pl.host_part_tok[g], t1 = (size_t)pl.host_part_tok[g + 1];
+        e = cudaStreamWaitEvent(st, ev(E_Q + g), 0);
+        if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: stream wait");
+        const int32_t *items = c->dev.host_items + off;
+        int rc = c->use_tc ? cpdr::launch_tc_fwd(c, items, n, dq, dk, dv, dg, dwy, dsi, dout, dfin, stream)
+                           : cpdr::launch_simt_fwd(c, items, n, dq, dk, dv, db, dg, dsi, dout, dfin, stream);
+        CPDR_TRY(launch_rc(rc, "cpdr_forward_host: forward"));
+        e = cudaEventRecord(ev(E_F + g), st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(os, ev(E_F + g), 0);
+        if (e == cudaSuccess && t1 > t0)
+            e = cudaMemcpyAsync((char *)o + t0 * o_tok, (const char *)dout + t0 * o_tok, (t1 - t0) * o_tok,
+                                cudaMemcpyDeviceToHost, os);
+        if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: device-to-host copy");
+    }
+    CPDR_TRY(launch_rc(cpdr::launch_zero_segments(c, nullptr, nullptr, nullptr, dfin, 2, stream),
+                       "cpdr_forward_host: zero fill"));
+    if (final_state) {
+        e = cudaMemcpyAsync(final_state, dfin, s.fin, cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: device-to-host copy");
+    }
+    e = cudaEventRecord(ev(E_OUT), os);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev(E_OUT), 0);
     if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: stream wait");
-    CPDR_TRY(cpdr_fwd(c, dq, dk, dv, db, dg, dwy, dsi, dout, dfin, stream));
-    e = cudaMemcpyAsync(o, dout, s.o, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess && final_state) e = cudaMemcpyAsync(final_state, dfin, s.fin, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return cuda_err(e, "cpdr_forward_host: device-to-host copy");
     return CPDR_OK;
 }
 

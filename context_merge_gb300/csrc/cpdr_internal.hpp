@@ -11,7 +11,8 @@
 
 namespace cpdr {
 
-constexpr int kChunk = 64;  // chunk size fixed by the article's Code Flow (chunk_size=64)
+constexpr int kChunk = 64;      // chunk size fixed by the article's Code Flow (chunk_size=64)
+constexpr int kHostParts = 4;   // token groups of the host-buffer path's pipeline
 
 // A chain of segments r0 < r1 of one row b crossed by one sequence: the merge
 // scan writes S_init for segments r0+1 .. r1 ([FLA-CP] §2.1 merge, §5.2).
@@ -85,6 +86,12 @@ struct Plan {
     int32_t max_pre_chunks = 0, max_fwd_chunks = 0;
     std::vector<int32_t> frag_chunk0;        // first global chunk of each fragment (+ total)
     std::vector<WyChunk> wy_chunks;          // every chunk of every fragment
+    // host-buffer path: fragments in kHostParts groups of consecutive memory
+    // tokens, so that the forward of a group can start once its q is in and
+    // its o can leave while the next group runs
+    std::vector<int32_t> host_items;         // fragments, group by group (longest first inside)
+    int32_t host_part_off[kHostParts + 1] = {};   // group g: host_items[off[g] .. off[g+1])
+    int64_t host_part_tok[kHostParts + 1] = {};   // group g: memory tokens [tok[g], tok[g+1])
     int32_t conv_width = 0;                  // causal conv1d kernel size (0: no conv path)
     std::vector<ConvTile> conv_tiles;        // conv work units, fragment by fragment
     std::vector<int64_t> conv_halo;          // halo rows, conv_width - 1 memory positions each
@@ -108,6 +115,7 @@ struct DeviceTables {
     int32_t *frag_chunk0 = nullptr;
     WyChunk *wy_chunks = nullptr;
     ConvTile *conv_tiles = nullptr;
+    int32_t *host_items = nullptr;
     int64_t *conv_halo = nullptr;
     int32_t *status = nullptr;   // device status word (bounded waits)
 };
@@ -126,8 +134,9 @@ struct cpdr_ctx {
     void *ev_fork = nullptr, *ev_join = nullptr;
     // host-buffer path: a copy stream for the host-to-device copies and the
     // events that let compute start on the inputs that have arrived
-    void *copy_stream = nullptr;
-    void *ev_start = nullptr, *ev_in0 = nullptr, *ev_in1 = nullptr, *ev_in2 = nullptr;
+    void *copy_stream = nullptr, *out_stream = nullptr;
+    static constexpr int kHostEvents = 4 + 2 * cpdr::kHostParts;   // start, in0, in1, out, q[g], f[g]
+    void *host_ev[kHostEvents] = {};
 };
 
 namespace cpdr {
@@ -136,7 +145,8 @@ namespace cpdr {
 // (0 = success) of the launch it enqueued.
 int launch_simt_pre(const cpdr_ctx *c, const void *k, const void *v, const void *beta,
                     const float *g, float *S_ext, float *M, void *stream);
-int launch_simt_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v,
+// items: fragment indices to run (n_items of them); the plan's fwd_order for all
+int launch_simt_fwd(const cpdr_ctx *c, const int32_t *items, int n_items, const void *q, const void *k, const void *v,
                     const void *beta, const float *g, const float *S_init, void *o,
                     float *final_state, void *stream);
 int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init,
@@ -163,7 +173,8 @@ int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *
                   float *S_ext, float *M, void *stream);
 int launch_conv1d(const cpdr_ctx *c, const void *x, const float *weight, const float *bias, int channels,
                   int activation, void *y, void *stream);
-int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const float *g,
+int launch_tc_fwd(const cpdr_ctx *c, const int32_t *items, int n_items, const void *q, const void *k, const void *v,
+                  const float *g,
                   const void *wy, const float *S_init, void *o, float *final_state, void *stream);
 
 }  // namespace cpdr

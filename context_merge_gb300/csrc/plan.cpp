@@ -158,6 +158,38 @@ cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err) {
     std::stable_sort(p.fwd_order.begin(), p.fwd_order.end(),
                      [&](int32_t a, int32_t b) { return p.frags[a].len > p.frags[b].len; });
     for (auto &f : p.frags) p.max_fwd_chunks = std::max(p.max_fwd_chunks, chunks(f.len));
+    // host-buffer pipeline: fragments in memory order (they tile the token
+    // axis), cut at fragment boundaries into kHostParts groups of about
+    // equal tokens; longest first inside a group
+    {
+        std::vector<int32_t> mem(p.frags.size());
+        std::iota(mem.begin(), mem.end(), 0);
+        std::stable_sort(mem.begin(), mem.end(),
+                         [&](int32_t a, int32_t b) { return p.frags[a].tok0 < p.frags[b].tok0; });
+        const int64_t total = (int64_t)p.B * p.T;
+        std::vector<std::vector<int32_t>> groups(kHostParts);
+        int g = 0;
+        int64_t acc = 0;
+        for (int32_t fi : mem) {
+            while (g + 1 < kHostParts && acc >= (int64_t)(g + 1) * total / kHostParts) g++;
+            groups[g].push_back(fi);
+            acc += p.frags[fi].len;
+        }
+        int64_t cursor = 0;
+        for (int gi = 0; gi < kHostParts; gi++) {
+            std::stable_sort(groups[gi].begin(), groups[gi].end(),
+                             [&](int32_t a, int32_t b) { return p.frags[a].len > p.frags[b].len; });
+            p.host_part_off[gi] = (int32_t)p.host_items.size();
+            p.host_part_tok[gi] = cursor;
+            for (int32_t fi : groups[gi]) {
+                p.host_items.push_back(fi);
+                cursor += p.frags[fi].len;
+            }
+        }
+        p.host_part_off[kHostParts] = (int32_t)p.host_items.size();
+        p.host_part_tok[kHostParts] = cursor;
+        if (cursor != total) return fail(err, CPDR_ERR_INVALID, "internal: fragments do not tile the token axis");
+    }
     // longest pre items first as well
     std::stable_sort(p.pre_items.begin(), p.pre_items.end(),
                      [&](int32_t a, int32_t b) { return p.frags[a].len > p.frags[b].len; });

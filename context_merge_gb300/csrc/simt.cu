@@ -483,15 +483,15 @@ __global__ void zero_slabs_kernel(const int32_t *__restrict__ list, float *__res
 }
 
 template <typename TIn, int D, bool PERDIM>
-int launch_fwd_t(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta,
-                 const float *g, const float *S_init, void *o, float *fs, cudaStream_t st) {
+int launch_fwd_t(const cpdr_ctx *c, const int32_t *items, int n_items, const void *q, const void *k, const void *v,
+                 const void *beta, const float *g, const float *S_init, void *o, float *fs, cudaStream_t st) {
     const auto &p = c->plan;
     auto kern = simt_fwd_kernel<TIn, D, PERDIM>;
     const size_t sm = smem_bytes<D>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return (int)e;
-    dim3 grid((unsigned)p.frags.size(), (unsigned)p.Hq, (unsigned)(D / BV));
-    kern<<<grid, NT, sm, st>>>(c->dev.frags, c->dev.fwd_order, (const TIn *)q, (const TIn *)k,
+    dim3 grid((unsigned)n_items, (unsigned)p.Hq, (unsigned)(D / BV));
+    kern<<<grid, NT, sm, st>>>(c->dev.frags, items, (const TIn *)q, (const TIn *)k,
                                (const TIn *)v, (const TIn *)beta, g, S_init, (TIn *)o, fs, p.H, p.G,
                                p.vfirst, p.scale);
     return (int)cudaGetLastError();
@@ -513,10 +513,11 @@ int launch_pre_t(const cpdr_ctx *c, const void *k, const void *v, const void *be
 }
 
 template <typename TIn, int D>
-int dispatch_gate_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *b,
-                      const float *g, const float *Si, void *o, float *fs, cudaStream_t st) {
-    return c->plan.gate_kind == CPDR_GATE_PER_DIM ? launch_fwd_t<TIn, D, true>(c, q, k, v, b, g, Si, o, fs, st)
-                                                  : launch_fwd_t<TIn, D, false>(c, q, k, v, b, g, Si, o, fs, st);
+int dispatch_gate_fwd(const cpdr_ctx *c, const int32_t *it, int n, const void *q, const void *k, const void *v,
+                      const void *b, const float *g, const float *Si, void *o, float *fs, cudaStream_t st) {
+    return c->plan.gate_kind == CPDR_GATE_PER_DIM
+               ? launch_fwd_t<TIn, D, true>(c, it, n, q, k, v, b, g, Si, o, fs, st)
+               : launch_fwd_t<TIn, D, false>(c, it, n, q, k, v, b, g, Si, o, fs, st);
 }
 template <typename TIn, int D>
 int dispatch_gate_pre(const cpdr_ctx *c, const void *k, const void *v, const void *b, const float *g,
@@ -527,16 +528,16 @@ int dispatch_gate_pre(const cpdr_ctx *c, const void *k, const void *v, const voi
 
 }  // namespace
 
-int launch_simt_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta,
-                    const float *g, const float *S_init, void *o, float *fs, void *stream) {
+int launch_simt_fwd(const cpdr_ctx *c, const int32_t *items, int n, const void *q, const void *k, const void *v,
+                    const void *beta, const float *g, const float *S_init, void *o, float *fs, void *stream) {
     cudaStream_t st = (cudaStream_t)stream;
     const auto &p = c->plan;
-    if (p.frags.empty()) return 0;
+    if (n <= 0) return 0;
     if (p.in_dtype == CPDR_DTYPE_F32)
-        return p.dk == 64 ? dispatch_gate_fwd<float, 64>(c, q, k, v, beta, g, S_init, o, fs, st)
-                          : dispatch_gate_fwd<float, 128>(c, q, k, v, beta, g, S_init, o, fs, st);
-    return p.dk == 64 ? dispatch_gate_fwd<__nv_bfloat16, 64>(c, q, k, v, beta, g, S_init, o, fs, st)
-                      : dispatch_gate_fwd<__nv_bfloat16, 128>(c, q, k, v, beta, g, S_init, o, fs, st);
+        return p.dk == 64 ? dispatch_gate_fwd<float, 64>(c, items, n, q, k, v, beta, g, S_init, o, fs, st)
+                          : dispatch_gate_fwd<float, 128>(c, items, n, q, k, v, beta, g, S_init, o, fs, st);
+    return p.dk == 64 ? dispatch_gate_fwd<__nv_bfloat16, 64>(c, items, n, q, k, v, beta, g, S_init, o, fs, st)
+                      : dispatch_gate_fwd<__nv_bfloat16, 128>(c, items, n, q, k, v, beta, g, S_init, o, fs, st);
 }
 
 int launch_simt_pre(const cpdr_ctx *c, const void *k, const void *v, const void *beta, const float *g,

@@ -1137,10 +1137,10 @@ int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *
     return 0;
 }
 
-int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const float *g, const void *wy,
-                  const float *S_init, void *o, float *final_state, void *stream) {
+int launch_tc_fwd(const cpdr_ctx *c, const int32_t *items, int n_items, const void *q, const void *k, const void *v,
+                  const float *g, const void *wy, const float *S_init, void *o, float *final_state, void *stream) {
     const auto &p = c->plan;
-    if (p.frags.empty()) return 0;
+    if (n_items <= 0) return 0;
     CUtensorMap tq, tk, tv;
     const int64_t tokens = (int64_t)p.B * p.T;
     const bool kda = p.gate_kind == CPDR_GATE_PER_DIM;   // Q and K come pre-gated in the units
@@ -1149,7 +1149,7 @@ int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v
         return (int)cudaErrorInvalidValue;
     Params prm{};
     prm.frags = c->dev.frags;
-    prm.items = c->dev.fwd_order;
+    prm.items = items;
     prm.chunk0 = c->dev.frag_chunk0;
     prm.wy = (const uint8_t *)wy;
     prm.g = g;
@@ -1165,10 +1165,9 @@ int launch_tc_fwd(const cpdr_ctx *c, const void *q, const void *k, const void *v
     // one chain per (fragment, query head): grouped query heads each run
     // their state head's chain
     if (kda)
-        return launch_chain<MODE_FWD_KDA, ROLE_S>(tq, tk, tv, prm, (unsigned)p.frags.size(), (unsigned)p.Hq,
+        return launch_chain<MODE_FWD_KDA, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.Hq,
                                                   (cudaStream_t)stream);
-    return launch_chain<MODE_FWD, ROLE_S>(tq, tk, tv, prm, (unsigned)p.frags.size(), (unsigned)p.Hq,
-                                          (cudaStream_t)stream);
+    return launch_chain<MODE_FWD, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.Hq, (cudaStream_t)stream);
 }
 
 }  // namespace cpdr

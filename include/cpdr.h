@@ -44,8 +44,8 @@
  * Memory.  Every tensor argument is a DEVICE pointer owned by the caller, and
  *          must be 16-byte aligned.  The library owns only the cpdr_ctx
  *          (host tables plus small device metadata allocated at create,
- *          a copy stream and four events for cpdr_forward_host, and on the
- *          tensor-core path one more stream and two events).
+ *          two copy streams and twelve events for cpdr_forward_host, and on
+ *          the tensor-core path one more stream and two events).
  *          No call below allocates device memory.
  * Streams. cpdr_preprocess forks its M-chain kernel onto the context's
  *          internal stream and joins it back into `stream` before returning
@@ -266,8 +266,11 @@ cpdr_status cpdr_plan_conv_tokens(const cpdr_ctx *ctx, int32_t *out, int32_t cap
  * cpdr_host_workspace_bytes() bytes (256-byte aligned device memory).
  * The host-to-device copies run on the context's copy stream, ordered after
  * all work enqueued on `stream` before the call, in the order the stages
- * need them (k, beta, gate, then v, then q); each stage waits on `stream`
- * for its own inputs only, so compute overlaps the later copies.
+ * need them (k, beta, gate, then v, then q in four groups of consecutive
+ * tokens); each stage waits on `stream` for its own inputs only, the
+ * forward runs group by group, and each group's o is copied back on the
+ * context's output stream while the next group runs; `stream` waits for
+ * the last copy before anything later on it.
  */
 cpdr_status cpdr_host_workspace_bytes(const cpdr_ctx *ctx, size_t *bytes);
 cpdr_status cpdr_forward_host(const cpdr_ctx *ctx, const void *q, const void *k, const void *v,
