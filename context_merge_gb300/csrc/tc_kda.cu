@@ -71,11 +71,29 @@ __device__ __forceinline__ uint32_t img_off(int i, int d) {
 __device__ __forceinline__ void put_bf16(uint8_t *img, uint32_t off, float x) {
     *reinterpret_cast<__nv_bfloat16 *>(img + off) = __float2bfloat16_rn(x);
 }
-// hi = bf16(x), lo = bf16(x - hi)
-__device__ __forceinline__ void put_hilo(uint8_t *hi, uint8_t *lo, uint32_t off, float x) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    *reinterpret_cast<__nv_bfloat16 *>(hi + off) = h;
-    *reinterpret_cast<__nv_bfloat16 *>(lo + off) = __float2bfloat16_rn(x - __bfloat162float(h));
+// 8 values as 8 bf16 (one 16-byte chunk)
+__device__ __forceinline__ uint4 pack8f(const float *x) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        w[e] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+// hi = bf16(x) and lo = bf16(x - hi) of 8 values, one 16-byte store each
+__device__ __forceinline__ void store_hilo8(uint8_t *hi, uint8_t *lo, uint32_t off, const float *x, uint4 &h) {
+    h = pack8f(x);
+    const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+    float r[8];
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hw[e]));
+        r[2 * e] = x[2 * e] - f.x;
+        r[2 * e + 1] = x[2 * e + 1] - f.y;
+    }
+    *reinterpret_cast<uint4 *>(hi + off) = h;
+    *reinterpret_cast<uint4 *>(lo + off) = pack8f(r);
 }
 
 __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid_constant__ KdaParams p) {
@@ -132,32 +150,64 @@ __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid
     const bool exact = *steep != 0;
 
     // ---- gated tiles; unless exact, the factorised operands replace the
-    // inputs in place (thread owns column d, rows i0, i0 + 2, ...)
-    {
-        const int d = tid & (D - 1), i0 = tid >> 7;
-        const float gr = Gr[d], gc = GCv[d];
-        for (int i = i0; i < C; i += 2) {
-            const float Gi = GF[i * KP_LD + d];
-            const float kv = KB[i * KP_LD + d];
-            const float qv = __bfloat162float(QB[i * KQ_LD + d]);
-            const uint32_t off = img_off(i, d);
-            const float gi = exp2f(Gi);
-            put_hilo(dst + kKdaOffKg, dst + kKdaOffKgLo, off, kv * gi);
-            put_hilo(dst + kKdaOffKgam, dst + kKdaOffKgamLo, off, kv * exp2f(gc - Gi));
-            put_bf16(dst + kKdaOffQg, off, qv * gi);
-            if (!exact) {
-                const float e = exp2f(Gi - gr);
-                GF[i * KP_LD + d] = kv * exp2f(gr - Gi);
-                KB[i * KP_LD + d] = kv * e;
-                QB[i * KQ_LD + d] = __float2bfloat16_rn(qv * e);
+    // inputs in place.  A thread takes 8 consecutive key dims of a row (one
+    // 16-byte chunk of each image): items (row, group of 8), 4 per thread.
+    for (int item = tid; item < C * (D / 8); item += KP_THREADS) {
+        const int i = item >> 4, d0 = (item & 15) * 8;
+        float Gv[8], kv[8], qv[8], gr[8], gc[8];
+        *reinterpret_cast<float4 *>(Gv) = *reinterpret_cast<const float4 *>(GF + i * KP_LD + d0);
+        *reinterpret_cast<float4 *>(Gv + 4) = *reinterpret_cast<const float4 *>(GF + i * KP_LD + d0 + 4);
+        *reinterpret_cast<float4 *>(kv) = *reinterpret_cast<const float4 *>(KB + i * KP_LD + d0);
+        *reinterpret_cast<float4 *>(kv + 4) = *reinterpret_cast<const float4 *>(KB + i * KP_LD + d0 + 4);
+        *reinterpret_cast<float4 *>(gr) = *reinterpret_cast<const float4 *>(Gr + d0);
+        *reinterpret_cast<float4 *>(gr + 4) = *reinterpret_cast<const float4 *>(Gr + d0 + 4);
+        *reinterpret_cast<float4 *>(gc) = *reinterpret_cast<const float4 *>(GCv + d0);
+        *reinterpret_cast<float4 *>(gc + 4) = *reinterpret_cast<const float4 *>(GCv + d0 + 4);
+        {
+            const uint4 q8 = *reinterpret_cast<const uint4 *>(QB + i * KQ_LD + d0);
+            const uint32_t qw[4] = {q8.x, q8.y, q8.z, q8.w};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qw[e]));
+                qv[2 * e] = f.x;
+                qv[2 * e + 1] = f.y;
             }
+        }
+        float kg[8], kgam[8], qg[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const float gi = exp2f(Gv[e]);
+            kg[e] = kv[e] * gi;
+            kgam[e] = kv[e] * exp2f(gc[e] - Gv[e]);
+            qg[e] = qv[e] * gi;
+        }
+        const uint32_t off = img_off(i, d0);
+        uint4 h_kg, h_kgam;
+        store_hilo8(dst + kKdaOffKg, dst + kKdaOffKgLo, off, kg, h_kg);
+        store_hilo8(dst + kKdaOffKgam, dst + kKdaOffKgamLo, off, kgam, h_kgam);
+        *reinterpret_cast<uint4 *>(dst + kKdaOffQg + off) = pack8f(qg);
+        if (!exact) {
+            float ke[8], kf[8], qe[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const float ef = exp2f(Gv[e] - gr[e]);
+                ke[e] = kv[e] * ef;
+                kf[e] = kv[e] * exp2f(gr[e] - Gv[e]);
+                qe[e] = qv[e] * ef;
+            }
+            *reinterpret_cast<float4 *>(GF + i * KP_LD + d0) = *reinterpret_cast<const float4 *>(kf);
+            *reinterpret_cast<float4 *>(GF + i * KP_LD + d0 + 4) = *reinterpret_cast<const float4 *>(kf + 4);
+            *reinterpret_cast<float4 *>(KB + i * KP_LD + d0) = *reinterpret_cast<const float4 *>(ke);
+            *reinterpret_cast<float4 *>(KB + i * KP_LD + d0 + 4) = *reinterpret_cast<const float4 *>(ke + 4);
+            *reinterpret_cast<uint4 *>(QB + i * KQ_LD + d0) = pack8f(qe);
         }
     }
     __syncthreads();
 
     // ---- A (strict lower, times beta_i) and P (lower incl. the diagonal):
     // thread (bi, bj) owns rows bi + 16 r and columns bj + 16 c (r, c < 4),
-    // so the 16 column rows a warp reads are consecutive (no bank conflicts)
+    // so the 16 column rows a warp reads are consecutive (no bank conflicts);
+    // pairs with c > r lie above the diagonal and are skipped
     const int bi = tid >> 4, bj = tid & 15;
     float a[4][4], pp[4][4];
 #pragma unroll
@@ -180,7 +230,7 @@ __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid
 #pragma unroll
             for (int r = 0; r < 4; r++)
 #pragma unroll
-                for (int c = 0; c < 4; c++) {
+                for (int c = 0; c <= r; c++) {   // column block c > r lies above the diagonal
                     a[r][c] = fmaf(ke[r].x, kf[c].x, a[r][c]);
                     a[r][c] = fmaf(ke[r].y, kf[c].y, a[r][c]);
                     a[r][c] = fmaf(ke[r].z, kf[c].z, a[r][c]);
