@@ -50,10 +50,14 @@ constexpr int D = 128;
 constexpr int NTHREADS = 512;
 
 // Modes: bit 0 = pre-process (else forward), bit 1 = per-dim gate (KDA),
-// whose gate is folded into operand tiles precomputed per chunk (tc_kda.cu).
-enum Mode { MODE_FWD = 0, MODE_PRE = 1, MODE_FWD_KDA = 2, MODE_PRE_KDA = 3 };
+// whose gate is folded into operand tiles precomputed per chunk (tc_kda.cu);
+// bit 2 = layout variants in the forward (grouped query heads, [dv, dk]
+// states), kept out of the plain forward's code (measured 4% slower with
+// them compiled in).  The per-dim modes always handle the variants.
+enum Mode { MODE_FWD = 0, MODE_PRE = 1, MODE_FWD_KDA = 2, MODE_PRE_KDA = 3, MODE_FWD_VAR = 4 };
 __host__ __device__ constexpr bool mode_fwd(int m) { return (m & 1) == 0; }
 __host__ __device__ constexpr bool mode_kda(int m) { return (m & 2) != 0; }
+__host__ __device__ constexpr bool mode_var(int m) { return (m & 4) != 0 || (m & 3) != 0; }
 enum Role { ROLE_S = 0, ROLE_M = 1 };
 
 // Optional event trace (compile with -DCPDR_TRACE): CTA (0, 0) of each
@@ -353,8 +357,9 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
             tma_load_3d(st + L.kc0, tk, fb, 0, r.h, tok);
             tma_load_3d(st + L.kc1, tk, fb, 64, r.h, tok);
             if (mode_fwd(MODE)) {
-                tma_load_3d(st + L.qc0, tq, fb, 0, r.hq, tok);
-                tma_load_3d(st + L.qc1, tq, fb, 64, r.hq, tok);
+                const int hq = mode_var(MODE) ? r.hq : r.h;
+                tma_load_3d(st + L.qc0, tq, fb, 0, hq, tok);
+                tma_load_3d(st + L.qc1, tq, fb, 64, hq, tok);
             }
             if (mode_fwd(MODE) || ROLE == ROLE_S) {
                 tma_load_3d(st + L.vc0, tv, fb, 0, r.h, tok);
@@ -451,10 +456,14 @@ __device__ __forceinline__ Descs make_descs(const Run &r) {
     d.wb = mndesc(b0 + L.wb, 16384);
     d.wblo = mndesc(b0 + L.wb_lo, 16384);
     d.mask = kdesc(b0 + L.mask);
-    d.kgam0 = mndesc(b0 + L.kgam, L.k_lbo);
-    d.kglo0 = mndesc(b0 + L.kglo, L.k_lbo);
-    d.kgamlo0 = mndesc(b0 + L.kgamlo, L.k_lbo);
-    d.pt0 = kdesc(b0 + L.pt);
+    if (mode_kda(MODE)) {
+        d.kgam0 = mndesc(b0 + L.kgam, L.k_lbo);
+        d.kglo0 = mndesc(b0 + L.kglo, L.k_lbo);
+        d.kgamlo0 = mndesc(b0 + L.kgamlo, L.k_lbo);
+        d.pt0 = kdesc(b0 + L.pt);
+    } else {
+        d.kgam0 = d.kglo0 = d.kgamlo0 = d.pt0 = 0;
+    }
     return d;
 }
 template <int MODE, int ROLE>
@@ -645,8 +654,9 @@ __device__ __forceinline__ void run_wepi(const Run &r) {
             if (w == 4) TR(2, t, 3);
             tc_fence_after();
             const int nv = rows_of(r, t);
-            const int64_t ostride = (int64_t)p.Hq * D;
-            __nv_bfloat16 *op = p.o + ((r.tok0 + (int64_t)t * C) * p.Hq + r.hq) * D + row;
+            const int Hq = mode_var(MODE) ? p.Hq : p.H, hq = mode_var(MODE) ? r.hq : r.h;
+            const int64_t ostride = (int64_t)Hq * D;
+            __nv_bfloat16 *op = p.o + ((r.tok0 + (int64_t)t * C) * Hq + hq) * D + row;
             const float sc = -p.scale;   // the accumulator holds -O^T
             float a[32], b[32];
             tmem_ld32(lane_base + TM_O, a);
@@ -732,7 +742,7 @@ __device__ __forceinline__ void run_state(const Run &r) {
         float x = 0.f;
         if (SPLIT) x = (dk == row) ? 1.f : 0.f;
         else if (FWD && (r.flags & CPDR_FRAG_CONT_PREV))
-            x = p.S_init[sidx + (p.vfirst ? (int64_t)row * D + dk : (int64_t)dk * D + row)];
+            x = p.S_init[sidx + ((mode_var(MODE) && p.vfirst) ? (int64_t)row * D + dk : (int64_t)dk * D + row)];
         S[i] = x;
     }
     put_state();
@@ -807,8 +817,9 @@ __device__ __forceinline__ void run_state(const Run &r) {
         if (issuer) {
             tc_fence_after();
             // P_S = (Delta diag Gamma)^T K  (per-dim gate: Delta^T Kgam)
-            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kgam0, ch), false);
-            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg<MODE, ROLE>(d.kgam0, ch), true);
+            const uint64_t kps = KDA ? d.kgam0 : d.kmn0;   // scalar gate: one K tile for every product
+            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(kps, ch), false);
+            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg<MODE, ROLE>(kps, ch), true);
             if (SPLIT && KDA) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kgamlo0, ch), true);
             mma_commit(&r.bar[B_PSFULL]);
             TR(1, ch, 4);
@@ -858,9 +869,9 @@ __device__ __forceinline__ void run_state(const Run &r) {
     // outputs of the chain
     if (FWD) {
         // the first query head of a group writes the state's final value
-        if ((r.flags & CPDR_FRAG_ENDS_SEQ) && p.final_state && r.hq % p.G == 0) {
+        if ((r.flags & CPDR_FRAG_ENDS_SEQ) && p.final_state && (!mode_var(MODE) || r.hq % p.G == 0)) {
             const int64_t fidx = ((int64_t)r.seq * H + r.h) * D * D;
-            if (p.vfirst) {   // [dv][dk]: this thread's row is contiguous
+            if (mode_var(MODE) && p.vfirst) {   // [dv][dk]: this thread's row is contiguous
                 float4 *dst = reinterpret_cast<float4 *>(p.final_state + fidx + (int64_t)row * D + 64 * half);
 #pragma unroll
                 for (int i = 0; i < 16; i++) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
@@ -920,8 +931,9 @@ __device__ __forceinline__ void run_issuer(const Run &r) {
         if ((bad = named_bar_or(kStateBar, 288, ok ? 0 : 1))) break;
         if (lead) {
             tc_fence_after();
-            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kgam0, ch), false);
-            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg<MODE, ROLE>(d.kgam0, ch), true);
+            const uint64_t kps = mode_kda(MODE) ? d.kgam0 : d.kmn0;
+            mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(kps, ch), false);
+            if (SPLIT) mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB_LO, stg<MODE, ROLE>(kps, ch), true);
             if (SPLIT && mode_kda(MODE))
                 mma_tmn<128, 64>(tm + TM_PS, tm + TM_DGB, stg<MODE, ROLE>(d.kgamlo0, ch), true);
             mma_commit(&r.bar[B_PSFULL]);
@@ -958,7 +970,7 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     r.seq = f.seq;
     r.flags = f.flags;
     r.hq = blockIdx.y;
-    r.h = r.hq / p.G;
+    r.h = mode_var(MODE) ? r.hq / p.G : r.hq;
     r.n = (f.len + C - 1) / C;
     r.nlast = f.len - (r.n - 1) * C;
     r.chunk0 = p.chunk0[fi];
@@ -1053,6 +1065,7 @@ static_assert(make_lay(MODE_FWD, ROLE_S).total + 1024 <= kMaxSmem, "forward layo
 static_assert(make_lay(MODE_PRE, ROLE_S).total + 1024 <= kMaxSmem, "pre-process S layout exceeds shared memory");
 static_assert(make_lay(MODE_PRE, ROLE_M).total + 1024 <= kMaxSmem, "pre-process M layout exceeds shared memory");
 static_assert(make_lay(MODE_FWD_KDA, ROLE_S).total + 1024 <= kMaxSmem, "per-dim forward layout exceeds shared memory");
+static_assert(make_lay(MODE_FWD_VAR, ROLE_S).total == make_lay(MODE_FWD, ROLE_S).total, "variant forward layout");
 static_assert(make_lay(MODE_PRE_KDA, ROLE_S).total + 1024 <= kMaxSmem, "per-dim pre-process S layout too large");
 static_assert(make_lay(MODE_PRE_KDA, ROLE_M).total + 1024 <= kMaxSmem, "per-dim pre-process M layout too large");
 static_assert(make_lay(MODE_FWD_KDA, ROLE_S).tx_bytes < (1u << 20) && make_lay(MODE_PRE_KDA, ROLE_M).tx_bytes < (1u << 20),
@@ -1166,6 +1179,9 @@ int launch_tc_fwd(const cpdr_ctx *c, const int32_t *items, int n_items, const vo
     // their state head's chain
     if (kda)
         return launch_chain<MODE_FWD_KDA, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.Hq,
+                                                  (cudaStream_t)stream);
+    if (p.G > 1 || p.vfirst)
+        return launch_chain<MODE_FWD_VAR, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.Hq,
                                                   (cudaStream_t)stream);
     return launch_chain<MODE_FWD, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.Hq, (cudaStream_t)stream);
 }
