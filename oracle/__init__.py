@@ -15,6 +15,10 @@ the article "flash-linear-attention 上下文并行CP 从 CP2TP、Ring CP 到 Tr
                     per-fragment forward from S_init.
 * ``chunked`` / ``chunked_pre`` -- [FLA-CP] §2.2: the chunk form in WY
                     representation restated in fp64 (pins the chunk equations).
+* ``backward``   -- the reverse of the per-token scan: gradients of
+                    sum <do, o> + sum <dht, S_final> (the backward that
+                    [FLA-CP] §2.2 and §4 split into pre-process, reverse merge
+                    and chunk chains has this result).
 
 Inputs q, k, v, beta are the exact values the GPU receives: float32 arrays, or
 bfloat16 bit patterns passed as uint16 arrays.  Gates are float32 natural-log
@@ -67,7 +71,9 @@ def _load():
             lib.oracle_chunked.argtypes = [pp, ctypes.c_int, vp, vp, vp, vp, fp, dp, dp]
             lib.oracle_chunked_pre.argtypes = [pp, ctypes.c_int, vp, vp, vp, fp, ctypes.c_int,
                                                ctypes.c_int64, ctypes.c_int64, dp, dp]
-            for f in (lib.oracle_scan, lib.oracle_segmented, lib.oracle_chunked, lib.oracle_chunked_pre):
+            lib.oracle_backward.argtypes = [pp, vp, vp, vp, vp, fp, vp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
+            for f in (lib.oracle_scan, lib.oracle_segmented, lib.oracle_chunked, lib.oracle_chunked_pre,
+                      lib.oracle_backward):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -204,3 +210,33 @@ class Problem:
                                     self._ptr(S), self._ptr(M))
         assert rc == 0
         return S, M
+
+
+def _backward(self, do, dht=None, nthreads=None):
+    """Gradients of sum <do, o> + sum <dht, S_final> (fp64): dict with dq,
+    dk [B,T,H,dk], dv [B,T,H,dv], dbeta [B,T,H], dg (the gate's shape).
+    ``do`` has the input dtype of q, k, v (fp32 array or bf16 bits)."""
+    lib = _load()
+    if self.Hq != self.H:
+        raise ValueError("the backward oracle covers Hq == H only")
+    d_o, ddt = as_oracle_array(do)
+    if ddt != self._p.in_dtype or d_o.shape != (self.B, self.T, self.H, self.dv):
+        raise ValueError("do must be [B, T, H, dv] in the input dtype")
+    out = dict(dq=np.zeros((self.B, self.T, self.H, self.dk)), dk=np.zeros((self.B, self.T, self.H, self.dk)),
+               dv=np.zeros((self.B, self.T, self.H, self.dv)), dbeta=np.zeros((self.B, self.T, self.H)),
+               dg=np.zeros(self.g.shape))
+    dhtp = None
+    if dht is not None:
+        dht = np.ascontiguousarray(dht, dtype=np.float64)
+        assert dht.shape == (self.N, self.H, self.dk, self.dv)
+        dhtp = self._ptr(dht)
+    rc = lib.oracle_backward(ctypes.byref(self._p), self._ptr(self.q), self._ptr(self.k), self._ptr(self.v),
+                             self._ptr(self.beta), self._ptr(self.g), self._ptr(d_o), dhtp, self._ptr(out["dq"]),
+                             self._ptr(out["dk"]), self._ptr(out["dv"]), self._ptr(out["dbeta"]),
+                             self._ptr(out["dg"]), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"backward not covered (code {rc})")
+    return out
+
+
+Problem.backward = _backward

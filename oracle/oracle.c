@@ -530,3 +530,142 @@ int oracle_chunked_pre(const oracle_problem *P, int C, const void *k, const void
     chunk_pass(P, C, NULL, k, v, beta, g, h, t0, t1, S_ext, M, NULL);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* 4. the backward of the per-token scan (order 0, Hq == H)             */
+/* ------------------------------------------------------------------ */
+/*
+ * Gradients of L = sum_t <do_t, o_t> + sum_n <dht_n, S_final,n> with
+ * respect to q, k, v, beta and the log gates, by the reverse of the
+ * per-token update (the chain rule written out, no chunking):
+ *   P = Diag(alpha) S_{t-1},  u = v - P^T k,  S_t = P + beta k u^T,
+ *   o_t = scale S_t^T q_t.
+ * With G = dL/dS_t (after adding scale q_t do_t^T from o_t):
+ *   dq_t = scale S_t do_t,       g_u = beta G^T k,       dv_t = g_u,
+ *   dbeta_t = k^T G u,           dk_t = beta G u - P g_u,
+ *   dP = G - k g_u^T,            dalpha_d = sum_c dP_dc S_{t-1,dc},
+ *   dg_t = alpha dalpha (per key dim; summed over d for a scalar gate),
+ *   dL/dS_{t-1} = Diag(alpha) dP.
+ * States are recomputed forward from checkpoints every 64 tokens.
+ */
+typedef struct {
+    const oracle_problem *P;
+    const void *q, *k, *v, *beta, *dout; const float *g;
+    const double *dht;
+    double *dq, *dk, *dv, *dbeta, *dg;
+} bwd_ctx;
+
+static void bwd_item(void *vctx, int64_t item, double *scratch) {
+    (void)scratch;
+    bwd_ctx *c = (bwd_ctx *)vctx;
+    const oracle_problem *P = c->P;
+    const int n = (int)(item / P->H), h = (int)(item % P->H);
+    const int dk = P->dk, dv = P->dv, H = P->H;
+    const size_t sz = (size_t)dk * dv;
+    const int CK = 64;
+    int64_t s, e;
+    seq_range(P, n, &s, &e);
+    const int64_t len = e - s;
+    const int64_t nck = (len + CK - 1) / CK;
+    double *ck = (double *)malloc(sizeof(double) * sz * (size_t)(nck > 0 ? nck : 1));
+    double *st = (double *)malloc(sizeof(double) * sz * (CK + 1));
+    double *G = (double *)malloc(sizeof(double) * sz);
+    double *Pm = (double *)malloc(sizeof(double) * sz);
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)(8 * (dk + dv) + 64));
+    double *kk = tmp, *qq = kk + dk, *al = qq + dk, *u = al + dk, *gu = u + dv, *vv = gu + dv, *dd = vv + dv;
+    /* forward: checkpoints of the state before tokens s, s + CK, ... */
+    double *S = st;
+    memset(S, 0, sizeof(double) * sz);
+    for (int64_t t = s; t < e; t++) {
+        if ((t - s) % CK == 0) memcpy(ck + (size_t)((t - s) / CK) * sz, S, sizeof(double) * sz);
+        apply_tokens(P, NULL, c->k, c->v, c->beta, c->g, h, t, t + 1, S, dv, 1, NULL, tmp);
+    }
+    if (c->dht) memcpy(G, c->dht + ((size_t)n * H + h) * sz, sizeof(double) * sz);
+    else memset(G, 0, sizeof(double) * sz);
+    for (int64_t m = nck - 1; m >= 0; m--) {
+        const int64_t t0 = s + m * CK, t1 = (t0 + CK < e) ? t0 + CK : e;
+        const int nb = (int)(t1 - t0);
+        /* st[i] = state before token t0 + i, st[nb] = after the block */
+        memcpy(st, ck + (size_t)m * sz, sizeof(double) * sz);
+        for (int i = 0; i < nb; i++) {
+            memcpy(st + (size_t)(i + 1) * sz, st + (size_t)i * sz, sizeof(double) * sz);
+            apply_tokens(P, NULL, c->k, c->v, c->beta, c->g, h, t0 + i, t0 + i + 1, st + (size_t)(i + 1) * sz,
+                         dv, 1, NULL, tmp + 4 * (dk + dv));
+        }
+        for (int i = nb - 1; i >= 0; i--) {
+            const int64_t t = t0 + i, th = t * H + h;
+            const double *Sp = st + (size_t)i * sz, *St = st + (size_t)(i + 1) * sz;
+            for (int d = 0; d < dk; d++) {
+                kk[d] = ld_in(c->k, th * dk + d, P->in_dtype);
+                qq[d] = ld_in(c->q, th * dk + d, P->in_dtype);
+                al[d] = exp((double)(P->gate_kind == 0 ? c->g[th] : c->g[th * dk + d]));
+            }
+            for (int cc = 0; cc < dv; cc++) {
+                vv[cc] = ld_in(c->v, th * dv + cc, P->in_dtype);
+                dd[cc] = P->scale * ld_in(c->dout, th * dv + cc, P->in_dtype);
+            }
+            const double b = ld_in(c->beta, th, P->in_dtype);
+            /* dq_t = scale S_t do_t; G += scale q_t do_t^T */
+            for (int d = 0; d < dk; d++) {
+                double acc = 0.0;
+                for (int cc = 0; cc < dv; cc++) acc += St[d * dv + cc] * dd[cc];
+                c->dq[th * dk + d] = acc;
+                for (int cc = 0; cc < dv; cc++) G[d * dv + cc] += qq[d] * dd[cc];
+            }
+            /* P = Diag(alpha) S_{t-1}, u = v - P^T k */
+            for (int d = 0; d < dk; d++)
+                for (int cc = 0; cc < dv; cc++) Pm[d * dv + cc] = al[d] * Sp[d * dv + cc];
+            for (int cc = 0; cc < dv; cc++) {
+                double acc = 0.0;
+                for (int d = 0; d < dk; d++) acc += Pm[d * dv + cc] * kk[d];
+                u[cc] = vv[cc] - acc;
+            }
+            /* g_u = beta G^T k */
+            for (int cc = 0; cc < dv; cc++) {
+                double acc = 0.0;
+                for (int d = 0; d < dk; d++) acc += G[d * dv + cc] * kk[d];
+                gu[cc] = b * acc;
+                c->dv[th * dv + cc] = gu[cc];
+            }
+            /* dbeta = k^T G u; dk = beta G u - P g_u */
+            double dbeta = 0.0;
+            for (int d = 0; d < dk; d++) {
+                double Gu = 0.0, Pg = 0.0;
+                for (int cc = 0; cc < dv; cc++) {
+                    Gu += G[d * dv + cc] * u[cc];
+                    Pg += Pm[d * dv + cc] * gu[cc];
+                }
+                dbeta += kk[d] * Gu;
+                c->dk[th * dk + d] = b * Gu - Pg;
+            }
+            c->dbeta[th] = dbeta;
+            /* dP = G - k g_u^T; dalpha; G <- Diag(alpha) dP */
+            double dgs = 0.0;
+            for (int d = 0; d < dk; d++) {
+                double da = 0.0;
+                for (int cc = 0; cc < dv; cc++) {
+                    const double dP = G[d * dv + cc] - kk[d] * gu[cc];
+                    da += dP * Sp[d * dv + cc];
+                    G[d * dv + cc] = al[d] * dP;
+                }
+                if (P->gate_kind == 0) dgs += al[d] * da;
+                else c->dg[th * dk + d] = al[d] * da;
+            }
+            if (P->gate_kind == 0) c->dg[th] = dgs;
+        }
+    }
+    free(ck); free(st); free(G); free(Pm); free(tmp);
+}
+
+/* dout: [B*T, H, dv] in the input dtype; dht: [N, H, dk, dv] (nullable);
+ * dq, dk: [B*T, H, dk]; dv: [B*T, H, dv]; dbeta: [B*T, H]; dg like the gate.
+ * Returns 2 for grouped query heads and 1 for order 1 (not covered). */
+int oracle_backward(const oracle_problem *P, const void *q, const void *k, const void *v, const void *beta,
+                    const float *g, const void *dout, const double *dht, double *dq, double *dk, double *dv,
+                    double *dbeta, double *dg, int nthreads) {
+    if (q_group(P) != 1) return 2;
+    if (P->order != 0) return 1;
+    bwd_ctx c = {P, q, k, v, beta, dout, g, dht, dq, dk, dv, dbeta, dg};
+    run_pool(bwd_item, &c, (int64_t)P->num_seqs * P->H, nthreads, 1);
+    return 0;
+}
