@@ -29,7 +29,8 @@ EXPORTED = ["cpdr_ctx_create", "cpdr_ctx_destroy", "cpdr_buffer_sizes", "cpdr_pl
             "cpdr_plan_fragments", "cpdr_plan_counts", "cpdr_wy_bytes", "cpdr_wy_build", "cpdr_preprocess",
             "cpdr_merge", "cpdr_fwd", "cpdr_host_workspace_bytes",
             "cpdr_forward_host", "cpdr_forward_noalloc", "cpdr_check_device_status", "cpdr_selftest_wait_timeout",
-            "cpdr_conv1d_fwd", "cpdr_plan_conv_tokens", "cpdr_last_error", "cpdr_version"]
+            "cpdr_conv1d_fwd", "cpdr_plan_conv_tokens", "cpdr_bwd_workspace_bytes", "cpdr_bwd",
+            "cpdr_last_error", "cpdr_version"]
 
 
 class CpdrError(RuntimeError):
@@ -81,6 +82,8 @@ def load():
         lib.cpdr_host_workspace_bytes.argtypes = [vp, ctypes.POINTER(sz)]
         lib.cpdr_conv1d_fwd.argtypes = [vp, vp, vp, vp, ctypes.c_int32, ctypes.c_int32, vp, vp]
         lib.cpdr_plan_conv_tokens.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]
+        lib.cpdr_bwd_workspace_bytes.argtypes = [vp, ctypes.POINTER(sz)]
+        lib.cpdr_bwd.argtypes = [vp] * 16 + [sz, vp]
         lib.cpdr_forward_host.argtypes = [vp] * 9 + [sz, vp]
         lib.cpdr_forward_noalloc.argtypes = [vp] * 9
         lib.cpdr_check_device_status.argtypes = [vp, vp]
@@ -282,6 +285,32 @@ class Context:
         self._check_inputs(q=q, k=k, v=v, beta=beta, g=g, o=o)
         _check(self._lib.cpdr_forward_noalloc(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(o),
                                               _ptr(final_state), _stream(stream)))
+
+    # ---- backward ------------------------------------------------------------
+    def bwd_workspace_bytes(self):
+        n = ctypes.c_size_t()
+        _check(self._lib.cpdr_bwd_workspace_bytes(self._h, ctypes.byref(n)))
+        return n.value
+
+    def backward(self, q, k, v, beta, g, do, S_init, M, dht=None, workspace=None, stream=None):
+        """Gradients of sum <do, o> + sum <dht, final_state> (fp32 tensors
+        dq, dk, dv, dbeta, dg).  S_init and M are the buffers the forward's
+        merge and pre-process filled for the same inputs."""
+        self._check_inputs(q=q, k=k, v=v, beta=beta, g=g)
+        if tuple(do.shape) != tuple(v.shape) or do.dtype != v.dtype or not do.is_contiguous():
+            raise ValueError("do must match v")
+        dev = q.device
+        f32 = torch.float32
+        out = dict(dq=torch.empty(q.shape, dtype=f32, device=dev), dk=torch.empty(k.shape, dtype=f32, device=dev),
+                   dv=torch.empty(v.shape, dtype=f32, device=dev),
+                   dbeta=torch.empty(beta.shape, dtype=f32, device=dev), dg=torch.empty(g.shape, dtype=f32, device=dev))
+        if workspace is None:
+            workspace = torch.empty(self.bwd_workspace_bytes(), dtype=torch.uint8, device=dev)
+        _check(self._lib.cpdr_bwd(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(do), _ptr(dht),
+                                  _ptr(S_init), _ptr(M), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                                  _ptr(out["dbeta"]), _ptr(out["dg"]), _ptr(workspace),
+                                  ctypes.c_size_t(workspace.numel()), _stream(stream)))
+        return out
 
     # ---- causal conv1d on the same segments -------------------------------
     def conv_pre_tokens(self):

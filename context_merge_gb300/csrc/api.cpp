@@ -44,6 +44,7 @@ void free_tables(cpdr::DeviceTables &t) {
     cudaFree(t.wy_chunks);
     cudaFree(t.conv_tiles);
     cudaFree(t.host_items);
+    cudaFree(t.bwd_pre_items);
     cudaFree(t.conv_halo);
     cudaFree(t.status);
     t = cpdr::DeviceTables();
@@ -161,6 +162,7 @@ cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
         if (e == cudaSuccess) e = upload(&t.wy_chunks, p.wy_chunks);
         if (e == cudaSuccess) e = upload(&t.conv_tiles, p.conv_tiles);
         if (e == cudaSuccess) e = upload(&t.host_items, p.host_items);
+        if (e == cudaSuccess) e = upload(&t.bwd_pre_items, p.bwd_pre_items);
         if (e == cudaSuccess) e = upload(&t.conv_halo, p.conv_halo);
         if (e == cudaSuccess) e = cudaMalloc((void **)&t.status, 64);
         if (e == cudaSuccess) e = cudaMemset(t.status, 0, 64);
@@ -330,6 +332,58 @@ cpdr_status cpdr_conv1d_fwd(const cpdr_ctx *c, const void *x, const float *weigh
     const char *xb = (const char *)x, *yb = (const char *)y;
     if (xb < yb + nbytes && yb < xb + nbytes) return set_err(CPDR_ERR_INVALID, "cpdr_conv1d_fwd: y overlaps x");
     return launch_rc(cpdr::launch_conv1d(c, x, weight, bias, channels, activation, y, stream), "cpdr_conv1d_fwd");
+}
+
+cpdr_status cpdr_bwd_workspace_bytes(const cpdr_ctx *c, size_t *bytes) {
+    if (!c || !bytes) return set_err(CPDR_ERR_INVALID, "null argument");
+    const Sizes s = sizes_of(c->plan);
+    *bytes = 2 * round256(s.sext) +
+             round256((size_t)cpdr::bwd_grid(c) * cpdr::bwd_scratch_floats_per_cta(c) * sizeof(float));
+    return CPDR_OK;
+}
+
+cpdr_status cpdr_bwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta,
+                     const float *gate, const void *dout, const float *dht, const float *S_init, const float *M,
+                     float *dq, float *dk, float *dv, float *dbeta, float *dgate, void *ws, size_t ws_bytes,
+                     void *stream) {
+    CPDR_TRY(check_ctx(c));
+    const auto &p = c->plan;
+    if (p.Hq != p.H) return set_err(CPDR_ERR_UNSUPPORTED, "cpdr_bwd: grouped query heads are not covered");
+    if (p.vfirst) return set_err(CPDR_ERR_UNSUPPORTED, "cpdr_bwd: the [dv, dk] state layout is not covered");
+    CPDR_TRY(check_ptr(q, "q"));
+    CPDR_TRY(check_ptr(k, "k"));
+    CPDR_TRY(check_ptr(v, "v"));
+    CPDR_TRY(check_ptr(beta, "beta"));
+    CPDR_TRY(check_ptr(gate, "gate"));
+    CPDR_TRY(check_ptr(dout, "dout"));
+    CPDR_TRY(check_ptr(dht, "dht", true));
+    CPDR_TRY(check_ptr(S_init, "S_init"));
+    CPDR_TRY(check_ptr(M, "M"));
+    CPDR_TRY(check_ptr(dq, "dq"));
+    CPDR_TRY(check_ptr(dk, "dk"));
+    CPDR_TRY(check_ptr(dv, "dv"));
+    CPDR_TRY(check_ptr(dbeta, "dbeta"));
+    CPDR_TRY(check_ptr(dgate, "dgate"));
+    CPDR_TRY(check_ptr(ws, "workspace"));
+    size_t need = 0;
+    cpdr_bwd_workspace_bytes(c, &need);
+    if (ws_bytes < need) return set_err(CPDR_ERR_WORKSPACE, "cpdr_bwd: workspace too small");
+    if (((uintptr_t)ws & 255u) != 0) return set_err(CPDR_ERR_INVALID, "cpdr_bwd: workspace not 256-byte aligned");
+    const Sizes s = sizes_of(p);
+    char *w = (char *)ws;
+    float *dS_ext = (float *)w;
+    float *dS_end = (float *)(w + round256(s.sext));
+    float *scratch = (float *)(w + 2 * round256(s.sext));
+    const size_t tok = (size_t)p.B * (size_t)p.T;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(dq, 0, tok * p.H * p.dk * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dk, 0, tok * p.H * p.dk * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, tok * p.H * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dgate, 0, s.gate, st);
+    if (e != cudaSuccess) return cuda_err(e, "cpdr_bwd: zero fill");
+    return launch_rc(cpdr::launch_bwd(c, q, k, v, beta, gate, dout, dht, S_init, M, dS_ext, dS_end, scratch, dq, dk,
+                                      dv, dbeta, dgate, stream),
+                     "cpdr_bwd");
 }
 
 cpdr_status cpdr_plan_conv_tokens(const cpdr_ctx *c, int32_t *out, int32_t cap) {

@@ -1,0 +1,372 @@
+// Backward of the segmented delta-rule forward on CUDA cores (fp32): the
+// gradients of sum <do, o> + sum <dht, S_final> with respect to q, k, v,
+// beta and the gates, organised as the article "flash-linear-attention
+// 上下文并行CP ..." ([FLA-CP]) organises its backward (§2.2, §4: pre-process
+// of the backward, the merge run in reverse with the transposed transfer
+// matrices, then the state-gradient chains):
+//   1. every segment's first fragment that continues a sequence runs the
+//      reverse chain from its local end gradient (dht where the sequence
+//      ends in it, else zero) and keeps the state gradient at its start,
+//      dS_ext (the pre-process of the backward);
+//   2. per sequence crossing cuts, the reverse merge
+//      G = dS_ext[r1];  for j = r1-1 .. r0+1:  G <- M_j^T G + dS_ext[j],
+//      giving the gradient at the end of every segment's continuing last
+//      fragment (dS_end);
+//   3. every fragment runs the reverse chain from dht (sequence ends in it),
+//      dS_end (continues) or zero, and emits the input gradients.
+// The chain is the reverse of the per-token update (the chain rule written
+// out): with P = Diag(alpha) S_{t-1}, u = v - P^T k and G = dL/dS_t,
+//   G += scale q do^T,  dq = scale S_t do,  g_u = beta G^T k,  dv = g_u,
+//   dbeta = k^T G u,  dk = beta G u - P g_u,  dP = G - k g_u^T,
+//   dg = alpha * sum_c dP S_{t-1} (per key dim; summed for a scalar gate),
+//   dL/dS_{t-1} = Diag(alpha) dP.
+// The forward states are recomputed per token: from S_init (or zero) the
+// chain first stores the state at every 64-token boundary, then walks the
+// chunks backwards, recomputing each chunk's states into a per-CTA scratch.
+//
+// One CTA = one (fragment, head, 32-value-column tile), persistent over the
+// work list.  A thread holds D/8 rows of one column (column = thread / 8),
+// so reductions over the key dim are 8-lane shuffles; reductions over the
+// value columns (dq, dk, dg, dbeta) go through shared memory and then
+// atomically into the fp32 outputs, which the caller zeroes first.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "cpdr_internal.hpp"
+
+namespace cpdr {
+namespace {
+
+constexpr int BT = 256;     // threads per CTA
+constexpr int BVT = 32;     // value columns per CTA
+constexpr int CKB = 64;     // tokens between checkpoints
+
+__device__ __forceinline__ float ldv(const float *p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ldv(const __nv_bfloat16 *p, int64_t i) { return __bfloat162float(p[i]); }
+
+struct BwdParams {
+    const cpdr_fragment *frags;
+    const int32_t *items;     // fragment indices of this pass
+    int n_items;
+    int mode;                 // 0: pre-process (dS_ext only), 1: main (input gradients)
+    int H, B;
+    float scale;
+    const void *q, *k, *v, *beta, *dout;
+    const float *g;
+    const float *dht;         // [N, H, D, D] or null
+    const float *S_init;      // [R, B, H, D, D]
+    const float *dS_end;      // [R, B, H, D, D] (main)
+    float *dS_ext;            // [R, B, H, D, D] (pre-process)
+    float *dq, *dk, *dv, *dbeta, *dg;
+    float *scratch;           // per CTA: ckpt_floats + CKB * D * BVT floats
+    int64_t ckpt_floats;      // max checkpoints per fragment * D * BVT
+};
+
+template <typename TIn, int D, bool PERDIM>
+__global__ void __launch_bounds__(BT) bwd_chain_kernel(const __grid_constant__ BwdParams p) {
+    constexpr int NR = D / 8;                      // rows per thread
+    __shared__ float kk[D], qq[D], al[D], vv[BVT], dd[BVT];
+    __shared__ float red[8][3][D];                 // per-warp partial sums over columns: dq, dk, dalpha
+    __shared__ float redb[8];
+    __shared__ float sb;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int c = tid >> 3, r8 = tid & 7;          // column in the tile, row group
+    const int ntile = D / BVT;
+    const TIn *q = (const TIn *)p.q, *k = (const TIn *)p.k, *v = (const TIn *)p.v, *beta = (const TIn *)p.beta,
+              *dout = (const TIn *)p.dout;
+    float *ck = p.scratch + (int64_t)blockIdx.x * (p.ckpt_floats + (int64_t)CKB * D * BVT);
+    float *tok = ck + p.ckpt_floats;
+    for (int item = blockIdx.x; item < p.n_items * p.H * ntile; item += gridDim.x) {
+        const int tile = item % ntile, h = (item / ntile) % p.H;
+        const cpdr_fragment f = p.frags[p.items[item / (ntile * p.H)]];
+        const int col = tile * BVT + c;            // value dim of this thread
+        const int64_t sidx = ((int64_t)f.seg * p.H + h) * D * D;
+        // token vectors of token t into shared memory
+        auto load_tok = [&](int64_t t, bool with_q) {
+            const int64_t th = t * p.H + h;
+            for (int d = tid; d < D; d += BT) {
+                kk[d] = ldv(k, th * D + d);
+                if (with_q) qq[d] = ldv(q, th * D + d);
+                al[d] = exp2f(p.g[PERDIM ? th * D + d : th] * 1.4426950408889634f);
+            }
+            if (tid < BVT) {
+                vv[tid] = ldv(v, th * D + tile * BVT + tid);
+                if (with_q) dd[tid] = p.scale * ldv(dout, th * D + tile * BVT + tid);
+            }
+            if (tid == 0) sb = ldv(beta, th);
+        };
+        // one forward token on the register state s (rows r8 + 8 i, column col)
+        auto fwd_tok = [&](float (&s)[NR]) {
+            float pk = 0.f;
+#pragma unroll
+            for (int i = 0; i < NR; i++) {
+                s[i] *= al[r8 + 8 * i];
+                pk = fmaf(s[i], kk[r8 + 8 * i], pk);
+            }
+            pk += __shfl_xor_sync(0xffffffffu, pk, 1);
+            pk += __shfl_xor_sync(0xffffffffu, pk, 2);
+            pk += __shfl_xor_sync(0xffffffffu, pk, 4);
+            const float bu = sb * (vv[c] - pk);
+#pragma unroll
+            for (int i = 0; i < NR; i++) s[i] = fmaf(kk[r8 + 8 * i], bu, s[i]);
+        };
+        // ---- forward: checkpoints at every 64-token boundary
+        float s[NR];
+#pragma unroll
+        for (int i = 0; i < NR; i++)
+            s[i] = (f.flags & CPDR_FRAG_CONT_PREV) ? p.S_init[sidx + (int64_t)(r8 + 8 * i) * D + col] : 0.f;
+        const int nck = (f.len + CKB - 1) / CKB;
+        for (int t = 0; t < f.len; t++) {
+            if (t % CKB == 0) {
+#pragma unroll
+                for (int i = 0; i < NR; i++) ck[((int64_t)(t / CKB) * BVT * 8 + tid) * NR + i] = s[i];
+            }
+            __syncthreads();
+            load_tok(f.tok0 + t, false);
+            __syncthreads();
+            fwd_tok(s);
+        }
+        // ---- the end gradient
+        float G[NR];
+        {
+            const float *src = nullptr;
+            int64_t base = 0;
+            if (f.flags & CPDR_FRAG_ENDS_SEQ) {
+                if (p.dht) { src = p.dht; base = ((int64_t)f.seq * p.H + h) * D * D; }
+            } else if ((f.flags & CPDR_FRAG_CONT_NEXT) && p.mode == 1) {
+                src = p.dS_end;
+                base = sidx;
+            }
+#pragma unroll
+            for (int i = 0; i < NR; i++) G[i] = src ? src[base + (int64_t)(r8 + 8 * i) * D + col] : 0.f;
+        }
+        // ---- reverse over the chunks
+        for (int m = nck - 1; m >= 0; m--) {
+            const int t0 = m * CKB, nb = min(CKB, f.len - t0);
+#pragma unroll
+            for (int i = 0; i < NR; i++) s[i] = ck[((int64_t)m * BVT * 8 + tid) * NR + i];
+            for (int i0 = 0; i0 < nb; i0++) {
+#pragma unroll
+                for (int i = 0; i < NR; i++) tok[((int64_t)i0 * BVT * 8 + tid) * NR + i] = s[i];
+                __syncthreads();
+                load_tok(f.tok0 + t0 + i0, false);
+                __syncthreads();
+                fwd_tok(s);
+            }
+            // s = state after the chunk's last token
+            for (int i0 = nb - 1; i0 >= 0; i0--) {
+                const int64_t t = f.tok0 + t0 + i0, th = t * p.H + h;
+                float sp[NR];
+#pragma unroll
+                for (int i = 0; i < NR; i++) sp[i] = tok[((int64_t)i0 * BVT * 8 + tid) * NR + i];
+                __syncthreads();
+                load_tok(t, true);
+                __syncthreads();
+                const float b = sb;
+                // dq partial (S_t do) and G += q do^T; P = Diag(alpha) S_{t-1}
+                float pdq[NR], pk = 0.f, gk = 0.f;
+#pragma unroll
+                for (int i = 0; i < NR; i++) {
+                    const int d = r8 + 8 * i;
+                    pdq[i] = s[i] * dd[c];
+                    G[i] = fmaf(qq[d], dd[c], G[i]);
+                    pk = fmaf(al[d] * sp[i], kk[d], pk);
+                    gk = fmaf(G[i], kk[d], gk);
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    pk += __shfl_xor_sync(0xffffffffu, pk, o);
+                    gk += __shfl_xor_sync(0xffffffffu, gk, o);
+                }
+                const float u = vv[c] - pk, gu = b * gk;
+                if (p.mode == 1 && r8 == 0) p.dv[th * D + col] = gu;
+                // dk partial, dalpha partial, dbeta partial; then G <- Diag(alpha) dP
+                float pdk[NR], pda[NR], pb = 0.f;
+#pragma unroll
+                for (int i = 0; i < NR; i++) {
+                    const int d = r8 + 8 * i;
+                    const float Gu = G[i] * u;
+                    pb = fmaf(kk[d], Gu, pb);
+                    pdk[i] = b * Gu - al[d] * sp[i] * gu;
+                    const float dP = G[i] - kk[d] * gu;
+                    pda[i] = dP * sp[i];             // dP * S_{t-1}
+                    G[i] = al[d] * dP;
+                }
+                if (p.mode == 1) {
+                    // sum over the warp's 4 columns, then across the 8 warps
+#pragma unroll
+                    for (int i = 0; i < NR; i++) {
+#pragma unroll
+                        for (int o = 8; o < 32; o <<= 1) {
+                            pdq[i] += __shfl_xor_sync(0xffffffffu, pdq[i], o);
+                            pdk[i] += __shfl_xor_sync(0xffffffffu, pdk[i], o);
+                            pda[i] += __shfl_xor_sync(0xffffffffu, pda[i], o);
+                        }
+                    }
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) pb += __shfl_xor_sync(0xffffffffu, pb, o);
+                    if (lane < 8) {
+#pragma unroll
+                        for (int i = 0; i < NR; i++) {
+                            red[w][0][lane + 8 * i] = pdq[i];
+                            red[w][1][lane + 8 * i] = pdk[i];
+                            red[w][2][lane + 8 * i] = pda[i];
+                        }
+                    }
+                    if (lane == 0) redb[w] = pb;
+                    __syncthreads();
+                    for (int e = tid; e < 3 * D; e += BT) {
+                        const int which = e / D, d = e % D;
+                        float acc = 0.f;
+#pragma unroll
+                        for (int ww = 0; ww < 8; ww++) acc += red[ww][which][d];
+                        if (which == 0) atomicAdd(p.dq + th * D + d, acc);
+                        else if (which == 1) atomicAdd(p.dk + th * D + d, acc);
+                        else if (PERDIM) atomicAdd(p.dg + th * D + d, al[d] * acc);
+                        else red[0][2][d] = al[d] * acc;   // scalar gate: summed below
+                    }
+                    if (tid == 0) {
+                        float acc = 0.f;
+#pragma unroll
+                        for (int ww = 0; ww < 8; ww++) acc += redb[ww];
+                        atomicAdd(p.dbeta + th, acc);
+                    }
+                    if (!PERDIM) {
+                        __syncthreads();
+                        if (w == 0) {
+                            float acc = 0.f;
+                            for (int d = lane; d < D; d += 32) acc += red[0][2][d];
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                            if (lane == 0) atomicAdd(p.dg + th, acc);
+                        }
+                    }
+                }
+                // the state before this token is the next one's S_t
+#pragma unroll
+                for (int i = 0; i < NR; i++) s[i] = sp[i];
+            }
+        }
+        // ---- the pre-process keeps the gradient at the fragment start
+        if (p.mode == 0) {
+#pragma unroll
+            for (int i = 0; i < NR; i++) p.dS_ext[sidx + (int64_t)(r8 + 8 * i) * D + col] = G[i];
+        }
+        __syncthreads();
+    }
+}
+
+// Reverse merge: grid (chains, H, D / BVT); thread = rows r8 + 8 i of one column.
+template <int D>
+__global__ void __launch_bounds__(BT) bwd_merge_kernel(const MergeChain *__restrict__ chains,
+                                                       const float *__restrict__ dS_ext, const float *__restrict__ M,
+                                                       float *__restrict__ dS_end, int H, int B) {
+    constexpr int NR = D / 8;
+    __shared__ float Gs[D][BVT + 1];
+    const MergeChain ch = chains[blockIdx.x];
+    const int h = blockIdx.y, tile = blockIdx.z;
+    const int c = threadIdx.x >> 3, r8 = threadIdx.x & 7, col = tile * BVT + c;
+    auto idx_of = [&](int r) { return ((int64_t)(r * B + ch.b) * H + h) * D * D; };
+    float G[NR];
+#pragma unroll
+    for (int i = 0; i < NR; i++) {
+        G[i] = dS_ext[idx_of(ch.r1) + (int64_t)(r8 + 8 * i) * D + col];
+        dS_end[idx_of(ch.r1 - 1) + (int64_t)(r8 + 8 * i) * D + col] = G[i];
+    }
+    for (int j = ch.r1 - 1; j > ch.r0; j--) {
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < NR; i++) Gs[r8 + 8 * i][c] = G[i];
+        __syncthreads();
+        const float *Mj = M + idx_of(j);
+#pragma unroll
+        for (int i = 0; i < NR; i++) {
+            const int d = r8 + 8 * i;
+            float acc = dS_ext[idx_of(j) + (int64_t)d * D + col];
+            for (int l = 0; l < D; l++) acc = fmaf(__ldg(Mj + (int64_t)l * D + d), Gs[l][c], acc);   // (M^T G)[d]
+            G[i] = acc;
+            dS_end[idx_of(j - 1) + (int64_t)d * D + col] = acc;
+        }
+    }
+}
+
+template <typename TIn, int D, bool PERDIM>
+int launch_chain_t(const BwdParams &prm, int grid, cudaStream_t st) {
+    bwd_chain_kernel<TIn, D, PERDIM><<<grid, BT, 0, st>>>(prm);
+    return (int)cudaGetLastError();
+}
+
+template <int D>
+int dispatch_chain(const cpdr_ctx *c, const BwdParams &prm, int grid, cudaStream_t st) {
+    const bool perdim = c->plan.gate_kind == CPDR_GATE_PER_DIM;
+    if (c->plan.in_dtype == CPDR_DTYPE_F32)
+        return perdim ? launch_chain_t<float, D, true>(prm, grid, st) : launch_chain_t<float, D, false>(prm, grid, st);
+    return perdim ? launch_chain_t<__nv_bfloat16, D, true>(prm, grid, st)
+                  : launch_chain_t<__nv_bfloat16, D, false>(prm, grid, st);
+}
+
+}  // namespace
+
+int bwd_grid(const cpdr_ctx *c) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+    const int64_t work = (int64_t)c->plan.frags.size() * c->plan.H * (c->plan.dk / BVT);
+    return (int)std::max<int64_t>(1, std::min<int64_t>(work, (int64_t)sms * 4));
+}
+
+size_t bwd_scratch_floats_per_cta(const cpdr_ctx *c) {
+    const auto &p = c->plan;
+    int32_t maxlen = 0;
+    for (const auto &f : p.frags) maxlen = std::max(maxlen, f.len);
+    const int64_t nck = (maxlen + CKB - 1) / CKB;
+    return (size_t)(nck + CKB) * p.dk * BVT;
+}
+
+int launch_bwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta, const float *g,
+               const void *dout, const float *dht, const float *S_init, const float *M, float *dS_ext,
+               float *dS_end, float *scratch, float *dq, float *dk, float *dv, float *dbeta, float *dg,
+               void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    const auto &p = c->plan;
+    BwdParams prm{};
+    prm.frags = c->dev.frags;
+    prm.H = p.H;
+    prm.B = p.B;
+    prm.scale = p.scale;
+    prm.q = q; prm.k = k; prm.v = v; prm.beta = beta; prm.dout = dout; prm.g = g;
+    prm.dht = dht; prm.S_init = S_init; prm.dS_end = dS_end; prm.dS_ext = dS_ext;
+    prm.dq = dq; prm.dk = dk; prm.dv = dv; prm.dbeta = dbeta; prm.dg = dg;
+    prm.scratch = scratch;
+    prm.ckpt_floats = (int64_t)bwd_scratch_floats_per_cta(c) - (int64_t)CKB * p.dk * BVT;
+    const int grid = bwd_grid(c);
+    int rc = 0;
+    // 1. the pre-process: segments' first fragments that continue a sequence
+    if (!p.bwd_pre_items.empty()) {
+        prm.items = c->dev.bwd_pre_items;
+        prm.n_items = (int)p.bwd_pre_items.size();
+        prm.mode = 0;
+        rc = p.dk == 64 ? dispatch_chain<64>(c, prm, grid, st) : dispatch_chain<128>(c, prm, grid, st);
+        if (rc) return rc;
+    }
+    // 2. the reverse merge
+    if (!p.chains.empty()) {
+        dim3 mg((unsigned)p.chains.size(), (unsigned)p.H, (unsigned)(p.dk / BVT));
+        if (p.dk == 64)
+            bwd_merge_kernel<64><<<mg, BT, 0, st>>>(c->dev.chains, dS_ext, M, dS_end, p.H, p.B);
+        else
+            bwd_merge_kernel<128><<<mg, BT, 0, st>>>(c->dev.chains, dS_ext, M, dS_end, p.H, p.B);
+        rc = (int)cudaGetLastError();
+        if (rc) return rc;
+    }
+    // 3. every fragment, with its end gradient
+    prm.items = c->dev.fwd_order;
+    prm.n_items = (int)p.frags.size();
+    prm.mode = 1;
+    return p.dk == 64 ? dispatch_chain<64>(c, prm, grid, st) : dispatch_chain<128>(c, prm, grid, st);
+}
+
+}  // namespace cpdr

@@ -89,6 +89,7 @@ struct Plan {
     // host-buffer path: fragments in kHostParts groups of consecutive memory
     // tokens, so that the forward of a group can start once its q is in and
     // its o can leave while the next group runs
+    std::vector<int32_t> bwd_pre_items;      // fragments continuing a sequence (backward pre-process)
     std::vector<int32_t> host_items;         // fragments, group by group (longest first inside)
     int32_t host_part_off[kHostParts + 1] = {};   // group g: host_items[off[g] .. off[g+1])
     int64_t host_part_tok[kHostParts + 1] = {};   // group g: memory tokens [tok[g], tok[g+1])
@@ -116,6 +117,7 @@ struct DeviceTables {
     WyChunk *wy_chunks = nullptr;
     ConvTile *conv_tiles = nullptr;
     int32_t *host_items = nullptr;
+    int32_t *bwd_pre_items = nullptr;
     int64_t *conv_halo = nullptr;
     int32_t *status = nullptr;   // device status word (bounded waits)
 };
@@ -171,6 +173,13 @@ int launch_tc_wy(const cpdr_ctx *c, const void *k, const void *beta, const float
                  void *stream);
 int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy,
                   float *S_ext, float *M, void *stream);
+// Backward (bwd.cu): scratch per CTA and the grid it is sized for.
+size_t bwd_scratch_floats_per_cta(const cpdr_ctx *c);
+int bwd_grid(const cpdr_ctx *c);
+int launch_bwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta, const float *g,
+               const void *dout, const float *dht, const float *S_init, const float *M, float *dS_ext,
+               float *dS_end, float *scratch, float *dq, float *dk, float *dv, float *dbeta, float *dg,
+               void *stream);
 int launch_conv1d(const cpdr_ctx *c, const void *x, const float *weight, const float *bias, int channels,
                   int activation, void *y, void *stream);
 int launch_tc_fwd(const cpdr_ctx *c, const int32_t *items, int n_items, const void *q, const void *k, const void *v,

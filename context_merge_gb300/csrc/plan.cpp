@@ -190,6 +190,8 @@ cpdr_status build_plan(const cpdr_desc &d, Plan &p, std::string &err) {
         p.host_part_tok[kHostParts] = cursor;
         if (cursor != total) return fail(err, CPDR_ERR_INVALID, "internal: fragments do not tile the token axis");
     }
+    for (size_t i = 0; i < p.frags.size(); i++)
+        if (p.frags[i].flags & CPDR_FRAG_CONT_PREV) p.bwd_pre_items.push_back((int32_t)i);
     // longest pre items first as well
     std::stable_sort(p.pre_items.begin(), p.pre_items.end(),
                      [&](int32_t a, int32_t b) { return p.frags[a].len > p.frags[b].len; });

@@ -252,6 +252,37 @@ cpdr_status cpdr_fwd(const cpdr_ctx *ctx, const void *q, const void *k, const vo
 cpdr_status cpdr_conv1d_fwd(const cpdr_ctx *ctx, const void *x, const float *weight, const float *bias,
                             int32_t channels, int32_t activation, void *y, void *stream);
 
+/*
+ * Backward ([FLA-CP] §2.2 and §4 split it into a pre-process, the merge run
+ * in reverse with the transposed transfer matrices, and state-gradient
+ * chains): the gradients of  sum_t <do_t, o_t> + sum_n <dht_n, final_state_n>
+ * with respect to q, k, v, beta and the gate, for the same inputs the
+ * forward ran on.
+ *   1. each segment's first fragment that continues a sequence runs the
+ *      reverse chain from its local end gradient (dht if its sequence ends
+ *      there, else 0) and keeps the state gradient at its start, dS_ext;
+ *   2. per sequence crossing cuts:  G = dS_ext[r1];
+ *      for j = r1-1 .. r0+1:  G <- M_j^T G + dS_ext[j]  (the gradient at the
+ *      end of every continuing fragment);
+ *   3. every fragment runs the reverse chain from that end gradient (or dht,
+ *      or 0) and writes the input gradients.
+ * The reverse chain is the per-token chain rule, on CUDA cores in fp32,
+ * with the forward states recomputed from S_init per token.
+ * In (device): q, k, v, beta, gate and do ([B, T, H, dv], the input dtype)
+ * as for cpdr_fwd; dht [N, H, dk, dv] fp32 or NULL (zero); S_init and M as
+ * cpdr_merge and cpdr_preprocess left them for these inputs.  Out (device,
+ * fp32, zeroed and written here): dq, dk [B, T, H, dk], dv [B, T, H, dv],
+ * dbeta [B, T, H], dgate (the gate's shape).  workspace: device memory of
+ * cpdr_bwd_workspace_bytes() bytes, 256-byte aligned.
+ * Errors: CPDR_ERR_UNSUPPORTED for grouped query heads or the [dv, dk]
+ * state layout; CPDR_ERR_WORKSPACE; CPDR_ERR_INVALID; CPDR_ERR_CUDA.
+ */
+cpdr_status cpdr_bwd_workspace_bytes(const cpdr_ctx *ctx, size_t *bytes);
+cpdr_status cpdr_bwd(const cpdr_ctx *ctx, const void *q, const void *k, const void *v, const void *beta,
+                     const float *gate, const void *dout, const float *dht, const float *S_init, const float *M,
+                     float *dq, float *dk, float *dv, float *dbeta, float *dgate, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
 /* pre_num_conv_tokens ([FLA-CP] §3.3) per segment, host memory: how many of
  * the W - 1 tokens before segment s's start belong to its first sequence
  * (0 when the segment starts a sequence), out[0 .. min(cap, nseg)). */

@@ -1,0 +1,93 @@
+"""GPU parity of the backward (cpdr_bwd) against the fp64 backward oracle
+(the reverse of the per-token scan, pinned by finite differences): the
+article's cut patterns at R = 2/4/8, fixed rows, packed batches with short
+and empty sequences, the zigzag layout, both gates and both dtypes, with and
+without a final-state gradient.  The forward path (WY build, pre-process,
+merge) runs first through the C-ABI and its S_init and M feed the backward.
+
+Bars, per gradient tensor and per (sequence, head), ||x - ref|| / ||ref||:
+fp32 inputs 1e-4 (fp32 arithmetic everywhere, forward included); bf16
+inputs 5e-3, the article's gradient acceptance line ([FLA-CP] §5.2) -- the
+backward itself is fp32, but S_init and M come from the tensor-core forward,
+whose bf16 operands carry about 1e-3 relative error into the states."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from context_merge_gb300 import cpdr, inputs
+from oracle import layout as olayout
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda(cpdr_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    torch.cuda.set_device(0)
+
+
+def run_case(w, lengths=None, with_dht=True, seed=7, **kw):
+    inp = inputs.make_inputs(w, device="cpu", lengths=lengths, **kw)
+    B, T, H, d, R = inp["B"], inp["T"], inp["H"], inp["d"], inp["R"]
+    gen = torch.Generator().manual_seed(seed)
+    do = torch.randn((B, T, H, d), generator=gen).to(w.torch_dtype)
+    N = B if inp["cu_seqlens"] is None else len(inp["cu_seqlens"]) - 1
+    dht = torch.randn((N, H, d, d), generator=gen) if with_dht else None
+    zig = w.layout == "zigzag"
+    ctx = cpdr.Context(B, T, H, d, R, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"], layout=w.layout)
+    place = (lambda x: olayout.to_zigzag(x, R)) if zig else (lambda x: x)
+    dev = {k: place(inp[k]).contiguous().cuda() for k in ("q", "k", "v", "beta", "g")}
+    o, bufs = ctx.run(dev["q"], dev["k"], dev["v"], dev["beta"], dev["g"])
+    grads = ctx.backward(dev["q"], dev["k"], dev["v"], dev["beta"], dev["g"], place(do).contiguous().cuda(),
+                         bufs["S_init"], bufs["M"], dht=dht.cuda() if dht is not None else None)
+    torch.cuda.synchronize()
+    ctx.check_device_status()
+    unplace = (lambda x: olayout.from_zigzag(x, R)) if zig else (lambda x: x)
+    got = {k: unplace(v.cpu()).double().numpy() for k, v in grads.items()}
+    ref = oracle.Problem(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], cu_seqlens=inp["cu_seqlens"]).backward(
+        do, dht=dht.double().numpy() if dht is not None else None)
+    cu = [int(x) for x in inp["cu_seqlens"]] if inp["cu_seqlens"] is not None else None
+    errs = {}
+    for key in ("dq", "dk", "dv", "dbeta", "dg"):
+        worst = 0.0
+        spans = [(b, 0, T) for b in range(B)] if cu is None else [(0, cu[n], cu[n + 1]) for n in range(len(cu) - 1)]
+        for b, s, e in spans:
+            if e == s:
+                continue
+            for h in range(H):
+                x, r = got[key][b, s:e, h], ref[key][b, s:e, h]
+                den = np.linalg.norm(r)
+                num = np.linalg.norm(x - r)
+                worst = max(worst, float(num / den) if den > 0 else float(num > 0) * np.inf)
+        errs[key] = worst
+    tol = 1e-4 if w.dtype == "fp32" else 5e-3
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"over tolerance: {bad} (all: {errs})"
+    return errs
+
+
+CUTS = [([3000, 4000, 3240], 2), ([7000, 3240], 4), ([400, 624], 2), ([2048], 8), ([300, 0, 17, 700, 7], 4)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("gate", ["gdn", "kda"])
+@pytest.mark.parametrize("cut", CUTS, ids=[f"R{r}-{'-'.join(map(str, l))}" for l, r in CUTS])
+def test_backward_cut_patterns(cut, gate, dtype):
+    lengths, R = cut
+    base = inputs.WORKLOADS["kda_bf16_t32768_h32_d128_r16" if gate == "kda" else "gdn_bf16_b2_t8192_h16_d128_r8"]
+    w = inputs.Workload("bwd", gate, dtype, 1, sum(lengths), 2, 128, R, gate_dist=base.gate_dist, seed=41)
+    print(cut, gate, dtype, run_case(w, lengths=lengths))
+
+
+@pytest.mark.parametrize("case", [
+    dict(B=2, T=1024, R=4, d=128, layout="contiguous", dht=True),
+    dict(B=3, T=192, R=3, d=64, layout="contiguous", dht=False),
+    dict(B=1, T=1024, R=2, d=128, layout="zigzag", dht=True),
+    dict(B=1, T=130, R=1, d=64, layout="contiguous", dht=True),
+])
+def test_backward_rows_and_layouts(case):
+    w = inputs.Workload("bwd", "gdn", "bf16", case["B"], case["T"], 2, case["d"], case["R"], seed=43,
+                        layout=case["layout"])
+    print(case, run_case(w, with_dht=case["dht"]))
