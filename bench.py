@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-heads", type=int, default=4)
     ap.add_argument("--force-simt", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward (gradients of the forward) instead of the forward")
     # profiling aids: shrink the workload (same shapes otherwise) for ncu captures
     ap.add_argument("--T", type=int, default=None, help="override tokens per row (profiling only)")
     ap.add_argument("--H", type=int, default=None, help="override heads (profiling only)")
@@ -521,6 +523,74 @@ def run_conv(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- backward
+BWD_METRIC = "tokens/sec (backward: gradients of q, k, v, beta, gate; 1 GB300)"
+
+
+def bwd_oracle_sample(inp, w, heads=1):
+    """Time the fp64 backward oracle on the first `heads` heads, full T."""
+    import oracle
+    hs = min(heads, inp["H"])
+    sub = {k: inp[k][:, :, :hs].contiguous().cpu() for k in ("q", "k", "v", "beta", "g")}
+    do = torch.randn(sub["v"].shape, generator=torch.Generator().manual_seed(5)).to(sub["v"].dtype)
+    P = oracle.Problem(sub["q"], sub["k"], sub["v"], sub["beta"], sub["g"], cu_seqlens=inp["cu_seqlens"])
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    P.backward(do, nthreads=threads)
+    return time.perf_counter() - t0, inp["B"] * inp["T"] * hs, threads
+
+
+def run_backward(args, ws, rank):
+    from context_merge_gb300 import cpdr
+    w = inputs.WORKLOADS[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = inputs.make_inputs(w, device=dev, seed=w.seed + 1000 * rank, T=args.T, H=args.H)
+    B, T, H, d, R = inp["B"], inp["T"], inp["H"], inp["d"], inp["R"]
+    ctx = cpdr.Context(B, T, H, d, R, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"],
+                       force_simt=args.force_simt)
+    q, k, v, beta, g = (inp[x] for x in ("q", "k", "v", "beta", "g"))
+    o, bufs = ctx.run(q, k, v, beta, g)
+    do = torch.randn(v.shape, device=dev, dtype=torch.float32).to(v.dtype)
+    dht = torch.randn(bufs["final_state"].shape, device=dev)
+    work = torch.empty(ctx.bwd_workspace_bytes(), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    step = lambda: ctx.backward(q, k, v, beta, g, do, bufs["S_init"], bufs["M"], dht=dht, workspace=work,
+                                stream=stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ctx.check_device_status()
+    clocks = ClockSampler() if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop() if clocks else None
+    ms = max_over_ranks(start.elapsed_time(end), ws) / args.steps
+    if rank != 0:
+        return
+    tokens = B * T
+    cpu = None
+    if not args.no_cpu_baseline:
+        dt, ht, threads = bwd_oracle_sample(inp, w)
+        cpu = {"value": ht / H / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"fp64 backward oracle on 1 of {H} heads, full T ({dt:.1f} s wall); tokens scaled by heads"}
+    line = {"metric": BWD_METRIC, "value": tokens * ws / (ms / 1e3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "op": "backward", "B": B, "T": T, "H": H, "d": d, "R": R,
+                       "gate": w.gate, "in_dtype": w.dtype, "parallelism": f"replicas{ws}"},
+            "roofline": None, "cpu_baseline": cpu, "e2e": None, "gpu_launches": None, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup(args)
@@ -529,6 +599,8 @@ def main():
         (run_conv_reference if conv else run_reference)(args, ws, rank)
     elif conv:
         run_conv(args, ws, rank)
+    elif args.backward:
+        run_backward(args, ws, rank)
     else:
         run_ours(args, ws, rank, local)
     if ws > 1:

@@ -23,6 +23,7 @@
 // The forward states are recomputed per token: from S_init (or zero) the
 // chain first stores the state at every 64-token boundary, then walks the
 // chunks backwards, recomputing each chunk's states into a per-CTA scratch.
+// Each token's vectors are loaded while the previous token is processed.
 //
 // One CTA = one (fragment, head, 32-value-column tile), persistent over the
 // work list.  A thread holds D/8 rows of one column (column = thread / 8),
@@ -65,12 +66,13 @@ struct BwdParams {
 };
 
 template <typename TIn, int D, bool PERDIM>
-__global__ void __launch_bounds__(BT) bwd_chain_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(BT, 2) bwd_chain_kernel(const __grid_constant__ BwdParams p) {
     constexpr int NR = D / 8;                      // rows per thread
-    __shared__ float kk[D], qq[D], al[D], vv[BVT], dd[BVT];
+    // token vectors, double-buffered: the next token's are loaded while the
+    // current one is processed (one barrier per token)
+    __shared__ float kk[2][D], qq[2][D], al[2][D], vv[2][BVT], dd[2][BVT], sbv[2];
     __shared__ float red[8][3][D];                 // per-warp partial sums over columns: dq, dk, dalpha
     __shared__ float redb[8];
-    __shared__ float sb;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int c = tid >> 3, r8 = tid & 7;          // column in the tile, row group
     const int ntile = D / BVT;
@@ -83,34 +85,70 @@ __global__ void __launch_bounds__(BT) bwd_chain_kernel(const __grid_constant__ B
         const cpdr_fragment f = p.frags[p.items[item / (ntile * p.H)]];
         const int col = tile * BVT + c;            // value dim of this thread
         const int64_t sidx = ((int64_t)f.seg * p.H + h) * D * D;
-        // token vectors of token t into shared memory
-        auto load_tok = [&](int64_t t, bool with_q) {
-            const int64_t th = t * p.H + h;
-            for (int d = tid; d < D; d += BT) {
-                kk[d] = ldv(k, th * D + d);
-                if (with_q) qq[d] = ldv(q, th * D + d);
-                al[d] = exp2f(p.g[PERDIM ? th * D + d : th] * 1.4426950408889634f);
+        // this thread's share of a token's vectors: threads < D the key-dim
+        // entries, the next BVT the value columns, the next one beta
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f;
+        auto fetch = [&](int t, bool with_q) {
+            const int64_t th = (f.tok0 + t) * p.H + h;
+            if (tid < D) {
+                x0 = ldv(k, th * D + tid);
+                x1 = with_q ? ldv(q, th * D + tid) : 0.f;
+                x2 = exp2f(p.g[PERDIM ? th * D + tid : th] * 1.4426950408889634f);
+            } else if (tid < D + BVT) {
+                x0 = ldv(v, th * D + tile * BVT + tid - D);
+                x1 = with_q ? p.scale * ldv(dout, th * D + tile * BVT + tid - D) : 0.f;
+            } else if (tid == D + BVT) {
+                x0 = ldv(beta, th);
             }
-            if (tid < BVT) {
-                vv[tid] = ldv(v, th * D + tile * BVT + tid);
-                if (with_q) dd[tid] = p.scale * ldv(dout, th * D + tile * BVT + tid);
+        };
+        auto stash = [&](int b) {
+            if (tid < D) {
+                kk[b][tid] = x0;
+                qq[b][tid] = x1;
+                al[b][tid] = x2;
+            } else if (tid < D + BVT) {
+                vv[b][tid - D] = x0;
+                dd[b][tid - D] = x1;
+            } else if (tid == D + BVT) {
+                sbv[b] = x0;
             }
-            if (tid == 0) sb = ldv(beta, th);
         };
         // one forward token on the register state s (rows r8 + 8 i, column col)
-        auto fwd_tok = [&](float (&s)[NR]) {
+        auto fwd_tok = [&](float (&s)[NR], int b) {
             float pk = 0.f;
 #pragma unroll
             for (int i = 0; i < NR; i++) {
-                s[i] *= al[r8 + 8 * i];
-                pk = fmaf(s[i], kk[r8 + 8 * i], pk);
+                s[i] *= al[b][r8 + 8 * i];
+                pk = fmaf(s[i], kk[b][r8 + 8 * i], pk);
             }
             pk += __shfl_xor_sync(0xffffffffu, pk, 1);
             pk += __shfl_xor_sync(0xffffffffu, pk, 2);
             pk += __shfl_xor_sync(0xffffffffu, pk, 4);
-            const float bu = sb * (vv[c] - pk);
+            const float bu = sbv[b] * (vv[b][c] - pk);
 #pragma unroll
-            for (int i = 0; i < NR; i++) s[i] = fmaf(kk[r8 + 8 * i], bu, s[i]);
+            for (int i = 0; i < NR; i++) s[i] = fmaf(kk[b][r8 + 8 * i], bu, s[i]);
+        };
+        // forward over tokens [t0, t1) of the fragment from s; state before
+        // token t0 + i goes to dst[i] (dst null: the checkpoints instead)
+        auto forward = [&](float (&s)[NR], int t0, int t1, float *dst) {
+            __syncthreads();   // the previous pass's readers are done
+            fetch(t0, false);
+            stash(0);
+            __syncthreads();
+            for (int t = t0; t < t1; t++) {
+                const int b = (t - t0) & 1;
+                if (dst) {
+#pragma unroll
+                    for (int i = 0; i < NR; i++) dst[((int64_t)(t - t0) * BT + tid) * NR + i] = s[i];
+                } else if (t % CKB == 0) {
+#pragma unroll
+                    for (int i = 0; i < NR; i++) ck[((int64_t)(t / CKB) * BT + tid) * NR + i] = s[i];
+                }
+                if (t + 1 < t1) fetch(t + 1, false);
+                fwd_tok(s, b);
+                if (t + 1 < t1) stash(b ^ 1);
+                __syncthreads();
+            }
         };
         // ---- forward: checkpoints at every 64-token boundary
         float s[NR];
@@ -118,16 +156,7 @@ __global__ void __launch_bounds__(BT) bwd_chain_kernel(const __grid_constant__ B
         for (int i = 0; i < NR; i++)
             s[i] = (f.flags & CPDR_FRAG_CONT_PREV) ? p.S_init[sidx + (int64_t)(r8 + 8 * i) * D + col] : 0.f;
         const int nck = (f.len + CKB - 1) / CKB;
-        for (int t = 0; t < f.len; t++) {
-            if (t % CKB == 0) {
-#pragma unroll
-                for (int i = 0; i < NR; i++) ck[((int64_t)(t / CKB) * BVT * 8 + tid) * NR + i] = s[i];
-            }
-            __syncthreads();
-            load_tok(f.tok0 + t, false);
-            __syncthreads();
-            fwd_tok(s);
-        }
+        forward(s, 0, f.len, nullptr);
         // ---- the end gradient
         float G[NR];
         {
@@ -146,41 +175,36 @@ __global__ void __launch_bounds__(BT) bwd_chain_kernel(const __grid_constant__ B
         for (int m = nck - 1; m >= 0; m--) {
             const int t0 = m * CKB, nb = min(CKB, f.len - t0);
 #pragma unroll
-            for (int i = 0; i < NR; i++) s[i] = ck[((int64_t)m * BVT * 8 + tid) * NR + i];
-            for (int i0 = 0; i0 < nb; i0++) {
-#pragma unroll
-                for (int i = 0; i < NR; i++) tok[((int64_t)i0 * BVT * 8 + tid) * NR + i] = s[i];
-                __syncthreads();
-                load_tok(f.tok0 + t0 + i0, false);
-                __syncthreads();
-                fwd_tok(s);
-            }
+            for (int i = 0; i < NR; i++) s[i] = ck[((int64_t)m * BT + tid) * NR + i];
+            forward(s, t0, t0 + nb, tok);
             // s = state after the chunk's last token
+            fetch(t0 + nb - 1, true);
+            stash(0);
+            __syncthreads();
             for (int i0 = nb - 1; i0 >= 0; i0--) {
-                const int64_t t = f.tok0 + t0 + i0, th = t * p.H + h;
+                const int b = (nb - 1 - i0) & 1;
+                const int64_t th = (f.tok0 + t0 + i0) * p.H + h;
+                if (i0 > 0) fetch(t0 + i0 - 1, true);
                 float sp[NR];
 #pragma unroll
-                for (int i = 0; i < NR; i++) sp[i] = tok[((int64_t)i0 * BVT * 8 + tid) * NR + i];
-                __syncthreads();
-                load_tok(t, true);
-                __syncthreads();
-                const float b = sb;
+                for (int i = 0; i < NR; i++) sp[i] = tok[((int64_t)i0 * BT + tid) * NR + i];
+                const float bt = sbv[b];
                 // dq partial (S_t do) and G += q do^T; P = Diag(alpha) S_{t-1}
                 float pdq[NR], pk = 0.f, gk = 0.f;
 #pragma unroll
                 for (int i = 0; i < NR; i++) {
                     const int d = r8 + 8 * i;
-                    pdq[i] = s[i] * dd[c];
-                    G[i] = fmaf(qq[d], dd[c], G[i]);
-                    pk = fmaf(al[d] * sp[i], kk[d], pk);
-                    gk = fmaf(G[i], kk[d], gk);
+                    pdq[i] = s[i] * dd[b][c];
+                    G[i] = fmaf(qq[b][d], dd[b][c], G[i]);
+                    pk = fmaf(al[b][d] * sp[i], kk[b][d], pk);
+                    gk = fmaf(G[i], kk[b][d], gk);
                 }
 #pragma unroll
                 for (int o = 1; o < 8; o <<= 1) {
                     pk += __shfl_xor_sync(0xffffffffu, pk, o);
                     gk += __shfl_xor_sync(0xffffffffu, gk, o);
                 }
-                const float u = vv[c] - pk, gu = b * gk;
+                const float u = vv[b][c] - pk, gu = bt * gk;
                 if (p.mode == 1 && r8 == 0) p.dv[th * D + col] = gu;
                 // dk partial, dalpha partial, dbeta partial; then G <- Diag(alpha) dP
                 float pdk[NR], pda[NR], pb = 0.f;
@@ -188,11 +212,11 @@ __global__ void __launch_bounds__(BT) bwd_chain_kernel(const __grid_constant__ B
                 for (int i = 0; i < NR; i++) {
                     const int d = r8 + 8 * i;
                     const float Gu = G[i] * u;
-                    pb = fmaf(kk[d], Gu, pb);
-                    pdk[i] = b * Gu - al[d] * sp[i] * gu;
-                    const float dP = G[i] - kk[d] * gu;
+                    pb = fmaf(kk[b][d], Gu, pb);
+                    pdk[i] = bt * Gu - al[b][d] * sp[i] * gu;
+                    const float dP = G[i] - kk[b][d] * gu;
                     pda[i] = dP * sp[i];             // dP * S_{t-1}
-                    G[i] = al[d] * dP;
+                    G[i] = al[b][d] * dP;
                 }
                 if (p.mode == 1) {
                     // sum over the warp's 4 columns, then across the 8 warps
@@ -217,6 +241,7 @@ __global__ void __launch_bounds__(BT) bwd_chain_kernel(const __grid_constant__ B
                     }
                     if (lane == 0) redb[w] = pb;
                     __syncthreads();
+                    float dgs = 0.f;   // scalar gate: this thread's share of sum_d alpha dalpha
                     for (int e = tid; e < 3 * D; e += BT) {
                         const int which = e / D, d = e % D;
                         float acc = 0.f;
@@ -224,8 +249,8 @@ __global__ void __launch_bounds__(BT) bwd_chain_kernel(const __grid_constant__ B
                         for (int ww = 0; ww < 8; ww++) acc += red[ww][which][d];
                         if (which == 0) atomicAdd(p.dq + th * D + d, acc);
                         else if (which == 1) atomicAdd(p.dk + th * D + d, acc);
-                        else if (PERDIM) atomicAdd(p.dg + th * D + d, al[d] * acc);
-                        else red[0][2][d] = al[d] * acc;   // scalar gate: summed below
+                        else if (PERDIM) atomicAdd(p.dg + th * D + d, al[b][d] * acc);
+                        else dgs += al[b][d] * acc;
                     }
                     if (tid == 0) {
                         float acc = 0.f;
@@ -234,19 +259,16 @@ __global__ void __launch_bounds__(BT) bwd_chain_kernel(const __grid_constant__ B
                         atomicAdd(p.dbeta + th, acc);
                     }
                     if (!PERDIM) {
-                        __syncthreads();
-                        if (w == 0) {
-                            float acc = 0.f;
-                            for (int d = lane; d < D; d += 32) acc += red[0][2][d];
 #pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                            if (lane == 0) atomicAdd(p.dg + th, acc);
-                        }
+                        for (int o = 16; o > 0; o >>= 1) dgs += __shfl_xor_sync(0xffffffffu, dgs, o);
+                        if (lane == 0 && dgs != 0.f) atomicAdd(p.dg + th, dgs);
                     }
                 }
                 // the state before this token is the next one's S_t
 #pragma unroll
                 for (int i = 0; i < NR; i++) s[i] = sp[i];
+                if (i0 > 0) stash(b ^ 1);
+                __syncthreads();
             }
         }
         // ---- the pre-process keeps the gradient at the fragment start
@@ -254,7 +276,6 @@ __global__ void __launch_bounds__(BT) bwd_chain_kernel(const __grid_constant__ B
 #pragma unroll
             for (int i = 0; i < NR; i++) p.dS_ext[sidx + (int64_t)(r8 + 8 * i) * D + col] = G[i];
         }
-        __syncthreads();
     }
 }
 
