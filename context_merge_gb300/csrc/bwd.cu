@@ -23,7 +23,9 @@
 // The forward states are recomputed per token: from S_init (or zero) the
 // chain first stores the state at every 64-token boundary, then walks the
 // chunks backwards, recomputing each chunk's states into a per-CTA scratch.
-// Each token's vectors are loaded while the previous token is processed.
+// A chunk's token vectors are staged in shared memory at once, so the token
+// steps read no global memory; only the reverse pass's sums over the value
+// columns need a block barrier per token.
 //
 // One CTA = one (fragment, head, 32-value-column tile), persistent over the
 // work list.  A thread holds D/8 rows of one column (column = thread / 8),
@@ -65,14 +67,25 @@ struct BwdParams {
     int64_t ckpt_floats;      // max checkpoints per fragment * D * BVT
 };
 
+// Shared memory of one chunk's token vectors (raw input types; the gate as
+// alpha = e^g in fp32), then the per-warp partial sums of the reverse pass.
+template <typename TIn, int D, bool PERDIM>
+struct BwdSmem {
+    static constexpr int NA = PERDIM ? D : 1;
+    TIn kc[CKB][D], qc[CKB][D], vc[CKB][BVT], dc[CKB][BVT];
+    float ac[CKB][NA], bc[CKB];
+    float red[8][3][D];
+    float redb[8];
+};
+
+__device__ __forceinline__ float tof(float x) { return x; }
+__device__ __forceinline__ float tof(__nv_bfloat16 x) { return __bfloat162float(x); }
+
 template <typename TIn, int D, bool PERDIM>
 __global__ void __launch_bounds__(BT, 2) bwd_chain_kernel(const __grid_constant__ BwdParams p) {
     constexpr int NR = D / 8;                      // rows per thread
-    // token vectors, double-buffered: the next token's are loaded while the
-    // current one is processed (one barrier per token)
-    __shared__ float kk[2][D], qq[2][D], al[2][D], vv[2][BVT], dd[2][BVT], sbv[2];
-    __shared__ float red[8][3][D];                 // per-warp partial sums over columns: dq, dk, dalpha
-    __shared__ float redb[8];
+    extern __shared__ __align__(16) uint8_t bsm[];
+    BwdSmem<TIn, D, PERDIM> &sm = *reinterpret_cast<BwdSmem<TIn, D, PERDIM> *>(bsm);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int c = tid >> 3, r8 = tid & 7;          // column in the tile, row group
     const int ntile = D / BVT;
@@ -85,78 +98,60 @@ __global__ void __launch_bounds__(BT, 2) bwd_chain_kernel(const __grid_constant_
         const cpdr_fragment f = p.frags[p.items[item / (ntile * p.H)]];
         const int col = tile * BVT + c;            // value dim of this thread
         const int64_t sidx = ((int64_t)f.seg * p.H + h) * D * D;
-        // this thread's share of a token's vectors: threads < D the key-dim
-        // entries, the next BVT the value columns, the next one beta
-        float x0 = 0.f, x1 = 0.f, x2 = 0.f;
-        auto fetch = [&](int t, bool with_q) {
-            const int64_t th = (f.tok0 + t) * p.H + h;
-            if (tid < D) {
-                x0 = ldv(k, th * D + tid);
-                x1 = with_q ? ldv(q, th * D + tid) : 0.f;
-                x2 = exp2f(p.g[PERDIM ? th * D + tid : th] * 1.4426950408889634f);
-            } else if (tid < D + BVT) {
-                x0 = ldv(v, th * D + tile * BVT + tid - D);
-                x1 = with_q ? p.scale * ldv(dout, th * D + tile * BVT + tid - D) : 0.f;
-            } else if (tid == D + BVT) {
-                x0 = ldv(beta, th);
+        // all token vectors of tokens [t0, t0 + nb) into shared memory, every
+        // load independent (one latency per chunk); q and do for the reverse
+        auto stage = [&](int t0, int nb, bool with_q) {
+            __syncthreads();   // the previous chunk's readers are done
+            for (int e = tid; e < nb * D; e += BT) {
+                const int i = e / D, d = e % D;
+                const int64_t th = (f.tok0 + t0 + i) * p.H + h;
+                sm.kc[i][d] = k[th * D + d];
+                if (with_q) sm.qc[i][d] = q[th * D + d];
+                if (PERDIM) sm.ac[i][d] = exp2f(p.g[th * D + d] * 1.4426950408889634f);
             }
-        };
-        auto stash = [&](int b) {
-            if (tid < D) {
-                kk[b][tid] = x0;
-                qq[b][tid] = x1;
-                al[b][tid] = x2;
-            } else if (tid < D + BVT) {
-                vv[b][tid - D] = x0;
-                dd[b][tid - D] = x1;
-            } else if (tid == D + BVT) {
-                sbv[b] = x0;
+            for (int e = tid; e < nb * BVT; e += BT) {
+                const int i = e / BVT, cc = e % BVT;
+                const int64_t th = (f.tok0 + t0 + i) * p.H + h;
+                sm.vc[i][cc] = v[th * D + tile * BVT + cc];
+                if (with_q) sm.dc[i][cc] = dout[th * D + tile * BVT + cc];
             }
+            for (int i = tid; i < nb; i += BT) {
+                const int64_t th = (f.tok0 + t0 + i) * p.H + h;
+                sm.bc[i] = tof(beta[th]);
+                if (!PERDIM) sm.ac[i][0] = exp2f(p.g[th] * 1.4426950408889634f);
+            }
+            __syncthreads();
         };
-        // one forward token on the register state s (rows r8 + 8 i, column col)
-        auto fwd_tok = [&](float (&s)[NR], int b) {
+        auto alpha = [&](int i, int d) -> float { return PERDIM ? sm.ac[i][d] : sm.ac[i][0]; };
+        // one forward token (chunk row i) on the register state s
+        auto fwd_tok = [&](float (&s)[NR], int i) {
             float pk = 0.f;
 #pragma unroll
-            for (int i = 0; i < NR; i++) {
-                s[i] *= al[b][r8 + 8 * i];
-                pk = fmaf(s[i], kk[b][r8 + 8 * i], pk);
+            for (int j = 0; j < NR; j++) {
+                const int d = r8 + 8 * j;
+                s[j] *= alpha(i, d);
+                pk = fmaf(s[j], tof(sm.kc[i][d]), pk);
             }
             pk += __shfl_xor_sync(0xffffffffu, pk, 1);
             pk += __shfl_xor_sync(0xffffffffu, pk, 2);
             pk += __shfl_xor_sync(0xffffffffu, pk, 4);
-            const float bu = sbv[b] * (vv[b][c] - pk);
+            const float bu = sm.bc[i] * (tof(sm.vc[i][c]) - pk);
 #pragma unroll
-            for (int i = 0; i < NR; i++) s[i] = fmaf(kk[b][r8 + 8 * i], bu, s[i]);
-        };
-        // forward over tokens [t0, t1) of the fragment from s; state before
-        // token t0 + i goes to dst[i] (dst null: the checkpoints instead)
-        auto forward = [&](float (&s)[NR], int t0, int t1, float *dst) {
-            __syncthreads();   // the previous pass's readers are done
-            fetch(t0, false);
-            stash(0);
-            __syncthreads();
-            for (int t = t0; t < t1; t++) {
-                const int b = (t - t0) & 1;
-                if (dst) {
-#pragma unroll
-                    for (int i = 0; i < NR; i++) dst[((int64_t)(t - t0) * BT + tid) * NR + i] = s[i];
-                } else if (t % CKB == 0) {
-#pragma unroll
-                    for (int i = 0; i < NR; i++) ck[((int64_t)(t / CKB) * BT + tid) * NR + i] = s[i];
-                }
-                if (t + 1 < t1) fetch(t + 1, false);
-                fwd_tok(s, b);
-                if (t + 1 < t1) stash(b ^ 1);
-                __syncthreads();
-            }
+            for (int j = 0; j < NR; j++) s[j] = fmaf(tof(sm.kc[i][r8 + 8 * j]), bu, s[j]);
         };
         // ---- forward: checkpoints at every 64-token boundary
         float s[NR];
 #pragma unroll
-        for (int i = 0; i < NR; i++)
-            s[i] = (f.flags & CPDR_FRAG_CONT_PREV) ? p.S_init[sidx + (int64_t)(r8 + 8 * i) * D + col] : 0.f;
+        for (int j = 0; j < NR; j++)
+            s[j] = (f.flags & CPDR_FRAG_CONT_PREV) ? p.S_init[sidx + (int64_t)(r8 + 8 * j) * D + col] : 0.f;
         const int nck = (f.len + CKB - 1) / CKB;
-        forward(s, 0, f.len, nullptr);
+        for (int m = 0; m < nck; m++) {
+            const int t0 = m * CKB, nb = min(CKB, f.len - t0);
+#pragma unroll
+            for (int j = 0; j < NR; j++) ck[((int64_t)m * BT + tid) * NR + j] = s[j];
+            stage(t0, nb, false);
+            for (int i = 0; i < nb; i++) fwd_tok(s, i);
+        }
         // ---- the end gradient
         float G[NR];
         {
@@ -169,93 +164,104 @@ __global__ void __launch_bounds__(BT, 2) bwd_chain_kernel(const __grid_constant_
                 base = sidx;
             }
 #pragma unroll
-            for (int i = 0; i < NR; i++) G[i] = src ? src[base + (int64_t)(r8 + 8 * i) * D + col] : 0.f;
+            for (int j = 0; j < NR; j++) G[j] = src ? src[base + (int64_t)(r8 + 8 * j) * D + col] : 0.f;
         }
         // ---- reverse over the chunks
         for (int m = nck - 1; m >= 0; m--) {
             const int t0 = m * CKB, nb = min(CKB, f.len - t0);
+            stage(t0, nb, true);
 #pragma unroll
-            for (int i = 0; i < NR; i++) s[i] = ck[((int64_t)m * BT + tid) * NR + i];
-            forward(s, t0, t0 + nb, tok);
-            // s = state after the chunk's last token
-            fetch(t0 + nb - 1, true);
-            stash(0);
-            __syncthreads();
-            for (int i0 = nb - 1; i0 >= 0; i0--) {
-                const int b = (nb - 1 - i0) & 1;
-                const int64_t th = (f.tok0 + t0 + i0) * p.H + h;
-                if (i0 > 0) fetch(t0 + i0 - 1, true);
+            for (int j = 0; j < NR; j++) s[j] = ck[((int64_t)m * BT + tid) * NR + j];
+            for (int i = 0; i < nb; i++) {   // the chunk's states, before each token
+#pragma unroll
+                for (int j = 0; j < NR; j++) tok[((int64_t)i * BT + tid) * NR + j] = s[j];
+                fwd_tok(s, i);
+            }
+            // s = state after the chunk's last token; the state before token i
+            // is loaded one token ahead (spn), hiding the scratch latency
+            float spn[NR];
+#pragma unroll
+            for (int j = 0; j < NR; j++) spn[j] = tok[((int64_t)(nb - 1) * BT + tid) * NR + j];
+            for (int i = nb - 1; i >= 0; i--) {
+                const int64_t th = (f.tok0 + t0 + i) * p.H + h;
                 float sp[NR];
 #pragma unroll
-                for (int i = 0; i < NR; i++) sp[i] = tok[((int64_t)i0 * BT + tid) * NR + i];
-                const float bt = sbv[b];
+                for (int j = 0; j < NR; j++) sp[j] = spn[j];
+                if (i > 0) {
+#pragma unroll
+                    for (int j = 0; j < NR; j++) spn[j] = tok[((int64_t)(i - 1) * BT + tid) * NR + j];
+                }
+                const float bt = sm.bc[i], ddc = p.scale * tof(sm.dc[i][c]);
                 // dq partial (S_t do) and G += q do^T; P = Diag(alpha) S_{t-1}
                 float pdq[NR], pk = 0.f, gk = 0.f;
 #pragma unroll
-                for (int i = 0; i < NR; i++) {
-                    const int d = r8 + 8 * i;
-                    pdq[i] = s[i] * dd[b][c];
-                    G[i] = fmaf(qq[b][d], dd[b][c], G[i]);
-                    pk = fmaf(al[b][d] * sp[i], kk[b][d], pk);
-                    gk = fmaf(G[i], kk[b][d], gk);
+                for (int j = 0; j < NR; j++) {
+                    const int d = r8 + 8 * j;
+                    const float kd = tof(sm.kc[i][d]);
+                    pdq[j] = s[j] * ddc;
+                    G[j] = fmaf(tof(sm.qc[i][d]), ddc, G[j]);
+                    pk = fmaf(alpha(i, d) * sp[j], kd, pk);
+                    gk = fmaf(G[j], kd, gk);
                 }
 #pragma unroll
                 for (int o = 1; o < 8; o <<= 1) {
                     pk += __shfl_xor_sync(0xffffffffu, pk, o);
                     gk += __shfl_xor_sync(0xffffffffu, gk, o);
                 }
-                const float u = vv[b][c] - pk, gu = bt * gk;
+                const float u = tof(sm.vc[i][c]) - pk, gu = bt * gk;
                 if (p.mode == 1 && r8 == 0) p.dv[th * D + col] = gu;
                 // dk partial, dalpha partial, dbeta partial; then G <- Diag(alpha) dP
                 float pdk[NR], pda[NR], pb = 0.f;
 #pragma unroll
-                for (int i = 0; i < NR; i++) {
-                    const int d = r8 + 8 * i;
-                    const float Gu = G[i] * u;
-                    pb = fmaf(kk[b][d], Gu, pb);
-                    pdk[i] = bt * Gu - al[b][d] * sp[i] * gu;
-                    const float dP = G[i] - kk[b][d] * gu;
-                    pda[i] = dP * sp[i];             // dP * S_{t-1}
-                    G[i] = al[b][d] * dP;
+                for (int j = 0; j < NR; j++) {
+                    const int d = r8 + 8 * j;
+                    const float kd = tof(sm.kc[i][d]), al = alpha(i, d);
+                    const float Gu = G[j] * u;
+                    pb = fmaf(kd, Gu, pb);
+                    pdk[j] = bt * Gu - al * sp[j] * gu;
+                    const float dP = G[j] - kd * gu;
+                    pda[j] = dP * sp[j];             // dP * S_{t-1}
+                    G[j] = al * dP;
                 }
                 if (p.mode == 1) {
                     // sum over the warp's 4 columns, then across the 8 warps
 #pragma unroll
-                    for (int i = 0; i < NR; i++) {
+                    for (int j = 0; j < NR; j++) {
 #pragma unroll
                         for (int o = 8; o < 32; o <<= 1) {
-                            pdq[i] += __shfl_xor_sync(0xffffffffu, pdq[i], o);
-                            pdk[i] += __shfl_xor_sync(0xffffffffu, pdk[i], o);
-                            pda[i] += __shfl_xor_sync(0xffffffffu, pda[i], o);
+                            pdq[j] += __shfl_xor_sync(0xffffffffu, pdq[j], o);
+                            pdk[j] += __shfl_xor_sync(0xffffffffu, pdk[j], o);
+                            pda[j] += __shfl_xor_sync(0xffffffffu, pda[j], o);
                         }
                     }
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) pb += __shfl_xor_sync(0xffffffffu, pb, o);
+                    __syncthreads();   // the previous token's sums were read
                     if (lane < 8) {
 #pragma unroll
-                        for (int i = 0; i < NR; i++) {
-                            red[w][0][lane + 8 * i] = pdq[i];
-                            red[w][1][lane + 8 * i] = pdk[i];
-                            red[w][2][lane + 8 * i] = pda[i];
+                        for (int j = 0; j < NR; j++) {
+                            sm.red[w][0][lane + 8 * j] = pdq[j];
+                            sm.red[w][1][lane + 8 * j] = pdk[j];
+                            sm.red[w][2][lane + 8 * j] = pda[j];
                         }
                     }
-                    if (lane == 0) redb[w] = pb;
+                    if (lane == 0) sm.redb[w] = pb;
                     __syncthreads();
                     float dgs = 0.f;   // scalar gate: this thread's share of sum_d alpha dalpha
                     for (int e = tid; e < 3 * D; e += BT) {
                         const int which = e / D, d = e % D;
                         float acc = 0.f;
 #pragma unroll
-                        for (int ww = 0; ww < 8; ww++) acc += red[ww][which][d];
+                        for (int ww = 0; ww < 8; ww++) acc += sm.red[ww][which][d];
                         if (which == 0) atomicAdd(p.dq + th * D + d, acc);
                         else if (which == 1) atomicAdd(p.dk + th * D + d, acc);
-                        else if (PERDIM) atomicAdd(p.dg + th * D + d, al[b][d] * acc);
-                        else dgs += al[b][d] * acc;
+                        else if (PERDIM) atomicAdd(p.dg + th * D + d, alpha(i, d) * acc);
+                        else dgs += alpha(i, d) * acc;
                     }
                     if (tid == 0) {
                         float acc = 0.f;
 #pragma unroll
-                        for (int ww = 0; ww < 8; ww++) acc += redb[ww];
+                        for (int ww = 0; ww < 8; ww++) acc += sm.redb[ww];
                         atomicAdd(p.dbeta + th, acc);
                     }
                     if (!PERDIM) {
@@ -266,15 +272,13 @@ __global__ void __launch_bounds__(BT, 2) bwd_chain_kernel(const __grid_constant_
                 }
                 // the state before this token is the next one's S_t
 #pragma unroll
-                for (int i = 0; i < NR; i++) s[i] = sp[i];
-                if (i0 > 0) stash(b ^ 1);
-                __syncthreads();
+                for (int j = 0; j < NR; j++) s[j] = sp[j];
             }
         }
         // ---- the pre-process keeps the gradient at the fragment start
         if (p.mode == 0) {
 #pragma unroll
-            for (int i = 0; i < NR; i++) p.dS_ext[sidx + (int64_t)(r8 + 8 * i) * D + col] = G[i];
+            for (int j = 0; j < NR; j++) p.dS_ext[sidx + (int64_t)(r8 + 8 * j) * D + col] = G[j];
         }
     }
 }
@@ -315,7 +319,11 @@ __global__ void __launch_bounds__(BT) bwd_merge_kernel(const MergeChain *__restr
 
 template <typename TIn, int D, bool PERDIM>
 int launch_chain_t(const BwdParams &prm, int grid, cudaStream_t st) {
-    bwd_chain_kernel<TIn, D, PERDIM><<<grid, BT, 0, st>>>(prm);
+    const size_t sm = sizeof(BwdSmem<TIn, D, PERDIM>);
+    cudaError_t e = cudaFuncSetAttribute(bwd_chain_kernel<TIn, D, PERDIM>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return (int)e;
+    bwd_chain_kernel<TIn, D, PERDIM><<<grid, BT, sm, st>>>(prm);
     return (int)cudaGetLastError();
 }
 
