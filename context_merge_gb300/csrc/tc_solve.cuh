@@ -1,5 +1,6 @@
-// One-warp solve of the per-chunk WY inverse, shared by the WY build of the
-// scalar-gate path (tc_wy.cu) and the per-dim-gate preparation (tc_kda.cu).
+// Solves of the per-chunk WY inverse T = (I + A)^-1: one warp per unit (the
+// per-dim-gate preparation, tc_kda.cu) or a pair of warps per unit (the WY
+// build of the scalar-gate path, tc_wy.cu).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -11,13 +12,59 @@ namespace tc {
 
 constexpr int kLS = 68;   // row stride (floats) of the A scratch
 
+// Converts T (rows in S[64][kLS], columns 0..63; the upper-right 32 x 32
+// block is taken as zero whatever S holds there) into T' = T diag(beta) and
+// T'' = T diag(beta gamma) (hi, lo), bf16, 16-byte pieces: lane l takes
+// columns 8c .. 8c + 7 (c = l & 7) of rows 4p + r, p in [p0, p0 + np), with
+// r = (l >> 3) ^ (c >> 2) so that the eight lanes of each quarter-warp read
+// distinct bank groups; a warp stores four whole tile rows at a time.
+__device__ __forceinline__ void store_tiles(const float *S, uint8_t *dst, const float *beta, const float *gam, int p0,
+                                            int np) {
+    const int l = threadIdx.x & 31;
+    const int c = l & 7, r = (l >> 3) ^ (c >> 2);
+    float bc[8], gc[8];
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+        bc[e] = beta[8 * c + e];
+        gc[e] = bc[e] * gam[8 * c + e];
+    }
+#pragma unroll 4
+    for (int p = p0; p < p0 + np; p++) {
+        const int i = 4 * p + r;
+        float t[8];
+        if (i < 32 && c >= 4) {
+#pragma unroll
+            for (int e = 0; e < 8; e++) t[e] = 0.f;
+        } else {
+            const float4 a0 = *reinterpret_cast<const float4 *>(S + i * kLS + 8 * c);
+            const float4 a1 = *reinterpret_cast<const float4 *>(S + i * kLS + 8 * c + 4);
+            t[0] = a0.x; t[1] = a0.y; t[2] = a0.z; t[3] = a0.w;
+            t[4] = a1.x; t[5] = a1.y; t[6] = a1.z; t[7] = a1.w;
+        }
+        uint32_t u[4], hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            u[e] = pack_bf16(t[2 * e] * bc[2 * e], t[2 * e + 1] * bc[2 * e + 1]);
+            const float w0 = t[2 * e] * gc[2 * e], w1 = t[2 * e + 1] * gc[2 * e + 1];
+            hi[e] = pack_bf16(w0, w1);
+            const float2 h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hi[e]));
+            lo[e] = pack_bf16(w0 - h.x, w1 - h.y);
+        }
+        const uint32_t o = sw128((uint32_t)i, (uint32_t)c);
+        *reinterpret_cast<uint4 *>(dst + o) = make_uint4(u[0], u[1], u[2], u[3]);
+        *reinterpret_cast<uint4 *>(dst + kWyTileBytes + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(dst + 2 * kWyTileBytes + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
 // One warp: T = (I + A)^-1 of the 64 x 64 unit lower-triangular matrix whose
 // strictly lower part A is in S[64][68] (zeros elsewhere), by rows:
 //   T_ij = delta_ij - sum_{k < i} A_ik T_kj.
 // Lane l keeps x1[i] = T_il (i = 0..63) and x2[m] = T_{32+m, 32+l} (m = 0..31;
 // T_{i, 32+l} = 0 for i < 32).  Then writes T' = T diag(beta) and
-// T'' = T diag(beta gamma) (hi, lo) as bf16 into the unit's three tiles.
-__device__ __forceinline__ void solve_unit(const float *S, uint8_t *dst, const float *beta, const float *gam) {
+// T'' = T diag(beta gamma) (hi, lo) as bf16 into the unit's three tiles,
+// reusing S (which it overwrites) to turn columns into rows.
+__device__ __forceinline__ void solve_unit(float *S, uint8_t *dst, const float *beta, const float *gam) {
     const int l = threadIdx.x & 31;
     float x1[64], x2[32];
 #pragma unroll
@@ -40,26 +87,157 @@ __device__ __forceinline__ void solve_unit(const float *S, uint8_t *dst, const f
         x1[i] = (i == l ? 1.f : 0.f) - ((a1[0] + a1[1]) + (a1[2] + a1[3]));
         if (i >= 32) x2[i - 32] = (i - 32 == l ? 1.f : 0.f) - ((a2[0] + a2[1]) + (a2[2] + a2[3]));
     }
-    // column scales of this lane's two columns
-    const float b1 = beta[l], b2 = beta[32 + l];
-    const float c1 = b1 * gam[l], c2 = b2 * gam[32 + l];
-    const uint32_t co1 = (uint32_t)(l & 7) * 2, q1 = (uint32_t)(l >> 3);
+    // T goes back through the scratch (every A row has been read): lane l
+    // writes columns l and 32 + l, then the rows leave as 16-byte pieces
+    __syncwarp();
 #pragma unroll
     for (int i = 0; i < 64; i++) {
-        const float t1 = x1[i], t2 = i >= 32 ? x2[i - 32] : 0.f;
-        const uint32_t o1 = sw128(i, q1) + co1, o2 = sw128(i, 4 + q1) + co1;
-        const float u1 = t1 * b1, u2 = t2 * b2;
-        const float w1 = t1 * c1, w2 = t2 * c2;
-        const __nv_bfloat16 h1 = __float2bfloat16_rn(w1), h2 = __float2bfloat16_rn(w2);
-        *reinterpret_cast<__nv_bfloat16 *>(dst + o1) = __float2bfloat16_rn(u1);
-        *reinterpret_cast<__nv_bfloat16 *>(dst + o2) = __float2bfloat16_rn(u2);
-        *reinterpret_cast<__nv_bfloat16 *>(dst + kWyTileBytes + o1) = h1;
-        *reinterpret_cast<__nv_bfloat16 *>(dst + kWyTileBytes + o2) = h2;
-        *reinterpret_cast<__nv_bfloat16 *>(dst + 2 * kWyTileBytes + o1) =
-            __float2bfloat16_rn(w1 - __bfloat162float(h1));
-        *reinterpret_cast<__nv_bfloat16 *>(dst + 2 * kWyTileBytes + o2) =
-            __float2bfloat16_rn(w2 - __bfloat162float(h2));
+        S[i * kLS + l] = x1[i];
+        if (i >= 32) S[i * kLS + 32 + l] = x2[i - 32];
     }
+    __syncwarp();
+    store_tiles(S, dst, beta, gam, 0, 16);
+    __syncwarp();   // the scratch has been read before the caller reuses it
+}
+
+// Two warps (role 0 and 1, meeting at named barrier `bar_id`) solve one unit
+// by blocks of the unit lower-triangular L = I + A, inverting blocks bottom
+// up and forming every off-diagonal block as a product, which reuses each
+// shared-memory value for several outputs (a forward substitution reads one
+// broadcast value per product and runs out of shared-memory wavefronts):
+//   16 x 16 diagonal blocks: forward substitution, T_i = e_i - sum_{k<i}
+//       A_ik T_k, one block per half-warp, lane = column;
+//   32 x 32 diagonal blocks (role r takes rows/cols 32r ..): with s, t its
+//       two 16-blocks, T_ts = -T_tt (A_ts T_ss), 2 x 4 outputs per lane;
+//   the 64 x 64 unit: T21 = -T22 (A21 T11), 4 x 4 outputs per lane over
+//       both warps.
+// T replaces A in S block by block; the products go through the upper-right
+// 32 x 32 block of S, which A leaves unused (it is treated as zero after).
+// Row sets are interleaved (rows rg, rg + 8, ...) so that the distinct rows
+// a warp reads at once fall in distinct bank groups.
+__device__ __forceinline__ void fma44(float (&x)[4][4], const float4 (&a)[4], const float4 (&b)[4]) {
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+        const float av[4] = {a[r].x, a[r].y, a[r].z, a[r].w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            x[r][0] = fmaf(av[e], b[e].x, x[r][0]);
+            x[r][1] = fmaf(av[e], b[e].y, x[r][1]);
+            x[r][2] = fmaf(av[e], b[e].z, x[r][2]);
+            x[r][3] = fmaf(av[e], b[e].w, x[r][3]);
+        }
+    }
+}
+__device__ __forceinline__ void fma24(float (&x)[2][4], const float4 (&a)[2], const float4 (&b)[4]) {
+#pragma unroll
+    for (int r = 0; r < 2; r++) {
+        const float av[4] = {a[r].x, a[r].y, a[r].z, a[r].w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            x[r][0] = fmaf(av[e], b[e].x, x[r][0]);
+            x[r][1] = fmaf(av[e], b[e].y, x[r][1]);
+            x[r][2] = fmaf(av[e], b[e].z, x[r][2]);
+            x[r][3] = fmaf(av[e], b[e].w, x[r][3]);
+        }
+    }
+}
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
+}
+
+__device__ __forceinline__ void solve_unit_pair(float *S, uint8_t *dst, const float *beta, const float *gam, int role,
+                                                int bar_id) {
+    const int l = threadIdx.x & 31;
+    const int o = 32 * role;
+    {
+        // 16 x 16 diagonal blocks o and o + 16, one per half-warp
+        const int c = l & 15, b0 = o + 16 * (l >> 4);
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k4 = 0; k4 < 4; k4++) {
+                if (4 * k4 >= i) break;
+                const float4 v = ld4(S + (b0 + i) * kLS + b0 + 4 * k4);
+                const float av[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; e++)
+                    if (4 * k4 + e < i) a[e] = fmaf(av[e], y[4 * k4 + e], a[e]);
+            }
+            y[i] = (i == c ? 1.f : 0.f) - ((a[0] + a[1]) + (a[2] + a[3]));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 16; i++) S[(b0 + i) * kLS + b0 + c] = y[i];
+        __syncwarp();
+    }
+    {
+        // this role's 32-block: X1 = A_ts T_ss into rows 16 role .. of the
+        // upper-right block, then T_ts = -T_tt X1 over A_ts
+        const int rg = l >> 2, cg = l & 3;
+        const int s0 = o, t0 = o + 16, x0 = 16 * role;
+        float x[2][4] = {};
+#pragma unroll
+        for (int k4 = 0; k4 < 4; k4++) {
+            const float4 av[2] = {ld4(S + (t0 + rg) * kLS + s0 + 4 * k4), ld4(S + (t0 + rg + 8) * kLS + s0 + 4 * k4)};
+            float4 bv[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) bv[e] = ld4(S + (s0 + 4 * k4 + e) * kLS + s0 + 4 * cg);
+            fma24(x, av, bv);
+        }
+#pragma unroll
+        for (int r = 0; r < 2; r++) st4(S + (x0 + rg + 8 * r) * kLS + 32 + 4 * cg, x[r][0], x[r][1], x[r][2], x[r][3]);
+        __syncwarp();
+        float z[2][4] = {};
+#pragma unroll
+        for (int k4 = 0; k4 < 4; k4++) {
+            const float4 av[2] = {ld4(S + (t0 + rg) * kLS + t0 + 4 * k4), ld4(S + (t0 + rg + 8) * kLS + t0 + 4 * k4)};
+            float4 bv[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) bv[e] = ld4(S + (x0 + 4 * k4 + e) * kLS + 32 + 4 * cg);
+            fma24(z, av, bv);
+        }
+#pragma unroll
+        for (int r = 0; r < 2; r++) st4(S + (t0 + rg + 8 * r) * kLS + s0 + 4 * cg, -z[r][0], -z[r][1], -z[r][2], -z[r][3]);
+    }
+    named_bar(bar_id, 64);   // T11 and T22 complete
+    // the unit: lane (rg, cg) of the pair takes rows 8r + rg (r = 0..3) and
+    // columns 4cg .. 4cg + 3 of a 32 x 32 block
+    const int rg = (32 * role + l) >> 3, cg = l & 7;
+    {
+        float x[4][4] = {};   // X = A21 T11 into the upper-right block
+#pragma unroll 2
+        for (int k4 = 0; k4 < 8; k4++) {
+            float4 av[4], bv[4];
+#pragma unroll
+            for (int r = 0; r < 4; r++) av[r] = ld4(S + (32 + 8 * r + rg) * kLS + 4 * k4);
+#pragma unroll
+            for (int e = 0; e < 4; e++) bv[e] = ld4(S + (4 * k4 + e) * kLS + 4 * cg);
+            fma44(x, av, bv);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; r++) st4(S + (8 * r + rg) * kLS + 32 + 4 * cg, x[r][0], x[r][1], x[r][2], x[r][3]);
+    }
+    named_bar(bar_id, 64);   // X complete; A21 no longer read
+    {
+        float z[4][4] = {};   // T21 = -T22 X over A21
+#pragma unroll 2
+        for (int k4 = 0; k4 < 8; k4++) {
+            float4 av[4], bv[4];
+#pragma unroll
+            for (int r = 0; r < 4; r++) av[r] = ld4(S + (32 + 8 * r + rg) * kLS + 32 + 4 * k4);
+#pragma unroll
+            for (int e = 0; e < 4; e++) bv[e] = ld4(S + (4 * k4 + e) * kLS + 32 + 4 * cg);
+            fma44(z, av, bv);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; r++)
+            st4(S + (32 + 8 * r + rg) * kLS + 4 * cg, -z[r][0], -z[r][1], -z[r][2], -z[r][3]);
+    }
+    named_bar(bar_id, 64);   // T complete in S
+    store_tiles(S, dst, beta, gam, 8 * role, 8);
 }
 
 }  // namespace tc

@@ -12,18 +12,18 @@
 // The solves of different chunks are independent, so they run here in one
 // fully parallel launch; the chain kernels (tc_chain.cu) stream the tiles.
 //
-// CTA = 9 warps, 8 units per iteration.  Warp 8 issues the loads and MMAs:
+// CTA = 17 warps, 8 units per iteration.  Warp 16 issues the loads and MMAs:
 // one M = 128, N = 128 MMA per pair of units computes [K_a; K_b][K_a; K_b]^T,
 // whose diagonal blocks are K_a K_a^T (TMEM lanes 0..63) and K_b K_b^T (lanes
-// 64..127); four pairs fill the 512 TMEM columns.  Warps 0..7 first form A
-// for every unit from TMEM (a warp reaches only its own 32 TMEM lanes, so each
-// unit's rows are formed by two warps), then warp w solves unit w alone by
-// forward substitution, T_i = e_i - sum_{k<i} A_ik T_k, row by row, with the
-// unit's T in registers: lane l holds column l (64 rows) and column 32 + l
-// (rows 32..63; rows above are zero).  No barrier inside a solve, one
-// broadcast shared-memory read per four products.  The next iteration's K
-// tiles and products are issued while the units are being solved.  Waits are
-// bounded as in the chain kernels.
+// 64..127); four pairs fill the 512 TMEM columns.  Warps 0..15 first form A
+// for every unit from TMEM (warp w: 32 rows of pair w / 4 from its own TMEM
+// lane quarter w % 4), then warps 2u and 2u + 1 solve unit u together by
+// 32 x 32 blocks (tc_solve.cuh): each inverts one diagonal block by forward
+// substitution, T_i = e_i - sum_{k<i} A_ik T_k, with its column in registers,
+// then the two share the off-diagonal block's products by rows.  The pair
+// halves the serial depth of a solve and puts four solver warps on each SM
+// sub-partition.  The next iteration's K tiles and products are issued while
+// the units are being solved.  Waits are bounded as in the chain kernels.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,8 +39,9 @@ namespace {
 using namespace tc;
 
 constexpr int D = 128;
-constexpr int WY_SOLVERS = 8;                     // solver warps = units per iteration
-constexpr int WY_THREADS = 32 * (WY_SOLVERS + 1);
+constexpr int WY_SOLVERS = 8;                     // units per iteration
+constexpr int WY_WARPS = 2 * WY_SOLVERS;          // solver warps: a pair per unit
+constexpr int WY_THREADS = 32 * (WY_WARPS + 1);
 constexpr uint32_t WY_TMEM_COLS = 512;
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base)
@@ -55,7 +56,8 @@ constexpr uint32_t O_CTL = O_BARS + 64;
 constexpr uint32_t O_TSLOT = O_CTL + 16;
 constexpr uint32_t WY_SMEM = O_TSLOT + 16;
 static_assert(WY_SMEM + 1024 <= 232448, "WY layout exceeds shared memory");
-constexpr int kSolveBarId = 1;                    // named barrier of the 8 solver warps
+constexpr int kSolveBarId = 1;                    // named barrier of the 16 solver warps
+constexpr int kPairBarId0 = 2;                    // named barriers 2 .. 9: one per solver pair
 
 struct WyParams {
     const WyChunk *chunks;
@@ -134,12 +136,12 @@ tc_wy_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ WyP
         mbar_init(&bar[WB_KFREE0], 1);
         mbar_init(&bar[WB_KFREE1], 1);
         mbar_init(&bar[WB_PFULL], 1);
-        mbar_init(&bar[WB_TFREE], WY_SOLVERS);
+        mbar_init(&bar[WB_TFREE], WY_WARPS);
         mbar_init(&bar[WB_DRAIN], 1);
         ctl->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (w == WY_SOLVERS) {
+    if (w == WY_WARPS) {
         if (lane == 0) tma_prefetch_desc(&tk);
         tmem_alloc(tslot, WY_TMEM_COLS);
         tmem_relinquish();
@@ -149,7 +151,7 @@ tc_wy_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ WyP
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (w == WY_SOLVERS) {
+    if (w == WY_WARPS) {
         // ---------------------------------------------------------- loads and products
         if (lane == 0) {
             const uint32_t b0 = smem_u32(base);
@@ -213,25 +215,24 @@ tc_wy_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ WyP
         }
     } else {
         // ---------------------------------------------------------- form and solve
-        const int q = w & 3;
-        // gates of this warp's first unit
-        if ((int)blockIdx.x < ngroups) {
-            const int u0 = blockIdx.x * WY_SOLVERS + w;
-            if (u0 < p.n_units) write_gates(wy_gates(base, 0, w), load_gate_inputs(p, u0));
+        const int q = w & 3, pair = w >> 2;
+        const int u_own = w >> 1, role = w & 1;   // the unit this warp solves, and its part
+        // gates of this pair's first unit
+        if ((int)blockIdx.x < ngroups && role == 0) {
+            const int u0 = blockIdx.x * WY_SOLVERS + u_own;
+            if (u0 < p.n_units) write_gates(wy_gates(base, 0, u_own), load_gate_inputs(p, u0));
         }
-        named_bar(kSolveBarId, 32 * WY_SOLVERS);
+        named_bar(kSolveBarId, 32 * WY_WARPS);
         int it = 0;
         for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x, it++) {
             const int slot = it & 1;
             const bool pok = wy_warp_wait(&bar[WB_PFULL], it & 1, ctl, p.status, 89);
             if (pok) {
                 tc_fence_after();
-                // A rows from TMEM: lanes 32q.. of pairs 2(w>>2), 2(w>>2)+1; unit
-                // a of a pair (q < 2) holds lanes 0..63, unit b (q >= 2) 64..127
-                for (int pp = 0; pp < 2; pp++) {
-                    const int pair = 2 * (w >> 2) + pp;
-                    const int ul = 2 * pair + (q >> 1);
-                    if (grp * WY_SOLVERS + ul >= p.n_units) continue;
+                // A rows from TMEM: lanes 32q.. of pair w / 4; unit a of the
+                // pair (q < 2) holds lanes 0..63, unit b (q >= 2) 64..127
+                const int ul = 2 * pair + (q >> 1);
+                if (grp * WY_SOLVERS + ul < p.n_units) {
                     const WyGates gs = wy_gates(base, slot, ul);
                     float *S = reinterpret_cast<float *>(base + O_SCR + ul * SCR_BYTES);
                     const int i = 32 * (q & 1) + lane;
@@ -248,11 +249,14 @@ tc_wy_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ WyP
                             const float4 f4 = *reinterpret_cast<const float4 *>(gs.f + j0);
                             const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
                             float e4[4];
+                            if (exact) {   // steep gates: the factored form could overflow
 #pragma unroll
-                            for (int u = 0; u < 4; u++) {
-                                const float x = vv[4 * q4 + u];
-                                const float val = exact ? bi * exp2f(Gi - gs.G[j0 + u]) * x : bei * fv[u] * x;
-                                e4[u] = (j0 + u < i) ? val : 0.f;
+                                for (int u = 0; u < 4; u++)
+                                    e4[u] = (j0 + u < i) ? bi * exp2f(Gi - gs.G[j0 + u]) * vv[4 * q4 + u] : 0.f;
+                            } else {
+#pragma unroll
+                                for (int u = 0; u < 4; u++)
+                                    e4[u] = (j0 + u < i) ? bei * fv[u] * vv[4 * q4 + u] : 0.f;
                             }
                             *reinterpret_cast<float4 *>(S + i * kLS + j0) = make_float4(e4[0], e4[1], e4[2], e4[3]);
                         }
@@ -263,24 +267,25 @@ tc_wy_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ WyP
                 if (lane == 0) mbar_arrive(&bar[WB_TFREE]);
             }
             // every unit's A is in place; leave together if any wait gave up
-            if (named_bar_or(kSolveBarId, 32 * WY_SOLVERS, pok ? 0 : 1)) break;
-            const int unit = grp * WY_SOLVERS + w;
+            if (named_bar_or(kSolveBarId, 32 * WY_WARPS, pok ? 0 : 1)) break;
+            const int unit = grp * WY_SOLVERS + u_own;
             // the next iteration's gate inputs load while this unit is solved
             const int ngrp = grp + gridDim.x;
-            const GateIn nxt = load_gate_inputs(p, ngrp < ngroups ? ngrp * WY_SOLVERS + w : p.n_units);
+            const bool nxt_ok = role == 0 && ngrp < ngroups && ngrp * WY_SOLVERS + u_own < p.n_units;
+            const GateIn nxt = load_gate_inputs(p, nxt_ok ? ngrp * WY_SOLVERS + u_own : p.n_units);
             if (unit < p.n_units) {
-                const float *S = reinterpret_cast<const float *>(base + O_SCR + w * SCR_BYTES);
-                const WyGates gs = wy_gates(base, slot, w);
-                solve_unit(S, p.wy + (size_t)unit * kWyUnitBytes, gs.beta, gs.gam);
+                float *S = reinterpret_cast<float *>(base + O_SCR + u_own * SCR_BYTES);
+                const WyGates gs = wy_gates(base, slot, u_own);
+                solve_unit_pair(S, p.wy + (size_t)unit * kWyUnitBytes, gs.beta, gs.gam, role, kPairBarId0 + u_own);
             }
-            if (ngrp < ngroups && ngrp * WY_SOLVERS + w < p.n_units) write_gates(wy_gates(base, slot ^ 1, w), nxt);
-            named_bar(kSolveBarId, 32 * WY_SOLVERS);   // scratch and gate slot free
+            if (nxt_ok) write_gates(wy_gates(base, slot ^ 1, u_own), nxt);
+            named_bar(kSolveBarId, 32 * WY_WARPS);   // scratch and gate slot free
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (w == WY_SOLVERS) tmem_dealloc(tmem, WY_TMEM_COLS);
+    if (w == WY_WARPS) tmem_dealloc(tmem, WY_TMEM_COLS);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
