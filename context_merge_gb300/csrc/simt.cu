@@ -356,11 +356,16 @@ simt_pre_kernel(const cpdr_fragment *__restrict__ frags, const int32_t *__restri
 
 // Merge: grid (chains, H, D / MBV).  S = S_ext[r0]; then for j = r0+1 .. r1-1:
 // S <- M_j S + S_ext[j]; S_init[j] written after each step (S_init[r0+1] = S_ext[r0]).
-// Each thread owns an (RPT x 4) register tile of the (D x MBV) state tile; M_j is
-// staged row-major in shared memory with cp.async, MNBUF - 1 steps ahead, and
-// the step's S_ext tile is loaded into registers one step ahead.
+// The CTA's (D x MBV) state tile stays in shared memory; M_j is staged
+// row-major with cp.async, MNBUF - 1 steps ahead.  The K = D sum of a step is
+// split over the four quarters of the CTA: a thread accumulates a (D/32 x 4)
+// register tile (rows rb + 32a, columns 4cb ..) over its quarter of K, so
+// that every value it loads from shared memory feeds four products; quarters
+// 1-3 pass their partial sums through shared memory to quarter 0, which adds
+// S_ext[j] and writes the new state.  The S_ext[j] tile is staged with M_j.
 constexpr int MBV = 16;
-constexpr int MNBUF = 3;
+constexpr int MNBUF = 2;
+constexpr int MT = 512;        // merge threads: four quarters of 128
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
@@ -375,30 +380,47 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // VF: S_ext and S_init in the state_v_first layout [dv][dk]; the tile stays
 // (key dim x value dim) in shared memory and only the global accesses turn.
 template <int D, bool VF>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(MT, 1)
 merge_kernel(const MergeChain *__restrict__ chains, const float *__restrict__ S_ext,
              const float *__restrict__ M, float *__restrict__ S_init, int H, int B) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     constexpr int LM = D + 4;                                  // padded row stride (16-byte rows)
-    constexpr int RPT = D / 64;                                // rows per thread
+    constexpr int RT = D / 32;                                 // rows per thread
+    constexpr int KQ = D / 4;                                  // K per quarter of the CTA
+    constexpr int NQ = MT / 4;                                 // threads per quarter
     float *Mn = reinterpret_cast<float *>(smem_raw);           // [MNBUF][D][LM]
     float *Ss = Mn + MNBUF * D * LM;                           // [D][MBV]
+    float *Red = Ss + D * MBV;                                 // [3][RT][NQ][4] partial sums of quarters 1-3
+    float *En = Red + 3 * RT * NQ * 4;                         // [MNBUF][D * MBV] S_ext tiles ([D][MBV]; VF: [MBV][D])
     const MergeChain ch = chains[blockIdx.x];
     const int h = blockIdx.y, col0 = blockIdx.z * MBV;
     auto idx_of = [&](int r) { return ((int64_t)(r * B + ch.b) * H + h) * D * D; };
-    // stage M_j into buffer j % MNBUF (one commit group per step, empty past the end)
+    // stage M_j and the S_ext[j] tile into buffer (j - r0 - 1) % MNBUF (one
+    // commit group per step, empty past the end)
     auto stage_M = [&](int j) {
         if (j < ch.r1) {
+            const int bi = (j - ch.r0 - 1) % MNBUF;
             const float *Mj = M + idx_of(j);
-            float *dst = Mn + ((j - ch.r0 - 1) % MNBUF) * D * LM;
-            for (int idx = threadIdx.x; idx < D * D / 4; idx += NT) {
+            float *dst = Mn + bi * D * LM;
+            for (int idx = threadIdx.x; idx < D * D / 4; idx += MT) {
                 const int d = idx / (D / 4), l4 = idx % (D / 4);
                 cp_async16(dst + d * LM + 4 * l4, Mj + d * D + 4 * l4);
+            }
+            const float *Ej = S_ext + idx_of(j);
+            float *edst = En + bi * D * MBV;
+            if (threadIdx.x < D * MBV / 4) {
+                if (VF) {   // columns col0 .. col0 + MBV - 1 are whole rows of [dv][dk]
+                    const int c = threadIdx.x / (D / 4), d4 = threadIdx.x % (D / 4);
+                    cp_async16(edst + c * D + 4 * d4, Ej + (int64_t)(col0 + c) * D + 4 * d4);
+                } else {
+                    const int d = threadIdx.x / (MBV / 4), c4 = threadIdx.x % (MBV / 4);
+                    cp_async16(edst + d * MBV + 4 * c4, Ej + (int64_t)d * D + col0 + 4 * c4);
+                }
             }
         }
         cp_async_commit();
     };
-    for (int idx = threadIdx.x; idx < D * MBV; idx += NT) {
+    for (int idx = threadIdx.x; idx < D * MBV; idx += MT) {
         const int d = VF ? idx % D : idx / MBV, c = VF ? idx / D : idx % MBV;
         const int64_t off = st_off<D>(d, col0 + c, VF);
         const float x = S_ext[idx_of(ch.r0) + off];
@@ -407,65 +429,71 @@ merge_kernel(const MergeChain *__restrict__ chains, const float *__restrict__ S_
     }
 #pragma unroll
     for (int k = 1; k < MNBUF; k++) stage_M(ch.r0 + k);
-    const int rb = threadIdx.x >> 2, cb = (threadIdx.x & 3) * 4;
-    float4 ext[RPT];   // S_ext tile of the current step, loaded one step ahead
-    auto load_ext = [&](int j) {
-#pragma unroll
-        for (int r = 0; r < RPT; r++) {
-            const float *src = S_ext + idx_of(j);
-            const int d = RPT * rb + r;
-            if (VF)
-                ext[r] = make_float4(src[st_off<D>(d, col0 + cb, true)], src[st_off<D>(d, col0 + cb + 1, true)],
-                                     src[st_off<D>(d, col0 + cb + 2, true)], src[st_off<D>(d, col0 + cb + 3, true)]);
-            else
-                ext[r] = *reinterpret_cast<const float4 *>(src + d * D + col0 + cb);
-        }
-    };
-    if (ch.r0 + 1 < ch.r1) load_ext(ch.r0 + 1);
+    const int kh = threadIdx.x / NQ, u = threadIdx.x % NQ;
+    const int rb = u >> 2, cb = (u & 3) * 4;
     for (int j = ch.r0 + 1; j < ch.r1; j++) {
         const int buf = (j - ch.r0 - 1) % MNBUF;
         cp_async_wait<MNBUF - 2>();
         __syncthreads();   // M_j staged; the previous step's state tile written
         stage_M(j + MNBUF - 1);
         const float *Mb = Mn + buf * D * LM;
-        float acc[RPT][4];
+        const float *Eb = En + buf * D * MBV;
+        float acc[RT][4];
 #pragma unroll
-        for (int r = 0; r < RPT; r++) {
-            acc[r][0] = ext[r].x; acc[r][1] = ext[r].y; acc[r][2] = ext[r].z; acc[r][3] = ext[r].w;
+        for (int a = 0; a < RT; a++) {
+            const int d = rb + 32 * a;
+            float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (kh == 0)
+                e = VF ? make_float4(Eb[cb * D + d], Eb[(cb + 1) * D + d], Eb[(cb + 2) * D + d], Eb[(cb + 3) * D + d])
+                       : *reinterpret_cast<const float4 *>(Eb + d * MBV + cb);
+            acc[a][0] = e.x; acc[a][1] = e.y; acc[a][2] = e.z; acc[a][3] = e.w;
         }
-        if (j + 1 < ch.r1) load_ext(j + 1);
+        const int l0 = kh * KQ;
 #pragma unroll 2
-        for (int l = 0; l < D; l += 4) {
+        for (int l = l0; l < l0 + KQ; l += 4) {
             float4 sv[4];
 #pragma unroll
-            for (int u = 0; u < 4; u++) sv[u] = *reinterpret_cast<const float4 *>(Ss + (l + u) * MBV + cb);
+            for (int e = 0; e < 4; e++) sv[e] = *reinterpret_cast<const float4 *>(Ss + (l + e) * MBV + cb);
 #pragma unroll
-            for (int r = 0; r < RPT; r++) {
-                const float4 m = *reinterpret_cast<const float4 *>(Mb + (RPT * rb + r) * LM + l);
+            for (int a = 0; a < RT; a++) {
+                const float4 m = *reinterpret_cast<const float4 *>(Mb + (rb + 32 * a) * LM + l);
                 const float mv[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    acc[r][0] = fmaf(mv[u], sv[u].x, acc[r][0]);
-                    acc[r][1] = fmaf(mv[u], sv[u].y, acc[r][1]);
-                    acc[r][2] = fmaf(mv[u], sv[u].z, acc[r][2]);
-                    acc[r][3] = fmaf(mv[u], sv[u].w, acc[r][3]);
+                for (int e = 0; e < 4; e++) {
+                    acc[a][0] = fmaf(mv[e], sv[e].x, acc[a][0]);
+                    acc[a][1] = fmaf(mv[e], sv[e].y, acc[a][1]);
+                    acc[a][2] = fmaf(mv[e], sv[e].z, acc[a][2]);
+                    acc[a][3] = fmaf(mv[e], sv[e].w, acc[a][3]);
                 }
             }
         }
-        __syncthreads();   // every thread has read the old state tile
+        if (kh > 0) {
 #pragma unroll
-        for (int r = 0; r < RPT; r++) {
-            const int d = RPT * rb + r;
-            const float4 o = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-            *reinterpret_cast<float4 *>(Ss + d * MBV + cb) = o;
+            for (int a = 0; a < RT; a++)
+                *reinterpret_cast<float4 *>(Red + (((kh - 1) * RT + a) * NQ + u) * 4) =
+                    make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        }
+        __syncthreads();   // partial sums written; every thread has read the old state tile
+        if (kh == 0) {
             float *dst = S_init + idx_of(j + 1);
-            if (VF) {
-                dst[st_off<D>(d, col0 + cb, true)] = o.x;
-                dst[st_off<D>(d, col0 + cb + 1, true)] = o.y;
-                dst[st_off<D>(d, col0 + cb + 2, true)] = o.z;
-                dst[st_off<D>(d, col0 + cb + 3, true)] = o.w;
-            } else {
-                *reinterpret_cast<float4 *>(dst + d * D + col0 + cb) = o;
+#pragma unroll
+            for (int a = 0; a < RT; a++) {
+                float4 o = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+#pragma unroll
+                for (int q = 0; q < 3; q++) {
+                    const float4 pr = *reinterpret_cast<const float4 *>(Red + ((q * RT + a) * NQ + u) * 4);
+                    o.x += pr.x; o.y += pr.y; o.z += pr.z; o.w += pr.w;
+                }
+                const int d = rb + 32 * a;
+                *reinterpret_cast<float4 *>(Ss + d * MBV + cb) = o;
+                if (VF) {
+                    dst[st_off<D>(d, col0 + cb, true)] = o.x;
+                    dst[st_off<D>(d, col0 + cb + 1, true)] = o.y;
+                    dst[st_off<D>(d, col0 + cb + 2, true)] = o.z;
+                    dst[st_off<D>(d, col0 + cb + 3, true)] = o.w;
+                } else {
+                    *reinterpret_cast<float4 *>(dst + d * D + col0 + cb) = o;
+                }
             }
         }
     }
@@ -555,10 +583,10 @@ template <int D, bool VF>
 int launch_merge_t(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init, cudaStream_t st) {
     const auto &p = c->plan;
     dim3 grid((unsigned)p.chains.size(), (unsigned)p.H, (unsigned)(D / MBV));
-    const size_t sm = sizeof(float) * (MNBUF * D * (D + 4) + D * MBV);
+    const size_t sm = sizeof(float) * (MNBUF * D * (D + 4) + D * MBV + 3 * (D / 32) * MT + MNBUF * D * MBV);
     cudaError_t e = cudaFuncSetAttribute(merge_kernel<D, VF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return (int)e;
-    merge_kernel<D, VF><<<grid, NT, sm, st>>>(c->dev.chains, S_ext, M, S_init, p.H, p.B);
+    merge_kernel<D, VF><<<grid, MT, sm, st>>>(c->dev.chains, S_ext, M, S_init, p.H, p.B);
     return (int)cudaGetLastError();
 }
 
