@@ -153,6 +153,8 @@ int launch_simt_fwd(const cpdr_ctx *c, const int32_t *items, int n_items, const 
                     float *final_state, void *stream);
 int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init,
                  void *stream);
+// The merge on the tensor cores (tc_merge.cu; bf16 hi/lo splits, d = 128).
+int launch_tc_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init, void *stream);
 int launch_zero_segments(const cpdr_ctx *c, float *S_ext, float *M, float *S_init,
                          float *final_state, int which, void *stream);
 // True when the tcgen05 kernels cover this problem (bf16, dk = dv = 128, scalar gate).

@@ -594,6 +594,7 @@ int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S
     cudaStream_t st = (cudaStream_t)stream;
     const auto &p = c->plan;
     if (p.chains.empty()) return 0;
+    if (c->use_tc && p.dk == 128) return launch_tc_merge(c, S_ext, M, S_init, stream);
     if (p.dk == 64)
         return p.vfirst ? launch_merge_t<64, true>(c, S_ext, M, S_init, st)
                         : launch_merge_t<64, false>(c, S_ext, M, S_init, st);
