@@ -582,12 +582,29 @@ def run_backward(args, ws, rank):
         dt, ht, threads = bwd_oracle_sample(inp, w)
         cpu = {"value": ht / H / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"fp64 backward oracle on 1 of {H} heads, full T ({dt:.1f} s wall); tokens scaled by heads"}
+    # algorithmic bytes of one backward: per (token, head) q, k, v, do, beta, g
+    # in and dq, dk, dv (fp32), dbeta, dg out; per (segment, head) the S_init
+    # and M states read.  The backward is three launches (continuing-fragment
+    # pass, reverse merge, main pass; one when no sequence crosses a segment)
+    # timed together, so its line carries the whole backward's figure.
+    es = 4 if w.dtype == "fp32" else 2
+    gate_w = d if w.gate == "kda" else 1
+    counts = ctx.counts()
+    tok_bytes = H * (4 * d * es + es + gate_w * 4 + 3 * d * 4 + 4 + gate_w * 4)
+    state_bytes = R * B * H * d * d * 4 * 2
+    nbytes = tokens * tok_bytes + state_bytes
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": None, "kernel": f"bwd(all launches):{w.name}", "peak_source": peak_kind,
+            "algorithmic_bytes_per_launch": nbytes, "ms_per_launch": ms}
+    launches = (1 + (2 if counts["chains"] else 0)) * args.steps
     line = {"metric": BWD_METRIC, "value": tokens * ws / (ms / 1e3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "op": "backward", "B": B, "T": T, "H": H, "d": d, "R": R,
                        "gate": w.gate, "in_dtype": w.dtype, "parallelism": f"replicas{ws}"},
-            "roofline": None, "cpu_baseline": cpu, "e2e": None, "gpu_launches": None, "clocks": clk}
+            "roofline": roof, "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": clk}
     print(json.dumps(line), flush=True)
 
 
