@@ -22,6 +22,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -102,7 +103,9 @@ class ClockSampler:
 
     def start(self):
         try:
-            out_dir = os.path.join(ROOT, "gpurun_out")
+            # raw samples go to CPDR_CLOCK_DIR (default: the temp directory);
+            # the JSON line carries their summary
+            out_dir = os.environ.get("CPDR_CLOCK_DIR") or tempfile.gettempdir()
             os.makedirs(out_dir, exist_ok=True)
             self.path = os.path.join(out_dir, f"clocks_{os.getpid()}.csv")
             self.fh = open(self.path, "w")
