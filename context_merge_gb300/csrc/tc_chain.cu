@@ -511,9 +511,12 @@ __device__ __forceinline__ void run_mma(const Run &r) {
         mma_commit(&r.bar[B_WFULL]);
         if (HAS_U) {
             // the Delta accumulator is free once chunk t-1's Delta was read;
-            // U goes in after chunk t-1's P_S has completed
+            // in the pre-process U goes in after chunk t-1's P_S has
+            // completed; the forward issues it as soon as the Delta tile is
+            // free (measured 2% faster A/B: it then completes during the
+            // state update instead of after it)
             if (t >= 1 && !mbar_wait(&r.bar[B_DLREADY], (t - 1) & 1, ctl, st, 23)) break;
-            if (t >= 1 && !mbar_wait(&r.bar[B_PSFULL], (t - 1) & 1, ctl, st, 25)) break;
+            if (!FWD && t >= 1 && !mbar_wait(&r.bar[B_PSFULL], (t - 1) & 1, ctl, st, 25)) break;
             tc_fence_after();
             mma_mnk<64, 64>(tm + TM_DL, stg<MODE, ROLE>(d.vmn0, t), stg<MODE, ROLE>(d.t10, t), 8192, false);
             mma_commit(&r.bar[B_UFULL]);
