@@ -215,7 +215,12 @@ cpdr_status cpdr_preprocess(const cpdr_ctx *ctx, const void *k, const void *v, c
  * first fragment continues a sequence begun in segment r - n_pre,
  *     S = 0;  for j = r - n_pre .. r - 1:  S <- M_j S + S_ext,j
  * and S_init[r] = S; all other entries are zeroed.  Evaluated as one
- * sequential scan per sequence (equal in exact arithmetic).
+ * sequential scan per sequence (equal in exact arithmetic).  Precision: on
+ * the tensor-core path (bf16 inputs, d = 128) each product M_j S runs on the
+ * tensor cores with M_j and S split into bf16 hi/lo pairs and fp32
+ * accumulation (about 2^-16 relative per step); otherwise all fp32.
+ * In: S_ext, M (device, as cpdr_preprocess wrote them).  Out: S_init
+ * (device).  Errors: CPDR_ERR_INVALID, CPDR_ERR_CUDA.
  */
 cpdr_status cpdr_merge(const cpdr_ctx *ctx, const float *S_ext, const float *M, float *S_init,
                        void *stream);
