@@ -194,3 +194,42 @@ def test_conv_width_validation(cpdr_lib):
         assert ei.value.status == st
     with pytest.raises(cpdr.CpdrError):
         mk(0).conv_pre_tokens()
+
+
+# ---- seeded random length mixes: structure and the plan's counters -------
+def _random_case(rng):
+    R = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+    L = int(rng.integers(1, 40))
+    T = R * L
+    n = int(rng.integers(1, 12))
+    cuts = sorted(int(x) for x in rng.integers(0, T + 1, size=n - 1))
+    bounds = [0] + cuts + [T]
+    lengths = [bounds[i + 1] - bounds[i] for i in range(n)]
+    return lengths, R
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_mixes_structure_and_counters(cpdr_lib, seed):
+    rng = __import__("numpy").random.default_rng(5000 + seed)
+    lengths, R = _random_case(rng)
+    cu = [0]
+    for x in lengths:
+        cu.append(cu[-1] + x)
+    T = cu[-1]
+    L = T // R
+    ctx = ctx_for(lengths, R)
+    frags = ctx.fragments()
+    check_structure(frags, cu, R)
+    c = ctx.counts()
+    assert c["fragments"] == len(frags)
+    # the pre-process runs each segment's fragment that continues past it
+    assert c["pre_items"] == sum(1 for f in frags if f[4] & cpdr.FRAG_CONT_NEXT)
+    # one merge chain per sequence that spans at least two segments
+    spans = [(cu[i] // L, (cu[i + 1] - 1) // L) for i in range(len(lengths)) if lengths[i] > 0]
+    assert c["chains"] == sum(1 for a, b in spans if b > a)
+    assert c["empty_seqs"] == sum(1 for x in lengths if x == 0)
+    # S_ext/M are zeroed where no fragment continues; S_init where none is continued
+    cont_next = {f[2] for f in frags if f[4] & cpdr.FRAG_CONT_NEXT}
+    cont_prev = {f[2] for f in frags if f[4] & cpdr.FRAG_CONT_PREV}
+    assert c["zero_pre"] == R - len(cont_next)
+    assert c["zero_init"] == R - len(cont_prev)
