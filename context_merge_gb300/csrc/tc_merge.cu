@@ -128,10 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_merge_kernel(const __grid_cons
         // element (n, d) of B^T: atom d / 64, 16-byte chunk (d % 64) / 8
         const uint32_t boff = (uint32_t)(d >> 6) * kBAtom + (uint32_t)((d & 7) * 2);
         const uint32_t bchunk = (uint32_t)((d & 63) >> 3);
-        // global rows of the tile (row d: 32 floats): [dv][dk] states are
+        // global rows of the tile (row d: NB floats): [dv][dk] states are
         // column-major per thread, so lanes read consecutive floats; [dk][dv]
-        // rows go through a per-warp scratch so that a warp moves four whole
-        // 128-byte rows per access instead of 32 separate lines
+        // rows go through a per-warp scratch so that a warp moves whole
+        // rows per access instead of 32 separate pieces
         float *xs = reinterpret_cast<float *>(base + O_X) + w * 32 * kXS;
         // coalesced side: NB / 4 lanes per row, 128 / NB rows per access
         constexpr int kLPR = NB / 4, kRPI = 32 / kLPR;
