@@ -4,6 +4,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <new>
 #include <string>
 
@@ -138,14 +139,17 @@ cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
     if (!out) return set_err(CPDR_ERR_INVALID, "null output pointer");
     *out = nullptr;
     if (!desc) return set_err(CPDR_ERR_INVALID, "null descriptor");
-    cpdr_ctx *c = new (std::nothrow) cpdr_ctx();
-    if (!c) return set_err(CPDR_ERR_INVALID, "out of host memory");
-    std::string err;
-    cpdr_status s = cpdr::build_plan(*desc, c->plan, err);
-    if (s != CPDR_OK) {
-        delete c;
-        return set_err(s, err);
+    std::shared_ptr<cpdr::Plan> plan;
+    try {
+        plan = std::make_shared<cpdr::Plan>();
+    } catch (const std::bad_alloc &) {
+        return set_err(CPDR_ERR_INVALID, "out of host memory");
     }
+    std::string err;
+    cpdr_status s = cpdr::build_plan(*desc, *plan, err);
+    if (s != CPDR_OK) return set_err(s, err);
+    cpdr_ctx *c = new (std::nothrow) cpdr_ctx(std::move(plan));
+    if (!c) return set_err(CPDR_ERR_INVALID, "out of host memory");
     c->use_tc = cpdr::tc_supported(c->plan) && !(desc->flags & CPDR_FLAG_FORCE_SIMT);
     if (!(desc->flags & CPDR_FLAG_HOST_ONLY)) {
         cudaError_t e = cudaGetDevice(&c->device);
@@ -490,14 +494,27 @@ cpdr_status cpdr_forward_host(const cpdr_ctx *c, const void *q, const void *k, c
 }
 
 cpdr_status cpdr_check_device_status(const cpdr_ctx *c, void *stream) {
-    CPDR_TRY(check_ctx(c));
+    if (!c) return set_err(CPDR_ERR_INVALID, "null context");
+    int32_t *word = nullptr;
+    if (c->has_device) {
+        CPDR_TRY(check_ctx(c));
+        word = c->dev.status;
+    } else {
+        // a host-only context has no status word of its own: its kernels ran
+        // through the allocation-free entry point, whose array holds the word
+        int dev = -1;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_err(e, "cudaGetDevice");
+        word = cpdr::noalloc_status_word(dev);
+        if (!word) return CPDR_OK;   // nothing has run on this device
+    }
     int32_t h[16];
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = cudaMemcpyAsync(h, c->dev.status, sizeof(h), cudaMemcpyDeviceToHost, st);
+    cudaError_t e = cudaMemcpyAsync(h, word, sizeof(h), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_err(e, "cpdr_check_device_status");
     if (h[0] != 0) {
-        cudaMemsetAsync(c->dev.status, 0, 64, st);
+        cudaMemsetAsync(word, 0, 64, st);
         cudaStreamSynchronize(st);
         char buf[160];
         snprintf(buf, sizeof(buf), "a bounded device wait gave up: code %d (site %d, block %d)", h[0], h[1], h[2]);

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <memory>
 #include <string>
 #include <vector>
 
@@ -125,7 +126,12 @@ struct DeviceTables {
 }  // namespace cpdr
 
 struct cpdr_ctx {
-    cpdr::Plan plan;
+    // The plan is built once and never changed afterwards; a copy of the
+    // context (the allocation-free entry point's view with its own device
+    // tables) shares it without copying it.
+    std::shared_ptr<const cpdr::Plan> plan_store;
+    const cpdr::Plan &plan;
+    explicit cpdr_ctx(std::shared_ptr<const cpdr::Plan> p) : plan_store(std::move(p)), plan(*plan_store) {}
     cpdr::DeviceTables dev;
     bool has_device = false;
     bool use_tc = false;        // tcgen05 kernels for the bf16, d = 128 path
@@ -159,6 +165,10 @@ int launch_zero_segments(const cpdr_ctx *c, float *S_ext, float *M, float *S_ini
                          float *final_state, int which, void *stream);
 // True when the tcgen05 kernels cover this problem (bf16, dk = dv = 128, scalar gate).
 bool tc_supported(const Plan &p);
+
+// Status word of the allocation-free entry point's device array on device
+// `dev` (noalloc.cu); nullptr until that entry point has been set up there.
+int32_t *noalloc_status_word(int dev);
 
 // Sets this thread's last-error message and returns the status.
 cpdr_status fail_with(cpdr_status s, const std::string &msg);

@@ -26,7 +26,7 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_cpdr_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;                 // serialises set-up and the context swap below
+std::mutex g_mu;                 // serialises the set-up and the use of the array
 void *g_scratch_addr[256] = {};  // device address of the array, per device (set up once)
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -83,7 +83,7 @@ extern "C" cpdr_status cpdr_forward_noalloc(const cpdr_ctx *c, const void *q, co
     cpdr::DeviceTables t;
     char *cur = base;
     auto take = [&](size_t n) { char *r = cur; cur += n; return r; };
-    t.status = reinterpret_cast<int32_t *>(take(b_status));
+    int32_t *array_status = reinterpret_cast<int32_t *>(take(b_status));
     t.frags = reinterpret_cast<cpdr_fragment *>(take(b_frags));
     t.pre_items = reinterpret_cast<int32_t *>(take(b_pre));
     t.fwd_order = reinterpret_cast<int32_t *>(take(b_ord));
@@ -97,10 +97,22 @@ extern "C" cpdr_status cpdr_forward_noalloc(const cpdr_ctx *c, const void *q, co
     float *M = reinterpret_cast<float *>(take(b_m));
     float *S_init = reinterpret_cast<float *>(take(b_sext));
     void *wy = b_wy ? take(b_wy) : nullptr;
-    // the array keeps the previous call's contents: clear the status word,
-    // copy this context's tables (the exchange buffers are fully written)
+    // Expired waits go to the context's own status word when it has one (a
+    // regular context), else to the array's; cpdr_check_device_status reads
+    // whichever of the two the context has.  The array keeps the previous
+    // call's contents: clear its status word, copy this context's tables
+    // (the exchange buffers are fully written by the stages).
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    e = cudaMemsetAsync(t.status, 0, b_status, st);
+    e = cudaSuccess;
+    if (c->has_device) {
+        if (dev != c->device)
+            return cpdr::fail_with(CPDR_ERR_INVALID,
+                                   "cpdr_forward_noalloc: current device differs from the context's device");
+        t.status = c->dev.status;
+    } else {
+        t.status = array_status;
+        e = cudaMemsetAsync(array_status, 0, b_status, st);
+    }
     auto put = [&](void *dst, const void *src, size_t n) {
         if (e == cudaSuccess && n) e = cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st);
     };
@@ -115,21 +127,30 @@ extern "C" cpdr_status cpdr_forward_noalloc(const cpdr_ctx *c, const void *q, co
     put(t.wy_chunks, p.wy_chunks.data(), p.wy_chunks.size() * sizeof(cpdr::WyChunk));
     if (e != cudaSuccess)
         return cpdr::fail_with(CPDR_ERR_CUDA, std::string("cpdr_forward_noalloc: table upload: ") + cudaGetErrorString(e));
-    // run the three stages against the static tables: the context is
-    // pointed at them for the duration of the launches and restored after
-    cpdr_ctx *mc = const_cast<cpdr_ctx *>(c);
-    const cpdr::DeviceTables saved = mc->dev;
-    const bool saved_has = mc->has_device;
-    const int saved_dev = mc->device;
-    mc->dev = t;
-    mc->has_device = true;
-    mc->device = dev;
-    cpdr_status s = cpdr_wy_build(c, q, k, beta, gate, wy, stream);
-    if (s == CPDR_OK) s = cpdr_preprocess(c, k, v, beta, gate, wy, S_ext, M, stream);
-    if (s == CPDR_OK) s = cpdr_merge(c, S_ext, M, S_init, stream);
-    if (s == CPDR_OK) s = cpdr_fwd(c, q, k, v, beta, gate, wy, S_init, o, final_state, stream);
-    mc->dev = saved;
-    mc->has_device = saved_has;
-    mc->device = saved_dev;
+    // Run the three stages on a view of the context that points at the
+    // array's tables: the view shares the caller's plan and leaves the
+    // caller's context untouched.  Every stage runs on the caller's stream
+    // (the view has no second stream of its own).
+    cpdr_ctx view(*c);
+    view.dev = t;
+    view.has_device = true;
+    view.device = dev;
+    view.aux_stream = view.ev_fork = view.ev_join = nullptr;
+    view.copy_stream = view.out_stream = nullptr;
+    for (void *&ev : view.host_ev) ev = nullptr;
+    cpdr_status s = cpdr_wy_build(&view, q, k, beta, gate, wy, stream);
+    if (s == CPDR_OK) s = cpdr_preprocess(&view, k, v, beta, gate, wy, S_ext, M, stream);
+    if (s == CPDR_OK) s = cpdr_merge(&view, S_ext, M, S_init, stream);
+    if (s == CPDR_OK) s = cpdr_fwd(&view, q, k, v, beta, gate, wy, S_init, o, final_state, stream);
     return s;
 }
+
+namespace cpdr {
+// Status word of the array on device `dev` (nullptr until the allocation-free
+// entry point has been set up there).
+int32_t *noalloc_status_word(int dev) {
+    if (dev < 0 || dev >= 256) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    return static_cast<int32_t *>(g_scratch_addr[dev]);
+}
+}  // namespace cpdr

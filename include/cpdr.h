@@ -333,10 +333,15 @@ cpdr_status cpdr_forward_host(const cpdr_ctx *ctx, const void *q, const void *k,
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Every call shares the one array and overwrites
  * it: calls whose work overlaps on the GPU (other streams, other contexts)
- * race, and a call must not run concurrently with another call on the same
- * context from another host thread.  A bounded wait that expires inside this
- * call records its code in the array's status word (cleared at the start of
- * every call), not in the context's.
+ * race.  The context is only read (the call runs its stages on a private
+ * view of it that shares the plan), so other calls may use the context
+ * meanwhile.  The plan tables are copied into the array from pageable host
+ * memory on `stream`, so the call may block the host until those small
+ * copies are staged.  A bounded wait that expires inside this call records
+ * its code in the context's status word when the context has one, else (a
+ * CPDR_FLAG_HOST_ONLY context) in the array's status word, which is cleared
+ * at the start of every call: read it with cpdr_check_device_status on the
+ * same context and device before the next allocation-free call there.
  */
 cpdr_status cpdr_forward_noalloc(const cpdr_ctx *ctx, const void *q, const void *k, const void *v,
                                  const void *beta, const float *gate, void *o, float *final_state, void *stream);
@@ -346,7 +351,11 @@ cpdr_status cpdr_forward_noalloc(const cpdr_ctx *ctx, const void *q, const void 
  * of polls; when a wait gives up, the kernel records a nonzero code in the
  * context's device status word and returns instead of hanging.  This call
  * synchronises `stream`, reads and clears that word, and returns
- * CPDR_ERR_TIMEOUT (with the code in the message) if it was set.
+ * CPDR_ERR_TIMEOUT (with the code in the message) if it was set.  For a
+ * context created with CPDR_FLAG_HOST_ONLY, whose kernels can only have run
+ * through cpdr_forward_noalloc, it reads and clears the status word of that
+ * entry point's array on the current device (CPDR_OK if the entry point has
+ * not run on this device).
  */
 cpdr_status cpdr_check_device_status(const cpdr_ctx *ctx, void *stream);
 
