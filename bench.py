@@ -376,6 +376,20 @@ def run_ours(args, ws, rank, local):
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": traffic, "kernel": kernel_tag, "peak_source": peak_kind,
             "algorithmic_bytes_per_launch": nbytes[dom], "ms_per_launch": mean_ms[dom]}
+    # every stage against the same peak (the pre-process is two kernels on
+    # two streams, timed together), and the whole path: the algorithmic
+    # bytes per step over the step time -- the pre-process, merge and forward
+    # passes (the WY build reads the same k, beta, g those passes read, so
+    # the path counts them once)
+    stages = {s: {"ms": mean_ms[s], "algorithmic_bytes": nbytes[s],
+                  "achieved_gbs": nbytes[s] / (mean_ms[s] / 1e3) / 1e9 if mean_ms[s] > 0 else None,
+                  "frac": nbytes[s] / (mean_ms[s] / 1e3) / 1e9 / peak if mean_ms[s] > 0 else None}
+              for s in ("wy", "pre", "merge", "fwd")}
+    path_bytes = sum(nbytes[s] for s in ("pre", "merge", "fwd"))
+    ms_step = elapsed_ms / args.steps
+    path = {"algorithmic_bytes_per_step": path_bytes, "ms_per_step": ms_step,
+            "achieved_gbs": path_bytes / (ms_step / 1e3) / 1e9,
+            "frac": path_bytes / (ms_step / 1e3) / 1e9 / peak, "peak": peak, "peak_source": peak_kind}
     cpu = None
     if not args.no_cpu_baseline:
         try:
@@ -396,6 +410,8 @@ def run_ours(args, ws, rank, local):
                        **variant_keys(w, inp)),
         "stage_ms": mean_ms,
         "roofline": roof,
+        "stage_roofline": stages,
+        "path_roofline": path,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": counts["launches"] * args.steps,
