@@ -341,8 +341,10 @@ cpdr_status cpdr_conv1d_fwd(const cpdr_ctx *c, const void *x, const float *weigh
 cpdr_status cpdr_bwd_workspace_bytes(const cpdr_ctx *c, size_t *bytes) {
     if (!c || !bytes) return set_err(CPDR_ERR_INVALID, "null argument");
     const Sizes s = sizes_of(c->plan);
-    *bytes = 2 * round256(s.sext) +
-             round256((size_t)cpdr::bwd_grid(c) * cpdr::bwd_scratch_floats_per_cta(c) * sizeof(float));
+    const size_t scratch = cpdr::bwd_uses_tc(c)
+                               ? cpdr::bwd_tc_scratch_bytes(c)
+                               : (size_t)cpdr::bwd_grid(c) * cpdr::bwd_scratch_floats_per_cta(c) * sizeof(float);
+    *bytes = 2 * round256(s.sext) + round256(scratch);
     return CPDR_OK;
 }
 
@@ -380,11 +382,13 @@ cpdr_status cpdr_bwd(const cpdr_ctx *c, const void *q, const void *k, const void
     float *scratch = (float *)(w + 2 * round256(s.sext));
     const size_t tok = (size_t)p.B * (size_t)p.T;
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(dq, 0, tok * p.H * p.dk * sizeof(float), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dk, 0, tok * p.H * p.dk * sizeof(float), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, tok * p.H * sizeof(float), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dgate, 0, s.gate, st);
-    if (e != cudaSuccess) return cuda_err(e, "cpdr_bwd: zero fill");
+    if (!cpdr::bwd_uses_tc(c)) {   // the CUDA-core chains add their sums atomically
+        cudaError_t e = cudaMemsetAsync(dq, 0, tok * p.H * p.dk * sizeof(float), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dk, 0, tok * p.H * p.dk * sizeof(float), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, tok * p.H * sizeof(float), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dgate, 0, s.gate, st);
+        if (e != cudaSuccess) return cuda_err(e, "cpdr_bwd: zero fill");
+    }
     return launch_rc(cpdr::launch_bwd(c, q, k, v, beta, gate, dout, dht, S_init, M, dS_ext, dS_end, scratch, dq, dk,
                                       dv, dbeta, dgate, stream),
                      "cpdr_bwd");

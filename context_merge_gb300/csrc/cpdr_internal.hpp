@@ -185,6 +185,23 @@ int launch_tc_wy(const cpdr_ctx *c, const void *k, const void *beta, const float
                  void *stream);
 int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy,
                   float *S_ext, float *M, void *stream);
+// Backward on the tensor cores (tc_chain.cu): the forward recomputation
+// storing each chunk's starting state and Delta, and the state-gradient
+// chains (pre-process of the backward, main pass).
+int launch_tc_rec(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy,
+                  const float *S_init, float *st_S, float *st_D, void *stream);
+int launch_tc_bwd_chain(const cpdr_ctx *c, const int32_t *items, int n_items, int pre, const void *q, const void *k,
+                        const void *dout, const float *g, const void *wy, const float *dht, const float *dS_end,
+                        float *dS_ext, float *st_dS, float *st_dD, void *stream);
+// Input gradients per (chunk, head) from the recomputed states and the
+// state-gradient chain's outputs (bwd_grad.cu).
+int launch_bwd_grad(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta,
+                    const float *g, const void *dout, const float *st_S, const float *st_D, const float *st_dS,
+                    const float *st_dD, float *dq, float *dk, float *dv, float *dbeta, float *dg, void *stream);
+// The backward runs on the tensor cores (bf16, d = 128, scalar gate, Hq == H,
+// [dk, dv] states); its scratch bytes (bwd.cu).
+bool bwd_uses_tc(const cpdr_ctx *c);
+size_t bwd_tc_scratch_bytes(const cpdr_ctx *c);
 // Backward (bwd.cu): scratch per CTA and the grid it is sized for.
 size_t bwd_scratch_floats_per_cta(const cpdr_ctx *c);
 int bwd_grid(const cpdr_ctx *c);

@@ -54,10 +54,19 @@ constexpr int NTHREADS = 512;
 // bit 2 = layout variants in the forward (grouped query heads, [dv, dk]
 // states), kept out of the plain forward's code (measured 4% slower with
 // them compiled in).  The per-dim modes always handle the variants.
-enum Mode { MODE_FWD = 0, MODE_PRE = 1, MODE_FWD_KDA = 2, MODE_PRE_KDA = 3, MODE_FWD_VAR = 4 };
+// The backward adds two modes: MODE_REC (bit 3) is the pre-process S chain
+// run over every fragment from its initial state, storing the state at each
+// chunk start and each chunk's Delta (the forward recomputation the input
+// gradients need); MODE_BWD (bit 4) runs the state-gradient chain of the
+// chunk form in reverse chunk order with the forward's warp roles and
+// stage layout (V's slots hold dO).
+enum Mode { MODE_FWD = 0, MODE_PRE = 1, MODE_FWD_KDA = 2, MODE_PRE_KDA = 3, MODE_FWD_VAR = 4, MODE_REC = 9,
+            MODE_BWD = 16 };
 __host__ __device__ constexpr bool mode_fwd(int m) { return (m & 1) == 0; }
 __host__ __device__ constexpr bool mode_kda(int m) { return (m & 2) != 0; }
 __host__ __device__ constexpr bool mode_var(int m) { return (m & 4) != 0 || (m & 3) != 0; }
+__host__ __device__ constexpr bool mode_rec(int m) { return (m & 8) != 0; }
+__host__ __device__ constexpr bool mode_bwd(int m) { return (m & 16) != 0; }
 enum Role { ROLE_S = 0, ROLE_M = 1 };
 
 // Optional event trace (compile with -DCPDR_TRACE): CTA (0, 0) of each
@@ -110,6 +119,12 @@ struct Params {
     int Hq, G;                // query heads of q and o, query heads per state (Hq = G H)
     int vfirst;               // dk x dv states stored [dv][dk]
     float scale;
+    // backward: per (chunk, head) unit u = global chunk * H + head
+    float *st_S;              // MODE_REC: S at each chunk start; MODE_BWD (main): dS after each chunk; [u][dk][dv]
+    float *st_D;              // MODE_REC: Delta; MODE_BWD (main): dDelta; [u][64][dv]
+    const float *dht;         // MODE_BWD: gradient of the final states [N][H][dk][dv] (nullable)
+    const float *dS_end;      // MODE_BWD main: gradient at the end of continuing fragments [R*B][H][dk][dv]
+    int bwd_pre;              // MODE_BWD: 1 = backward pre-process (dS at the fragment start into S_ext)
 };
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base).
@@ -221,6 +236,8 @@ struct Run {
     int64_t tok0;
     int seg, seq, flags;
     const Params *p;
+    // chunk processed at iteration t (the backward runs in reverse)
+    __device__ __forceinline__ int cof(int t, bool rev) const { return rev ? n - 1 - t : t; }
 };
 
 // gate slot arrays
@@ -299,8 +316,10 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
     const int lane = threadIdx.x & 31;
     const int H = r.p->H;
     int issued[3] = {-1, -1, -1};
-    // in-chunk gates of chunk c (padded rows: 0) -> its gate slot
-    auto produce_gates = [&](int c) {
+    constexpr bool REV = mode_bwd(MODE);
+    // in-chunk gates of the chunk of iteration t (padded rows: 0) -> its gate slot
+    auto produce_gates = [&](int t) {
+        const int c = r.cof(t, REV);
         const int nv = rows_of(r, c);
         const int64_t tk0 = r.tok0 + (int64_t)c * C;
         const int i0 = 2 * lane, i1 = 2 * lane + 1;
@@ -308,7 +327,7 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
         if (i0 < nv) g0 = r.p->g[(tk0 + i0) * H + r.h] * kLog2e;
         if (i1 < nv) g1 = r.p->g[(tk0 + i1) * H + r.h] * kLog2e;
         const LaneGates lg = scan_gates(g0, g1);
-        const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(c));
+        const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(t));
         gs.Gam[i0] = exp2f(lg.GC - lg.G0);
         gs.Gam[i1] = exp2f(lg.GC - lg.G1);
         if (mode_fwd(MODE)) {
@@ -322,7 +341,7 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
             gs.gC[1] = lg.exact ? 1.f : 0.f;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&r.bar[B_GATE0 + gate_slot<MODE, ROLE>(c)]);
+        if (lane == 0) mbar_arrive(&r.bar[B_GATE0 + gate_slot<MODE, ROLE>(t)]);
     };
     constexpr bool KDA = mode_kda(MODE);
     if (!KDA) produce_gates(0);
@@ -334,7 +353,8 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         TR(0, t, 0);
         uint64_t *fb = &r.bar[B_FULL0 + s];
-        const int tok = (int)(r.tok0 + (int64_t)t * C);
+        const int cc = r.cof(t, REV);   // the chunk this stage holds
+        const int tok = (int)(r.tok0 + (int64_t)cc * C);
         if (KDA) {
             if (lane == 0) {
                 // the unit's operand images, and V
@@ -365,7 +385,7 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
                 tma_load_3d(st + L.vc0, tv, fb, 0, r.h, tok);
                 tma_load_3d(st + L.vc1, tv, fb, 64, r.h, tok);
             }
-            const uint8_t *src = r.p->wy + ((size_t)(r.chunk0 + t) * H + r.h) * kWyUnitBytes + L.wy_off;
+            const uint8_t *src = r.p->wy + ((size_t)(r.chunk0 + cc) * H + r.h) * kWyUnitBytes + L.wy_off;
             bulk_load(st + L.t1, src, 2 * (uint32_t)kWyTileBytes, fb);
         }
         // gates one chunk ahead of the stage ring
@@ -418,6 +438,15 @@ __device__ __forceinline__ void mma_mnk(uint32_t d, uint64_t a, uint64_t b, uint
     }
 }
 
+// A MN-major, B MN-major (2048 B per k-step each)
+template <int N, int K>
+__device__ __forceinline__ void mma_mnmn(uint32_t d, uint64_t a, uint64_t b, bool acc) {
+    constexpr uint32_t id = idesc_bf16(128, N, true, true);
+#pragma unroll
+    for (int k = 0; k < K / 16; k++)
+        mma_bf16(d, a + (uint64_t)(k * 128), b + (uint64_t)(k * 128), id, (acc || k > 0) ? 1u : 0u);
+}
+
 // D(128 x N) (+)= A(128 x K, in TMEM from column a) * B(MN-major, 2048 B per k-step)
 template <int N, int K>
 __device__ __forceinline__ void mma_tmn(uint32_t d, uint32_t a, uint64_t b, bool acc) {
@@ -441,6 +470,7 @@ __device__ __forceinline__ void mma_tk(uint32_t d, uint32_t a, uint64_t b, uint3
 struct Descs {
     uint64_t stack0, kmn0, vmn0, q0, t10, t20, wb, wblo, mask;
     uint64_t kgam0, kglo0, kgamlo0, pt0;   // per-dim gate: P_S operands (hi, lo), W's lo operand, P
+    uint64_t wbk, maskmn, qmn0;            // backward: W tile K-major, mask MN-major, gamma ⊙ Q MN-major
 };
 template <int MODE, int ROLE>
 __device__ __forceinline__ Descs make_descs(const Run &r) {
@@ -456,6 +486,9 @@ __device__ __forceinline__ Descs make_descs(const Run &r) {
     d.wb = mndesc(b0 + L.wb, 16384);
     d.wblo = mndesc(b0 + L.wb_lo, 16384);
     d.mask = kdesc(b0 + L.mask);
+    d.wbk = kdesc(b0 + L.wb);
+    d.maskmn = mndesc(b0 + L.mask, 8192);
+    d.qmn0 = mndesc(b0 + L.qc0, L.qc1 - L.qc0);
     if (mode_kda(MODE)) {
         d.kgam0 = mndesc(b0 + L.kgam, L.k_lbo);
         d.kglo0 = mndesc(b0 + L.kglo, L.k_lbo);
@@ -488,6 +521,8 @@ __device__ __forceinline__ void run_mma(const Run &r) {
     Ctl *ctl = r.ctl;
     const Descs d = make_descs<MODE, ROLE>(r);
     constexpr uint32_t KATOM = L.kc1 - L.kc0;
+    // the backward's first products from dO (X1) are issued by the state warps
+    constexpr bool MMA_U = HAS_U && !mode_bwd(MODE);
     for (int t = 0; t < r.n; t++) {
         if (!mbar_wait(&r.bar[B_FULL0 + t % NS], (t / NS) & 1, ctl, st, 20)) break;
         // TMEM columns of W and P are free once chunk t-1's were read; the
@@ -509,7 +544,7 @@ __device__ __forceinline__ void run_mma(const Run &r) {
         // per-dim gate: the gated K tile is rounded too, W += lo(Kg) hi(T'')
         if (SPLIT && KDA) mma_mnk<64, 64>(tm + TM_W, stg<MODE, ROLE>(d.kglo0, t), tpp, 8192, true);
         mma_commit(&r.bar[B_WFULL]);
-        if (HAS_U) {
+        if (MMA_U) {
             // the Delta accumulator is free once chunk t-1's Delta was read;
             // in the pre-process U goes in after chunk t-1's P_S has
             // completed; the forward issues it as soon as the Delta tile is
@@ -552,9 +587,14 @@ __device__ __forceinline__ void run_mask(const Run &r) {
         return;
     }
     const int i = 32 * (w - 2) + lane;   // row of Q K^T (TMEM lane 64 + i)
+    constexpr bool BWD = mode_bwd(MODE);
     for (int ch = 0; ch < r.n; ch++) {
         if (!warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 50)) return;
         const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(ch));
+        // backward: the output scale goes into gamma ⊙ Q and the mask (both
+        // multiply dO), and rows past the chunk's end are zero (dO there
+        // belongs to the next fragment)
+        const float rs = BWD ? (i < rows_of(r, r.cof(ch, true)) ? r.p->scale : 0.f) : 1.f;
         if (w == 2) TR(4, ch, 0);
         if (!warp_wait(r, B_PFULL, ch & 1, 51)) return;
         if (w == 2) TR(4, ch, 1);
@@ -564,7 +604,7 @@ __device__ __forceinline__ void run_mask(const Run &r) {
         // S^T (gamma ⊙ Q)^T and Delta^T mask^T accumulate into one TMEM tile
         {
             uint8_t *st = r.base + (ch % (int)L.nstage) * L.stage_bytes;
-            const __nv_bfloat162 g2 = __float2bfloat162_rn(gs.gam[i]);
+            const __nv_bfloat162 g2 = __float2bfloat162_rn(rs * gs.gam[i]);
 #pragma unroll
             for (int a = 0; a < 2; a++) {
                 uint8_t *tile = st + (a ? L.qc1 : L.qc0);
@@ -598,7 +638,7 @@ __device__ __forceinline__ void run_mask(const Run &r) {
                 for (int u = 0; u < 4; u++) {
                     const float x = v[4 * q4 + u];
                     const float val = exact ? x * exp2f(Gi - gs.G[j0 + u]) : x * ei * fv[u];
-                    m[j0 + u] = (j0 + u <= i) ? val : 0.f;
+                    m[j0 + u] = (j0 + u <= i) ? rs * val : 0.f;
                 }
             }
         }
@@ -652,7 +692,7 @@ __device__ __forceinline__ void run_wepi(const Run &r) {
     if (!w_epilogue(0)) return;
     for (int t = 0; t < r.n; t++) {
         if (t + 1 < r.n && !w_epilogue(t + 1)) return;
-        if (FWD) {
+        if (FWD && !mode_bwd(MODE)) {
             if (!warp_wait(r, B_OFULL, t & 1, 43)) return;
             if (w == 4) TR(2, t, 3);
             tc_fence_after();
@@ -698,6 +738,152 @@ __device__ __forceinline__ void neg_pairs(const float *x, uint32_t (&hi)[NC], ui
     }
 }
 
+// Backward state warps: the state-gradient chain of the chunk form, chunks
+// in reverse.  dS^T (rows = value dims) lives in their registers; per chunk,
+// with the chunk's dO, Q, K, the WY product W and the masked product P (the
+// reverse-mode derivative of the chunk equations of [FLA-CP] §2.2; the
+// backward flow of §4):
+//   dDelta^T = dO~^T P + Gamma ⊙ (dS'^T K^T)                    (X1 + Gamma X2)
+//   dS^T     = gamma^C dS'^T + dO~^T (gamma ⊙ Q) - dDelta^T W   (X3 + X4)
+// where dS' is the gradient after the chunk and dO~ = scale dO (the scale
+// lives in the mask and in gamma ⊙ Q, which the mask warps prepare).  Lane 0
+// of warp 8 issues X1, X2 and then X3, X4 right after the warps meet at their
+// named barrier.  The main pass stores dS' and dDelta of every chunk; the
+// pre-process keeps only the gradient at the fragment's start (S_ext).
+template <int MODE, int ROLE>
+__device__ __forceinline__ void run_state_bwd(const Run &r, float (&S)[64], int64_t sidx) {
+    constexpr Lay L = make_lay(MODE, ROLE);
+    constexpr int NS = (int)L.nstage;
+    const Params &p = *r.p;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = w & 3, half = (w - 8) >> 2;
+    const int row = 32 * q + lane;                       // TMEM lane: value dim
+    const uint32_t tm = r.tmem;
+    const uint32_t lane_base = tm + ((uint32_t)(32 * q) << 16);
+    const bool issuer = (w == 8 && lane == 0);
+    const int H = p.H;
+    int32_t *st = p.status;
+    Ctl *ctl = r.ctl;
+    const Descs d = make_descs<MODE, ROLE>(r);
+    constexpr uint32_t KATOM = L.kc1 - L.kc0;
+    const bool main_pass = p.bwd_pre == 0;
+    // dS^T[row][64 half .. 64 half + 63] as the bf16 A operand of X2
+    auto put_grad = [&]() {
+#pragma unroll
+        for (int part = 0; part < 2; part++) {
+            uint32_t hi[16];
+#pragma unroll
+            for (int c2 = 0; c2 < 16; c2++) hi[c2] = pack_bf16(S[32 * part + 2 * c2], S[32 * part + 2 * c2 + 1]);
+            tmem_st16(lane_base + TM_SB + 32 * half + 16 * part, hi);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+    };
+    // the end gradient: dht where the sequence ends in this fragment; in the
+    // main pass dS_end where the fragment continues into the next segment
+    const float *src = nullptr;
+    int64_t base = 0;
+    if (r.flags & CPDR_FRAG_ENDS_SEQ) {
+        if (p.dht) {
+            src = p.dht;
+            base = ((int64_t)r.seq * H + r.h) * D * D;
+        }
+    } else if ((r.flags & CPDR_FRAG_CONT_NEXT) && main_pass) {
+        src = p.dS_end;
+        base = sidx;
+    }
+#pragma unroll
+    for (int i = 0; i < 64; i++) S[i] = src ? src[base + (int64_t)(64 * half + i) * D + row] : 0.f;
+    put_grad();
+    int bad = named_bar_or(kStateBar, 256, 0);
+    for (int t = 0; t < r.n && !bad; t++) {
+        const int c = r.cof(t, true);
+        const int nv = rows_of(r, c);
+        const int64_t unit = (int64_t)(r.chunk0 + c) * H + r.h;
+        if (main_pass) {   // dS' of the chunk, [dk][dv]
+            float *dst = p.st_S + unit * D * D + row;
+#pragma unroll
+            for (int i = 0; i < 64; i++) dst[(int64_t)(64 * half + i) * D] = S[i];
+        }
+        // ---- X1 = dO^T mask, X2 = dS'^T K^T
+        if (issuer) {
+            if (mbar_wait(&r.bar[B_MREADY], t & 1, ctl, st, 70)) {
+                tc_fence_after();
+                mma_mnmn<64, 64>(tm + TM_DL, stg<MODE, ROLE>(d.vmn0, t), d.maskmn, false);
+                mma_commit(&r.bar[B_MFREE]);
+                mma_tk<64, 128>(tm + TM_O, tm + TM_SB, stg<MODE, ROLE>(d.stack0, t), KATOM, false);
+                mma_commit(&r.bar[B_DLFULL]);
+            }
+        }
+        bool ok = warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(t), gate_parity<MODE, ROLE>(t), 71);
+        const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(t));
+        if (ok) ok = warp_wait(r, B_DLFULL, t & 1, 72);
+        if (ok) {
+            tc_fence_after();
+            float x1[32], x2[32];
+            tmem_ld32(lane_base + TM_DL + 32 * half, x1);
+            tmem_ld32(lane_base + TM_O + 32 * half, x2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 32; jj++) {
+                const int j = 32 * half + jj;
+                x1[jj] = (j < nv) ? fmaf(gs.Gam[j], x2[jj], x1[jj]) : 0.f;
+            }
+            if (main_pass) {   // dDelta of the chunk, [64][dv]
+                float *dst = p.st_D + unit * C * D + row;
+#pragma unroll
+                for (int jj = 0; jj < 32; jj++) dst[(int64_t)(32 * half + jj) * D] = x1[jj];
+            }
+            uint32_t hi[16];   // -dDelta^T, the A operand of X4
+            neg_pairs<16>(x1, hi, nullptr);
+            tmem_st16(lane_base + TM_DGB + 16 * half, hi);
+            tmem_st_wait();
+            tc_fence_before();
+        }
+        if ((bad = named_bar_or(kStateBar, 256, ok ? 0 : 1))) break;
+        // ---- X3 = dO^T (gamma ⊙ Q), X4 = (-dDelta^T) W, one accumulator
+        if (issuer) {
+            tc_fence_after();
+            bool iok = mbar_wait(&r.bar[B_QREADY0 + (t & 1)], (t >> 1) & 1, ctl, st, 73);
+            if (iok) iok = mbar_wait(&r.bar[B_WREADY], t & 1, ctl, st, 74);
+            if (iok) {
+                tc_fence_after();
+                mma_mnmn<128, 64>(tm + TM_PS, stg<MODE, ROLE>(d.vmn0, t), stg<MODE, ROLE>(d.qmn0, t), false);
+                mma_tk<128, 64>(tm + TM_PS, tm + TM_DGB, d.wbk, 8192, true);
+                mma_commit(&r.bar[B_PSFULL]);
+                mma_commit(&r.bar[B_WBFREE]);
+                mma_commit(&r.bar[B_EMPTY0 + t % NS]);
+            }
+        }
+        // ---- dS <- gamma^C dS' + X3 + X4
+        ok = warp_wait(r, B_PSFULL, t & 1, 75);
+        if (ok) {
+            tc_fence_after();
+            const float gC = gs.gC[0];
+#pragma unroll
+            for (int piece = 0; piece < 2; piece++) {
+                float v[32];
+                tmem_ld32(lane_base + TM_PS + 64 * half + 32 * piece, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; i++) S[32 * piece + i] = fmaf(gC, S[32 * piece + i], v[i]);
+            }
+            put_grad();
+        }
+        bad = named_bar_or(kStateBar, 256, (ok && !ctl->abort) ? 0 : 1);
+    }
+    if (issuer) {   // drain every MMA this thread issued
+        mma_commit(&r.bar[B_DRAIN2]);
+        Ctl local;
+        local.abort = 0;
+        mbar_wait(&r.bar[B_DRAIN2], 0, &local, st, 76);
+    }
+    if (bad || main_pass) return;
+    // the pre-process: the gradient at the fragment's start, [dk][dv]
+#pragma unroll
+    for (int i = 0; i < 64; i++) p.S_ext[sidx + (int64_t)(64 * half + i) * D + row] = S[i];
+}
+
 // State warps (8-15): Delta epilogue and S update; lane 0 of warp 8 issues the
 // chain's own products (Delta, O, P_S) right after the warps meet at a named
 // barrier, so the critical path has no mbarrier hand-off to another warp.
@@ -725,6 +911,11 @@ __device__ __forceinline__ void run_state(const Run &r) {
     constexpr uint32_t QATOM = L.qc1 - L.qc0;
     float S[64];
     const int64_t sidx = ((int64_t)r.seg * H + r.h) * D * D;
+    if constexpr (mode_bwd(MODE)) {
+        run_state_bwd<MODE, ROLE>(r, S, sidx);
+        return;
+    }
+    constexpr bool REC = mode_rec(MODE);
     // -S^T[row][64 half .. 64 half + 63] as the bf16 A operand (hi, lo) of the
     // next Delta and O products
     auto put_state = [&]() {
@@ -744,13 +935,19 @@ __device__ __forceinline__ void run_state(const Run &r) {
         const int dk = 64 * half + i;
         float x = 0.f;
         if (SPLIT) x = (dk == row) ? 1.f : 0.f;
-        else if (FWD && (r.flags & CPDR_FRAG_CONT_PREV))
+        else if ((FWD || REC) && (r.flags & CPDR_FRAG_CONT_PREV))
             x = p.S_init[sidx + ((mode_var(MODE) && p.vfirst) ? (int64_t)row * D + dk : (int64_t)dk * D + row)];
         S[i] = x;
     }
     put_state();
     int bad = named_bar_or(kStateBar, kBarThreads, 0);
     for (int ch = 0; ch < r.n && !bad; ch++) {
+        const int64_t unit = (int64_t)(r.chunk0 + ch) * H + r.h;
+        if (REC) {   // the state at the chunk's start, [dk][dv]
+            float *dst = p.st_S + unit * D * D + row;
+#pragma unroll
+            for (int i = 0; i < 64; i++) dst[(int64_t)(64 * half + i) * D] = S[i];
+        }
         // ---- Delta (and O) products of chunk ch
         if (issuer) {
             bool ok = mbar_wait(&r.bar[B_WREADY], ch & 1, ctl, st, 64);
@@ -790,6 +987,12 @@ __device__ __forceinline__ void run_state(const Run &r) {
             float v[32];
             tmem_ld32(lane_base + TM_DL + 32 * half, v);
             tmem_ld_wait();
+            if (REC) {   // the chunk's Delta, [64][dv] (rows past the chunk's end: 0)
+                const int nv = rows_of(r, ch);
+                float *dst = p.st_D + unit * C * D + row;
+#pragma unroll
+                for (int jj = 0; jj < 32; jj++) dst[(int64_t)(32 * half + jj) * D] = (32 * half + jj < nv) ? v[jj] : 0.f;
+            }
             if (FWD) {   // -Delta^T for the masked output product
                 uint32_t d16[16];
                 neg_pairs<16>(v, d16, nullptr);
@@ -868,7 +1071,7 @@ __device__ __forceinline__ void run_state(const Run &r) {
         local.abort = 0;
         mbar_wait(&r.bar[B_DRAIN2], 0, &local, st, 69);
     }
-    if (bad) return;
+    if (bad || REC) return;
     // outputs of the chain
     if (FWD) {
         // the first query head of a group writes the state's final value
@@ -1075,6 +1278,8 @@ static_assert(make_lay(MODE_FWD_KDA, ROLE_S).tx_bytes < (1u << 20) && make_lay(M
               "stage bytes exceed the mbarrier transaction count");
 static_assert(make_lay(MODE_FWD, ROLE_S).ngate <= kMaxGateSlots && make_lay(MODE_PRE, ROLE_M).ngate <= kMaxGateSlots,
               "gate slots exceed their barriers");
+static_assert(make_lay(MODE_BWD, ROLE_S).total == make_lay(MODE_FWD, ROLE_S).total, "backward uses the forward layout");
+static_assert(make_lay(MODE_REC, ROLE_S).total == make_lay(MODE_PRE, ROLE_S).total, "recompute uses the S layout");
 
 size_t smem_for(int mode, int role) { return make_lay(mode, role).total + 1024; }
 
@@ -1187,6 +1392,71 @@ int launch_tc_fwd(const cpdr_ctx *c, const int32_t *items, int n_items, const vo
         return launch_chain<MODE_FWD_VAR, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.Hq,
                                                   (cudaStream_t)stream);
     return launch_chain<MODE_FWD, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.Hq, (cudaStream_t)stream);
+}
+
+}  // namespace cpdr
+
+namespace cpdr {
+
+// Backward, recomputation of the forward (MODE_REC): every fragment's S chain
+// from its initial state (S_init where it continues a sequence), storing S at
+// each chunk start (st_S, [unit][dk][dv]) and each chunk's Delta (st_D,
+// [unit][64][dv]); unit = global chunk * H + head.
+int launch_tc_rec(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy,
+                  const float *S_init, float *st_S, float *st_D, void *stream) {
+    const auto &p = c->plan;
+    if (p.frags.empty()) return 0;
+    CUtensorMap tk, tv;
+    const int64_t tokens = (int64_t)p.B * p.T;
+    if (!make_tmap(&tk, k, tokens, p.H) || !make_tmap(&tv, v, tokens, p.H)) return (int)cudaErrorInvalidValue;
+    Params prm{};
+    prm.frags = c->dev.frags;
+    prm.items = c->dev.fwd_order;
+    prm.chunk0 = c->dev.frag_chunk0;
+    prm.wy = (const uint8_t *)wy;
+    prm.g = g;
+    prm.S_init = S_init;
+    prm.status = c->dev.status;
+    prm.H = p.H;
+    prm.Hq = p.H;
+    prm.G = 1;
+    prm.scale = p.scale;
+    prm.st_S = st_S;
+    prm.st_D = st_D;
+    return launch_chain<MODE_REC, ROLE_S>(tk, tk, tv, prm, (unsigned)p.frags.size(), (unsigned)p.H,
+                                          (cudaStream_t)stream);
+}
+
+// Backward, state-gradient chains (MODE_BWD) over `items`: pre = 1 writes the
+// gradient at each fragment's start into dS_ext; pre = 0 stores dS after each
+// chunk (st_dS, [unit][dk][dv]) and dDelta (st_dD, [unit][64][dv]).
+int launch_tc_bwd_chain(const cpdr_ctx *c, const int32_t *items, int n_items, int pre, const void *q, const void *k,
+                        const void *dout, const float *g, const void *wy, const float *dht, const float *dS_end,
+                        float *dS_ext, float *st_dS, float *st_dD, void *stream) {
+    const auto &p = c->plan;
+    if (n_items <= 0) return 0;
+    CUtensorMap tq, tk, tv;
+    const int64_t tokens = (int64_t)p.B * p.T;
+    if (!make_tmap(&tq, q, tokens, p.H) || !make_tmap(&tk, k, tokens, p.H) || !make_tmap(&tv, dout, tokens, p.H))
+        return (int)cudaErrorInvalidValue;
+    Params prm{};
+    prm.frags = c->dev.frags;
+    prm.items = items;
+    prm.chunk0 = c->dev.frag_chunk0;
+    prm.wy = (const uint8_t *)wy;
+    prm.g = g;
+    prm.S_ext = dS_ext;
+    prm.status = c->dev.status;
+    prm.H = p.H;
+    prm.Hq = p.H;
+    prm.G = 1;
+    prm.scale = p.scale;
+    prm.st_S = st_dS;
+    prm.st_D = st_dD;
+    prm.dht = dht;
+    prm.dS_end = dS_end;
+    prm.bwd_pre = pre;
+    return launch_chain<MODE_BWD, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.H, (cudaStream_t)stream);
 }
 
 }  // namespace cpdr
