@@ -371,7 +371,7 @@ size_t bwd_tc_scratch_bytes(const cpdr_ctx *c) {
     const auto &p = c->plan;
     const size_t units = p.wy_chunks.size() * (size_t)p.H;
     const size_t st = units * (size_t)p.dk * p.dv * sizeof(float), dl = units * 64 * (size_t)p.dv * sizeof(float);
-    return r256(wy_bytes(c)) + 2 * r256(st) + 2 * r256(dl);
+    return r256(wy_bytes(c)) + r256(units * 64 * 64 * sizeof(float)) + 2 * r256(st) + 2 * r256(dl);
 }
 
 // The backward on the tensor cores ([FLA-CP] §2.2, §4): the WY tiles; the
@@ -384,13 +384,14 @@ int launch_bwd_tc(const cpdr_ctx *c, const void *q, const void *k, const void *v
                   const void *dout, const float *dht, const float *S_init, const float *M, float *dS_ext,
                   float *dS_end, void *scratch, float *dq, float *dk, float *dv, float *dbeta, float *dg,
                   void *stream) {
-    cudaStream_t st = (cudaStream_t)stream;
     const auto &p = c->plan;
     const size_t units = p.wy_chunks.size() * (size_t)p.H;
     const size_t stb = units * (size_t)p.dk * p.dv * sizeof(float), dlb = units * 64 * (size_t)p.dv * sizeof(float);
     char *w = (char *)scratch;
     void *wy = w;
     w += r256(wy_bytes(c));
+    float *tmat = (float *)w;
+    w += r256(units * 64 * 64 * sizeof(float));
     float *st_S = (float *)w;
     w += r256(stb);
     float *st_dS = (float *)w;
@@ -398,7 +399,7 @@ int launch_bwd_tc(const cpdr_ctx *c, const void *q, const void *k, const void *v
     float *st_D = (float *)w;
     w += r256(dlb);
     float *st_dD = (float *)w;
-    int rc = launch_tc_wy(c, k, beta, g, wy, stream);
+    int rc = launch_tc_wy_t(c, k, beta, g, wy, tmat, stream);
     if (rc) return rc;
     rc = launch_tc_rec(c, k, v, g, wy, S_init, st_S, st_D, stream);
     if (rc) return rc;
@@ -407,16 +408,13 @@ int launch_bwd_tc(const cpdr_ctx *c, const void *q, const void *k, const void *v
                                  nullptr, dS_ext, nullptr, nullptr, stream);
         if (rc) return rc;
     }
-    if (!p.chains.empty()) {
-        dim3 mg((unsigned)p.chains.size(), (unsigned)p.H, (unsigned)(p.dk / BVT));
-        bwd_merge_kernel<128><<<mg, BT, 0, st>>>(c->dev.chains, dS_ext, M, dS_end, p.H, p.B);
-        rc = (int)cudaGetLastError();
-        if (rc) return rc;
-    }
+    rc = launch_tc_merge_rev(c, dS_ext, M, dS_end, stream);
+    if (rc) return rc;
     rc = launch_tc_bwd_chain(c, c->dev.fwd_order, (int)p.frags.size(), 0, q, k, dout, g, wy, dht, dS_end, nullptr,
                              st_dS, st_dD, stream);
     if (rc) return rc;
-    return launch_bwd_grad(c, q, k, v, beta, g, dout, st_S, st_D, st_dS, st_dD, dq, dk, dv, dbeta, dg, stream);
+    return launch_bwd_grad(c, q, k, v, beta, g, dout, tmat, st_S, st_D, st_dS, st_dD, dq, dk, dv, dbeta, dg,
+                           stream);
 }
 
 int launch_bwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta, const float *g,

@@ -22,10 +22,10 @@
 //   dG_C += sum_id (k ⊙ dk_Gamma)_id + gamma^C sum_d (dS' ⊙ S)_dd'  (summed)
 //   dg_t = sum_{s >= t in the chunk} dG_s
 // — the reverse-mode derivative of the chunk equations, written with every
-// gate factor as a bounded e^(G_i - G_j), j <= i.  The 14 matrix products
-// run on the tensor cores as warp-level mma.sync (tf32 operands, fp32
-// accumulation) from shared memory; the solve for T is a column-parallel
-// substitution.  Rows past the chunk's end are zero and not written.
+// gate factor as a bounded e^(G_i - G_j), j <= i.  The matrix products run
+// on the tensor cores as warp-level mma.sync (tf32 operands, fp32
+// accumulation) from shared memory; T comes from the WY build (fp32).  Rows
+// past the chunk's end are zero and not written.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -45,6 +45,7 @@ struct GradParams {
     const WyChunk *chunks;       // per global chunk: first token, valid rows
     const __nv_bfloat16 *q, *k, *v, *beta, *dout;
     const float *g;
+    const float *T;                  // per unit: the WY inverse T = (I + A)^-1, 64 x 64 (from the WY build)
     const float *S, *Dl, *dS, *dD;   // per unit: S [dk][dv], Delta [64][dv], dS' [dk][dv], dDelta [64][dv]
     float *dq, *dk, *dv, *dbeta, *dg;
     int H;
@@ -66,7 +67,7 @@ constexpr int OFF_T1 = OFF_OB;
 constexpr int OFF_T2 = OFF_W + C * PF * 4;
 constexpr int OFF_T3 = OFF_T2;
 constexpr int OFF_VEC = OFF_T2 + C * PS * 4;         // G, gam, Gam, beta, dG, dbeta (64 each), misc, solve sums
-constexpr int SMEM = OFF_VEC + (6 * C + 16 + 4 * C) * 4;
+constexpr int SMEM = OFF_VEC + (6 * C + 16) * 4;
 static_assert(PS * 4 == PB * 2, "T1 rows must overlay dO rows");
 static_assert(SMEM <= 232448, "gradient kernel shared memory");
 
@@ -341,24 +342,15 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__
         }
     }
     __syncthreads();
-    // ---- T = (I + A)^-1 by rows: T_i = e_i - sum_{l < i} A_il T_l.  Thread
-    // (j = tid % 64, part = tid / 64) sums l in its quarter of [j, i).
+    // ---- T = (I + A)^-1 of this unit, solved by the WY build (fp32)
     {
-        const int j = tid & 63, part = tid >> 6;
-        for (int e = tid; e < C * PS; e += NT) T2[e] = 0.f;
-        __syncthreads();
-        float *red = misc + 16;   // [4][64] partial sums
-        for (int i = 0; i < C; i++) {
-            float s = 0.f;
-            if (j < i) {
-                for (int l = j + part; l < i; l += 4) s = fmaf(bet[i] * T1[i * PS + l], T2[l * PS + j], s);
-            }
-            red[part * C + j] = s;
-            __syncthreads();
-            if (part == 0) T2[i * PS + j] = (j == i) ? 1.f : (j < i ? -(red[j] + red[C + j] + red[2 * C + j] + red[3 * C + j]) : 0.f);
-            __syncthreads();
+        const float *Tg = p.T + unit * C * C;
+        for (int e = tid; e < C * C / 4; e += NT) {
+            const int i = e / (C / 4), j = 4 * (e % (C / 4));
+            *reinterpret_cast<float4 *>(T2 + i * PS + j) = *reinterpret_cast<const float4 *>(Tg + i * C + j);
         }
     }
+    __syncthreads();
     // ---- TtW = T^T dW, TtU = T^T dDelta (64 x 128, register tiles)
     const Fv TT{T2, 1, PS};
     {
@@ -558,8 +550,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__
 // recomputed chunk states and Delta (st_S, st_D) and the state-gradient
 // chain's dS' and dDelta (st_dS, st_dD).  dq, dk, dv, dbeta, dg: fp32.
 int launch_bwd_grad(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta,
-                    const float *g, const void *dout, const float *st_S, const float *st_D, const float *st_dS,
-                    const float *st_dD, float *dq, float *dk, float *dv, float *dbeta, float *dg, void *stream) {
+                    const float *g, const void *dout, const float *tmat, const float *st_S, const float *st_D,
+                    const float *st_dS, const float *st_dD, float *dq, float *dk, float *dv, float *dbeta, float *dg,
+                    void *stream) {
     const auto &pl = c->plan;
     const int64_t units = (int64_t)pl.wy_chunks.size() * pl.H;
     if (units == 0) return 0;
@@ -572,6 +565,7 @@ int launch_bwd_grad(const cpdr_ctx *c, const void *q, const void *k, const void 
     prm.beta = (const __nv_bfloat16 *)beta;
     prm.dout = (const __nv_bfloat16 *)dout;
     prm.g = g;
+    prm.T = tmat;
     prm.S = st_S;
     prm.Dl = st_D;
     prm.dS = st_dS;

@@ -161,6 +161,8 @@ int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S
                  void *stream);
 // The merge on the tensor cores (tc_merge.cu; bf16 hi/lo splits, d = 128).
 int launch_tc_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init, void *stream);
+// The backward's reverse merge G <- M_j^T G + dS_ext[j] on the tensor cores.
+int launch_tc_merge_rev(const cpdr_ctx *c, const float *dS_ext, const float *M, float *dS_end, void *stream);
 int launch_zero_segments(const cpdr_ctx *c, float *S_ext, float *M, float *S_init,
                          float *final_state, int which, void *stream);
 // True when the tcgen05 kernels cover this problem (bf16, dk = dv = 128, scalar gate).
@@ -183,6 +185,9 @@ int launch_tc_kda_prep(const cpdr_ctx *c, const void *k, const void *q, const vo
                        void *wy, void *stream);
 int launch_tc_wy(const cpdr_ctx *c, const void *k, const void *beta, const float *g, void *wy,
                  void *stream);
+// The same, also writing T of every unit as fp32 64 x 64 into tmat (the backward).
+int launch_tc_wy_t(const cpdr_ctx *c, const void *k, const void *beta, const float *g, void *wy, float *tmat,
+                   void *stream);
 int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy,
                   float *S_ext, float *M, void *stream);
 // Backward on the tensor cores (tc_chain.cu): the forward recomputation
@@ -196,8 +201,9 @@ int launch_tc_bwd_chain(const cpdr_ctx *c, const int32_t *items, int n_items, in
 // Input gradients per (chunk, head) from the recomputed states and the
 // state-gradient chain's outputs (bwd_grad.cu).
 int launch_bwd_grad(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta,
-                    const float *g, const void *dout, const float *st_S, const float *st_D, const float *st_dS,
-                    const float *st_dD, float *dq, float *dk, float *dv, float *dbeta, float *dg, void *stream);
+                    const float *g, const void *dout, const float *tmat, const float *st_S, const float *st_D,
+                    const float *st_dS, const float *st_dD, float *dq, float *dk, float *dv, float *dbeta, float *dg,
+                    void *stream);
 // The backward runs on the tensor cores (bf16, d = 128, scalar gate, Hq == H,
 // [dk, dv] states); its scratch bytes (bwd.cu).
 bool bwd_uses_tc(const cpdr_ctx *c);

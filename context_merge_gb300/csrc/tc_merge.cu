@@ -16,6 +16,14 @@
 // TMEM lane quarter): they read D, add S_ext[j], write the new state's hi/lo
 // images as the next B operand (K-major: B^T[n][k] = S[k][n]) and S_init[j+1].
 // Every wait is bounded as in the chain kernels.
+//
+// The same kernel runs the backward's reverse merge (rev = 1): along each
+// chain, from its last segment down,
+//   G = dS_ext[r1];  dS_end[r1-1] = G
+//   for j = r1-1 .. r0+1:  G <- M_j^T G + dS_ext[j];  dS_end[j-1] = G
+// with the transposed transfer matrices of the article's backward (§2.2).
+// M_j's bf16 image is the same; the products read it as an MN-major A
+// operand, which is M_j^T.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -64,6 +72,7 @@ struct MergeArgs {
     float *S_init;
     int32_t *status;
     int H, B, vfirst;
+    int rev;          // 1: the reverse merge (M_j^T, chain walked from r1 down)
 };
 
 // Warp-uniform bounded wait: lane 0 waits, the verdict is broadcast, and
@@ -98,8 +107,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_merge_kernel(const __grid_cons
     uint32_t *tslot = reinterpret_cast<uint32_t *>(base + O_TSLOT);
     const MergeChain ch = p.chains[blockIdx.x];
     const int h = blockIdx.y, col0 = blockIdx.z * NB;
-    const int nsteps = ch.r1 - ch.r0 - 1;   // steps j = r0+1 .. r1-1
+    const int nsteps = ch.r1 - ch.r0 - 1;   // steps j = r0+1 .. r1-1 (reverse: r1-1 .. r0+1)
     auto idx_of = [&](int r) { return ((int64_t)(r * p.B + ch.b) * p.H + h) * D * D; };
+    const bool rev = p.rev != 0;
+    const int first = rev ? ch.r1 : ch.r0;                                       // segment of the first S_ext
+    auto jstep = [&](int step) { return rev ? ch.r1 - 1 - step : ch.r0 + 1 + step; };
+    auto out_of = [&](int j) { return rev ? j - 1 : j + 1; };                    // segment written after j
 
     if (threadIdx.x == 0) {
         mbar_init(&bar[MB_AFULL0], kCvtWarps);
@@ -194,14 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_merge_kernel(const __grid_cons
             if (lane == 0) mbar_arrive(&bar[MB_BFULL]);
         };
         float s[NB], e[NB];
-        load_row(p.S_ext + idx_of(ch.r0), s);
-        store_row(p.S_init + idx_of(ch.r0 + 1), s);
+        load_row(p.S_ext + idx_of(first), s);
+        store_row(p.S_init + idx_of(out_of(first)), s);
         if (nsteps > 0) {
             put_b(s);
-            load_row(p.S_ext + idx_of(ch.r0 + 1), e);
+            load_row(p.S_ext + idx_of(jstep(0)), e);
         }
         for (int step = 0; step < nsteps; step++) {
-            const int j = ch.r0 + 1 + step;
+            const int j = jstep(step);
             if (!warp_wait_bar(&bar[MB_DFULL], step & 1, ctl, p.status, 130)) break;
             tc_fence_after();
             float v[32];
@@ -212,13 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_merge_kernel(const __grid_cons
             for (int n = 0; n < NB; n++) s[n] = v[n] + e[n];
             tc_fence_before();
             if (step + 1 < nsteps) put_b(s);   // the next product may start
-            store_row(p.S_init + idx_of(j + 1), s);
-            if (step + 1 < nsteps) load_row(p.S_ext + idx_of(j + 1), e);
+            store_row(p.S_init + idx_of(out_of(j)), s);
+            if (step + 1 < nsteps) load_row(p.S_ext + idx_of(jstep(step + 1)), e);
         }
     } else if (w == kMmaWarp) {
         // ------------------------------------------------------------ products
         if (lane == 0) {
-            constexpr uint32_t id = idesc_bf16(128, NB, false, false);
+            // A = M_j (K-major image) or, reverse, M_j^T (the same image read MN-major)
+            const uint32_t id = rev ? idesc_bf16(128, NB, true, false) : idesc_bf16(128, NB, false, false);
             const uint32_t a0 = smem_u32(base + O_A), b0 = smem_u32(base + O_B);
             for (int step = 0; step < nsteps; step++) {
                 const int buf = step & 1;
@@ -231,10 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_merge_kernel(const __grid_cons
                 const uint32_t as[3] = {ahi, alo, ahi}, bs[3] = {bhi, bhi, blo};
 #pragma unroll
                 for (int t = 0; t < 3; t++) {
-                    const uint64_t ad = sdesc(as[t], 16, 1024), bd = sdesc(bs[t], 16, 1024);   // K-major, 128-byte swizzle
+                    // K-major: 128-byte swizzle, K atoms kAAtom apart; MN-major: M atoms
+                    // kAAtom apart (LBO), 16 K rows per step
+                    const uint64_t ad = rev ? sdesc(as[t], kAAtom, 1024) : sdesc(as[t], 16, 1024);
+                    const uint64_t bd = sdesc(bs[t], 16, 1024);
 #pragma unroll
                     for (int k = 0; k < D / 16; k++) {
-                        const uint64_t ao = ((k & 3) * 32 + (k >> 2) * kAAtom) >> 4;
+                        const uint64_t ao = rev ? (uint64_t)(k * 128) : ((k & 3) * 32 + (k >> 2) * kAAtom) >> 4;
                         const uint64_t bo = ((k & 3) * 32 + (k >> 2) * kBAtom) >> 4;
                         mma_bf16(tmem, ad + ao, bd + bo, id, (t > 0 || k > 0) ? 1u : 0u);
                     }
@@ -257,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_merge_kernel(const __grid_cons
         const uint32_t achunk = (uint32_t)((lane & 15) >> 1);
         float4 x[16];
         auto load_m = [&](int step) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.M + idx_of(ch.r0 + 1 + step)) + (16 * cw) * (D / 4) + lane;
+            const float4 *src = reinterpret_cast<const float4 *>(p.M + idx_of(jstep(step))) + (16 * cw) * (D / 4) + lane;
 #pragma unroll
             for (int i = 0; i < 16; i++) x[i] = src[i * (D / 4)];
         };
@@ -290,7 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_merge_kernel(const __grid_cons
 
 }  // namespace
 
-int launch_tc_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init, void *stream) {
+namespace {
+int launch_merge_dir(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init, int rev, void *stream) {
     const auto &pl = c->plan;
     if (pl.chains.empty()) return 0;
     MergeArgs a{};
@@ -301,7 +319,8 @@ int launch_tc_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float
     a.status = c->dev.status;
     a.H = pl.H;
     a.B = pl.B;
-    a.vfirst = pl.vfirst ? 1 : 0;
+    a.vfirst = (pl.vfirst && !rev) ? 1 : 0;
+    a.rev = rev;
     // 16-column tiles while they fit one wave (one CTA per SM), else 32
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
@@ -317,6 +336,16 @@ int launch_tc_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float
     };
     if (ctas16 <= sms) return go(tc_merge_kernel<16>, 16, MLay<16>::kSmem + 1024);
     return go(tc_merge_kernel<32>, 32, MLay<32>::kSmem + 1024);
+}
+}  // namespace
+
+int launch_tc_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S_init, void *stream) {
+    return launch_merge_dir(c, S_ext, M, S_init, 0, stream);
+}
+
+// The backward's reverse merge: dS_end from dS_ext and M ([dk][dv] states).
+int launch_tc_merge_rev(const cpdr_ctx *c, const float *dS_ext, const float *M, float *dS_end, void *stream) {
+    return launch_merge_dir(c, dS_ext, M, dS_end, 1, stream);
 }
 
 }  // namespace cpdr

@@ -146,8 +146,21 @@ __device__ __forceinline__ void st4(float *p, float a, float b, float c, float d
     *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
 }
 
+// T itself as fp32 64 x 64 row-major (the upper-right 32 x 32 block, scratch
+// during the solve, written as zero): role r of the pair writes rows
+// 32 r .. 32 r + 31, the lanes across each row.
+__device__ __forceinline__ void store_t_f32(const float *S, float *dst, int role) {
+    const int l = threadIdx.x & 31;
+#pragma unroll 4
+    for (int rr = 0; rr < 32; rr++) {
+        const int i = 32 * role + rr;
+        dst[i * 64 + l] = S[i * kLS + l];
+        dst[i * 64 + 32 + l] = i < 32 ? 0.f : S[i * kLS + 32 + l];
+    }
+}
+
 __device__ __forceinline__ void solve_unit_pair(float *S, uint8_t *dst, const float *beta, const float *gam, int role,
-                                                int bar_id) {
+                                                int bar_id, float *tdst = nullptr) {
     const int l = threadIdx.x & 31;
     const int o = 32 * role;
     {
@@ -238,6 +251,7 @@ __device__ __forceinline__ void solve_unit_pair(float *S, uint8_t *dst, const fl
     }
     named_bar(bar_id, 64);   // T complete in S
     store_tiles(S, dst, beta, gam, 8 * role, 8);
+    if (tdst) store_t_f32(S, tdst, role);
 }
 
 }  // namespace tc

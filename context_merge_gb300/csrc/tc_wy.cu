@@ -64,6 +64,7 @@ struct WyParams {
     const __nv_bfloat16 *beta;
     const float *g;
     uint8_t *wy;
+    float *tmat;   // nullable: T of every unit as fp32 64 x 64 (the backward's input gradients read it)
     int32_t *status;
     int n_units;   // chunks x heads
     int H;
@@ -276,7 +277,8 @@ tc_wy_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ WyP
             if (unit < p.n_units) {
                 float *S = reinterpret_cast<float *>(base + O_SCR + u_own * SCR_BYTES);
                 const WyGates gs = wy_gates(base, slot, u_own);
-                solve_unit_pair(S, p.wy + (size_t)unit * kWyUnitBytes, gs.beta, gs.gam, role, kPairBarId0 + u_own);
+                solve_unit_pair(S, p.wy + (size_t)unit * kWyUnitBytes, gs.beta, gs.gam, role, kPairBarId0 + u_own,
+                                p.tmat ? p.tmat + (size_t)unit * 64 * 64 : nullptr);
             }
             if (nxt_ok) write_gates(wy_gates(base, slot ^ 1, u_own), nxt);
             named_bar(kSolveBarId, 32 * WY_WARPS);   // scratch and gate slot free
@@ -314,6 +316,11 @@ size_t wy_bytes(const cpdr_ctx *c) {
 }
 
 int launch_tc_wy(const cpdr_ctx *c, const void *k, const void *beta, const float *g, void *wy, void *stream) {
+    return launch_tc_wy_t(c, k, beta, g, wy, nullptr, stream);
+}
+
+int launch_tc_wy_t(const cpdr_ctx *c, const void *k, const void *beta, const float *g, void *wy, float *tmat,
+                   void *stream) {
     const auto &pl = c->plan;
     const int64_t units = (int64_t)pl.wy_chunks.size() * pl.H;
     if (units == 0) return 0;
@@ -336,6 +343,7 @@ int launch_tc_wy(const cpdr_ctx *c, const void *k, const void *beta, const float
     prm.beta = (const __nv_bfloat16 *)beta;
     prm.g = g;
     prm.wy = (uint8_t *)wy;
+    prm.tmat = tmat;
     prm.status = c->dev.status;
     prm.n_units = (int)units;
     prm.H = pl.H;

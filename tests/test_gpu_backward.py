@@ -2,14 +2,19 @@
 (the reverse of the per-token scan, pinned by finite differences): the
 article's cut patterns at R = 2/4/8, fixed rows, packed batches with short
 and empty sequences, the zigzag layout, both gates and both dtypes, with and
-without a final-state gradient.  The forward path (WY build, pre-process,
-merge) runs first through the C-ABI and its S_init and M feed the backward.
+without a final-state gradient, and longer chains on the headline's and the
+merge-sensitive gate distributions.  The forward path (WY build,
+pre-process, merge) runs first through the C-ABI and its S_init and M feed
+the backward.
 
 Bars, per gradient tensor and per (sequence, head), ||x - ref|| / ||ref||:
-fp32 inputs 1e-4 (fp32 arithmetic everywhere, forward included); bf16
-inputs 5e-3, the article's gradient acceptance line ([FLA-CP] §5.2) -- the
-backward itself is fp32, but S_init and M come from the tensor-core forward,
-whose bf16 operands carry about 1e-3 relative error into the states."""
+fp32 inputs 1e-4 (the fp32 CUDA-core path, forward included); bf16 inputs
+5e-3, the article's gradient acceptance line ([FLA-CP] §5.2).  For bf16,
+d = 128 and the scalar gate the backward runs on the tensor cores (the
+recomputed states and the state-gradient chain with bf16 operands, the
+input gradients with tf32 products); its errors sit near 1e-3 to 2.6e-3."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -91,3 +96,13 @@ def test_backward_rows_and_layouts(case):
     w = inputs.Workload("bwd", "gdn", "bf16", case["B"], case["T"], 2, case["d"], case["R"], seed=43,
                         layout=case["layout"])
     print(case, run_case(w, with_dht=case["dht"]))
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("gdn_bf16_t262144_h16_d128_r64", dict(T=16384, H=2, R=16)),    # headline gate, 16-chunk fragments
+    ("merge_bf16_t16384_h4_d128_r16", dict(T=8192, H=2, R=8)),      # slow decay: cross-segment gradients matter
+], ids=["headline-gate", "merge-sensitive"])
+def test_backward_long_chains(name, kw):
+    kw = dict(kw)
+    w = dataclasses.replace(inputs.WORKLOADS[name], R=kw.pop("R"))
+    print(name, run_case(w, **kw))
