@@ -603,9 +603,12 @@ def run_backward(args, ws, rank):
                "sample": f"fp64 backward oracle on 1 of {H} heads, full T ({dt:.1f} s wall); tokens scaled by heads"}
     # algorithmic bytes of one backward: per (token, head) q, k, v, do, beta, g
     # in and dq, dk, dv (fp32), dbeta, dg out; per (segment, head) the S_init
-    # and M states read.  The backward is three launches (continuing-fragment
-    # pass, reverse merge, main pass; one when no sequence crosses a segment)
-    # timed together, so its line carries the whole backward's figure.
+    # and M states read.  The backward's launches are timed together, so its
+    # line carries the whole backward's figure: on the tensor-core path (bf16,
+    # d = 128, scalar gate) the WY build, the recomputed forward, the
+    # state-gradient chains of the continuing fragments, the reverse merge,
+    # the main chains and the input gradients; otherwise the CUDA-core
+    # continuing-fragment pass, reverse merge and main pass.
     es = 4 if w.dtype == "fp32" else 2
     gate_w = d if w.gate == "kda" else 1
     counts = ctx.counts()
@@ -617,7 +620,8 @@ def run_backward(args, ws, rank):
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": None, "kernel": f"bwd(all launches):{w.name}", "peak_source": peak_kind,
             "algorithmic_bytes_per_launch": nbytes, "ms_per_launch": ms}
-    launches = (1 + (2 if counts["chains"] else 0)) * args.steps
+    tc_bwd = counts["tc"] and w.gate == "gdn" and inp["Hq"] == H
+    launches = ((4 if tc_bwd else 1) + (2 if counts["chains"] else 0)) * args.steps
     line = {"metric": BWD_METRIC, "value": tokens * ws / (ms / 1e3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",

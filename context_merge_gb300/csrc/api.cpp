@@ -355,7 +355,6 @@ cpdr_status cpdr_bwd(const cpdr_ctx *c, const void *q, const void *k, const void
     CPDR_TRY(check_ctx(c));
     const auto &p = c->plan;
     if (p.Hq != p.H) return set_err(CPDR_ERR_UNSUPPORTED, "cpdr_bwd: grouped query heads are not covered");
-    if (p.vfirst) return set_err(CPDR_ERR_UNSUPPORTED, "cpdr_bwd: the [dv, dk] state layout is not covered");
     CPDR_TRY(check_ptr(q, "q"));
     CPDR_TRY(check_ptr(k, "k"));
     CPDR_TRY(check_ptr(v, "v"));

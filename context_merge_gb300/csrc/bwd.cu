@@ -55,6 +55,7 @@ struct BwdParams {
     int n_items;
     int mode;                 // 0: pre-process (dS_ext only), 1: main (input gradients)
     int H, B;
+    int vfirst;               // S_init and dht stored [dv][dk]
     float scale;
     const void *q, *k, *v, *beta, *dout;
     const float *g;
@@ -143,7 +144,9 @@ __global__ void __launch_bounds__(BT, 2) bwd_chain_kernel(const __grid_constant_
         float s[NR];
 #pragma unroll
         for (int j = 0; j < NR; j++)
-            s[j] = (f.flags & CPDR_FRAG_CONT_PREV) ? p.S_init[sidx + (int64_t)(r8 + 8 * j) * D + col] : 0.f;
+            s[j] = (f.flags & CPDR_FRAG_CONT_PREV)
+                       ? p.S_init[sidx + (p.vfirst ? (int64_t)col * D + r8 + 8 * j : (int64_t)(r8 + 8 * j) * D + col)]
+                       : 0.f;
         const int nck = (f.len + CKB - 1) / CKB;
         for (int m = 0; m < nck; m++) {
             const int t0 = m * CKB, nb = min(CKB, f.len - t0);
@@ -157,14 +160,16 @@ __global__ void __launch_bounds__(BT, 2) bwd_chain_kernel(const __grid_constant_
         {
             const float *src = nullptr;
             int64_t base = 0;
+            bool tr = false;   // dht in the [dv][dk] layout
             if (f.flags & CPDR_FRAG_ENDS_SEQ) {
-                if (p.dht) { src = p.dht; base = ((int64_t)f.seq * p.H + h) * D * D; }
+                if (p.dht) { src = p.dht; base = ((int64_t)f.seq * p.H + h) * D * D; tr = p.vfirst != 0; }
             } else if ((f.flags & CPDR_FRAG_CONT_NEXT) && p.mode == 1) {
                 src = p.dS_end;
                 base = sidx;
             }
 #pragma unroll
-            for (int j = 0; j < NR; j++) G[j] = src ? src[base + (int64_t)(r8 + 8 * j) * D + col] : 0.f;
+            for (int j = 0; j < NR; j++)
+                G[j] = src ? src[base + (tr ? (int64_t)col * D + r8 + 8 * j : (int64_t)(r8 + 8 * j) * D + col)] : 0.f;
         }
         // ---- reverse over the chunks
         for (int m = nck - 1; m >= 0; m--) {
@@ -357,7 +362,7 @@ size_t bwd_scratch_floats_per_cta(const cpdr_ctx *c) {
 
 bool bwd_uses_tc(const cpdr_ctx *c) {
     const auto &p = c->plan;
-    return c->use_tc && p.gate_kind == CPDR_GATE_SCALAR && p.Hq == p.H && !p.vfirst;
+    return c->use_tc && p.gate_kind == CPDR_GATE_SCALAR && p.Hq == p.H;
 }
 
 namespace {
@@ -430,6 +435,7 @@ int launch_bwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, c
     prm.frags = c->dev.frags;
     prm.H = p.H;
     prm.B = p.B;
+    prm.vfirst = p.vfirst ? 1 : 0;
     prm.scale = p.scale;
     prm.q = q; prm.k = k; prm.v = v; prm.beta = beta; prm.dout = dout; prm.g = g;
     prm.dht = dht; prm.S_init = S_init; prm.dS_end = dS_end; prm.dS_ext = dS_ext;

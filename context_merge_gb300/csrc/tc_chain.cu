@@ -783,17 +783,20 @@ __device__ __forceinline__ void run_state_bwd(const Run &r, float (&S)[64], int6
     // main pass dS_end where the fragment continues into the next segment
     const float *src = nullptr;
     int64_t base = 0;
+    bool tr = false;   // dht in the [dv][dk] layout
     if (r.flags & CPDR_FRAG_ENDS_SEQ) {
         if (p.dht) {
             src = p.dht;
             base = ((int64_t)r.seq * H + r.h) * D * D;
+            tr = p.vfirst != 0;
         }
     } else if ((r.flags & CPDR_FRAG_CONT_NEXT) && main_pass) {
         src = p.dS_end;
         base = sidx;
     }
 #pragma unroll
-    for (int i = 0; i < 64; i++) S[i] = src ? src[base + (int64_t)(64 * half + i) * D + row] : 0.f;
+    for (int i = 0; i < 64; i++)
+        S[i] = src ? src[base + (tr ? (int64_t)row * D + 64 * half + i : (int64_t)(64 * half + i) * D + row)] : 0.f;
     put_grad();
     int bad = named_bar_or(kStateBar, 256, 0);
     for (int t = 0; t < r.n && !bad; t++) {
@@ -1421,6 +1424,7 @@ int launch_tc_rec(const cpdr_ctx *c, const void *k, const void *v, const float *
     prm.Hq = p.H;
     prm.G = 1;
     prm.scale = p.scale;
+    prm.vfirst = p.vfirst;
     prm.st_S = st_S;
     prm.st_D = st_D;
     return launch_chain<MODE_REC, ROLE_S>(tk, tk, tv, prm, (unsigned)p.frags.size(), (unsigned)p.H,
@@ -1456,6 +1460,7 @@ int launch_tc_bwd_chain(const cpdr_ctx *c, const int32_t *items, int n_items, in
     prm.dht = dht;
     prm.dS_end = dS_end;
     prm.bwd_pre = pre;
+    prm.vfirst = p.vfirst;
     return launch_chain<MODE_BWD, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.H, (cudaStream_t)stream);
 }
 

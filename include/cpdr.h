@@ -271,16 +271,24 @@ cpdr_status cpdr_conv1d_fwd(const cpdr_ctx *ctx, const void *x, const float *wei
  *      end of every continuing fragment);
  *   3. every fragment runs the reverse chain from that end gradient (or dht,
  *      or 0) and writes the input gradients.
- * The reverse chain is the per-token chain rule, on CUDA cores in fp32,
- * with the forward states recomputed from S_init per token.
+ * For bf16 inputs, dk = dv = 128 and the scalar gate the chains run in chunk
+ * form on the tensor cores: the forward is recomputed with every chunk's
+ * starting state and Delta kept, the state-gradient chain runs chunk by
+ * chunk in reverse (tcgen05), the reverse merge on the tensor cores, and a
+ * parallel kernel forms the input gradients of every (chunk, head); the
+ * workspace then holds the WY tiles, the fp32 inverse T and four fp32
+ * tensors per (chunk, head) (about 216 KiB each).  Otherwise the reverse
+ * chain is the per-token chain rule, on CUDA cores in fp32, with the
+ * forward states recomputed from S_init per token.
  * In (device): q, k, v, beta, gate and do ([B, T, H, dv], the input dtype)
- * as for cpdr_fwd; dht [N, H, dk, dv] fp32 or NULL (zero); S_init and M as
- * cpdr_merge and cpdr_preprocess left them for these inputs.  Out (device,
- * fp32, zeroed and written here): dq, dk [B, T, H, dk], dv [B, T, H, dv],
- * dbeta [B, T, H], dgate (the gate's shape).  workspace: device memory of
- * cpdr_bwd_workspace_bytes() bytes, 256-byte aligned.
- * Errors: CPDR_ERR_UNSUPPORTED for grouped query heads or the [dv, dk]
- * state layout; CPDR_ERR_WORKSPACE; CPDR_ERR_INVALID; CPDR_ERR_CUDA.
+ * as for cpdr_fwd; dht [N, H, dk, dv] fp32 (with CPDR_FLAG_STATE_V_FIRST
+ * [N, H, dv, dk]) or NULL (zero); S_init and M as cpdr_merge and
+ * cpdr_preprocess left them for these inputs.  Out (device, fp32, written
+ * here): dq, dk [B, T, H, dk], dv [B, T, H, dv], dbeta [B, T, H], dgate (the
+ * gate's shape).  workspace: device memory of cpdr_bwd_workspace_bytes()
+ * bytes, 256-byte aligned.
+ * Errors: CPDR_ERR_UNSUPPORTED for grouped query heads; CPDR_ERR_WORKSPACE;
+ * CPDR_ERR_INVALID; CPDR_ERR_CUDA.
  */
 cpdr_status cpdr_bwd_workspace_bytes(const cpdr_ctx *ctx, size_t *bytes);
 cpdr_status cpdr_bwd(const cpdr_ctx *ctx, const void *q, const void *k, const void *v, const void *beta,

@@ -41,12 +41,17 @@ def run_case(w, lengths=None, with_dht=True, seed=7, **kw):
     N = B if inp["cu_seqlens"] is None else len(inp["cu_seqlens"]) - 1
     dht = torch.randn((N, H, d, d), generator=gen) if with_dht else None
     zig = w.layout == "zigzag"
-    ctx = cpdr.Context(B, T, H, d, R, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"], layout=w.layout)
+    vf = bool(w.state_v_first)
+    ctx = cpdr.Context(B, T, H, d, R, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"], layout=w.layout,
+                       state_v_first=vf)
     place = (lambda x: olayout.to_zigzag(x, R)) if zig else (lambda x: x)
     dev = {k: place(inp[k]).contiguous().cuda() for k in ("q", "k", "v", "beta", "g")}
     o, bufs = ctx.run(dev["q"], dev["k"], dev["v"], dev["beta"], dev["g"])
+    dht_dev = None
+    if dht is not None:   # [dv, dk] states take dht transposed
+        dht_dev = (dht.transpose(-1, -2) if vf else dht).contiguous().cuda()
     grads = ctx.backward(dev["q"], dev["k"], dev["v"], dev["beta"], dev["g"], place(do).contiguous().cuda(),
-                         bufs["S_init"], bufs["M"], dht=dht.cuda() if dht is not None else None)
+                         bufs["S_init"], bufs["M"], dht=dht_dev)
     torch.cuda.synchronize()
     ctx.check_device_status()
     unplace = (lambda x: olayout.from_zigzag(x, R)) if zig else (lambda x: x)
@@ -106,3 +111,10 @@ def test_backward_long_chains(name, kw):
     kw = dict(kw)
     w = dataclasses.replace(inputs.WORKLOADS[name], R=kw.pop("R"))
     print(name, run_case(w, **kw))
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp32", 64)])
+def test_backward_state_v_first(dtype, d):
+    """[dv, dk] states ([FLA-CP] §5.1 runs its gradient tests with state_v_first)."""
+    w = inputs.Workload("bwd", "gdn", dtype, 1, 2048, 2, d, 4, seed=45, state_v_first=True)
+    print(dtype, d, run_case(w, lengths=[700, 1348]))
