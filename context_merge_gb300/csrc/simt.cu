@@ -17,7 +17,10 @@
 // partial chunk carry k = v = q = beta = g = 0, which is the identity map.
 // For the per-dim gate (KDA) the exponentials are factored around the
 // chunk's middle row r: 2^(G_i - G_j) = 2^(G_i - G_r) 2^(G_r - G_j), each
-// factor bounded by the decay over half a chunk.
+// factor bounded by the decay over half a chunk.  A chunk whose decay
+// exceeds 2^100 either way of row r (where a factor could overflow) takes
+// exact per-term exponentials for A and Q K^T instead, and the unfactored
+// forms k 2^G, q 2^G, k 2^(G_C - G) for the rest.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -58,11 +61,14 @@ struct Smem {
     float S[D * LB];       // state tile (D x BV)
     float Dl[C * LB];      // Delta
     float g1[C];           // GDN: cumulative log2 gate per row
-    float gref[D], gC[D];  // KDA: G at the reference row and at the last row
+    float gref[D], gC[D];  // KDA: G at the reference row (0 when exact) and at the last row
     // KDA: the per-dim cumulative gates [C][LD] live in WU until the solve
     __device__ float *Gk() { return WU; }
     float beta[C];
+    int exact;             // KDA: this chunk takes exact per-term exponentials
 };
+
+constexpr float kFactorBound = 100.f;   // largest |G_i - G_r| (log2) of the factored form
 
 template <int D>
 constexpr size_t smem_bytes() { return sizeof(Smem<D>); }
@@ -97,11 +103,14 @@ __device__ void load_chunk(Smem<D> &s, const TIn *q, const TIn *k, const TIn *be
     }
     __syncthreads();
     // in-chunk cumulative sums (one thread per gate column)
+    int far = 0;
     if (PERDIM) {
         for (int d = tid; d < D; d += NT) {
             float acc = 0.f;
             for (int i = 0; i < C; i++) { acc += s.Gk()[i * LD + d]; s.Gk()[i * LD + d] = acc; }
-            s.gref[d] = s.Gk()[(C / 2 - 1) * LD + d];
+            const float gr = s.Gk()[(C / 2 - 1) * LD + d];
+            for (int i = 0; i < C; i++) far |= fabsf(s.Gk()[i * LD + d] - gr) > kFactorBound;
+            s.gref[d] = gr;
             s.gC[d] = acc;
         }
     } else if (tid < 32) {
@@ -116,8 +125,9 @@ __device__ void load_chunk(Smem<D> &s, const TIn *q, const TIn *k, const TIn *be
         s.g1[2 * tid] = excl + a0;
         s.g1[2 * tid + 1] = x;
     }
-    __syncthreads();
-    if (PERDIM) {
+    const int exact = __syncthreads_or(far);
+    if (tid == 0) s.exact = exact;
+    if (PERDIM && !exact) {
         for (int idx = tid; idx < C * D; idx += NT) {
             const int i = idx / D, d = idx % D;
             const float gi = s.Gk()[i * LD + d], gr = s.gref[d];
@@ -126,8 +136,49 @@ __device__ void load_chunk(Smem<D> &s, const TIn *q, const TIn *k, const TIn *be
             s.Ki[i * LD + d] = kv * exp2f(gi - gr);
             s.Qi[i * LD + d] = s.Qi[i * LD + d] * exp2f(gi - gr);
         }
-        __syncthreads();
     }
+    __syncthreads();
+}
+
+// Per-dim gate, exact branch: A_ij = beta_i sum_d k_id k_jd 2^(G_id - G_jd)
+// (j < i) and Q K^T ⊙ Lambda with one exponential per term (Ki, Qi hold k
+// and q; the cumulative gates are still in WU); then the tiles take the
+// unfactored forms Ki = k 2^G, Qi = q 2^G, Kj = k 2^(G_C - G) and gref = 0.
+template <int D, bool WITH_Q>
+__device__ void build_A_QK_exact(Smem<D> &s) {
+    constexpr int LD = Smem<D>::LD, LA = Smem<D>::LA;
+    const int tid = threadIdx.x;
+    const int j = tid % C, ib = tid / C;   // 4 blocks of 16 rows
+    const float *Gk = s.Gk();
+    float acc[16], accq[16];
+#pragma unroll
+    for (int r = 0; r < 16; r++) { acc[r] = 0.f; accq[r] = 0.f; }
+    for (int d = 0; d < D; d++) {
+        const float kj = s.Ki[j * LD + d], gj = Gk[j * LD + d];
+#pragma unroll
+        for (int r = 0; r < 16; r++) {
+            const int i = ib * 16 + r;
+            if (j > i) continue;
+            const float lam = exp2f(Gk[i * LD + d] - gj) * kj;
+            acc[r] = fmaf(s.Ki[i * LD + d], lam, acc[r]);
+            if (WITH_Q) accq[r] = fmaf(s.Qi[i * LD + d], lam, accq[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 16; r++) {
+        const int i = ib * 16 + r;
+        s.A[i * LA + j] = (j < i) ? s.beta[i] * acc[r] : 0.f;
+        if (WITH_Q) s.QK[i * LA + j] = (j <= i) ? accq[r] : 0.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < C * D; idx += NT) {
+        const int i = idx / D, d = idx % D;
+        const float gi = Gk[i * LD + d], kv = s.Ki[i * LD + d];
+        s.Kj[i * LD + d] = kv * exp2f(s.gC[d] - gi);
+        s.Ki[i * LD + d] = kv * exp2f(gi);
+        s.Qi[i * LD + d] = s.Qi[i * LD + d] * exp2f(gi);
+    }
+    for (int d = tid; d < D; d += NT) s.gref[d] = 0.f;
 }
 
 // A (strictly lower, scaled by beta_i) and QK ⊙ Lambda (lower incl. diagonal).
@@ -140,6 +191,10 @@ __device__ void build_A_QK(Smem<D> &s) {
     float acc[16], accq[16];
 #pragma unroll
     for (int r = 0; r < 16; r++) { acc[r] = 0.f; accq[r] = 0.f; }
+    if (PERDIM && s.exact) {
+        build_A_QK_exact<D, WITH_Q>(s);
+        return;
+    }
     for (int d = 0; d < D; d++) {
         const float kj = Kjs[j * LD + d];
 #pragma unroll
@@ -247,7 +302,7 @@ __device__ void state_step(Smem<D> &s, int n) {
     for (int r = 0; r < RPT; r++) {
         const int d = db * RPT + r;
         acc[r] = s.S[d * LB + c] * exp2f(PERDIM ? s.gC[d] : gC);
-        cf[r] = PERDIM ? exp2f(s.gC[d] - s.gref[d]) : 0.f;
+        cf[r] = PERDIM ? (s.exact ? 1.f : exp2f(s.gC[d] - s.gref[d])) : 0.f;
     }
     for (int j = 0; j < C; j++) {
         const float dl = s.Dl[j * LB + c];
@@ -255,7 +310,7 @@ __device__ void state_step(Smem<D> &s, int n) {
 #pragma unroll
         for (int r = 0; r < RPT; r++) {
             const int d = db * RPT + r;
-            // KDA: Gamma_jd k_jd = Kj_jd * 2^(G_C,d - G_ref,d)
+            // KDA: Gamma_jd k_jd = Kj_jd * 2^(G_C,d - G_ref,d) (exact: Kj_jd)
             const float kg = PERDIM ? s.Kj[j * LD + d] * cf[r] : s.Ki[j * LD + d] * gam;
             acc[r] = fmaf(kg, dl, acc[r]);
         }

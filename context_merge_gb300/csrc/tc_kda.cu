@@ -13,13 +13,18 @@
 // so that, in the chain, W = T' Kg, U = T' V, the state decays by Diag(gC)
 // and takes Delta^T Kgam, and the output is (Qg) S + P Delta.
 //
-// A and P are fp32 sums of the factorised products (k 2^(G - G_r)) .
-// (k 2^(G_r - G)) (the q factor rounded to bf16: P is a bf16 tile); a unit
-// whose in-chunk decay exceeds 2^100 either way of row r takes exact
-// per-term exponentials instead.  One CTA per unit, two per SM (CUDA
-// cores): coalesced loads, column scans, the gated tiles, A and P; then a
-// second kernel solves T, one warp per unit with the scalar-gate path's
-// solver, many units per SM at once.
+// A and P are sums of the factorised products (k 2^(G - G_r)) .
+// (k 2^(G_r - G)) over the key dims, one 64 x 64 x 128 contraction each, on
+// the tensor cores: the row operand X = [k 2^(G - G_r); q 2^(G - G_r)]
+// (128 rows, A then P) goes into TMEM, the column operand F = k 2^(G_r - G)
+// into shared memory, both split into bf16 hi and lo, and three products
+// X_hi F_hi + X_lo F_hi + X_hi F_lo accumulate A and P in fp32 (the dropped
+// lo . lo term is about 2^-16 of each product).  A unit whose in-chunk decay
+// exceeds 2^100 either way of row r takes exact per-term exponentials on the
+// CUDA cores instead.  One CTA per unit, two per SM: coalesced loads, column
+// scans, the gated tiles, the operands, the products and their epilogue;
+// then a second kernel solves T, one warp per unit with the scalar-gate
+// path's solver, many units per SM at once.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -46,30 +51,40 @@ struct KdaParams {
     const __nv_bfloat16 *k, *q, *beta;
     const float *g;
     uint8_t *wy;
+    int32_t *status;
     int H;
 };
 
-// Shared memory (two CTAs per SM):
-//   GF  [64][KP_LD] fp32: G (log2 cumsum), then k 2^(G_r - G)      ("KF")
-//   KB  [64][KP_LD] fp32: k, then k 2^(G - G_r)                     ("KE")
-//   QB  [64][KQ_LD] bf16: q, then bf16(q 2^(G - G_r))
-// then beta, G_r, G_C and the steep flag.
+// Shared memory (two CTAs per SM), from a 1 KiB-aligned base:
+//   GF  [64][KP_LD] fp32: the gates, then G (log2 cumsum per key dim)
+//   KB, QB [64][KQ_LD] bf16: k, q
+//   FH, FL: hi and lo of k 2^(G_r - G) as two swizzled 64-column bf16
+//           images each (the column operand of A and P)
+// then beta, G_r, G_C, the steep flag, the MMA barrier, the abort flag and
+// the TMEM slot.  At 101 KiB a preparation CTA cannot share an SM with a
+// chain CTA (130 KiB or more), which holds all of TMEM.
 constexpr int KQ_LD = D + 8;     // bf16 row stride (16-byte rows, offset banks)
 constexpr int KP_OFF_KB = C * KP_LD * 4;
-constexpr int KP_OFF_QB = 2 * C * KP_LD * 4;
-constexpr int KP_OFF_BETA = KP_OFF_QB + C * KQ_LD * 2;
+constexpr int KP_OFF_QB = KP_OFF_KB + C * KQ_LD * 2;
+constexpr int KP_OFF_FH = (KP_OFF_QB + C * KQ_LD * 2 + 1023) & ~1023;
+constexpr int KP_OFF_FL = KP_OFF_FH + 2 * 8192;
+constexpr int KP_OFF_BETA = KP_OFF_FL + 2 * 8192;
 constexpr int KP_OFF_GR = KP_OFF_BETA + C * 4;
 constexpr int KP_OFF_GC = KP_OFF_GR + D * 4;
 constexpr int KP_OFF_FLAG = KP_OFF_GC + D * 4;
-constexpr size_t KP_SMEM = (size_t)KP_OFF_FLAG + 16;
+constexpr int KP_OFF_BAR = KP_OFF_FLAG + 16;
+constexpr int KP_OFF_CTL = KP_OFF_BAR + 16;
+constexpr int KP_OFF_TSLOT = KP_OFF_CTL + 16;
+constexpr size_t KP_SMEM = (size_t)KP_OFF_TSLOT + 16 + 1024;   // + alignment slack
 static_assert(2 * (KP_SMEM + 1024) <= 233472, "two preparation CTAs must fit an SM");
+static_assert(KP_SMEM + 1024 + (130 << 10) + 1024 > 233472, "a preparation CTA must not share an SM with a chain CTA");
+// TMEM columns: X_hi [0, 64), X_lo [64, 128), the A / P accumulator [128, 192)
+constexpr uint32_t KP_TMEM_COLS = 256;
+constexpr uint32_t KP_COL_XLO = 64, KP_COL_ACC = 128;
 
 // element (i, d) of a 64 x 128 bf16 tile stored as two swizzled 64-column images
 __device__ __forceinline__ uint32_t img_off(int i, int d) {
     return (uint32_t)(d >> 6) * 8192u + sw128((uint32_t)i, (uint32_t)((d & 63) >> 3)) + (uint32_t)(d & 7) * 2u;
-}
-__device__ __forceinline__ void put_bf16(uint8_t *img, uint32_t off, float x) {
-    *reinterpret_cast<__nv_bfloat16 *>(img + off) = __float2bfloat16_rn(x);
 }
 // 8 values as 8 bf16 (one 16-byte chunk)
 __device__ __forceinline__ uint4 pack8f(const float *x) {
@@ -81,98 +96,140 @@ __device__ __forceinline__ uint4 pack8f(const float *x) {
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
-// hi = bf16(x) and lo = bf16(x - hi) of 8 values, one 16-byte store each
-__device__ __forceinline__ void store_hilo8(uint8_t *hi, uint8_t *lo, uint32_t off, const float *x, uint4 &h) {
-    h = pack8f(x);
-    const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
-    float r[8];
+// hi = bf16(x) and lo = bf16(x - hi) of 8 values as 4 + 4 packed pairs
+__device__ __forceinline__ void split8(const float *x, uint32_t *hi, uint32_t *lo) {
 #pragma unroll
     for (int e = 0; e < 4; e++) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hw[e]));
-        r[2 * e] = x[2 * e] - f.x;
-        r[2 * e + 1] = x[2 * e + 1] - f.y;
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        const float2 f = __bfloat1622float2(h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(x[2 * e] - f.x, x[2 * e + 1] - f.y);
+        hi[e] = *reinterpret_cast<const uint32_t *>(&h);
+        lo[e] = *reinterpret_cast<const uint32_t *>(&l);
     }
-    *reinterpret_cast<uint4 *>(hi + off) = h;
-    *reinterpret_cast<uint4 *>(lo + off) = pack8f(r);
+}
+// the same, one 16-byte store each at byte offset `off` of the two images
+__device__ __forceinline__ void store_hilo8(uint8_t *hi, uint8_t *lo, uint32_t off, const float *x) {
+    uint32_t h[4], l[4];
+    split8(x, h, l);
+    *reinterpret_cast<uint4 *>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+// 8 consecutive bf16 (one 16-byte chunk) as floats
+__device__ __forceinline__ void unpack8(uint4 v, float *x) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
+}
+// 16-byte asynchronous global-to-shared copy; `valid` false fills zeros
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void ld8f(const float *p, float *x) {
+    *reinterpret_cast<float4 *>(x) = *reinterpret_cast<const float4 *>(p);
+    *reinterpret_cast<float4 *>(x + 4) = *reinterpret_cast<const float4 *>(p + 4);
 }
 
 __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid_constant__ KdaParams p) {
-    extern __shared__ __align__(16) uint8_t smb[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smb = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *GF = reinterpret_cast<float *>(smb);
-    float *KB = reinterpret_cast<float *>(smb + KP_OFF_KB);
+    __nv_bfloat16 *KB = reinterpret_cast<__nv_bfloat16 *>(smb + KP_OFF_KB);
     __nv_bfloat16 *QB = reinterpret_cast<__nv_bfloat16 *>(smb + KP_OFF_QB);
+    uint8_t *FH = smb + KP_OFF_FH, *FL = smb + KP_OFF_FL;
     float *beta = reinterpret_cast<float *>(smb + KP_OFF_BETA);
     float *Gr = reinterpret_cast<float *>(smb + KP_OFF_GR), *GCv = reinterpret_cast<float *>(smb + KP_OFF_GC);
     int *steep = reinterpret_cast<int *>(smb + KP_OFF_FLAG);
-    const int tid = threadIdx.x;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smb + KP_OFF_BAR);
+    Ctl *ctl = reinterpret_cast<Ctl *>(smb + KP_OFF_CTL);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smb + KP_OFF_TSLOT);
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x, h = unit % p.H;
     const WyChunk ck = p.chunks[unit / p.H];
     const int nv = ck.nv;
     uint8_t *dst = p.wy + (size_t)unit * kKdaUnitBytes;
     auto tok = [&](int i) { return (ck.tok0 + i) * p.H + h; };
 
-    // ---- loads: g, k, q of the chunk (padded rows: 0), every load independent
-    for (int e = tid; e < C * D / 4; e += KP_THREADS) {
-        const int i = e / (D / 4), d = 4 * (e % (D / 4));
-        float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        uint2 k2 = make_uint2(0u, 0u), q2 = make_uint2(0u, 0u);
-        if (i < nv) {
-            g4 = __ldg(reinterpret_cast<const float4 *>(p.g + (int64_t)tok(i) * D + d));
-            k2 = __ldg(reinterpret_cast<const uint2 *>(p.k + (int64_t)tok(i) * D + d));
-            q2 = __ldg(reinterpret_cast<const uint2 *>(p.q + (int64_t)tok(i) * D + d));
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        ctl->abort = 0;
+        *steep = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (w == 0) {
+        tmem_alloc(tslot, KP_TMEM_COLS);
+        tmem_relinquish();
+    }
+
+    // ---- loads: g, k, q of the chunk as 16-byte asynchronous copies, all in
+    // flight at once (padded rows: zero-filled)
+    {
+        const uint32_t gf = smem_u32(GF), kb = smem_u32(KB), qb = smem_u32(QB);
+#pragma unroll
+        for (int m = 0; m < C * D / 4 / KP_THREADS; m++) {   // g: 32 copies per row
+            const int e = tid + m * KP_THREADS, i = e >> 5, d = 4 * (e & 31);
+            const int src = i < nv ? i : 0;
+            cp_async16(gf + (uint32_t)(i * KP_LD + d) * 4u, p.g + (int64_t)tok(src) * D + d, i < nv);
         }
-        *reinterpret_cast<float4 *>(GF + i * KP_LD + d) = g4;
-        const float2 ka = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&k2.x));
-        const float2 kb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&k2.y));
-        *reinterpret_cast<float4 *>(KB + i * KP_LD + d) = make_float4(ka.x, ka.y, kb.x, kb.y);
-        *reinterpret_cast<uint2 *>(QB + i * KQ_LD + d) = q2;
+#pragma unroll
+        for (int m = 0; m < C * D / 8 / KP_THREADS; m++) {   // k, q: 16 copies per row each
+            const int e = tid + m * KP_THREADS, i = e >> 4, d = 8 * (e & 15);
+            const int src = i < nv ? i : 0;
+            cp_async16(kb + (uint32_t)(i * KQ_LD + d) * 2u, p.k + (int64_t)tok(src) * D + d, i < nv);
+            cp_async16(qb + (uint32_t)(i * KQ_LD + d) * 2u, p.q + (int64_t)tok(src) * D + d, i < nv);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
     if (tid < C) beta[tid] = tid < nv ? __bfloat162float(p.beta[tok(tid)]) : 0.f;
-    if (tid == 0) *steep = 0;
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
 
-    // ---- in-chunk cumulative log2 gates per key dim
-    if (tid < D) {
+    // ---- in-chunk cumulative log2 gates per key dim: two threads per column,
+    // rows [0, 32) and [32, 64); the second half then adds the first's total
+    {
+        const int d = tid & (D - 1), h2 = tid >> 7;
         float run = 0.f;
-        int far = 0;
-        for (int i = 0; i < C; i++) {
-            run += GF[i * KP_LD + tid] * kLog2e;
-            GF[i * KP_LD + tid] = run;
+        for (int i = 32 * h2; i < 32 * h2 + 32; i++) {
+            run += GF[i * KP_LD + d] * kLog2e;
+            GF[i * KP_LD + d] = run;
         }
-        const float gr = GF[kRef * KP_LD + tid];
-        for (int i = 0; i < C; i++) far |= fabsf(GF[i * KP_LD + tid] - gr) > kFactorBound;
-        Gr[tid] = gr;
-        GCv[tid] = run;
-        reinterpret_cast<float *>(dst + kKdaOffGC)[tid] = exp2f(run);
+        __syncthreads();
+        const float gr = GF[kRef * KP_LD + d];   // the first half's total (kRef = 31)
+        int far = 0;
+        if (h2 == 1) {
+            for (int i = 32; i < 64; i++) {
+                const float x = GF[i * KP_LD + d] + gr;
+                GF[i * KP_LD + d] = x;
+                far |= fabsf(x - gr) > kFactorBound;
+            }
+            Gr[d] = gr;
+            GCv[d] = GF[(C - 1) * KP_LD + d];
+            reinterpret_cast<float *>(dst + kKdaOffGC)[d] = exp2f(GCv[d]);
+        } else {
+            for (int i = 0; i < 32; i++) far |= fabsf(GF[i * KP_LD + d] - gr) > kFactorBound;
+        }
         if (__any_sync(0xffffffffu, far) && (tid & 31) == 0) atomicOr(steep, 1);
     }
     __syncthreads();
     const bool exact = *steep != 0;
 
-    // ---- gated tiles; unless exact, the factorised operands replace the
-    // inputs in place.  A thread takes 8 consecutive key dims of a row (one
-    // 16-byte chunk of each image): items (row, group of 8), 4 per thread.
+    // ---- gated tiles, and unless exact the column operand F (hi, lo).  A
+    // thread takes 8 consecutive key dims of a row (one 16-byte chunk of
+    // each image): items (row, group of 8), 4 per thread.
     for (int item = tid; item < C * (D / 8); item += KP_THREADS) {
         const int i = item >> 4, d0 = (item & 15) * 8;
-        float Gv[8], kv[8], qv[8], gr[8], gc[8];
-        *reinterpret_cast<float4 *>(Gv) = *reinterpret_cast<const float4 *>(GF + i * KP_LD + d0);
-        *reinterpret_cast<float4 *>(Gv + 4) = *reinterpret_cast<const float4 *>(GF + i * KP_LD + d0 + 4);
-        *reinterpret_cast<float4 *>(kv) = *reinterpret_cast<const float4 *>(KB + i * KP_LD + d0);
-        *reinterpret_cast<float4 *>(kv + 4) = *reinterpret_cast<const float4 *>(KB + i * KP_LD + d0 + 4);
-        *reinterpret_cast<float4 *>(gr) = *reinterpret_cast<const float4 *>(Gr + d0);
-        *reinterpret_cast<float4 *>(gr + 4) = *reinterpret_cast<const float4 *>(Gr + d0 + 4);
-        *reinterpret_cast<float4 *>(gc) = *reinterpret_cast<const float4 *>(GCv + d0);
-        *reinterpret_cast<float4 *>(gc + 4) = *reinterpret_cast<const float4 *>(GCv + d0 + 4);
-        {
-            const uint4 q8 = *reinterpret_cast<const uint4 *>(QB + i * KQ_LD + d0);
-            const uint32_t qw[4] = {q8.x, q8.y, q8.z, q8.w};
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qw[e]));
-                qv[2 * e] = f.x;
-                qv[2 * e + 1] = f.y;
-            }
-        }
+        float Gv[8], kv[8], qv[8], gc[8];
+        ld8f(GF + i * KP_LD + d0, Gv);
+        ld8f(GCv + d0, gc);
+        unpack8(*reinterpret_cast<const uint4 *>(KB + i * KQ_LD + d0), kv);
+        unpack8(*reinterpret_cast<const uint4 *>(QB + i * KQ_LD + d0), qv);
         float kg[8], kgam[8], qg[8];
 #pragma unroll
         for (int e = 0; e < 8; e++) {
@@ -182,99 +239,155 @@ __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid
             qg[e] = qv[e] * gi;
         }
         const uint32_t off = img_off(i, d0);
-        uint4 h_kg, h_kgam;
-        store_hilo8(dst + kKdaOffKg, dst + kKdaOffKgLo, off, kg, h_kg);
-        store_hilo8(dst + kKdaOffKgam, dst + kKdaOffKgamLo, off, kgam, h_kgam);
+        store_hilo8(dst + kKdaOffKg, dst + kKdaOffKgLo, off, kg);
+        store_hilo8(dst + kKdaOffKgam, dst + kKdaOffKgamLo, off, kgam);
         *reinterpret_cast<uint4 *>(dst + kKdaOffQg + off) = pack8f(qg);
         if (!exact) {
-            float ke[8], kf[8], qe[8];
+            float gr[8], kf[8];
+            ld8f(Gr + d0, gr);
 #pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const float ef = exp2f(Gv[e] - gr[e]);
-                ke[e] = kv[e] * ef;
-                kf[e] = kv[e] * exp2f(gr[e] - Gv[e]);
-                qe[e] = qv[e] * ef;
-            }
-            *reinterpret_cast<float4 *>(GF + i * KP_LD + d0) = *reinterpret_cast<const float4 *>(kf);
-            *reinterpret_cast<float4 *>(GF + i * KP_LD + d0 + 4) = *reinterpret_cast<const float4 *>(kf + 4);
-            *reinterpret_cast<float4 *>(KB + i * KP_LD + d0) = *reinterpret_cast<const float4 *>(ke);
-            *reinterpret_cast<float4 *>(KB + i * KP_LD + d0 + 4) = *reinterpret_cast<const float4 *>(ke + 4);
-            *reinterpret_cast<uint4 *>(QB + i * KQ_LD + d0) = pack8f(qe);
+            for (int e = 0; e < 8; e++) kf[e] = kv[e] * exp2f(gr[e] - Gv[e]);
+            store_hilo8(FH, FL, off, kf);
         }
     }
-    __syncthreads();
 
-    // ---- A (strict lower, times beta_i) and P (lower incl. the diagonal):
-    // thread (bi, bj) owns rows bi + 16 r and columns bj + 16 c (r, c < 4),
-    // so the 16 column rows a warp reads are consecutive (no bank conflicts);
-    // pairs with c > r lie above the diagonal and are skipped
-    const int bi = tid >> 4, bj = tid & 15;
-    float a[4][4], pp[4][4];
-#pragma unroll
-    for (int r = 0; r < 4; r++)
-#pragma unroll
-        for (int c = 0; c < 4; c++) a[r][c] = pp[r][c] = 0.f;
+    // ---- the row operand X into TMEM: thread = one row of X (its warp's
+    // lane quadrant: rows 0..63 the k rows of A, 64..127 the q rows of P),
+    // half of the key dims per warp of a quadrant; lanes hold two K
+    // elements per 32-bit column (lower key dim in the low half)
+    const int quad = w & 3, half = w >> 2;
+    const int xr = 32 * quad + lane, xi = xr & 63;
+    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
     if (!exact) {
-        for (int d = 0; d < D; d += 4) {
-            float4 ke[4], kf[4];
-            float qe[4][4];
+        const __nv_bfloat16 *src = xr < 64 ? KB : QB;
 #pragma unroll
-            for (int r = 0; r < 4; r++) {
-                ke[r] = *reinterpret_cast<const float4 *>(KB + (bi + 16 * r) * KP_LD + d);
-                kf[r] = *reinterpret_cast<const float4 *>(GF + (bj + 16 * r) * KP_LD + d);
-                const uint2 q2 = *reinterpret_cast<const uint2 *>(QB + (bi + 16 * r) * KQ_LD + d);
-                const float2 qa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q2.x));
-                const float2 qb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q2.y));
-                qe[r][0] = qa.x; qe[r][1] = qa.y; qe[r][2] = qb.x; qe[r][3] = qb.y;
+        for (int s = 0; s < 2; s++) {
+            uint32_t hw[16], lw[16];
+#pragma unroll
+            for (int gq = 0; gq < 4; gq++) {
+                const int d0 = 64 * half + 32 * s + 8 * gq;
+                float Gv[8], gr[8], xv[8];
+                ld8f(GF + xi * KP_LD + d0, Gv);
+                ld8f(Gr + d0, gr);
+                unpack8(*reinterpret_cast<const uint4 *>(src + xi * KQ_LD + d0), xv);
+#pragma unroll
+                for (int e = 0; e < 8; e++) xv[e] *= exp2f(Gv[e] - gr[e]);
+                split8(xv, hw + 4 * gq, lw + 4 * gq);
             }
+            const uint32_t col = 32u * half + 16u * s;
+            tmem_st16(trow + col, hw);
+            tmem_st16(trow + KP_COL_XLO + col, lw);
+        }
+        tmem_st_wait();
+    }
+    fence_async_smem();   // F's stores become visible to the tensor core
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    float *Ag = reinterpret_cast<float *>(dst);
+    if (!exact) {
+        // ---- A and P (128 x 64, fp32 in TMEM) = X_hi F_hi + X_lo F_hi + X_hi F_lo
+        if (tid == 0) {
+            const uint32_t fh = smem_u32(FH), fl = smem_u32(FL);
+            constexpr uint32_t idesc = idesc_bf16(128, 64, false, false);
 #pragma unroll
-            for (int r = 0; r < 4; r++)
+            for (int pass = 0; pass < 3; pass++) {
+                const uint32_t xcol = pass == 1 ? KP_COL_XLO : 0u;
+                const uint32_t fb = pass == 2 ? fl : fh;
 #pragma unroll
-                for (int c = 0; c <= r; c++) {   // column block c > r lies above the diagonal
-                    a[r][c] = fmaf(ke[r].x, kf[c].x, a[r][c]);
-                    a[r][c] = fmaf(ke[r].y, kf[c].y, a[r][c]);
-                    a[r][c] = fmaf(ke[r].z, kf[c].z, a[r][c]);
-                    a[r][c] = fmaf(ke[r].w, kf[c].w, a[r][c]);
-                    pp[r][c] = fmaf(qe[r][0], kf[c].x, pp[r][c]);
-                    pp[r][c] = fmaf(qe[r][1], kf[c].y, pp[r][c]);
-                    pp[r][c] = fmaf(qe[r][2], kf[c].z, pp[r][c]);
-                    pp[r][c] = fmaf(qe[r][3], kf[c].w, pp[r][c]);
+                for (int kk = 0; kk < D / 16; kk++) {
+                    const uint32_t koff = (uint32_t)(kk & 3) * 32u + (uint32_t)(kk >> 2) * 8192u;
+                    mma_bf16_ts(tmem + KP_COL_ACC, tmem + xcol + 8u * kk, sdesc(fb + koff, 16, 1024), idesc,
+                                (pass | kk) != 0 ? 1u : 0u);
                 }
+            }
+            mma_commit(bar);
+        }
+        int ok = 0;
+        if (lane == 0) ok = mbar_wait(bar, 0, ctl, p.status, 120) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) {
+            tc_fence_after();
+            // epilogue: warp = lane quadrant x half of the columns
+            float vv[32];
+            tmem_ld32(trow + KP_COL_ACC + 32u * half, vv);
+            tmem_ld_wait();
+            const int j0 = 32 * half;
+            if (xr < 64) {   // A row xi: strict lower part, times beta_i
+                const float bi = beta[xi];
+#pragma unroll
+                for (int q4 = 0; q4 < 8; q4++) {
+                    float4 a4;
+                    const int j = j0 + 4 * q4;
+                    a4.x = j < xi ? bi * vv[4 * q4] : 0.f;
+                    a4.y = j + 1 < xi ? bi * vv[4 * q4 + 1] : 0.f;
+                    a4.z = j + 2 < xi ? bi * vv[4 * q4 + 2] : 0.f;
+                    a4.w = j + 3 < xi ? bi * vv[4 * q4 + 3] : 0.f;
+                    *reinterpret_cast<float4 *>(Ag + xi * C + j) = a4;
+                }
+            } else {         // P row xi: lower part including the diagonal
+#pragma unroll
+                for (int c8 = 0; c8 < 4; c8++) {
+                    float pv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) pv[e] = j0 + 8 * c8 + e <= xi ? vv[8 * c8 + e] : 0.f;
+                    *reinterpret_cast<uint4 *>(dst + kKdaOffP + sw128((uint32_t)xi, (uint32_t)((j0 >> 3) + c8))) =
+                        pack8f(pv);
+                }
+            }
+        } else if (lane == 0) {
+            // the products did not complete in time (status recorded): wait
+            // for them once more before the TMEM is released
+            Ctl local;
+            local.abort = 0;
+            mbar_wait(bar, 0, &local, p.status, 121);
         }
     } else {
-        // exact exponentials per term (decays beyond 2^100 around row r)
+        // ---- exact exponentials per term (decays beyond 2^100 around row r),
+        // on the CUDA cores: thread (bi, bj) owns rows bi + 16 r and columns
+        // bj + 16 c (r, c < 4); pairs with j > i lie above the diagonal
+        const int bi = tid >> 4, bj = tid & 15;
+        float a[4][4], pp[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; r++)
+#pragma unroll
+            for (int c = 0; c < 4; c++) a[r][c] = pp[r][c] = 0.f;
         for (int d = 0; d < D; d++) {
 #pragma unroll
             for (int r = 0; r < 4; r++) {
                 const int i = bi + 16 * r;
-                const float Gi = GF[i * KP_LD + d], kv = KB[i * KP_LD + d];
+                const float Gi = GF[i * KP_LD + d], kv = __bfloat162float(KB[i * KQ_LD + d]);
                 const float qv = __bfloat162float(QB[i * KQ_LD + d]);
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
                     const int j = bj + 16 * c;
                     if (j > i) continue;
-                    const float lam = exp2f(Gi - GF[j * KP_LD + d]) * KB[j * KP_LD + d];
+                    const float lam = exp2f(Gi - GF[j * KP_LD + d]) * __bfloat162float(KB[j * KQ_LD + d]);
                     a[r][c] = fmaf(kv, lam, a[r][c]);
                     pp[r][c] = fmaf(qv, lam, pp[r][c]);
                 }
             }
         }
-    }
-    // A (fp32, row-major 64 x 64) and beta go into the unit's first tiles,
-    // which the solve reads and then overwrites with T', hi(T''), lo(T'')
-    float *Ag = reinterpret_cast<float *>(dst);
 #pragma unroll
-    for (int r = 0; r < 4; r++) {
-        const int i = bi + 16 * r;
+        for (int r = 0; r < 4; r++) {
+            const int i = bi + 16 * r;
 #pragma unroll
-        for (int c = 0; c < 4; c++) {
-            const int j = bj + 16 * c;
-            Ag[i * C + j] = j < i ? beta[i] * a[r][c] : 0.f;
-            put_bf16(dst + kKdaOffP, sw128((uint32_t)i, (uint32_t)(j >> 3)) + (uint32_t)(j & 7) * 2u,
-                     j <= i ? pp[r][c] : 0.f);
+            for (int c = 0; c < 4; c++) {
+                const int j = bj + 16 * c;
+                Ag[i * C + j] = j < i ? beta[i] * a[r][c] : 0.f;
+                *reinterpret_cast<__nv_bfloat16 *>(dst + kKdaOffP + sw128((uint32_t)i, (uint32_t)(j >> 3)) +
+                                                   (uint32_t)(j & 7) * 2u) = __float2bfloat16_rn(j <= i ? pp[r][c] : 0.f);
+            }
         }
     }
+    // A and beta go into the unit's first tiles, which the solve reads and
+    // then overwrites with T', hi(T''), lo(T'')
     if (tid < C) reinterpret_cast<float *>(dst + 2 * kWyTileBytes)[tid] = beta[tid];
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (w == 0) tmem_dealloc(tmem, KP_TMEM_COLS);
 }
 
 // T = (I + A)^-1 of every unit, one warp per unit (persistent warps): A and
@@ -321,6 +434,7 @@ int launch_tc_kda_prep(const cpdr_ctx *c, const void *k, const void *q, const vo
     prm.beta = (const __nv_bfloat16 *)beta;
     prm.g = g;
     prm.wy = (uint8_t *)wy;
+    prm.status = c->dev.status;
     prm.H = pl.H;
     cudaError_t e = cudaFuncSetAttribute(tc_kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)KP_SMEM);

@@ -97,12 +97,26 @@ def test_tiny_and_ragged(case, gate, dtype):
     print(case, compare(run_gpu(inp), run_oracle(inp), inp))
 
 
+@pytest.mark.parametrize("gate", ["gdn", "kda"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_steep_decay(dtype):
+def test_steep_decay(dtype, gate):
     """alpha ~ sigmoid(N(-3, 0.5)) ~ 0.05 per token: the in-chunk decay spans
     far more than 2^100, which takes the exact-exponential branch."""
-    w = inputs.Workload("steep", "gdn", dtype, 1, 2048, 4, 128, 4, gate_dist=("sigmoid", -3.0, 0.5), seed=21)
+    w = inputs.Workload("steep", gate, dtype, 1, 2048, 4, 128, 4, gate_dist=("sigmoid", -3.0, 0.5), seed=21)
     inp = inputs.make_inputs(w, device="cpu")
+    print(compare(run_gpu(inp), run_oracle(inp), inp))
+
+
+def test_kda_steep_and_mild_units():
+    """Per-dim gates where a few (chunk, head) units decay steeply in a few key
+    dims and the rest mildly: both branches of the preparation (the tensor-core
+    products and the exact per-term exponentials) in one call."""
+    inp = gen("kda_bf16_t32768_h32_d128_r16", B=1, T=2048, H=4)
+    g = inp["g"].clone()
+    g[0, 64 * 3:64 * 4, 1, :3] = -6.0     # chunk 3, head 1: span about 280 in log2
+    g[0, 64 * 17 + 40:64 * 18, 2, 100] = -12.0
+    inp["g"] = g
+    inp["R"] = 4
     print(compare(run_gpu(inp), run_oracle(inp), inp))
 
 
