@@ -213,16 +213,15 @@ class Problem:
 
 
 def _backward(self, do, dht=None, nthreads=None):
-    """Gradients of sum <do, o> + sum <dht, S_final> (fp64): dict with dq,
-    dk [B,T,H,dk], dv [B,T,H,dv], dbeta [B,T,H], dg (the gate's shape).
-    ``do`` has the input dtype of q, k, v (fp32 array or bf16 bits)."""
+    """Gradients of sum <do, o> + sum <dht, S_final> (fp64): dict with dq
+    [B,T,Hq,dk], dk [B,T,H,dk], dv [B,T,H,dv], dbeta [B,T,H], dg (the gate's
+    shape).  ``do`` is [B,T,Hq,dv] in the input dtype of q, k, v (fp32 array
+    or bf16 bits)."""
     lib = _load()
-    if self.Hq != self.H:
-        raise ValueError("the backward oracle covers Hq == H only")
     d_o, ddt = as_oracle_array(do)
-    if ddt != self._p.in_dtype or d_o.shape != (self.B, self.T, self.H, self.dv):
-        raise ValueError("do must be [B, T, H, dv] in the input dtype")
-    out = dict(dq=np.zeros((self.B, self.T, self.H, self.dk)), dk=np.zeros((self.B, self.T, self.H, self.dk)),
+    if ddt != self._p.in_dtype or d_o.shape != (self.B, self.T, self.Hq, self.dv):
+        raise ValueError("do must be [B, T, Hq, dv] in the input dtype")
+    out = dict(dq=np.zeros((self.B, self.T, self.Hq, self.dk)), dk=np.zeros((self.B, self.T, self.H, self.dk)),
                dv=np.zeros((self.B, self.T, self.H, self.dv)), dbeta=np.zeros((self.B, self.T, self.H)),
                dg=np.zeros(self.g.shape))
     dhtp = None

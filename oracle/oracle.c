@@ -532,7 +532,7 @@ int oracle_chunked_pre(const oracle_problem *P, int C, const void *k, const void
 }
 
 /* ------------------------------------------------------------------ */
-/* 4. the backward of the per-token scan (order 0, Hq == H)             */
+/* 4. the backward of the per-token scan (order 0)                      */
 /* ------------------------------------------------------------------ */
 /*
  * Gradients of L = sum_t <do_t, o_t> + sum_n <dht_n, S_final,n> with
@@ -546,6 +546,10 @@ int oracle_chunked_pre(const oracle_problem *P, int C, const void *k, const void
  *   dP = G - k g_u^T,            dalpha_d = sum_c dP_dc S_{t-1,dc},
  *   dg_t = alpha dalpha (per key dim; summed over d for a scalar gate),
  *   dL/dS_{t-1} = Diag(alpha) dP.
+ * With grouped query heads (Hq = G H, [FLA-CP] §5.1) the G query heads hq of
+ * state head h each read S_t: o_t,hq = scale S_t^T q_t,hq, so each has its
+ * own dq_t,hq = scale S_t do_t,hq and G collects scale q_t,hq do_t,hq^T of
+ * every one of them; the rest of the step is the state head's.
  * States are recomputed forward from checkpoints every 64 tokens.
  */
 typedef struct {
@@ -560,7 +564,7 @@ static void bwd_item(void *vctx, int64_t item, double *scratch) {
     bwd_ctx *c = (bwd_ctx *)vctx;
     const oracle_problem *P = c->P;
     const int n = (int)(item / P->H), h = (int)(item % P->H);
-    const int dk = P->dk, dv = P->dv, H = P->H;
+    const int dk = P->dk, dv = P->dv, H = P->H, Gq = q_group(P), Hq = H * Gq;
     const size_t sz = (size_t)dk * dv;
     const int CK = 64;
     int64_t s, e;
@@ -597,20 +601,21 @@ static void bwd_item(void *vctx, int64_t item, double *scratch) {
             const double *Sp = st + (size_t)i * sz, *St = st + (size_t)(i + 1) * sz;
             for (int d = 0; d < dk; d++) {
                 kk[d] = ld_in(c->k, th * dk + d, P->in_dtype);
-                qq[d] = ld_in(c->q, th * dk + d, P->in_dtype);
                 al[d] = exp((double)(P->gate_kind == 0 ? c->g[th] : c->g[th * dk + d]));
             }
-            for (int cc = 0; cc < dv; cc++) {
-                vv[cc] = ld_in(c->v, th * dv + cc, P->in_dtype);
-                dd[cc] = P->scale * ld_in(c->dout, th * dv + cc, P->in_dtype);
-            }
+            for (int cc = 0; cc < dv; cc++) vv[cc] = ld_in(c->v, th * dv + cc, P->in_dtype);
             const double b = ld_in(c->beta, th, P->in_dtype);
-            /* dq_t = scale S_t do_t; G += scale q_t do_t^T */
-            for (int d = 0; d < dk; d++) {
-                double acc = 0.0;
-                for (int cc = 0; cc < dv; cc++) acc += St[d * dv + cc] * dd[cc];
-                c->dq[th * dk + d] = acc;
-                for (int cc = 0; cc < dv; cc++) G[d * dv + cc] += qq[d] * dd[cc];
+            /* per query head of this state: dq_t = scale S_t do_t; G += scale q_t do_t^T */
+            for (int gq = 0; gq < Gq; gq++) {
+                const int64_t tq = t * Hq + (int64_t)h * Gq + gq;
+                for (int d = 0; d < dk; d++) qq[d] = ld_in(c->q, tq * dk + d, P->in_dtype);
+                for (int cc = 0; cc < dv; cc++) dd[cc] = P->scale * ld_in(c->dout, tq * dv + cc, P->in_dtype);
+                for (int d = 0; d < dk; d++) {
+                    double acc = 0.0;
+                    for (int cc = 0; cc < dv; cc++) acc += St[d * dv + cc] * dd[cc];
+                    c->dq[tq * dk + d] = acc;
+                    for (int cc = 0; cc < dv; cc++) G[d * dv + cc] += qq[d] * dd[cc];
+                }
             }
             /* P = Diag(alpha) S_{t-1}, u = v - P^T k */
             for (int d = 0; d < dk; d++)
@@ -657,13 +662,12 @@ static void bwd_item(void *vctx, int64_t item, double *scratch) {
     free(ck); free(st); free(G); free(Pm); free(tmp);
 }
 
-/* dout: [B*T, H, dv] in the input dtype; dht: [N, H, dk, dv] (nullable);
- * dq, dk: [B*T, H, dk]; dv: [B*T, H, dv]; dbeta: [B*T, H]; dg like the gate.
- * Returns 2 for grouped query heads and 1 for order 1 (not covered). */
+/* dout: [B*T, Hq, dv] in the input dtype; dht: [N, H, dk, dv] (nullable);
+ * dq: [B*T, Hq, dk]; dk: [B*T, H, dk]; dv: [B*T, H, dv]; dbeta: [B*T, H];
+ * dg like the gate.  Returns 1 for order 1 (not covered). */
 int oracle_backward(const oracle_problem *P, const void *q, const void *k, const void *v, const void *beta,
                     const float *g, const void *dout, const double *dht, double *dq, double *dk, double *dv,
                     double *dbeta, double *dg, int nthreads) {
-    if (q_group(P) != 1) return 2;
     if (P->order != 0) return 1;
     bwd_ctx c = {P, q, k, v, beta, dout, g, dht, dq, dk, dv, dbeta, dg};
     run_pool(bwd_item, &c, (int64_t)P->num_seqs * P->H, nthreads, 1);
