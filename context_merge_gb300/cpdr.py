@@ -294,11 +294,12 @@ class Context:
 
     def backward(self, q, k, v, beta, g, do, S_init, M, dht=None, workspace=None, stream=None):
         """Gradients of sum <do, o> + sum <dht, final_state> (fp32 tensors
-        dq, dk, dv, dbeta, dg).  S_init and M are the buffers the forward's
-        merge and pre-process filled for the same inputs."""
+        dq, dk, dv, dbeta, dg).  do is shaped like o ([B, T, Hq, dv]); S_init
+        and M are the buffers the forward's merge and pre-process filled for
+        the same inputs."""
         self._check_inputs(q=q, k=k, v=v, beta=beta, g=g)
-        if tuple(do.shape) != tuple(v.shape) or do.dtype != v.dtype or not do.is_contiguous():
-            raise ValueError("do must match v")
+        if tuple(do.shape) != tuple(q.shape[:3]) + (v.shape[3],) or do.dtype != v.dtype or not do.is_contiguous():
+            raise ValueError("do must be shaped like o, in the dtype of v")
         dev = q.device
         f32 = torch.float32
         out = dict(dq=torch.empty(q.shape, dtype=f32, device=dev), dk=torch.empty(k.shape, dtype=f32, device=dev),

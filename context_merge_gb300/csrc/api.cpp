@@ -354,7 +354,9 @@ cpdr_status cpdr_bwd(const cpdr_ctx *c, const void *q, const void *k, const void
                      void *stream) {
     CPDR_TRY(check_ctx(c));
     const auto &p = c->plan;
-    if (p.Hq != p.H) return set_err(CPDR_ERR_UNSUPPORTED, "cpdr_bwd: grouped query heads are not covered");
+    if (!cpdr::bwd_uses_tc(c) && !cpdr::bwd_simt_fits(c))
+        return set_err(CPDR_ERR_UNSUPPORTED,
+                       "cpdr_bwd: the query heads of one state do not fit the backward chain's shared memory");
     CPDR_TRY(check_ptr(q, "q"));
     CPDR_TRY(check_ptr(k, "k"));
     CPDR_TRY(check_ptr(v, "v"));
@@ -382,7 +384,7 @@ cpdr_status cpdr_bwd(const cpdr_ctx *c, const void *q, const void *k, const void
     const size_t tok = (size_t)p.B * (size_t)p.T;
     cudaStream_t st = (cudaStream_t)stream;
     if (!cpdr::bwd_uses_tc(c)) {   // the CUDA-core chains add their sums atomically
-        cudaError_t e = cudaMemsetAsync(dq, 0, tok * p.H * p.dk * sizeof(float), st);
+        cudaError_t e = cudaMemsetAsync(dq, 0, tok * p.Hq * p.dk * sizeof(float), st);
         if (e == cudaSuccess) e = cudaMemsetAsync(dk, 0, tok * p.H * p.dk * sizeof(float), st);
         if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, tok * p.H * sizeof(float), st);
         if (e == cudaSuccess) e = cudaMemsetAsync(dgate, 0, s.gate, st);

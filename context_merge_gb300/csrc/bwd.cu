@@ -20,6 +20,9 @@
 //   dbeta = k^T G u,  dk = beta G u - P g_u,  dP = G - k g_u^T,
 //   dg = alpha * sum_c dP S_{t-1} (per key dim; summed for a scalar gate),
 //   dL/dS_{t-1} = Diag(alpha) dP.
+// With grouped query heads (Hq = G H, [FLA-CP] §5.1) the first line runs
+// for each of the state's G query heads: G += scale q_g do_g^T and
+// dq_g = scale S_t do_g.
 // The forward states are recomputed per token: from S_init (or zero) the
 // chain first stores the state at every 64-token boundary, then walks the
 // chunks backwards, recomputing each chunk's states into a per-CTA scratch.
@@ -55,6 +58,7 @@ struct BwdParams {
     int n_items;
     int mode;                 // 0: pre-process (dS_ext only), 1: main (input gradients)
     int H, B;
+    int G;                    // query heads per state (q, do, dq have G H heads)
     int vfirst;               // S_init and dht stored [dv][dk]
     float scale;
     const void *q, *k, *v, *beta, *dout;
@@ -70,14 +74,21 @@ struct BwdParams {
 
 // Shared memory of one chunk's token vectors (raw input types; the gate as
 // alpha = e^g in fp32), then the per-warp partial sums of the reverse pass.
+// The query-head parts follow the struct, one block per query head of the
+// state: q rows [G][CKB][D], do columns [G][CKB][BVT], and the partial sums
+// [8 warps][2 + G][D] (dk, dalpha, then dq of each query head).
 template <typename TIn, int D, bool PERDIM>
 struct BwdSmem {
     static constexpr int NA = PERDIM ? D : 1;
-    TIn kc[CKB][D], qc[CKB][D], vc[CKB][BVT], dc[CKB][BVT];
+    TIn kc[CKB][D], vc[CKB][BVT];
     float ac[CKB][NA], bc[CKB];
-    float red[8][3][D];
     float redb[8];
 };
+template <typename TIn, int D, bool PERDIM>
+constexpr size_t bwd_smem_bytes(int G) {
+    return (sizeof(BwdSmem<TIn, D, PERDIM>) + 15) / 16 * 16 + (size_t)G * CKB * D * sizeof(TIn) +
+           (size_t)G * CKB * BVT * sizeof(TIn) + (size_t)8 * (2 + G) * D * sizeof(float);
+}
 
 __device__ __forceinline__ float tof(float x) { return x; }
 __device__ __forceinline__ float tof(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -87,6 +98,11 @@ __global__ void __launch_bounds__(BT, 2) bwd_chain_kernel(const __grid_constant_
     constexpr int NR = D / 8;                      // rows per thread
     extern __shared__ __align__(16) uint8_t bsm[];
     BwdSmem<TIn, D, PERDIM> &sm = *reinterpret_cast<BwdSmem<TIn, D, PERDIM> *>(bsm);
+    const int GQ = p.G, Hq = p.H * GQ;
+    TIn *qc = reinterpret_cast<TIn *>(bsm + (sizeof(BwdSmem<TIn, D, PERDIM>) + 15) / 16 * 16);   // [G][CKB][D]
+    TIn *dc = qc + (size_t)GQ * CKB * D;                                                          // [G][CKB][BVT]
+    float *red = reinterpret_cast<float *>(dc + (size_t)GQ * CKB * BVT);                          // [8][2 + G][D]
+    auto redp = [&](int ww, int which) { return red + ((size_t)ww * (2 + GQ) + which) * D; };
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int c = tid >> 3, r8 = tid & 7;          // column in the tile, row group
     const int ntile = D / BVT;
@@ -107,14 +123,24 @@ __global__ void __launch_bounds__(BT, 2) bwd_chain_kernel(const __grid_constant_
                 const int i = e / D, d = e % D;
                 const int64_t th = (f.tok0 + t0 + i) * p.H + h;
                 sm.kc[i][d] = k[th * D + d];
-                if (with_q) sm.qc[i][d] = q[th * D + d];
                 if (PERDIM) sm.ac[i][d] = exp2f(p.g[th * D + d] * 1.4426950408889634f);
+            }
+            if (with_q) {
+                for (int e = tid; e < GQ * nb * D; e += BT) {
+                    const int gq = e / (nb * D), i = (e / D) % nb, d = e % D;
+                    const int64_t tq = (f.tok0 + t0 + i) * Hq + (int64_t)h * GQ + gq;
+                    qc[((size_t)gq * CKB + i) * D + d] = q[tq * D + d];
+                }
+                for (int e = tid; e < GQ * nb * BVT; e += BT) {
+                    const int gq = e / (nb * BVT), i = (e / BVT) % nb, cc = e % BVT;
+                    const int64_t tq = (f.tok0 + t0 + i) * Hq + (int64_t)h * GQ + gq;
+                    dc[((size_t)gq * CKB + i) * BVT + cc] = dout[tq * D + tile * BVT + cc];
+                }
             }
             for (int e = tid; e < nb * BVT; e += BT) {
                 const int i = e / BVT, cc = e % BVT;
                 const int64_t th = (f.tok0 + t0 + i) * p.H + h;
                 sm.vc[i][cc] = v[th * D + tile * BVT + cc];
-                if (with_q) sm.dc[i][cc] = dout[th * D + tile * BVT + cc];
             }
             for (int i = tid; i < nb; i += BT) {
                 const int64_t th = (f.tok0 + t0 + i) * p.H + h;
@@ -196,15 +222,37 @@ __global__ void __launch_bounds__(BT, 2) bwd_chain_kernel(const __grid_constant_
 #pragma unroll
                     for (int j = 0; j < NR; j++) spn[j] = tok[((int64_t)(i - 1) * BT + tid) * NR + j];
                 }
-                const float bt = sm.bc[i], ddc = p.scale * tof(sm.dc[i][c]);
-                // dq partial (S_t do) and G += q do^T; P = Diag(alpha) S_{t-1}
-                float pdq[NR], pk = 0.f, gk = 0.f;
+                const float bt = sm.bc[i];
+                if (p.mode == 1) __syncthreads();   // the previous token's sums were read
+                // per query head: dq partial (S_t do), summed over the warp's
+                // 4 columns into this warp's slot, and G += q do^T
+                for (int gq = 0; gq < GQ; gq++) {
+                    const float ddc = p.scale * tof(dc[((size_t)gq * CKB + i) * BVT + c]);
+                    const TIn *qrow = qc + ((size_t)gq * CKB + i) * D;
+                    float pdq[NR];
+#pragma unroll
+                    for (int j = 0; j < NR; j++) {
+                        pdq[j] = s[j] * ddc;
+                        G[j] = fmaf(tof(qrow[r8 + 8 * j]), ddc, G[j]);
+                    }
+                    if (p.mode == 1) {
+#pragma unroll
+                        for (int j = 0; j < NR; j++) {
+#pragma unroll
+                            for (int o = 8; o < 32; o <<= 1) pdq[j] += __shfl_xor_sync(0xffffffffu, pdq[j], o);
+                        }
+                        if (lane < 8) {
+#pragma unroll
+                            for (int j = 0; j < NR; j++) redp(w, 2 + gq)[lane + 8 * j] = pdq[j];
+                        }
+                    }
+                }
+                // P = Diag(alpha) S_{t-1}: P^T k and G^T k
+                float pk = 0.f, gk = 0.f;
 #pragma unroll
                 for (int j = 0; j < NR; j++) {
                     const int d = r8 + 8 * j;
                     const float kd = tof(sm.kc[i][d]);
-                    pdq[j] = s[j] * ddc;
-                    G[j] = fmaf(tof(sm.qc[i][d]), ddc, G[j]);
                     pk = fmaf(alpha(i, d) * sp[j], kd, pk);
                     gk = fmaf(G[j], kd, gk);
                 }
@@ -234,34 +282,35 @@ __global__ void __launch_bounds__(BT, 2) bwd_chain_kernel(const __grid_constant_
                     for (int j = 0; j < NR; j++) {
 #pragma unroll
                         for (int o = 8; o < 32; o <<= 1) {
-                            pdq[j] += __shfl_xor_sync(0xffffffffu, pdq[j], o);
                             pdk[j] += __shfl_xor_sync(0xffffffffu, pdk[j], o);
                             pda[j] += __shfl_xor_sync(0xffffffffu, pda[j], o);
                         }
                     }
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) pb += __shfl_xor_sync(0xffffffffu, pb, o);
-                    __syncthreads();   // the previous token's sums were read
                     if (lane < 8) {
 #pragma unroll
                         for (int j = 0; j < NR; j++) {
-                            sm.red[w][0][lane + 8 * j] = pdq[j];
-                            sm.red[w][1][lane + 8 * j] = pdk[j];
-                            sm.red[w][2][lane + 8 * j] = pda[j];
+                            redp(w, 0)[lane + 8 * j] = pdk[j];
+                            redp(w, 1)[lane + 8 * j] = pda[j];
                         }
                     }
                     if (lane == 0) sm.redb[w] = pb;
                     __syncthreads();
                     float dgs = 0.f;   // scalar gate: this thread's share of sum_d alpha dalpha
-                    for (int e = tid; e < 3 * D; e += BT) {
+                    const int64_t tqd = ((f.tok0 + t0 + i) * Hq + (int64_t)h * GQ) * D;   // dq of query head 0
+                    for (int e = tid; e < (2 + GQ) * D; e += BT) {
                         const int which = e / D, d = e % D;
                         float acc = 0.f;
 #pragma unroll
-                        for (int ww = 0; ww < 8; ww++) acc += sm.red[ww][which][d];
-                        if (which == 0) atomicAdd(p.dq + th * D + d, acc);
-                        else if (which == 1) atomicAdd(p.dk + th * D + d, acc);
-                        else if (PERDIM) atomicAdd(p.dg + th * D + d, alpha(i, d) * acc);
-                        else dgs += alpha(i, d) * acc;
+                        for (int ww = 0; ww < 8; ww++) acc += redp(ww, which)[d];
+                        if (which == 0) atomicAdd(p.dk + th * D + d, acc);
+                        else if (which == 1) {
+                            if (PERDIM) atomicAdd(p.dg + th * D + d, alpha(i, d) * acc);
+                            else dgs += alpha(i, d) * acc;
+                        } else {
+                            atomicAdd(p.dq + tqd + (int64_t)(which - 2) * D + d, acc);
+                        }
                     }
                     if (tid == 0) {
                         float acc = 0.f;
@@ -324,7 +373,7 @@ __global__ void __launch_bounds__(BT) bwd_merge_kernel(const MergeChain *__restr
 
 template <typename TIn, int D, bool PERDIM>
 int launch_chain_t(const BwdParams &prm, int grid, cudaStream_t st) {
-    const size_t sm = sizeof(BwdSmem<TIn, D, PERDIM>);
+    const size_t sm = bwd_smem_bytes<TIn, D, PERDIM>(prm.G);
     cudaError_t e = cudaFuncSetAttribute(bwd_chain_kernel<TIn, D, PERDIM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return (int)e;
@@ -358,6 +407,23 @@ size_t bwd_scratch_floats_per_cta(const cpdr_ctx *c) {
     for (const auto &f : p.frags) maxlen = std::max(maxlen, f.len);
     const int64_t nck = (maxlen + CKB - 1) / CKB;
     return (size_t)(nck + CKB) * p.dk * BVT;
+}
+
+// Whether the CUDA-core chain's shared memory holds the G query heads' rows
+// of one chunk.
+bool bwd_simt_fits(const cpdr_ctx *c) {
+    const auto &p = c->plan;
+    const int G = p.Hq / p.H;
+    const bool f32 = p.in_dtype == CPDR_DTYPE_F32, perdim = p.gate_kind == CPDR_GATE_PER_DIM;
+    size_t need;
+    if (p.dk == 64)
+        need = f32 ? (perdim ? bwd_smem_bytes<float, 64, true>(G) : bwd_smem_bytes<float, 64, false>(G))
+                   : (perdim ? bwd_smem_bytes<__nv_bfloat16, 64, true>(G) : bwd_smem_bytes<__nv_bfloat16, 64, false>(G));
+    else
+        need = f32 ? (perdim ? bwd_smem_bytes<float, 128, true>(G) : bwd_smem_bytes<float, 128, false>(G))
+                   : (perdim ? bwd_smem_bytes<__nv_bfloat16, 128, true>(G)
+                             : bwd_smem_bytes<__nv_bfloat16, 128, false>(G));
+    return need <= 232448;
 }
 
 bool bwd_uses_tc(const cpdr_ctx *c) {
@@ -435,6 +501,7 @@ int launch_bwd(const cpdr_ctx *c, const void *q, const void *k, const void *v, c
     prm.frags = c->dev.frags;
     prm.H = p.H;
     prm.B = p.B;
+    prm.G = p.Hq / p.H;
     prm.vfirst = p.vfirst ? 1 : 0;
     prm.scale = p.scale;
     prm.q = q; prm.k = k; prm.v = v; prm.beta = beta; prm.dout = dout; prm.g = g;

@@ -206,6 +206,7 @@ int launch_bwd_grad(const cpdr_ctx *c, const void *q, const void *k, const void 
                     void *stream);
 // The backward runs on the tensor cores (bf16, d = 128, scalar gate, Hq == H,
 // [dk, dv] states); its scratch bytes (bwd.cu).
+bool bwd_simt_fits(const cpdr_ctx *c);
 bool bwd_uses_tc(const cpdr_ctx *c);
 size_t bwd_tc_scratch_bytes(const cpdr_ctx *c);
 // Backward (bwd.cu): scratch per CTA and the grid it is sized for.

@@ -279,16 +279,21 @@ cpdr_status cpdr_conv1d_fwd(const cpdr_ctx *ctx, const void *x, const float *wei
  * workspace then holds the WY tiles, the fp32 inverse T and four fp32
  * tensors per (chunk, head) (about 216 KiB each).  Otherwise the reverse
  * chain is the per-token chain rule, on CUDA cores in fp32, with the
- * forward states recomputed from S_init per token.
- * In (device): q, k, v, beta, gate and do ([B, T, H, dv], the input dtype)
+ * forward states recomputed from S_init per token.  With grouped query
+ * heads (Hq = G H) each state's chain takes the G query heads that read it
+ * ([FLA-CP] §5.1): its state gradient collects scale q do^T of every one of
+ * them, and each gets its own dq.
+ * In (device): q, k, v, beta, gate and do ([B, T, Hq, dv], the input dtype)
  * as for cpdr_fwd; dht [N, H, dk, dv] fp32 (with CPDR_FLAG_STATE_V_FIRST
  * [N, H, dv, dk]) or NULL (zero); S_init and M as cpdr_merge and
  * cpdr_preprocess left them for these inputs.  Out (device, fp32, written
- * here): dq, dk [B, T, H, dk], dv [B, T, H, dv], dbeta [B, T, H], dgate (the
- * gate's shape).  workspace: device memory of cpdr_bwd_workspace_bytes()
- * bytes, 256-byte aligned.
- * Errors: CPDR_ERR_UNSUPPORTED for grouped query heads; CPDR_ERR_WORKSPACE;
- * CPDR_ERR_INVALID; CPDR_ERR_CUDA.
+ * here): dq [B, T, Hq, dk], dk [B, T, H, dk], dv [B, T, H, dv], dbeta
+ * [B, T, H], dgate (the gate's shape).  workspace: device memory of
+ * cpdr_bwd_workspace_bytes() bytes, 256-byte aligned.
+ * Errors: CPDR_ERR_UNSUPPORTED when the G query heads' rows of one chunk do
+ * not fit the CUDA-core chain's shared memory (at d = 128: G above 8 for
+ * bf16 with the scalar gate, 6 with the per-dim gate; 4 and 3 for fp32);
+ * CPDR_ERR_WORKSPACE; CPDR_ERR_INVALID; CPDR_ERR_CUDA.
  */
 cpdr_status cpdr_bwd_workspace_bytes(const cpdr_ctx *ctx, size_t *bytes);
 cpdr_status cpdr_bwd(const cpdr_ctx *ctx, const void *q, const void *k, const void *v, const void *beta,

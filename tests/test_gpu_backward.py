@@ -3,7 +3,8 @@
 article's cut patterns at R = 2/4/8, fixed rows, packed batches with short
 and empty sequences, the zigzag layout, both gates and both dtypes, with and
 without a final-state gradient, and longer chains on the headline's and the
-merge-sensitive gate distributions.  The forward path (WY build,
+merge-sensitive gate distributions, grouped query heads (G = 2, 3) on both
+gates with [dv, dk] states and the zigzag layout.  The forward path (WY build,
 pre-process, merge) runs first through the C-ABI and its S_init and M feed
 the backward.
 
@@ -36,14 +37,15 @@ def _cuda(cpdr_lib):
 def run_case(w, lengths=None, with_dht=True, seed=7, **kw):
     inp = inputs.make_inputs(w, device="cpu", lengths=lengths, **kw)
     B, T, H, d, R = inp["B"], inp["T"], inp["H"], inp["d"], inp["R"]
+    Hq = inp["Hq"]
     gen = torch.Generator().manual_seed(seed)
-    do = torch.randn((B, T, H, d), generator=gen).to(w.torch_dtype)
+    do = torch.randn((B, T, Hq, d), generator=gen).to(w.torch_dtype)
     N = B if inp["cu_seqlens"] is None else len(inp["cu_seqlens"]) - 1
     dht = torch.randn((N, H, d, d), generator=gen) if with_dht else None
     zig = w.layout == "zigzag"
     vf = bool(w.state_v_first)
     ctx = cpdr.Context(B, T, H, d, R, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"], layout=w.layout,
-                       state_v_first=vf)
+                       state_v_first=vf, Hq=Hq)
     place = (lambda x: olayout.to_zigzag(x, R)) if zig else (lambda x: x)
     dev = {k: place(inp[k]).contiguous().cuda() for k in ("q", "k", "v", "beta", "g")}
     o, bufs = ctx.run(dev["q"], dev["k"], dev["v"], dev["beta"], dev["g"])
@@ -66,7 +68,7 @@ def run_case(w, lengths=None, with_dht=True, seed=7, **kw):
         for b, s, e in spans:
             if e == s:
                 continue
-            for h in range(H):
+            for h in range(Hq if key == "dq" else H):
                 x, r = got[key][b, s:e, h], ref[key][b, s:e, h]
                 den = np.linalg.norm(r)
                 num = np.linalg.norm(x - r)
@@ -118,3 +120,22 @@ def test_backward_state_v_first(dtype, d):
     """[dv, dk] states ([FLA-CP] §5.1 runs its gradient tests with state_v_first)."""
     w = inputs.Workload("bwd", "gdn", dtype, 1, 2048, 2, d, 4, seed=45, state_v_first=True)
     print(dtype, d, run_case(w, lengths=[700, 1348]))
+
+
+@pytest.mark.parametrize("case", [
+    dict(gate="gdn", dtype="bf16", G=2, lengths=[700, 1348], R=4),
+    dict(gate="kda", dtype="bf16", G=2, lengths=[1000, 0, 1048], R=2),
+    dict(gate="gdn", dtype="fp32", G=3, lengths=[517, 1531], R=4, d=64),
+    dict(gate="kda", dtype="fp32", G=2, lengths=[2048], R=8),
+    dict(gate="gdn", dtype="bf16", G=2, lengths=[2048], R=4, vfirst=True, layout="zigzag"),
+], ids=["gdn-bf16-g2", "kda-bf16-g2", "gdn-fp32-g3-d64", "kda-fp32-g2", "gdn-bf16-g2-vfirst-zigzag"])
+def test_backward_grouped_query_heads(case):
+    """G query heads per state ([FLA-CP] §5.1): each state's chain takes the
+    scale q do^T of all of its query heads, each query head its own dq."""
+    base = inputs.WORKLOADS["kda_bf16_t32768_h32_d128_r16" if case["gate"] == "kda" else "gdn_bf16_b2_t8192_h16_d128_r8"]
+    H = 2
+    w = inputs.Workload("bwd", case["gate"], case["dtype"], 1, sum(case["lengths"]), H, case.get("d", 128), case["R"],
+                        gate_dist=base.gate_dist, seed=47, Hq=H * case["G"], layout=case.get("layout", "contiguous"),
+                        state_v_first=case.get("vfirst", False))
+    lengths = case["lengths"] if case.get("layout", "contiguous") == "contiguous" else None
+    print(case, run_case(w, lengths=lengths))
