@@ -54,6 +54,8 @@ def parse():
     # profiling aids: shrink the workload (same shapes otherwise) for ncu captures
     ap.add_argument("--T", type=int, default=None, help="override tokens per row (profiling only)")
     ap.add_argument("--H", type=int, default=None, help="override heads (profiling only)")
+    ap.add_argument("--Hq", type=int, default=None,
+                    help="override query heads, a multiple of the heads (profiling only)")
     return ap.parse_args()
 
 
@@ -211,7 +213,7 @@ def variant_keys(w, inp):
     out = {}
     if w.layout != "contiguous":
         out["layout"] = w.layout
-    if w.Hq:
+    if w.Hq or (inp is not None and inp["Hq"] != inp["H"]):
         out["Hq"] = w.Hq if inp is None else inp["Hq"]
     if w.state_v_first:
         out["state_v_first"] = True
@@ -272,7 +274,7 @@ def run_ours(args, ws, rank, local):
     from context_merge_gb300 import cpdr
     w = inputs.WORKLOADS[args.workload]
     dev = torch.device("cuda", torch.cuda.current_device())
-    inp = inputs.make_inputs(w, device=dev, seed=w.seed + 1000 * rank, T=args.T, H=args.H)
+    inp = inputs.make_inputs(w, device=dev, seed=w.seed + 1000 * rank, T=args.T, H=args.H, Hq=args.Hq)
     B, T, H, d, R = inp["B"], inp["T"], inp["H"], inp["d"], inp["R"]
     ctx = cpdr.Context(B, T, H, d, R, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"],
                        force_simt=args.force_simt, layout=w.layout, Hq=inp["Hq"], state_v_first=w.state_v_first)
@@ -550,8 +552,10 @@ def bwd_oracle_sample(inp, w, heads=1):
     """Time the fp64 backward oracle on the first `heads` heads, full T."""
     import oracle
     hs = min(heads, inp["H"])
-    sub = {k: inp[k][:, :, :hs].contiguous().cpu() for k in ("q", "k", "v", "beta", "g")}
-    do = torch.randn(sub["v"].shape, generator=torch.Generator().manual_seed(5)).to(sub["v"].dtype)
+    G = inp["Hq"] // inp["H"]
+    sub = {k: inp[k][:, :, :hs * (G if k == "q" else 1)].contiguous().cpu() for k in ("q", "k", "v", "beta", "g")}
+    do = torch.randn(sub["q"].shape[:3] + sub["v"].shape[3:],
+                     generator=torch.Generator().manual_seed(5)).to(sub["v"].dtype)
     P = oracle.Problem(sub["q"], sub["k"], sub["v"], sub["beta"], sub["g"], cu_seqlens=inp["cu_seqlens"])
     threads = oracle.default_threads()
     t0 = time.perf_counter()
@@ -563,13 +567,14 @@ def run_backward(args, ws, rank):
     from context_merge_gb300 import cpdr
     w = inputs.WORKLOADS[args.workload]
     dev = torch.device("cuda", torch.cuda.current_device())
-    inp = inputs.make_inputs(w, device=dev, seed=w.seed + 1000 * rank, T=args.T, H=args.H)
+    inp = inputs.make_inputs(w, device=dev, seed=w.seed + 1000 * rank, T=args.T, H=args.H, Hq=args.Hq)
     B, T, H, d, R = inp["B"], inp["T"], inp["H"], inp["d"], inp["R"]
+    Hq = inp["Hq"]
     ctx = cpdr.Context(B, T, H, d, R, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"],
-                       force_simt=args.force_simt)
+                       force_simt=args.force_simt, layout=w.layout, Hq=Hq, state_v_first=w.state_v_first)
     q, k, v, beta, g = (inp[x] for x in ("q", "k", "v", "beta", "g"))
     o, bufs = ctx.run(q, k, v, beta, g)
-    do = torch.randn(v.shape, device=dev, dtype=torch.float32).to(v.dtype)
+    do = torch.randn(o.shape, device=dev, dtype=torch.float32).to(v.dtype)
     dht = torch.randn(bufs["final_state"].shape, device=dev)
     work = torch.empty(ctx.bwd_workspace_bytes(), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -601,9 +606,9 @@ def run_backward(args, ws, rank):
         dt, ht, threads = bwd_oracle_sample(inp, w)
         cpu = {"value": ht / H / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"fp64 backward oracle on 1 of {H} heads, full T ({dt:.1f} s wall); tokens scaled by heads"}
-    # algorithmic bytes of one backward: per (token, head) q, k, v, do, beta, g
-    # in and dq, dk, dv (fp32), dbeta, dg out; per (segment, head) the S_init
-    # and M states read.  The backward's launches are timed together, so its
+    # algorithmic bytes of one backward: per (token, head) k, v, beta, g in
+    # and dk, dv (fp32), dbeta, dg out; per (token, query head) q, do in and
+    # dq (fp32) out; per (segment, head) the S_init and M states read.  The backward's launches are timed together, so its
     # line carries the whole backward's figure: on the tensor-core path (bf16,
     # d = 128, scalar gate) the WY build, the recomputed forward, the
     # state-gradient chains of the continuing fragments, the reverse merge,
@@ -612,7 +617,7 @@ def run_backward(args, ws, rank):
     es = 4 if w.dtype == "fp32" else 2
     gate_w = d if w.gate == "kda" else 1
     counts = ctx.counts()
-    tok_bytes = H * (4 * d * es + es + gate_w * 4 + 3 * d * 4 + 4 + gate_w * 4)
+    tok_bytes = H * (2 * d * es + es + gate_w * 4 + 2 * d * 4 + 4 + gate_w * 4) + Hq * (2 * d * es + d * 4)
     state_bytes = R * B * H * d * d * 4 * 2
     nbytes = tokens * tok_bytes + state_bytes
     peak, peak_kind = hbm_peak()
@@ -620,13 +625,14 @@ def run_backward(args, ws, rank):
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": None, "kernel": f"bwd(all launches):{w.name}", "peak_source": peak_kind,
             "algorithmic_bytes_per_launch": nbytes, "ms_per_launch": ms}
-    tc_bwd = counts["tc"] and w.gate == "gdn" and inp["Hq"] == H
+    tc_bwd = counts["tc"] and w.gate == "gdn" and Hq == H
     launches = ((4 if tc_bwd else 1) + (2 if counts["chains"] else 0)) * args.steps
     line = {"metric": BWD_METRIC, "value": tokens * ws / (ms / 1e3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "op": "backward", "B": B, "T": T, "H": H, "d": d, "R": R,
-                       "gate": w.gate, "in_dtype": w.dtype, "parallelism": f"replicas{ws}"},
+            "config": dict({"workload": w.name, "op": "backward", "B": B, "T": T, "H": H, "d": d, "R": R,
+                            "gate": w.gate, "in_dtype": w.dtype, "parallelism": f"replicas{ws}"},
+                           **variant_keys(w, inp)),
             "roofline": roof, "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": clk}
     print(json.dumps(line), flush=True)
 

@@ -62,6 +62,10 @@ constexpr size_t kKdaOffQg = kKdaOffKgamLo + 16384;
 constexpr size_t kKdaOffP = kKdaOffQg + 16384;
 constexpr size_t kKdaUnitBytes = kKdaOffP + kWyTileBytes;   // 113 KiB
 static_assert(kKdaUnitBytes % 1024 == 0, "KDA unit must keep 1 KiB alignment");
+// Grouped query heads (G query heads per state head): the unit holds Qg and
+// P of its state's first query head; those of query heads 1 .. G-1 follow
+// all units, laid out as in the unit, [chunk][head][G - 1] x 24 KiB.
+constexpr size_t kKdaQpBytes = kKdaUnitBytes - kKdaOffQg;
 
 // Host plan ([FLA-CP] §3.2-§3.3): fragments per segment and the derived
 // work lists.  All token indices are on the flattened [B*T] axis.

@@ -108,6 +108,7 @@ struct Params {
     const int32_t *items;
     const int32_t *chunk0;    // first global chunk of each fragment (WY tile order)
     const uint8_t *wy;        // WY tiles: [chunk][head][T', hi(T''), lo(T'')]
+    const uint8_t *kda_qp;    // per-dim gate, grouped query heads: Qg and P of query heads 1 .. G-1
     const float *g;
     const float *S_init;
     __nv_bfloat16 *o;
@@ -359,10 +360,18 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
             if (lane == 0) {
                 // the unit's operand images, and V
                 uint8_t *st = r.base + s * L.stage_bytes;
-                const uint8_t *unit = r.p->wy + ((size_t)(r.chunk0 + t) * H + r.h) * kKdaUnitBytes;
+                const size_t u = (size_t)(r.chunk0 + t) * H + r.h;
+                const uint8_t *unit = r.p->wy + u * kKdaUnitBytes;
+                // the forward's Qg and P (the last copy) belong to the query
+                // head: query heads past a state's first keep theirs after
+                // the units
+                const int gq = mode_fwd(MODE) ? r.hq - r.h * r.p->G : 0;
+                const uint8_t *qp = gq == 0 ? unit + kKdaOffQg
+                                            : r.p->kda_qp + (u * (r.p->G - 1) + (gq - 1)) * kKdaQpBytes;
                 mbar_arrive_expect_tx(fb, L.tx_bytes);
 #pragma unroll
-                for (int i = 0; i < (int)L.ncp; i++) bulk_load(st + L.cp_dst[i], unit + L.cp_src[i], L.cp_len[i], fb);
+                for (int i = 0; i < (int)L.ncp; i++)
+                    bulk_load(st + L.cp_dst[i], (mode_fwd(MODE) && i == 2) ? qp : unit + L.cp_src[i], L.cp_len[i], fb);
                 if (mode_fwd(MODE) || ROLE == ROLE_S) {
                     tma_load_3d(st + L.vc0, tv, fb, 0, r.h, tok);
                     tma_load_3d(st + L.vc1, tv, fb, 64, r.h, tok);
@@ -1307,11 +1316,9 @@ extern "C" int cpdr_debug_trace(unsigned long long *host, int n) {
 }
 #endif
 
-// bf16, d = 128; the per-dim gate's pre-gated query tiles are per state
-// head, so grouped query heads take the CUDA-core kernels there
+// bf16, d = 128 (both gates, grouped query heads and both state layouts)
 bool tc_supported(const Plan &p) {
-    if (p.in_dtype != CPDR_DTYPE_BF16 || p.dk != 128 || p.dv != 128) return false;
-    return p.gate_kind == CPDR_GATE_SCALAR || p.Hq == p.H;
+    return p.in_dtype == CPDR_DTYPE_BF16 && p.dk == 128 && p.dv == 128;
 }
 
 int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy, float *S_ext,
@@ -1386,6 +1393,7 @@ int launch_tc_fwd(const cpdr_ctx *c, const int32_t *items, int n_items, const vo
     prm.G = p.G;
     prm.vfirst = p.vfirst;
     prm.scale = p.scale;
+    if (kda) prm.kda_qp = (const uint8_t *)wy + p.wy_chunks.size() * (size_t)p.H * kKdaUnitBytes;
     // one chain per (fragment, query head): grouped query heads each run
     // their state head's chain
     if (kda)

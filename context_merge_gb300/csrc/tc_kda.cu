@@ -51,8 +51,9 @@ struct KdaParams {
     const __nv_bfloat16 *k, *q, *beta;
     const float *g;
     uint8_t *wy;
+    uint8_t *qp;         // grouped query heads: Qg and P of query heads 1 .. G-1 of every unit
     int32_t *status;
-    int H;
+    int H, G;            // state heads, query heads per state
 };
 
 // Shared memory (two CTAs per SM), from a 1 KiB-aligned base:
@@ -134,6 +135,51 @@ __device__ __forceinline__ void ld8f(const float *p, float *x) {
     *reinterpret_cast<float4 *>(x + 4) = *reinterpret_cast<const float4 *>(p + 4);
 }
 
+// Exact exponentials per term (decays beyond 2^100 around row r), on the
+// CUDA cores: A (strict lower, times beta; skipped when Ag is null) and P
+// (lower including the diagonal, bf16 image at Pimg).  Thread (bi, bj) owns
+// rows bi + 16 r and columns bj + 16 c (r, c < 4), so the column rows a warp
+// reads are consecutive; pairs with j > i lie above the diagonal.
+__device__ __noinline__ void exact_a_p(const float *GF, const __nv_bfloat16 *KB, const __nv_bfloat16 *QB,
+                                       const float *beta, float *Ag, uint8_t *Pimg) {
+    const int tid = threadIdx.x, bi = tid >> 4, bj = tid & 15;
+    float a[4][4], pp[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; r++)
+#pragma unroll
+        for (int c = 0; c < 4; c++) a[r][c] = pp[r][c] = 0.f;
+    for (int d = 0; d < D; d++) {
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const int i = bi + 16 * r;
+            const float Gi = GF[i * KP_LD + d], kv = __bfloat162float(KB[i * KQ_LD + d]);
+            const float qv = __bfloat162float(QB[i * KQ_LD + d]);
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                const int j = bj + 16 * c;
+                if (j > i) continue;
+                const float lam = exp2f(Gi - GF[j * KP_LD + d]) * __bfloat162float(KB[j * KQ_LD + d]);
+                a[r][c] = fmaf(kv, lam, a[r][c]);
+                pp[r][c] = fmaf(qv, lam, pp[r][c]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+        const int i = bi + 16 * r;
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            const int j = bj + 16 * c;
+            if (Ag) Ag[i * C + j] = j < i ? beta[i] * a[r][c] : 0.f;
+            *reinterpret_cast<__nv_bfloat16 *>(Pimg + sw128((uint32_t)i, (uint32_t)(j >> 3)) + (uint32_t)(j & 7) * 2u) =
+                __float2bfloat16_rn(j <= i ? pp[r][c] : 0.f);
+        }
+    }
+}
+
+// GQA: the state has several query heads (a pass per query head); without
+// it the single pass compiles to straight-line code.
+template <bool GQA>
 __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid_constant__ KdaParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smb = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -153,6 +199,13 @@ __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid
     const int nv = ck.nv;
     uint8_t *dst = p.wy + (size_t)unit * kKdaUnitBytes;
     auto tok = [&](int i) { return (ck.tok0 + i) * p.H + h; };
+    // row i of query head gq of this state (q has G H heads)
+    auto qtok = [&](int i, int gq) { return ((ck.tok0 + i) * p.H + h) * p.G + gq; };
+    // Qg and P of query head gq: in the unit for the first, else in the
+    // query-head region, laid out as in the unit
+    auto qp_dst = [&](int gq) {
+        return gq == 0 ? dst + kKdaOffQg : p.qp + ((size_t)unit * (p.G - 1) + (gq - 1)) * kKdaQpBytes;
+    };
 
     if (tid == 0) {
         mbar_init(bar, 1);
@@ -180,7 +233,7 @@ __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid
             const int e = tid + m * KP_THREADS, i = e >> 4, d = 8 * (e & 15);
             const int src = i < nv ? i : 0;
             cp_async16(kb + (uint32_t)(i * KQ_LD + d) * 2u, p.k + (int64_t)tok(src) * D + d, i < nv);
-            cp_async16(qb + (uint32_t)(i * KQ_LD + d) * 2u, p.q + (int64_t)tok(src) * D + d, i < nv);
+            cp_async16(qb + (uint32_t)(i * KQ_LD + d) * 2u, p.q + (int64_t)qtok(src, 0) * D + d, i < nv);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
@@ -220,165 +273,174 @@ __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid
     __syncthreads();
     const bool exact = *steep != 0;
 
-    // ---- gated tiles, and unless exact the column operand F (hi, lo).  A
-    // thread takes 8 consecutive key dims of a row (one 16-byte chunk of
-    // each image): items (row, group of 8), 4 per thread.
-    for (int item = tid; item < C * (D / 8); item += KP_THREADS) {
-        const int i = item >> 4, d0 = (item & 15) * 8;
-        float Gv[8], kv[8], qv[8], gc[8];
-        ld8f(GF + i * KP_LD + d0, Gv);
-        ld8f(GCv + d0, gc);
-        unpack8(*reinterpret_cast<const uint4 *>(KB + i * KQ_LD + d0), kv);
-        unpack8(*reinterpret_cast<const uint4 *>(QB + i * KQ_LD + d0), qv);
-        float kg[8], kgam[8], qg[8];
-#pragma unroll
-        for (int e = 0; e < 8; e++) {
-            const float gi = exp2f(Gv[e]);
-            kg[e] = kv[e] * gi;
-            kgam[e] = kv[e] * exp2f(gc[e] - Gv[e]);
-            qg[e] = qv[e] * gi;
-        }
-        const uint32_t off = img_off(i, d0);
-        store_hilo8(dst + kKdaOffKg, dst + kKdaOffKgLo, off, kg);
-        store_hilo8(dst + kKdaOffKgam, dst + kKdaOffKgamLo, off, kgam);
-        *reinterpret_cast<uint4 *>(dst + kKdaOffQg + off) = pack8f(qg);
-        if (!exact) {
-            float gr[8], kf[8];
-            ld8f(Gr + d0, gr);
-#pragma unroll
-            for (int e = 0; e < 8; e++) kf[e] = kv[e] * exp2f(gr[e] - Gv[e]);
-            store_hilo8(FH, FL, off, kf);
-        }
-    }
-
-    // ---- the row operand X into TMEM: thread = one row of X (its warp's
-    // lane quadrant: rows 0..63 the k rows of A, 64..127 the q rows of P),
-    // half of the key dims per warp of a quadrant; lanes hold two K
-    // elements per 32-bit column (lower key dim in the low half)
+    float *Ag = reinterpret_cast<float *>(dst);
     const int quad = w & 3, half = w >> 2;
     const int xr = 32 * quad + lane, xi = xr & 63;
     const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
-    if (!exact) {
-        const __nv_bfloat16 *src = xr < 64 ? KB : QB;
-#pragma unroll
-        for (int s = 0; s < 2; s++) {
-            uint32_t hw[16], lw[16];
-#pragma unroll
-            for (int gq = 0; gq < 4; gq++) {
-                const int d0 = 64 * half + 32 * s + 8 * gq;
-                float Gv[8], gr[8], xv[8];
-                ld8f(GF + xi * KP_LD + d0, Gv);
-                ld8f(Gr + d0, gr);
-                unpack8(*reinterpret_cast<const uint4 *>(src + xi * KQ_LD + d0), xv);
-#pragma unroll
-                for (int e = 0; e < 8; e++) xv[e] *= exp2f(Gv[e] - gr[e]);
-                split8(xv, hw + 4 * gq, lw + 4 * gq);
-            }
-            const uint32_t col = 32u * half + 16u * s;
-            tmem_st16(trow + col, hw);
-            tmem_st16(trow + KP_COL_XLO + col, lw);
-        }
-        tmem_st_wait();
-    }
-    fence_async_smem();   // F's stores become visible to the tensor core
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    float *Ag = reinterpret_cast<float *>(dst);
-    if (!exact) {
-        // ---- A and P (128 x 64, fp32 in TMEM) = X_hi F_hi + X_lo F_hi + X_hi F_lo
-        if (tid == 0) {
-            const uint32_t fh = smem_u32(FH), fl = smem_u32(FL);
-            constexpr uint32_t idesc = idesc_bf16(128, 64, false, false);
-#pragma unroll
-            for (int pass = 0; pass < 3; pass++) {
-                const uint32_t xcol = pass == 1 ? KP_COL_XLO : 0u;
-                const uint32_t fb = pass == 2 ? fl : fh;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; kk++) {
-                    const uint32_t koff = (uint32_t)(kk & 3) * 32u + (uint32_t)(kk >> 2) * 8192u;
-                    mma_bf16_ts(tmem + KP_COL_ACC, tmem + xcol + 8u * kk, sdesc(fb + koff, 16, 1024), idesc,
-                                (pass | kk) != 0 ? 1u : 0u);
-                }
-            }
-            mma_commit(bar);
-        }
-        int ok = 0;
-        if (lane == 0) ok = mbar_wait(bar, 0, ctl, p.status, 120) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) {
+    // one pass per query head of this state (one without grouped query
+    // heads): the first pass also builds the k tiles, F, X's k rows and A
+    const int npass = GQA ? p.G : 1;
+#pragma unroll 1
+    for (int gq = 0; gq < npass; gq++) {
+        const bool first = !GQA || gq == 0;
+        uint8_t *qd = qp_dst(gq);
+        if (!first) {
+            // the previous pass's reads of QB and of the accumulator are done
+            tc_fence_before();
+            __syncthreads();
             tc_fence_after();
-            // epilogue: warp = lane quadrant x half of the columns
-            float vv[32];
-            tmem_ld32(trow + KP_COL_ACC + 32u * half, vv);
-            tmem_ld_wait();
-            const int j0 = 32 * half;
-            if (xr < 64) {   // A row xi: strict lower part, times beta_i
-                const float bi = beta[xi];
+            const uint32_t qb = smem_u32(QB);
 #pragma unroll
-                for (int q4 = 0; q4 < 8; q4++) {
-                    float4 a4;
-                    const int j = j0 + 4 * q4;
-                    a4.x = j < xi ? bi * vv[4 * q4] : 0.f;
-                    a4.y = j + 1 < xi ? bi * vv[4 * q4 + 1] : 0.f;
-                    a4.z = j + 2 < xi ? bi * vv[4 * q4 + 2] : 0.f;
-                    a4.w = j + 3 < xi ? bi * vv[4 * q4 + 3] : 0.f;
-                    *reinterpret_cast<float4 *>(Ag + xi * C + j) = a4;
+            for (int m = 0; m < C * D / 8 / KP_THREADS; m++) {
+                const int e = tid + m * KP_THREADS, i = e >> 4, d = 8 * (e & 15);
+                const int src = i < nv ? i : 0;
+                cp_async16(qb + (uint32_t)(i * KQ_LD + d) * 2u, p.q + (int64_t)qtok(src, gq) * D + d, i < nv);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            __syncthreads();
+        }
+
+        // ---- gated tiles, and unless exact the column operand F (hi, lo).  A
+        // thread takes 8 consecutive key dims of a row (one 16-byte chunk of
+        // each image): items (row, group of 8), 4 per thread.
+        if (first) {
+            for (int item = tid; item < C * (D / 8); item += KP_THREADS) {
+                const int i = item >> 4, d0 = (item & 15) * 8;
+                float Gv[8], kv[8], qv[8], gc[8];
+                ld8f(GF + i * KP_LD + d0, Gv);
+                ld8f(GCv + d0, gc);
+                unpack8(*reinterpret_cast<const uint4 *>(KB + i * KQ_LD + d0), kv);
+                unpack8(*reinterpret_cast<const uint4 *>(QB + i * KQ_LD + d0), qv);
+                float kg[8], kgam[8], qg[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const float gi = exp2f(Gv[e]);
+                    kg[e] = kv[e] * gi;
+                    kgam[e] = kv[e] * exp2f(gc[e] - Gv[e]);
+                    qg[e] = qv[e] * gi;
                 }
-            } else {         // P row xi: lower part including the diagonal
+                const uint32_t off = img_off(i, d0);
+                store_hilo8(dst + kKdaOffKg, dst + kKdaOffKgLo, off, kg);
+                store_hilo8(dst + kKdaOffKgam, dst + kKdaOffKgamLo, off, kgam);
+                *reinterpret_cast<uint4 *>(qd + off) = pack8f(qg);
+                if (!exact) {
+                    float gr[8], kf[8];
+                    ld8f(Gr + d0, gr);
 #pragma unroll
-                for (int c8 = 0; c8 < 4; c8++) {
-                    float pv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; e++) pv[e] = j0 + 8 * c8 + e <= xi ? vv[8 * c8 + e] : 0.f;
-                    *reinterpret_cast<uint4 *>(dst + kKdaOffP + sw128((uint32_t)xi, (uint32_t)((j0 >> 3) + c8))) =
-                        pack8f(pv);
+                    for (int e = 0; e < 8; e++) kf[e] = kv[e] * exp2f(gr[e] - Gv[e]);
+                    store_hilo8(FH, FL, off, kf);
                 }
             }
-        } else if (lane == 0) {
-            // the products did not complete in time (status recorded): wait
-            // for them once more before the TMEM is released
-            Ctl local;
-            local.abort = 0;
-            mbar_wait(bar, 0, &local, p.status, 121);
-        }
-    } else {
-        // ---- exact exponentials per term (decays beyond 2^100 around row r),
-        // on the CUDA cores: thread (bi, bj) owns rows bi + 16 r and columns
-        // bj + 16 c (r, c < 4); pairs with j > i lie above the diagonal
-        const int bi = tid >> 4, bj = tid & 15;
-        float a[4][4], pp[4][4];
+        } else {   // the query head's tile alone
+            for (int item = tid; item < C * (D / 8); item += KP_THREADS) {
+                const int i = item >> 4, d0 = (item & 15) * 8;
+                float Gv[8], qv[8];
+                ld8f(GF + i * KP_LD + d0, Gv);
+                unpack8(*reinterpret_cast<const uint4 *>(QB + i * KQ_LD + d0), qv);
 #pragma unroll
-        for (int r = 0; r < 4; r++)
-#pragma unroll
-            for (int c = 0; c < 4; c++) a[r][c] = pp[r][c] = 0.f;
-        for (int d = 0; d < D; d++) {
-#pragma unroll
-            for (int r = 0; r < 4; r++) {
-                const int i = bi + 16 * r;
-                const float Gi = GF[i * KP_LD + d], kv = __bfloat162float(KB[i * KQ_LD + d]);
-                const float qv = __bfloat162float(QB[i * KQ_LD + d]);
-#pragma unroll
-                for (int c = 0; c < 4; c++) {
-                    const int j = bj + 16 * c;
-                    if (j > i) continue;
-                    const float lam = exp2f(Gi - GF[j * KP_LD + d]) * __bfloat162float(KB[j * KQ_LD + d]);
-                    a[r][c] = fmaf(kv, lam, a[r][c]);
-                    pp[r][c] = fmaf(qv, lam, pp[r][c]);
-                }
+                for (int e = 0; e < 8; e++) qv[e] *= exp2f(Gv[e]);
+                *reinterpret_cast<uint4 *>(qd + img_off(i, d0)) = pack8f(qv);
             }
         }
+
+        // ---- the row operand X into TMEM: thread = one row of X (its warp's
+        // lane quadrant: rows 0..63 the k rows of A, 64..127 the q rows of
+        // P), half of the key dims per warp of a quadrant; lanes hold two K
+        // elements per 32-bit column (lower key dim in the low half)
+        if (!exact && (first || xr >= 64)) {
+            const __nv_bfloat16 *src = xr < 64 ? KB : QB;
 #pragma unroll
-        for (int r = 0; r < 4; r++) {
-            const int i = bi + 16 * r;
+            for (int s = 0; s < 4; s++) {   // 16 key dims (8 columns) per step
+                uint32_t hw[8], lw[8];
 #pragma unroll
-            for (int c = 0; c < 4; c++) {
-                const int j = bj + 16 * c;
-                Ag[i * C + j] = j < i ? beta[i] * a[r][c] : 0.f;
-                *reinterpret_cast<__nv_bfloat16 *>(dst + kKdaOffP + sw128((uint32_t)i, (uint32_t)(j >> 3)) +
-                                                   (uint32_t)(j & 7) * 2u) = __float2bfloat16_rn(j <= i ? pp[r][c] : 0.f);
+                for (int g2 = 0; g2 < 2; g2++) {
+                    const int d0 = 64 * half + 16 * s + 8 * g2;
+                    float Gv[8], gr[8], xv[8];
+                    ld8f(GF + xi * KP_LD + d0, Gv);
+                    ld8f(Gr + d0, gr);
+                    unpack8(*reinterpret_cast<const uint4 *>(src + xi * KQ_LD + d0), xv);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) xv[e] *= exp2f(Gv[e] - gr[e]);
+                    split8(xv, hw + 4 * g2, lw + 4 * g2);
+                }
+                const uint32_t col = 32u * half + 8u * s;
+                tmem_st8(trow + col, hw);
+                tmem_st8(trow + KP_COL_XLO + col, lw);
             }
+            tmem_st_wait();
+        }
+        fence_async_smem();   // F's stores become visible to the tensor core
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        if (!exact) {
+            // ---- A and P (128 x 64, fp32 in TMEM) = X_hi F_hi + X_lo F_hi + X_hi F_lo
+            if (tid == 0) {
+                const uint32_t fh = smem_u32(FH), fl = smem_u32(FL);
+                constexpr uint32_t idesc = idesc_bf16(128, 64, false, false);
+#pragma unroll
+                for (int pass = 0; pass < 3; pass++) {
+                    const uint32_t xcol = pass == 1 ? KP_COL_XLO : 0u;
+                    const uint32_t fb = pass == 2 ? fl : fh;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++) {
+                        const uint32_t koff = (uint32_t)(kk & 3) * 32u + (uint32_t)(kk >> 2) * 8192u;
+                        mma_bf16_ts(tmem + KP_COL_ACC, tmem + xcol + 8u * kk, sdesc(fb + koff, 16, 1024), idesc,
+                                    (pass | kk) != 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar);
+            }
+            int ok = 0;
+            if (lane == 0) ok = mbar_wait(bar, (uint32_t)(gq & 1), ctl, p.status, 120) ? 1 : 0;
+            ok = __syncthreads_and(__shfl_sync(0xffffffffu, ok, 0));   // one verdict for the CTA
+            if (ok) {
+                tc_fence_after();
+                const int j0 = 32 * half;
+                if (xr < 64) {   // A row xi: strict lower part, times beta_i (first pass)
+                    if (first) {
+                        float vv[32];
+                        tmem_ld32(trow + KP_COL_ACC + 32u * half, vv);
+                        tmem_ld_wait();
+                        const float bi = beta[xi];
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; q4++) {
+                            float4 a4;
+                            const int j = j0 + 4 * q4;
+                            a4.x = j < xi ? bi * vv[4 * q4] : 0.f;
+                            a4.y = j + 1 < xi ? bi * vv[4 * q4 + 1] : 0.f;
+                            a4.z = j + 2 < xi ? bi * vv[4 * q4 + 2] : 0.f;
+                            a4.w = j + 3 < xi ? bi * vv[4 * q4 + 3] : 0.f;
+                            *reinterpret_cast<float4 *>(Ag + xi * C + j) = a4;
+                        }
+                    }
+                } else {         // P row xi: lower part including the diagonal
+                    float vv[32];
+                    tmem_ld32(trow + KP_COL_ACC + 32u * half, vv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; c8++) {
+                        float pv[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e++) pv[e] = j0 + 8 * c8 + e <= xi ? vv[8 * c8 + e] : 0.f;
+                        *reinterpret_cast<uint4 *>(qd + (kKdaOffP - kKdaOffQg) +
+                                                   sw128((uint32_t)xi, (uint32_t)((j0 >> 3) + c8))) = pack8f(pv);
+                    }
+                }
+            } else {
+                if (lane == 0) {
+                    // the products did not complete in time (status recorded):
+                    // wait for them once more before the TMEM is released
+                    Ctl local;
+                    local.abort = 0;
+                    mbar_wait(bar, (uint32_t)(gq & 1), &local, p.status, 121);
+                }
+                break;
+            }
+        } else {
+            exact_a_p(GF, KB, QB, beta, first ? Ag : nullptr, qd + (kKdaOffP - kKdaOffQg));
         }
     }
     // A and beta go into the unit's first tiles, which the solve reads and
@@ -434,12 +496,14 @@ int launch_tc_kda_prep(const cpdr_ctx *c, const void *k, const void *q, const vo
     prm.beta = (const __nv_bfloat16 *)beta;
     prm.g = g;
     prm.wy = (uint8_t *)wy;
+    prm.qp = (uint8_t *)wy + (size_t)units * kKdaUnitBytes;
     prm.status = c->dev.status;
     prm.H = pl.H;
-    cudaError_t e = cudaFuncSetAttribute(tc_kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)KP_SMEM);
+    prm.G = pl.G;
+    auto kern = pl.G > 1 ? tc_kda_prep_kernel<true> : tc_kda_prep_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)KP_SMEM);
     if (e != cudaSuccess) return (int)e;
-    tc_kda_prep_kernel<<<(unsigned)units, KP_THREADS, KP_SMEM, (cudaStream_t)stream>>>(prm);
+    kern<<<(unsigned)units, KP_THREADS, KP_SMEM, (cudaStream_t)stream>>>(prm);
     e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
     const size_t ssm = KS_WARPS * KS_SCRATCH;

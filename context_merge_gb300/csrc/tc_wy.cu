@@ -311,8 +311,9 @@ EncodeTiledFn wy_encode_fn() {
 
 size_t wy_bytes(const cpdr_ctx *c) {
     if (!c->use_tc) return 0;
-    const size_t unit = c->plan.gate_kind == CPDR_GATE_PER_DIM ? kKdaUnitBytes : kWyUnitBytes;
-    return c->plan.wy_chunks.size() * (size_t)c->plan.H * unit;
+    const size_t units = c->plan.wy_chunks.size() * (size_t)c->plan.H;
+    if (c->plan.gate_kind != CPDR_GATE_PER_DIM) return units * kWyUnitBytes;
+    return units * (kKdaUnitBytes + (size_t)(c->plan.G - 1) * kKdaQpBytes);
 }
 
 int launch_tc_wy(const cpdr_ctx *c, const void *k, const void *beta, const float *g, void *wy, void *stream) {

@@ -92,8 +92,12 @@ def test_wy_workspace_covers_every_chunk_of_every_fragment(cpdr_lib, kw):
     # per-dim gate: the WY tiles plus the pre-gated operand tiles, 113 KiB
     kda = make(**dict(kw, gate="kda"))
     assert kda.counts()["tc"] == 1 and kda.wy_bytes() == chunks * kw["H"] * 113 * 1024
-    # grouped query heads with the per-dim gate run on the CUDA cores
-    assert make(**dict(kw, gate="kda", Hq=2 * kw["H"])).wy_bytes() == 0
+    # grouped query heads with the per-dim gate: query heads past each
+    # state's first keep their Qg and P (24 KiB) after the units
+    for G in (2, 3):
+        gq = make(**dict(kw, gate="kda", Hq=G * kw["H"]))
+        assert gq.counts()["tc"] == 1
+        assert gq.wy_bytes() == chunks * kw["H"] * (113 + (G - 1) * 24) * 1024
 
 
 def test_selftest_rejects_host_only_context(cpdr_lib):
