@@ -625,8 +625,15 @@ def run_backward(args, ws, rank):
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": None, "kernel": f"bwd(all launches):{w.name}", "peak_source": peak_kind,
             "algorithmic_bytes_per_launch": nbytes, "ms_per_launch": ms}
-    tc_bwd = counts["tc"] and w.gate == "gdn" and Hq == H
-    launches = ((4 if tc_bwd else 1) + (2 if counts["chains"] else 0)) * args.steps
+    # tensor-core path: WY build, recomputed forward, one main state-gradient
+    # chain per query head of a state, input gradients; with cut sequences
+    # also a pre-process chain per query head and the reverse merge
+    G = Hq // H
+    tc_bwd = counts["tc"] and w.gate == "gdn"
+    if tc_bwd:
+        launches = (3 + G + ((G + 1) if counts["chains"] else 0)) * args.steps
+    else:
+        launches = (1 + (2 if counts["chains"] else 0)) * args.steps
     line = {"metric": BWD_METRIC, "value": tokens * ws / (ms / 1e3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",

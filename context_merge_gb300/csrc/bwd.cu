@@ -49,8 +49,6 @@ constexpr int BT = 256;     // threads per CTA
 constexpr int BVT = 32;     // value columns per CTA
 constexpr int CKB = 64;     // tokens between checkpoints
 
-__device__ __forceinline__ float ldv(const float *p, int64_t i) { return p[i]; }
-__device__ __forceinline__ float ldv(const __nv_bfloat16 *p, int64_t i) { return __bfloat162float(p[i]); }
 
 struct BwdParams {
     const cpdr_fragment *frags;
@@ -428,7 +426,7 @@ bool bwd_simt_fits(const cpdr_ctx *c) {
 
 bool bwd_uses_tc(const cpdr_ctx *c) {
     const auto &p = c->plan;
-    return c->use_tc && p.gate_kind == CPDR_GATE_SCALAR && p.Hq == p.H;
+    return c->use_tc && p.gate_kind == CPDR_GATE_SCALAR;
 }
 
 namespace {
@@ -474,15 +472,19 @@ int launch_bwd_tc(const cpdr_ctx *c, const void *q, const void *k, const void *v
     if (rc) return rc;
     rc = launch_tc_rec(c, k, v, g, wy, S_init, st_S, st_D, stream);
     if (rc) return rc;
+    // the state-gradient chains once per query head of a state (the first
+    // pass writes, the others add: the chain is linear in its q, dO terms)
     if (!p.bwd_pre_items.empty()) {
-        rc = launch_tc_bwd_chain(c, c->dev.bwd_pre_items, (int)p.bwd_pre_items.size(), 1, q, k, dout, g, wy, dht,
-                                 nullptr, dS_ext, nullptr, nullptr, stream);
+        for (int gq = 0; gq < p.G && !rc; gq++)
+            rc = launch_tc_bwd_chain(c, c->dev.bwd_pre_items, (int)p.bwd_pre_items.size(), 1, gq, q, k, dout, g, wy,
+                                     dht, nullptr, dS_ext, nullptr, nullptr, stream);
         if (rc) return rc;
     }
     rc = launch_tc_merge_rev(c, dS_ext, M, dS_end, stream);
     if (rc) return rc;
-    rc = launch_tc_bwd_chain(c, c->dev.fwd_order, (int)p.frags.size(), 0, q, k, dout, g, wy, dht, dS_end, nullptr,
-                             st_dS, st_dD, stream);
+    for (int gq = 0; gq < p.G && !rc; gq++)
+        rc = launch_tc_bwd_chain(c, c->dev.fwd_order, (int)p.frags.size(), 0, gq, q, k, dout, g, wy, dht, dS_end,
+                                 nullptr, st_dS, st_dD, stream);
     if (rc) return rc;
     return launch_bwd_grad(c, q, k, v, beta, g, dout, tmat, st_S, st_D, st_dS, st_dD, dq, dk, dv, dbeta, dg,
                            stream);

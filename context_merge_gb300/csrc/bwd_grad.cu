@@ -1,5 +1,7 @@
 // Input gradients of the chunked backward, one CTA per (chunk, head) unit,
-// all units in parallel (bf16 inputs, d = 128, scalar gate).
+// all units in parallel (bf16 inputs, d = 128, scalar gate).  With grouped
+// query heads the unit makes one pass per query head of its state for dq
+// and the q, dO parts of dk and dG (dS' and dDelta already sum over them).
 //
 // The chunk form of the article "flash-linear-attention 上下文并行CP ..."
 // ([FLA-CP] §2.2; the backward flow of §4) gives, per chunk, with the state
@@ -48,7 +50,7 @@ struct GradParams {
     const float *T;                  // per unit: the WY inverse T = (I + A)^-1, 64 x 64 (from the WY build)
     const float *S, *Dl, *dS, *dD;   // per unit: S [dk][dv], Delta [64][dv], dS' [dk][dv], dDelta [64][dv]
     float *dq, *dk, *dv, *dbeta, *dg;
-    int H;
+    int H, G;                        // state heads; query heads per state (q, dO, dq have G H heads)
     float scale;
 };
 
@@ -124,6 +126,9 @@ __device__ __forceinline__ void zero(float (&c)[N][4]) {
     for (int i = 0; i < N; i++) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
 }
 
+// GQA: several query heads per state (a pass per query head); without it
+// the single pass compiles with its branches resolved.
+template <bool GQA>
 __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__ GradParams p) {
     extern __shared__ __align__(16) uint8_t sm[];
     __nv_bfloat16 *Qb = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_QB);
@@ -147,17 +152,34 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__
     const WyChunk ck = p.chunks[unit / p.H];
     const int nv = ck.nv;
     auto tok = [&](int i) { return (ck.tok0 + i) * p.H + h; };
+    // row i of query head gq of this state
+    auto qtok = [&](int i, int gq) { return ((ck.tok0 + i) * p.H + h) * p.G + gq; };
 
-    // ---- loads (rows past the chunk's end: 0)
+    // q and dO of query head gq into Qb, Ob (rows past the chunk's end: 0)
+    auto load_qo = [&](int gq) {
+        for (int e = tid; e < C * (D / 8); e += NT) {
+            const int i = e / (D / 8), d = 8 * (e % (D / 8));
+            uint4 qv = make_uint4(0, 0, 0, 0), ov = qv;
+            if (i < nv) {
+                const int64_t o = (int64_t)qtok(i, gq) * D + d;
+                qv = *reinterpret_cast<const uint4 *>(p.q + o);
+                ov = *reinterpret_cast<const uint4 *>(p.dout + o);
+            }
+            *reinterpret_cast<uint4 *>(Qb + i * PB + d) = qv;
+            *reinterpret_cast<uint4 *>(Ob + i * PB + d) = ov;
+        }
+    };
+    // ---- loads (rows past the chunk's end: 0): q, dO of the first query
+    // head, k, v (one loop: every load independent), then Delta, dDelta
     for (int e = tid; e < C * (D / 8); e += NT) {
         const int i = e / (D / 8), d = 8 * (e % (D / 8));
         uint4 qv = make_uint4(0, 0, 0, 0), kv = qv, vv = qv, ov = qv;
         if (i < nv) {
-            const int64_t o = (int64_t)tok(i) * D + d;
-            qv = *reinterpret_cast<const uint4 *>(p.q + o);
+            const int64_t o = (int64_t)tok(i) * D + d, oq = (int64_t)qtok(i, 0) * D + d;
+            qv = *reinterpret_cast<const uint4 *>(p.q + oq);
             kv = *reinterpret_cast<const uint4 *>(p.k + o);
             vv = *reinterpret_cast<const uint4 *>(p.v + o);
-            ov = *reinterpret_cast<const uint4 *>(p.dout + o);
+            ov = *reinterpret_cast<const uint4 *>(p.dout + oq);
         }
         *reinterpret_cast<uint4 *>(Qb + i * PB + d) = qv;
         *reinterpret_cast<uint4 *>(Kb + i * PB + d) = kv;
@@ -199,7 +221,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__
         bet[i1] = i1 < nv ? bf(p.beta + tok(i1)) : 0.f;
         if (lane == 0) misc[0] = __expf(GC);
     }
-    __syncthreads();
 
     // Register tiles of 64 x 128 outputs: warp w owns rows m0 = 16 (w % 4)
     // .. + 15 and, in each 64-column half hh, columns 64 hh + 32 (w / 4) ..
@@ -216,112 +237,138 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__
             n8[4 * hh + nt] = nh[hh][nt];
         }
     float dQ[8][4], dK[8][4];
-    zero(dQ);
     zero(dK);
     float dg0 = 0.f, dg1 = 0.f;   // this thread's share of dG for rows r0, r1
     float db0 = 0.f, db1 = 0.f;   // and of dbeta
-    const Bv Ov{Ob, PB, 1}, Kv{Kb, PB, 1}, Qv{Qb, PB, 1}, Vv{Vb, PB, 1};
+    const Bv Ov{Ob, PB, 1}, Kv{Kb, PB, 1}, Qv{Qb, PB, 1};
     const Bv KvT{Kb, 1, PB};
     const float sc = p.scale;
+    float dgc_part = 0.f;   // sum (dS' ⊙ S)
+    float dgc_k = 0.f;      // sum (k ⊙ dk_Gamma)
 
-    // ---- S halves: dq_1 = gamma ⊙ (dO~ S^T), dW = -dDelta S^T, and
-    // dgC = sum (dS' ⊙ S) (read straight from global)
-    float dgc_part = 0.f;
-    for (int hh = 0; hh < 2; hh++) {
-        __syncthreads();
-        for (int e = tid; e < C * (D / 4); e += NT) {
-            const int i = e / (D / 4), d = 4 * (e % (D / 4));
-            const float4 a = *reinterpret_cast<const float4 *>(Sg + (int64_t)(64 * hh + i) * D + d);
-            *reinterpret_cast<float4 *>(R + i * PF + d) = a;
-            const float4 b = *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + d);
-            dgc_part += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+    // ---- one pass per query head of this state (one without grouped query
+    // heads): its dq, and its parts of dk and dG; the first pass also forms
+    // dW = -dDelta S^T and sum (dS' ⊙ S) from the same S halves
+    const int npass = GQA ? p.G : 1;
+#pragma unroll 1
+    for (int gq = 0; gq < npass; gq++) {
+        const bool first = !GQA || gq == 0;
+        if (!first) {
+            __syncthreads();   // the previous pass's reads of Q and dO (T1) are done
+            load_qo(gq);
         }
-        __syncthreads();
-        // columns d = 64 hh + cw + 8 nt + ...: B(v, d') = S[64 hh + d'][v] = R[d'][v]
-        const Fv RT{R, 1, PF};
-        const int nl[4] = {cw, cw + 8, cw + 16, cw + 24};
-        float acc[4][4];
-        zero(acc);
-        warp_mm<4, D>(acc, Ov, m0, RT, nl);
+        // ---- S halves: dq_1 = gamma ⊙ (dO~ S^T) (and, first pass, dW and
+        // sum (dS' ⊙ S), dS' read straight from global)
+        for (int hh = 0; hh < 2; hh++) {
+            __syncthreads();
+            for (int e = tid; e < C * (D / 4); e += NT) {
+                const int i = e / (D / 4), d = 4 * (e % (D / 4));
+                const float4 a = *reinterpret_cast<const float4 *>(Sg + (int64_t)(64 * hh + i) * D + d);
+                *reinterpret_cast<float4 *>(R + i * PF + d) = a;
+                if (first) {
+                    const float4 b = *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + d);
+                    dgc_part += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+                }
+            }
+            __syncthreads();
+            // columns d = 64 hh + cw + 8 nt + ...: B(v, d') = S[64 hh + d'][v] = R[d'][v]
+            const Fv RT{R, 1, PF};
+            const int nl[4] = {cw, cw + 8, cw + 16, cw + 24};
+            float acc[4][4];
+            zero(acc);
+            warp_mm<4, D>(acc, Ov, m0, RT, nl);
 #pragma unroll
-        for (int nt = 0; nt < 4; nt++) {
-            dQ[4 * hh + nt][0] = sc * acc[nt][0] * gam[r0];
-            dQ[4 * hh + nt][1] = sc * acc[nt][1] * gam[r0];
-            dQ[4 * hh + nt][2] = sc * acc[nt][2] * gam[r1];
-            dQ[4 * hh + nt][3] = sc * acc[nt][3] * gam[r1];
-        }
-        zero(acc);
-        warp_mm<4, D>(acc, Fv{DD, PF, 1}, m0, RT, nl);
+            for (int nt = 0; nt < 4; nt++) {
+                dQ[4 * hh + nt][0] = sc * acc[nt][0] * gam[r0];
+                dQ[4 * hh + nt][1] = sc * acc[nt][1] * gam[r0];
+                dQ[4 * hh + nt][2] = sc * acc[nt][2] * gam[r1];
+                dQ[4 * hh + nt][3] = sc * acc[nt][3] * gam[r1];
+            }
+            if (first) {
+                zero(acc);
+                warp_mm<4, D>(acc, Fv{DD, PF, 1}, m0, RT, nl);
 #pragma unroll
-        for (int nt = 0; nt < 4; nt++) {
-            const int col = 64 * hh + cw + 8 * nt + 2 * tg;
-            WB[r0 * PF + col] = -acc[nt][0];
-            WB[r0 * PF + col + 1] = -acc[nt][1];
-            WB[r1 * PF + col] = -acc[nt][2];
-            WB[r1 * PF + col + 1] = -acc[nt][3];
+                for (int nt = 0; nt < 4; nt++) {
+                    const int col = 64 * hh + cw + 8 * nt + 2 * tg;
+                    WB[r0 * PF + col] = -acc[nt][0];
+                    WB[r0 * PF + col + 1] = -acc[nt][1];
+                    WB[r1 * PF + col] = -acc[nt][2];
+                    WB[r1 * PF + col + 1] = -acc[nt][3];
+                }
+            }
         }
-    }
-    // ---- dS' halves: dk_Gamma = Gamma ⊙ (Delta dS'^T)
-    float dgc_k = 0.f;   // sum (k ⊙ dk_Gamma)
-    for (int hh = 0; hh < 2; hh++) {
+        // ---- dS' halves (first pass): dk_Gamma = Gamma ⊙ (Delta dS'^T)
+        for (int hh = 0; hh < 2 && first; hh++) {
+            __syncthreads();
+            for (int e = tid; e < C * (D / 4); e += NT) {
+                const int i = e / (D / 4), d = 4 * (e % (D / 4));
+                *reinterpret_cast<float4 *>(R + i * PF + d) =
+                    *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + d);
+            }
+            __syncthreads();
+            const Fv RT{R, 1, PF};
+            const int nl[4] = {cw, cw + 8, cw + 16, cw + 24};
+            float acc[4][4];
+            zero(acc);
+            warp_mm<4, D>(acc, Fv{DL, PF, 1}, m0, RT, nl);
+#pragma unroll
+            for (int nt = 0; nt < 4; nt++) {
+                const int col = 64 * hh + cw + 8 * nt + 2 * tg;
+                const float v0 = Gam[r0] * acc[nt][0], v1 = Gam[r0] * acc[nt][1];
+                const float v2 = Gam[r1] * acc[nt][2], v3 = Gam[r1] * acc[nt][3];
+                dK[4 * hh + nt][0] += v0; dK[4 * hh + nt][1] += v1;
+                dK[4 * hh + nt][2] += v2; dK[4 * hh + nt][3] += v3;
+                const float k0 = bf(Kb + r0 * PB + col) * v0 + bf(Kb + r0 * PB + col + 1) * v1;
+                const float k1 = bf(Kb + r1 * PB + col) * v2 + bf(Kb + r1 * PB + col + 1) * v3;
+                dg0 -= k0;
+                dg1 -= k1;
+                dgc_k += k0 + k1;
+            }
+        }
         __syncthreads();
-        for (int e = tid; e < C * (D / 4); e += NT) {
-            const int i = e / (D / 4), d = 4 * (e % (D / 4));
-            *reinterpret_cast<float4 *>(R + i * PF + d) =
-                *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + d);
+        // ---- dP = lower_incl(dO~ Delta^T), dPL = dP ⊙ Lambda  (64 x 64 into T1)
+        {
+            const int nl[4] = {cw, cw + 8, cw + 16, cw + 24};
+            float acc[4][4];
+            zero(acc);
+            warp_mm<4, D>(acc, Ov, m0, Fv{DL, 1, PF}, nl);
+            __syncthreads();   // T1 overlays dO: the other column warp reads these rows
+#pragma unroll
+            for (int nt = 0; nt < 4; nt++) {
+                const int j = cw + 8 * nt + 2 * tg;
+                auto lam = [&](int i, int jj) { return jj <= i ? __expf(Gv[i] - Gv[jj]) : 0.f; };
+                T1[r0 * PS + j] = sc * acc[nt][0] * lam(r0, j);
+                T1[r0 * PS + j + 1] = sc * acc[nt][1] * lam(r0, j + 1);
+                T1[r1 * PS + j] = sc * acc[nt][2] * lam(r1, j);
+                T1[r1 * PS + j + 1] = sc * acc[nt][3] * lam(r1, j + 1);
+            }
         }
         __syncthreads();
-        const Fv RT{R, 1, PF};
-        const int nl[4] = {cw, cw + 8, cw + 16, cw + 24};
-        float acc[4][4];
-        zero(acc);
-        warp_mm<4, D>(acc, Fv{DL, PF, 1}, m0, RT, nl);
+        // dq += dPL K;  dk_1 = dPL^T Q (through K / gamma)
+        {
+            warp_mm<8, C>(dQ, Fv{T1, PS, 1}, m0, Kv, n8);
+            float acc[8][4];
+            zero(acc);
+            warp_mm<8, C>(acc, Fv{T1, 1, PS}, m0, Qv, n8);
 #pragma unroll
-        for (int nt = 0; nt < 4; nt++) {
-            const int col = 64 * hh + cw + 8 * nt + 2 * tg;
-            const float v0 = Gam[r0] * acc[nt][0], v1 = Gam[r0] * acc[nt][1];
-            const float v2 = Gam[r1] * acc[nt][2], v3 = Gam[r1] * acc[nt][3];
-            dK[4 * hh + nt][0] += v0; dK[4 * hh + nt][1] += v1;
-            dK[4 * hh + nt][2] += v2; dK[4 * hh + nt][3] += v3;
-            const float k0 = bf(Kb + r0 * PB + col) * v0 + bf(Kb + r0 * PB + col + 1) * v1;
-            const float k1 = bf(Kb + r1 * PB + col) * v2 + bf(Kb + r1 * PB + col + 1) * v3;
-            dg0 -= k0;
-            dg1 -= k1;
-            dgc_k += k0 + k1;
-        }
-    }
-    __syncthreads();
-    // ---- dP = lower_incl(dO~ Delta^T), dPL = dP ⊙ Lambda  (64 x 64 into T1)
-    {
-        const int nl[4] = {cw, cw + 8, cw + 16, cw + 24};
-        float acc[4][4];
-        zero(acc);
-        warp_mm<4, D>(acc, Ov, m0, Fv{DL, 1, PF}, nl);
-        __syncthreads();   // T1 overlays dO: the other column warp reads these rows
+            for (int nt = 0; nt < 8; nt++) {
+                const int col = n8[nt] + 2 * tg;
 #pragma unroll
-        for (int nt = 0; nt < 4; nt++) {
-            const int j = cw + 8 * nt + 2 * tg;
-            auto lam = [&](int i, int jj) { return jj <= i ? __expf(Gv[i] - Gv[jj]) : 0.f; };
-            T1[r0 * PS + j] = sc * acc[nt][0] * lam(r0, j);
-            T1[r0 * PS + j + 1] = sc * acc[nt][1] * lam(r0, j + 1);
-            T1[r1 * PS + j] = sc * acc[nt][2] * lam(r1, j);
-            T1[r1 * PS + j + 1] = sc * acc[nt][3] * lam(r1, j + 1);
+                for (int e = 0; e < 4; e++) dK[nt][e] += acc[nt][e];
+                dg0 -= bf(Kb + r0 * PB + col) * acc[nt][0] + bf(Kb + r0 * PB + col + 1) * acc[nt][1];
+                dg1 -= bf(Kb + r1 * PB + col) * acc[nt][2] + bf(Kb + r1 * PB + col + 1) * acc[nt][3];
+            }
         }
-    }
-    __syncthreads();
-    // dq += dPL K;  dk_1 = dPL^T Q (through K / gamma)
-    {
-        warp_mm<8, C>(dQ, Fv{T1, PS, 1}, m0, Kv, n8);
-        float acc[8][4];
-        zero(acc);
-        warp_mm<8, C>(acc, Fv{T1, 1, PS}, m0, Qv, n8);
+        // ---- dq of this query head; dG_i += sum_d q dq
 #pragma unroll
         for (int nt = 0; nt < 8; nt++) {
             const int col = n8[nt] + 2 * tg;
-#pragma unroll
-            for (int e = 0; e < 4; e++) dK[nt][e] += acc[nt][e];
-            dg0 -= bf(Kb + r0 * PB + col) * acc[nt][0] + bf(Kb + r0 * PB + col + 1) * acc[nt][1];
-            dg1 -= bf(Kb + r1 * PB + col) * acc[nt][2] + bf(Kb + r1 * PB + col + 1) * acc[nt][3];
+            dg0 += bf(Qb + r0 * PB + col) * dQ[nt][0] + bf(Qb + r0 * PB + col + 1) * dQ[nt][1];
+            dg1 += bf(Qb + r1 * PB + col) * dQ[nt][2] + bf(Qb + r1 * PB + col + 1) * dQ[nt][3];
+            if (r0 < nv)
+                *reinterpret_cast<float2 *>(p.dq + (int64_t)qtok(r0, gq) * D + col) = make_float2(dQ[nt][0], dQ[nt][1]);
+            if (r1 < nv)
+                *reinterpret_cast<float2 *>(p.dq + (int64_t)qtok(r1, gq) * D + col) = make_float2(dQ[nt][2], dQ[nt][3]);
         }
     }
     __syncthreads();
@@ -483,20 +530,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__
             dg1 -= bf(Kb + r1 * PB + col) * acc[nt][2] + bf(Kb + r1 * PB + col + 1) * acc[nt][3];
         }
     }
-    // ---- outputs: dq, dk; dG_i += sum_d q dq
+    // ---- output dk
 #pragma unroll
     for (int nt = 0; nt < 8; nt++) {
         const int col = n8[nt] + 2 * tg;
-        dg0 += bf(Qb + r0 * PB + col) * dQ[nt][0] + bf(Qb + r0 * PB + col + 1) * dQ[nt][1];
-        dg1 += bf(Qb + r1 * PB + col) * dQ[nt][2] + bf(Qb + r1 * PB + col + 1) * dQ[nt][3];
-        if (r0 < nv) {
-            *reinterpret_cast<float2 *>(p.dq + (int64_t)tok(r0) * D + col) = make_float2(dQ[nt][0], dQ[nt][1]);
+        if (r0 < nv)
             *reinterpret_cast<float2 *>(p.dk + (int64_t)tok(r0) * D + col) = make_float2(dK[nt][0], dK[nt][1]);
-        }
-        if (r1 < nv) {
-            *reinterpret_cast<float2 *>(p.dq + (int64_t)tok(r1) * D + col) = make_float2(dQ[nt][2], dQ[nt][3]);
+        if (r1 < nv)
             *reinterpret_cast<float2 *>(p.dk + (int64_t)tok(r1) * D + col) = make_float2(dK[nt][2], dK[nt][3]);
-        }
     }
     // row sums over the 4 lanes of a group, then over the two column warps
 #pragma unroll
@@ -576,10 +617,12 @@ int launch_bwd_grad(const cpdr_ctx *c, const void *q, const void *k, const void 
     prm.dbeta = dbeta;
     prm.dg = dg;
     prm.H = pl.H;
+    prm.G = pl.G;
     prm.scale = pl.scale;
-    cudaError_t e = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    auto kern = pl.G > 1 ? bwd_grad_kernel<true> : bwd_grad_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return (int)e;
-    bwd_grad_kernel<<<(unsigned)units, NT, SMEM, (cudaStream_t)stream>>>(prm);
+    kern<<<(unsigned)units, NT, SMEM, (cudaStream_t)stream>>>(prm);
     return (int)cudaGetLastError();
 }
 

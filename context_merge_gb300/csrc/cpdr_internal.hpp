@@ -199,9 +199,9 @@ int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *
 // chains (pre-process of the backward, main pass).
 int launch_tc_rec(const cpdr_ctx *c, const void *k, const void *v, const float *g, const void *wy,
                   const float *S_init, float *st_S, float *st_D, void *stream);
-int launch_tc_bwd_chain(const cpdr_ctx *c, const int32_t *items, int n_items, int pre, const void *q, const void *k,
-                        const void *dout, const float *g, const void *wy, const float *dht, const float *dS_end,
-                        float *dS_ext, float *st_dS, float *st_dD, void *stream);
+int launch_tc_bwd_chain(const cpdr_ctx *c, const int32_t *items, int n_items, int pre, int gq, const void *q,
+                        const void *k, const void *dout, const float *g, const void *wy, const float *dht,
+                        const float *dS_end, float *dS_ext, float *st_dS, float *st_dD, void *stream);
 // Input gradients per (chunk, head) from the recomputed states and the
 // state-gradient chain's outputs (bwd_grad.cu).
 int launch_bwd_grad(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta,

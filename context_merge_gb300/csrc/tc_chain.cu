@@ -59,14 +59,18 @@ constexpr int NTHREADS = 512;
 // chunk start and each chunk's Delta (the forward recomputation the input
 // gradients need); MODE_BWD (bit 4) runs the state-gradient chain of the
 // chunk form in reverse chunk order with the forward's warp roles and
-// stage layout (V's slots hold dO).
+// stage layout (V's slots hold dO); MODE_BWD_ACC (bit 5) is its pass for a
+// state's query heads past the first.
 enum Mode { MODE_FWD = 0, MODE_PRE = 1, MODE_FWD_KDA = 2, MODE_PRE_KDA = 3, MODE_FWD_VAR = 4, MODE_REC = 9,
-            MODE_BWD = 16 };
+            MODE_BWD = 16, MODE_BWD_ACC = 48 };
 __host__ __device__ constexpr bool mode_fwd(int m) { return (m & 1) == 0; }
 __host__ __device__ constexpr bool mode_kda(int m) { return (m & 2) != 0; }
 __host__ __device__ constexpr bool mode_var(int m) { return (m & 4) != 0 || (m & 3) != 0; }
 __host__ __device__ constexpr bool mode_rec(int m) { return (m & 8) != 0; }
 __host__ __device__ constexpr bool mode_bwd(int m) { return (m & 16) != 0; }
+// the backward's later query-head passes (grouped query heads): no end
+// gradient, and the stored sums are added to the first pass's
+__host__ __device__ constexpr bool mode_acc(int m) { return (m & 32) != 0; }
 enum Role { ROLE_S = 0, ROLE_M = 1 };
 
 // Optional event trace (compile with -DCPDR_TRACE): CTA (0, 0) of each
@@ -126,6 +130,9 @@ struct Params {
     const float *dht;         // MODE_BWD: gradient of the final states [N][H][dk][dv] (nullable)
     const float *dS_end;      // MODE_BWD main: gradient at the end of continuing fragments [R*B][H][dk][dv]
     int bwd_pre;              // MODE_BWD: 1 = backward pre-process (dS at the fragment start into S_ext)
+    int bwd_gq;               // MODE_BWD, grouped query heads: this pass's query head of each state
+                              // (q and dO of head h G + bwd_gq); passes past the first start from
+                              // zero and add their dS' / dDelta / dS_ext into the first pass's
 };
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base).
@@ -385,14 +392,16 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
             mbar_arrive_expect_tx(fb, L.tx_bytes);
             tma_load_3d(st + L.kc0, tk, fb, 0, r.h, tok);
             tma_load_3d(st + L.kc1, tk, fb, 64, r.h, tok);
+            // the backward's q and dO (in V's slots) are the pass's query head's
+            const int hb = mode_bwd(MODE) ? r.h * r.p->G + r.p->bwd_gq : r.h;
             if (mode_fwd(MODE)) {
-                const int hq = mode_var(MODE) ? r.hq : r.h;
+                const int hq = mode_var(MODE) ? r.hq : hb;
                 tma_load_3d(st + L.qc0, tq, fb, 0, hq, tok);
                 tma_load_3d(st + L.qc1, tq, fb, 64, hq, tok);
             }
             if (mode_fwd(MODE) || ROLE == ROLE_S) {
-                tma_load_3d(st + L.vc0, tv, fb, 0, r.h, tok);
-                tma_load_3d(st + L.vc1, tv, fb, 64, r.h, tok);
+                tma_load_3d(st + L.vc0, tv, fb, 0, hb, tok);
+                tma_load_3d(st + L.vc1, tv, fb, 64, hb, tok);
             }
             const uint8_t *src = r.p->wy + ((size_t)(r.chunk0 + cc) * H + r.h) * kWyUnitBytes + L.wy_off;
             bulk_load(st + L.t1, src, 2 * (uint32_t)kWyTileBytes, fb);
@@ -793,7 +802,9 @@ __device__ __forceinline__ void run_state_bwd(const Run &r, float (&S)[64], int6
     const float *src = nullptr;
     int64_t base = 0;
     bool tr = false;   // dht in the [dv][dk] layout
-    if (r.flags & CPDR_FRAG_ENDS_SEQ) {
+    constexpr bool accum = mode_acc(MODE);   // a later query head's pass: no end gradient, sums added
+    if (accum) {
+    } else if (r.flags & CPDR_FRAG_ENDS_SEQ) {
         if (p.dht) {
             src = p.dht;
             base = ((int64_t)r.seq * H + r.h) * D * D;
@@ -814,8 +825,13 @@ __device__ __forceinline__ void run_state_bwd(const Run &r, float (&S)[64], int6
         const int64_t unit = (int64_t)(r.chunk0 + c) * H + r.h;
         if (main_pass) {   // dS' of the chunk, [dk][dv]
             float *dst = p.st_S + unit * D * D + row;
+            if constexpr (accum) {
 #pragma unroll
-            for (int i = 0; i < 64; i++) dst[(int64_t)(64 * half + i) * D] = S[i];
+                for (int i = 0; i < 64; i++) dst[(int64_t)(64 * half + i) * D] += S[i];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; i++) dst[(int64_t)(64 * half + i) * D] = S[i];
+            }
         }
         // ---- X1 = dO^T mask, X2 = dS'^T K^T
         if (issuer) {
@@ -843,8 +859,13 @@ __device__ __forceinline__ void run_state_bwd(const Run &r, float (&S)[64], int6
             }
             if (main_pass) {   // dDelta of the chunk, [64][dv]
                 float *dst = p.st_D + unit * C * D + row;
+                if constexpr (accum) {
 #pragma unroll
-                for (int jj = 0; jj < 32; jj++) dst[(int64_t)(32 * half + jj) * D] = x1[jj];
+                    for (int jj = 0; jj < 32; jj++) dst[(int64_t)(32 * half + jj) * D] += x1[jj];
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj++) dst[(int64_t)(32 * half + jj) * D] = x1[jj];
+                }
             }
             uint32_t hi[16];   // -dDelta^T, the A operand of X4
             neg_pairs<16>(x1, hi, nullptr);
@@ -892,8 +913,13 @@ __device__ __forceinline__ void run_state_bwd(const Run &r, float (&S)[64], int6
     }
     if (bad || main_pass) return;
     // the pre-process: the gradient at the fragment's start, [dk][dv]
+    if constexpr (accum) {
 #pragma unroll
-    for (int i = 0; i < 64; i++) p.S_ext[sidx + (int64_t)(64 * half + i) * D + row] = S[i];
+        for (int i = 0; i < 64; i++) p.S_ext[sidx + (int64_t)(64 * half + i) * D + row] += S[i];
+    } else {
+#pragma unroll
+        for (int i = 0; i < 64; i++) p.S_ext[sidx + (int64_t)(64 * half + i) * D + row] = S[i];
+    }
 }
 
 // State warps (8-15): Delta epilogue and S update; lane 0 of warp 8 issues the
@@ -1291,6 +1317,7 @@ static_assert(make_lay(MODE_FWD_KDA, ROLE_S).tx_bytes < (1u << 20) && make_lay(M
 static_assert(make_lay(MODE_FWD, ROLE_S).ngate <= kMaxGateSlots && make_lay(MODE_PRE, ROLE_M).ngate <= kMaxGateSlots,
               "gate slots exceed their barriers");
 static_assert(make_lay(MODE_BWD, ROLE_S).total == make_lay(MODE_FWD, ROLE_S).total, "backward uses the forward layout");
+static_assert(make_lay(MODE_BWD_ACC, ROLE_S).total == make_lay(MODE_BWD, ROLE_S).total, "the accumulating pass too");
 static_assert(make_lay(MODE_REC, ROLE_S).total == make_lay(MODE_PRE, ROLE_S).total, "recompute uses the S layout");
 
 size_t smem_for(int mode, int role) { return make_lay(mode, role).total + 1024; }
@@ -1441,15 +1468,18 @@ int launch_tc_rec(const cpdr_ctx *c, const void *k, const void *v, const float *
 
 // Backward, state-gradient chains (MODE_BWD) over `items`: pre = 1 writes the
 // gradient at each fragment's start into dS_ext; pre = 0 stores dS after each
-// chunk (st_dS, [unit][dk][dv]) and dDelta (st_dD, [unit][64][dv]).
-int launch_tc_bwd_chain(const cpdr_ctx *c, const int32_t *items, int n_items, int pre, const void *q, const void *k,
-                        const void *dout, const float *g, const void *wy, const float *dht, const float *dS_end,
-                        float *dS_ext, float *st_dS, float *st_dD, void *stream) {
+// chunk (st_dS, [unit][dk][dv]) and dDelta (st_dD, [unit][64][dv]).  With
+// grouped query heads the chain is linear in its q / dO terms, so it runs
+// once per query head of a state (gq = 0 .. G-1): the first pass starts
+// from the end gradients and writes, the others start from zero and add.
+int launch_tc_bwd_chain(const cpdr_ctx *c, const int32_t *items, int n_items, int pre, int gq, const void *q,
+                        const void *k, const void *dout, const float *g, const void *wy, const float *dht,
+                        const float *dS_end, float *dS_ext, float *st_dS, float *st_dD, void *stream) {
     const auto &p = c->plan;
     if (n_items <= 0) return 0;
     CUtensorMap tq, tk, tv;
     const int64_t tokens = (int64_t)p.B * p.T;
-    if (!make_tmap(&tq, q, tokens, p.H) || !make_tmap(&tk, k, tokens, p.H) || !make_tmap(&tv, dout, tokens, p.H))
+    if (!make_tmap(&tq, q, tokens, p.Hq) || !make_tmap(&tk, k, tokens, p.H) || !make_tmap(&tv, dout, tokens, p.Hq))
         return (int)cudaErrorInvalidValue;
     Params prm{};
     prm.frags = c->dev.frags;
@@ -1468,7 +1498,12 @@ int launch_tc_bwd_chain(const cpdr_ctx *c, const int32_t *items, int n_items, in
     prm.dht = dht;
     prm.dS_end = dS_end;
     prm.bwd_pre = pre;
+    prm.G = p.G;
+    prm.bwd_gq = gq;
     prm.vfirst = p.vfirst;
+    if (gq > 0)
+        return launch_chain<MODE_BWD_ACC, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.H,
+                                                  (cudaStream_t)stream);
     return launch_chain<MODE_BWD, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.H, (cudaStream_t)stream);
 }
 

@@ -189,7 +189,10 @@ cpdr_status cpdr_plan_counts(const cpdr_ctx *ctx, int32_t out[8]);
  * qg = q 2^g): per (chunk, head) it writes, after the three tiles above
  * (built with gamma = 1), the per-dim chunk decay 2^(G_C), the bf16 tiles
  * k 2^G (hi, lo), k 2^(G_C - G) (hi, lo), q 2^G and the masked intra-chunk
- * product (Q K^T ⊙ Lambda) -- 113 KiB per (chunk, head).
+ * product (Q K^T ⊙ Lambda) -- 113 KiB per (chunk, head).  With grouped
+ * query heads (Hq = G H) the unit holds q 2^G and the product of its state's
+ * first query head; those of query heads 1 .. G-1 (24 KiB each) follow all
+ * units, [chunk][head][G - 1].
  * In: q (device; read only for the per-dim gate, else may be NULL), k,
  * beta, gate (device).  Out: wy (device, caller-owned).
  */
@@ -282,7 +285,9 @@ cpdr_status cpdr_conv1d_fwd(const cpdr_ctx *ctx, const void *x, const float *wei
  * forward states recomputed from S_init per token.  With grouped query
  * heads (Hq = G H) each state's chain takes the G query heads that read it
  * ([FLA-CP] §5.1): its state gradient collects scale q do^T of every one of
- * them, and each gets its own dq.
+ * them, and each gets its own dq (on the tensor cores the chunk-form
+ * state-gradient chain, linear in those terms, runs once per query head and
+ * sums, and the input-gradient kernel makes a pass per query head).
  * In (device): q, k, v, beta, gate and do ([B, T, Hq, dv], the input dtype)
  * as for cpdr_fwd; dht [N, H, dk, dv] fp32 (with CPDR_FLAG_STATE_V_FIRST
  * [N, H, dv, dk]) or NULL (zero); S_init and M as cpdr_merge and
