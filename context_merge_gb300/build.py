@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcpdr.so")
 SOURCES = ["api.cpp", "plan.cpp", "simt.cu", "tc_wy.cu", "tc_chain.cu", "noalloc.cu", "selftest.cu",
-           "conv1d.cu", "tc_kda.cu", "bwd.cu", "tc_merge.cu", "bwd_grad.cu"]
+           "conv1d.cu", "tc_kda.cu", "bwd.cu", "tc_merge.cu", "bwd_grad.cu", "bwd_grad_kda.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

@@ -426,7 +426,8 @@ bool bwd_simt_fits(const cpdr_ctx *c) {
 
 bool bwd_uses_tc(const cpdr_ctx *c) {
     const auto &p = c->plan;
-    return c->use_tc && p.gate_kind == CPDR_GATE_SCALAR;
+    // the per-dim gate's query tiles belong to one query head per state
+    return c->use_tc && (p.gate_kind == CPDR_GATE_SCALAR || p.G == 1);
 }
 
 namespace {
@@ -468,7 +469,9 @@ int launch_bwd_tc(const cpdr_ctx *c, const void *q, const void *k, const void *v
     float *st_D = (float *)w;
     w += r256(dlb);
     float *st_dD = (float *)w;
-    int rc = launch_tc_wy_t(c, k, beta, g, wy, tmat, stream);
+    const bool kda = p.gate_kind == CPDR_GATE_PER_DIM;
+    int rc = kda ? launch_tc_kda_prep_t(c, k, q, beta, g, wy, tmat, stream)
+                 : launch_tc_wy_t(c, k, beta, g, wy, tmat, stream);
     if (rc) return rc;
     rc = launch_tc_rec(c, k, v, g, wy, S_init, st_S, st_D, stream);
     if (rc) return rc;
@@ -486,6 +489,9 @@ int launch_bwd_tc(const cpdr_ctx *c, const void *q, const void *k, const void *v
         rc = launch_tc_bwd_chain(c, c->dev.fwd_order, (int)p.frags.size(), 0, gq, q, k, dout, g, wy, dht, dS_end,
                                  nullptr, st_dS, st_dD, stream);
     if (rc) return rc;
+    if (kda)
+        return launch_bwd_grad_kda(c, q, k, v, beta, g, dout, tmat, st_S, st_D, st_dS, st_dD, dq, dk, dv, dbeta, dg,
+                                   stream);
     return launch_bwd_grad(c, q, k, v, beta, g, dout, tmat, st_S, st_D, st_dS, st_dD, dq, dk, dv, dbeta, dg,
                            stream);
 }

@@ -1,0 +1,603 @@
+// Input gradients of the chunked backward for the per-dim gate (KDA), one
+// CTA per (chunk, head) unit, all units in parallel (bf16 inputs, d = 128).
+//
+// The chunk form of the article "flash-linear-attention 上下文并行CP ..."
+// ([FLA-CP] §2.2; the backward flow of §4) with a gate per key dim: G[i][d]
+// is the in-chunk cumulative log gate (natural log), E = e^G, Kg = K ⊙ E,
+// Kn = K ⊙ e^-G, KgC = K ⊙ e^(G_C - G), Qg = Q ⊙ E; A = strict_lower(diag(beta)
+// Kg Kn^T), T = (I + A)^-1, W = T diag(beta) Kg, U = T diag(beta) V,
+// P = lower_incl(Qg Kn^T).  Given the chunk's starting state S, Delta, the
+// state gradient dS' after the chunk and dDelta (the last two from the
+// state-gradient chain), dO~ = scale dO, the reverse-mode derivative is
+//   dP   = lower_incl(dO~ Delta^T)
+//   dQ   = E ⊙ (dO~ S^T) + E ⊙ (dP Kn)
+//   dW   = -dDelta S^T;  TtW = T^T dW;  TtU = T^T dDelta;  dV = beta ⊙ TtU
+//   dA   = -strict_lower(TtW W^T + TtU U^T);  bdA = diag(beta) dA
+//   dK   = E ⊙ (beta ⊙ TtW + bdA Kn) + e^-G ⊙ (dP^T Qg + bdA^T Kg)
+//          + e^(G_C - G) ⊙ (Delta dS'^T)
+//   dbeta = rowsum(TtW ⊙ Kg) + rowsum(TtU ⊙ V) + rowsum(dA ⊙ (Kg Kn^T))
+//   dG   = Q ⊙ dQ + K ⊙ [E ⊙ (beta TtW + bdA Kn) - e^-G ⊙ (dP^T Qg + bdA^T Kg)
+//          - e^(G_C - G) ⊙ (Delta dS'^T)],  the last row also taking
+//          colsum(K ⊙ e^(G_C - G) ⊙ (Delta dS'^T)) + e^(G_C) rowsum(dS' ⊙ S)
+//   dg   = the reverse cumulative sum of dG down the chunk, per key dim.
+// The per-dim factors are bounded only in pairs, e^(G_i - G_j) with j <= i,
+// so the products run on operands factored around the reference row r = 31
+// as the preparation does: k e^(G_r - G) and k e^(G - G_r) (or q e^(G - G_r))
+// meet in one contraction, and the outputs take e^(G - G_r) or e^(G_r - G).
+// A unit whose decay exceeds about 2^100 either way of row r takes every such
+// contraction with exact per-term exponentials instead.  The matrix products
+// run on the tensor cores as warp-level mma.sync (tf32 operands, fp32
+// accumulation); T comes from the preparation (fp32).  Rows past the
+// chunk's end are zero and not written.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "bwd_mma.cuh"
+#include "cpdr_internal.hpp"
+
+namespace cpdr {
+namespace {
+
+using namespace bwdmm;
+
+constexpr int D = 128;
+constexpr int C = 64;
+constexpr int NT = 256;          // 8 warps
+constexpr int PB = D + 8;        // bf16 row pitch (elements)
+constexpr int PF = D + 4;        // fp32 row pitch of 64 x 128 tiles
+constexpr int PS = C + 4;        // fp32 row pitch of 64 x 64 tiles
+constexpr int kRef = 31;         // reference row of the factored exponentials
+constexpr float kSteep = 69.f;   // largest |G - G_r| (natural log, about 2^100) of the factored form
+
+struct KdaGradParams {
+    const WyChunk *chunks;
+    const __nv_bfloat16 *q, *k, *v, *beta, *dout;
+    const float *g;                  // [tokens][H][D] natural-log per-dim gates
+    const float *T;                  // per unit: T = (I + A)^-1, 64 x 64 (from the preparation)
+    const float *S, *Dl, *dS, *dD;   // per unit: S [dk][dv], Delta [64][dv], dS' [dk][dv], dDelta [64][dv]
+    float *dq, *dk, *dv, *dbeta, *dg;
+    int H;
+    float scale;
+};
+
+// shared memory (bytes)
+constexpr int OFF_KB = 0;                            // k (bf16)
+constexpr int OFF_OB = OFF_KB + C * PB * 2;          // dO (bf16); then T1 = dP, then Y
+constexpr int OFF_G = OFF_OB + C * PB * 2;           // G (fp32)
+constexpr int OFF_DL = OFF_G + C * PF * 4;           // Delta, then TtU
+constexpr int OFF_DD = OFF_DL + C * PF * 4;          // dDelta, then U
+constexpr int OFF_R = OFF_DD + C * PF * 4;           // S / dS' halves, then W, then dG
+constexpr int OFF_W = OFF_R + C * PF * 4;            // dW, then TtW
+constexpr int OFF_T2 = OFF_W + C * PF * 4;           // T, then bdA
+constexpr int OFF_VEC = OFF_T2 + C * PS * 4;         // G_r, G_C, e^G_C, dG_C (128 each), beta, dbeta (64), flag
+constexpr int SMEM = OFF_VEC + (4 * D + 2 * C + 4) * 4;
+static_assert(PS * 4 == PB * 2, "T1 rows must overlay dO rows");
+static_assert(SMEM <= 232448, "gradient kernel shared memory");
+
+// ---- operand views with per-dim factors, formed on the fly from k (or q) and G
+// k e^(G_r - G) and k e^(G - G_r): element (j, d), or (d, j) transposed
+template <bool UP, bool TR>
+struct KfacV {
+    const __nv_bfloat16 *k;
+    const float *G, *Gr;
+    __device__ __forceinline__ float at(int r, int c) const {
+        const int j = TR ? c : r, d = TR ? r : c;
+        const float x = UP ? Gr[d] - G[j * PF + d] : G[j * PF + d] - Gr[d];
+        return bf(k + j * PB + d) * __expf(x);
+    }
+};
+// q e^(G - G_r) from global memory (rows past the chunk's end: 0)
+struct QeV {
+    const __nv_bfloat16 *q;   // row 0 of the chunk
+    int64_t rs;               // row stride (elements)
+    int nv;
+    const float *G, *Gr;
+    __device__ __forceinline__ float at(int r, int c) const {
+        return r < nv ? bf(q + r * rs + c) * __expf(G[r * PF + c] - Gr[c]) : 0.f;
+    }
+};
+// beta_j k e^G
+struct KgbV {
+    const __nv_bfloat16 *k;
+    const float *G, *beta;
+    __device__ __forceinline__ float at(int r, int c) const {
+        return beta[r] * bf(k + r * PB + c) * __expf(G[r * PF + c]);
+    }
+};
+// beta_j v from global memory
+struct VbV {
+    const __nv_bfloat16 *v;
+    int64_t rs;
+    int nv;
+    const float *beta;
+    __device__ __forceinline__ float at(int r, int c) const {
+        return r < nv ? beta[r] * bf(v + r * rs + c) : 0.f;
+    }
+};
+
+__global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_constant__ KdaGradParams p) {
+    extern __shared__ __align__(16) uint8_t sm[];
+    __nv_bfloat16 *Kb = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_KB);
+    __nv_bfloat16 *Ob = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OB);
+    float *GF = reinterpret_cast<float *>(sm + OFF_G);
+    float *DL = reinterpret_cast<float *>(sm + OFF_DL);
+    float *DD = reinterpret_cast<float *>(sm + OFF_DD);
+    float *R = reinterpret_cast<float *>(sm + OFF_R);
+    float *WB = reinterpret_cast<float *>(sm + OFF_W);
+    float *T1 = reinterpret_cast<float *>(sm + OFF_OB);
+    float *T2 = reinterpret_cast<float *>(sm + OFF_T2);
+    float *Gr = reinterpret_cast<float *>(sm + OFF_VEC);
+    float *GC = Gr + D, *gCv = GC + D, *dGC = gCv + D, *bet = dGC + D, *dbet = bet + C;
+    int *flag = reinterpret_cast<int *>(dbet + C);
+
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, tg = lane & 3;
+    const int64_t unit = blockIdx.x;
+    const int h = (int)(unit % p.H);
+    const WyChunk ck = p.chunks[unit / p.H];
+    const int nv = ck.nv;
+    auto tok = [&](int i) { return (ck.tok0 + i) * p.H + h; };
+    const int64_t rowstride = (int64_t)p.H * D;   // elements between consecutive tokens of one head
+
+    // ---- loads (rows past the chunk's end: 0): k, dO, g, Delta, dDelta, T
+    for (int e = tid; e < C * (D / 8); e += NT) {
+        const int i = e / (D / 8), d = 8 * (e % (D / 8));
+        uint4 kv = make_uint4(0, 0, 0, 0), ov = kv;
+        if (i < nv) {
+            const int64_t o = (int64_t)tok(i) * D + d;
+            kv = *reinterpret_cast<const uint4 *>(p.k + o);
+            ov = *reinterpret_cast<const uint4 *>(p.dout + o);
+        }
+        *reinterpret_cast<uint4 *>(Kb + i * PB + d) = kv;
+        *reinterpret_cast<uint4 *>(Ob + i * PB + d) = ov;
+    }
+    const float *Sg = p.S + unit * D * D, *dSg = p.dS + unit * D * D;
+    const float *Dlg = p.Dl + unit * C * D, *dDg = p.dD + unit * C * D;
+    for (int e = tid; e < C * (D / 4); e += NT) {
+        const int i = e / (D / 4), d = 4 * (e % (D / 4));
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, gg = a;
+        if (i < nv) {
+            a = *reinterpret_cast<const float4 *>(Dlg + i * D + d);
+            b = *reinterpret_cast<const float4 *>(dDg + i * D + d);
+            gg = *reinterpret_cast<const float4 *>(p.g + (int64_t)tok(i) * D + d);
+        }
+        *reinterpret_cast<float4 *>(DL + i * PF + d) = a;
+        *reinterpret_cast<float4 *>(DD + i * PF + d) = b;
+        *reinterpret_cast<float4 *>(GF + i * PF + d) = gg;
+    }
+    {
+        const float *Tg = p.T + unit * C * C;
+        for (int e = tid; e < C * C / 4; e += NT) {
+            const int i = e / (C / 4), j = 4 * (e % (C / 4));
+            *reinterpret_cast<float4 *>(T2 + i * PS + j) = *reinterpret_cast<const float4 *>(Tg + i * C + j);
+        }
+    }
+    if (tid < C) {
+        bet[tid] = tid < nv ? bf(p.beta + tok(tid)) : 0.f;
+        dbet[tid] = 0.f;
+    }
+    if (tid < D) dGC[tid] = 0.f;
+    if (tid == 0) *flag = 0;
+    __syncthreads();
+
+    // ---- in-chunk cumulative log gates per key dim: two threads per column,
+    // rows [0, 32) and [32, 64); the second half then adds the first's total
+    {
+        const int d = tid & (D - 1), h2 = tid >> 7;
+        float run = 0.f;
+        for (int i = 32 * h2; i < 32 * h2 + 32; i++) {
+            run += GF[i * PF + d];
+            GF[i * PF + d] = run;
+        }
+        __syncthreads();
+        const float gr = GF[kRef * PF + d];   // the first half's total
+        int far = 0;
+        if (h2 == 1) {
+            for (int i = 32; i < 64; i++) {
+                const float x = GF[i * PF + d] + gr;
+                GF[i * PF + d] = x;
+                far |= fabsf(x - gr) > kSteep;
+            }
+            Gr[d] = gr;
+            GC[d] = GF[(C - 1) * PF + d];
+            gCv[d] = __expf(GC[d]);
+        } else {
+            for (int i = 0; i < 32; i++) far |= fabsf(GF[i * PF + d] - gr) > kSteep;
+        }
+        if (__any_sync(0xffffffffu, far) && lane == 0) atomicOr(flag, 1);
+    }
+    __syncthreads();
+    const bool steep = *flag != 0;
+
+    // Register tiles of 64 x 128 outputs: warp w owns rows m0 = 16 (w % 4)
+    // .. + 15 and, in each 64-column half hh, columns 64 hh + 32 (w / 4) ..
+    // + 31 (four 8-column tiles); thread: rows m0 + g, m0 + g + 8, columns
+    // 2 tg, 2 tg + 1 of each tile.  Element e of a tile: row (e < 2 ? r0 :
+    // r1), column base + 2 tg + (e & 1).
+    const int m0 = 16 * (w & 3), cw = 32 * (w >> 2);
+    const int r0 = m0 + g, r1 = m0 + g + 8;
+    int n8[8];
+#pragma unroll
+    for (int hh = 0; hh < 2; hh++)
+#pragma unroll
+        for (int nt = 0; nt < 4; nt++) n8[4 * hh + nt] = 64 * hh + cw + 8 * nt;
+    const int nl[4] = {cw, cw + 8, cw + 16, cw + 24};
+    auto erow = [&](int e) { return e < 2 ? r0 : r1; };
+    auto Gat = [&](int i, int d) { return GF[i * PF + d]; };
+    auto kat = [&](int i, int d) { return bf(Kb + i * PB + d); };
+    auto qat = [&](int i, int d) { return i < nv ? bf(p.q + (int64_t)tok(i) * D + d) : 0.f; };
+    float dQ[8][4], dK[8][4], dG[8][4];
+    zero(dQ);
+    zero(dK);
+    zero(dG);
+    float db0 = 0.f, db1 = 0.f;   // this thread's share of dbeta for rows r0, r1
+    const Bv Ov{Ob, PB, 1};
+    const float sc = p.scale;
+    const KfacV<true, false> Kf{Kb, GF, Gr};
+    const KfacV<false, false> Ke{Kb, GF, Gr};
+    const KfacV<true, true> KfT{Kb, GF, Gr};
+    const QeV Qe{p.q + (int64_t)tok(0) * D, rowstride, nv, GF, Gr};
+
+    // ---- S halves: dQ_1 = E ⊙ (dO~ S^T), dW = -dDelta S^T, and the last
+    // row's e^(G_C) rowsum(dS' ⊙ S) (dS' read straight from global)
+    for (int hh = 0; hh < 2; hh++) {
+        __syncthreads();
+#pragma unroll 2
+        for (int m = 0; m < 8; m++) {   // warp w takes row w + 8 m of the half, lane = 4 value columns
+            const int i = w + 8 * m, c4 = 4 * lane;
+            const float4 a = *reinterpret_cast<const float4 *>(Sg + (int64_t)(64 * hh + i) * D + c4);
+            *reinterpret_cast<float4 *>(R + i * PF + c4) = a;
+            const float4 b = *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + c4);
+            float part = a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (lane == 0) dGC[64 * hh + i] += gCv[64 * hh + i] * part;
+        }
+        __syncthreads();
+        const Fv RT{R, 1, PF};   // B(v, d') = S[64 hh + d'][v]
+        float acc[4][4];
+        zero(acc);
+        warp_mm<4, D>(acc, Ov, m0, RT, nl);
+#pragma unroll
+        for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int i = erow(e), d = 64 * hh + nl[nt] + 2 * tg + (e & 1);
+                dQ[4 * hh + nt][e] = sc * acc[nt][e] * __expf(Gat(i, d));
+            }
+        zero(acc);
+        warp_mm<4, D>(acc, Fv{DD, PF, 1}, m0, RT, nl);
+#pragma unroll
+        for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) WB[erow(e) * PF + 64 * hh + nl[nt] + 2 * tg + (e & 1)] = -acc[nt][e];
+    }
+    // ---- dS' halves: X = Delta dS'^T;  dK += e^(G_C - G) ⊙ X, dG -= K ⊙ that,
+    // the last row's colsum of K ⊙ that
+    for (int hh = 0; hh < 2; hh++) {
+        __syncthreads();
+        for (int e = tid; e < C * (D / 4); e += NT) {
+            const int i = e / (D / 4), d = 4 * (e % (D / 4));
+            *reinterpret_cast<float4 *>(R + i * PF + d) =
+                *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + d);
+        }
+        __syncthreads();
+        float acc[4][4];
+        zero(acc);
+        warp_mm<4, D>(acc, Fv{DL, PF, 1}, m0, Fv{R, 1, PF}, nl);
+#pragma unroll
+        for (int nt = 0; nt < 4; nt++) {
+            float colp[2] = {0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int i = erow(e), d = 64 * hh + nl[nt] + 2 * tg + (e & 1);
+                const float x = acc[nt][e] * __expf(GC[d] - Gat(i, d));
+                const float kx = kat(i, d) * x;
+                dK[4 * hh + nt][e] += x;
+                dG[4 * hh + nt][e] -= kx;
+                colp[e & 1] += kx;
+            }
+            // the 8 lanes g of a column hold its 16 rows of this warp
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                colp[0] += __shfl_xor_sync(0xffffffffu, colp[0], o);
+                colp[1] += __shfl_xor_sync(0xffffffffu, colp[1], o);
+            }
+            if (g == 0) {
+                atomicAdd(dGC + 64 * hh + nl[nt] + 2 * tg, colp[0]);
+                atomicAdd(dGC + 64 * hh + nl[nt] + 2 * tg + 1, colp[1]);
+            }
+        }
+    }
+    __syncthreads();
+    // ---- dP = lower_incl(dO~ Delta^T) (64 x 64 into T1, over dO's rows)
+    {
+        float acc[4][4];
+        zero(acc);
+        warp_mm<4, D>(acc, Ov, m0, Fv{DL, 1, PF}, nl);
+        __syncthreads();   // T1 overlays dO: the other column warp reads these rows
+#pragma unroll
+        for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int i = erow(e), j = nl[nt] + 2 * tg + (e & 1);
+                T1[i * PS + j] = j <= i ? sc * acc[nt][e] : 0.f;
+            }
+    }
+    __syncthreads();
+    // ---- dQ += E ⊙ (dP Kn);  dK += e^-G ⊙ (dP^T Qg), dG -= K ⊙ that
+    {
+        float acc[8][4];
+        zero(acc);
+        if (!steep) {
+            warp_mm<8, C>(acc, Fv{T1, PS, 1}, m0, Kf, n8);
+#pragma unroll
+            for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int i = erow(e), d = n8[nt] + 2 * tg + (e & 1);
+                    dQ[nt][e] += acc[nt][e] * __expf(Gat(i, d) - Gr[d]);
+                }
+            zero(acc);
+            warp_mm<8, C>(acc, Fv{T1, 1, PS}, m0, Qe, n8);
+#pragma unroll
+            for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int j = erow(e), d = n8[nt] + 2 * tg + (e & 1);
+                    acc[nt][e] *= __expf(Gr[d] - Gat(j, d));
+                }
+        } else {   // exact per-term exponentials
+#pragma unroll
+            for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int i = erow(e), d = n8[nt] + 2 * tg + (e & 1);
+                    const float Gi = Gat(i, d);
+                    float s1 = 0.f, s2 = 0.f;
+                    for (int j = 0; j <= i; j++) s1 = fmaf(T1[i * PS + j] * kat(j, d), __expf(Gi - Gat(j, d)), s1);
+                    for (int i2 = i; i2 < C; i2++)   // output row i as the key row
+                        s2 = fmaf(T1[i2 * PS + i] * qat(i2, d), __expf(Gat(i2, d) - Gi), s2);
+                    dQ[nt][e] += s1;
+                    acc[nt][e] = s2;
+                }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int j = erow(e), d = n8[nt] + 2 * tg + (e & 1);
+                dK[nt][e] += acc[nt][e];
+                dG[nt][e] -= kat(j, d) * acc[nt][e];
+            }
+    }
+    // ---- dQ is complete: dG += Q ⊙ dQ, and dq out
+#pragma unroll
+    for (int nt = 0; nt < 8; nt++) {
+        const int col = n8[nt] + 2 * tg;
+        dG[nt][0] += qat(r0, col) * dQ[nt][0];
+        dG[nt][1] += qat(r0, col + 1) * dQ[nt][1];
+        dG[nt][2] += qat(r1, col) * dQ[nt][2];
+        dG[nt][3] += qat(r1, col + 1) * dQ[nt][3];
+        if (r0 < nv) *reinterpret_cast<float2 *>(p.dq + (int64_t)tok(r0) * D + col) = make_float2(dQ[nt][0], dQ[nt][1]);
+        if (r1 < nv) *reinterpret_cast<float2 *>(p.dq + (int64_t)tok(r1) * D + col) = make_float2(dQ[nt][2], dQ[nt][3]);
+    }
+    __syncthreads();   // every warp has read dP
+    // ---- Y = Kg Kn^T (lower part; into T1)
+    {
+        float acc[4][4];
+        zero(acc);
+        if (!steep) {
+            warp_mm<4, D>(acc, Ke, m0, KfT, nl);
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int i = erow(e), j = nl[nt] + 2 * tg + (e & 1);
+                    float s = 0.f;
+                    if (j < i)
+                        for (int d = 0; d < D; d++) s = fmaf(kat(i, d) * kat(j, d), __expf(Gat(i, d) - Gat(j, d)), s);
+                    acc[nt][e] = s;
+                }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) T1[erow(e) * PS + nl[nt] + 2 * tg + (e & 1)] = acc[nt][e];
+    }
+    const Fv TT{T2, 1, PS};
+    // ---- TtW = T^T dW: dK += E ⊙ beta TtW, dG += K ⊙ that, dbeta += rowsum(TtW ⊙ Kg)
+    {
+        float acc[8][4];
+        zero(acc);
+        warp_mm<8, C>(acc, TT, m0, Fv{WB, PF, 1}, n8);
+#pragma unroll
+        for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int i = erow(e), d = n8[nt] + 2 * tg + (e & 1);
+                const float kE = kat(i, d) * __expf(Gat(i, d));
+                const float x = bet[i] * acc[nt][e] * __expf(Gat(i, d));
+                dK[nt][e] += x;
+                dG[nt][e] += kat(i, d) * x;
+                if (e < 2) db0 += acc[nt][e] * kE; else db1 += acc[nt][e] * kE;
+            }
+        __syncthreads();   // every warp has read dW
+#pragma unroll
+        for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) WB[erow(e) * PF + n8[nt] + 2 * tg + (e & 1)] = acc[nt][e];
+    }
+    // ---- TtU = T^T dDelta: dv = beta TtU, dbeta += rowsum(TtU ⊙ V)
+    {
+        float acc[8][4];
+        zero(acc);
+        warp_mm<8, C>(acc, TT, m0, Fv{DD, PF, 1}, n8);
+#pragma unroll
+        for (int nt = 0; nt < 8; nt++) {
+            const int col = n8[nt] + 2 * tg;
+            if (r0 < nv) {
+                const __nv_bfloat16 *vr = p.v + (int64_t)tok(r0) * D + col;
+                db0 += acc[nt][0] * bf(vr) + acc[nt][1] * bf(vr + 1);
+                *reinterpret_cast<float2 *>(p.dv + (int64_t)tok(r0) * D + col) =
+                    make_float2(bet[r0] * acc[nt][0], bet[r0] * acc[nt][1]);
+            }
+            if (r1 < nv) {
+                const __nv_bfloat16 *vr = p.v + (int64_t)tok(r1) * D + col;
+                db1 += acc[nt][2] * bf(vr) + acc[nt][3] * bf(vr + 1);
+                *reinterpret_cast<float2 *>(p.dv + (int64_t)tok(r1) * D + col) =
+                    make_float2(bet[r1] * acc[nt][2], bet[r1] * acc[nt][3]);
+            }
+        }
+        __syncthreads();   // every warp has read Delta (TtU replaces it) and dDelta
+#pragma unroll
+        for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) DL[erow(e) * PF + n8[nt] + 2 * tg + (e & 1)] = acc[nt][e];
+    }
+    // ---- W = T diag(beta) Kg (into R), U = T diag(beta) V (into DD)
+    {
+        float acc[8][4];
+        zero(acc);
+        warp_mm<8, C>(acc, Fv{T2, PS, 1}, m0, KgbV{Kb, GF, bet}, n8);
+#pragma unroll
+        for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) R[erow(e) * PF + n8[nt] + 2 * tg + (e & 1)] = acc[nt][e];
+        zero(acc);
+        warp_mm<8, C>(acc, Fv{T2, PS, 1}, m0, VbV{p.v + (int64_t)tok(0) * D, rowstride, nv, bet}, n8);
+#pragma unroll
+        for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) DD[erow(e) * PF + n8[nt] + 2 * tg + (e & 1)] = acc[nt][e];
+    }
+    __syncthreads();
+    // ---- dA = -strict_lower(TtW W^T + TtU U^T); dbeta += rowsum(dA ⊙ Y); bdA = beta dA (into T2)
+    {
+        float acc[4][4];
+        zero(acc);
+        warp_mm<4, D>(acc, Fv{WB, PF, 1}, m0, Fv{R, 1, PF}, nl);
+        warp_mm<4, D>(acc, Fv{DL, PF, 1}, m0, Fv{DD, 1, PF}, nl);
+        __syncthreads();   // every warp has read T (bdA replaces it)
+#pragma unroll
+        for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int i = erow(e), j = nl[nt] + 2 * tg + (e & 1);
+                const float dA = j < i ? -acc[nt][e] : 0.f;
+                if (e < 2) db0 += dA * T1[i * PS + j]; else db1 += dA * T1[i * PS + j];
+                T2[i * PS + j] = bet[i] * dA;
+            }
+    }
+    __syncthreads();
+    // ---- dK += E ⊙ (bdA Kn) (dG += K ⊙ that) and e^-G ⊙ (bdA^T Kg) (dG -= K ⊙ that)
+    {
+        float acc[8][4], acc2[8][4];
+        zero(acc);
+        zero(acc2);
+        if (!steep) {
+            warp_mm<8, C>(acc, Fv{T2, PS, 1}, m0, Kf, n8);
+            warp_mm<8, C>(acc2, Fv{T2, 1, PS}, m0, Ke, n8);
+#pragma unroll
+            for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int i = erow(e), d = n8[nt] + 2 * tg + (e & 1);
+                    acc[nt][e] *= __expf(Gat(i, d) - Gr[d]);
+                    acc2[nt][e] *= __expf(Gr[d] - Gat(i, d));
+                }
+        } else {   // exact per-term exponentials
+#pragma unroll
+            for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int i = erow(e), d = n8[nt] + 2 * tg + (e & 1);
+                    const float Gi = Gat(i, d);
+                    float s1 = 0.f, s2 = 0.f;
+                    for (int j = 0; j < i; j++) s1 = fmaf(T2[i * PS + j] * kat(j, d), __expf(Gi - Gat(j, d)), s1);
+                    for (int i2 = i + 1; i2 < C; i2++)
+                        s2 = fmaf(T2[i2 * PS + i] * kat(i2, d), __expf(Gat(i2, d) - Gi), s2);
+                    acc[nt][e] = s1;
+                    acc2[nt][e] = s2;
+                }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int i = erow(e), d = n8[nt] + 2 * tg + (e & 1);
+                dK[nt][e] += acc[nt][e] + acc2[nt][e];
+                dG[nt][e] += kat(i, d) * (acc[nt][e] - acc2[nt][e]);
+            }
+    }
+    // ---- outputs: dk; dbeta; dG into shared memory (R), the last row's
+    // terms added, then the reverse cumulative sum down each key dim
+#pragma unroll
+    for (int nt = 0; nt < 8; nt++) {
+        const int col = n8[nt] + 2 * tg;
+        if (r0 < nv) *reinterpret_cast<float2 *>(p.dk + (int64_t)tok(r0) * D + col) = make_float2(dK[nt][0], dK[nt][1]);
+        if (r1 < nv) *reinterpret_cast<float2 *>(p.dk + (int64_t)tok(r1) * D + col) = make_float2(dK[nt][2], dK[nt][3]);
+    }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+        db0 += __shfl_xor_sync(0xffffffffu, db0, o);
+        db1 += __shfl_xor_sync(0xffffffffu, db1, o);
+    }
+    if (tg == 0) {
+        atomicAdd(dbet + r0, db0);
+        atomicAdd(dbet + r1, db1);
+    }
+    __syncthreads();   // every warp has read W (R)
+#pragma unroll
+    for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) R[erow(e) * PF + n8[nt] + 2 * tg + (e & 1)] = dG[nt][e];
+    __syncthreads();
+    if (tid < C && tid < nv) p.dbeta[tok(tid)] = dbet[tid];
+    if (tid < D) {
+        const int d = tid;
+        float run = dGC[d];   // the last row's extra terms (rows past the end carry zero dG)
+        for (int i = C - 1; i >= 0; i--) {
+            run += R[i * PF + d];
+            if (i < nv) p.dg[(int64_t)tok(i) * D + d] = run;
+        }
+    }
+}
+
+}  // namespace
+
+int launch_bwd_grad_kda(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta,
+                        const float *g, const void *dout, const float *tmat, const float *st_S, const float *st_D,
+                        const float *st_dS, const float *st_dD, float *dq, float *dk, float *dv, float *dbeta,
+                        float *dg, void *stream) {
+    const auto &pl = c->plan;
+    const int64_t units = (int64_t)pl.wy_chunks.size() * pl.H;
+    if (units == 0) return 0;
+    if (units > (int64_t)0x7fffffff) return (int)cudaErrorInvalidValue;
+    KdaGradParams prm{};
+    prm.chunks = c->dev.wy_chunks;
+    prm.q = (const __nv_bfloat16 *)q;
+    prm.k = (const __nv_bfloat16 *)k;
+    prm.v = (const __nv_bfloat16 *)v;
+    prm.beta = (const __nv_bfloat16 *)beta;
+    prm.dout = (const __nv_bfloat16 *)dout;
+    prm.g = g;
+    prm.T = tmat;
+    prm.S = st_S;
+    prm.Dl = st_D;
+    prm.dS = st_dS;
+    prm.dD = st_dD;
+    prm.dq = dq;
+    prm.dk = dk;
+    prm.dv = dv;
+    prm.dbeta = dbeta;
+    prm.dg = dg;
+    prm.H = pl.H;
+    prm.scale = pl.scale;
+    cudaError_t e = cudaFuncSetAttribute(bwd_grad_kda_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return (int)e;
+    bwd_grad_kda_kernel<<<(unsigned)units, NT, SMEM, (cudaStream_t)stream>>>(prm);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace cpdr

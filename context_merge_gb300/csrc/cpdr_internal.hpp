@@ -187,6 +187,9 @@ size_t wy_bytes(const cpdr_ctx *c);
 
 int launch_tc_kda_prep(const cpdr_ctx *c, const void *k, const void *q, const void *beta, const float *g,
                        void *wy, void *stream);
+// The same, also writing T of every unit as fp32 64 x 64 into tmat (the backward).
+int launch_tc_kda_prep_t(const cpdr_ctx *c, const void *k, const void *q, const void *beta, const float *g,
+                         void *wy, float *tmat, void *stream);
 int launch_tc_wy(const cpdr_ctx *c, const void *k, const void *beta, const float *g, void *wy,
                  void *stream);
 // The same, also writing T of every unit as fp32 64 x 64 into tmat (the backward).
@@ -208,6 +211,11 @@ int launch_bwd_grad(const cpdr_ctx *c, const void *q, const void *k, const void 
                     const float *g, const void *dout, const float *tmat, const float *st_S, const float *st_D,
                     const float *st_dS, const float *st_dD, float *dq, float *dk, float *dv, float *dbeta, float *dg,
                     void *stream);
+// The same for the per-dim gate (bwd_grad_kda.cu): T from the preparation.
+int launch_bwd_grad_kda(const cpdr_ctx *c, const void *q, const void *k, const void *v, const void *beta,
+                        const float *g, const void *dout, const float *tmat, const float *st_S, const float *st_D,
+                        const float *st_dS, const float *st_dD, float *dq, float *dk, float *dv, float *dbeta,
+                        float *dg, void *stream);
 // The backward runs on the tensor cores (bf16, d = 128, scalar gate, Hq == H,
 // [dk, dv] states); its scratch bytes (bwd.cu).
 bool bwd_simt_fits(const cpdr_ctx *c);

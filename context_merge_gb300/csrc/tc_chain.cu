@@ -62,7 +62,7 @@ constexpr int NTHREADS = 512;
 // stage layout (V's slots hold dO); MODE_BWD_ACC (bit 5) is its pass for a
 // state's query heads past the first.
 enum Mode { MODE_FWD = 0, MODE_PRE = 1, MODE_FWD_KDA = 2, MODE_PRE_KDA = 3, MODE_FWD_VAR = 4, MODE_REC = 9,
-            MODE_BWD = 16, MODE_BWD_ACC = 48 };
+            MODE_REC_KDA = 11, MODE_BWD = 16, MODE_BWD_KDA = 18, MODE_BWD_ACC = 48 };
 __host__ __device__ constexpr bool mode_fwd(int m) { return (m & 1) == 0; }
 __host__ __device__ constexpr bool mode_kda(int m) { return (m & 2) != 0; }
 __host__ __device__ constexpr bool mode_var(int m) { return (m & 4) != 0 || (m & 3) != 0; }
@@ -367,7 +367,7 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
             if (lane == 0) {
                 // the unit's operand images, and V
                 uint8_t *st = r.base + s * L.stage_bytes;
-                const size_t u = (size_t)(r.chunk0 + t) * H + r.h;
+                const size_t u = (size_t)(r.chunk0 + cc) * H + r.h;
                 const uint8_t *unit = r.p->wy + u * kKdaUnitBytes;
                 // the forward's Qg and P (the last copy) belong to the query
                 // head: query heads past a state's first keep theirs after
@@ -379,9 +379,10 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
 #pragma unroll
                 for (int i = 0; i < (int)L.ncp; i++)
                     bulk_load(st + L.cp_dst[i], (mode_fwd(MODE) && i == 2) ? qp : unit + L.cp_src[i], L.cp_len[i], fb);
-                if (mode_fwd(MODE) || ROLE == ROLE_S) {
-                    tma_load_3d(st + L.vc0, tv, fb, 0, r.h, tok);
-                    tma_load_3d(st + L.vc1, tv, fb, 64, r.h, tok);
+                if (mode_fwd(MODE) || ROLE == ROLE_S) {   // V (the backward: dO)
+                    const int hv = mode_bwd(MODE) ? r.h * r.p->G + r.p->bwd_gq : r.h;
+                    tma_load_3d(st + L.vc0, tv, fb, 0, hv, tok);
+                    tma_load_3d(st + L.vc1, tv, fb, 64, hv, tok);
                 }
             }
             issued[s] = t;
@@ -489,6 +490,7 @@ struct Descs {
     uint64_t stack0, kmn0, vmn0, q0, t10, t20, wb, wblo, mask;
     uint64_t kgam0, kglo0, kgamlo0, pt0;   // per-dim gate: P_S operands (hi, lo), W's lo operand, P
     uint64_t wbk, maskmn, qmn0;            // backward: W tile K-major, mask MN-major, gamma ⊙ Q MN-major
+    uint64_t kgamk0, ptmn0;                // backward, per-dim gate: Kgam K-major, P MN-major
 };
 template <int MODE, int ROLE>
 __device__ __forceinline__ Descs make_descs(const Run &r) {
@@ -512,8 +514,10 @@ __device__ __forceinline__ Descs make_descs(const Run &r) {
         d.kglo0 = mndesc(b0 + L.kglo, L.k_lbo);
         d.kgamlo0 = mndesc(b0 + L.kgamlo, L.k_lbo);
         d.pt0 = kdesc(b0 + L.pt);
+        d.kgamk0 = kdesc(b0 + L.kgam);
+        d.ptmn0 = mndesc(b0 + L.pt, 8192);
     } else {
-        d.kgam0 = d.kglo0 = d.kgamlo0 = d.pt0 = 0;
+        d.kgam0 = d.kglo0 = d.kgamlo0 = d.pt0 = d.kgamk0 = d.ptmn0 = 0;
     }
     return d;
 }
@@ -596,6 +600,28 @@ __device__ __forceinline__ void run_mask(const Run &r) {
         for (int ch = 0; ch < r.n; ch++) {
             if (ch >= 1 && !warp_wait(r, B_MFREE, (ch - 1) & 1, 53)) return;
             if (!warp_wait(r, B_FULL0 + ch % NS, (ch / NS) & 1, 54)) return;
+            if (mode_bwd(MODE)) {
+                // backward: the output scale into q 2^G and P (both multiply
+                // dO), rows past the chunk's end zero (dO there belongs to the
+                // next fragment)
+                const int i = 32 * (w - 2) + lane;
+                const float rs = i < rows_of(r, r.cof(ch, true)) ? r.p->scale : 0.f;
+                const __nv_bfloat162 g2 = __float2bfloat162_rn(rs);
+                uint8_t *stb = r.base + (ch % NS) * L.stage_bytes;
+#pragma unroll
+                for (int a = 0; a < 3; a++) {
+                    uint8_t *tile = stb + (a == 0 ? L.qc0 : a == 1 ? L.qc1 : L.pt);
+#pragma unroll
+                    for (int c = 0; c < 8; c++) {
+                        uint4 u = *reinterpret_cast<uint4 *>(tile + sw128(i, c));
+                        __nv_bfloat162 *hh = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+                        for (int e = 0; e < 4; e++) hh[e] = __hmul2(hh[e], g2);
+                        *reinterpret_cast<uint4 *>(tile + sw128(i, c)) = u;
+                    }
+                }
+                fence_async_smem();
+            }
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&r.bar[B_QREADY0 + (ch & 1)]);
@@ -784,6 +810,7 @@ __device__ __forceinline__ void run_state_bwd(const Run &r, float (&S)[64], int6
     Ctl *ctl = r.ctl;
     const Descs d = make_descs<MODE, ROLE>(r);
     constexpr uint32_t KATOM = L.kc1 - L.kc0;
+    constexpr bool KDA = mode_kda(MODE);   // per-dim gate: Gamma lives in Kgam, gamma in q 2^G, the mask is P
     const bool main_pass = p.bwd_pre == 0;
     // dS^T[row][64 half .. 64 half + 63] as the bf16 A operand of X2
     auto put_grad = [&]() {
@@ -833,18 +860,24 @@ __device__ __forceinline__ void run_state_bwd(const Run &r, float (&S)[64], int6
                 for (int i = 0; i < 64; i++) dst[(int64_t)(64 * half + i) * D] = S[i];
             }
         }
-        // ---- X1 = dO^T mask, X2 = dS'^T K^T
+        // ---- X1 = dO^T mask, X2 = dS'^T K^T  (per-dim gate: dO^T P, dS'^T Kgam^T)
         if (issuer) {
             if (mbar_wait(&r.bar[B_MREADY], t & 1, ctl, st, 70)) {
                 tc_fence_after();
-                mma_mnmn<64, 64>(tm + TM_DL, stg<MODE, ROLE>(d.vmn0, t), d.maskmn, false);
+                mma_mnmn<64, 64>(tm + TM_DL, stg<MODE, ROLE>(d.vmn0, t),
+                                 KDA ? stg<MODE, ROLE>(d.ptmn0, t) : d.maskmn, false);
                 mma_commit(&r.bar[B_MFREE]);
-                mma_tk<64, 128>(tm + TM_O, tm + TM_SB, stg<MODE, ROLE>(d.stack0, t), KATOM, false);
+                mma_tk<64, 128>(tm + TM_O, tm + TM_SB, stg<MODE, ROLE>(KDA ? d.kgamk0 : d.stack0, t), KATOM, false);
                 mma_commit(&r.bar[B_DLFULL]);
             }
         }
-        bool ok = warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(t), gate_parity<MODE, ROLE>(t), 71);
+        bool ok = KDA || warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(t), gate_parity<MODE, ROLE>(t), 71);
         const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(t));
+        if (KDA && w == 8) {
+            // the chunk's per-dim decay, kept past the stage's release
+            const float4 g4 = reinterpret_cast<const float4 *>(r.base + (t % NS) * L.stage_bytes + L.gcv)[lane];
+            reinterpret_cast<float4 *>(r.base + L.gcs)[lane] = g4;
+        }
         if (ok) ok = warp_wait(r, B_DLFULL, t & 1, 72);
         if (ok) {
             tc_fence_after();
@@ -855,7 +888,7 @@ __device__ __forceinline__ void run_state_bwd(const Run &r, float (&S)[64], int6
 #pragma unroll
             for (int jj = 0; jj < 32; jj++) {
                 const int j = 32 * half + jj;
-                x1[jj] = (j < nv) ? fmaf(gs.Gam[j], x2[jj], x1[jj]) : 0.f;
+                x1[jj] = (j < nv) ? fmaf(KDA ? 1.f : gs.Gam[j], x2[jj], x1[jj]) : 0.f;
             }
             if (main_pass) {   // dDelta of the chunk, [64][dv]
                 float *dst = p.st_D + unit * C * D + row;
@@ -888,18 +921,20 @@ __device__ __forceinline__ void run_state_bwd(const Run &r, float (&S)[64], int6
                 mma_commit(&r.bar[B_EMPTY0 + t % NS]);
             }
         }
-        // ---- dS <- gamma^C dS' + X3 + X4
+        // ---- dS <- gamma^C dS' + X3 + X4  (per-dim gate: Diag(gamma^C), per key dim)
         ok = warp_wait(r, B_PSFULL, t & 1, 75);
         if (ok) {
             tc_fence_after();
-            const float gC = gs.gC[0];
+            const float gC = KDA ? 0.f : gs.gC[0];
+            const float *gcd = reinterpret_cast<const float *>(r.base + L.gcs) + 64 * half;
 #pragma unroll
             for (int piece = 0; piece < 2; piece++) {
                 float v[32];
                 tmem_ld32(lane_base + TM_PS + 64 * half + 32 * piece, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; i++) S[32 * piece + i] = fmaf(gC, S[32 * piece + i], v[i]);
+                for (int i = 0; i < 32; i++)
+                    S[32 * piece + i] = fmaf(KDA ? gcd[32 * piece + i] : gC, S[32 * piece + i], v[i]);
             }
             put_grad();
         }
@@ -1319,6 +1354,10 @@ static_assert(make_lay(MODE_FWD, ROLE_S).ngate <= kMaxGateSlots && make_lay(MODE
 static_assert(make_lay(MODE_BWD, ROLE_S).total == make_lay(MODE_FWD, ROLE_S).total, "backward uses the forward layout");
 static_assert(make_lay(MODE_BWD_ACC, ROLE_S).total == make_lay(MODE_BWD, ROLE_S).total, "the accumulating pass too");
 static_assert(make_lay(MODE_REC, ROLE_S).total == make_lay(MODE_PRE, ROLE_S).total, "recompute uses the S layout");
+static_assert(make_lay(MODE_REC_KDA, ROLE_S).total == make_lay(MODE_PRE_KDA, ROLE_S).total,
+              "per-dim recompute uses the per-dim S layout");
+static_assert(make_lay(MODE_BWD_KDA, ROLE_S).total == make_lay(MODE_FWD_KDA, ROLE_S).total,
+              "per-dim backward uses the per-dim forward layout");
 
 size_t smem_for(int mode, int role) { return make_lay(mode, role).total + 1024; }
 
@@ -1462,6 +1501,9 @@ int launch_tc_rec(const cpdr_ctx *c, const void *k, const void *v, const float *
     prm.vfirst = p.vfirst;
     prm.st_S = st_S;
     prm.st_D = st_D;
+    if (p.gate_kind == CPDR_GATE_PER_DIM)   // K comes pre-gated in the units
+        return launch_chain<MODE_REC_KDA, ROLE_S>(tk, tk, tv, prm, (unsigned)p.frags.size(), (unsigned)p.H,
+                                                  (cudaStream_t)stream);
     return launch_chain<MODE_REC, ROLE_S>(tk, tk, tv, prm, (unsigned)p.frags.size(), (unsigned)p.H,
                                           (cudaStream_t)stream);
 }
@@ -1501,6 +1543,11 @@ int launch_tc_bwd_chain(const cpdr_ctx *c, const int32_t *items, int n_items, in
     prm.G = p.G;
     prm.bwd_gq = gq;
     prm.vfirst = p.vfirst;
+    if (p.gate_kind == CPDR_GATE_PER_DIM) {   // Q, K, P come pre-gated in the units (one query head per state)
+        if (gq > 0) return (int)cudaErrorInvalidValue;
+        return launch_chain<MODE_BWD_KDA, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.H,
+                                                  (cudaStream_t)stream);
+    }
     if (gq > 0)
         return launch_chain<MODE_BWD_ACC, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.H,
                                                   (cudaStream_t)stream);

@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid
 // solver overwrites the unit's first three tiles with T', hi(T''), lo(T'').
 constexpr int KS_WARPS = 4;
 constexpr size_t KS_SCRATCH = (size_t)C * kLS * 4 + 2 * C * 4;   // A, beta, ones
-__global__ void __launch_bounds__(32 * KS_WARPS) tc_kda_solve_kernel(uint8_t *wy, int n_units) {
+__global__ void __launch_bounds__(32 * KS_WARPS) tc_kda_solve_kernel(uint8_t *wy, int n_units, float *tmat) {
     extern __shared__ __align__(16) uint8_t sms[];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float *S = reinterpret_cast<float *>(sms + w * KS_SCRATCH);
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(32 * KS_WARPS) tc_kda_solve_kernel(uint8_t *wy
         beta[lane] = bg[lane];
         beta[32 + lane] = bg[32 + lane];
         __syncwarp();
-        solve_unit(S, dst, beta, one);
+        solve_unit(S, dst, beta, one, tmat ? tmat + (size_t)unit * C * C : nullptr);
         __syncwarp();
     }
 }
@@ -485,6 +485,11 @@ __global__ void __launch_bounds__(32 * KS_WARPS) tc_kda_solve_kernel(uint8_t *wy
 
 int launch_tc_kda_prep(const cpdr_ctx *c, const void *k, const void *q, const void *beta, const float *g,
                        void *wy, void *stream) {
+    return launch_tc_kda_prep_t(c, k, q, beta, g, wy, nullptr, stream);
+}
+
+int launch_tc_kda_prep_t(const cpdr_ctx *c, const void *k, const void *q, const void *beta, const float *g,
+                         void *wy, float *tmat, void *stream) {
     const auto &pl = c->plan;
     const int64_t units = (int64_t)pl.wy_chunks.size() * pl.H;
     if (units == 0) return 0;
@@ -515,7 +520,7 @@ int launch_tc_kda_prep(const cpdr_ctx *c, const void *k, const void *q, const vo
     if (sms <= 0) sms = 148;
     const int64_t blocks = (units + KS_WARPS - 1) / KS_WARPS;
     const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * 3);
-    tc_kda_solve_kernel<<<grid, 32 * KS_WARPS, ssm, (cudaStream_t)stream>>>((uint8_t *)wy, (int)units);
+    tc_kda_solve_kernel<<<grid, 32 * KS_WARPS, ssm, (cudaStream_t)stream>>>((uint8_t *)wy, (int)units, tmat);
     return (int)cudaGetLastError();
 }
 

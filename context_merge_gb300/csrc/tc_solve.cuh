@@ -64,7 +64,8 @@ __device__ __forceinline__ void store_tiles(const float *S, uint8_t *dst, const 
 // T_{i, 32+l} = 0 for i < 32).  Then writes T' = T diag(beta) and
 // T'' = T diag(beta gamma) (hi, lo) as bf16 into the unit's three tiles,
 // reusing S (which it overwrites) to turn columns into rows.
-__device__ __forceinline__ void solve_unit(float *S, uint8_t *dst, const float *beta, const float *gam) {
+__device__ __forceinline__ void solve_unit(float *S, uint8_t *dst, const float *beta, const float *gam,
+                                           float *tdst = nullptr) {
     const int l = threadIdx.x & 31;
     float x1[64], x2[32];
 #pragma unroll
@@ -96,6 +97,13 @@ __device__ __forceinline__ void solve_unit(float *S, uint8_t *dst, const float *
         if (i >= 32) S[i * kLS + 32 + l] = x2[i - 32];
     }
     __syncwarp();
+    if (tdst) {   // T as fp32 64 x 64 (A's upper part, zero, above the diagonal blocks)
+#pragma unroll 4
+        for (int i = 0; i < 64; i++) {
+            tdst[i * 64 + l] = S[i * kLS + l];
+            tdst[i * 64 + 32 + l] = S[i * kLS + 32 + l];
+        }
+    }
     store_tiles(S, dst, beta, gam, 0, 16);
     __syncwarp();   // the scratch has been read before the caller reuses it
 }

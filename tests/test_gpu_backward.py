@@ -115,6 +115,21 @@ def test_backward_long_chains(name, kw):
     print(name, run_case(w, **kw))
 
 
+@pytest.mark.parametrize("case", [
+    dict(T=4096, H=2, R=8, gate_dist=None),                       # the per-dim workload's gates, 8-chunk fragments
+    dict(T=2048, H=2, R=4, gate_dist=("sigmoid", -3.0, 0.5)),     # steep per-dim decay: the exact branch
+    dict(T=2048, H=2, R=4, gate_dist=("sigmoid", 1.0, 2.5)),      # a wide spread of per-dim decays
+], ids=["kda-gates", "kda-steep", "kda-spread"])
+def test_backward_per_dim_gate(case):
+    """Per-dim gate on the tensor cores (bf16, d = 128): the preparation's T,
+    the recomputed forward and the state-gradient chain on the unit's
+    pre-gated tiles, the input gradients with the per-dim factors folded into
+    the operands (exact per-term exponentials for steep units)."""
+    base = inputs.WORKLOADS["kda_bf16_t32768_h32_d128_r16"]
+    w = dataclasses.replace(base, R=case["R"], gate_dist=case["gate_dist"] or base.gate_dist)
+    print(case, run_case(w, T=case["T"], H=case["H"], lengths=[case["T"] // 3, case["T"] - case["T"] // 3]))
+
+
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp32", 64)])
 def test_backward_state_v_first(dtype, d):
     """[dv, dk] states ([FLA-CP] §5.1 runs its gradient tests with state_v_first)."""
