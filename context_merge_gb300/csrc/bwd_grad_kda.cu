@@ -64,9 +64,9 @@ struct KdaGradParams {
 constexpr int OFF_KB = 0;                            // k (bf16)
 constexpr int OFF_OB = OFF_KB + C * PB * 2;          // dO (bf16); then T1 = dP, then Y
 constexpr int OFF_G = OFF_OB + C * PB * 2;           // G (fp32)
-constexpr int OFF_DL = OFF_G + C * PF * 4;           // Delta, then TtU
+constexpr int OFF_DL = OFF_G + C * PF * 4;           // Delta; q e^(G - G_r), k e^(G - G_r); TtU; k e^(G - G_r)
 constexpr int OFF_DD = OFF_DL + C * PF * 4;          // dDelta, then U
-constexpr int OFF_R = OFF_DD + C * PF * 4;           // S / dS' halves, then W, then dG
+constexpr int OFF_R = OFF_DD + C * PF * 4;           // S / dS' halves; k e^(G_r - G); W; k e^(G_r - G); dG
 constexpr int OFF_W = OFF_R + C * PF * 4;            // dW, then TtW
 constexpr int OFF_T2 = OFF_W + C * PF * 4;           // T, then bdA
 constexpr int OFF_VEC = OFF_T2 + C * PS * 4;         // G_r, G_C, e^G_C, dG_C (128 each), beta, dbeta (64), flag
@@ -74,28 +74,7 @@ constexpr int SMEM = OFF_VEC + (4 * D + 2 * C + 4) * 4;
 static_assert(PS * 4 == PB * 2, "T1 rows must overlay dO rows");
 static_assert(SMEM <= 232448, "gradient kernel shared memory");
 
-// ---- operand views with per-dim factors, formed on the fly from k (or q) and G
-// k e^(G_r - G) and k e^(G - G_r): element (j, d), or (d, j) transposed
-template <bool UP, bool TR>
-struct KfacV {
-    const __nv_bfloat16 *k;
-    const float *G, *Gr;
-    __device__ __forceinline__ float at(int r, int c) const {
-        const int j = TR ? c : r, d = TR ? r : c;
-        const float x = UP ? Gr[d] - G[j * PF + d] : G[j * PF + d] - Gr[d];
-        return bf(k + j * PB + d) * __expf(x);
-    }
-};
-// q e^(G - G_r) from global memory (rows past the chunk's end: 0)
-struct QeV {
-    const __nv_bfloat16 *q;   // row 0 of the chunk
-    int64_t rs;               // row stride (elements)
-    int nv;
-    const float *G, *Gr;
-    __device__ __forceinline__ float at(int r, int c) const {
-        return r < nv ? bf(q + r * rs + c) * __expf(G[r * PF + c] - Gr[c]) : 0.f;
-    }
-};
+// ---- operand views with per-dim factors, formed on the fly
 // beta_j k e^G
 struct KgbV {
     const __nv_bfloat16 *k;
@@ -225,6 +204,20 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
     auto Gat = [&](int i, int d) { return GF[i * PF + d]; };
     auto kat = [&](int i, int d) { return bf(Kb + i * PB + d); };
     auto qat = [&](int i, int d) { return i < nv ? bf(p.q + (int64_t)tok(i) * D + d) : 0.f; };
+    // a factored operand into an fp32 tile: k (or q) ⊙ e^(+-(G - G_r))
+    auto stage = [&](float *dst, bool from_q, bool up) {
+        for (int e = tid; e < C * (D / 4); e += NT) {
+            const int i = e / (D / 4), d = 4 * (e % (D / 4));
+            float4 x;
+            float *xv = reinterpret_cast<float *>(&x);
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const float gd = Gat(i, d + u) - Gr[d + u];
+                xv[u] = (from_q ? qat(i, d + u) : kat(i, d + u)) * __expf(up ? -gd : gd);
+            }
+            *reinterpret_cast<float4 *>(dst + i * PF + d) = x;
+        }
+    };
     float dQ[8][4], dK[8][4], dG[8][4];
     zero(dQ);
     zero(dK);
@@ -232,10 +225,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
     float db0 = 0.f, db1 = 0.f;   // this thread's share of dbeta for rows r0, r1
     const Bv Ov{Ob, PB, 1};
     const float sc = p.scale;
-    const KfacV<true, false> Kf{Kb, GF, Gr};
-    const KfacV<false, false> Ke{Kb, GF, Gr};
-    const KfacV<true, true> KfT{Kb, GF, Gr};
-    const QeV Qe{p.q + (int64_t)tok(0) * D, rowstride, nv, GF, Gr};
 
     // ---- S halves: dQ_1 = E ⊙ (dO~ S^T), dW = -dDelta S^T, and the last
     // row's e^(G_C) rowsum(dS' ⊙ S) (dS' read straight from global)
@@ -323,13 +312,17 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
                 T1[i * PS + j] = j <= i ? sc * acc[nt][e] : 0.f;
             }
     }
+    if (!steep) {   // Delta and the dS' half are dead: the factored operands of the next products
+        stage(R, false, true);
+        stage(DL, true, false);
+    }
     __syncthreads();
     // ---- dQ += E ⊙ (dP Kn);  dK += e^-G ⊙ (dP^T Qg), dG -= K ⊙ that
     {
         float acc[8][4];
         zero(acc);
         if (!steep) {
-            warp_mm<8, C>(acc, Fv{T1, PS, 1}, m0, Kf, n8);
+            warp_mm<8, C>(acc, Fv{T1, PS, 1}, m0, Fv{R, PF, 1}, n8);
 #pragma unroll
             for (int nt = 0; nt < 8; nt++)
 #pragma unroll
@@ -338,7 +331,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
                     dQ[nt][e] += acc[nt][e] * __expf(Gat(i, d) - Gr[d]);
                 }
             zero(acc);
-            warp_mm<8, C>(acc, Fv{T1, 1, PS}, m0, Qe, n8);
+            warp_mm<8, C>(acc, Fv{T1, 1, PS}, m0, Fv{DL, PF, 1}, n8);
 #pragma unroll
             for (int nt = 0; nt < 8; nt++)
 #pragma unroll
@@ -381,13 +374,17 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
         if (r0 < nv) *reinterpret_cast<float2 *>(p.dq + (int64_t)tok(r0) * D + col) = make_float2(dQ[nt][0], dQ[nt][1]);
         if (r1 < nv) *reinterpret_cast<float2 *>(p.dq + (int64_t)tok(r1) * D + col) = make_float2(dQ[nt][2], dQ[nt][3]);
     }
-    __syncthreads();   // every warp has read dP
+    __syncthreads();   // every warp has read dP and q e^(G - G_r)
+    if (!steep) {
+        stage(DL, false, false);
+        __syncthreads();
+    }
     // ---- Y = Kg Kn^T (lower part; into T1)
     {
         float acc[4][4];
         zero(acc);
         if (!steep) {
-            warp_mm<4, D>(acc, Ke, m0, KfT, nl);
+            warp_mm<4, D>(acc, Fv{DL, PF, 1}, m0, Fv{R, 1, PF}, nl);
         } else {
 #pragma unroll
             for (int nt = 0; nt < 4; nt++)
@@ -490,14 +487,19 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
             }
     }
     __syncthreads();
+    if (!steep) {   // W and TtU are dead: the factored k operands again
+        stage(R, false, true);
+        stage(DL, false, false);
+        __syncthreads();
+    }
     // ---- dK += E ⊙ (bdA Kn) (dG += K ⊙ that) and e^-G ⊙ (bdA^T Kg) (dG -= K ⊙ that)
     {
         float acc[8][4], acc2[8][4];
         zero(acc);
         zero(acc2);
         if (!steep) {
-            warp_mm<8, C>(acc, Fv{T2, PS, 1}, m0, Kf, n8);
-            warp_mm<8, C>(acc2, Fv{T2, 1, PS}, m0, Ke, n8);
+            warp_mm<8, C>(acc, Fv{T2, PS, 1}, m0, Fv{R, PF, 1}, n8);
+            warp_mm<8, C>(acc2, Fv{T2, 1, PS}, m0, Fv{DL, PF, 1}, n8);
 #pragma unroll
             for (int nt = 0; nt < 8; nt++)
 #pragma unroll
@@ -547,7 +549,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
         atomicAdd(dbet + r0, db0);
         atomicAdd(dbet + r1, db1);
     }
-    __syncthreads();   // every warp has read W (R)
+    __syncthreads();   // every warp has read R
 #pragma unroll
     for (int nt = 0; nt < 8; nt++)
 #pragma unroll
