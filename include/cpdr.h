@@ -274,12 +274,14 @@ cpdr_status cpdr_conv1d_fwd(const cpdr_ctx *ctx, const void *x, const float *wei
  *      end of every continuing fragment);
  *   3. every fragment runs the reverse chain from that end gradient (or dht,
  *      or 0) and writes the input gradients.
- * For bf16 inputs, dk = dv = 128 and the scalar gate the chains run in chunk
- * form on the tensor cores: the forward is recomputed with every chunk's
- * starting state and Delta kept, the state-gradient chain runs chunk by
- * chunk in reverse (tcgen05), the reverse merge on the tensor cores, and a
- * parallel kernel forms the input gradients of every (chunk, head); the
- * workspace then holds the WY tiles, the fp32 inverse T and four fp32
+ * For bf16 inputs and dk = dv = 128 (the scalar gate, or the per-dim gate
+ * with one query head per state) the chains run in chunk form on the tensor
+ * cores: the forward is recomputed with every chunk's starting state and
+ * Delta kept, the state-gradient chain runs chunk by chunk in reverse
+ * (tcgen05), the reverse merge on the tensor cores, and a parallel kernel
+ * forms the input gradients of every (chunk, head) (for the per-dim gate
+ * with its factors folded into the operands); the workspace then holds the
+ * WY tiles (the per-dim gate's units), the fp32 inverse T and four fp32
  * tensors per (chunk, head) (about 216 KiB each).  Otherwise the reverse
  * chain is the per-token chain rule, on CUDA cores in fp32, with the
  * forward states recomputed from S_init per token.  With grouped query
