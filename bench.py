@@ -629,7 +629,7 @@ def run_backward(args, ws, rank):
     # chain per query head of a state, input gradients; with cut sequences
     # also a pre-process chain per query head and the reverse merge
     G = Hq // H
-    tc_bwd = counts["tc"] and (w.gate == "gdn" or G == 1)
+    tc_bwd = bool(counts["tc"])
     if tc_bwd:   # the per-dim gate's preparation is two launches (preparation, solve)
         launches = (3 + G + ((G + 1) if counts["chains"] else 0) + (1 if w.gate == "kda" else 0)) * args.steps
     else:

@@ -424,11 +424,8 @@ bool bwd_simt_fits(const cpdr_ctx *c) {
     return need <= 232448;
 }
 
-bool bwd_uses_tc(const cpdr_ctx *c) {
-    const auto &p = c->plan;
-    // the per-dim gate's query tiles belong to one query head per state
-    return c->use_tc && (p.gate_kind == CPDR_GATE_SCALAR || p.G == 1);
-}
+// bf16, d = 128: both gates, grouped query heads and both state layouts
+bool bwd_uses_tc(const cpdr_ctx *c) { return c->use_tc; }
 
 namespace {
 size_t r256(size_t x) { return (x + 255) & ~size_t(255); }

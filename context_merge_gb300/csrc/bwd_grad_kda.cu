@@ -56,7 +56,7 @@ struct KdaGradParams {
     const float *T;                  // per unit: T = (I + A)^-1, 64 x 64 (from the preparation)
     const float *S, *Dl, *dS, *dD;   // per unit: S [dk][dv], Delta [64][dv], dS' [dk][dv], dDelta [64][dv]
     float *dq, *dk, *dv, *dbeta, *dg;
-    int H;
+    int H, G;                        // state heads; query heads per state (q, dO, dq have G H heads)
     float scale;
 };
 
@@ -75,6 +75,16 @@ static_assert(PS * 4 == PB * 2, "T1 rows must overlay dO rows");
 static_assert(SMEM <= 232448, "gradient kernel shared memory");
 
 // ---- operand views with per-dim factors, formed on the fly
+// q e^(G - G_r) from global memory (rows past the chunk's end: 0)
+struct QeV {
+    const __nv_bfloat16 *q;   // row 0 of the chunk, this query head
+    int64_t rs;               // row stride (elements)
+    int nv;
+    const float *G, *Gr;
+    __device__ __forceinline__ float at(int r, int c) const {
+        return r < nv ? bf(q + r * rs + c) * __expf(G[r * PF + c] - Gr[c]) : 0.f;
+    }
+};
 // beta_j k e^G
 struct KgbV {
     const __nv_bfloat16 *k;
@@ -94,6 +104,9 @@ struct VbV {
     }
 };
 
+// GQA: several query heads per state, one pass each for the parts of the
+// gradients that involve q and dO (dS' and dDelta already sum over them).
+template <bool GQA>
 __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_constant__ KdaGradParams p) {
     extern __shared__ __align__(16) uint8_t sm[];
     __nv_bfloat16 *Kb = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_KB);
@@ -115,16 +128,18 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
     const WyChunk ck = p.chunks[unit / p.H];
     const int nv = ck.nv;
     auto tok = [&](int i) { return (ck.tok0 + i) * p.H + h; };
+    // row i of query head gq of this state
+    auto qtok = [&](int i, int gq) { return ((ck.tok0 + i) * p.H + h) * p.G + gq; };
     const int64_t rowstride = (int64_t)p.H * D;   // elements between consecutive tokens of one head
+    int cur = 0;                                  // the pass's query head
 
     // ---- loads (rows past the chunk's end: 0): k, dO, g, Delta, dDelta, T
     for (int e = tid; e < C * (D / 8); e += NT) {
         const int i = e / (D / 8), d = 8 * (e % (D / 8));
         uint4 kv = make_uint4(0, 0, 0, 0), ov = kv;
         if (i < nv) {
-            const int64_t o = (int64_t)tok(i) * D + d;
-            kv = *reinterpret_cast<const uint4 *>(p.k + o);
-            ov = *reinterpret_cast<const uint4 *>(p.dout + o);
+            kv = *reinterpret_cast<const uint4 *>(p.k + (int64_t)tok(i) * D + d);
+            ov = *reinterpret_cast<const uint4 *>(p.dout + (int64_t)qtok(i, 0) * D + d);
         }
         *reinterpret_cast<uint4 *>(Kb + i * PB + d) = kv;
         *reinterpret_cast<uint4 *>(Ob + i * PB + d) = ov;
@@ -203,7 +218,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
     auto erow = [&](int e) { return e < 2 ? r0 : r1; };
     auto Gat = [&](int i, int d) { return GF[i * PF + d]; };
     auto kat = [&](int i, int d) { return bf(Kb + i * PB + d); };
-    auto qat = [&](int i, int d) { return i < nv ? bf(p.q + (int64_t)tok(i) * D + d) : 0.f; };
+    auto qat = [&](int i, int d) { return i < nv ? bf(p.q + (int64_t)qtok(i, cur) * D + d) : 0.f; };
     // a factored operand into an fp32 tile: k (or q) ⊙ e^(+-(G - G_r))
     auto stage = [&](float *dst, bool from_q, bool up) {
         for (int e = tid; e < C * (D / 4); e += NT) {
@@ -226,8 +241,25 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
     const Bv Ov{Ob, PB, 1};
     const float sc = p.scale;
 
-    // ---- S halves: dQ_1 = E ⊙ (dO~ S^T), dW = -dDelta S^T, and the last
-    // row's e^(G_C) rowsum(dS' ⊙ S) (dS' read straight from global)
+    // ---- one pass per query head of this state (one without grouped query
+    // heads): its dq, and its parts of dk and dG; the first pass also forms
+    // dW, the dS' terms and rowsum(dS' ⊙ S)
+    const int npass = GQA ? p.G : 1;
+#pragma unroll 1
+    for (int gq = 0; gq < npass; gq++) {
+    const bool first = !GQA || gq == 0;
+    cur = gq;
+    if (!first) {
+        __syncthreads();   // the previous pass's reads of dP (over dO's rows) are done
+        for (int e = tid; e < C * (D / 8); e += NT) {
+            const int i = e / (D / 8), d = 8 * (e % (D / 8));
+            uint4 ov = make_uint4(0, 0, 0, 0);
+            if (i < nv) ov = *reinterpret_cast<const uint4 *>(p.dout + (int64_t)qtok(i, gq) * D + d);
+            *reinterpret_cast<uint4 *>(Ob + i * PB + d) = ov;
+        }
+    }
+    // ---- S halves: dQ_1 = E ⊙ (dO~ S^T) (first pass: dW = -dDelta S^T, and
+    // the last row's e^(G_C) rowsum(dS' ⊙ S), dS' read straight from global)
     for (int hh = 0; hh < 2; hh++) {
         __syncthreads();
 #pragma unroll 2
@@ -235,11 +267,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
             const int i = w + 8 * m, c4 = 4 * lane;
             const float4 a = *reinterpret_cast<const float4 *>(Sg + (int64_t)(64 * hh + i) * D + c4);
             *reinterpret_cast<float4 *>(R + i * PF + c4) = a;
-            const float4 b = *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + c4);
-            float part = a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+            if (first) {
+                const float4 b = *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + c4);
+                float part = a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if (lane == 0) dGC[64 * hh + i] += gCv[64 * hh + i] * part;
+                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (lane == 0) dGC[64 * hh + i] += gCv[64 * hh + i] * part;
+            }
         }
         __syncthreads();
         const Fv RT{R, 1, PF};   // B(v, d') = S[64 hh + d'][v]
@@ -253,16 +287,18 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
                 const int i = erow(e), d = 64 * hh + nl[nt] + 2 * tg + (e & 1);
                 dQ[4 * hh + nt][e] = sc * acc[nt][e] * __expf(Gat(i, d));
             }
-        zero(acc);
-        warp_mm<4, D>(acc, Fv{DD, PF, 1}, m0, RT, nl);
+        if (first) {
+            zero(acc);
+            warp_mm<4, D>(acc, Fv{DD, PF, 1}, m0, RT, nl);
 #pragma unroll
-        for (int nt = 0; nt < 4; nt++)
+            for (int nt = 0; nt < 4; nt++)
 #pragma unroll
-            for (int e = 0; e < 4; e++) WB[erow(e) * PF + 64 * hh + nl[nt] + 2 * tg + (e & 1)] = -acc[nt][e];
+                for (int e = 0; e < 4; e++) WB[erow(e) * PF + 64 * hh + nl[nt] + 2 * tg + (e & 1)] = -acc[nt][e];
+        }
     }
-    // ---- dS' halves: X = Delta dS'^T;  dK += e^(G_C - G) ⊙ X, dG -= K ⊙ that,
-    // the last row's colsum of K ⊙ that
-    for (int hh = 0; hh < 2; hh++) {
+    // ---- dS' halves (first pass): X = Delta dS'^T;  dK += e^(G_C - G) ⊙ X,
+    // dG -= K ⊙ that, the last row's colsum of K ⊙ that
+    for (int hh = 0; hh < 2 && first; hh++) {
         __syncthreads();
         for (int e = tid; e < C * (D / 4); e += NT) {
             const int i = e / (D / 4), d = 4 * (e % (D / 4));
@@ -312,9 +348,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
                 T1[i * PS + j] = j <= i ? sc * acc[nt][e] : 0.f;
             }
     }
-    if (!steep) {   // Delta and the dS' half are dead: the factored operands of the next products
+    if (!steep) {   // the S / dS' half is dead (and without grouped query heads Delta): the factored operands
         stage(R, false, true);
-        stage(DL, true, false);
+        if (!GQA) stage(DL, true, false);
     }
     __syncthreads();
     // ---- dQ += E ⊙ (dP Kn);  dK += e^-G ⊙ (dP^T Qg), dG -= K ⊙ that
@@ -331,7 +367,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
                     dQ[nt][e] += acc[nt][e] * __expf(Gat(i, d) - Gr[d]);
                 }
             zero(acc);
-            warp_mm<8, C>(acc, Fv{T1, 1, PS}, m0, Fv{DL, PF, 1}, n8);
+            if (GQA)   // Delta is still needed by the next pass: q e^(G - G_r) formed on the fly
+                warp_mm<8, C>(acc, Fv{T1, 1, PS}, m0,
+                              QeV{p.q + (int64_t)qtok(0, gq) * D, rowstride * p.G, nv, GF, Gr}, n8);
+            else
+                warp_mm<8, C>(acc, Fv{T1, 1, PS}, m0, Fv{DL, PF, 1}, n8);
 #pragma unroll
             for (int nt = 0; nt < 8; nt++)
 #pragma unroll
@@ -371,9 +411,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
         dG[nt][1] += qat(r0, col + 1) * dQ[nt][1];
         dG[nt][2] += qat(r1, col) * dQ[nt][2];
         dG[nt][3] += qat(r1, col + 1) * dQ[nt][3];
-        if (r0 < nv) *reinterpret_cast<float2 *>(p.dq + (int64_t)tok(r0) * D + col) = make_float2(dQ[nt][0], dQ[nt][1]);
-        if (r1 < nv) *reinterpret_cast<float2 *>(p.dq + (int64_t)tok(r1) * D + col) = make_float2(dQ[nt][2], dQ[nt][3]);
+        if (r0 < nv)
+            *reinterpret_cast<float2 *>(p.dq + (int64_t)qtok(r0, gq) * D + col) = make_float2(dQ[nt][0], dQ[nt][1]);
+        if (r1 < nv)
+            *reinterpret_cast<float2 *>(p.dq + (int64_t)qtok(r1, gq) * D + col) = make_float2(dQ[nt][2], dQ[nt][3]);
     }
+    }   // query heads
     __syncthreads();   // every warp has read dP and q e^(G - G_r)
     if (!steep) {
         stage(DL, false, false);
@@ -595,10 +638,12 @@ int launch_bwd_grad_kda(const cpdr_ctx *c, const void *q, const void *k, const v
     prm.dbeta = dbeta;
     prm.dg = dg;
     prm.H = pl.H;
+    prm.G = pl.G;
     prm.scale = pl.scale;
-    cudaError_t e = cudaFuncSetAttribute(bwd_grad_kda_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    auto kern = pl.G > 1 ? bwd_grad_kda_kernel<true> : bwd_grad_kda_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return (int)e;
-    bwd_grad_kda_kernel<<<(unsigned)units, NT, SMEM, (cudaStream_t)stream>>>(prm);
+    kern<<<(unsigned)units, NT, SMEM, (cudaStream_t)stream>>>(prm);
     return (int)cudaGetLastError();
 }
 

@@ -62,7 +62,7 @@ constexpr int NTHREADS = 512;
 // stage layout (V's slots hold dO); MODE_BWD_ACC (bit 5) is its pass for a
 // state's query heads past the first.
 enum Mode { MODE_FWD = 0, MODE_PRE = 1, MODE_FWD_KDA = 2, MODE_PRE_KDA = 3, MODE_FWD_VAR = 4, MODE_REC = 9,
-            MODE_REC_KDA = 11, MODE_BWD = 16, MODE_BWD_KDA = 18, MODE_BWD_ACC = 48 };
+            MODE_REC_KDA = 11, MODE_BWD = 16, MODE_BWD_KDA = 18, MODE_BWD_ACC = 48, MODE_BWD_KDA_ACC = 50 };
 __host__ __device__ constexpr bool mode_fwd(int m) { return (m & 1) == 0; }
 __host__ __device__ constexpr bool mode_kda(int m) { return (m & 2) != 0; }
 __host__ __device__ constexpr bool mode_var(int m) { return (m & 4) != 0 || (m & 3) != 0; }
@@ -372,7 +372,7 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
                 // the forward's Qg and P (the last copy) belong to the query
                 // head: query heads past a state's first keep theirs after
                 // the units
-                const int gq = mode_fwd(MODE) ? r.hq - r.h * r.p->G : 0;
+                const int gq = mode_bwd(MODE) ? r.p->bwd_gq : mode_fwd(MODE) ? r.hq - r.h * r.p->G : 0;
                 const uint8_t *qp = gq == 0 ? unit + kKdaOffQg
                                             : r.p->kda_qp + (u * (r.p->G - 1) + (gq - 1)) * kKdaQpBytes;
                 mbar_arrive_expect_tx(fb, L.tx_bytes);
@@ -1249,7 +1249,8 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     r.seq = f.seq;
     r.flags = f.flags;
     r.hq = blockIdx.y;
-    r.h = mode_var(MODE) ? r.hq / p.G : r.hq;
+    // the forward's grid runs over query heads; the backward's over state heads
+    r.h = (mode_var(MODE) && !mode_bwd(MODE)) ? r.hq / p.G : r.hq;
     r.n = (f.len + C - 1) / C;
     r.nlast = f.len - (r.n - 1) * C;
     r.chunk0 = p.chunk0[fi];
@@ -1356,7 +1357,8 @@ static_assert(make_lay(MODE_BWD_ACC, ROLE_S).total == make_lay(MODE_BWD, ROLE_S)
 static_assert(make_lay(MODE_REC, ROLE_S).total == make_lay(MODE_PRE, ROLE_S).total, "recompute uses the S layout");
 static_assert(make_lay(MODE_REC_KDA, ROLE_S).total == make_lay(MODE_PRE_KDA, ROLE_S).total,
               "per-dim recompute uses the per-dim S layout");
-static_assert(make_lay(MODE_BWD_KDA, ROLE_S).total == make_lay(MODE_FWD_KDA, ROLE_S).total,
+static_assert(make_lay(MODE_BWD_KDA, ROLE_S).total == make_lay(MODE_FWD_KDA, ROLE_S).total &&
+                  make_lay(MODE_BWD_KDA_ACC, ROLE_S).total == make_lay(MODE_FWD_KDA, ROLE_S).total,
               "per-dim backward uses the per-dim forward layout");
 
 size_t smem_for(int mode, int role) { return make_lay(mode, role).total + 1024; }
@@ -1543,8 +1545,11 @@ int launch_tc_bwd_chain(const cpdr_ctx *c, const int32_t *items, int n_items, in
     prm.G = p.G;
     prm.bwd_gq = gq;
     prm.vfirst = p.vfirst;
-    if (p.gate_kind == CPDR_GATE_PER_DIM) {   // Q, K, P come pre-gated in the units (one query head per state)
-        if (gq > 0) return (int)cudaErrorInvalidValue;
+    if (p.gate_kind == CPDR_GATE_PER_DIM) {   // Q, K, P come pre-gated in the units
+        prm.kda_qp = (const uint8_t *)wy + p.wy_chunks.size() * (size_t)p.H * kKdaUnitBytes;
+        if (gq > 0)
+            return launch_chain<MODE_BWD_KDA_ACC, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.H,
+                                                          (cudaStream_t)stream);
         return launch_chain<MODE_BWD_KDA, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.H,
                                                   (cudaStream_t)stream);
     }

@@ -274,8 +274,7 @@ cpdr_status cpdr_conv1d_fwd(const cpdr_ctx *ctx, const void *x, const float *wei
  *      end of every continuing fragment);
  *   3. every fragment runs the reverse chain from that end gradient (or dht,
  *      or 0) and writes the input gradients.
- * For bf16 inputs and dk = dv = 128 (the scalar gate, or the per-dim gate
- * with one query head per state) the chains run in chunk form on the tensor
+ * For bf16 inputs and dk = dv = 128 (either gate) the chains run in chunk form on the tensor
  * cores: the forward is recomputed with every chunk's starting state and
  * Delta kept, the state-gradient chain runs chunk by chunk in reverse
  * (tcgen05), the reverse merge on the tensor cores, and a parallel kernel

@@ -145,13 +145,15 @@ def test_backward_state_v_first(dtype, d):
     dict(gate="gdn", dtype="bf16", G=2, lengths=[2048], R=4, vfirst=True, layout="zigzag"),
     dict(gate="gdn", dtype="bf16", G=3, lengths=[1500, 0, 548], R=4),
     dict(gate="gdn", dtype="bf16", G=2, lengths=[8192], R=8, workload="merge_bf16_t16384_h4_d128_r16"),
+    dict(gate="kda", dtype="bf16", G=3, lengths=[1500, 548], R=4),
+    dict(gate="kda", dtype="bf16", G=2, lengths=[2048], R=4, vfirst=True, layout="zigzag"),
 ], ids=["gdn-bf16-g2", "kda-bf16-g2", "gdn-fp32-g3-d64", "kda-fp32-g2", "gdn-bf16-g2-vfirst-zigzag",
-        "gdn-bf16-g3", "gdn-bf16-g2-merge-sensitive"])
+        "gdn-bf16-g3", "gdn-bf16-g2-merge-sensitive", "kda-bf16-g3", "kda-bf16-g2-vfirst-zigzag"])
 def test_backward_grouped_query_heads(case):
     """G query heads per state ([FLA-CP] §5.1): each state's chain takes the
     scale q do^T of all of its query heads, each query head its own dq (bf16,
-    d = 128, scalar gate: the tensor-core backward with a state-gradient
-    chain pass per query head; the rest on the CUDA-core chain)."""
+    d = 128: the tensor-core backward with a state-gradient chain pass per
+    query head, both gates; fp32 and d = 64 on the CUDA-core chain)."""
     base = inputs.WORKLOADS[case.get("workload") or
                             ("kda_bf16_t32768_h32_d128_r16" if case["gate"] == "kda" else "gdn_bf16_b2_t8192_h16_d128_r8")]
     H = 2
