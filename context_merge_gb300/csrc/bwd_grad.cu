@@ -147,6 +147,15 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__
         }
         *reinterpret_cast<float4 *>(DL + i * PF + d) = a;
         *reinterpret_cast<float4 *>(DD + i * PF + d) = b;
+        // the first half of dS' (the first pass starts with it) and T
+        *reinterpret_cast<float4 *>(R + i * PF + d) = *reinterpret_cast<const float4 *>(dSg + (int64_t)i * D + d);
+    }
+    {   // T = (I + A)^-1 of this unit, solved by the WY build (fp32)
+        const float *Tg = p.T + unit * C * C;
+        for (int e = tid; e < C * C / 4; e += NT) {
+            const int i = e / (C / 4), j = 4 * (e % (C / 4));
+            *reinterpret_cast<float4 *>(T2 + i * PS + j) = *reinterpret_cast<const float4 *>(Tg + i * C + j);
+        }
     }
     if (tid < C) {
         dGrow[tid] = 0.f;
@@ -207,23 +216,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__
             __syncthreads();   // the previous pass's reads of Q and dO (T1) are done
             load_qo(gq);
         }
-        // ---- S halves: dq_1 = gamma ⊙ (dO~ S^T) (and, first pass, dW and
-        // sum (dS' ⊙ S), dS' read straight from global)
-        for (int hh = 0; hh < 2; hh++) {
-            __syncthreads();
-            for (int e = tid; e < C * (D / 4); e += NT) {
-                const int i = e / (D / 4), d = 4 * (e % (D / 4));
-                const float4 a = *reinterpret_cast<const float4 *>(Sg + (int64_t)(64 * hh + i) * D + d);
-                *reinterpret_cast<float4 *>(R + i * PF + d) = a;
-                if (first) {
-                    const float4 b = *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + d);
-                    dgc_part += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
-                }
-            }
-            __syncthreads();
-            // columns d = 64 hh + cw + 8 nt + ...: B(v, d') = S[64 hh + d'][v] = R[d'][v]
-            const Fv RT{R, 1, PF};
-            const int nl[4] = {cw, cw + 8, cw + 16, cw + 24};
+        // ---- S halves: dq_1 = gamma ⊙ (dO~ S^T) (first pass: dW = -dDelta S^T);
+        // dS' halves (first pass): dk_Gamma = Gamma ⊙ (Delta dS'^T); and
+        // sum (dS' ⊙ S).  One 64 x 128 fp32 half at a time in R.
+        const int nl[4] = {cw, cw + 8, cw + 16, cw + 24};
+        const Fv RT{R, 1, PF};   // B(v, d') = R[d'][v]
+        auto s_phase = [&](int hh) {
             float acc[4][4];
             zero(acc);
             warp_mm<4, D>(acc, Ov, m0, RT, nl);
@@ -246,18 +244,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__
                     WB[r1 * PF + col + 1] = -acc[nt][3];
                 }
             }
-        }
-        // ---- dS' halves (first pass): dk_Gamma = Gamma ⊙ (Delta dS'^T)
-        for (int hh = 0; hh < 2 && first; hh++) {
-            __syncthreads();
-            for (int e = tid; e < C * (D / 4); e += NT) {
-                const int i = e / (D / 4), d = 4 * (e % (D / 4));
-                *reinterpret_cast<float4 *>(R + i * PF + d) =
-                    *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + d);
-            }
-            __syncthreads();
-            const Fv RT{R, 1, PF};
-            const int nl[4] = {cw, cw + 8, cw + 16, cw + 24};
+        };
+        auto ds_phase = [&](int hh) {
             float acc[4][4];
             zero(acc);
             warp_mm<4, D>(acc, Fv{DL, PF, 1}, m0, RT, nl);
@@ -273,6 +261,51 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__
                 dg0 -= k0;
                 dg1 -= k1;
                 dgc_k += k0 + k1;
+            }
+        };
+        if (first) {
+            // the next half's global loads are in flight (registers: a thread
+            // holds rows w + 8 m, columns 4 lane) while the current half is used;
+            // R starts with dS' half 0 (loaded with the inputs)
+            float4 pf[8];
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {
+                const float *sh = Sg + (int64_t)64 * hh * D;   // S half hh in flight
+#pragma unroll
+                for (int m = 0; m < 8; m++) pf[m] = *reinterpret_cast<const float4 *>(sh + (w + 8 * m) * D + 4 * lane);
+                __syncthreads();
+                ds_phase(hh);
+#pragma unroll
+                for (int m = 0; m < 8; m++) {   // sum (dS' ⊙ S) over this thread's elements
+                    const float4 x = *reinterpret_cast<const float4 *>(R + (w + 8 * m) * PF + 4 * lane);
+                    dgc_part += x.x * pf[m].x + x.y * pf[m].y + x.z * pf[m].z + x.w * pf[m].w;
+                }
+                __syncthreads();
+#pragma unroll
+                for (int m = 0; m < 8; m++) *reinterpret_cast<float4 *>(R + (w + 8 * m) * PF + 4 * lane) = pf[m];
+                if (hh == 0) {   // dS' half 1 in flight
+#pragma unroll
+                    for (int m = 0; m < 8; m++)
+                        pf[m] = *reinterpret_cast<const float4 *>(dSg + (64 + w + 8 * m) * D + 4 * lane);
+                }
+                __syncthreads();
+                s_phase(hh);
+                if (hh == 0) {
+                    __syncthreads();
+#pragma unroll
+                    for (int m = 0; m < 8; m++) *reinterpret_cast<float4 *>(R + (w + 8 * m) * PF + 4 * lane) = pf[m];
+                }
+            }
+        } else {
+            for (int hh = 0; hh < 2; hh++) {
+                __syncthreads();
+                for (int e = tid; e < C * (D / 4); e += NT) {
+                    const int i = e / (D / 4), d = 4 * (e % (D / 4));
+                    *reinterpret_cast<float4 *>(R + i * PF + d) =
+                        *reinterpret_cast<const float4 *>(Sg + (int64_t)(64 * hh + i) * D + d);
+                }
+                __syncthreads();
+                s_phase(hh);
             }
         }
         __syncthreads();
@@ -339,16 +372,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kernel(const __grid_constant__
         }
     }
     __syncthreads();
-    // ---- T = (I + A)^-1 of this unit, solved by the WY build (fp32)
-    {
-        const float *Tg = p.T + unit * C * C;
-        for (int e = tid; e < C * C / 4; e += NT) {
-            const int i = e / (C / 4), j = 4 * (e % (C / 4));
-            *reinterpret_cast<float4 *>(T2 + i * PS + j) = *reinterpret_cast<const float4 *>(Tg + i * C + j);
-        }
-    }
     __syncthreads();
-    // ---- TtW = T^T dW, TtU = T^T dDelta (64 x 128, register tiles)
+    // ---- TtW = T^T dW, TtU = T^T dDelta (64 x 128, register tiles); T was loaded with the inputs
     const Fv TT{T2, 1, PS};
     {
         float acc[8][4];
