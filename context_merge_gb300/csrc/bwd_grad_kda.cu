@@ -157,6 +157,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
         *reinterpret_cast<float4 *>(DL + i * PF + d) = a;
         *reinterpret_cast<float4 *>(DD + i * PF + d) = b;
         *reinterpret_cast<float4 *>(GF + i * PF + d) = gg;
+        // the first half of dS' (the first pass starts with it)
+        *reinterpret_cast<float4 *>(R + i * PF + d) = *reinterpret_cast<const float4 *>(dSg + (int64_t)i * D + d);
     }
     {
         const float *Tg = p.T + unit * C * C;
@@ -258,25 +260,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
             *reinterpret_cast<uint4 *>(Ob + i * PB + d) = ov;
         }
     }
-    // ---- S halves: dQ_1 = E ⊙ (dO~ S^T) (first pass: dW = -dDelta S^T, and
-    // the last row's e^(G_C) rowsum(dS' ⊙ S), dS' read straight from global)
-    for (int hh = 0; hh < 2; hh++) {
-        __syncthreads();
-#pragma unroll 2
-        for (int m = 0; m < 8; m++) {   // warp w takes row w + 8 m of the half, lane = 4 value columns
-            const int i = w + 8 * m, c4 = 4 * lane;
-            const float4 a = *reinterpret_cast<const float4 *>(Sg + (int64_t)(64 * hh + i) * D + c4);
-            *reinterpret_cast<float4 *>(R + i * PF + c4) = a;
-            if (first) {
-                const float4 b = *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + c4);
-                float part = a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                if (lane == 0) dGC[64 * hh + i] += gCv[64 * hh + i] * part;
-            }
-        }
-        __syncthreads();
-        const Fv RT{R, 1, PF};   // B(v, d') = S[64 hh + d'][v]
+    // ---- S halves: dQ_1 = E ⊙ (dO~ S^T) (first pass: dW = -dDelta S^T);
+    // dS' halves (first pass): X = Delta dS'^T, dK += e^(G_C - G) ⊙ X, dG -= K ⊙
+    // that, the last row's colsum of K ⊙ that; and the last row's
+    // e^(G_C) rowsum(dS' ⊙ S).  One 64 x 128 fp32 half at a time in R.
+    const Fv RT{R, 1, PF};   // B(v, d') = R[d'][v]
+    auto s_phase = [&](int hh) {
         float acc[4][4];
         zero(acc);
         warp_mm<4, D>(acc, Ov, m0, RT, nl);
@@ -295,20 +284,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
 #pragma unroll
                 for (int e = 0; e < 4; e++) WB[erow(e) * PF + 64 * hh + nl[nt] + 2 * tg + (e & 1)] = -acc[nt][e];
         }
-    }
-    // ---- dS' halves (first pass): X = Delta dS'^T;  dK += e^(G_C - G) ⊙ X,
-    // dG -= K ⊙ that, the last row's colsum of K ⊙ that
-    for (int hh = 0; hh < 2 && first; hh++) {
-        __syncthreads();
-        for (int e = tid; e < C * (D / 4); e += NT) {
-            const int i = e / (D / 4), d = 4 * (e % (D / 4));
-            *reinterpret_cast<float4 *>(R + i * PF + d) =
-                *reinterpret_cast<const float4 *>(dSg + (int64_t)(64 * hh + i) * D + d);
-        }
-        __syncthreads();
+    };
+    auto ds_phase = [&](int hh) {
         float acc[4][4];
         zero(acc);
-        warp_mm<4, D>(acc, Fv{DL, PF, 1}, m0, Fv{R, 1, PF}, nl);
+        warp_mm<4, D>(acc, Fv{DL, PF, 1}, m0, RT, nl);
 #pragma unroll
         for (int nt = 0; nt < 4; nt++) {
             float colp[2] = {0.f, 0.f};
@@ -331,6 +311,54 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
                 atomicAdd(dGC + 64 * hh + nl[nt] + 2 * tg, colp[0]);
                 atomicAdd(dGC + 64 * hh + nl[nt] + 2 * tg + 1, colp[1]);
             }
+        }
+    };
+    if (first) {
+        // the next half's global loads are in flight (registers: a thread holds
+        // rows w + 8 m, columns 4 lane) while the current half is used; R
+        // starts with dS' half 0 (loaded with the inputs)
+        float4 pf[8];
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+            const float *sh = Sg + (int64_t)64 * hh * D;   // S half hh in flight
+#pragma unroll
+            for (int m = 0; m < 8; m++) pf[m] = *reinterpret_cast<const float4 *>(sh + (w + 8 * m) * D + 4 * lane);
+            __syncthreads();
+            ds_phase(hh);
+#pragma unroll
+            for (int m = 0; m < 8; m++) {   // e^(G_C) rowsum(dS' ⊙ S): a warp holds whole rows
+                const float4 x = *reinterpret_cast<const float4 *>(R + (w + 8 * m) * PF + 4 * lane);
+                float part = x.x * pf[m].x + x.y * pf[m].y + x.z * pf[m].z + x.w * pf[m].w;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (lane == 0) atomicAdd(dGC + 64 * hh + w + 8 * m, gCv[64 * hh + w + 8 * m] * part);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int m = 0; m < 8; m++) *reinterpret_cast<float4 *>(R + (w + 8 * m) * PF + 4 * lane) = pf[m];
+            if (hh == 0) {   // dS' half 1 in flight
+#pragma unroll
+                for (int m = 0; m < 8; m++)
+                    pf[m] = *reinterpret_cast<const float4 *>(dSg + (64 + w + 8 * m) * D + 4 * lane);
+            }
+            __syncthreads();
+            s_phase(hh);
+            if (hh == 0) {
+                __syncthreads();
+#pragma unroll
+                for (int m = 0; m < 8; m++) *reinterpret_cast<float4 *>(R + (w + 8 * m) * PF + 4 * lane) = pf[m];
+            }
+        }
+    } else {
+        for (int hh = 0; hh < 2; hh++) {
+            __syncthreads();
+            for (int e = tid; e < C * (D / 4); e += NT) {
+                const int i = e / (D / 4), d = 4 * (e % (D / 4));
+                *reinterpret_cast<float4 *>(R + i * PF + d) =
+                    *reinterpret_cast<const float4 *>(Sg + (int64_t)(64 * hh + i) * D + d);
+            }
+            __syncthreads();
+            s_phase(hh);
         }
     }
     __syncthreads();
