@@ -93,15 +93,11 @@ struct KgbV {
         return beta[r] * bf(k + r * PB + c) * __expf(G[r * PF + c]);
     }
 };
-// beta_j v from global memory
+// beta_j v, v staged in shared memory (fp32)
 struct VbV {
-    const __nv_bfloat16 *v;
-    int64_t rs;
-    int nv;
+    const float *v;
     const float *beta;
-    __device__ __forceinline__ float at(int r, int c) const {
-        return r < nv ? beta[r] * bf(v + r * rs + c) : 0.f;
-    }
+    __device__ __forceinline__ float at(int r, int c) const { return beta[r] * v[r * PF + c]; }
 };
 
 // GQA: several query heads per state, one pass each for the parts of the
@@ -473,6 +469,27 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
 #pragma unroll
             for (int e = 0; e < 4; e++) T1[erow(e) * PS + nl[nt] + 2 * tg + (e & 1)] = acc[nt][e];
     }
+    __syncthreads();   // every warp has read k e^(G_r - G) (R)
+    // v into R (fp32, rows past the chunk's end 0) for rowsum(TtU ⊙ V) and U
+    for (int e = tid; e < C * (D / 8); e += NT) {
+        const int i = e / (D / 8), d = 8 * (e % (D / 8));
+        float x[8];
+        if (i < nv) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(p.v + (int64_t)tok(i) * D + d);
+            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&uw[c]));
+                x[2 * c] = f.x;
+                x[2 * c + 1] = f.y;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; c++) x[c] = 0.f;
+        }
+        *reinterpret_cast<float4 *>(R + i * PF + d) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4 *>(R + i * PF + d + 4) = make_float4(x[4], x[5], x[6], x[7]);
+    }
     const Fv TT{T2, 1, PS};
     // ---- TtW = T^T dW: dK += E ⊙ beta TtW, dG += K ⊙ that, dbeta += rowsum(TtW ⊙ Kg)
     {
@@ -504,18 +521,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
 #pragma unroll
         for (int nt = 0; nt < 8; nt++) {
             const int col = n8[nt] + 2 * tg;
-            if (r0 < nv) {
-                const __nv_bfloat16 *vr = p.v + (int64_t)tok(r0) * D + col;
-                db0 += acc[nt][0] * bf(vr) + acc[nt][1] * bf(vr + 1);
+            db0 += acc[nt][0] * R[r0 * PF + col] + acc[nt][1] * R[r0 * PF + col + 1];
+            db1 += acc[nt][2] * R[r1 * PF + col] + acc[nt][3] * R[r1 * PF + col + 1];
+            if (r0 < nv)
                 *reinterpret_cast<float2 *>(p.dv + (int64_t)tok(r0) * D + col) =
                     make_float2(bet[r0] * acc[nt][0], bet[r0] * acc[nt][1]);
-            }
-            if (r1 < nv) {
-                const __nv_bfloat16 *vr = p.v + (int64_t)tok(r1) * D + col;
-                db1 += acc[nt][2] * bf(vr) + acc[nt][3] * bf(vr + 1);
+            if (r1 < nv)
                 *reinterpret_cast<float2 *>(p.dv + (int64_t)tok(r1) * D + col) =
                     make_float2(bet[r1] * acc[nt][2], bet[r1] * acc[nt][3]);
-            }
         }
         __syncthreads();   // every warp has read Delta (TtU replaces it) and dDelta
 #pragma unroll
@@ -523,21 +536,22 @@ __global__ void __launch_bounds__(NT, 1) bwd_grad_kda_kernel(const __grid_consta
 #pragma unroll
             for (int e = 0; e < 4; e++) DL[erow(e) * PF + n8[nt] + 2 * tg + (e & 1)] = acc[nt][e];
     }
-    // ---- W = T diag(beta) Kg (into R), U = T diag(beta) V (into DD)
+    // ---- U = T diag(beta) V (into DD, from v in R), then W = T diag(beta) Kg (into R)
     {
         float acc[8][4];
         zero(acc);
-        warp_mm<8, C>(acc, Fv{T2, PS, 1}, m0, KgbV{Kb, GF, bet}, n8);
-#pragma unroll
-        for (int nt = 0; nt < 8; nt++)
-#pragma unroll
-            for (int e = 0; e < 4; e++) R[erow(e) * PF + n8[nt] + 2 * tg + (e & 1)] = acc[nt][e];
-        zero(acc);
-        warp_mm<8, C>(acc, Fv{T2, PS, 1}, m0, VbV{p.v + (int64_t)tok(0) * D, rowstride, nv, bet}, n8);
+        warp_mm<8, C>(acc, Fv{T2, PS, 1}, m0, VbV{R, bet}, n8);
 #pragma unroll
         for (int nt = 0; nt < 8; nt++)
 #pragma unroll
             for (int e = 0; e < 4; e++) DD[erow(e) * PF + n8[nt] + 2 * tg + (e & 1)] = acc[nt][e];
+        zero(acc);
+        warp_mm<8, C>(acc, Fv{T2, PS, 1}, m0, KgbV{Kb, GF, bet}, n8);
+        __syncthreads();   // every warp has read v (R)
+#pragma unroll
+        for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) R[erow(e) * PF + n8[nt] + 2 * tg + (e & 1)] = acc[nt][e];
     }
     __syncthreads();
     // ---- dA = -strict_lower(TtW W^T + TtU U^T); dbeta += rowsum(dA ⊙ Y); bdA = beta dA (into T2)
