@@ -25,6 +25,7 @@ CASES = [
     ("gdn_bf16_b2_t8192_h16_d128_r8", dict(B=1, T=2048, H=4), "bf16"),     # tcgen05 kernels
     ("gdn_bf16_varlen65536_n12_h16_d128_r32", dict(lengths=[700, 1100, 248]), "bf16"),
     ("kda_bf16_t32768_h32_d128_r16", dict(T=2048, H=2, R=4), "bf16"),       # per-dim gate
+    ("kda_bf16_t32768_h32_d128_r16", dict(T=2048, H=2, R=4, Hq=4), "bf16"),  # and grouped query heads
     ("gdn_fp32_t1024_h2_d64_r4", {}, "fp32"),                                # CUDA-core kernels
 ]
 
@@ -36,7 +37,7 @@ def rel_err(x, ref, kind):
     return float((x - ref).norm() / ref.norm())
 
 
-@pytest.mark.parametrize("name,kw,kind", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("name,kw,kind", CASES, ids=[c[0] + ("-gqa" if "Hq" in c[1] else "") for c in CASES])
 def test_noalloc_matches_regular_entry_points(cpdr_lib, name, kw, kind):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
@@ -48,15 +49,16 @@ def test_noalloc_matches_regular_entry_points(cpdr_lib, name, kw, kind):
     inp = inputs.make_inputs(w, device="cuda", lengths=lengths, **kw)
     q, k, v, beta, g = (inp[x] for x in ("q", "k", "v", "beta", "g"))
     args = (inp["B"], inp["T"], inp["H"], inp["d"], R)
-    ref_ctx = cpdr.Context(*args, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"])
+    Hq = inp["Hq"]
+    ref_ctx = cpdr.Context(*args, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"], Hq=Hq)
     o_ref, bufs = ref_ctx.run(q, k, v, beta, g)
     torch.cuda.synchronize()
-    ctx = cpdr.Context(*args, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"], host_only=True)
+    ctx = cpdr.Context(*args, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"], host_only=True, Hq=Hq)
     tol = 1e-4 if kind == "fp32" else 2e-2
     cpu = {x: inp[x].cpu() for x in ("q", "k", "v", "beta", "g")}
     ref = run_oracle(dict(inp, **cpu, R=R))
     for _ in range(2):   # two calls in a row share (and must clear) the static scratch
-        o = torch.full_like(v, float("nan"))
+        o = torch.full_like(o_ref, float("nan"))
         fs = torch.full_like(bufs["final_state"], float("nan"))
         ctx.forward_noalloc(q, k, v, beta, g, o, fs)
         torch.cuda.synchronize()
