@@ -1059,6 +1059,16 @@ __device__ __forceinline__ void run_state(const Run &r) {
             tc_fence_after();
             float v[32];
             tmem_ld32(lane_base + TM_DL + 32 * half, v);
+            if (SPLIT) {   // the hi(-M^T) lo(W)^T half of the Delta product
+#pragma unroll
+                for (int part = 0; part < 2; part++) {
+                    float u[16];
+                    tmem_ld16(lane_base + TM_DL + 64 + 32 * half + 16 * part, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; i++) v[16 * part + i] += u[i];
+                }
+            }
             tmem_ld_wait();
             if (REC) {   // the chunk's Delta, [64][dv] (rows past the chunk's end: 0)
                 const int nv = rows_of(r, ch);
@@ -1196,9 +1206,11 @@ __device__ __forceinline__ void run_issuer(const Run &r) {
                 if (!SPLIT) {
                     mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wb, HAS_U);
                 } else {
-                    mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wb, false);
+                    // hi(-M^T) [hi(W) | lo(W)]^T as one N = 128 product (the
+                    // two W images are one 64-column atom apart), its halves
+                    // summed by the epilogue; lo(-M^T) hi(W)^T onto the first
+                    mma_tmn<128, 128>(tm + TM_DL, tm + TM_SB, d.wb, false);
                     mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB_LO, d.wb, true);
-                    mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wblo, true);
                 }
                 mma_commit(&r.bar[B_WBFREE]);
                 mma_commit(&r.bar[B_DLFULL]);
@@ -1346,6 +1358,10 @@ static_assert(make_lay(MODE_PRE, ROLE_S).total + 1024 <= kMaxSmem, "pre-process 
 static_assert(make_lay(MODE_PRE, ROLE_M).total + 1024 <= kMaxSmem, "pre-process M layout exceeds shared memory");
 static_assert(make_lay(MODE_FWD_KDA, ROLE_S).total + 1024 <= kMaxSmem, "per-dim forward layout exceeds shared memory");
 static_assert(make_lay(MODE_FWD_VAR, ROLE_S).total == make_lay(MODE_FWD, ROLE_S).total, "variant forward layout");
+// the M chain's fused Delta product reads hi(W) | lo(W) as one N = 128 operand (atom stride 16 KiB)
+static_assert(make_lay(MODE_PRE, ROLE_M).wb_lo == make_lay(MODE_PRE, ROLE_M).wb + 16384 &&
+                  make_lay(MODE_PRE_KDA, ROLE_M).wb_lo == make_lay(MODE_PRE_KDA, ROLE_M).wb + 16384,
+              "W images of the M chain");
 static_assert(make_lay(MODE_PRE_KDA, ROLE_S).total + 1024 <= kMaxSmem, "per-dim pre-process S layout too large");
 static_assert(make_lay(MODE_PRE_KDA, ROLE_M).total + 1024 <= kMaxSmem, "per-dim pre-process M layout too large");
 static_assert(make_lay(MODE_FWD_KDA, ROLE_S).tx_bytes < (1u << 20) && make_lay(MODE_PRE_KDA, ROLE_M).tx_bytes < (1u << 20),
