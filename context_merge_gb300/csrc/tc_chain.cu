@@ -61,8 +61,11 @@ constexpr int NTHREADS = 512;
 // chunk form in reverse chunk order with the forward's warp roles and
 // stage layout (V's slots hold dO); MODE_BWD_ACC (bit 5) is its pass for a
 // state's query heads past the first.
+// MODE_FWD_G2 (bit 6) is the forward of two query heads per state (grouped
+// query heads, G = 2): one chain per state head emits both heads' outputs.
 enum Mode { MODE_FWD = 0, MODE_PRE = 1, MODE_FWD_KDA = 2, MODE_PRE_KDA = 3, MODE_FWD_VAR = 4, MODE_REC = 9,
-            MODE_REC_KDA = 11, MODE_BWD = 16, MODE_BWD_KDA = 18, MODE_BWD_ACC = 48, MODE_BWD_KDA_ACC = 50 };
+            MODE_REC_KDA = 11, MODE_BWD = 16, MODE_BWD_KDA = 18, MODE_BWD_ACC = 48, MODE_BWD_KDA_ACC = 50,
+            MODE_FWD_G2 = 68 };
 __host__ __device__ constexpr bool mode_fwd(int m) { return (m & 1) == 0; }
 __host__ __device__ constexpr bool mode_kda(int m) { return (m & 2) != 0; }
 __host__ __device__ constexpr bool mode_var(int m) { return (m & 4) != 0 || (m & 3) != 0; }
@@ -71,6 +74,7 @@ __host__ __device__ constexpr bool mode_bwd(int m) { return (m & 16) != 0; }
 // the backward's later query-head passes (grouped query heads): no end
 // gradient, and the stored sums are added to the first pass's
 __host__ __device__ constexpr bool mode_acc(int m) { return (m & 32) != 0; }
+__host__ __device__ constexpr bool mode_g2(int m) { return (m & 64) != 0; }
 enum Role { ROLE_S = 0, ROLE_M = 1 };
 
 // Optional event trace (compile with -DCPDR_TRACE): CTA (0, 0) of each
@@ -97,6 +101,14 @@ constexpr uint32_t TM_P = 0, TM_W = 64, TM_DL = 128, TM_O = 192, TM_PS = 256, TM
                    TM_DGB = 480;
 constexpr uint32_t TM_SB_LO = 0, TM_DGB_LO = 448;
 constexpr uint32_t TM_COLS = 512;
+// The two-head forward: W^T and the two heads' Q K^T take columns 0..63 in
+// turn, Delta^T 64..127, both heads' O^T 128..255 (head 0 first); the rest
+// as above.
+template <int MODE>
+struct TMap {
+    static constexpr uint32_t P = mode_g2(MODE) ? 0u : TM_P, W = mode_g2(MODE) ? 0u : TM_W,
+                              DL = mode_g2(MODE) ? 64u : TM_DL, O = mode_g2(MODE) ? 128u : TM_O;
+};
 
 // mbarrier indices
 enum Bar {
@@ -196,7 +208,14 @@ __host__ __device__ constexpr Lay make_lay(int mode, int role) {
         L.total = o;
         return L;
     }
-    if (mode_fwd(mode)) {
+    if (mode_g2(mode)) {
+        // per 64-column atom K | Q (head 0) | Q (head 1): [K; Q0] and [Q0; Q1]
+        // are the stacked A operands of the two heads' Q K^T, [Q0; Q1] the B
+        // operand of both heads' output product
+        L.stage_bytes = 81920; L.kc0 = 0; L.qc0 = 8192; L.kc1 = 24576; L.qc1 = 32768; L.vc0 = 49152; L.vc1 = 57344;
+        L.t1 = 65536; L.t2 = 73728;
+        L.k_lbo = 24576; L.v_lbo = 8192; L.wy_off = 0;
+    } else if (mode_fwd(mode)) {
         L.stage_bytes = 65536; L.kc0 = 0; L.qc0 = 8192; L.kc1 = 16384; L.qc1 = 24576; L.vc0 = 32768; L.vc1 = 40960;
         L.t1 = 49152; L.t2 = 57344;
         L.k_lbo = 16384; L.v_lbo = 8192; L.wy_off = 0;
@@ -210,8 +229,9 @@ __host__ __device__ constexpr Lay make_lay(int mode, int role) {
         L.k_lbo = 8192; L.v_lbo = 0; L.wy_off = (uint32_t)kWyTileBytes;
     }
     L.tx_bytes = L.stage_bytes;
-    // three stages: a chunk's loads start two chunks ahead
-    L.nstage = 3;
+    // three stages: a chunk's loads start two chunks ahead (the two-head
+    // forward: two, for the second Q tile)
+    L.nstage = mode_g2(mode) ? 2 : 3;
     // gate slots: a slot is rewritten once the chunk NG before it is
     // finished, which the stage ring guarantees for NG = stages + 2
     L.ngate = L.nstage + 2;
@@ -220,7 +240,7 @@ __host__ __device__ constexpr Lay make_lay(int mode, int role) {
     L.gate_floats = (mode_fwd(mode)) ? 5 * 64 + 4 : 64 + 4;
     const bool split = (!mode_fwd(mode) && role == ROLE_M);
     uint32_t o = L.nstage * L.stage_bytes;
-    L.mask = o; o += (mode_fwd(mode) ? 8192 : 0);
+    L.mask = o; o += (mode_g2(mode) ? 16384 : mode_fwd(mode) ? 8192 : 0);   // the two-head forward: two masks
     L.wb = o; o += 16384;
     L.wb_lo = o; o += (split ? 16384 : 0);
     L.gates = o; o += L.ngate * L.gate_floats * 4;
@@ -399,6 +419,10 @@ __device__ __forceinline__ void run_producer(const Run &r, const CUtensorMap *tq
                 const int hq = mode_var(MODE) ? r.hq : hb;
                 tma_load_3d(st + L.qc0, tq, fb, 0, hq, tok);
                 tma_load_3d(st + L.qc1, tq, fb, 64, hq, tok);
+                if (mode_g2(MODE)) {   // the second query head's rows right after the first's
+                    tma_load_3d(st + L.qc0 + 8192, tq, fb, 0, hq + 1, tok);
+                    tma_load_3d(st + L.qc1 + 8192, tq, fb, 64, hq + 1, tok);
+                }
             }
             if (mode_fwd(MODE) || ROLE == ROLE_S) {
                 tma_load_3d(st + L.vc0, tv, fb, 0, hb, tok);
@@ -545,6 +569,47 @@ __device__ __forceinline__ void run_mma(const Run &r) {
     constexpr uint32_t KATOM = L.kc1 - L.kc0;
     // the backward's first products from dO (X1) are issued by the state warps
     constexpr bool MMA_U = HAS_U && !mode_bwd(MODE);
+    if constexpr (mode_g2(MODE)) {
+        // Two query heads per state: chunk t's W^T and U^T, then head 0's and
+        // head 1's Q K^T in turn in the columns W^T used (each once its
+        // previous reader is done), after chunk t-1's Delta product completed.
+        // The mask-warp releases of the Q K^T columns alternate heads, so
+        // head 0's is always phase parity 0 and head 1's parity 1.
+        using T = TMap<MODE>;
+        constexpr uint32_t QATOM = L.qc1 - L.qc0;
+        for (int t = 0; t < r.n; t++) {
+            if (!mbar_wait(&r.bar[B_FULL0 + t % NS], (t / NS) & 1, ctl, st, 20)) break;
+            if (t >= 1 && !mbar_wait(&r.bar[B_WBFREE], (t - 1) & 1, ctl, st, 24)) break;
+            if (t >= 1 && !mbar_wait(&r.bar[B_PFREE], 1, ctl, st, 22)) break;   // head 1's product of chunk t-1 read
+            tc_fence_after();
+            TR(1, t, 0);
+            mma_mnk<64, 64>(tm + T::W, stg<MODE, ROLE>(d.kmn0, t), stg<MODE, ROLE>(d.t20, t), 8192, false);
+            mma_commit(&r.bar[B_WFULL]);
+            if (t >= 1 && !mbar_wait(&r.bar[B_DLREADY], (t - 1) & 1, ctl, st, 23)) break;
+            tc_fence_after();
+            mma_mnk<64, 64>(tm + T::DL, stg<MODE, ROLE>(d.vmn0, t), stg<MODE, ROLE>(d.t10, t), 8192, false);
+            mma_commit(&r.bar[B_UFULL]);
+            // head 0: P = [K; Q0] K^T, once the W epilogue has read W^T
+            if (!mbar_wait(&r.bar[B_WREADY], t & 1, ctl, st, 21)) break;
+            tc_fence_after();
+            mma_kk<64, 128, false>(tm + T::P, stg<MODE, ROLE>(d.stack0, t), KATOM, stg<MODE, ROLE>(d.stack0, t),
+                                   KATOM, false);
+            mma_commit(&r.bar[B_PFULL]);
+            // head 1: P = [Q0; Q1] K^T, once the mask warps have read head 0's
+            if (!mbar_wait(&r.bar[B_PFREE], 0, ctl, st, 22)) break;
+            tc_fence_after();
+            mma_kk<64, 128, false>(tm + T::P, stg<MODE, ROLE>(d.q0, t), QATOM, stg<MODE, ROLE>(d.stack0, t), KATOM,
+                                   false);
+            mma_commit(&r.bar[B_PFULL]);
+            mma_commit(&r.bar[B_EMPTY0 + t % NS]);   // this warp's reads of stage t
+            TR(1, t, 1);
+        }
+        mma_commit(&r.bar[B_DRAIN]);
+        Ctl local;
+        local.abort = 0;
+        mbar_wait(&r.bar[B_DRAIN], 0, &local, st, 30);
+        return;
+    }
     for (int t = 0; t < r.n; t++) {
         if (!mbar_wait(&r.bar[B_FULL0 + t % NS], (t / NS) & 1, ctl, st, 20)) break;
         // TMEM columns of W and P are free once chunk t-1's were read; the
@@ -632,6 +697,72 @@ __device__ __forceinline__ void run_mask(const Run &r) {
     }
     const int i = 32 * (w - 2) + lane;   // row of Q K^T (TMEM lane 64 + i)
     constexpr bool BWD = mode_bwd(MODE);
+    if constexpr (mode_g2(MODE)) {
+        // Two query heads: head 0's mask from the first Q K^T; once the second
+        // product (which reads head 0's Q rows unscaled) has completed, both
+        // heads' Q rows scaled by gamma_i in place, then head 1's mask.
+        for (int ch = 0; ch < r.n; ch++) {
+            if (!warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 50)) return;
+            const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(ch));
+            const float Gi = gs.G[i], ei = gs.e[i];
+            const bool exact = gs.gC[1] != 0.f;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; hh++) {
+                if (w == 2) TR(4, ch, hh);
+                if (!warp_wait(r, B_PFULL, (uint32_t)hh, 51)) return;
+                tc_fence_after();
+                if (hh == 1) {
+                    uint8_t *st = r.base + (ch % (int)L.nstage) * L.stage_bytes;
+                    const __nv_bfloat162 g2 = __float2bfloat162_rn(gs.gam[i]);
+#pragma unroll
+                    for (int a = 0; a < 4; a++) {
+                        uint8_t *tile = st + ((a & 1) ? L.qc1 : L.qc0) + (a >> 1) * 8192;
+#pragma unroll
+                        for (int c = 0; c < 8; c++) {
+                            uint4 u = *reinterpret_cast<uint4 *>(tile + sw128(i, c));
+                            __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+                            for (int e = 0; e < 4; e++) h[e] = __hmul2(h[e], g2);
+                            *reinterpret_cast<uint4 *>(tile + sw128(i, c)) = u;
+                        }
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&r.bar[B_QREADY0 + (ch & 1)]);
+                }
+                float m[64];
+#pragma unroll
+                for (int half = 0; half < 2; half++) {
+                    float v[32];
+                    tmem_ld32(r.tmem + ((uint32_t)(64 + 32 * (w - 2)) << 16) + TMap<MODE>::P + 32 * half, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; q4++) {
+                        const int j0 = 32 * half + 4 * q4;
+                        const float4 f4 = *reinterpret_cast<const float4 *>(gs.f + j0);
+                        const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; u++) {
+                            const float x = v[4 * q4 + u];
+                            const float val = exact ? x * exp2f(Gi - gs.G[j0 + u]) : x * ei * fv[u];
+                            m[j0 + u] = (j0 + u <= i) ? val : 0.f;
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&r.bar[B_PFREE]);
+                // the previous chunk's masks must have been consumed
+                if (hh == 0 && ch >= 1 && !warp_wait(r, B_MFREE, (ch - 1) & 1, 52)) return;
+                store_row<8>(r.base + L.mask + 8192 * hh, nullptr, i, 0, m);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&r.bar[B_MREADY]);
+            if (w == 2) TR(4, ch, 2);
+        }
+        return;
+    }
     for (int ch = 0; ch < r.n; ch++) {
         if (!warp_wait(r, B_GATE0 + gate_slot<MODE, ROLE>(ch), gate_parity<MODE, ROLE>(ch), 50)) return;
         const Gates gs = gates_of<MODE, ROLE>(r, gate_slot<MODE, ROLE>(ch));
@@ -719,8 +850,8 @@ __device__ __forceinline__ void run_wepi(const Run &r) {
         if (w == 4) TR(2, t, 0);
         tc_fence_after();
         float v0[32], v1[32];
-        tmem_ld32(lane_base + TM_W, v0);
-        tmem_ld32(lane_base + TM_W + 32, v1);
+        tmem_ld32(lane_base + TMap<MODE>::W, v0);
+        tmem_ld32(lane_base + TMap<MODE>::W + 32, v1);
         tmem_ld_wait();
         tc_fence_before();
         // the previous chunk's Delta product must have read the tile
@@ -745,6 +876,39 @@ __device__ __forceinline__ void run_wepi(const Run &r) {
             const int64_t ostride = (int64_t)Hq * D;
             __nv_bfloat16 *op = p.o + ((r.tok0 + (int64_t)t * C) * Hq + hq) * D + row;
             const float sc = -p.scale;   // the accumulator holds -O^T
+            if constexpr (mode_g2(MODE)) {
+                // both query heads (hq, hq + 1): head 0 read and stored, then
+                // head 1 read, the accumulator released, head 1 stored (one
+                // head's outputs in registers at a time)
+#pragma unroll 1
+                for (int hh = 0; hh < 2; hh++) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int piece = 0; piece < 4; piece++) {   // 16 columns at a time
+                        float a[16];
+                        tmem_ld16(lane_base + TMap<MODE>::O + 64 * hh + 16 * piece, a);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 8; k++) pk[8 * piece + k] = pack_bf16(sc * a[2 * k], sc * a[2 * k + 1]);
+                    }
+                    if (hh == 1) {
+                        if (w == 4) TR(2, t, 4);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&r.bar[B_OFREE]);
+                    }
+                    __nv_bfloat16 *q = op + hh * D;
+#pragma unroll
+                    for (int k = 0; k < 32; k++) {
+                        if (2 * k < nv) *q = __ushort_as_bfloat16((unsigned short)(pk[k] & 0xffffu));
+                        q += ostride;
+                        if (2 * k + 1 < nv) *q = __ushort_as_bfloat16((unsigned short)(pk[k] >> 16));
+                        q += ostride;
+                    }
+                }
+                if (w == 4) TR(2, t, 2);
+                continue;
+            }
             float a[32], b[32];
             tmem_ld32(lane_base + TM_O, a);
             tmem_ld32(lane_base + TM_O + 32, b);
@@ -982,6 +1146,8 @@ __device__ __forceinline__ void run_state(const Run &r) {
     Ctl *ctl = r.ctl;
     const Descs d = make_descs<MODE, ROLE>(r);
     constexpr uint32_t QATOM = L.qc1 - L.qc0;
+    constexpr uint32_t tDL = TMap<MODE>::DL, tO = TMap<MODE>::O;
+    constexpr int NO = mode_g2(MODE) ? 128 : 64;   // output columns: one or two query heads
     float S[64];
     const int64_t sidx = ((int64_t)r.seg * H + r.h) * D * D;
     if constexpr (mode_bwd(MODE)) {
@@ -1030,7 +1196,7 @@ __device__ __forceinline__ void run_state(const Run &r) {
                 TR(1, ch, 2);
                 // Delta^T (+)= (-S^T) W^T
                 if (!SPLIT) {
-                    mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wb, HAS_U);
+                    mma_tmn<64, 128>(tm + tDL, tm + TM_SB, d.wb, HAS_U);
                 } else {
                     mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB, d.wb, false);
                     mma_tmn<64, 128>(tm + TM_DL, tm + TM_SB_LO, d.wb, true);
@@ -1044,7 +1210,8 @@ __device__ __forceinline__ void run_state(const Run &r) {
                 if (ok) ok = mbar_wait(&r.bar[B_QREADY0 + (ch & 1)], (ch >> 1) & 1, ctl, st, 67);
                 if (ok) {
                     tc_fence_after();
-                    mma_tk<64, 128>(tm + TM_O, tm + TM_SB, stg<MODE, ROLE>(d.q0, ch), QATOM, false);
+                    // two heads: B = [gamma ⊙ Q0; gamma ⊙ Q1], N = 128
+                    mma_tk<NO, 128>(tm + tO, tm + TM_SB, stg<MODE, ROLE>(d.q0, ch), QATOM, false);
                 }
             }
             TR(1, ch, 3);
@@ -1058,7 +1225,7 @@ __device__ __forceinline__ void run_state(const Run &r) {
         if (ok) {
             tc_fence_after();
             float v[32];
-            tmem_ld32(lane_base + TM_DL + 32 * half, v);
+            tmem_ld32(lane_base + tDL + 32 * half, v);
             if (SPLIT) {   // the hi(-M^T) lo(W)^T half of the Delta product
 #pragma unroll
                 for (int part = 0; part < 2; part++) {
@@ -1118,7 +1285,8 @@ __device__ __forceinline__ void run_state(const Run &r) {
                 if (iok) {
                     tc_fence_after();
                     // -O^T += (-Delta^T) mask^T  (per-dim gate: the stage's P)
-                    mma_tk<64, 64>(tm + TM_O, tm + TM_DB, KDA ? stg<MODE, ROLE>(d.pt0, ch) : d.mask, 8192, true);
+                    // two heads: B = [mask0; mask1], N = 128
+                    mma_tk<NO, 64>(tm + tO, tm + TM_DB, KDA ? stg<MODE, ROLE>(d.pt0, ch) : d.mask, 8192, true);
                     mma_commit(&r.bar[B_OFULL]);
                     mma_commit(&r.bar[B_MFREE]);
                 }
@@ -1263,6 +1431,10 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     r.hq = blockIdx.y;
     // the forward's grid runs over query heads; the backward's over state heads
     r.h = (mode_var(MODE) && !mode_bwd(MODE)) ? r.hq / p.G : r.hq;
+    if (mode_g2(MODE)) {   // the grid runs over state heads; this chain serves hq and hq + 1
+        r.h = blockIdx.y;
+        r.hq = 2 * r.h;
+    }
     r.n = (f.len + C - 1) / C;
     r.nlast = f.len - (r.n - 1) * C;
     r.chunk0 = p.chunk0[fi];
@@ -1358,6 +1530,15 @@ static_assert(make_lay(MODE_PRE, ROLE_S).total + 1024 <= kMaxSmem, "pre-process 
 static_assert(make_lay(MODE_PRE, ROLE_M).total + 1024 <= kMaxSmem, "pre-process M layout exceeds shared memory");
 static_assert(make_lay(MODE_FWD_KDA, ROLE_S).total + 1024 <= kMaxSmem, "per-dim forward layout exceeds shared memory");
 static_assert(make_lay(MODE_FWD_VAR, ROLE_S).total == make_lay(MODE_FWD, ROLE_S).total, "variant forward layout");
+static_assert(make_lay(MODE_FWD_G2, ROLE_S).total + 1024 <= kMaxSmem && make_lay(MODE_FWD_G2, ROLE_S).ngate <= kMaxGateSlots,
+              "two-head forward layout exceeds shared memory");
+// the two-head forward's stacked operands: [K; Q0] and [Q0; Q1] contiguous per atom, the two masks adjacent
+static_assert(make_lay(MODE_FWD_G2, ROLE_S).qc0 == make_lay(MODE_FWD_G2, ROLE_S).kc0 + 8192 &&
+                  make_lay(MODE_FWD_G2, ROLE_S).kc1 - make_lay(MODE_FWD_G2, ROLE_S).kc0 ==
+                      make_lay(MODE_FWD_G2, ROLE_S).qc1 - make_lay(MODE_FWD_G2, ROLE_S).qc0 &&
+                  make_lay(MODE_FWD_G2, ROLE_S).qc0 + 16384 <= make_lay(MODE_FWD_G2, ROLE_S).kc1 &&
+                  make_lay(MODE_FWD_G2, ROLE_S).qc1 + 16384 <= make_lay(MODE_FWD_G2, ROLE_S).vc0,
+              "two-head forward stage layout");
 // the M chain's fused Delta product reads hi(W) | lo(W) as one N = 128 operand (atom stride 16 KiB)
 static_assert(make_lay(MODE_PRE, ROLE_M).wb_lo == make_lay(MODE_PRE, ROLE_M).wb + 16384 &&
                   make_lay(MODE_PRE_KDA, ROLE_M).wb_lo == make_lay(MODE_PRE_KDA, ROLE_M).wb + 16384,
@@ -1479,10 +1660,15 @@ int launch_tc_fwd(const cpdr_ctx *c, const int32_t *items, int n_items, const vo
     prm.scale = p.scale;
     if (kda) prm.kda_qp = (const uint8_t *)wy + p.wy_chunks.size() * (size_t)p.H * kKdaUnitBytes;
     // one chain per (fragment, query head): grouped query heads each run
-    // their state head's chain
+    // their state head's chain, except two query heads per state, which
+    // share one
     if (kda)
         return launch_chain<MODE_FWD_KDA, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.Hq,
                                                   (cudaStream_t)stream);
+    // two query heads per state: one chain per state head emits both
+    if (p.G == 2)
+        return launch_chain<MODE_FWD_G2, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.H,
+                                                 (cudaStream_t)stream);
     if (p.G > 1 || p.vfirst)
         return launch_chain<MODE_FWD_VAR, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.Hq,
                                                   (cudaStream_t)stream);
