@@ -23,8 +23,8 @@
 // exceeds 2^100 either way of row r takes exact per-term exponentials on the
 // CUDA cores instead.  One CTA per unit, two per SM: coalesced loads, column
 // scans, the gated tiles, the operands, the products and their epilogue;
-// then a second kernel solves T, one warp per unit with the scalar-gate
-// path's solver, many units per SM at once.
+// then a second kernel solves T, a pair of warps per unit with the
+// scalar-gate path's block solver, many units per SM at once.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -452,32 +452,40 @@ __global__ void __launch_bounds__(KP_THREADS, 2) tc_kda_prep_kernel(const __grid
     if (w == 0) tmem_dealloc(tmem, KP_TMEM_COLS);
 }
 
-// T = (I + A)^-1 of every unit, one warp per unit (persistent warps): A and
-// beta from the unit (written above) into this warp's scratch, then the
-// solver overwrites the unit's first three tiles with T', hi(T''), lo(T'').
-constexpr int KS_WARPS = 4;
+// T = (I + A)^-1 of every unit, a pair of warps per unit (persistent
+// pairs, four per CTA, three CTAs per SM): A and beta from the unit (written
+// above) into the pair's scratch, then the scalar-gate path's block solver
+// overwrites the unit's first three tiles with T', hi(T''), lo(T'').
+constexpr int KS_PAIRS = 4;
+constexpr int KS_WARPS = 2 * KS_PAIRS;
 constexpr size_t KS_SCRATCH = (size_t)C * kLS * 4 + 2 * C * 4;   // A, beta, ones
-__global__ void __launch_bounds__(32 * KS_WARPS) tc_kda_solve_kernel(uint8_t *wy, int n_units, float *tmat) {
+__global__ void __launch_bounds__(32 * KS_WARPS, 3) tc_kda_solve_kernel(uint8_t *wy, int n_units, float *tmat) {
     extern __shared__ __align__(16) uint8_t sms[];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float *S = reinterpret_cast<float *>(sms + w * KS_SCRATCH);
+    const int pr = w >> 1, role = w & 1;
+    const int bar_id = 1 + pr;   // named barrier of the pair
+    float *S = reinterpret_cast<float *>(sms + pr * KS_SCRATCH);
     float *beta = S + C * kLS, *one = beta + C;
-    one[lane] = 1.f;
-    one[32 + lane] = 1.f;
-    for (int unit = blockIdx.x * KS_WARPS + w; unit < n_units; unit += gridDim.x * KS_WARPS) {
+    if (role == 0) {
+        one[lane] = 1.f;
+        one[32 + lane] = 1.f;
+    }
+    for (int unit = blockIdx.x * KS_PAIRS + pr; unit < n_units; unit += gridDim.x * KS_PAIRS) {
         uint8_t *dst = wy + (size_t)unit * kKdaUnitBytes;
         const float4 *Ag = reinterpret_cast<const float4 *>(dst);
 #pragma unroll 4
-        for (int e = lane; e < C * C / 4; e += 32) {
+        for (int e = lane + 32 * role; e < C * C / 4; e += 64) {
             const int i = e / (C / 4), j = 4 * (e % (C / 4));
             *reinterpret_cast<float4 *>(S + i * kLS + j) = Ag[e];
         }
-        const float *bg = reinterpret_cast<const float *>(dst + 2 * kWyTileBytes);
-        beta[lane] = bg[lane];
-        beta[32 + lane] = bg[32 + lane];
-        __syncwarp();
-        solve_unit(S, dst, beta, one, tmat ? tmat + (size_t)unit * C * C : nullptr);
-        __syncwarp();
+        if (role == 0) {
+            const float *bg = reinterpret_cast<const float *>(dst + 2 * kWyTileBytes);
+            beta[lane] = bg[lane];
+            beta[32 + lane] = bg[32 + lane];
+        }
+        named_bar(bar_id, 64);   // A, beta (and the ones) in place; the unit's tiles read
+        solve_unit_pair(S, dst, beta, one, role, bar_id, tmat ? tmat + (size_t)unit * C * C : nullptr);
+        named_bar(bar_id, 64);   // the scratch has been read before the next unit's A
     }
 }
 
@@ -511,14 +519,14 @@ int launch_tc_kda_prep_t(const cpdr_ctx *c, const void *k, const void *q, const 
     kern<<<(unsigned)units, KP_THREADS, KP_SMEM, (cudaStream_t)stream>>>(prm);
     e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
-    const size_t ssm = KS_WARPS * KS_SCRATCH;
+    const size_t ssm = KS_PAIRS * KS_SCRATCH;   // one scratch per pair
     e = cudaFuncSetAttribute(tc_kda_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
     if (e != cudaSuccess) return (int)e;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 148;
-    const int64_t blocks = (units + KS_WARPS - 1) / KS_WARPS;
+    const int64_t blocks = (units + KS_PAIRS - 1) / KS_PAIRS;
     const int grid = (int)std::min<int64_t>(blocks, (int64_t)sms * 3);
     tc_kda_solve_kernel<<<grid, 32 * KS_WARPS, ssm, (cudaStream_t)stream>>>((uint8_t *)wy, (int)units, tmat);
     return (int)cudaGetLastError();
