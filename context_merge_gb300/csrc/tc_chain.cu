@@ -61,8 +61,9 @@ constexpr int NTHREADS = 512;
 // chunk form in reverse chunk order with the forward's warp roles and
 // stage layout (V's slots hold dO); MODE_BWD_ACC (bit 5) is its pass for a
 // state's query heads past the first.
-// MODE_FWD_G2 (bit 6) is the forward of two query heads per state (grouped
-// query heads, G = 2): one chain per state head emits both heads' outputs.
+// MODE_FWD_G2 (bit 6) is the forward of grouped query heads two at a time:
+// with an even group size G each chain emits two query heads' outputs (G/2
+// chains per state head).
 enum Mode { MODE_FWD = 0, MODE_PRE = 1, MODE_FWD_KDA = 2, MODE_PRE_KDA = 3, MODE_FWD_VAR = 4, MODE_REC = 9,
             MODE_REC_KDA = 11, MODE_BWD = 16, MODE_BWD_KDA = 18, MODE_BWD_ACC = 48, MODE_BWD_KDA_ACC = 50,
             MODE_FWD_G2 = 68 };
@@ -1431,9 +1432,10 @@ __device__ __forceinline__ void chain_body(uint8_t *base, const CUtensorMap *tq,
     r.hq = blockIdx.y;
     // the forward's grid runs over query heads; the backward's over state heads
     r.h = (mode_var(MODE) && !mode_bwd(MODE)) ? r.hq / p.G : r.hq;
-    if (mode_g2(MODE)) {   // the grid runs over state heads; this chain serves hq and hq + 1
-        r.h = blockIdx.y;
-        r.hq = 2 * r.h;
+    if (mode_g2(MODE)) {   // G/2 chains per state head; chain j serves query heads h G + 2j and + 1
+        const int pairs = p.G / 2;
+        r.h = blockIdx.y / pairs;
+        r.hq = r.h * p.G + 2 * (blockIdx.y % pairs);
     }
     r.n = (f.len + C - 1) / C;
     r.nlast = f.len - (r.n - 1) * C;
@@ -1660,14 +1662,14 @@ int launch_tc_fwd(const cpdr_ctx *c, const int32_t *items, int n_items, const vo
     prm.scale = p.scale;
     if (kda) prm.kda_qp = (const uint8_t *)wy + p.wy_chunks.size() * (size_t)p.H * kKdaUnitBytes;
     // one chain per (fragment, query head): grouped query heads each run
-    // their state head's chain, except two query heads per state, which
-    // share one
+    // their state head's chain, except with an even group size, where each
+    // chain serves two query heads
     if (kda)
         return launch_chain<MODE_FWD_KDA, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.Hq,
                                                   (cudaStream_t)stream);
-    // two query heads per state: one chain per state head emits both
-    if (p.G == 2)
-        return launch_chain<MODE_FWD_G2, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.H,
+    // an even number of query heads per state: each chain emits two of them
+    if (p.G % 2 == 0)
+        return launch_chain<MODE_FWD_G2, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)(p.H * (p.G / 2)),
                                                  (cudaStream_t)stream);
     if (p.G > 1 || p.vfirst)
         return launch_chain<MODE_FWD_VAR, ROLE_S>(tq, tk, tv, prm, (unsigned)n_items, (unsigned)p.Hq,

@@ -37,6 +37,7 @@ VARIANTS = {
     "vfirst": dict(state_v_first=True),
     "gqa2": dict(Hq=4),
     "gqa3-vfirst-zigzag": dict(Hq=6, layout="zigzag", state_v_first=True),
+    "gqa4": dict(Hq=8),
 }
 CUTS = [
     ([3000, 4000, 3240], 2),
