@@ -1,0 +1,324 @@
+"""A model of the forward chain kernel's synchronisation (csrc/tc_chain.cu),
+checked by randomised interleavings on the CPU.
+
+Each warp role (producer, MMA warp, mask warps, W/O epilogue warps, state
+warps with the issuing lane) is written as the sequence of mbarrier waits,
+arrivals, tensor-core products (asynchronous: their commits arrive when the
+product completes, in issue order per issuing thread, in any order across
+threads) and the shared-memory / TMEM accesses the kernel performs per
+chunk, in the kernel's order.  A random scheduler runs them to completion
+many times and fails on
+
+* a deadlock (no role can proceed),
+* a parity wait on a barrier that has already completed two phases past the
+  one waited for (the hardware would report the wrong phase), and
+* a data hazard: an access whose producer has not completed, or a write over
+  data a reader has not consumed (each access states what must have
+  happened before it).
+
+Every role (and the products of each issuing thread) gets a random speed
+for the whole schedule, so that one role lagging far behind the others is
+explored as well as fair interleavings.
+
+Models: the single-head forward (MODE_FWD) and the forward of two query
+heads per chain (MODE_FWD_G2: both heads' Q K^T in turn in the columns W^T
+uses, both heads' outputs in one accumulator).  The model is written from
+the kernel; it does not run it.  Each model is also run with one wait
+removed, which the checker must catch.
+"""
+import random
+from collections import defaultdict
+
+import pytest
+
+
+class Protocol:
+    """One random schedule of a set of role programs (generators of ops)."""
+
+    def __init__(self, progs, counts, seed):
+        self.rng = random.Random(seed)
+        self.progs = progs
+        self.counts = counts
+        # each role (and each thread's products) runs at a random speed for
+        # the whole schedule, so that one slow role lagging behind the rest
+        # is explored as well as fair interleavings
+        self.speed = {k: self.rng.choice([0.01, 0.1, 1.0]) for k in progs}
+
+    def run(self):
+        done, pend, acts, mdone = defaultdict(int), defaultdict(int), defaultdict(int), set()
+        cur = {k: next(g) for k, g in self.progs.items()}
+        inflight = defaultdict(list)
+        barwait = set()
+
+        def arrive(b):
+            pend[b] += 1
+            if pend[b] == self.counts.get(b, 1):
+                pend[b] = 0
+                done[b] += 1
+
+        while True:
+            runnable = []
+            for k, op in cur.items():
+                if op is None:
+                    continue
+                if op[0] == "wait":
+                    b, j = op[1], op[2]
+                    if done[b] >= j + 2:
+                        return f"barrier {b} two phases ahead of {k} (wants {j}, {done[b]} done)"
+                    if done[b] >= j + 1:
+                        runnable.append(k)
+                elif op[0] == "bar":
+                    if k not in barwait:
+                        runnable.append(k)
+                else:
+                    runnable.append(k)
+            # the state warps' named barrier
+            st = [k for k in cur if k.startswith("state") and cur[k] is not None]
+            if st and all(cur[k][0] == "bar" and k in barwait for k in st):
+                for k in st:
+                    barwait.discard(k)
+                    cur[k] = next(self.progs[k], None)
+                continue
+            choices = runnable + [("async", k) for k in inflight if inflight[k]]
+            if not choices:
+                if all(v is None for v in cur.values()):
+                    return None
+                return "deadlock: " + ", ".join(f"{k} at {v}" for k, v in cur.items() if v is not None)
+            c = self.rng.choices(choices, [self.speed[x[1] if isinstance(x, tuple) else x] for x in choices])[0]
+            if isinstance(c, tuple):   # the oldest product of that thread completes
+                label, bars = inflight[c[1]].pop(0)
+                mdone.add(label)
+                for b in bars:
+                    arrive(b)
+                continue
+            op = cur[c]
+            if op[0] == "bar":
+                barwait.add(c)
+                continue
+            if op[0] == "arrive":
+                arrive(op[1])
+            elif op[0] == "mma":
+                inflight[c].append((op[1], op[2]))
+            elif op[0] == "do":
+                acts[op[1]] += 1
+            elif op[0] == "need":
+                for cond in op[1]:
+                    if cond[0] == "mma" and cond[1] not in mdone:
+                        return f"hazard at {op[2]} ({c}): product {cond[1]} not complete"
+                    if cond[0] == "did" and acts[cond[1]] < cond[2]:
+                        return f"hazard at {op[2]} ({c}): {cond[1]} done by {acts[cond[1]]} of {cond[2]}"
+            cur[c] = next(self.progs[c], None)
+
+
+def counts(ns):
+    c = {("PFREE",): 2, ("WREADY",): 4, ("OFREE",): 4, ("MREADY",): 2, ("QREADY", 0): 2, ("QREADY", 1): 2,
+         ("DLREADY",): 8}
+    for s in range(ns):
+        c[("EMPTY", s)] = 2
+    return c
+
+
+def state_roles(n, NG, g2, skip):
+    """State warps 8..15; lane 0 of warp 8 issues Delta, O1, P_S and O2."""
+    def state(wi):
+        issuer = wi == 0
+        yield ("do", "put0")
+        yield ("bar",)
+        for ch in range(n):
+            if issuer:
+                yield ("wait", ("WREADY",), ch)
+                yield ("wait", ("UFULL",), ch)
+                yield ("need", [("did", f"wbw{ch}", 4), ("mma", f"U{ch}"), ("did", f"put{ch}", 8)], f"Delta {ch}")
+                yield ("mma", f"D{ch}", [("WBFREE",), ("DLFULL",)])
+                if ch >= 1 and skip != "OFREE":
+                    yield ("wait", ("OFREE",), ch - 1)
+                yield ("wait", ("QREADY", ch & 1), ch >> 1)
+                yield ("need", [("did", f"qscale{ch}", 2), ("did", f"put{ch}", 8)] +
+                       ([("did", f"oread{ch - 1}", 4)] if ch >= 1 else []), f"O1 {ch}")
+                yield ("mma", f"O1_{ch}", [])
+            yield ("wait", ("GATE", ch % NG), ch // NG)
+            yield ("wait", ("DLFULL",), ch)
+            yield ("need", [("mma", f"D{ch}")] + ([("mma", f"O2_{ch - 1}")] if ch >= 1 else []), f"Delta epilogue {ch}")
+            yield ("do", f"dlread{ch}")
+            yield ("do", f"dbw{ch}")
+            yield ("arrive", ("DLREADY",))
+            yield ("bar",)
+            if issuer:
+                yield ("need", [("did", f"dlread{ch}", 8), ("did", f"dbw{ch}", 8)], f"P_S {ch}")
+                yield ("mma", f"PS{ch}", [("PSFULL",)])
+                if skip != "MREADY":
+                    yield ("wait", ("MREADY",), ch)
+                yield ("need", [("did", f"maskw{ch}", 4 if g2 else 2), ("did", f"dbw{ch}", 8)], f"O2 {ch}")
+                yield ("mma", f"O2_{ch}", [("OFULL",), ("MFREE",)])
+                yield ("mma", f"E{ch}i", [("EMPTY", ch % (2 if g2 else 3))])
+            yield ("wait", ("PSFULL",), ch)
+            yield ("need", [("mma", f"PS{ch}"), ("mma", f"O1_{ch}")], f"state update {ch}")
+            yield ("do", f"put{ch + 1}")
+            yield ("bar",)
+    return {f"state{i}": state(i) for i in range(8)}
+
+
+def wepi_roles(n):
+    """W/O epilogue warps 4..7: W of chunk t+1 first, then O of chunk t."""
+    def wepi(wi):
+        def w_epi(t):
+            yield ("wait", ("WFULL",), t)
+            yield ("need", [("mma", f"W{t}")], f"W epilogue {t}")
+            yield ("do", f"wread{t}")
+            if t >= 1:
+                yield ("wait", ("WBFREE",), t - 1)
+            yield ("need", [("mma", f"D{t - 1}")] if t >= 1 else [], f"W tile {t}")
+            yield ("do", f"wbw{t}")
+            yield ("arrive", ("WREADY",))
+        yield from w_epi(0)
+        for t in range(n):
+            if t + 1 < n:
+                yield from w_epi(t + 1)
+            yield ("wait", ("OFULL",), t)
+            yield ("need", [("mma", f"O1_{t}"), ("mma", f"O2_{t}")], f"O epilogue {t}")
+            yield ("do", f"oread{t}")
+            yield ("arrive", ("OFREE",))
+    return {f"wepi{i}": wepi(i) for i in range(4)}
+
+
+def producer_role(n, NS, stage_reads):
+    NG = NS + 2
+
+    def producer():
+        yield ("arrive", ("GATE", 0))
+        for t in range(n):
+            if t >= NS:
+                yield ("wait", ("EMPTY", t % NS), t // NS - 1)
+                yield ("need", stage_reads(t - NS), f"load {t}")
+            yield ("do", f"load{t}")
+            yield ("arrive", ("FULL", t % NS))
+            if t + 1 < n:
+                yield ("arrive", ("GATE", (t + 1) % NG))
+    return producer()
+
+
+def single_head(n, skip=None):
+    NS, NG = 3, 5
+
+    def mma():
+        for t in range(n):
+            yield ("wait", ("FULL", t % NS), t // NS)
+            if t >= 1:
+                yield ("wait", ("WREADY",), t - 1)
+                yield ("wait", ("WBFREE",), t - 1)
+                if skip != "PFREE":
+                    yield ("wait", ("PFREE",), t - 1)
+            yield ("need", [("did", f"load{t}", 1)] + ([("did", f"pread{t - 1}", 2), ("did", f"wread{t - 1}", 4)]
+                                                       if t >= 1 else []), f"QK, W {t}")
+            yield ("mma", f"QK{t}", [("PFULL",)])
+            yield ("mma", f"W{t}", [("WFULL",)])
+            if t >= 1:
+                yield ("wait", ("DLREADY",), t - 1)
+            yield ("need", [("did", f"dlread{t - 1}", 8)] if t >= 1 else [], f"U {t}")
+            yield ("mma", f"U{t}", [("UFULL",), ("EMPTY", t % NS)])
+
+    def mask(wi):
+        for ch in range(n):
+            yield ("wait", ("GATE", ch % NG), ch // NG)
+            yield ("wait", ("PFULL",), ch)
+            yield ("need", [("mma", f"QK{ch}")], f"mask {ch}")
+            yield ("do", f"qscale{ch}")
+            yield ("arrive", ("QREADY", ch & 1))
+            yield ("do", f"pread{ch}")
+            yield ("arrive", ("PFREE",))
+            if ch >= 1:
+                yield ("wait", ("MFREE",), ch - 1)
+            yield ("need", [("mma", f"O2_{ch - 1}")] if ch >= 1 else [], f"mask tile {ch}")
+            yield ("do", f"maskw{ch}")
+            yield ("arrive", ("MREADY",))
+
+    def reads(u):
+        return [("mma", x) for x in (f"QK{u}", f"W{u}", f"U{u}", f"O1_{u}", f"PS{u}")]
+
+    progs = {"prod": producer_role(n, NS, reads), "mma": mma()}
+    progs.update({f"mask{i}": mask(i) for i in range(2)})
+    progs.update(wepi_roles(n))
+    progs.update(state_roles(n, NG, False, skip))
+    return progs, counts(NS)
+
+
+def two_heads(n, skip=None):
+    NS, NG = 2, 4
+
+    def mma():
+        for t in range(n):
+            yield ("wait", ("FULL", t % NS), t // NS)
+            if t >= 1:
+                yield ("wait", ("WBFREE",), t - 1)
+                if skip != "PFREE1":
+                    yield ("wait", ("PFREE",), 2 * t - 1)
+            yield ("need", [("did", f"load{t}", 1)] + ([("did", f"pread1_{t - 1}", 2)] if t >= 1 else []), f"W {t}")
+            yield ("mma", f"W{t}", [("WFULL",)])
+            if t >= 1:
+                yield ("wait", ("DLREADY",), t - 1)
+            yield ("need", [("did", f"dlread{t - 1}", 8)] if t >= 1 else [], f"U {t}")
+            yield ("mma", f"U{t}", [("UFULL",)])
+            if skip != "WREADY":
+                yield ("wait", ("WREADY",), t)
+            yield ("need", [("did", f"wread{t}", 4)], f"Q0 K^T {t}")
+            yield ("mma", f"QK0_{t}", [("PFULL",)])
+            if skip != "PFREE0":
+                yield ("wait", ("PFREE",), 2 * t)
+            yield ("need", [("did", f"pread0_{t}", 2)], f"Q1 K^T {t}")
+            yield ("mma", f"QK1_{t}", [("PFULL",)])
+            yield ("mma", f"E{t}", [("EMPTY", t % NS)])
+
+    def mask(wi):
+        for ch in range(n):
+            yield ("wait", ("GATE", ch % NG), ch // NG)
+            for hh in range(2):
+                yield ("wait", ("PFULL",), 2 * ch + hh)
+                yield ("need", [("mma", f"QK{hh}_{ch}")], f"mask {hh} {ch}")
+                if hh == 1:
+                    yield ("need", [("mma", f"QK0_{ch}"), ("mma", f"QK1_{ch}")], f"Q scaling {ch}")
+                    yield ("do", f"qscale{ch}")
+                    yield ("arrive", ("QREADY", ch & 1))
+                yield ("do", f"pread{hh}_{ch}")
+                yield ("arrive", ("PFREE",))
+                if hh == 0 and ch >= 1:
+                    yield ("wait", ("MFREE",), ch - 1)
+                yield ("need", [("mma", f"O2_{ch - 1}")] if ch >= 1 else [], f"mask tile {hh} {ch}")
+                yield ("do", f"maskw{ch}")
+            yield ("arrive", ("MREADY",))
+
+    def reads(u):
+        return [("mma", x) for x in (f"W{u}", f"U{u}", f"QK0_{u}", f"QK1_{u}", f"O1_{u}", f"PS{u}")] + \
+               [("did", f"qscale{u}", 2)]
+
+    progs = {"prod": producer_role(n, NS, reads), "mma": mma()}
+    progs.update({f"mask{i}": mask(i) for i in range(2)})
+    progs.update(wepi_roles(n))
+    progs.update(state_roles(n, NG, True, skip))
+    return progs, counts(NS)
+
+
+MODELS = {"single_head": single_head, "two_heads": two_heads}
+MUTATIONS = {"single_head": ["PFREE", "OFREE", "MREADY"],
+             "two_heads": ["PFREE0", "PFREE1", "WREADY", "OFREE", "MREADY"]}
+
+
+def failures(model, skip, seeds):
+    out = []
+    for n in (1, 2, 3, 4, 7):
+        for seed in range(seeds):
+            progs, cnt = MODELS[model](n, skip)
+            e = Protocol(progs, cnt, seed).run()
+            if e:
+                out.append((n, seed, e))
+    return out
+
+
+@pytest.mark.parametrize("model", list(MODELS))
+def test_protocol_has_no_deadlock_or_hazard(model):
+    bad = failures(model, None, 120)
+    assert not bad, bad[:3]
+
+
+@pytest.mark.parametrize("model,skip", [(m, s) for m in MODELS for s in MUTATIONS[m]])
+def test_checker_catches_a_missing_wait(model, skip):
+    assert failures(model, skip, 120), f"removing the {skip} wait went unnoticed"
