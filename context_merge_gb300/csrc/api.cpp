@@ -52,16 +52,12 @@ void free_tables(cpdr::DeviceTables &t) {
 }
 
 void free_streams(cpdr_ctx *c) {
-    for (void *e : {c->ev_fork, c->ev_join})
-        if (e) cudaEventDestroy((cudaEvent_t)e);
     for (void *&e : c->host_ev) {
         if (e) cudaEventDestroy((cudaEvent_t)e);
         e = nullptr;
     }
-    if (c->aux_stream) cudaStreamDestroy((cudaStream_t)c->aux_stream);
     if (c->copy_stream) cudaStreamDestroy((cudaStream_t)c->copy_stream);
     if (c->out_stream) cudaStreamDestroy((cudaStream_t)c->out_stream);
-    c->aux_stream = c->ev_fork = c->ev_join = nullptr;
     c->copy_stream = c->out_stream = nullptr;
 }
 
@@ -170,16 +166,6 @@ cpdr_status cpdr_ctx_create(const cpdr_desc *desc, cpdr_ctx **out) {
         if (e == cudaSuccess) e = upload(&t.conv_halo, p.conv_halo);
         if (e == cudaSuccess) e = cudaMalloc((void **)&t.status, 64);
         if (e == cudaSuccess) e = cudaMemset(t.status, 0, 64);
-        if (e == cudaSuccess && c->use_tc) {
-            cudaStream_t aux = nullptr;
-            cudaEvent_t ef = nullptr, ej = nullptr;
-            e = cudaStreamCreateWithFlags(&aux, cudaStreamNonBlocking);
-            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ef, cudaEventDisableTiming);
-            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ej, cudaEventDisableTiming);
-            c->aux_stream = aux;
-            c->ev_fork = ef;
-            c->ev_join = ej;
-        }
         if (e == cudaSuccess) {
             cudaStream_t cs = nullptr, os = nullptr;
             e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);

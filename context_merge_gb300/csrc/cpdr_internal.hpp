@@ -140,10 +140,6 @@ struct cpdr_ctx {
     bool has_device = false;
     bool use_tc = false;        // tcgen05 kernels for the bf16, d = 128 path
     int device = -1;
-    // second stream for the pre-process's M chains, forked from and joined
-    // back into the caller's stream with two events (created with the context)
-    void *aux_stream = nullptr;
-    void *ev_fork = nullptr, *ev_join = nullptr;
     // host-buffer path: a copy stream for the host-to-device copies and the
     // events that let compute start on the inputs that have arrived
     void *copy_stream = nullptr, *out_stream = nullptr;

@@ -130,12 +130,11 @@ extern "C" cpdr_status cpdr_forward_noalloc(const cpdr_ctx *c, const void *q, co
     // Run the three stages on a view of the context that points at the
     // array's tables: the view shares the caller's plan and leaves the
     // caller's context untouched.  Every stage runs on the caller's stream
-    // (the view has no second stream of its own).
+    // (the view has no copy streams of its own).
     cpdr_ctx view(*c);
     view.dev = t;
     view.has_device = true;
     view.device = dev;
-    view.aux_stream = view.ev_fork = view.ev_join = nullptr;
     view.copy_stream = view.out_stream = nullptr;
     for (void *&ev : view.host_ev) ev = nullptr;
     cpdr_status s = cpdr_wy_build(&view, q, k, beta, gate, wy, stream);

@@ -33,6 +33,8 @@
 // that makes every other wait fall through, drains its MMAs and loads, frees
 // TMEM and returns.
 #include <cuda.h>
+
+#include <algorithm>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -1495,6 +1497,22 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     chain_body<MODE, ROLE>(base, &tq, &tk, &tv, p, blockIdx.x);
 }
 
+// The pre-process as one launch: blockIdx.z = 0 runs the transfer-matrix (M)
+// chains, 1 the S chains.  Blocks are dispatched in grid order, so every M
+// chain (the longer kind) starts before the S chains, which then fill the
+// SMs the M chains leave: longest first within one launch.
+template <int MODE>
+__global__ void __launch_bounds__(NTHREADS, 1)
+tc_pre_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+              const __grid_constant__ Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    if (blockIdx.z == 0)
+        chain_body<MODE, ROLE_M>(base, &tk, &tk, &tv, p, blockIdx.x);
+    else
+        chain_body<MODE, ROLE_S>(base, &tk, &tk, &tv, p, blockIdx.x);
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -1562,6 +1580,16 @@ static_assert(make_lay(MODE_BWD_KDA, ROLE_S).total == make_lay(MODE_FWD_KDA, ROL
 
 size_t smem_for(int mode, int role) { return make_lay(mode, role).total + 1024; }
 
+template <int MODE>
+int launch_pre_pair(const CUtensorMap &tk, const CUtensorMap &tv, const Params &prm, unsigned items, unsigned H,
+                    cudaStream_t st) {
+    const size_t sm = std::max(smem_for(MODE, ROLE_S), smem_for(MODE, ROLE_M));
+    cudaError_t e = cudaFuncSetAttribute(tc_pre_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return (int)e;
+    tc_pre_kernel<MODE><<<dim3(items, H, 2), NTHREADS, sm, st>>>(tk, tv, prm);
+    return (int)cudaGetLastError();
+}
+
 template <int MODE, int ROLE>
 int launch_chain(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const Params &prm,
                  unsigned items, unsigned H, cudaStream_t st) {
@@ -1610,29 +1638,11 @@ int launch_tc_pre(const cpdr_ctx *c, const void *k, const void *v, const float *
     prm.G = 1;
     prm.vfirst = p.vfirst;
     prm.scale = p.scale;
-    // the S chains and the transfer-matrix chains, one kernel each; the M
-    // chains run on the context's second stream (forked from and joined back
-    // into the caller's), so each kernel's last wave overlaps the other's
-    cudaStream_t st = (cudaStream_t)stream;
-    cudaStream_t aux = (cudaStream_t)c->aux_stream;
-    if (aux) {
-        cudaError_t e = cudaEventRecord((cudaEvent_t)c->ev_fork, st);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(aux, (cudaEvent_t)c->ev_fork, 0);
-        if (e != cudaSuccess) return (int)e;
-    }
+    // the transfer-matrix chains and the S chains in one launch, the longer
+    // M chains dispatched first
     const unsigned items = (unsigned)p.pre_items.size(), H = (unsigned)p.H;
-    int rc = kda ? launch_chain<MODE_PRE_KDA, ROLE_M>(tk, tk, tv, prm, items, H, aux ? aux : st)
-                 : launch_chain<MODE_PRE, ROLE_M>(tk, tk, tv, prm, items, H, aux ? aux : st);
-    if (rc) return rc;
-    rc = kda ? launch_chain<MODE_PRE_KDA, ROLE_S>(tk, tk, tv, prm, items, H, st)
-             : launch_chain<MODE_PRE, ROLE_S>(tk, tk, tv, prm, items, H, st);
-    if (rc) return rc;
-    if (aux) {
-        cudaError_t e = cudaEventRecord((cudaEvent_t)c->ev_join, aux);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, (cudaEvent_t)c->ev_join, 0);
-        if (e != cudaSuccess) return (int)e;
-    }
-    return 0;
+    return kda ? launch_pre_pair<MODE_PRE_KDA>(tk, tv, prm, items, H, (cudaStream_t)stream)
+               : launch_pre_pair<MODE_PRE>(tk, tv, prm, items, H, (cudaStream_t)stream);
 }
 
 int launch_tc_fwd(const cpdr_ctx *c, const int32_t *items, int n_items, const void *q, const void *k, const void *v,
