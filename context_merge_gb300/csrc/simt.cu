@@ -660,8 +660,9 @@ int launch_merge(const cpdr_ctx *c, const float *S_ext, const float *M, float *S
 int launches_per_step(const cpdr_ctx *c) {
     const auto &p = c->plan;
     int n = 0;
-    n += (c->use_tc && !p.wy_chunks.empty()) ? 1 : 0;   // WY build (tensor-core path)
-    n += p.pre_items.empty() ? 0 : (c->use_tc ? 2 : 1);   // pre-process (S and M kernels on the tensor-core path)
+    // WY build (tensor-core path; the per-dim gate's preparation and solve)
+    n += (c->use_tc && !p.wy_chunks.empty()) ? (p.gate_kind == CPDR_GATE_PER_DIM ? 2 : 1) : 0;
+    n += p.pre_items.empty() ? 0 : 1;          // pre-process (S and M chains in one launch on the tensor cores)
     n += p.zero_pre.empty() ? 0 : 2;           // zero S_ext and M
     n += p.zero_init.empty() ? 0 : 1;          // zero S_init
     n += p.chains.empty() ? 0 : 1;             // merge
