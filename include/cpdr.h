@@ -44,15 +44,13 @@
  * Memory.  Every tensor argument is a DEVICE pointer owned by the caller, and
  *          must be 16-byte aligned.  The library owns only the cpdr_ctx
  *          (host tables plus small device metadata allocated at create,
- *          two copy streams and twelve events for cpdr_forward_host, and on
- *          the tensor-core path one more stream and two events).
+ *          and two copy streams and twelve events for cpdr_forward_host).
  *          No call below allocates device memory.
- * Streams. cpdr_preprocess forks its M-chain kernel onto the context's
- *          internal stream and joins it back into `stream` before returning
- *          (event record / wait), so ordering on `stream` is as if it ran
- *          there; a context must not be used from two host threads at once.
  * Streams. `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *          stream).  Calls enqueue work and return; they never synchronise.
+ *          Every stage runs on `stream` (cpdr_forward_host also uses the
+ *          context's copy streams, ordered against `stream` by events); a
+ *          context must not be used from two host threads at once.
  * Errors.  Every call validates its arguments on the host before any
  *          launch and returns a cpdr_status; on failure nothing is launched
  *          and cpdr_last_error() gives a message (thread-local).  Launch
