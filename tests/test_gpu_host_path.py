@@ -18,15 +18,16 @@ def _cuda(cpdr_lib):
     torch.cuda.set_device(0)
 
 
-@pytest.mark.parametrize("name,T,H", [("gdn_bf16_b2_t8192_h16_d128_r8", 4096, 4),
-                                      ("kda_bf16_t32768_h32_d128_r16", 4096, 4),
-                                      ("gdn_fp32_t1024_h2_d64_r4", 1024, 2),
-                                      ("gdn_bf16_varlen65536_n12_h16_d128_r32", 65536, 2)])
-def test_host_path_matches_device_path(name, T, H):
+@pytest.mark.parametrize("name,T,H,Hq", [("gdn_bf16_b2_t8192_h16_d128_r8", 4096, 4, None),
+                                         ("gdn_bf16_b2_t8192_h16_d128_r8", 4096, 4, 8),   # two query heads per chain
+                                         ("kda_bf16_t32768_h32_d128_r16", 4096, 4, None),
+                                         ("gdn_fp32_t1024_h2_d64_r4", 1024, 2, None),
+                                         ("gdn_bf16_varlen65536_n12_h16_d128_r32", 65536, 2, None)])
+def test_host_path_matches_device_path(name, T, H, Hq):
     w = inputs.WORKLOADS[name]
-    inp = inputs.make_inputs(w, device="cpu", T=T, H=H)
+    inp = inputs.make_inputs(w, device="cpu", T=T, H=H, Hq=Hq)
     B, T, d, R = inp["B"], inp["T"], inp["d"], inp["R"]
-    ctx = cpdr.Context(B, T, H, d, R, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"])
+    ctx = cpdr.Context(B, T, H, d, R, gate=w.gate, dtype=w.dtype, cu_seqlens=inp["cu_seqlens"], Hq=inp["Hq"])
     dev = {k: inp[k].cuda() for k in ("q", "k", "v", "beta", "g")}
     o_dev, bufs = ctx.run(dev["q"], dev["k"], dev["v"], dev["beta"], dev["g"])
     host = {k: inp[k].contiguous().pin_memory() for k in ("q", "k", "v", "beta", "g")}

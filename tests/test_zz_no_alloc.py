@@ -23,6 +23,7 @@ pytestmark = pytest.mark.gpu
 CASES = [
     # (workload, overrides, tolerance kind)
     ("gdn_bf16_b2_t8192_h16_d128_r8", dict(B=1, T=2048, H=4), "bf16"),     # tcgen05 kernels
+    ("gdn_bf16_b2_t8192_h16_d128_r8", dict(B=1, T=2048, H=4, Hq=8), "bf16"),  # two query heads per chain
     ("gdn_bf16_varlen65536_n12_h16_d128_r32", dict(lengths=[700, 1100, 248]), "bf16"),
     ("kda_bf16_t32768_h32_d128_r16", dict(T=2048, H=2, R=4), "bf16"),       # per-dim gate
     ("kda_bf16_t32768_h32_d128_r16", dict(T=2048, H=2, R=4, Hq=4), "bf16"),  # and grouped query heads
