@@ -289,14 +289,12 @@ __device__ __forceinline__ uint32_t gate_parity(int c) { return (uint32_t)(c / (
 
 __device__ __forceinline__ int rows_of(const Run &r, int chunk) { return chunk == r.n - 1 ? r.nlast : C; }
 
-// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, then
-// every lane performs its own (now immediate) acquire.
+// Warp-uniform bounded wait: every lane waits (and acquires) itself, and
+// the warp leaves with one verdict (a lane whose bounded wait gave up makes
+// the whole warp give up).
 __device__ __forceinline__ bool warp_wait(const Run &r, int b, uint32_t parity, int site) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(&r.bar[b], parity, r.ctl, r.p->status, site) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_try_wait(&r.bar[b], parity);
-    return ok != 0;
+    const bool ok = mbar_wait(&r.bar[b], parity, r.ctl, r.p->status, site);
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // ------------------------------------------------------------------ bf16 row stores
