@@ -289,12 +289,9 @@ __device__ __forceinline__ uint32_t gate_parity(int c) { return (uint32_t)(c / (
 
 __device__ __forceinline__ int rows_of(const Run &r, int chunk) { return chunk == r.n - 1 ? r.nlast : C; }
 
-// Warp-uniform bounded wait: every lane waits (and acquires) itself, and
-// the warp leaves with one verdict (a lane whose bounded wait gave up makes
-// the whole warp give up).
+// Warp-uniform bounded wait on barrier b of the CTA.
 __device__ __forceinline__ bool warp_wait(const Run &r, int b, uint32_t parity, int site) {
-    const bool ok = mbar_wait(&r.bar[b], parity, r.ctl, r.p->status, site);
-    return __all_sync(0xffffffffu, ok) != 0;
+    return warp_wait_all(&r.bar[b], parity, r.ctl, r.p->status, site);
 }
 
 // ------------------------------------------------------------------ bf16 row stores

@@ -37,18 +37,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Non-blocking test of phase `parity` (never suspends the thread).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 // Same as mbar_try_wait, but the thread may stay suspended (not issuing) for up to `ns`
 // nanoseconds while the phase is incomplete; it resumes when the phase completes.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
@@ -101,30 +89,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Ctl *c
     return mbar_wait_slow(bar, parity, ctl, status, site);
 }
 
-// Bounded wait for a single thread on a latency-critical path: polls with
-// the non-suspending test (a suspended thread resumes several hundred
-// cycles after the phase completes), checking the clock and the abort flag
-// every 256 polls.  Same failure behaviour as mbar_wait.
-static __device__ __noinline__ bool mbar_poll_slow(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
-    const long long t0 = clock64();
-    for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 256; i++)
-            if (mbar_test_wait(bar, parity)) return true;
-        if (ctl->abort) return false;
-        if (clock64() - t0 > kWaitCycles) {
-            if (atomicCAS(status, 0, 1) == 0) {
-                status[1] = site;
-                status[2] = (int32_t)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
-            }
-            ctl->abort = 1;
-            return false;
-        }
-    }
-}
-__device__ __forceinline__ bool mbar_poll(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
-    if (mbar_test_wait(bar, parity)) return true;
-    return mbar_poll_slow(bar, parity, ctl, status, site);
+// Warp-uniform bounded wait: every lane waits (and acquires) itself and the
+// warp leaves with one verdict (a lane whose bounded wait gave up makes the
+// whole warp give up).  Measured in the chain kernels: a lane-0 wait, a
+// broadcast and a second wait by every lane cost about 300 cycles even on a
+// completed phase.
+__device__ __forceinline__ bool warp_wait_all(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
+    const bool ok = mbar_wait(bar, parity, ctl, status, site);
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // ------------------------------------------------------------------ fences

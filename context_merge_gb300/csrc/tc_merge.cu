@@ -75,14 +75,9 @@ struct MergeArgs {
     int rev;          // 1: the reverse merge (M_j^T, chain walked from r1 down)
 };
 
-// Warp-uniform bounded wait: lane 0 waits, the verdict is broadcast, and
-// every lane then observes the completed phase itself.
+// Warp-uniform bounded wait.
 __device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, ctl, status, site) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_try_wait(bar, parity);
-    return ok != 0;
+    return warp_wait_all(bar, parity, ctl, status, site);
 }
 
 // bf16 hi/lo of two values, packed (lower column in the low half)

@@ -78,13 +78,9 @@ __device__ __forceinline__ WyGates wy_gates(uint8_t *base, int slot, int unit) {
     return WyGates{q, q + 64, q + 128, q + 192, q + 256, q + 320};
 }
 
-// Warp-uniform bounded wait (lane 0 polls, the verdict is broadcast).
+// Warp-uniform bounded wait.
 __device__ __forceinline__ bool wy_warp_wait(uint64_t *bar, uint32_t parity, Ctl *ctl, int32_t *status, int site) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, ctl, status, site) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_try_wait(bar, parity);
-    return ok != 0;
+    return warp_wait_all(bar, parity, ctl, status, site);
 }
 
 // beta and log2 gates of rows 2*lane, 2*lane+1 of a unit (padded rows: 0)
