@@ -1,6 +1,6 @@
-// Solves of the per-chunk WY inverse T = (I + A)^-1: one warp per unit (the
-// per-dim-gate preparation, tc_kda.cu) or a pair of warps per unit (the WY
-// build of the scalar-gate path, tc_wy.cu).
+// Solve of the per-chunk WY inverse T = (I + A)^-1 by a pair of warps per
+// unit (the WY build of the scalar-gate path, tc_wy.cu, and the per-dim
+// gate's solve kernel, tc_kda.cu).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -55,57 +55,6 @@ __device__ __forceinline__ void store_tiles(const float *S, uint8_t *dst, const 
         *reinterpret_cast<uint4 *>(dst + kWyTileBytes + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4 *>(dst + 2 * kWyTileBytes + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-}
-
-// One warp: T = (I + A)^-1 of the 64 x 64 unit lower-triangular matrix whose
-// strictly lower part A is in S[64][68] (zeros elsewhere), by rows:
-//   T_ij = delta_ij - sum_{k < i} A_ik T_kj.
-// Lane l keeps x1[i] = T_il (i = 0..63) and x2[m] = T_{32+m, 32+l} (m = 0..31;
-// T_{i, 32+l} = 0 for i < 32).  Then writes T' = T diag(beta) and
-// T'' = T diag(beta gamma) (hi, lo) as bf16 into the unit's three tiles,
-// reusing S (which it overwrites) to turn columns into rows.
-__device__ __forceinline__ void solve_unit(float *S, uint8_t *dst, const float *beta, const float *gam,
-                                           float *tdst = nullptr) {
-    const int l = threadIdx.x & 31;
-    float x1[64], x2[32];
-#pragma unroll
-    for (int i = 0; i < 64; i++) {
-        float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k4 = 0; k4 < 16; k4++) {   // constant trip count: x1, x2 stay in registers
-            if (4 * k4 >= i) break;
-            const float4 a = *reinterpret_cast<const float4 *>(S + i * kLS + 4 * k4);
-            const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int k = 4 * k4 + e;
-                if (k < i) {
-                    a1[e] = fmaf(av[e], x1[k], a1[e]);
-                    if (k >= 32) a2[e] = fmaf(av[e], x2[k - 32], a2[e]);
-                }
-            }
-        }
-        x1[i] = (i == l ? 1.f : 0.f) - ((a1[0] + a1[1]) + (a1[2] + a1[3]));
-        if (i >= 32) x2[i - 32] = (i - 32 == l ? 1.f : 0.f) - ((a2[0] + a2[1]) + (a2[2] + a2[3]));
-    }
-    // T goes back through the scratch (every A row has been read): lane l
-    // writes columns l and 32 + l, then the rows leave as 16-byte pieces
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 64; i++) {
-        S[i * kLS + l] = x1[i];
-        if (i >= 32) S[i * kLS + 32 + l] = x2[i - 32];
-    }
-    __syncwarp();
-    if (tdst) {   // T as fp32 64 x 64 (A's upper part, zero, above the diagonal blocks)
-#pragma unroll 4
-        for (int i = 0; i < 64; i++) {
-            tdst[i * 64 + l] = S[i * kLS + l];
-            tdst[i * 64 + 32 + l] = S[i * kLS + 32 + l];
-        }
-    }
-    store_tiles(S, dst, beta, gam, 0, 16);
-    __syncwarp();   // the scratch has been read before the caller reuses it
 }
 
 // Two warps (role 0 and 1, meeting at named barrier `bar_id`) solve one unit
