@@ -20,9 +20,15 @@ Every role (and the products of each issuing thread) gets a random speed
 for the whole schedule, so that one role lagging far behind the others is
 explored as well as fair interleavings.
 
-Models: the single-head forward (MODE_FWD) and the forward of two query
-heads per chain (MODE_FWD_G2: both heads' Q K^T in turn in the columns W^T
-uses, both heads' outputs in one accumulator).  The model is written from
+A mutation removes every wait on one barrier in the roles it names (for
+the pre-process's WBFREE, both the MMA warp's and the W epilogue's: each
+alone keeps the W tile from being rewritten while Delta reads it).
+
+Models: the single-head forward (MODE_FWD), the forward of two query heads
+per chain (MODE_FWD_G2: both heads' Q K^T in turn in the columns W^T uses,
+both heads' outputs in one accumulator), and the pre-process's S and M
+chains (MODE_PRE: a non-state warp issuing Delta and P_S inside the state
+warps' named barrier).  The model is written from
 the kernel; it does not run it.  Each model is also run with one wait
 removed, which the checker must catch.
 """
@@ -297,9 +303,91 @@ def two_heads(n, skip=None):
     return progs, counts(NS)
 
 
-MODELS = {"single_head": single_head, "two_heads": two_heads}
+def preprocess(n, skip=None, role_s=True):
+    """The pre-process chains (MODE_PRE, S role with U = T'V, M role with
+    U = 0): lane 0 of warp 2 issues Delta and P_S and joins the state warps'
+    named barrier; the MMA warp issues W (and U after the previous P_S)."""
+    NS, NG = 3, 5
+
+    def mma():
+        for t in range(n):
+            yield ("wait", ("FULL", t % NS), t // NS)
+            if t >= 1:
+                yield ("wait", ("WREADY",), t - 1)
+                if skip != "WBFREE":   # W behind the chain's Delta (which then has read the W tile)
+                    yield ("wait", ("WBFREE",), t - 1)
+            yield ("need", [("did", f"load{t}", 1)] + ([("did", f"wread{t - 1}", 4)] if t >= 1 else []), f"W {t}")
+            yield ("mma", f"W{t}", [("WFULL",)] + ([] if role_s else [("EMPTY", t % NS)]))
+            if role_s:
+                if t >= 1:
+                    yield ("wait", ("DLREADY",), t - 1)
+                    yield ("wait", ("PSFULL",), t - 1)   # scheduling: U behind the previous P_S
+                yield ("need", [("did", f"dlread{t - 1}", 8)] if t >= 1 else [], f"U {t}")
+                yield ("mma", f"U{t}", [("UFULL",), ("EMPTY", t % NS)])
+
+    def wepi(wi):
+        for t in range(n):
+            yield ("wait", ("WFULL",), t)
+            yield ("need", [("mma", f"W{t}")], f"W epilogue {t}")
+            yield ("do", f"wread{t}")
+            if t >= 1 and skip != "WBFREE":
+                yield ("wait", ("WBFREE",), t - 1)
+            yield ("need", [("mma", f"D{t - 1}")] if t >= 1 else [], f"W tile {t}")
+            yield ("do", f"wbw{t}")
+            yield ("arrive", ("WREADY",))
+
+    def issuer():
+        yield ("bar",)
+        for ch in range(n):
+            if skip != "WREADY":
+                yield ("wait", ("WREADY",), ch)
+            if role_s and skip != "UFULL":
+                yield ("wait", ("UFULL",), ch)
+            yield ("need", [("did", f"wbw{ch}", 4), ("did", f"put{ch}", 8)] + ([("mma", f"U{ch}")] if role_s else []),
+                   f"Delta {ch}")
+            yield ("mma", f"D{ch}", [("WBFREE",), ("DLFULL",)])
+            yield ("bar",)
+            yield ("need", [("did", f"dbw{ch}", 8), ("did", f"dlread{ch}", 8)] +
+                   ([("did", f"psread{ch - 1}", 8)] if ch >= 1 else []), f"P_S {ch}")
+            yield ("mma", f"PS{ch}", [("PSFULL",), ("EMPTY", ch % NS)])
+            yield ("bar",)
+
+    def state(wi):
+        yield ("do", "put0")
+        yield ("bar",)
+        for ch in range(n):
+            yield ("wait", ("GATE", ch % NG), ch // NG)
+            yield ("wait", ("DLFULL",), ch)
+            yield ("need", [("mma", f"D{ch}")] + ([("mma", f"PS{ch - 1}")] if ch >= 1 else []), f"Delta epilogue {ch}")
+            yield ("do", f"dlread{ch}")
+            yield ("do", f"dbw{ch}")
+            if role_s:
+                yield ("arrive", ("DLREADY",))
+            yield ("bar",)
+            yield ("wait", ("PSFULL",), ch)
+            yield ("need", [("mma", f"PS{ch}"), ("mma", f"D{ch}")], f"state update {ch}")
+            yield ("do", f"psread{ch}")
+            yield ("do", f"put{ch + 1}")
+            yield ("bar",)
+
+    def reads(u):
+        return [("mma", x) for x in ([f"W{u}", f"PS{u}"] + ([f"U{u}"] if role_s else []))]
+
+    progs = {"prod": producer_role(n, NS, reads), "mma": mma(), "state_issuer": issuer()}
+    progs.update({f"wepi{i}": wepi(i) for i in range(4)})
+    progs.update({f"state{i}": state(i) for i in range(8)})
+    return progs, counts(NS)
+
+
+def preprocess_m(n, skip=None):
+    return preprocess(n, skip, role_s=False)
+
+
+MODELS = {"single_head": single_head, "two_heads": two_heads, "pre_s": preprocess, "pre_m": preprocess_m}
 MUTATIONS = {"single_head": ["PFREE", "OFREE", "MREADY"],
-             "two_heads": ["PFREE0", "PFREE1", "WREADY", "OFREE", "MREADY"]}
+             "two_heads": ["PFREE0", "PFREE1", "WREADY", "OFREE", "MREADY"],
+             "pre_s": ["WBFREE", "UFULL", "WREADY"],
+             "pre_m": ["WBFREE", "WREADY"]}
 
 
 def failures(model, skip, seeds):
