@@ -24,7 +24,8 @@ A mutation removes every wait on one barrier in the roles it names (for
 the pre-process's WBFREE, both the MMA warp's and the W epilogue's: each
 alone keeps the W tile from being rewritten while Delta reads it).
 
-Models: the single-head forward (MODE_FWD), the forward of two query heads
+Models: the single-head forward (MODE_FWD) and its per-dim-gate form
+(MODE_FWD_KDA: pre-gated Qg and P tiles with the stage), the forward of two query heads
 per chain (MODE_FWD_G2: both heads' Q K^T in turn in the columns W^T uses,
 both heads' outputs in one accumulator), and the pre-process's S and M
 chains (MODE_PRE: a non-state warp issuing Delta and P_S inside the state
@@ -124,8 +125,11 @@ def counts(ns):
     return c
 
 
-def state_roles(n, NG, g2, skip):
-    """State warps 8..15; lane 0 of warp 8 issues Delta, O1, P_S and O2."""
+def state_roles(n, NG, g2, skip, NS=None, kda=False):
+    """State warps 8..15; lane 0 of warp 8 issues Delta, O1, P_S and O2.
+    Per-dim gate: no gate slots (the decay comes with the stage, copied out
+    in the Delta epilogue)."""
+    NS = NS or (2 if g2 else 3)
     def state(wi):
         issuer = wi == 0
         yield ("do", "put0")
@@ -142,11 +146,15 @@ def state_roles(n, NG, g2, skip):
                 yield ("need", [("did", f"qscale{ch}", 2), ("did", f"put{ch}", 8)] +
                        ([("did", f"oread{ch - 1}", 4)] if ch >= 1 else []), f"O1 {ch}")
                 yield ("mma", f"O1_{ch}", [])
-            yield ("wait", ("GATE", ch % NG), ch // NG)
+            if not kda:
+                yield ("wait", ("GATE", ch % NG), ch // NG)
             yield ("wait", ("DLFULL",), ch)
             yield ("need", [("mma", f"D{ch}")] + ([("mma", f"O2_{ch - 1}")] if ch >= 1 else []), f"Delta epilogue {ch}")
             yield ("do", f"dlread{ch}")
             yield ("do", f"dbw{ch}")
+            if kda and wi == 0:   # warp 8 keeps the chunk's decay past the stage's release
+                yield ("need", [("did", f"load{ch}", 1)], f"decay copy {ch}")
+                yield ("do", f"gcopy{ch}")
             yield ("arrive", ("DLREADY",))
             yield ("bar",)
             if issuer:
@@ -156,7 +164,7 @@ def state_roles(n, NG, g2, skip):
                     yield ("wait", ("MREADY",), ch)
                 yield ("need", [("did", f"maskw{ch}", 4 if g2 else 2), ("did", f"dbw{ch}", 8)], f"O2 {ch}")
                 yield ("mma", f"O2_{ch}", [("OFULL",), ("MFREE",)])
-                yield ("mma", f"E{ch}i", [("EMPTY", ch % (2 if g2 else 3))])
+                yield ("mma", f"E{ch}i", [("EMPTY", ch % NS)])
             yield ("wait", ("PSFULL",), ch)
             yield ("need", [("mma", f"PS{ch}"), ("mma", f"O1_{ch}")], f"state update {ch}")
             yield ("do", f"put{ch + 1}")
@@ -383,9 +391,57 @@ def preprocess_m(n, skip=None):
     return preprocess(n, skip, role_s=False)
 
 
-MODELS = {"single_head": single_head, "two_heads": two_heads, "pre_s": preprocess, "pre_m": preprocess_m}
+def single_head_kda(n, skip=None):
+    """The per-dim gate's forward (MODE_FWD_KDA): the unit's pre-gated Qg and
+    P arrive with the stage (two stages), the mask warps only release them
+    one chunk ahead, no Q K^T product and no gate slots."""
+    NS = 2
+
+    def mma():
+        for t in range(n):
+            yield ("wait", ("FULL", t % NS), t // NS)
+            if t >= 1:
+                yield ("wait", ("WREADY",), t - 1)
+                yield ("wait", ("WBFREE",), t - 1)
+            yield ("need", [("did", f"load{t}", 1)] + ([("did", f"wread{t - 1}", 4)] if t >= 1 else []), f"W {t}")
+            yield ("mma", f"W{t}", [("WFULL",)])
+            if t >= 1 and skip != "DLREADY":
+                yield ("wait", ("DLREADY",), t - 1)
+            yield ("need", [("did", f"dlread{t - 1}", 8)] if t >= 1 else [], f"U {t}")
+            yield ("mma", f"U{t}", [("UFULL",), ("EMPTY", t % NS)])
+
+    def mask(wi):
+        for ch in range(n):
+            if ch >= 1 and skip != "MFREE":
+                yield ("wait", ("MFREE",), ch - 1)
+            yield ("wait", ("FULL", ch % NS), ch // NS)
+            yield ("do", f"qscale{ch}")     # releases the stage's Qg
+            yield ("arrive", ("QREADY", ch & 1))
+            yield ("do", f"maskw{ch}")      # and its P
+            yield ("arrive", ("MREADY",))
+
+    def producer():
+        for t in range(n):
+            if t >= NS:
+                yield ("wait", ("EMPTY", t % NS), t // NS - 1)
+                u = t - NS
+                yield ("need", [("mma", x) for x in (f"W{u}", f"U{u}", f"O1_{u}", f"PS{u}", f"O2_{u}")] +
+                       [("did", f"gcopy{u}", 1)], f"load {t}")
+            yield ("do", f"load{t}")
+            yield ("arrive", ("FULL", t % NS))
+
+    progs = {"prod": producer(), "mma": mma()}
+    progs.update({f"mask{i}": mask(i) for i in range(2)})
+    progs.update(wepi_roles(n))
+    progs.update(state_roles(n, 0, False, skip, NS=NS, kda=True))
+    return progs, counts(NS)
+
+
+MODELS = {"single_head": single_head, "two_heads": two_heads, "single_head_kda": single_head_kda,
+          "pre_s": preprocess, "pre_m": preprocess_m}
 MUTATIONS = {"single_head": ["PFREE", "OFREE", "MREADY"],
              "two_heads": ["PFREE0", "PFREE1", "WREADY", "OFREE", "MREADY"],
+             "single_head_kda": ["OFREE", "DLREADY", "MFREE"],
              "pre_s": ["WBFREE", "UFULL", "WREADY"],
              "pre_m": ["WBFREE", "WREADY"]}
 
