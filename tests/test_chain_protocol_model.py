@@ -25,13 +25,13 @@ the pre-process's WBFREE, both the MMA warp's and the W epilogue's: each
 alone keeps the W tile from being rewritten while Delta reads it).
 
 Models: the single-head forward (MODE_FWD) and its per-dim-gate form
-(MODE_FWD_KDA: pre-gated Qg and P tiles with the stage), the forward of two query heads
-per chain (MODE_FWD_G2: both heads' Q K^T in turn in the columns W^T uses,
-both heads' outputs in one accumulator), and the pre-process's S and M
-chains (MODE_PRE: a non-state warp issuing Delta and P_S inside the state
-warps' named barrier).  The model is written from
-the kernel; it does not run it.  Each model is also run with one wait
-removed, which the checker must catch.
+(MODE_FWD_KDA: pre-gated Qg and P tiles with the stage), the forward of two
+query heads per chain (MODE_FWD_G2: both heads' Q K^T in turn in the
+columns W^T uses, both heads' outputs in one accumulator), and the
+pre-process's S and M chains (MODE_PRE: a non-state warp issuing Delta and
+P_S inside the state warps' named barrier).  The model is written from the
+kernel; it does not run it.  Each model is also run with one wait removed,
+which the checker must catch.
 """
 import random
 from collections import defaultdict
