@@ -29,9 +29,10 @@ Models: the single-head forward (MODE_FWD) and its per-dim-gate form
 query heads per chain (MODE_FWD_G2: both heads' Q K^T in turn in the
 columns W^T uses, both heads' outputs in one accumulator), and the
 pre-process's S and M chains (MODE_PRE: a non-state warp issuing Delta and
-P_S inside the state warps' named barrier).  The model is written from the
-kernel; it does not run it.  Each model is also run with one wait removed,
-which the checker must catch.
+P_S inside the state warps' named barrier), and the backward's
+state-gradient chain (MODE_BWD).  The model is written from the kernel; it
+does not run it.  Each model is also run with one wait removed, which the
+checker must catch.
 """
 import random
 from collections import defaultdict
@@ -437,13 +438,105 @@ def single_head_kda(n, skip=None):
     return progs, counts(NS)
 
 
+def backward(n, skip=None):
+    """The state-gradient chain (MODE_BWD, scalar gate), chunks in reverse:
+    per chunk the issuing lane of warp 8 issues X1 = dO^T mask (into the
+    Delta columns) and X2 = dS'^T K^T (into the output columns), the state
+    warps form dDelta from both and write -dDelta^T, then X3 + X4 =
+    dO^T (gamma ⊙ Q) - dDelta^T W (into the P_S columns) updates dS.  The
+    MMA warp issues Q K^T and W as in the forward (no U)."""
+    NS, NG = 3, 5
+
+    def mma():
+        for t in range(n):
+            yield ("wait", ("FULL", t % NS), t // NS)
+            if t >= 1:
+                yield ("wait", ("WREADY",), t - 1)
+                if skip != "WBFREE":
+                    yield ("wait", ("WBFREE",), t - 1)
+                yield ("wait", ("PFREE",), t - 1)
+            yield ("need", [("did", f"load{t}", 1)] + ([("did", f"pread{t - 1}", 2), ("did", f"wread{t - 1}", 4)]
+                                                       if t >= 1 else []), f"QK, W {t}")
+            yield ("mma", f"QK{t}", [("PFULL",)])
+            yield ("mma", f"W{t}", [("WFULL",), ("EMPTY", t % NS)])
+
+    def mask(wi):
+        for ch in range(n):
+            yield ("wait", ("GATE", ch % NG), ch // NG)
+            yield ("wait", ("PFULL",), ch)
+            yield ("need", [("mma", f"QK{ch}")], f"mask {ch}")
+            yield ("do", f"qscale{ch}")
+            yield ("arrive", ("QREADY", ch & 1))
+            yield ("do", f"pread{ch}")
+            yield ("arrive", ("PFREE",))
+            if ch >= 1:
+                yield ("wait", ("MFREE",), ch - 1)
+            yield ("need", [("mma", f"X1_{ch - 1}")] if ch >= 1 else [], f"mask tile {ch}")
+            yield ("do", f"maskw{ch}")
+            yield ("arrive", ("MREADY",))
+
+    def wepi(wi):
+        for t in range(n):
+            yield ("wait", ("WFULL",), t)
+            yield ("need", [("mma", f"W{t}")], f"W epilogue {t}")
+            yield ("do", f"wread{t}")
+            if t >= 1 and skip != "WBFREE":
+                yield ("wait", ("WBFREE",), t - 1)
+            yield ("need", [("mma", f"X34_{t - 1}")] if t >= 1 else [], f"W tile {t}")
+            yield ("do", f"wbw{t}")
+            yield ("arrive", ("WREADY",))
+
+    def state(wi):
+        issuer = wi == 0
+        yield ("do", "put0")
+        yield ("bar",)
+        for t in range(n):
+            if issuer:
+                if skip != "MREADY":
+                    yield ("wait", ("MREADY",), t)
+                yield ("need", [("did", f"maskw{t}", 2), ("did", f"put{t}", 8)] +
+                       ([("did", f"dlread{t - 1}", 8)] if t >= 1 else []), f"X1, X2 {t}")
+                yield ("mma", f"X1_{t}", [("MFREE",)])
+                yield ("mma", f"X2_{t}", [("DLFULL",)])
+            yield ("wait", ("GATE", t % NG), t // NG)
+            yield ("wait", ("DLFULL",), t)
+            yield ("need", [("mma", f"X1_{t}"), ("mma", f"X2_{t}")] +
+                   ([("mma", f"X34_{t - 1}")] if t >= 1 else []), f"dDelta {t}")
+            yield ("do", f"dlread{t}")
+            yield ("do", f"dbw{t}")
+            yield ("bar",)
+            if issuer:
+                yield ("wait", ("QREADY", t & 1), t >> 1)
+                if skip != "WREADY":
+                    yield ("wait", ("WREADY",), t)
+                yield ("need", [("did", f"qscale{t}", 2), ("did", f"wbw{t}", 4), ("did", f"dbw{t}", 8)] +
+                       ([("did", f"psread{t - 1}", 8)] if t >= 1 else []), f"X3, X4 {t}")
+                yield ("mma", f"X34_{t}", [("PSFULL",), ("WBFREE",)])
+                yield ("mma", f"E{t}i", [("EMPTY", t % NS)])
+            yield ("wait", ("PSFULL",), t)
+            yield ("need", [("mma", f"X34_{t}"), ("mma", f"X2_{t}")], f"dS update {t}")
+            yield ("do", f"psread{t}")
+            yield ("do", f"put{t + 1}")
+            yield ("bar",)
+
+    def reads(u):
+        return [("mma", x) for x in (f"QK{u}", f"W{u}", f"X1_{u}", f"X2_{u}", f"X34_{u}")] + [("did", f"qscale{u}", 2)]
+
+    progs = {"prod": producer_role(n, NS, reads), "mma": mma()}
+    progs.update({f"mask{i}": mask(i) for i in range(2)})
+    progs.update({f"wepi{i}": wepi(i) for i in range(4)})
+    progs.update({f"state{i}": state(i) for i in range(8)})
+    return progs, counts(NS)
+
+
 MODELS = {"single_head": single_head, "two_heads": two_heads, "single_head_kda": single_head_kda,
-          "pre_s": preprocess, "pre_m": preprocess_m}
+          "pre_s": preprocess, "pre_m": preprocess_m, "backward": backward}
 MUTATIONS = {"single_head": ["PFREE", "OFREE", "MREADY"],
              "two_heads": ["PFREE0", "PFREE1", "WREADY", "OFREE", "MREADY"],
              "single_head_kda": ["OFREE", "DLREADY", "MFREE"],
              "pre_s": ["WBFREE", "UFULL", "WREADY"],
-             "pre_m": ["WBFREE", "WREADY"]}
+             "pre_m": ["WBFREE", "WREADY"],
+             "backward": ["WBFREE", "MREADY", "WREADY"]}
 
 
 def failures(model, skip, seeds):
